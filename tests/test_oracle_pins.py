@@ -1,0 +1,320 @@
+"""Pins for the float64 oracle: each checks it against something other than
+itself -- a closed form, an invariant, a special case that reduces to a
+textbook formula, exact rational arithmetic on tiny inputs, or another form
+of the same operator -- so that a dropped term, a wrong sign or index, or a
+transposed operand fails at least one of them.
+
+Page passages (LION rebuttal page on paperhub.cn, "LION: A bidirectional
+framework that trains like a Transformer and infers like an RNN"):
+  * Theorem 3.3: full form Y = SCALE(QK^T (.) M) V (Eq 25) equals the
+    bidirectional RNN (Eq 20-24) -- reply "Concern 1".
+  * Causal Linear-Transformer recurrence and its two-direction extension that
+    removes the diagonal once -- reply "1: Recurrence Form ...".
+  * All-ones mask when lambda_i = 1; scaling does not change the result --
+    reply "5) Mask M for Linear Transformer".
+  * Feature maps elu+1 (LIT) and normalised SiLU (LION-S) -- reply "4)".
+  * Mask built from a cumulative sum -- reply "P3: LION-S uses cumsum".
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+MASKS = (0, 1, 2)
+
+
+def _inputs(rng, B, H, L, d, mask_kind, lam_lo=0.3, lam_hi=0.99):
+    q = rng.standard_normal((B, H, L, d))
+    k = rng.standard_normal((B, H, L, d))
+    v = rng.standard_normal((B, H, L, d))
+    if mask_kind == 0:
+        ll = None
+    elif mask_kind == 1:
+        ll = np.log(rng.uniform(lam_lo, lam_hi, size=H))
+    else:
+        ll = np.log(rng.uniform(lam_lo, lam_hi, size=(B, H, L)))
+    return q, k, v, ll
+
+
+def _rel(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+def _rel_rows_kappa(o, y, ref, q, k, ll, mask_kind, phi_kind):
+    """max over rows of ||y_i - ref_i||_inf / (||ref_i||_inf * max(1, kappa_i)):
+    features that can be negative (SiLU) may make a row sum cancel."""
+    B, H, L, _ = q.shape
+    worst = 0.0
+    for b in range(B):
+        for h in range(H):
+            kap = o.row_kappa(q, k, ll, mask_kind, b, h, 0, L, phi_kind)
+            err = np.max(np.abs(y[b, h] - ref[b, h]), axis=-1)
+            nrm = np.max(np.abs(ref[b, h]), axis=-1)
+            worst = max(worst, float(np.max(err / (nrm * np.maximum(1.0, kap)))))
+    return worst
+
+
+# ---------------------------------------------------------------- P1 -----
+@pytest.mark.parametrize("mask_kind", MASKS)
+@pytest.mark.parametrize("phi_kind", (0, 1, 2, 3))
+def test_three_forms_agree_small(oracle_mod, mask_kind, phi_kind):
+    """Theorem 3.3: full == bidirectional RNN == chunkwise for L <= 16, every
+    chunk length (including 1, non-divisors and C >= L)."""
+    o = oracle_mod
+    rng = np.random.default_rng(100 + mask_kind * 10 + phi_kind)
+    for L in (1, 2, 3, 5, 8, 13, 16):
+        for d in (1, 3, 4):
+            q, k, v, ll = _inputs(rng, 2, 2, L, d, mask_kind)
+            if phi_kind == 3:           # identity features: keep row sums away from 0
+                q, k = np.abs(q) + 0.1, np.abs(k) + 0.1
+            silu = phi_kind == 2 or (phi_kind == 0 and mask_kind == 2)
+            if silu and d == 1:
+                continue                # phi = sign(x): row sums are exactly 0 or +-L
+            yf = o.full(q, k, v, ll, mask_kind, phi_kind)
+            yr = o.rnn(q, k, v, ll, mask_kind, phi_kind)
+            err = (lambda y: _rel_rows_kappa(o, y, yf, q, k, ll, mask_kind, phi_kind)) if silu \
+                else (lambda y: _rel(y, yf))
+            assert err(yr) < 1e-11, (L, d)
+            for C in sorted({1, 2, 3, 4, 5, L, L + 3}):
+                yc = o.chunk(q, k, v, ll, mask_kind, C, phi_kind)
+                assert err(yc) < 1e-11, (L, d, C)
+
+
+# ---------------------------------------------------------------- P2 -----
+@pytest.mark.parametrize("phi_kind", (1, 2))
+def test_lit_closed_form(oracle_mod, phi_kind):
+    """All-ones mask: y_i = phi(q_i)^T (sum_j phi(k_j) v_j^T) / phi(q_i)^T sum_j phi(k_j)
+    (linear attention by associativity; no L x L matrix)."""
+    o = oracle_mod
+    rng = np.random.default_rng(7)
+    q, k, v, _ = _inputs(rng, 2, 3, 37, 8, 0)
+    fq = torch.nn.functional.elu(torch.from_numpy(q)) + 1.0 if phi_kind == 1 else None
+    if phi_kind == 1:
+        fk = torch.nn.functional.elu(torch.from_numpy(k)) + 1.0
+    else:
+        fq = torch.nn.functional.normalize(torch.nn.functional.silu(torch.from_numpy(q)), dim=-1, eps=1e-12)
+        fk = torch.nn.functional.normalize(torch.nn.functional.silu(torch.from_numpy(k)), dim=-1, eps=1e-12)
+    kv = torch.einsum("bhjm,bhjn->bhmn", fk, torch.from_numpy(v))
+    ksum = fk.sum(dim=2)
+    num = torch.einsum("bhim,bhmn->bhin", fq, kv)
+    den = torch.einsum("bhim,bhm->bhi", fq, ksum)
+    ref = (num / den[..., None]).numpy()
+    for y in (o.full(q, k, v, None, 0, phi_kind), o.rnn(q, k, v, None, 0, phi_kind),
+              o.chunk(q, k, v, None, 0, 5, phi_kind)):
+        assert _rel(y, ref) < 1e-11
+
+
+# ---------------------------------------------------------------- P3 -----
+def test_d_mask_is_symmetric_toeplitz(oracle_mod):
+    """LION-D: M_ij = lambda^|i-j| for a fixed per-head lambda."""
+    o = oracle_mod
+    L = 23
+    for lam in (0.5, 0.9, 0.999):
+        ll = np.array([0.0, np.log(lam)])
+        M = o.mask(1, ll, L, b=0, h=1, H=2)
+        i = np.arange(L)
+        ref = lam ** np.abs(i[:, None] - i[None, :]).astype(np.float64)
+        assert np.allclose(M, ref, rtol=1e-13, atol=0)
+        assert np.array_equal(M, M.T)
+        for off in range(-L + 1, L):   # Toeplitz: constant along each diagonal
+            dg = np.diagonal(M, off)
+            assert np.allclose(dg, dg[0], rtol=1e-13, atol=0)
+
+
+def test_s_mask_index_convention(oracle_mod):
+    """LION-S reading: M_ij = prod_{k=min(i,j)+1}^{max(i,j)} lambda_k, M_ii = 1,
+    symmetric, lambda_0 unused, and equal to exp of cumsum differences."""
+    o = oracle_mod
+    lam = np.array([0.11, 0.5, 0.25, 0.8, 0.9])
+    ll = np.log(lam)[None, None, :]
+    M = o.mask(2, ll, 5, b=0, h=0, H=1)
+    assert np.allclose(np.diag(M), 1.0)
+    assert np.isclose(M[0, 1], 0.5) and np.isclose(M[1, 0], 0.5)
+    assert np.isclose(M[0, 2], 0.5 * 0.25) and np.isclose(M[2, 0], 0.5 * 0.25)
+    assert np.isclose(M[1, 4], 0.25 * 0.8 * 0.9)
+    assert np.isclose(M[4, 1], 0.25 * 0.8 * 0.9)
+    assert np.allclose(M, M.T, rtol=1e-14)
+    P = np.cumsum(np.log(lam))
+    i = np.arange(5)
+    ref = np.exp(-np.abs(P[:, None] - P[None, :]))
+    assert np.allclose(M, ref, rtol=1e-13)
+    ll2 = ll.copy()
+    ll2[0, 0, 0] = np.log(0.999)     # lambda_0 never enters the mask
+    assert np.array_equal(o.mask(2, ll2, 5, H=1), M)
+    del i
+
+
+# ---------------------------------------------------------------- P4 -----
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_convex_hull_positive_features(oracle_mod, mask_kind):
+    """elu+1 features give s_ij > 0 and M_ij > 0, so y_i is a convex
+    combination of the v_j: each coordinate lies in [min_j v_jn, max_j v_jn]."""
+    o = oracle_mod
+    rng = np.random.default_rng(11 + mask_kind)
+    q, k, v, ll = _inputs(rng, 2, 2, 40, 6, mask_kind)
+    y = o.chunk(q, k, v, ll, mask_kind, 7, 1)
+    lo = v.min(axis=2, keepdims=True)
+    hi = v.max(axis=2, keepdims=True)
+    assert np.all(y >= lo - 1e-12) and np.all(y <= hi + 1e-12)
+
+
+# ---------------------------------------------------------------- P5 -----
+def test_unit_decay_reduces_to_lit(oracle_mod):
+    o = oracle_mod
+    rng = np.random.default_rng(21)
+    q, k, v, _ = _inputs(rng, 2, 2, 19, 5, 0)
+    ref = o.full(q, k, v, None, 0, 1)
+    yd = o.rnn(q, k, v, np.zeros(2), 1, 1)
+    ys = o.chunk(q, k, v, np.zeros((2, 2, 19)), 2, 4, 1)
+    assert _rel(yd, ref) < 1e-12 and _rel(ys, ref) < 1e-12
+
+
+@pytest.mark.parametrize("mask_kind", (1, 2))
+def test_vanishing_decay_gives_identity(oracle_mod, mask_kind):
+    """lambda -> 0 (log lambda = -1e4): M = I, so y_i = s_ii v_i / s_ii = v_i."""
+    o = oracle_mod
+    rng = np.random.default_rng(31)
+    q, k, v, _ = _inputs(rng, 1, 2, 12, 4, 0)
+    ll = np.full(2, -1e4) if mask_kind == 1 else np.full((1, 2, 12), -1e4)
+    for y in (o.full(q, k, v, ll, mask_kind, 1), o.rnn(q, k, v, ll, mask_kind, 1),
+              o.chunk(q, k, v, ll, mask_kind, 5, 1)):
+        assert _rel(y, v) < 1e-12
+
+
+def test_forward_half_is_causal_linear_transformer(oracle_mod):
+    """With lambda = 1 the forward recurrence is the causal Linear Transformer:
+    S_i = S_{i-1} + k_i v_i^T, z_i = z_{i-1} + k_i, y_i = q_i^T S_i / q_i^T z_i
+    (rebuttal page, reply "1: Recurrence Form"), here unrolled with cumsum."""
+    o = oracle_mod
+    rng = np.random.default_rng(41)
+    q, k, v, _ = _inputs(rng, 1, 2, 30, 6, 0)
+    yF, cF = o.rnn_forward_half(q, k, v, None, 0, 1)
+    fq = np.where(q > 0, q + 1, np.exp(q))
+    fk = np.where(k > 0, k + 1, np.exp(k))
+    S = np.cumsum(fk[..., :, None] * v[..., None, :], axis=2)   # [B,H,L,d,d]
+    z = np.cumsum(fk, axis=2)
+    num = np.einsum("bhim,bhimn->bhin", fq, S)
+    den = np.einsum("bhim,bhim->bhi", fq, z)
+    assert _rel(yF, num) < 1e-12 and _rel(cF, den) < 1e-12
+
+
+# ---------------------------------------------------------------- P6 -----
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_sequence_reversal(oracle_mod, mask_kind):
+    """Reversing the tokens and using l'_k = l_{L-k} (k >= 1) reverses the output."""
+    o = oracle_mod
+    rng = np.random.default_rng(51 + mask_kind)
+    L = 17
+    q, k, v, ll = _inputs(rng, 1, 2, L, 4, mask_kind)
+    y = o.full(q, k, v, ll, mask_kind)
+    rq, rk, rv = q[:, :, ::-1], k[:, :, ::-1], v[:, :, ::-1]
+    if mask_kind == 2:
+        rll = np.empty_like(ll)
+        rll[..., 0] = -0.3                     # unused
+        rll[..., 1:] = ll[..., :0:-1]          # l'_k = l_{L-k}
+    else:
+        rll = ll
+    yr = o.rnn(rq, rk, rv, rll, mask_kind)
+    assert _rel(yr[:, :, ::-1], y) < 1e-12
+
+
+# ---------------------------------------------------------------- P7 -----
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_query_scale_invariance(oracle_mod, mask_kind):
+    """Row-sum normalisation: scaling q_i by c_i > 0 (identity features) leaves
+    y unchanged -- no temperature, no epsilon in the denominator."""
+    o = oracle_mod
+    rng = np.random.default_rng(61 + mask_kind)
+    q, k, v, ll = _inputs(rng, 1, 2, 14, 3, mask_kind)
+    q, k = np.abs(q) + 0.1, np.abs(k) + 0.1
+    c = rng.uniform(0.01, 100.0, size=(1, 2, 14, 1))
+    y1 = o.chunk(q, k, v, ll, mask_kind, 4, 3)
+    y2 = o.chunk(q * c, k, v, ll, mask_kind, 4, 3)
+    assert _rel(y2, y1) < 1e-12
+
+
+# ------------------------------------------------- exact tiny cases -----
+def _exact_bruteforce(q, k, v, lam):
+    """Exact rational y for one head with identity features."""
+    L, d = len(q), len(q[0])
+    y = []
+    for i in range(L):
+        num = [Fraction(0)] * d
+        den = Fraction(0)
+        for j in range(L):
+            m = Fraction(1)
+            for t in range(min(i, j) + 1, max(i, j) + 1):
+                m *= lam[t]
+            s = sum(q[i][a] * k[j][a] for a in range(d))
+            den += m * s
+            for n in range(d):
+                num[n] += m * s * v[j][n]
+        y.append([float(x / den) for x in num])
+    return np.array(y)
+
+
+def test_exact_rational_tiny(oracle_mod):
+    o = oracle_mod
+    q = [[Fraction(1), Fraction(2)], [Fraction(3), Fraction(1)], [Fraction(1, 2), Fraction(5)]]
+    k = [[Fraction(2), Fraction(1)], [Fraction(1), Fraction(1)], [Fraction(4), Fraction(1, 3)]]
+    v = [[Fraction(1), Fraction(-2)], [Fraction(-3), Fraction(1)], [Fraction(2), Fraction(7)]]
+    lam = [Fraction(1, 3), Fraction(1, 2), Fraction(1, 4)]
+    ref = _exact_bruteforce(q, k, v, lam)
+    arr = lambda m: np.array([[float(x) for x in r] for r in m])[None, None]  # noqa: E731
+    ll = np.log(np.array([float(x) for x in lam]))[None, None]
+    for y in (o.full(arr(q), arr(k), arr(v), ll, 2, 3), o.rnn(arr(q), arr(k), arr(v), ll, 2, 3),
+              o.chunk(arr(q), arr(k), arr(v), ll, 2, 2, 3)):
+        assert _rel(y[0, 0], ref) < 1e-14
+    # L = 2, d = 1 by hand: y_0 = (s00 v0 + lam1 s01 v1) / (s00 + lam1 s01)
+    q2, k2, v2 = np.array([[[[2.0], [1.0]]]]), np.array([[[[3.0], [5.0]]]]), np.array([[[[1.0], [4.0]]]])
+    ll2 = np.log(np.array([[[0.7, 0.25]]]))
+    y = o.full(q2, k2, v2, ll2, 2, 3)
+    y0 = (6 * 1 + 0.25 * 10 * 4) / (6 + 0.25 * 10)
+    y1 = (0.25 * 3 * 1 + 5 * 4) / (0.25 * 3 + 5)
+    assert np.allclose(y[0, 0, :, 0], [y0, y1], rtol=1e-14)
+
+
+# ---------------------------------------------------------------- phi ----
+def test_feature_maps(oracle_mod):
+    o = oracle_mod
+    rng = np.random.default_rng(71)
+    x = rng.standard_normal((9, 16)) * 3
+    t = torch.from_numpy(x)
+    assert np.allclose(o.phi(1, x), (torch.nn.functional.elu(t) + 1).numpy(), rtol=1e-14, atol=1e-15)
+    ref = torch.nn.functional.normalize(torch.nn.functional.silu(t), dim=-1, eps=1e-12).numpy()
+    assert np.allclose(o.phi(2, x), ref, rtol=1e-13, atol=1e-16)
+    assert np.array_equal(o.phi(3, x), x)
+    z = np.zeros((2, 8))
+    assert np.array_equal(o.phi(2, z), z)       # ||u|| clamped at 1e-12, no NaN
+
+
+# ------------------------------------------------------ sampled rows -----
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_sampled_rows_match_full(oracle_mod, mask_kind):
+    o = oracle_mod
+    rng = np.random.default_rng(81 + mask_kind)
+    q, k, v, ll = _inputs(rng, 2, 3, 29, 5, mask_kind)
+    y = o.full(q, k, v, ll, mask_kind)
+    idx = [0, 7, 28, 13]
+    yr = o.rows(q, k, v, ll, mask_kind, 1, 2, idx)
+    assert _rel(yr, y[1, 2, idx]) < 1e-13
+
+
+def test_kappa_is_one_for_positive_features(oracle_mod):
+    o = oracle_mod
+    rng = np.random.default_rng(91)
+    q, k, v, ll = _inputs(rng, 1, 1, 20, 4, 2)
+    kap = o.row_kappa(q, k, ll, 2, 0, 0, 0, 20, phi_kind=1)
+    assert np.allclose(kap, 1.0, rtol=1e-12)
+    kap2 = o.row_kappa(q, k, ll, 2, 0, 0, 0, 20)    # SiLU features may cancel
+    assert np.all(kap2 >= 1.0 - 1e-12)
+
+
+def test_invalid_arguments(oracle_mod):
+    o = oracle_mod
+    q = np.zeros((1, 1, 4, 2))
+    with pytest.raises(ValueError):
+        o.full(q, q, q, None, 1)                      # LION-D without decays
+    with pytest.raises(ValueError):
+        o.chunk(q, q, q, None, 0, 0)                  # chunk < 1
