@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Throughput of the LION chunkwise forward operator on GB300.
+
+One step = one call of the operator (feature map, log-decay prefix,
+intra-chunk attention, chunk states, scans, combine/normalise) over one batch
+of synthetic inputs already resident in HBM.  Default workload: ViT-B
+(B=64, H=12, L=197, d=64), LION-S, chunk 64.  The L=24,337 high-resolution
+workload is measured in the same run and reported under ``secondary``.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bidirectional_masked_linear_gb300 import lion, synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20      # > 129 MB L2
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            hbm = next((float(v) for k, v in d.items() if "hbm" in k.lower() and
+                        isinstance(v, (int, float))), None)
+            bf16 = d.get("bf16_tflops")
+            if hbm:
+                return hbm, float(bf16) if bf16 else FALLBACK_BF16_TFLOPS, "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def algorithmic_bytes(w, mask: str) -> int:
+    """Bytes the operator must move per call: q, k, v read once, y (fp32)
+    written once, plus the decays (per token for LION-S, per head for D)."""
+    el = 2 if w.dtype == "bf16" else 4
+    n = w.B * w.H * w.L * w.d
+    b = 3 * n * el + 4 * n
+    if mask == "s":
+        b += 4 * w.B * w.H * w.L
+    elif mask == "d":
+        b += 4 * w.H
+    return b
+
+
+def kernels_per_call(form: str, chunk: int, w) -> int:
+    """Kernel launches one operator call makes (the library launches exactly
+    one kernel per call on every current path)."""
+    del form, chunk, w
+    return 1
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                smax.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, ws, rank, local
+    return None, 1, 0, 0
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_device(call, steps, warmup, flush, stream):
+    """Per-step CUDA-event durations (ms) of `call` on `stream`, L2 flushed
+    before every step (outside the events)."""
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def measure(name, mask, chunk, form, steps, warmup, flush):
+    w = synth.WORKLOADS[name]
+    inp = synth.workload_inputs(name, mask)
+    dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
+    out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    fcode = lion.FORMS[form]
+    wsb = lion.workspace_bytes(w.B, w.H, w.L, w.d, fcode, chunk)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        lion.attn_fwd(dev["q"], dev["k"], dev["v"], dev["log_lambda"], inp["mask"], fcode, chunk,
+                      out=out, workspace=ws)
+
+    times = time_device(call, steps, warmup, flush, stream)
+    return w, inp, times, (dev, out, ws, call)
+
+
+def measure_e2e(w, inp, mask, chunk, form, steps, warmup):
+    """Same metric end to end: pinned host inputs copied in, the operator, the
+    output copied back, all inside the timed region."""
+    fcode = lion.FORMS[form]
+    host = {k: (None if inp[k] is None else inp[k].pin_memory()) for k in ("q", "k", "v", "log_lambda")}
+    dev = {k: (None if host[k] is None else torch.empty_like(host[k], device="cuda")) for k in host}
+    out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    wsb = lion.workspace_bytes(w.B, w.H, w.L, w.d, fcode, chunk)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k2 in dev:
+            if dev[k2] is not None:
+                dev[k2].copy_(host[k2], non_blocking=True)
+        lion.attn_fwd(dev["q"], dev["k"], dev["v"], dev["log_lambda"], inp["mask"], fcode, chunk,
+                      out=out, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline(name, mask, chunk, budget_s=10.0):
+    """The float64 oracle (chunk form, all host cores) on a bounded sample of
+    heads of the same workload; tokens/s counts B*L tokens per H heads."""
+    import oracle
+    w = synth.WORKLOADS[name]
+    inp = synth.workload_inputs(name, mask)
+    q, k, v, ll = (synth.as_f64(inp[x]) for x in ("q", "k", "v", "log_lambda"))
+    cores = oracle.threads(0)
+    # one batch row at a time (all H heads) until the budget is spent
+    done_heads, t0 = 0, time.perf_counter()
+    b = 0
+    while b < w.B and (time.perf_counter() - t0) < budget_s:
+        sl = slice(b, b + 1)
+        lls = None if ll is None else (ll if mask == "d" else ll[sl])
+        oracle.chunk(q[sl], k[sl], v[sl], lls, inp["mask"], chunk, threads=0)
+        done_heads += w.H
+        b += 1
+    dt = time.perf_counter() - t0
+    tokens = done_heads * w.L / w.H
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{b} of {w.B} batch rows ({done_heads} heads x L={w.L}), float64 chunk form "
+                      f"(chunk {chunk}), OpenMP over heads, {dt:.1f} s"}
+
+
+def run_reference(args, dist, ws, rank):
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    res = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(args.workload, args.mask, args.chunk, budget_s=budget)
+        if i >= args.warmup:
+            res.append(r)
+    val = statistics.median(r["value"] for r in res)
+    ms = w.B * w.L / val * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(args, w),
+            "cpu_baseline": dict(res[-1], value=val),
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+METRIC = "LION attn fwd tokens/s (chunkwise form)"
+
+
+def _config(args, w):
+    return {"workload": f"{w.name} B={w.B} H={w.H} L={w.L} d={w.d}", "mask": args.mask,
+            "form": args.form, "chunk": args.chunk, "input_dtype": w.dtype, "out_dtype": "f32",
+            "global_batch": w.B, "seq_len": w.L, "parallelism": f"replicas x{args.gpus}",
+            "l2": "flushed before every timed step (256 MiB write)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--workload", default="vit_b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--mask", default="s", choices=("lit", "d", "s"))
+    ap.add_argument("--chunk", type=int, default=64)
+    ap.add_argument("--form", default="chunk", choices=("chunk", "full", "rnn"))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    dist, ws, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, dist, ws, rank)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    from bidirectional_masked_linear_gb300 import build
+    lion.load(build.build())
+    hbm_peak, bf16_peak, peak_src = _peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    _barrier(dist)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t_wall = time.perf_counter()
+        w, inp, times, _keep = measure(args.workload, args.mask, args.chunk, args.form,
+                                       args.steps, args.warmup, flush)
+        t_wall = time.perf_counter() - t_wall
+    torch.cuda.synchronize()
+    _barrier(dist)
+    clocks = clk.summary()
+    ms = statistics.mean(times)
+    ms_all = _max_over_ranks(dist, ms)
+    tokens = w.B * w.L
+    value = ws * tokens / (ms_all * 1e-3)
+    abytes = algorithmic_bytes(w, args.mask)
+    achieved = abytes / (ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = measure_e2e(w, inp, args.mask, args.chunk, args.form, 50, 5)
+    e2e_ms = _max_over_ranks(dist, e2e_ms)
+
+    secondary = None
+    if not args.no_secondary and args.workload != "hires_2496":
+        w2, _, t2, _k2 = measure("hires_2496", args.mask if args.mask != "lit" else "s", args.chunk,
+                                 "chunk", 50, 3, flush)
+        ms2 = statistics.mean(t2)
+        b2 = algorithmic_bytes(w2, args.mask if args.mask != "lit" else "s")
+        secondary = {"workload": f"{w2.name} B={w2.B} H={w2.H} L={w2.L} d={w2.d}",
+                     "value": w2.B * w2.L / (ms2 * 1e-3), "unit": "tokens/s", "ms_per_step": ms2,
+                     "roofline": {"bound": "hbm", "achieved": b2 / (ms2 * 1e-3) / 1e9,
+                                  "peak": hbm_peak, "unit": "GB/s",
+                                  "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak}}
+        del _k2
+
+    cpu = None
+    if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:
+        cpu = cpu_baseline(args.workload, args.mask, args.chunk)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": _config(args, w),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "peak_source": peak_src, "algorithmic_bytes": abytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": ws * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * kernels_per_call(args.form, args.chunk, w),
+            "clocks": clocks,
+            "wall_s_timed_region": t_wall,
+            "secondary": secondary,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

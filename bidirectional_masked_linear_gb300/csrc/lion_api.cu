@@ -1,0 +1,181 @@
+// lion_api.cu -- the C ABI declared in include/lion.h: argument checks,
+// workspace handling and the choice of kernel for each form.
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/lion.h"
+#include "lion_common.cuh"
+#include "lion_internal.h"
+
+namespace {
+
+using lion::Problem;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A pointer the GPU can dereference: device or managed memory, or host memory
+// registered/allocated with a device mapping.  Host-only memory would make a
+// kernel fault, so it is refused here instead.
+bool device_accessible(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of the query
+    return false;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeHost && at.devicePointer != nullptr;
+}
+
+bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+
+// Workspace in floats for (form, path).
+size_t workspace_floats(int B, int H, int L, int d, int form, int chunk) {
+  (void)d;
+  (void)chunk;
+  if (form == LION_FORM_RNN || form == LION_FORM_CHUNK) return (size_t)B * H * L;
+  return 0;
+}
+
+lion_status validate(const lion_args* a) {
+  if (!a) return LION_ERR_INVALID_ARG;
+  if (!a->q || !a->k || !a->v || !a->out) return LION_ERR_INVALID_ARG;
+  if (a->B < 1 || a->H < 1 || a->L < 1 || !valid_d(a->d)) return LION_ERR_INVALID_ARG;
+  if (a->mask_kind < LION_MASK_LIT || a->mask_kind > LION_MASK_S) return LION_ERR_INVALID_ARG;
+  if (a->form < LION_FORM_FULL || a->form > LION_FORM_CHUNK) return LION_ERR_INVALID_ARG;
+  if (a->dtype != LION_DTYPE_BF16 && a->dtype != LION_DTYPE_FP32) return LION_ERR_INVALID_ARG;
+  if (a->phi < LION_PHI_DEFAULT || a->phi > LION_PHI_IDENTITY) return LION_ERR_INVALID_ARG;
+  if (a->form == LION_FORM_CHUNK && a->chunk < 1) return LION_ERR_INVALID_ARG;
+  if (a->mask_kind != LION_MASK_LIT && !a->log_lambda) return LION_ERR_INVALID_ARG;
+  // 32-bit launch and index limits: B*H heads on one grid axis, L*d per head.
+  if ((long long)a->B * a->H > 0x7fffffffLL || (long long)a->L * a->d > 0x7fffffffLL)
+    return LION_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->out, 16))
+    return LION_ERR_INVALID_ARG;
+  if (a->log_lambda && !aligned(a->log_lambda, 4)) return LION_ERR_INVALID_ARG;
+  if (a->workspace && !aligned(a->workspace, 256)) return LION_ERR_INVALID_ARG;
+  if (!device_accessible(a->q) || !device_accessible(a->k) || !device_accessible(a->v) ||
+      !device_accessible(a->out))
+    return LION_ERR_INVALID_ARG;
+  if (a->mask_kind != LION_MASK_LIT && !device_accessible(a->log_lambda)) return LION_ERR_INVALID_ARG;
+  if (a->workspace && !device_accessible(a->workspace)) return LION_ERR_INVALID_ARG;
+  if (a->form == LION_FORM_FULL && a->L > LION_FULL_MAX_L) return LION_ERR_UNSUPPORTED;
+  if (a->form == LION_FORM_CHUNK && a->chunk > lion::kSimtMaxChunk) return LION_ERR_UNSUPPORTED;
+  return LION_OK;
+}
+
+lion_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return LION_OK;
+  if (e == cudaErrorMemoryAllocation) return LION_ERR_NO_MEMORY;
+  return LION_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lion_abi_version(void) { return 1; }
+
+const char* lion_status_string(lion_status s) {
+  switch (s) {
+    case LION_OK: return "ok";
+    case LION_ERR_INVALID_ARG: return "invalid argument";
+    case LION_ERR_UNSUPPORTED: return "unsupported problem";
+    case LION_ERR_CUDA: return "CUDA error";
+    case LION_ERR_NO_MEMORY: return "out of device memory";
+    case LION_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk) {
+  if (B < 1 || H < 1 || L < 1 || !valid_d(d)) return 0;
+  return sizeof(float) * workspace_floats(B, H, L, d, form, chunk);
+}
+
+lion_status lion_attn_fwd_ex(const lion_args* a) {
+  lion_status st = validate(a);
+  if (st != LION_OK) return st;
+  Problem p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.log_lambda = a->log_lambda;
+  p.out = a->out;
+  p.B = a->B;
+  p.H = a->H;
+  p.L = a->L;
+  p.d = a->d;
+  p.mask_kind = a->mask_kind;
+  p.phi = lion::resolve_phi(a->mask_kind, a->phi);
+  p.dtype = a->dtype;
+  p.chunk = a->chunk;
+  cudaStream_t s = a->stream;
+
+  const size_t need = sizeof(float) * workspace_floats(a->B, a->H, a->L, a->d, a->form, a->chunk);
+  void* ws = a->workspace;
+  bool owned = false;
+  if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
+  if (need > 0 && !ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
+    }
+    owned = true;
+  }
+  cudaError_t e = cudaSuccess;
+  switch (a->form) {
+    case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
+    case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
+    case LION_FORM_CHUNK: e = lion::launch_chunk_simt(p, (float*)ws, s); break;
+  }
+  if (owned) {
+    cudaError_t f = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = f;
+  }
+  return from_cuda(e);
+}
+
+lion_status lion_attn_fwd(const void* q, const void* k, const void* v, const float* log_lambda,
+                          int B, int H, int L, int d, int mask_kind, int form, int chunk,
+                          float* out, cudaStream_t stream) {
+  lion_args a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.log_lambda = log_lambda;
+  a.out = out;
+  a.B = B;
+  a.H = H;
+  a.L = L;
+  a.d = d;
+  a.mask_kind = mask_kind;
+  a.form = form;
+  a.chunk = chunk;
+  a.dtype = LION_DTYPE_BF16;
+  a.phi = LION_PHI_DEFAULT;
+  a.stream = stream;
+  return lion_attn_fwd_ex(&a);
+}
+
+lion_status lion_rnn_step(const void* q, const void* k, const void* v, const float* log_lambda,
+                          float* S, float* z, float* y_part, float* c_part, int B, int H, int d,
+                          int mask_kind, int dtype, cudaStream_t stream) {
+  if (!q || !k || !v || !S || !z || !y_part || !c_part) return LION_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || !valid_d(d)) return LION_ERR_INVALID_ARG;
+  if (mask_kind < LION_MASK_LIT || mask_kind > LION_MASK_S) return LION_ERR_INVALID_ARG;
+  if (dtype != LION_DTYPE_BF16 && dtype != LION_DTYPE_FP32) return LION_ERR_INVALID_ARG;
+  if (mask_kind != LION_MASK_LIT && !log_lambda) return LION_ERR_INVALID_ARG;
+  if ((long long)B * H > 0x7fffffffLL) return LION_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, S, z, y_part, c_part};
+  for (const void* ptr : ptrs)
+    if (!aligned(ptr, 4) || !device_accessible(ptr)) return LION_ERR_INVALID_ARG;
+  if (mask_kind != LION_MASK_LIT && !device_accessible(log_lambda)) return LION_ERR_INVALID_ARG;
+  const int phi = lion::resolve_phi(mask_kind, LION_PHI_DEFAULT);
+  return from_cuda(lion::launch_rnn_step(q, k, v, log_lambda, S, z, y_part, c_part, B, H, d,
+                                         mask_kind, phi, dtype, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,34 @@
+// lion_internal.h -- interface between the C ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace lion {
+
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* log_lambda;
+  float* out;
+  int B, H, L, d;
+  int mask_kind;
+  int phi;     // resolved (never PHI_DEFAULT)
+  int dtype;   // DT_BF16 / DT_FP32
+  int chunk;
+};
+
+// SIMT (CUDA-core) kernels: any d in {16,32,64,128}, both dtypes.
+cudaError_t launch_full_simt(const Problem& p, cudaStream_t s);
+cudaError_t launch_rnn_simt(const Problem& p, float* ws_c /*[B*H*L]*/, cudaStream_t s);
+cudaError_t launch_chunk_simt(const Problem& p, float* ws_den /*[B*H*L]*/, cudaStream_t s);
+cudaError_t launch_rnn_step(const void* q, const void* k, const void* v, const float* log_lambda,
+                            float* S, float* z, float* y_part, float* c_part, int B, int H,
+                            int d, int mask_kind, int phi, int dtype, cudaStream_t s);
+
+// Largest chunk the SIMT chunk kernel takes (its chunk-local prefix lives in
+// shared memory).
+constexpr int kSimtMaxChunk = 1024;
+
+}  // namespace lion

@@ -1,0 +1,157 @@
+"""Python binding of liblion.so (the C ABI in ``include/lion.h``).
+
+Argument marshalling only: every step of the operator runs in the CUDA
+library.  Tensors are PyTorch CUDA tensors (PyTorch provides device memory and
+streams); they are passed to the library as raw pointers.  If the library has
+not been built the calls raise -- there is no other implementation to fall
+back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblion.so")
+
+# enums of include/lion.h
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = range(6)
+MASK_LIT, MASK_D, MASK_S = 0, 1, 2
+FORM_FULL, FORM_RNN, FORM_CHUNK = 0, 1, 2
+DTYPE_BF16, DTYPE_FP32 = 0, 1
+PHI_DEFAULT, PHI_ELU1, PHI_SILU_L2, PHI_IDENTITY = 0, 1, 2, 3
+FULL_MAX_L = 8192
+
+MASKS = {"lit": MASK_LIT, "d": MASK_D, "s": MASK_S}
+FORMS = {"full": FORM_FULL, "rnn": FORM_RNN, "chunk": FORM_CHUNK}
+
+
+class LionError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_lambda", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int),
+        ("mask_kind", ctypes.c_int), ("form", ctypes.c_int), ("chunk", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("phi", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "lion_rnn_step",
+           "lion_status_string", "lion_abi_version")
+
+
+def load(path: str = LIB_PATH):
+    """Load liblion.so (raises if it is missing: build it with ``build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"liblion.so not found at {path}: build it with "
+                           "bidirectional_masked_linear_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.lion_attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp]
+    lib.lion_attn_fwd.restype = i
+    lib.lion_attn_fwd_ex.argtypes = [ctypes.POINTER(_Args)]
+    lib.lion_attn_fwd_ex.restype = i
+    lib.lion_attn_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.lion_attn_workspace_bytes.restype = ctypes.c_size_t
+    lib.lion_rnn_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.lion_rnn_step.restype = i
+    lib.lion_status_string.argtypes = [i]
+    lib.lion_status_string.restype = ctypes.c_char_p
+    lib.lion_abi_version.argtypes = []
+    lib.lion_abi_version.restype = i
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().lion_status_string(status).decode()
+
+
+def _check(status: int):
+    if status != OK:
+        raise LionError(status, status_string(status))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_FP32
+    raise TypeError(f"q, k, v must be bfloat16 or float32, got {t.dtype}")
+
+
+def workspace_bytes(B, H, L, d, form, chunk=64) -> int:
+    return int(load().lion_attn_workspace_bytes(B, H, L, d, form, chunk))
+
+
+def attn_fwd(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None,
+             phi=PHI_DEFAULT, workspace=None, stream=None):
+    """Y = SCALE((phi(Q) phi(K)^T (.) M) V) for q, k, v of shape [B, H, L, d].
+
+    ``log_lambda``: None (LIT), [H] (D) or [B, H, L] (S), float32, on the GPU.
+    Returns ``out`` ([B, H, L, d] float32)."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    if isinstance(form, str):
+        form = FORMS[form]
+    B, H, L, d = q.shape
+    if out is None:
+        out = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    dt = _dtype_code(q)
+    if log_lambda is not None and log_lambda.dtype != torch.float32:
+        raise TypeError("log_lambda must be float32")
+    for t in (q, k, v, out) + ((log_lambda,) if log_lambda is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if q.dtype != k.dtype or q.dtype != v.dtype or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share dtype and shape")
+    stream_h = _stream_handle(stream)
+    if dt == DTYPE_BF16 and phi == PHI_DEFAULT and workspace is None:
+        st = lib.lion_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), B, H, L, d, mask_kind,
+                               form, chunk, _ptr(out), stream_h)
+    else:
+        a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(out), B, H, L, d, mask_kind,
+                  form, chunk, dt, phi, _ptr(workspace),
+                  0 if workspace is None else workspace.numel() * workspace.element_size(), stream_h)
+        st = lib.lion_attn_fwd_ex(ctypes.byref(a))
+    _check(st)
+    return out
+
+
+def rnn_step(q, k, v, log_lambda, S, z, y_part, c_part, mask_kind, stream=None):
+    """One token of one direction of the recurrent form for B*H heads, in place
+    on the caller-owned state ``S`` [B,H,d,d] and ``z`` [B,H,d] (float32)."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    B, H, d = q.shape
+    st = lib.lion_rnn_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(S), _ptr(z),
+                           _ptr(y_part), _ptr(c_part), B, H, d, mask_kind, _dtype_code(q),
+                           _stream_handle(stream))
+    _check(st)
+    return y_part, c_part

@@ -1,0 +1,154 @@
+/*
+ * lion.h -- C ABI of liblion.so, the GB300 (sm_103a) implementation of the
+ * LION bidirectional masked linear-attention operator.
+ *
+ * The operator (rebuttal page "LION: A bidirectional framework that trains
+ * like a Transformer and infers like an RNN", reply "Concern 1",
+ * Theorem 3.3 Eq 25):
+ *
+ *     Y = SCALE( (phi(Q) phi(K)^T) (.) M ) V
+ *
+ * per (batch b, head h), rows i, j in [0, L):
+ *   s_ij = phi(q_i) . phi(k_j)
+ *   M_ij = prod_{t = min(i,j)+1}^{max(i,j)} lambda_t,   M_ii = 1
+ *   y_i  = sum_j M_ij s_ij v_j / sum_j M_ij s_ij          (SCALE = row sum)
+ *
+ * Masks (rebuttal page, list of running examples; "LION Part IV - Results"):
+ *   LION_MASK_LIT  lambda = 1, M all ones ("LION-LIT" / "LION-fire").
+ *   LION_MASK_D    one fixed lambda per head, M_ij = lambda_h^|i-j|
+ *                  ("LION-D" / "LION-RETNET").
+ *   LION_MASK_S    a lambda per token ("LION-S", selective).
+ * Feature maps (rebuttal page, reply "4) Default non-linearity"):
+ *   elu(x)+1 for LIT and D, SiLU followed by an L2 normalisation over the
+ *   head dimension (norm clamped below at 1e-12) for S.
+ * Forms, all computing the same Y (Theorem 3.3; blog "LION Chunk"):
+ *   LION_FORM_FULL   quadratic attention with the mask generated on the fly.
+ *   LION_FORM_RNN    forward and backward recurrences (Theorem 3.3 Eq 20-24)
+ *                    keeping only y^{F/B}_i and c^{F/B}_i (reply "1:
+ *                    Recurrence Form", O(Ld + L) memory).
+ *   LION_FORM_CHUNK  chunkwise: masked attention inside chunks of `chunk`
+ *                    tokens, chunk states carried by forward and backward
+ *                    scans.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are row-major and contiguous.  q, k, v, out: [B][H][L][d].
+ *   - log_lambda holds log(lambda) (finite, <= 0): LIT ignores it (NULL
+ *     allowed); D: [H]; S: [B][H][L].  All float32.
+ *   - out is float32.  Every pointer is device memory owned by the caller.
+ *   - Calls are asynchronous on `stream`.  Argument errors are detected on
+ *     the host before anything is launched and return a status; nothing is
+ *     written then.  A launch or runtime failure returns LION_ERR_CUDA.
+ *   - d must be 16, 32, 64 or 128.  q, k, v, out and workspace must be
+ *     16-byte aligned.
+ *   - The library keeps no state between calls except a per-device cache of
+ *     device properties and of resolved driver entry points.
+ */
+#ifndef LION_H_
+#define LION_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LION_OK = 0,
+  LION_ERR_INVALID_ARG = 1,  /* null pointer, bad enum, size or alignment   */
+  LION_ERR_UNSUPPORTED = 2,  /* valid request this build does not handle   */
+  LION_ERR_CUDA = 3,         /* a CUDA call or kernel launch failed        */
+  LION_ERR_NO_MEMORY = 4,    /* workspace allocation failed                */
+  LION_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up         */
+} lion_status;
+
+typedef enum { LION_MASK_LIT = 0, LION_MASK_D = 1, LION_MASK_S = 2 } lion_mask_kind;
+typedef enum { LION_FORM_FULL = 0, LION_FORM_RNN = 1, LION_FORM_CHUNK = 2 } lion_form;
+typedef enum { LION_DTYPE_BF16 = 0, LION_DTYPE_FP32 = 1 } lion_dtype;
+typedef enum {
+  LION_PHI_DEFAULT = 0,   /* elu+1 for LIT and D, SiLU + L2 for S */
+  LION_PHI_ELU1 = 1,
+  LION_PHI_SILU_L2 = 2,
+  LION_PHI_IDENTITY = 3   /* phi(x) = x */
+} lion_phi;
+
+/* Largest L the FULL form accepts (its cost is O(L^2 d)); larger L returns
+ * LION_ERR_UNSUPPORTED. */
+#define LION_FULL_MAX_L 8192
+
+/*
+ * lion_attn_fwd -- the operator for bfloat16 q, k, v.
+ *   q, k, v     [B][H][L][d] bfloat16, device.
+ *   log_lambda  see conventions (device; NULL for LIT).
+ *   mask_kind   lion_mask_kind.   form: lion_form.
+ *   chunk       chunk length for LION_FORM_CHUNK (>= 1; any value, the
+ *               result does not depend on it up to rounding); ignored by the
+ *               other forms.
+ *   out         [B][H][L][d] float32, device, written entirely.
+ * Workspace, when the form needs one, is taken from the stream-ordered
+ * allocator (cudaMallocAsync/cudaFreeAsync on `stream`); use
+ * lion_attn_fwd_ex to pass one instead.
+ */
+lion_status lion_attn_fwd(const void* q, const void* k, const void* v,
+                          const float* log_lambda, int B, int H, int L, int d,
+                          int mask_kind, int form, int chunk, float* out,
+                          cudaStream_t stream);
+
+/* Every option of the operator in one struct. */
+typedef struct {
+  const void* q;             /* [B][H][L][d], dtype below                  */
+  const void* k;
+  const void* v;
+  const float* log_lambda;   /* see conventions                            */
+  float* out;                /* [B][H][L][d] float32                       */
+  int B, H, L, d;
+  int mask_kind;             /* lion_mask_kind                             */
+  int form;                  /* lion_form                                  */
+  int chunk;                 /* LION_FORM_CHUNK only                       */
+  int dtype;                 /* lion_dtype of q, k, v                      */
+  int phi;                   /* lion_phi                                   */
+  void* workspace;           /* device, 256-byte aligned, or NULL          */
+  size_t workspace_bytes;    /* >= lion_attn_workspace_bytes(...) if given */
+  cudaStream_t stream;
+} lion_args;
+
+/*
+ * lion_attn_fwd_ex -- as lion_attn_fwd with a dtype (BF16 or FP32 inputs), a
+ * feature-map override and an optional caller workspace.  With
+ * workspace == NULL the library allocates what it needs stream-ordered.
+ */
+lion_status lion_attn_fwd_ex(const lion_args* a);
+
+/* Workspace bytes lion_attn_fwd_ex needs for this problem (0 if none). */
+size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk);
+
+/*
+ * lion_rnn_step -- one token of one direction of the recurrent form, for
+ * B*H heads at once (Theorem 3.3 Eq 20-24; the causal Linear-Transformer
+ * recurrence of reply "1: Recurrence Form" with a decay):
+ *     S <- lambda * S + phi(k) v^T,    z <- lambda * z + phi(k)
+ *     y_part = phi(q)^T S,             c_part = phi(q)^T z
+ *   q, k, v     [B][H][d] in `dtype` (lion_dtype), device.
+ *   log_lambda  LIT: ignored; D: [H]; S: [B][H] (this token's lambda; for
+ *               the backward direction pass lambda of the token after it).
+ *   S           [B][H][d][d] float32, row m = feature of phi(k), updated in place.
+ *   z           [B][H][d] float32, updated in place.
+ *   y_part      [B][H][d] float32 out;  c_part [B][H] float32 out.
+ * The caller owns the state.  Combining the two directions into y_i uses
+ * y_i = (yF_i + yB_i - s_ii v_i) / (cF_i + cB_i - s_ii), s_ii = phi(q_i).phi(k_i).
+ */
+lion_status lion_rnn_step(const void* q, const void* k, const void* v,
+                          const float* log_lambda, float* S, float* z,
+                          float* y_part, float* c_part, int B, int H, int d,
+                          int mask_kind, int dtype, cudaStream_t stream);
+
+/* Static, human-readable text for a status. */
+const char* lion_status_string(lion_status s);
+
+/* Version of this ABI (bumped on any incompatible change). */
+int lion_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LION_H_ */

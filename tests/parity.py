@@ -1,0 +1,54 @@
+"""Comparison helpers for the GPU-vs-oracle parity tests.
+
+Error measure (per output row i of each head):
+
+    err_i = ||y_i - yref_i||_inf / ||yref_i||_inf
+
+must satisfy err_i <= tol * max(1, kappa_i), where
+kappa_i = sum_j M_ij |s_ij| / |sum_j M_ij s_ij| is the conditioning of the row
+sum.  kappa_i = 1 whenever the features are positive (elu+1); with SiLU
+features the row sum can cancel and the bound widens accordingly.  kappa is
+only computed (by the oracle, O(L d) per row) for rows that miss the plain
+bound, which keeps full-size checks fast.
+
+Tolerances: 2e-3 for bfloat16 inputs with float32 accumulation, 1e-5 for
+float32 inputs.
+"""
+import numpy as np
+
+TOL_BF16 = 2e-3
+TOL_FP32 = 1e-5
+
+
+def row_errors(y, ref):
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    num = np.max(np.abs(y - ref), axis=-1)
+    den = np.max(np.abs(ref), axis=-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = num / den
+    e[~np.isfinite(y).all(axis=-1)] = np.inf
+    e[(den == 0) & (num == 0)] = 0.0
+    return e
+
+
+def check_rows(oracle, y, ref, tol, q64, k64, ll64, mask_kind, phi_kind=0, max_kappa_rows=4096):
+    """Assert the per-row bound over y, ref of shape [B, H, L, d].  Returns a
+    summary dict (worst plain error, rows that needed kappa, worst scaled)."""
+    e = row_errors(y, ref)
+    bad = np.argwhere(e > tol)
+    worst_scaled = float(np.max(np.minimum(e, 1e300))) / tol if e.size else 0.0
+    if len(bad) > max_kappa_rows:
+        raise AssertionError(f"{len(bad)} rows exceed tol {tol} before conditioning "
+                             f"(worst {float(np.max(e)):.3e})")
+    scaled = []
+    for b, h, i in bad:
+        kap = oracle.row_kappa(q64, k64, ll64, mask_kind, int(b), int(h), int(i), int(i) + 1,
+                               phi_kind)[0]
+        s = e[b, h, i] / (tol * max(1.0, kap))
+        scaled.append(s)
+        assert s <= 1.0, (f"row (b={b}, h={h}, i={i}): err {e[b, h, i]:.3e} > "
+                          f"{tol:.1e} * max(1, kappa={kap:.3e})")
+    if scaled:
+        worst_scaled = max(float(np.max(np.where(e <= tol, e, 0))) / tol, max(scaled))
+    return {"max_err": float(np.max(e)), "kappa_rows": len(bad), "worst_scaled": worst_scaled}

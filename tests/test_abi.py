@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point include/lion.h declares, and rejects bad arguments
+with a status before launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lion.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bidirectional_masked_linear_gb300 import build, lion
+    path = build.build()
+    return lion.load(path)
+
+
+def _declared():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(lion_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    for want in ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_rnn_step", "lion_status_string",
+                 "lion_attn_workspace_bytes"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from bidirectional_masked_linear_gb300 import lion
+    out = subprocess.run(["nm", "-D", "--defined-only", lion.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b[TW] (\w+)", out))
+    for name in _declared():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_version(lib):
+    lib.lion_status_string.restype = ctypes.c_char_p
+    assert lib.lion_status_string(0) == b"ok"
+    assert b"invalid" in lib.lion_status_string(1)
+    assert lib.lion_status_string(99) == b"unknown status"
+    assert lib.lion_abi_version() == 1
+
+
+def test_workspace_query(lib):
+    from bidirectional_masked_linear_gb300 import lion
+    assert lion.workspace_bytes(2, 3, 10, 64, lion.FORM_FULL) == 0
+    assert lion.workspace_bytes(2, 3, 10, 64, lion.FORM_RNN) >= 2 * 3 * 10 * 4
+    assert lion.workspace_bytes(0, 3, 10, 64, lion.FORM_RNN) == 0
+    assert lion.workspace_bytes(1, 1, 10, 48, lion.FORM_RNN) == 0      # d unsupported
+
+
+def _fwd(lib, q=1, k=1, v=1, ll=None, B=1, H=1, L=8, d=64, mask=0, form=2, chunk=64, out=1):
+    vp = ctypes.c_void_p
+    return lib.lion_attn_fwd(vp(q * 4096 if q else 0), vp(k * 8192 if k else 0),
+                             vp(v * 12288 if v else 0), vp(ll), B, H, L, d, mask, form, chunk,
+                             vp(out * 16384 if out else 0), vp(0))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(k=0), dict(v=0), dict(out=0),
+    dict(B=0), dict(H=0), dict(L=0), dict(d=48), dict(d=0),
+    dict(mask=3), dict(mask=-1), dict(form=3), dict(chunk=0),
+    dict(mask=1, ll=None), dict(mask=2, ll=None),
+])
+def test_invalid_arguments_rejected_before_launch(lib, kw):
+    # All of these fail host-side validation; no pointer is dereferenced.
+    assert _fwd(lib, **kw) == 1
+
+
+def test_host_pointers_rejected(lib):
+    # Non-null but host-only memory (no GPU mapping): refused, never launched.
+    buf = (ctypes.c_char * 65536)()
+    base = ctypes.addressof(buf)
+    base = (base + 255) // 256 * 256
+    vp = ctypes.c_void_p
+    st = lib.lion_attn_fwd(vp(base), vp(base), vp(base), None, 1, 1, 8, 16, 0, 2, 4,
+                           vp(base), vp(0))
+    assert st == 1
+
+
+def test_misaligned_pointer_rejected(lib):
+    vp = ctypes.c_void_p
+    st = lib.lion_attn_fwd(vp(4096 + 2), vp(8192), vp(12288), None, 1, 1, 8, 64, 0, 2, 64,
+                           vp(16384), vp(0))
+    assert st == 1
+
+
+def test_rnn_step_invalid(lib):
+    vp = ctypes.c_void_p
+    args = [vp(4096)] * 3 + [vp(0)] + [vp(8192)] * 4
+    assert lib.lion_rnn_step(*args, 1, 1, 64, 0, 0, vp(0)) == 1      # not device memory
+    assert lib.lion_rnn_step(vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), 1, 1, 64, 0, 0,
+                             vp(0)) == 1
+    assert lib.lion_rnn_step(*args, 1, 1, 48, 0, 0, vp(0)) == 1
+    assert lib.lion_rnn_step(*args, 1, 1, 64, 1, 0, vp(0)) == 1      # LION-D without decay
+    assert lib.lion_rnn_step(*args, 1, 1, 64, 0, 7, vp(0)) == 1      # bad dtype
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding only marshals arguments: it never imports the oracle and
+    raises when the library is missing."""
+    src = open(os.path.join(ROOT, "bidirectional_masked_linear_gb300", "lion.py")).read()
+    assert "oracle" not in src
+    from bidirectional_masked_linear_gb300 import lion
+    saved = lion._lib
+    try:
+        lion._lib = None
+        with pytest.raises(RuntimeError):
+            lion.load("/nonexistent/liblion.so")
+    finally:
+        lion._lib = saved

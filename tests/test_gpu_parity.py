@@ -1,0 +1,220 @@
+"""GPU parity: the CUDA library (through its C ABI) against the float64 oracle
+on the same seeded inputs, element by element, for every mask and form, at
+small sizes (many tiles and ragged tails, edge cases) and at the full
+workload sizes."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from bidirectional_masked_linear_gb300 import lion, synth
+from parity import TOL_BF16, TOL_FP32, check_rows, row_errors
+
+pytestmark = pytest.mark.gpu
+
+MASK_NAME = {0: "lit", 1: "d", 2: "s"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bidirectional_masked_linear_gb300 import build
+    lion.load(build.build())
+
+
+def _cuda(inp):
+    out = {}
+    for key in ("q", "k", "v", "log_lambda"):
+        t = inp[key]
+        out[key] = None if t is None else t.cuda()
+    return out
+
+
+def run_gpu(inp, form, chunk=64, phi=0):
+    g = _cuda(inp)
+    y = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], form, chunk, phi=phi)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def f64(inp):
+    return (synth.as_f64(inp["q"]), synth.as_f64(inp["k"]), synth.as_f64(inp["v"]),
+            synth.as_f64(inp["log_lambda"]))
+
+
+def check(oracle_mod, y, ref, inp, tol, phi=0):
+    q, k, _, ll = f64(inp)
+    return check_rows(oracle_mod, y, ref, tol, q, k, ll, inp["mask"], phi)
+
+
+# --------------------------------------------------------------- tiny ---
+def test_tiny_lion_d_fp32_all_forms(oracle_mod):
+    """Tiny LION-D FP32 case (B=1, H=2, L=64, d=16, chunk 16): every form
+    against the brute-force oracle at 1e-5."""
+    inp = synth.workload_inputs("tiny_d_fp32", "d")
+    q, k, v, ll = f64(inp)
+    ref = oracle_mod.full(q, k, v, ll, 1)
+    for form, chunk in ((lion.FORM_FULL, 16), (lion.FORM_RNN, 16), (lion.FORM_CHUNK, 16),
+                        (lion.FORM_CHUNK, 5), (lion.FORM_CHUNK, 64)):
+        y = run_gpu(inp, form, chunk)
+        check(oracle_mod, y, ref, inp, TOL_FP32)
+
+
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+@pytest.mark.parametrize("dtype,tol", (("fp32", TOL_FP32), ("bf16", TOL_BF16)))
+def test_small_grid(oracle_mod, mask, dtype, tol):
+    """Ragged lengths, every head dim, every form, several chunk lengths."""
+    for L, d, chunks in ((1, 16, (1, 16)), (2, 32, (1, 3)), (17, 64, (4, 16, 64)),
+                         (65, 128, (32, 64)), (130, 64, (16, 64, 128, 200)),
+                         (197, 16, (32, 64, 128))):
+        inp = synth.make_inputs(2, 3, L, d, mask, dtype, seed=L * 7 + d)
+        q, k, v, ll = f64(inp)
+        ref = oracle_mod.full(q, k, v, ll, inp["mask"])
+        for form in (lion.FORM_FULL, lion.FORM_RNN):
+            check(oracle_mod, run_gpu(inp, form), ref, inp, tol)
+        for c in chunks:
+            check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, c), ref, inp, tol)
+
+
+@pytest.mark.parametrize("phi", (lion.PHI_ELU1, lion.PHI_SILU_L2, lion.PHI_IDENTITY))
+def test_feature_map_override(oracle_mod, phi):
+    inp = synth.make_inputs(1, 2, 70, 64, "s", "fp32", seed=5)
+    q, k, v, ll = f64(inp)
+    if phi == lion.PHI_IDENTITY:   # keep the row sums away from zero
+        for key in ("q", "k"):
+            inp[key] = inp[key].abs() + 0.1
+        q, k, v, ll = f64(inp)
+    ref = oracle_mod.full(q, k, v, ll, 2, phi)
+    for form in (lion.FORM_FULL, lion.FORM_RNN, lion.FORM_CHUNK):
+        check(oracle_mod, run_gpu(inp, form, 32, phi), ref, inp, TOL_FP32, phi)
+
+
+# ----------------------------------------------------------- edge cases --
+@pytest.mark.parametrize("mask", ("d", "s"))
+def test_vanishing_decay_is_identity(oracle_mod, mask):
+    """log lambda = -1e4: M = I and y_i = v_i."""
+    inp = synth.make_inputs(1, 2, 100, 64, mask, "bf16", seed=9)
+    inp["log_lambda"] = torch.full_like(inp["log_lambda"], -1e4)
+    v = synth.as_f64(inp["v"])
+    for form, c in ((lion.FORM_FULL, 64), (lion.FORM_RNN, 64), (lion.FORM_CHUNK, 64),
+                    (lion.FORM_CHUNK, 128), (lion.FORM_CHUNK, 7)):
+        e = row_errors(run_gpu(inp, form, c), v)
+        assert np.max(e) < TOL_BF16
+
+
+def test_unit_decay_equals_lit():
+    inp = synth.make_inputs(2, 2, 150, 64, "d", "bf16", seed=10)
+    inp["log_lambda"] = torch.zeros_like(inp["log_lambda"])
+    lit = dict(inp, log_lambda=None, mask=0)
+    for form in (lion.FORM_FULL, lion.FORM_RNN, lion.FORM_CHUNK):
+        a = run_gpu(inp, form, 64)
+        b = run_gpu(lit, form, 64)
+        assert np.max(row_errors(a, b)) < TOL_BF16
+
+
+def test_gpu_forms_agree():
+    """The three GPU forms agree with each other within the bf16 bound."""
+    for mask in ("lit", "d", "s"):
+        inp = synth.make_inputs(4, 3, 197, 64, mask, "bf16", seed=11)
+        ys = [run_gpu(inp, lion.FORM_FULL), run_gpu(inp, lion.FORM_RNN)] + \
+             [run_gpu(inp, lion.FORM_CHUNK, c) for c in (32, 64, 128)]
+        for y in ys[1:]:
+            e = row_errors(y, ys[0])
+            assert np.max(e) < TOL_BF16 or mask == "s"
+            if mask == "s":       # SiLU rows may be ill-conditioned: compare the bulk
+                assert np.quantile(e, 0.999) < TOL_BF16
+
+
+def test_errors_on_gpu():
+    inp = _cuda(synth.make_inputs(1, 1, 16, 64, "lit", "bf16"))
+    with pytest.raises(lion.LionError) as ei:
+        lion.attn_fwd(inp["q"], inp["k"], inp["v"], None, 0, lion.FORM_CHUNK, 0)
+    assert ei.value.status == lion.ERR_INVALID_ARG
+    big = torch.empty((1, 1, lion.FULL_MAX_L + 1, 16), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lion.LionError) as ei:
+        lion.attn_fwd(big, big, big, None, 0, lion.FORM_FULL)
+    assert ei.value.status == lion.ERR_UNSUPPORTED
+    host = torch.zeros((1, 1, 16, 64), dtype=torch.bfloat16)        # host memory
+    with pytest.raises(lion.LionError):
+        lion.attn_fwd(host, host, host, None, 0, lion.FORM_CHUNK,
+                      out=torch.empty((1, 1, 16, 64), device="cuda"))
+
+
+def test_rnn_step_matches_rnn_form(oracle_mod):
+    """Feeding tokens one at a time through lion_rnn_step, forward and then
+    backward (with lambda of the next token), and combining with the diagonal
+    removed once reproduces the operator."""
+    B, H, L, d = 2, 3, 24, 32
+    inp = synth.make_inputs(B, H, L, d, "s", "bf16", seed=12)
+    q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
+    ll = inp["log_lambda"].cuda()
+    yF = torch.empty((B, H, L, d), device="cuda")
+    cF = torch.empty((B, H, L), device="cuda")
+    yB = torch.empty_like(yF)
+    cB = torch.empty_like(cF)
+    for direction in (0, 1):
+        S = torch.zeros((B, H, d, d), device="cuda")
+        z = torch.zeros((B, H, d), device="cuda")
+        order = range(L) if direction == 0 else range(L - 1, -1, -1)
+        for i in order:
+            if direction == 0:
+                lam = ll[:, :, i].contiguous()
+            else:
+                lam = ll[:, :, i + 1].contiguous() if i + 1 < L else torch.full((B, H), -1e4, device="cuda")
+            yp = torch.empty((B, H, d), device="cuda")
+            cp = torch.empty((B, H), device="cuda")
+            lion.rnn_step(q[:, :, i].contiguous(), k[:, :, i].contiguous(), v[:, :, i].contiguous(),
+                          lam, S, z, yp, cp, lion.MASK_S)
+            (yF if direction == 0 else yB)[:, :, i] = yp
+            (cF if direction == 0 else cB)[:, :, i] = cp
+    torch.cuda.synchronize()
+    fq = torch.nn.functional.normalize(torch.nn.functional.silu(q.double()), dim=-1, eps=1e-12)
+    fk = torch.nn.functional.normalize(torch.nn.functional.silu(k.double()), dim=-1, eps=1e-12)
+    sii = (fq * fk).sum(-1)
+    y = (yF.double() + yB.double() - sii[..., None] * v.double()) / (cF.double() + cB.double() - sii)[..., None]
+    qq, kk, vv, lll = f64(inp)
+    ref = oracle_mod.full(qq, kk, vv, lll, 2)
+    check(oracle_mod, y.cpu().numpy(), ref, inp, TOL_BF16)
+
+
+# ----------------------------------------------------- full workloads ----
+@functools.lru_cache(maxsize=None)
+def _workload(name, mask):
+    return synth.workload_inputs(name, mask)
+
+
+@functools.lru_cache(maxsize=None)
+def _reference(name, mask):
+    import oracle
+    inp = _workload(name, mask)
+    q, k, v, ll = f64(inp)
+    if synth.WORKLOADS[name].L > 1024:
+        return oracle.rnn(q, k, v, ll, inp["mask"], threads=0)
+    return oracle.full(q, k, v, ll, inp["mask"], threads=0)
+
+
+FULL_CASES = [
+    ("vit_t_s", "s", lion.FORM_CHUNK, 64),
+    ("vit_b", "lit", lion.FORM_CHUNK, 32), ("vit_b", "lit", lion.FORM_CHUNK, 64),
+    ("vit_b", "lit", lion.FORM_CHUNK, 128), ("vit_b", "lit", lion.FORM_FULL, 64),
+    ("vit_b", "d", lion.FORM_CHUNK, 32), ("vit_b", "d", lion.FORM_CHUNK, 64),
+    ("vit_b", "d", lion.FORM_CHUNK, 128), ("vit_b", "d", lion.FORM_FULL, 64),
+    ("vit_b", "s", lion.FORM_CHUNK, 32), ("vit_b", "s", lion.FORM_CHUNK, 64),
+    ("vit_b", "s", lion.FORM_CHUNK, 128), ("vit_b", "s", lion.FORM_FULL, 64),
+    ("bert_large", "d", lion.FORM_CHUNK, 64), ("bert_large", "d", lion.FORM_CHUNK, 128),
+    ("bert_large", "s", lion.FORM_CHUNK, 64), ("bert_large", "s", lion.FORM_CHUNK, 128),
+    ("hires_2496", "d", lion.FORM_CHUNK, 64), ("hires_2496", "d", lion.FORM_CHUNK, 128),
+    ("hires_2496", "d", lion.FORM_RNN, 64),
+    ("hires_2496", "s", lion.FORM_CHUNK, 64), ("hires_2496", "s", lion.FORM_CHUNK, 128),
+    ("hires_2496", "s", lion.FORM_RNN, 64),
+]
+
+
+@pytest.mark.parametrize("name,mask,form,chunk", FULL_CASES)
+def test_full_workload(oracle_mod, name, mask, form, chunk):
+    inp = _workload(name, mask)
+    ref = _reference(name, mask)
+    y = run_gpu(inp, form, chunk)
+    check(oracle_mod, y, ref, inp, TOL_BF16)
