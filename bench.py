@@ -168,9 +168,17 @@ def time_device(call, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def measure(name, mask, chunk, form, steps, warmup, flush):
+def _workload(name, batch=0):
     w = synth.WORKLOADS[name]
-    inp = synth.workload_inputs(name, mask)
+    if batch:
+        import dataclasses
+        w = dataclasses.replace(w, B=batch)
+    return w
+
+
+def measure(name, mask, chunk, form, steps, warmup, flush, batch=0):
+    w = _workload(name, batch)
+    inp = synth.make_inputs(w.B, w.H, w.L, w.d, mask, w.dtype, w.seed, w.lam)
     dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
     out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
     fcode = lion.FORMS[form]
@@ -288,6 +296,9 @@ def main():
     ap.add_argument("--form", default="chunk", choices=("chunk", "full", "rnn"))
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -309,7 +320,7 @@ def main():
     with Clocks(local) as clk:
         t_wall = time.perf_counter()
         w, inp, times, _keep = measure(args.workload, args.mask, args.chunk, args.form,
-                                       args.steps, args.warmup, flush)
+                                       args.steps, args.warmup, flush, args.batch)
         t_wall = time.perf_counter() - t_wall
     torch.cuda.synchronize()
     _barrier(dist)
@@ -320,8 +331,12 @@ def main():
     value = ws * tokens / (ms_all * 1e-3)
     abytes = algorithmic_bytes(w, args.mask)
     achieved = abytes / (ms * 1e-3) / 1e9
-    e2e_ms, h2d, d2h = measure_e2e(w, inp, args.mask, args.chunk, args.form, 50, 5)
-    e2e_ms = _max_over_ranks(dist, e2e_ms)
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = measure_e2e(w, inp, args.mask, args.chunk, args.form, 50, 5)
+        e2e_ms = _max_over_ranks(dist, e2e_ms)
+        e2e = {"value": ws * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     secondary = None
     if not args.no_secondary and args.workload != "hires_2496":
@@ -351,8 +366,7 @@ def main():
                          "frac": achieved / hbm_peak, "traffic": None,
                          "peak_source": peak_src, "algorithmic_bytes": abytes},
             "cpu_baseline": cpu,
-            "e2e": {"value": ws * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": e2e,
             "gpu_launches": args.steps * kernels_per_call(args.form, args.chunk, w),
             "clocks": clocks,
             "wall_s_timed_region": t_wall,

@@ -6,6 +6,6 @@ ABI of ``include/lion.h``); :mod:`.lion` is its Python binding and
 """
 from .lion import (  # noqa: F401
     FORM_CHUNK, FORM_FULL, FORM_RNN, MASK_D, MASK_LIT, MASK_S, PHI_DEFAULT, PHI_ELU1,
-    PHI_IDENTITY, PHI_SILU_L2, LionError, attn_fwd, load, rnn_step, status_string,
+    PHI_IDENTITY, PHI_SILU_L2, LionError, attn_fwd, load, rnn_step, status_string, sync_status,
     workspace_bytes,
 )

@@ -60,7 +60,6 @@ lion_status validate(const lion_args* a) {
   if (a->mask_kind != LION_MASK_LIT && !device_accessible(a->log_lambda)) return LION_ERR_INVALID_ARG;
   if (a->workspace && !device_accessible(a->workspace)) return LION_ERR_INVALID_ARG;
   if (a->form == LION_FORM_FULL && a->L > LION_FULL_MAX_L) return LION_ERR_UNSUPPORTED;
-  if (a->form == LION_FORM_CHUNK && a->chunk > lion::kSimtMaxChunk) return LION_ERR_UNSUPPORTED;
   return LION_OK;
 }
 
@@ -112,7 +111,15 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
   p.chunk = a->chunk;
   cudaStream_t s = a->stream;
 
-  const size_t need = sizeof(float) * workspace_floats(a->B, a->H, a->L, a->d, a->form, a->chunk);
+  const bool use_tc = a->form == LION_FORM_CHUNK && lion::chunk_tc_supported(p);
+  if (a->form == LION_FORM_CHUNK && !use_tc && a->chunk > lion::kSimtMaxChunk) return LION_ERR_UNSUPPORTED;
+  int* dstatus = nullptr;
+  if (use_tc) {
+    dstatus = lion::device_status_ptr();
+    if (!dstatus) return LION_ERR_CUDA;
+  }
+  const size_t need =
+      use_tc ? 0 : sizeof(float) * workspace_floats(a->B, a->H, a->L, a->d, a->form, a->chunk);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
@@ -128,13 +135,30 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
   switch (a->form) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
-    case LION_FORM_CHUNK: e = lion::launch_chunk_simt(p, (float*)ws, s); break;
+    case LION_FORM_CHUNK:
+      e = use_tc ? lion::launch_chunk_tc(p, dstatus, s) : lion::launch_chunk_simt(p, (float*)ws, s);
+      break;
   }
   if (owned) {
     cudaError_t f = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = f;
   }
   return from_cuda(e);
+}
+
+lion_status lion_sync_status(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return LION_ERR_CUDA;
+  int* flag = lion::device_status_ptr();
+  if (!flag) return LION_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LION_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return LION_ERR_CUDA;
+    return LION_ERR_TIMEOUT;
+  }
+  return LION_OK;
 }
 
 lion_status lion_attn_fwd(const void* q, const void* k, const void* v, const float* log_lambda,

@@ -27,6 +27,15 @@ cudaError_t launch_rnn_step(const void* q, const void* k, const void* v, const f
                             float* S, float* z, float* y_part, float* c_part, int B, int H,
                             int d, int mask_kind, int phi, int dtype, cudaStream_t s);
 
+// Tensor-core chunkwise kernel (tcgen05 + TMEM + TMA): bf16, d = 64,
+// chunk = 64, L <= 256 (one CTA per head).
+bool chunk_tc_supported(const Problem& p);
+cudaError_t launch_chunk_tc(const Problem& p, int* status, cudaStream_t s);
+
+// Device-side status word that kernels set when a bounded wait gives up
+// (address on the current device; nullptr if it cannot be resolved).
+int* device_status_ptr();
+
 // Largest chunk the SIMT chunk kernel takes (its chunk-local prefix lives in
 // shared memory).
 constexpr int kSimtMaxChunk = 1024;

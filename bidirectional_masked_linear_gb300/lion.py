@@ -49,7 +49,7 @@ class _Args(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "lion_rnn_step",
-           "lion_status_string", "lion_abi_version")
+           "lion_status_string", "lion_abi_version", "lion_sync_status")
 
 
 def load(path: str = LIB_PATH):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
     lib.lion_rnn_step.restype = i
     lib.lion_status_string.argtypes = [i]
     lib.lion_status_string.restype = ctypes.c_char_p
+    lib.lion_sync_status.argtypes = [vp]
+    lib.lion_sync_status.restype = i
     lib.lion_abi_version.argtypes = []
     lib.lion_abi_version.restype = i
     _lib = lib
@@ -102,6 +104,12 @@ def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.float32:
         return DTYPE_FP32
     raise TypeError(f"q, k, v must be bfloat16 or float32, got {t.dtype}")
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise the stream and return the library's device status
+    (OK, or ERR_TIMEOUT if a kernel gave up on a bounded wait)."""
+    return int(load().lion_sync_status(_stream_handle(stream)))
 
 
 def workspace_bytes(B, H, L, d, form, chunk=64) -> int:

@@ -81,9 +81,10 @@ typedef enum {
  *   q, k, v     [B][H][L][d] bfloat16, device.
  *   log_lambda  see conventions (device; NULL for LIT).
  *   mask_kind   lion_mask_kind.   form: lion_form.
- *   chunk       chunk length for LION_FORM_CHUNK (>= 1; any value, the
- *               result does not depend on it up to rounding); ignored by the
- *               other forms.
+ *   chunk       chunk length for LION_FORM_CHUNK, 1 <= chunk <= 1024 (larger:
+ *               LION_ERR_UNSUPPORTED).  The result does not depend on it up
+ *               to rounding; bf16 with d = 64, chunk = 64 and L <= 256 runs
+ *               on the tensor cores.  Ignored by the other forms.
  *   out         [B][H][L][d] float32, device, written entirely.
  * Workspace, when the form needs one, is taken from the stream-ordered
  * allocator (cudaMallocAsync/cudaFreeAsync on `stream`); use
@@ -141,6 +142,16 @@ lion_status lion_rnn_step(const void* q, const void* k, const void* v,
                           const float* log_lambda, float* S, float* z,
                           float* y_part, float* c_part, int B, int H, int d,
                           int mask_kind, int dtype, cudaStream_t stream);
+
+/*
+ * lion_sync_status -- synchronise `stream`, then report whether any kernel
+ * of this library on the current device gave up on a bounded device-side
+ * wait since the last call (LION_ERR_TIMEOUT; the flag is then cleared).
+ * Kernels never spin unboundedly: a wait that runs out records the error,
+ * releases its tensor memory and returns.  LION_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+lion_status lion_sync_status(cudaStream_t stream);
 
 /* Static, human-readable text for a status. */
 const char* lion_status_string(lion_status s);

@@ -127,6 +127,12 @@ def test_gpu_forms_agree():
                 assert np.quantile(e, 0.999) < TOL_BF16
 
 
+def test_device_status_clean_after_calls():
+    inp = _cuda(synth.make_inputs(2, 2, 197, 64, "s", "bf16", seed=3))
+    lion.attn_fwd(inp["q"], inp["k"], inp["v"], inp["log_lambda"], 2, lion.FORM_CHUNK, 64)
+    assert lion.sync_status() == lion.OK
+
+
 def test_errors_on_gpu():
     inp = _cuda(synth.make_inputs(1, 1, 16, 64, "lit", "bf16"))
     with pytest.raises(lion.LionError) as ei:
