@@ -91,6 +91,17 @@ def test_feature_map_override(oracle_mod, phi):
         check(oracle_mod, run_gpu(inp, form, 32, phi), ref, inp, TOL_FP32, phi)
 
 
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_many_heads_ragged_lengths(oracle_mod, mask):
+    """More heads than SMs (each persistent CTA walks several heads) at every
+    chunk count and ragged tail the tensor-core chunk path takes."""
+    for L in (1, 5, 63, 64, 65, 128, 129, 200, 256):
+        inp = synth.make_inputs(50, 7, L, 64, mask, "bf16", seed=300 + L)
+        q, k, v, ll = f64(inp)
+        ref = oracle_mod.full(q, k, v, ll, inp["mask"], threads=0)
+        check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 64), ref, inp, TOL_BF16)
+
+
 # ----------------------------------------------------------- edge cases --
 @pytest.mark.parametrize("mask", ("d", "s"))
 def test_vanishing_decay_is_identity(oracle_mod, mask):
