@@ -1,0 +1,103 @@
+// lion_noalloc.cu -- the recurrent form of the operator for callers that
+// cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: code running inside a host framework
+// that owns every byte of device memory through its own allocator, or a
+// latency-critical loop where an allocation (and the implicit device-wide
+// synchronisation cudaMalloc/cudaFree may bring) is not allowed.  The
+// regular entry points either take a caller workspace or allocate one on
+// the stream; this one takes neither.  Its scratch -- the per-token forward
+// normaliser c^F_i that the backward sweep of the recurrent form reads back
+// -- lives in a fixed array of this library, `g_noalloc_cF`, sized for
+// LION_NOALLOC_MAX_HEAD_TOKENS = 2^20 head-tokens (B * H * L), i.e. 4 MiB.
+// Every GPU that loads the library holds that array until the process exits.
+//
+// Host code may not use the array's name as a device address (on the host it
+// is only a stand-in).  The device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, by the first call made on
+// that device; make that first call before any stream capture.
+//
+// All calls share the one array and it keeps the previous call's contents.
+// The recurrent kernel writes every c^F_i before it reads it, so nothing
+// needs clearing.  Calls whose executions overlap on the GPU (different
+// streams, no ordering between them) race on the array: order them.
+#include <stdint.h>
+
+#include "../../include/lion.h"
+#include "lion_common.cuh"
+#include "lion_internal.h"
+
+namespace {
+
+constexpr size_t kMaxHeadTokens = LION_NOALLOC_MAX_HEAD_TOKENS;
+
+static __device__ __align__(256) float g_noalloc_cF[kMaxHeadTokens];
+
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device).
+float* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_noalloc_ptr[dev]) {
+    float* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_cF) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+bool gpu_pointer(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeHost && at.devicePointer != nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" lion_status lion_attn_fwd_rnn_noalloc(const void* q, const void* k, const void* v,
+                                                 const float* log_lambda, int B, int H, int L, int d,
+                                                 int mask_kind, int dtype, float* out,
+                                                 cudaStream_t stream) {
+  if (!q || !k || !v || !out) return LION_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 1) return LION_ERR_INVALID_ARG;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return LION_ERR_INVALID_ARG;
+  if (mask_kind < LION_MASK_LIT || mask_kind > LION_MASK_S) return LION_ERR_INVALID_ARG;
+  if (dtype != LION_DTYPE_BF16 && dtype != LION_DTYPE_FP32) return LION_ERR_INVALID_ARG;
+  if (mask_kind != LION_MASK_LIT && !log_lambda) return LION_ERR_INVALID_ARG;
+  // the scratch holds one float per head-token
+  if ((unsigned long long)B * (unsigned long long)H * (unsigned long long)L > kMaxHeadTokens)
+    return LION_ERR_UNSUPPORTED;
+  if ((long long)L * d > 0x7fffffffLL) return LION_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LION_ERR_INVALID_ARG;
+  if (!gpu_pointer(q) || !gpu_pointer(k) || !gpu_pointer(v) || !gpu_pointer(out)) return LION_ERR_INVALID_ARG;
+  if (mask_kind != LION_MASK_LIT && !gpu_pointer(log_lambda)) return LION_ERR_INVALID_ARG;
+  float* scratch = noalloc_scratch();
+  if (!scratch) return LION_ERR_CUDA;
+  lion::Problem p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.log_lambda = log_lambda;
+  p.out = out;
+  p.B = B;
+  p.H = H;
+  p.L = L;
+  p.d = d;
+  p.mask_kind = mask_kind;
+  p.phi = lion::resolve_phi(mask_kind, LION_PHI_DEFAULT);
+  p.dtype = dtype;
+  p.chunk = 1;
+  return lion::launch_rnn_simt(p, scratch, stream) == cudaSuccess ? LION_OK : LION_ERR_CUDA;
+}

@@ -49,7 +49,9 @@ class _Args(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "lion_rnn_step",
-           "lion_status_string", "lion_abi_version", "lion_sync_status")
+           "lion_status_string", "lion_abi_version", "lion_sync_status",
+           "lion_attn_fwd_rnn_noalloc")
+NOALLOC_MAX_HEAD_TOKENS = 1 << 20
 
 
 def load(path: str = LIB_PATH):
@@ -72,6 +74,8 @@ def load(path: str = LIB_PATH):
     lib.lion_rnn_step.restype = i
     lib.lion_status_string.argtypes = [i]
     lib.lion_status_string.restype = ctypes.c_char_p
+    lib.lion_attn_fwd_rnn_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
+    lib.lion_attn_fwd_rnn_noalloc.restype = i
     lib.lion_sync_status.argtypes = [vp]
     lib.lion_sync_status.restype = i
     lib.lion_abi_version.argtypes = []
@@ -147,6 +151,21 @@ def attn_fwd(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None
                   form, chunk, dt, phi, _ptr(workspace),
                   0 if workspace is None else workspace.numel() * workspace.element_size(), stream_h)
         st = lib.lion_attn_fwd_ex(ctypes.byref(a))
+    _check(st)
+    return out
+
+
+def attn_fwd_rnn_noalloc(q, k, v, log_lambda, mask_kind, out=None, stream=None):
+    """The recurrent form without any device allocation: the library's fixed
+    scratch array holds the per-token normalisers (B*H*L <= 2^20)."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    B, H, L, d = q.shape
+    if out is None:
+        out = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    st = lib.lion_attn_fwd_rnn_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), B, H, L, d,
+                                       mask_kind, _dtype_code(q), _ptr(out), _stream_handle(stream))
     _check(st)
     return out
 

@@ -153,6 +153,30 @@ lion_status lion_rnn_step(const void* q, const void* k, const void* v,
  */
 lion_status lion_sync_status(cudaStream_t stream);
 
+/*
+ * lion_attn_fwd_rnn_noalloc -- the recurrent form (LION_FORM_RNN, default
+ * feature map) for callers that cannot allocate device memory: code inside
+ * a host framework that owns all device memory through its own allocator,
+ * or a latency-critical loop that must not call cudaMalloc/cudaFree (which
+ * may synchronise the device).  The paper has no counterpart; this is an
+ * interface convenience of this library.
+ *   Arguments as lion_attn_fwd_ex with form = LION_FORM_RNN; dtype is
+ *   LION_DTYPE_BF16 or LION_DTYPE_FP32 for q, k, v.
+ *   Scratch: a fixed device array of this library holding one float per
+ *   head-token, so B * H * L <= LION_NOALLOC_MAX_HEAD_TOKENS (4 MiB array,
+ *   held on every GPU that loads the library until the process exits);
+ *   larger problems return LION_ERR_UNSUPPORTED before anything launches.
+ *   Nothing is allocated, ever.  The first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress) for that device: make it
+ *   before any stream capture.  Every call shares the array; calls that
+ *   overlap on the GPU (unordered streams) race on it -- order them.
+ */
+#define LION_NOALLOC_MAX_HEAD_TOKENS (1u << 20)
+lion_status lion_attn_fwd_rnn_noalloc(const void* q, const void* k, const void* v,
+                                      const float* log_lambda, int B, int H, int L, int d,
+                                      int mask_kind, int dtype, float* out,
+                                      cudaStream_t stream);
+
 /* Static, human-readable text for a status. */
 const char* lion_status_string(lion_status s);
 
