@@ -63,10 +63,11 @@ def algorithmic_bytes(w, mask: str) -> int:
 
 
 def kernels_per_call(form: str, chunk: int, w) -> int:
-    """Kernel launches one operator call makes (the library launches exactly
-    one kernel per call on every current path)."""
-    del form, chunk, w
-    return 1
+    """Kernel launches one operator call makes: the tensor-core chunk path
+    (bf16, d=64, chunk 64) takes one launch up to 256 tokens and three
+    (pre-pass, segment scan, main pass) beyond; every other path one."""
+    tc = form == "chunk" and chunk == 64 and w.d == 64 and w.dtype == "bf16"
+    return 3 if tc and w.L > 256 else 1
 
 
 class Clocks:

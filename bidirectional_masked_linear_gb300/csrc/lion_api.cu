@@ -29,11 +29,9 @@ bool device_accessible(const void* p) {
 bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 
-// Workspace in floats for (form, path).
-size_t workspace_floats(int B, int H, int L, int d, int form, int chunk) {
-  (void)d;
-  (void)chunk;
-  if (form == LION_FORM_RNN || form == LION_FORM_CHUNK) return (size_t)B * H * L;
+// Workspace bytes for (form, path).
+size_t simt_workspace_bytes(int B, int H, int L, int form) {
+  if (form == LION_FORM_RNN || form == LION_FORM_CHUNK) return sizeof(float) * (size_t)B * H * L;
   return 0;
 }
 
@@ -89,7 +87,12 @@ const char* lion_status_string(lion_status s) {
 
 size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk) {
   if (B < 1 || H < 1 || L < 1 || !valid_d(d)) return 0;
-  return sizeof(float) * workspace_floats(B, H, L, d, form, chunk);
+  size_t need = simt_workspace_bytes(B, H, L, form);
+  if (form == LION_FORM_CHUNK && d == 64 && chunk == 64) {
+    const size_t tc = lion::chunk_tc_workspace_bytes(B, H, L);
+    if (tc > need) need = tc;
+  }
+  return need;
 }
 
 lion_status lion_attn_fwd_ex(const lion_args* a) {
@@ -118,8 +121,8 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
     dstatus = lion::device_status_ptr();
     if (!dstatus) return LION_ERR_CUDA;
   }
-  const size_t need =
-      use_tc ? 0 : sizeof(float) * workspace_floats(a->B, a->H, a->L, a->d, a->form, a->chunk);
+  const size_t need = use_tc ? lion::chunk_tc_workspace_bytes(a->B, a->H, a->L)
+                             : simt_workspace_bytes(a->B, a->H, a->L, a->form);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
@@ -136,7 +139,7 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
     case LION_FORM_CHUNK:
-      e = use_tc ? lion::launch_chunk_tc(p, dstatus, s) : lion::launch_chunk_simt(p, (float*)ws, s);
+      e = use_tc ? lion::launch_chunk_tc(p, ws, dstatus, s) : lion::launch_chunk_simt(p, (float*)ws, s);
       break;
   }
   if (owned) {

@@ -28,9 +28,12 @@ cudaError_t launch_rnn_step(const void* q, const void* k, const void* v, const f
                             int d, int mask_kind, int phi, int dtype, cudaStream_t s);
 
 // Tensor-core chunkwise kernel (tcgen05 + TMEM + TMA): bf16, d = 64,
-// chunk = 64, L <= 256 (one CTA per head).
+// chunk = 64, any L.  Sequences longer than 256 tokens take three launches
+// and a workspace of chunk_tc_workspace_bytes (0 for L <= 256).
 bool chunk_tc_supported(const Problem& p);
-cudaError_t launch_chunk_tc(const Problem& p, int* status, cudaStream_t s);
+size_t chunk_tc_workspace_bytes(int B, int H, int L);
+int chunk_tc_launches(int B, int H, int L);
+cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_t s);
 
 // Device-side status word that kernels set when a bounded wait gives up
 // (address on the current device; nullptr if it cannot be resolved).

@@ -1,5 +1,5 @@
 // lion_tc.cu -- chunkwise LION forward on the 5th-generation tensor cores
-// (tcgen05 + TMEM + TMA), bfloat16 inputs, head dim 64, chunk 64.
+// (tcgen05 + TMEM + TMA), bfloat16 inputs, head dim 64, chunk 64, any L.
 //
 // Chunkwise form ("LION Part IV - Results", "LION Chunk"; rebuttal page
 // "LION: A bidirectional framework ...", reply "4: Practicality of Recurrent
@@ -9,44 +9,58 @@
 //   intra     num_i += sum_{j in c} M_ij s_ij [v_j; 1],  M_ij = exp(p_max - p_min)
 //   states    U^F_c = sum_j exp(p_e - p_j) phi(k_j) [v_j; 1]^T
 //             U^B_c = sum_j exp(p_j - p_s) phi(k_j) [v_j; 1]^T
-//   scans     F_{c+1} = exp(T_c) F_c + U^F_c,
-//             G_{c-1} = exp(P_{s_{c+1}} - P_{s_c}) G_c + U^B_c
+//   scans     F_{c+1} = exp(T_c) F_c + U^F_c            (F_c anchored at e_{c-1})
+//             G_{c-1} = exp(P_{s_{c+1}} - P_{s_c}) G_c + U^B_c   (G_c at s_{c+1})
 //   apply     num_i += a_i phi(q_i) [F_c z^F_c] + b_i phi(q_i) [G_c z^G_c]
 //             a_i = exp(P_i - P_{e_{c-1}}),  b_i = exp(P_{s_{c+1}} - P_i)
 //   y_i = num_i[0:d] / num_i[d]
 //
+// The same recurrences chain 256-token blocks (four chunks) and segments of
+// blocks: the state leaving one block is the state entering the next.
+//
 // Normalisers ride on the tensor cores: products with V use B = [V_c | 1]
 // (N = 80; a constant tile whose first column is 1 is the second atom), so
 // U carries z as its column 64 and A V carries the intra-chunk row sum; the
-// scanned z vectors of all chunks sit in one small operand tile.
+// scanned z vectors sit in one small operand tile.
 //
 // Precision: MMA operands are fp16 (11-bit significand) with fp32
 // accumulation; phi(K), the decay-weighted phi(K), phi(Q), the chunk states,
-// z, V and the masked scores are each rounded once to fp16.  (One bf16
-// rounding of the unit-norm SiLU features costs ~5e-3 relative error; fp16
-// stays within about half of the 2e-3 budget.)  Precondition of this path:
+// z, V and the masked scores are each rounded once to fp16, and so are the
+// block boundary states exchanged through global memory for long sequences.
+// (One bf16 rounding of the unit-norm SiLU features costs ~5e-3 relative
+// error; fp16 stays within about half of the 2e-3 budget.)  Precondition:
 // |phi(q)|, |phi(k)|, |v| and the chunk states below the fp16 range (65504).
 //
-// Work split.  A persistent CTA (one per SM) walks heads bh = blockIdx.x,
-// blockIdx.x + gridDim.x, ...  Per head:
+// Work split.  Persistent CTAs (one per SM) walk work items.  An item is a
+// segment of one head: up to SEGB consecutive 256-token blocks.  Warp 16
+// issues TMA and tcgen05 MMAs; warps 0-15 do the CUDA-core stages and hand
+// tiles to it through mbarriers.  Per block:
 //   A  per chunk: phi(K_c) -> fp16 in place, V_c -> fp16 in place, the
 //      decay-weighted copies Kf_c, Kb_c; one M=128 MMA per chunk computes
 //      U^F_c (TMEM lanes 0-63) and U^B_c (lanes 64-127):
 //      A = [Kf_c ; Kb_c]^T (MN-major, two atoms), B = [V_c | 1] (MN-major).
-//   B  scans over chunks (lanes 0-63 forward, 64-127 backward), writing the
-//      states entering each chunk as fp16 operand tiles.
-//   C  a two-deep pipeline over chunks: S = phi(Q_c) phi(K_c)^T,
-//      O_F = phi(Q_c) F_c, O_G = phi(Q_c) G_c, Z = phi(Q_c) [z tiles]
-//      (M=64 MMAs) run while the previous chunk's epilogue works; the decay
-//      mask is applied to S on the CUDA cores (factorised as
-//      exp(p_i - p_0) exp(p_0 - p_j) when the chunk's decay range allows);
-//      O_I = A [V_c | 1]; the epilogue combines, normalises and stores fp32.
-//      As chunk c of this head retires, TMA refills its K/V tiles with chunk
-//      c of the next head; Q streams through a four-slot ring.
+//   B  scans over chunks (lanes 0-63 forward, 64-127 backward), starting
+//      from the states entering the block, writing fp16 operand tiles.
+//   C  (main pass only) a two-deep pipeline over chunks:
+//      S = phi(Q_c) phi(K_c)^T, O_F = phi(Q_c) F_c, O_G = phi(Q_c) G_c,
+//      Z = phi(Q_c) [z tiles] (M=64 MMAs) overlap the previous chunk's
+//      epilogue; the decay mask is applied to S on the CUDA cores
+//      (factorised as exp(p_i - p_0) exp(p_0 - p_j) when the chunk's decay
+//      range allows); O_I = A [V_c | 1]; the epilogue combines, normalises
+//      and stores fp32.  Retired K/V tiles are refilled with the next
+//      block's chunks; Q streams through a four-slot ring.
+// Sequences longer than one block take three launches:
+//   pre-pass  blocks of each segment right to left (phases A and B only):
+//             writes the backward state entering each block from the right
+//             within its segment, and the segment's two summary states;
+//   scan      a small CUDA-core kernel chains the segment summaries into the
+//             states entering each segment;
+//   main      blocks left to right, the forward state carried in registers,
+//             the backward state entering each block rebuilt from the
+//             pre-pass state plus the decayed segment-level state.
 //
-// Every mbarrier wait is bounded (one waiting thread, then a voting barrier);
-// on timeout the CTA records an error in `status`, releases its TMEM and
-// returns.
+// Every mbarrier wait is bounded; on timeout the kernel records an error in
+// `status`, releases its TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -60,49 +74,86 @@ namespace {
 
 using namespace tc;
 
-constexpr int kC = 64;           // chunk length handled here
-constexpr int kD = 64;           // head dim
-constexpr int kMaxChunks = 4;    // L <= 256
-constexpr int kThreads = 512;
-constexpr int kTile = kC * 128;  // bytes of one 64-row x 64-element 16-bit swizzled tile
+constexpr int kC = 64;            // chunk length
+constexpr int kD = 64;            // head dim
+constexpr int kMaxChunks = 4;     // chunks per block
+constexpr int kBlock = kC * kMaxChunks;   // 256 tokens
+constexpr int kWorkerWarps = 16;  // CUDA-core stages
+constexpr int kThreads = (kWorkerWarps + 1) * 32;  // + one TMA/MMA issuer warp
+constexpr int kTile = kC * 128;   // bytes of one 64-row x 64-element 16-bit swizzled tile
 constexpr int kQSlots = 4;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr uint32_t kSleepNs = 20000u;            // longest sleep inside one try_wait
 constexpr float kMaxFactorRange = 80.f;          // exp(80) stays finite in fp32
+constexpr int kStateCols = 80;                   // global state rows: 64 values, z, padding
+
+enum { MODE_MAIN = 0, MODE_PRE = 1 };
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr int OFF_K = 0;                               // phi(K) tiles, one per chunk
 constexpr int OFF_V = OFF_K + kMaxChunks * kTile;      // V tiles
 constexpr int OFF_ONES = OFF_V + kMaxChunks * kTile;   // column 0 = 1: the normaliser atom
-constexpr int OFF_WORK = OFF_ONES + kTile;             // phase A: Kf/Kb tiles; B/C: states + z
-constexpr int OFF_A = OFF_WORK + 2 * kMaxChunks * kTile;  // masked scores, 2 buffers
+constexpr int OFF_WORK = OFF_ONES + kTile;             // A: Kf/Kb tiles; B/C: F, G tiles + z
+constexpr int OFF_A = OFF_WORK + (2 * kMaxChunks + 1) * kTile;  // masked scores, 2 buffers
 constexpr int OFF_Q = OFF_A + 2 * kTile;               // Q ring
 constexpr int OFF_P = OFF_Q + kQSlots * kTile;         // float[256] chunk-local prefix
-constexpr int OFF_E = OFF_P + 256 * 4;                 // float[2][2][64] mask factors per region
+constexpr int OFF_E = OFF_P + kBlock * 4;              // float[2][2][64] mask factors per region
 constexpr int OFF_MISC = OFF_E + 2 * 2 * kC * 4;       // float[8]: l at chunk starts
-constexpr int OFF_BAR = OFF_MISC + 8 * 4;
-constexpr int OFF_TSLOT = OFF_BAR + 16 * 8;
+constexpr int OFF_UNI = OFF_MISC + 8 * 4;              // CTA-uniform worker bookkeeping
+constexpr int OFF_BAR = OFF_UNI + 16 * 4;
+constexpr int OFF_TSLOT = OFF_BAR + 24 * 8;
 constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;      // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-// work-region tiles in phases B/C: F_c (c = 1..3) at 0..2, G_c (c = 0..2) at
-// 3..5, the z tile at 6 (column 2c: z^F_c, column 2c+1: z^G_c)
-constexpr int W_Z = 6;
+// work tiles in phases B/C: F_c at c, G_c at 4 + c, the z tile at 8
+// (column 2c: z^F_c, column 2c+1: z^G_c)
+constexpr int W_F = 0, W_G = 4, W_Z = 8;
 
-constexpr int BAR_KV = 0;    // + chunk
-constexpr int BAR_Q = 4;     // + slot
-constexpr int BAR_M1 = 8;    // + region: S, O_F, O_G, Z done
-constexpr int BAR_M2 = 10;   // + region: O_I done
-constexpr int BAR_A = 12;    // phase-A MMAs done
+// mbarriers: TMA completions (count 1, transaction bytes), tensor-core
+// commits (count 1) and worker hand-offs (one arrival per worker warp)
+constexpr int BAR_KV = 0;    // + chunk slot: K_c, V_c landed
+constexpr int BAR_Q = 4;     // + Q slot: Q chunk landed
+constexpr int BAR_RA = 8;    // + chunk slot: phase-A operand tiles written
+constexpr int BAR_DA = 12;   // phase-A MMAs done
+constexpr int BAR_RB = 13;   // state tiles written
+constexpr int BAR_RP = 14;   // + region: phi(Q_c) written
+constexpr int BAR_M1 = 16;   // + region: S, O_F, O_G, Z done
+constexpr int BAR_RE = 18;   // + region: masked scores written
+constexpr int BAR_M2 = 20;   // + region: O_I done
+constexpr int BAR_FR = 22;   // + region: chunk retired (TMEM region, K/V tiles free)
+constexpr int kNumBars = 24;
+__host__ __device__ constexpr uint32_t bar_count(int b) {
+  return (b >= BAR_RA && b < BAR_DA) || b == BAR_RB || (b >= BAR_RP && b < BAR_M1) ||
+                 (b >= BAR_RE && b < BAR_M2) || b >= BAR_FR
+             ? (uint32_t)kWorkerWarps
+             : 1u;
+}
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSlot = 80;       // phase A/B: chunk-state slot (64 values + z + 15 zero)
-constexpr uint32_t kRegion = 240;    // phase C: per in-flight chunk
+constexpr uint32_t kRegion = 216;    // phase C: per in-flight chunk
 constexpr uint32_t R_SI = 0, R_OF = 80, R_OG = 144, R_Z = 208;
+// state kept across the blocks of a segment (80 columns; lanes 0-63 forward
+// direction, 64-127 backward):
+//   main: forward state entering the next block / backward state entering the segment
+//   pre:  the segment's forward summary / backward state entering the next block
+constexpr uint32_t TM_KEEP = 2 * kRegion;   // 432
+
+// long-sequence exchange buffers (global, per block / per segment)
+constexpr int kGlocBytes = kD * kD * 2 + kD * 4;       // fp16 64x64 state + fp32 z
+constexpr int kSegSumFloats = 2 * kD * kStateCols + 4;  // U^F_seg, U^B_seg, T_seg
+constexpr int kSegInFloats = 2 * kD * kStateCols;      // F_in, G_in of the segment
 
 struct TcParams {
   float* out;
   const float* log_lambda;
   int BH, H, L;
+  int NBL;        // 256-token blocks per head
+  int SEGB;       // blocks per segment
+  int nseg;       // segments per head
+  uint8_t* gloc;       // [BH][NBL] backward state entering each block (within its segment)
+  float* segsum;       // [BH][nseg] segment summaries (pre-pass output)
+  const float* segin;  // [BH][nseg] states entering each segment (scan output)
   int* status;
 };
 
@@ -166,7 +217,45 @@ __device__ __forceinline__ uint64_t mnmaj(const uint8_t* tile, int k, uint32_t l
   return desc_sw128(smem_u32(tile) + 2048 * k, lbo, 1024);
 }
 
-template <int MASK, int PHI>
+__device__ __forceinline__ int nchunks_of(int L, int b) {
+  return min(kMaxChunks, (L - b * kBlock + kC - 1) / kC);
+}
+
+// Walks this CTA's blocks in processing order: items (segments of heads)
+// blockIdx.x, + gridDim.x, ...; blocks of a segment left to right (main) or
+// right to left (pre-pass).
+struct BlockCursor {
+  int item, b;
+  __device__ void first_of_item(const TcParams& p, int mode) {
+    const int seg = item % p.nseg;
+    b = mode == MODE_MAIN ? seg * p.SEGB : min(p.NBL, (seg + 1) * p.SEGB) - 1;
+  }
+  __device__ void begin(const TcParams& p, int mode) {
+    item = blockIdx.x;
+    if (item < p.BH * p.nseg) first_of_item(p, mode);
+  }
+  __device__ bool valid(const TcParams& p) const { return item < p.BH * p.nseg; }
+  __device__ void next(const TcParams& p, int mode) {
+    const int seg = item % p.nseg;
+    const int lo = seg * p.SEGB, hi = min(p.NBL, (seg + 1) * p.SEGB) - 1;
+    if (mode == MODE_MAIN ? b < hi : b > lo) {
+      b += mode == MODE_MAIN ? 1 : -1;
+    } else {
+      item += gridDim.x;
+      if (valid(p)) first_of_item(p, mode);
+    }
+  }
+};
+
+template <int MASK>
+__device__ __forceinline__ float ell_at(const TcParams& p, int bh, int t, float lh) {
+  if (t >= p.L) return 0.f;
+  if (MASK == MASK_S) return p.log_lambda[(size_t)bh * p.L + t];
+  if (MASK == MASK_D) return lh;
+  return 0.f;
+}
+
+template <int MASK, int PHI, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     lion_chunk64_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                            const __grid_constant__ CUtensorMap mapV, TcParams prm) {
@@ -179,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sMisc = reinterpret_cast<float*>(smem + OFF_MISC);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 8);
   auto Kt = [&](int c) { return smem + OFF_K + c * kTile; };
   auto Vt = [&](int c) { return smem + OFF_V + c * kTile; };
   auto Wt = [&](int i) { return sWork + i * kTile; };
@@ -186,22 +276,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto Qt = [&](int slot) { return smem + OFF_Q + slot * kTile; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = prm.L, NC = (L + kC - 1) / kC;
-  const int quarter = warp & 3, wg = warp >> 2;   // TMEM lane quarter, column group
-  bool ok = true;                                 // uniform across the CTA
-
-  // thread 0 waits on an mbarrier phase; the rest park in the voting barrier
-  auto wait_all = [&](int b, uint32_t parity) {
-    bool mine = true;
-    if (tid == 0) mine = mbar_wait(&bars[b], parity, kWaitCycles);
-    ok = __syncthreads_and(mine) && ok;
-  };
+  const int L = prm.L;
+  const int quarter = warp & 3, wg = (warp >> 2) & 3;   // TMEM lane quarter, column group
 
   if (tid == 0) {
-    prefetch_tmap(&mapQ);
     prefetch_tmap(&mapK);
     prefetch_tmap(&mapV);
-    for (int b = 0; b < 13; ++b) mbar_init(&bars[b], 1);
+    if (MODE == MODE_MAIN) prefetch_tmap(&mapQ);
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b));
+    *s_abort = 0;
     fence_mbar_init();
   }
   for (int x = tid; x < kC * 8; x += kThreads) {
@@ -214,321 +297,553 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
-  auto issue_kv = [&](int bh_, int c) {
-    mbar_arrive_expect_tx(&bars[BAR_KV + c], (uint32_t)(2 * kTile));
-    tma_load_3d(Kt(c), &mapK, &bars[BAR_KV + c], 0, c * kC, bh_);
-    tma_load_3d(Vt(c), &mapV, &bars[BAR_KV + c], 0, c * kC, bh_);
-  };
-  // the g-th Q chunk this CTA processes -> (head, chunk)
-  auto issue_q = [&](int g) {
-    const int itg = g / NC, c = g - itg * NC;
-    const int bh_ = blockIdx.x + itg * gridDim.x;
-    if (bh_ >= prm.BH) return;
-    const int sl = g % kQSlots;
-    mbar_arrive_expect_tx(&bars[BAR_Q + sl], (uint32_t)kTile);
-    tma_load_3d(Qt(sl), &mapQ, &bars[BAR_Q + sl], 0, c * kC, bh_);
-  };
-  if (tid == 0) {
-    for (int c = 0; c < NC; ++c) issue_kv(blockIdx.x, c);
-    for (int g = 0; g < kQSlots; ++g) issue_q(g);
-  }
-
-  int gq = 0;   // chunks this CTA has taken through phase C
-  int it = 0;
-  for (int bh = blockIdx.x; bh < prm.BH && ok; bh += gridDim.x, ++it) {
-    const int h = bh % prm.H;
-    const float lh = MASK == MASK_D ? prm.log_lambda[h] : 0.f;
-    // chunk-local inclusive prefixes (one warp per chunk, 2 tokens per lane)
-    if (warp < NC) {
-      const int c = warp, s = c * kC;
-      float l0 = 0.f, l1 = 0.f;
-      const int t0 = s + 2 * lane, t1 = t0 + 1;
-      if (MASK == MASK_S) {
-        const float* ll = prm.log_lambda + (size_t)bh * L;
-        l0 = t0 < L ? ll[t0] : 0.f;
-        l1 = t1 < L ? ll[t1] : 0.f;
-      } else if (MASK == MASK_D) {
-        l0 = t0 < L ? lh : 0.f;
-        l1 = t1 < L ? lh : 0.f;
+  // bounded wait on a barrier phase; any timeout makes every later wait return at once
+  auto waitb = [&](int b, uint32_t parity) -> bool {
+    if (*s_abort) return false;
+    if (mbar_try_wait(&bars[b], parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_sleep(&bars[b], parity, kSleepNs)) {
+      if (*s_abort) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        *s_abort = 1;
+        return false;
       }
-      const float pair = l0 + l1;
-      float x = pair;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      const float excl = x - pair;
-      sP[s + 2 * lane] = excl + l0;
-      sP[s + 2 * lane + 1] = excl + l0 + l1;
-      if (lane == 0) sMisc[c] = l0;   // l at s_c
     }
-    if (tid == 0) sMisc[NC] = 0.f;    // no token after the sequence
-    __syncthreads();
+    return true;
+  };
 
-    // ---------------- phase A: chunk states ------------------------------
-    for (int c = 0; c < NC; ++c) {
-      wait_all(BAR_KV + c, it & 1);
-      if (!ok) break;
-      const int len = min(kC, L - c * kC);
-      const int r = tid >> 3, c8 = tid & 7;
-      float x[8];
-      unpack8_bf(*chunk16(Kt(c), r, c8), x);
-      phi8<PHI>(x);      // every lane: phi8 shuffles within the row's 8 lanes
-      if (r >= len) {    // padding tokens contribute nothing
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      }
-      const uint4 kh = pack8_h(x);
-      *chunk16(Kt(c), r, c8) = kh;
-      unpack8_h(kh, x);  // the decay weights multiply the fp16 phi(k) that S sees
-      float wf = 1.f, wb = 1.f;
-      if (MASK != MASK_LIT) {
-        const float pj = sP[c * kC + r];
-        wf = __expf(sP[c * kC + len - 1] - pj);
-        wb = __expf(pj - sP[c * kC]);
-      }
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = wf * x[e];
-      *chunk16(Wt(2 * c), r, c8) = pack8_h(y);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = wb * x[e];
-      *chunk16(Wt(2 * c + 1), r, c8) = pack8_h(y);
-      float v8[8];
-      unpack8_bf(*chunk16(Vt(c), r, c8), v8);
-      *chunk16(Vt(c), r, c8) = pack8_h(v8);
-    }
-    if (!ok) break;
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
+  if (warp == kWorkerWarps) {
+    // =================== issuer warp: TMA and MMA =============================
+    if (lane == 0) {
+      int kvn[kMaxChunks] = {0, 0, 0, 0};   // loads issued per K/V slot
+      int ran[kMaxChunks] = {0, 0, 0, 0};   // phase-A hand-offs consumed per slot
+      auto issue_kv = [&](const BlockCursor& cur, int c) {
+        const int bh_ = cur.item / prm.nseg;
+        mbar_arrive_expect_tx(&bars[BAR_KV + c], (uint32_t)(2 * kTile));
+        tma_load_3d(Kt(c), &mapK, &bars[BAR_KV + c], 0, cur.b * kBlock + c * kC, bh_);
+        tma_load_3d(Vt(c), &mapV, &bars[BAR_KV + c], 0, cur.b * kBlock + c * kC, bh_);
+        ++kvn[c];
+      };
+      // Q ring: a second cursor runs kQSlots chunks ahead of consumption
+      BlockCursor qcur;
+      qcur.begin(prm, MODE);
+      int qc = 0, qg = 0;
+      auto issue_q_next = [&]() {
+        if (!qcur.valid(prm)) return;
+        const int sl = qg % kQSlots;
+        mbar_arrive_expect_tx(&bars[BAR_Q + sl], (uint32_t)kTile);
+        tma_load_3d(Qt(sl), &mapQ, &bars[BAR_Q + sl], 0, qcur.b * kBlock + qc * kC, qcur.item / prm.nseg);
+        ++qg;
+        if (++qc == nchunks_of(L, qcur.b)) {
+          qc = 0;
+          qcur.next(prm, MODE);
+        }
+      };
       const uint32_t idA = idesc_f16(128, 80, true, true);
-      for (int c = 0; c < NC; ++c) {
-        const uint32_t lbo_v = (uint32_t)(sOnes - Vt(c));
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tbase + kSlot * c, mnmaj(Wt(2 * c), k, kTile), mnmaj(Vt(c), k, lbo_v), idA, k > 0 ? 1u : 0u);
-      }
-      mma_commit(&bars[BAR_A]);
-    }
-    wait_all(BAR_A, it & 1);
-    if (!ok) break;
-    tc_fence_after();
-
-    // ---------------- phase B: scans -> fp16 state operand tiles ----------
-    {
-      // zero the z tile's first 16 columns (stale phase-A data otherwise)
-      if (tid < 2 * kC) *chunk16(Wt(W_Z), tid >> 1, tid & 1) = make_uint4(0u, 0u, 0u, 0u);
-      __syncthreads();
-      const bool fwd = quarter < 2;
-      const int m = 32 * (quarter & 1) + lane;
-      const int ncol = wg == 3 ? 2 : 1;   // column group 3 also carries the z column
-      float stv[2][16];
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) stv[a][e] = 0.f;
-      for (int cc = 0; cc < NC; ++cc) {
-        const int c = fwd ? cc : NC - 1 - cc;
-        const int len = min(kC, L - c * kC);
-        const bool write = fwd ? c > 0 : c < NC - 1;
-        uint8_t* dst = fwd ? Wt(c - 1) : Wt(3 + c);
-        float u[2][16];
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-          if (a < ncol) tmem_ld16(lane_addr(tbase, warp, kSlot * c + (a == 0 ? 16 * wg : 64)), u[a]);
-        if (write) {   // state entering chunk c
-          *chunk16(dst, m, 2 * wg) = pack8_h(stv[0]);
-          *chunk16(dst, m, 2 * wg + 1) = pack8_h(stv[0] + 8);
-          if (wg == 3) *elem16(Wt(W_Z), m, 2 * c + (fwd ? 0 : 1)) = __float2half_rn(stv[1][0]);
-        }
-        tmem_wait_ld();
-        float decay = 1.f;
-        if (MASK != MASK_LIT) {
-          const float T = sP[c * kC + len - 1];
-          decay = fwd ? __expf(T) : __expf(T - sMisc[c] + sMisc[c + 1]);
-        }
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-          if (a < ncol)
-#pragma unroll
-            for (int e = 0; e < 16; ++e) stv[a][e] = decay * stv[a][e] + u[a][e];
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---------------- phase C: two-deep pipeline over chunks ---------------
-    const uint32_t idS = idesc_f16(64, 64, false, false);
-    const uint32_t idO = idesc_f16(64, 64, false, true);
-    const uint32_t idI = idesc_f16(64, 80, false, true);
-    const uint32_t idZ = idesc_f16(64, 8, false, true);
-    const int i_row = 16 * quarter + lane;     // M=64 accumulator row of this lane
-    const bool row_thread = lane < 16;
-
-    // phi(Q_c) -> fp16, mask factors of chunk c, then the first MMA group
-    auto prep_and_mma1 = [&](int c, int g) {
-      const int sl = g % kQSlots, rg = g & 1;
-      wait_all(BAR_Q + sl, (g / kQSlots) & 1);
-      if (!ok) return;
-      const int len = min(kC, L - c * kC);
-      {
-        const int r = tid >> 3, c8 = tid & 7;
-        float x[8];
-        unpack8_bf(*chunk16(Qt(sl), r, c8), x);
-        phi8<PHI>(x);
-        if (r >= len) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-        *chunk16(Qt(sl), r, c8) = pack8_h(x);
-      }
-      if (MASK != MASK_LIT && tid < 2 * kC) {
-        // E[t] = exp(p_t - p_0), Einv[t] = exp(p_0 - p_t)
-        const int t = tid & 63;
-        const float d = sP[c * kC + t] - sP[c * kC];
-        sE[(rg * 2 + (tid >> 6)) * kC + t] = tid < 64 ? __expf(d) : __expf(-d);
-      }
-      fence_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
+      const uint32_t idS = idesc_f16(64, 64, false, false);
+      const uint32_t idO = idesc_f16(64, 64, false, true);
+      const uint32_t idI = idesc_f16(64, 80, false, true);
+      const uint32_t idZ = idesc_f16(64, 8, false, true);
+      auto mma1 = [&](int c, int g, bool hasF, bool hasG) {
+        const int rg = g & 1, sl = g % kQSlots;
         const uint32_t base = tbase + kRegion * rg;
         const uint8_t* qt = Qt(sl);
 #pragma unroll
         for (int k = 0; k < 4; ++k) mma_bf16(base + R_SI, kmaj(qt, k), kmaj(Kt(c), k), idS, k > 0 ? 1u : 0u);
-        if (c > 0) {
+        if (hasF) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(base + R_OF, kmaj(qt, k), mnmaj(Wt(c - 1), k, kTile), idO, k > 0 ? 1u : 0u);
+            mma_bf16(base + R_OF, kmaj(qt, k), mnmaj(Wt(W_F + c), k, kTile), idO, k > 0 ? 1u : 0u);
         }
-        if (c < NC - 1) {
+        if (hasG) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(base + R_OG, kmaj(qt, k), mnmaj(Wt(3 + c), k, kTile), idO, k > 0 ? 1u : 0u);
+            mma_bf16(base + R_OG, kmaj(qt, k), mnmaj(Wt(W_G + c), k, kTile), idO, k > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) mma_bf16(base + R_Z, kmaj(qt, k), mnmaj(Wt(W_Z), k, kTile), idZ, k > 0 ? 1u : 0u);
         mma_commit(&bars[BAR_M1 + rg]);
-      }
-    };
-
-    // masked scores -> fp16 A tile, then O_I = A [V_c | 1]
-    auto epi1_and_mma2 = [&](int c, int g) {
-      const int rg = g & 1, sl = g % kQSlots;
-      wait_all(BAR_M1 + rg, (g >> 1) & 1);
-      if (!ok) return;
-      tc_fence_after();
-      if (tid == 0) issue_q(g + kQSlots);   // this Q slot's MMAs are done
-      const int s = c * kC, len = min(kC, L - s);
-      const uint32_t base = tbase + kRegion * rg;
-      float w[16];
-      tmem_ld16(lane_addr(base, warp, R_SI + 16 * wg), w);
-      tmem_wait_ld();
-      if (row_thread) {
-        const int i = i_row;
-        const float* E = sE + (rg * 2) * kC;
-        const float* Einv = E + kC;
-        const bool factor = (MASK == MASK_LIT) || (sP[s] - sP[s + len - 1] < kMaxFactorRange);
-        const float Ei = MASK == MASK_LIT ? 1.f : E[i];
-        const float Einvi = MASK == MASK_LIT ? 1.f : Einv[i];
-        const float pi = sP[s + i];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = 16 * wg + e;
-          float mval;
-          if (MASK == MASK_LIT) {
-            mval = 1.f;
-          } else if (factor) {
-            mval = j <= i ? Ei * Einv[j] : Einvi * E[j];
-          } else {
-            const float pj = sP[s + j];
-            mval = __expf(j <= i ? pi - pj : pj - pi);
-          }
-          w[e] = (i < len && j < len) ? w[e] * mval : 0.f;
-        }
-        *chunk16(At(rg), i, 2 * wg) = pack8_h(w);
-        *chunk16(At(rg), i, 2 * wg + 1) = pack8_h(w + 8);
-      }
-      fence_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
+      };
+      auto mma2 = [&](int c, int g) {
+        const int rg = g & 1;
+        const uint32_t base = tbase + kRegion * rg;
         const uint32_t lbo_v = (uint32_t)(sOnes - Vt(c));
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_bf16(base + R_SI, kmaj(At(rg), k), mnmaj(Vt(c), k, lbo_v), idI, k > 0 ? 1u : 0u);
         mma_commit(&bars[BAR_M2 + rg]);
-      }
-      (void)sl;
-    };
+      };
 
-    // combine, normalise, store; then hand chunk c's K/V tiles to the next head
-    auto epi2 = [&](int c, int g) {
-      const int rg = g & 1;
-      wait_all(BAR_M2 + rg, (g >> 1) & 1);
-      if (!ok) return;
-      tc_fence_after();
-      const int s = c * kC, len = min(kC, L - s);
-      const bool hasF = c > 0, hasG = c < NC - 1;
-      const uint32_t base = tbase + kRegion * rg;
-      float oi[16], of[16], og[16], zz[16];
-      tmem_ld16(lane_addr(base, warp, R_SI + 16 * wg), oi);
-      const float dI = tmem_ld1(lane_addr(base, warp, R_SI + 64));
-      if (hasF) tmem_ld16(lane_addr(base, warp, R_OF + 16 * wg), of);
-      if (hasG) tmem_ld16(lane_addr(base, warp, R_OG + 16 * wg), og);
-      const float dF = tmem_ld1(lane_addr(base, warp, R_Z + 2 * c));
-      const float dG = tmem_ld1(lane_addr(base, warp, R_Z + 2 * c + 1));
-      tmem_wait_ld();
-      (void)zz;
-      if (row_thread && i_row < len) {
-        const int i = i_row;
-        const float pi = sP[s + i];
-        float a = 0.f, b = 0.f;
-        if (hasF) a = MASK == MASK_LIT ? 1.f : __expf(pi);
-        if (hasG) b = MASK == MASK_LIT ? 1.f : __expf(sP[s + len - 1] - pi + sMisc[c + 1]);
-        float den = dI;
-        if (hasF) den += a * dF;
-        if (hasG) den += b * dG;
-        const float inv = 1.f / den;
-        float y[16];
+      BlockCursor cur;
+      cur.begin(prm, MODE);
+      if (cur.valid(prm))
+        for (int c = 0; c < nchunks_of(L, cur.b); ++c) issue_kv(cur, c);
+      if (MODE == MODE_MAIN)
+        for (int i = 0; i < kQSlots; ++i) issue_q_next();
+      int g = 0, nb = 0;   // chunks through phase C, blocks done
+      bool good = true;
+      while (cur.valid(prm) && good) {
+        const int NC = nchunks_of(L, cur.b);
+        BlockCursor nxt = cur;
+        nxt.next(prm, MODE);
+        const bool has_next = nxt.valid(prm);
+        const int NCn = has_next ? nchunks_of(L, nxt.b) : 0;
+        // K/V slots this block does not use are free now: start the next block's loads
+        if (has_next)
+          for (int c = NC; c < NCn; ++c) issue_kv(nxt, c);
+        // phase A: one stacked MMA per chunk as soon as its tiles are ready
+        for (int c = 0; c < NC && good; ++c) {
+          good = waitb(BAR_RA + c, ran[c] & 1);
+          ++ran[c];
+          if (!good) break;
+          tc_fence_after();
+          const uint32_t lbo_v = (uint32_t)(sOnes - Vt(c));
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float acc = oi[e];
-          if (hasF) acc += a * of[e];
-          if (hasG) acc += b * og[e];
-          y[e] = acc * inv;
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tbase + kSlot * c, mnmaj(Wt(2 * c), k, kTile), mnmaj(Vt(c), k, lbo_v), idA, k > 0 ? 1u : 0u);
         }
-        float* orow = prm.out + ((size_t)bh * L + s + i) * kD + 16 * wg;
+        if (!good) break;
+        mma_commit(&bars[BAR_DA]);
+        if (MODE == MODE_PRE) {
+          // the K/V tiles are free once the phase-A MMAs have read them
+          good = waitb(BAR_DA, nb & 1);
+          if (!good) break;
+          if (has_next)
+            for (int c = 0; c < min(NC, NCn); ++c) issue_kv(nxt, c);
+        } else {
+          const bool hasFin = cur.b > 0, hasGin = cur.b < prm.NBL - 1;
+          good = waitb(BAR_RB, nb & 1);
+          if (!good) break;
+          tc_fence_after();
+          // phase C, in the order the workers produce their hand-offs
+          auto hf = [&](int c) { return c > 0 || hasFin; };
+          auto hg = [&](int c) { return c < NC - 1 || hasGin; };
+          good = waitb(BAR_RP + (g & 1), (g >> 1) & 1);
+          if (!good) break;
+          tc_fence_after();
+          mma1(0, g, hf(0), hg(0));
+          if (NC > 1) {
+            good = waitb(BAR_RP + ((g + 1) & 1), ((g + 1) >> 1) & 1);
+            if (!good) break;
+            tc_fence_after();
+            mma1(1, g + 1, hf(1), hg(1));
+          }
+          good = waitb(BAR_RE + (g & 1), (g >> 1) & 1);
+          if (!good) break;
+          tc_fence_after();
+          mma2(0, g);
+          issue_q_next();
+          for (int c = 1; c < NC && good; ++c) {
+            const int gc = g + c;
+            good = waitb(BAR_RE + (gc & 1), (gc >> 1) & 1);
+            if (!good) break;
+            tc_fence_after();
+            mma2(c, gc);
+            issue_q_next();
+            good = waitb(BAR_FR + ((gc - 1) & 1), ((gc - 1) >> 1) & 1);
+            if (!good) break;
+            if (c - 1 < NCn) issue_kv(nxt, c - 1);
+            if (c + 1 < NC) {
+              good = waitb(BAR_RP + ((gc + 1) & 1), ((gc + 1) >> 1) & 1);
+              if (!good) break;
+              tc_fence_after();
+              mma1(c + 1, gc + 1, hf(c + 1), hg(c + 1));
+            }
+          }
+          if (!good) break;
+          good = waitb(BAR_FR + ((g + NC - 1) & 1), ((g + NC - 1) >> 1) & 1);
+          if (!good) break;
+          if (NC - 1 < NCn) issue_kv(nxt, NC - 1);
+          g += NC;
+        }
+        ++nb;
+        cur = nxt;
+      }
+    }
+  } else {
+    // =================== worker warps: CUDA-core stages =======================
+    const int i_row = 16 * quarter + lane;   // M=64 accumulator row of this lane
+    const bool row_thread = lane < 16;
+    auto arrive = [&](int b) {   // every worker warp arrives once
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[b]);
+    };
+    auto worker_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kWorkerWarps * 32) : "memory"); };
+    // CTA-uniform bookkeeping lives in shared memory (register budget):
+    // [0..3] K/V loads consumed per slot, [4] rsum, [5] tseg, [6] lseg_after, [7] tcum
+    int* uni_i = reinterpret_cast<int*>(smem + OFF_UNI);
+    float* uni_f = reinterpret_cast<float*>(smem + OFF_UNI);
+    if (tid < 8) uni_i[tid] = 0;
+    worker_sync();
+    bool good = true;
+    int g = 0, nb = 0;
+    // phase-B thread role: state row m of the forward (quarters 0-1) or
+    // backward (2-3) direction, columns 16*wg.. (+ the z column for wg 3)
+    const bool fwd = quarter < 2;
+    const int m = 32 * (quarter & 1) + lane;
+    // the kept state (TM_KEEP) of this thread's row and columns
+    const uint32_t keep_addr = lane_addr(tbase, warp, TM_KEEP + 16 * wg);
+    const uint32_t keepz_addr = lane_addr(tbase, warp, TM_KEEP + 64);
+    auto keep_load = [&](float* v, float* vz) {
+      tmem_ld16(keep_addr, v);
+      float zz[16];
+      if (wg == 3) tmem_ld16(keepz_addr, zz);
+      tmem_wait_ld();
+      *vz = wg == 3 ? zz[0] : 0.f;
+    };
+    auto keep_store = [&](const float* v, float vz) {
+      tmem_st16(keep_addr, v);
+      if (wg == 3) {
+        float zz[16];
 #pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4*>(orow + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+        for (int e = 0; e < 16; ++e) zz[e] = 0.f;
+        zz[0] = vz;
+        tmem_st16(keepz_addr, zz);
+      }
+      tmem_wait_st();
+    };
+    BlockCursor cur;
+    cur.begin(prm, MODE);
+    int item_prev = -1;
+    while (cur.valid(prm) && good) {
+      const int bh = cur.item / prm.nseg, seg = cur.item % prm.nseg, b = cur.b;
+      const int h = bh % prm.H;
+      const float lh = MASK == MASK_D ? prm.log_lambda[h] : 0.f;
+      const int NC = nchunks_of(L, b);
+      const int bs = b * kBlock;
+      const bool hasFin = b > 0, hasGin = b < prm.NBL - 1;
+      const bool new_item = cur.item != item_prev;
+      item_prev = cur.item;
+      if (new_item) {
+        // per-segment starting states (long sequences only)
+        const size_t so = (size_t)cur.item;
+        float kv[16], kz = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) kv[e] = 0.f;
+        float tseg = 0.f, lseg_after = 0.f;
+        if (MODE == MODE_MAIN && prm.NBL > 1) {
+          const float* sin = prm.segin + so * kSegInFloats;
+          const float* src = sin + (fwd ? 0 : kD * kStateCols) + m * kStateCols;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) kv[e] = src[16 * wg + e];
+          if (wg == 3) kz = src[64];
+          tseg = prm.segsum[so * kSegSumFloats + 2 * kD * kStateCols];
+          lseg_after = ell_at<MASK>(prm, bh, min(prm.NBL, (seg + 1) * prm.SEGB) * kBlock, lh);
+        }
+        keep_store(kv, kz);
+        worker_sync();   // every worker has read the previous item's bookkeeping
+        if (tid == 0) {
+          uni_f[4] = 0.f;
+          uni_f[5] = tseg;
+          uni_f[6] = lseg_after;
+          uni_f[7] = 0.f;
+        }
+      }
+      // chunk-local inclusive prefixes (one warp per chunk, 2 tokens per lane)
+      if (warp < NC) {
+        const int c = warp, s = bs + c * kC;
+        const int t0 = s + 2 * lane, t1 = t0 + 1;
+        const float l0 = ell_at<MASK>(prm, bh, t0, lh), l1 = ell_at<MASK>(prm, bh, t1, lh);
+        const float pair = l0 + l1;
+        float x = pair;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        const float excl = x - pair;
+        sP[c * kC + 2 * lane] = excl + l0;
+        sP[c * kC + 2 * lane + 1] = excl + l0 + l1;
+        if (lane == 0) sMisc[c] = l0;   // l at s_c
+      }
+      if (tid == 0) sMisc[NC] = ell_at<MASK>(prm, bh, bs + NC * kC, lh);   // l after the block
+      worker_sync();
+      float tblk = 0.f;   // sum of l over the block
+      for (int c = 0; c < NC; ++c) tblk += sP[c * kC + min(kC, L - bs - c * kC) - 1];
+
+      // ---------------- phase A: phi(K), V, decay-weighted copies ---------
+      for (int c = 0; c < NC; ++c) {
+        good = waitb(BAR_KV + c, uni_i[c] & 1);
+        if (!good) break;
+        const int len = min(kC, L - bs - c * kC);
+        const int r = tid >> 3, c8 = tid & 7;
+        float x[8];
+        unpack8_bf(*chunk16(Kt(c), r, c8), x);
+        phi8<PHI>(x);      // every lane: phi8 shuffles within the row's 8 lanes
+        if (r >= len) {    // padding tokens contribute nothing
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        const uint4 kh = pack8_h(x);
+        *chunk16(Kt(c), r, c8) = kh;
+        unpack8_h(kh, x);  // the decay weights multiply the fp16 phi(k) that S sees
+        float wf = 1.f, wb = 1.f;
+        if (MASK != MASK_LIT) {
+          const float pj = sP[c * kC + r];
+          wf = __expf(sP[c * kC + len - 1] - pj);
+          wb = __expf(pj - sP[c * kC]);
+        }
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = wf * x[e];
+        *chunk16(Wt(2 * c), r, c8) = pack8_h(y);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = wb * x[e];
+        *chunk16(Wt(2 * c + 1), r, c8) = pack8_h(y);
+        float v8[8];
+        unpack8_bf(*chunk16(Vt(c), r, c8), v8);
+        *chunk16(Vt(c), r, c8) = pack8_h(v8);
+        fence_async_smem();
+        arrive(BAR_RA + c);
+      }
+      if (!good) break;
+
+      // ---------------- phase B: scans -> fp16 state operand tiles --------
+      good = waitb(BAR_DA, nb & 1);
+      if (!good) break;
+      tc_fence_after();
+      if (MODE == MODE_MAIN && tid < 2 * kC) *chunk16(Wt(W_Z), tid >> 1, tid & 1) = make_uint4(0u, 0u, 0u, 0u);
+      worker_sync();   // z tile cleared; every worker has read this block's K/V counters
+      if (tid == 0)
+        for (int c = 0; c < NC; ++c) ++uni_i[c];
+      {
+        // the state entering the block from this thread's direction: 16
+        // columns (st) plus, for column group 3, the normaliser z (stz)
+        float st[16], stz;
+        {
+          float kv[16], kz;
+          keep_load(kv, &kz);
+          if (MODE == MODE_MAIN) {
+            if (fwd) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) st[e] = kv[e];
+              stz = kz;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) st[e] = 0.f;
+              stz = 0.f;
+              if (hasGin) {
+                // G entering block b = G_loc(b) + exp(P_{s_seg_end} - P_{s_{b+1}}) G_in(seg)
+                const uint8_t* gl = prm.gloc + ((size_t)bh * prm.NBL + b) * kGlocBytes;
+                const __half* gv = reinterpret_cast<const __half*>(gl) + m * kD + 16 * wg;
+                const float rb = uni_f[5] - uni_f[7] - tblk;   // sum of l over this segment's blocks after b
+                const float f = __expf(rb - sMisc[NC] + uni_f[6]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) st[e] = __half2float(gv[e]) + f * kv[e];
+                if (wg == 3) stz = reinterpret_cast<const float*>(gl + kD * kD * 2)[m] + f * kz;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) st[e] = fwd ? 0.f : kv[e];
+            stz = fwd ? 0.f : kz;
+            if (!fwd) {
+              // the pre-pass records the backward state entering block b
+              uint8_t* gl = prm.gloc + ((size_t)bh * prm.NBL + b) * kGlocBytes;
+              __half* gv = reinterpret_cast<__half*>(gl) + m * kD + 16 * wg;
+#pragma unroll
+              for (int e = 0; e < 16; e += 2)
+                *reinterpret_cast<__half2*>(gv + e) = __floats2half2_rn(st[e], st[e + 1]);
+              if (wg == 3) reinterpret_cast<float*>(gl + kD * kD * 2)[m] = stz;
+            }
+          }
+        }
+        for (int cc = 0; cc < NC; ++cc) {
+          const int c = fwd ? cc : NC - 1 - cc;
+          const int len = min(kC, L - bs - c * kC);
+          float u[16];
+          tmem_ld16(lane_addr(tbase, warp, kSlot * c + 16 * wg), u);
+          float uz = 0.f;
+          if (wg == 3) uz = tmem_ld1(lane_addr(tbase, warp, kSlot * c + 64));
+          if (MODE == MODE_MAIN && (fwd ? (c > 0 || hasFin) : (c < NC - 1 || hasGin))) {
+            uint8_t* dst = fwd ? Wt(W_F + c) : Wt(W_G + c);   // state entering chunk c
+            *chunk16(dst, m, 2 * wg) = pack8_h(st);
+            *chunk16(dst, m, 2 * wg + 1) = pack8_h(st + 8);
+            if (wg == 3) *elem16(Wt(W_Z), m, 2 * c + (fwd ? 0 : 1)) = __float2half_rn(stz);
+          }
+          tmem_wait_ld();
+          float decay = 1.f;
+          if (MASK != MASK_LIT) {
+            const float T = sP[c * kC + len - 1];
+            decay = fwd ? __expf(T) : __expf(T - sMisc[c] + sMisc[c + 1]);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) st[e] = decay * st[e] + u[e];
+          stz = decay * stz + uz;
+        }
+        // states leaving the block
+        if (MODE == MODE_MAIN) {
+          if (fwd) keep_store(st, stz);
+        } else {
+          if (fwd) {
+            // U^F of the block, decayed to the segment end
+            float kv[16], kz;
+            keep_load(kv, &kz);
+            const float f = __expf(uni_f[4]);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) kv[e] += f * st[e];
+            keep_store(kv, kz + f * stz);
+          } else {
+            keep_store(st, stz);
+          }
+        }
       }
       tc_fence_before();
-      __syncthreads();
-      // K_c and V_c are no longer read: refill them with the next head's chunk c
-      if (tid == 0 && bh + (int)gridDim.x < prm.BH) issue_kv(bh + gridDim.x, c);
-    };
+      if (MODE == MODE_PRE) {
+        // segment summaries once the leftmost block is done
+        const int seg_lo = seg * prm.SEGB;
+        if (b == seg_lo) {
+          float* ss = prm.segsum + (size_t)cur.item * kSegSumFloats;
+          float* dst = ss + (fwd ? 0 : kD * kStateCols) + m * kStateCols;
+          float sv[16], sz;
+          keep_load(sv, &sz);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dst[16 * wg + e] = sv[e];
+          if (wg == 3) {
+            dst[64] = sz;
+#pragma unroll
+            for (int e = 65; e < kStateCols; ++e) dst[e] = 0.f;
+          }
+          if (tid == 0) ss[2 * kD * kStateCols] = uni_f[4] + tblk;
+        }
+        // TMEM slots are rewritten by the next block's phase A only after
+        // every worker passed this point
+        worker_sync();
+        if (tid == 0) uni_f[4] += tblk;
+      } else {
+        fence_async_smem();
+        arrive(BAR_RB);
 
-    prep_and_mma1(0, gq);
-    if (NC > 1 && ok) prep_and_mma1(1, gq + 1);
-    if (ok) epi1_and_mma2(0, gq);
-    for (int c = 1; c < NC && ok; ++c) {
-      epi1_and_mma2(c, gq + c);
-      if (ok) epi2(c - 1, gq + c - 1);
-      if (ok && c + 1 < NC) prep_and_mma1(c + 1, gq + c + 1);
+        // ---------------- phase C: two-deep pipeline over chunks ----------
+        auto hf = [&](int c) { return c > 0 || hasFin; };
+        auto hg = [&](int c) { return c < NC - 1 || hasGin; };
+        auto prep = [&](int c, int gg) -> bool {
+          const int sl = gg % kQSlots, rg = gg & 1;
+          if (!waitb(BAR_Q + sl, (gg / kQSlots) & 1)) return false;
+          const int len = min(kC, L - bs - c * kC);
+          const int r = tid >> 3, c8 = tid & 7;
+          float x[8];
+          unpack8_bf(*chunk16(Qt(sl), r, c8), x);
+          phi8<PHI>(x);
+          if (r >= len) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          }
+          *chunk16(Qt(sl), r, c8) = pack8_h(x);
+          if (MASK != MASK_LIT && tid < 2 * kC) {
+            // E[t] = exp(p_t - p_0), Einv[t] = exp(p_0 - p_t)
+            const int t = tid & 63;
+            const float d = sP[c * kC + t] - sP[c * kC];
+            sE[(rg * 2 + (tid >> 6)) * kC + t] = tid < 64 ? __expf(d) : __expf(-d);
+          }
+          fence_async_smem();
+          arrive(BAR_RP + rg);
+          if (MASK != MASK_LIT) worker_sync();   // mask factors visible to every worker
+          return true;
+        };
+        auto epi1 = [&](int c, int gg) -> bool {
+          const int rg = gg & 1;
+          if (!waitb(BAR_M1 + rg, (gg >> 1) & 1)) return false;
+          tc_fence_after();
+          const int len = min(kC, L - bs - c * kC);
+          const uint32_t base = tbase + kRegion * rg;
+          float w[16];
+          tmem_ld16(lane_addr(base, warp, R_SI + 16 * wg), w);
+          tmem_wait_ld();
+          if (row_thread) {
+            const int i = i_row;
+            const float* E = sE + (rg * 2) * kC;
+            const float* Einv = E + kC;
+            const bool factor = (MASK == MASK_LIT) || (sP[c * kC] - sP[c * kC + len - 1] < kMaxFactorRange);
+            const float Ei = MASK == MASK_LIT ? 1.f : E[i];
+            const float Einvi = MASK == MASK_LIT ? 1.f : Einv[i];
+            const float pi = sP[c * kC + i];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = 16 * wg + e;
+              float mval;
+              if (MASK == MASK_LIT) {
+                mval = 1.f;
+              } else if (factor) {
+                mval = j <= i ? Ei * Einv[j] : Einvi * E[j];
+              } else {
+                const float pj = sP[c * kC + j];
+                mval = __expf(j <= i ? pi - pj : pj - pi);
+              }
+              w[e] = (i < len && j < len) ? w[e] * mval : 0.f;
+            }
+            *chunk16(At(rg), i, 2 * wg) = pack8_h(w);
+            *chunk16(At(rg), i, 2 * wg + 1) = pack8_h(w + 8);
+          }
+          fence_async_smem();
+          tc_fence_before();
+          arrive(BAR_RE + rg);
+          return true;
+        };
+        auto epi2 = [&](int c, int gg) -> bool {
+          const int rg = gg & 1;
+          if (!waitb(BAR_M2 + rg, (gg >> 1) & 1)) return false;
+          tc_fence_after();
+          const int s = c * kC, len = min(kC, L - bs - s);
+          const bool hasF = hf(c), hasG = hg(c);
+          const uint32_t base = tbase + kRegion * rg;
+          float oi[16], of[16], og[16];
+          tmem_ld16(lane_addr(base, warp, R_SI + 16 * wg), oi);
+          const float dI = tmem_ld1(lane_addr(base, warp, R_SI + 64));
+          if (hasF) tmem_ld16(lane_addr(base, warp, R_OF + 16 * wg), of);
+          if (hasG) tmem_ld16(lane_addr(base, warp, R_OG + 16 * wg), og);
+          const float dF = tmem_ld1(lane_addr(base, warp, R_Z + 2 * c));
+          const float dG = tmem_ld1(lane_addr(base, warp, R_Z + 2 * c + 1));
+          tmem_wait_ld();
+          tc_fence_before();
+          arrive(BAR_FR + rg);   // this region (and chunk c's K/V tiles) may be reused
+          if (row_thread && i_row < len) {
+            const int i = i_row;
+            const float pi = sP[s + i];
+            float a = 0.f, bb = 0.f;
+            if (hasF) a = MASK == MASK_LIT ? 1.f : __expf(pi);
+            if (hasG) bb = MASK == MASK_LIT ? 1.f : __expf(sP[s + len - 1] - pi + sMisc[c + 1]);
+            float den = dI;
+            if (hasF) den += a * dF;
+            if (hasG) den += bb * dG;
+            const float inv = 1.f / den;
+            float y[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float acc = oi[e];
+              if (hasF) acc += a * of[e];
+              if (hasG) acc += bb * og[e];
+              y[e] = acc * inv;
+            }
+            float* orow = prm.out + ((size_t)bh * L + bs + s + i) * kD + 16 * wg;
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4*>(orow + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+          }
+          return true;
+        };
+
+        good = prep(0, g);
+        if (good && NC > 1) good = prep(1, g + 1);
+        if (good) good = epi1(0, g);
+        for (int c = 1; c < NC && good; ++c) {
+          good = epi1(c, g + c);
+          if (good) good = epi2(c - 1, g + c - 1);
+          if (good && c + 1 < NC) good = prep(c + 1, g + c + 1);
+        }
+        if (good) good = epi2(NC - 1, g + NC - 1);
+        g += NC;
+        // the next block's prefix overwrites sP/sMisc: every worker must be done reading them
+        worker_sync();
+        if (tid == 0) uni_f[7] += tblk;
+      }
+      ++nb;
+      cur.next(prm, MODE);
     }
-    if (ok) epi2(NC - 1, gq + NC - 1);
-    gq += NC;
   }
 
-  if (!ok && tid == 0) atomicExch(prm.status, 1);
-  tc_fence_before();
   __syncthreads();
+  if (tid == 0 && *s_abort) atomicExch(prm.status, 1);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -536,9 +851,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Chains segment summaries into the states entering each segment:
+//   F_in(s+1) = exp(T_seg(s)) F_in(s) + U^F_seg(s),            F_in(0) = 0
+//   G_in(s-1) = exp(P_{s_seg(s+1)} - P_{s_seg(s)}) G_in(s) + U^B_seg(s), G_in(last) = 0
+template <int MASK>
+__global__ void __launch_bounds__(256) lion_segment_scan_kernel(TcParams prm, float* segin) {
+  const int bh = blockIdx.x, h = bh % prm.H;
+  const float lh = MASK == MASK_D ? prm.log_lambda[h] : 0.f;
+  const int segtok = prm.SEGB * kBlock;
+  for (int e = threadIdx.x; e < kD * kStateCols; e += blockDim.x) {
+    float F = 0.f;
+    for (int s = 0; s < prm.nseg; ++s) {
+      const float* ss = prm.segsum + ((size_t)bh * prm.nseg + s) * kSegSumFloats;
+      segin[((size_t)bh * prm.nseg + s) * kSegInFloats + e] = F;
+      F = __expf(ss[2 * kD * kStateCols]) * F + ss[e];
+    }
+    float G = 0.f;
+    for (int s = prm.nseg - 1; s >= 0; --s) {
+      const float* ss = prm.segsum + ((size_t)bh * prm.nseg + s) * kSegSumFloats;
+      segin[((size_t)bh * prm.nseg + s) * kSegInFloats + kD * kStateCols + e] = G;
+      const float lfirst = ell_at<MASK>(prm, bh, s * segtok, lh);
+      const float lnext = ell_at<MASK>(prm, bh, (s + 1) * segtok, lh);
+      G = __expf(ss[2 * kD * kStateCols] - lfirst + lnext) * G + ss[kD * kStateCols + e];
+    }
+  }
+}
+
 __device__ int g_lion_status;
 
-// ------------------------------------------------------------- host side --
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -585,33 +925,49 @@ int* device_status_ptr() {
 }
 
 bool chunk_tc_supported(const Problem& p) {
-  return p.dtype == DT_BF16 && p.d == kD && p.chunk == kC && p.L <= kMaxChunks * kC;
+  return p.dtype == DT_BF16 && p.d == kD && p.chunk == kC;
 }
 
+namespace {
 
-cudaError_t launch_chunk_tc(const Problem& p, int* status, cudaStream_t s) {
-  CUtensorMap mq, mk, mv;
-  const int BH = p.B * p.H;
-  if (!make_map(&mq, p.q, p.L, BH) || !make_map(&mk, p.k, p.L, BH) || !make_map(&mv, p.v, p.L, BH))
-    return cudaErrorInvalidValue;
-  TcParams prm;
-  prm.out = p.out;
-  prm.log_lambda = p.log_lambda;
-  prm.BH = BH;
-  prm.H = p.H;
-  prm.L = p.L;
-  prm.status = status;
-  static int num_sms = 0;
-  if (!num_sms) {
+int num_sms() {
+  static int n = 0;
+  if (!n) {
     int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (num_sms <= 0) num_sms = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
   }
-  const int grid = BH < num_sms ? BH : num_sms;
+  return n;
+}
+
+struct TcPlan {
+  int NBL, SEGB, nseg;
+  size_t gloc_bytes, segsum_bytes, segin_bytes;
+};
+
+TcPlan plan_tc(int B, int H, int L) {
+  TcPlan t;
+  const int BH = B * H;
+  t.NBL = (L + kBlock - 1) / kBlock;
+  t.nseg = 1;
+  if (t.NBL > 1 && BH < num_sms()) t.nseg = min(t.NBL, max(1, num_sms() / BH));
+  t.SEGB = (t.NBL + t.nseg - 1) / t.nseg;
+  t.nseg = (t.NBL + t.SEGB - 1) / t.SEGB;
+  t.gloc_bytes = t.NBL > 1 ? (size_t)BH * t.NBL * kGlocBytes : 0;
+  t.segsum_bytes = t.NBL > 1 ? (size_t)BH * t.nseg * kSegSumFloats * 4 : 0;
+  t.segin_bytes = t.NBL > 1 ? (size_t)BH * t.nseg * kSegInFloats * 4 : 0;
+  return t;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+template <int MODE>
+cudaError_t launch_mode(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const TcParams& prm, int grid, cudaStream_t s) {
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, TcParams) = nullptr;
 #define LION_TC_CASE(M, F) \
-  if (p.mask_kind == M && p.phi == F) kern = lion_chunk64_tc_kernel<M, F>;
+  if (p.mask_kind == M && p.phi == F) kern = lion_chunk64_tc_kernel<M, F, MODE>;
   LION_TC_CASE(MASK_LIT, PHI_ELU1)
   LION_TC_CASE(MASK_LIT, PHI_SILU_L2)
   LION_TC_CASE(MASK_LIT, PHI_IDENTITY)
@@ -627,6 +983,55 @@ cudaError_t launch_chunk_tc(const Problem& p, int* status, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chunk_tc_workspace_bytes(int B, int H, int L) {
+  const TcPlan t = plan_tc(B, H, L);
+  if (t.NBL == 1) return 0;
+  return align256(t.gloc_bytes) + align256(t.segsum_bytes) + align256(t.segin_bytes);
+}
+
+int chunk_tc_launches(int B, int H, int L) { return plan_tc(B, H, L).NBL > 1 ? 3 : 1; }
+
+cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  const int BH = p.B * p.H;
+  if (!make_map(&mq, p.q, p.L, BH) || !make_map(&mk, p.k, p.L, BH) || !make_map(&mv, p.v, p.L, BH))
+    return cudaErrorInvalidValue;
+  const TcPlan t = plan_tc(p.B, p.H, p.L);
+  TcParams prm;
+  prm.out = p.out;
+  prm.log_lambda = p.log_lambda;
+  prm.BH = BH;
+  prm.H = p.H;
+  prm.L = p.L;
+  prm.NBL = t.NBL;
+  prm.SEGB = t.SEGB;
+  prm.nseg = t.nseg;
+  prm.gloc = nullptr;
+  prm.segsum = nullptr;
+  prm.segin = nullptr;
+  prm.status = status;
+  const int items = BH * t.nseg;
+  const int grid = items < num_sms() ? items : num_sms();
+  if (t.NBL > 1) {
+    if (!ws) return cudaErrorInvalidValue;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    prm.gloc = w;
+    prm.segsum = reinterpret_cast<float*>(w + align256(t.gloc_bytes));
+    float* segin = reinterpret_cast<float*>(w + align256(t.gloc_bytes) + align256(t.segsum_bytes));
+    prm.segin = segin;
+    cudaError_t e = launch_mode<MODE_PRE>(p, mq, mk, mv, prm, grid, s);
+    if (e != cudaSuccess) return e;
+    if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<BH, 256, 0, s>>>(prm, segin);
+    else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<BH, 256, 0, s>>>(prm, segin);
+    else lion_segment_scan_kernel<MASK_S><<<BH, 256, 0, s>>>(prm, segin);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return launch_mode<MODE_MAIN>(p, mq, mk, mv, prm, grid, s);
 }
 
 }  // namespace lion

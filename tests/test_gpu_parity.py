@@ -102,6 +102,18 @@ def test_many_heads_ragged_lengths(oracle_mod, mask):
         check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 64), ref, inp, TOL_BF16)
 
 
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_long_sequences_blocks_and_segments(oracle_mod, mask):
+    """Sequences longer than one 256-token block: the tensor-core path chains
+    blocks (and, with few heads, segments of blocks across CTAs) through its
+    pre-pass, segment scan and main pass."""
+    for B, H, L in ((1, 2, 257), (1, 2, 700), (2, 1, 2000), (8, 5, 2000), (1, 6, 3000)):
+        inp = synth.make_inputs(B, H, L, 64, mask, "bf16", seed=500 + L + B)
+        q, k, v, ll = f64(inp)
+        ref = oracle_mod.rnn(q, k, v, ll, inp["mask"], threads=0)
+        check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 64), ref, inp, TOL_BF16)
+
+
 # ----------------------------------------------------------- edge cases --
 @pytest.mark.parametrize("mask", ("d", "s"))
 def test_vanishing_decay_is_identity(oracle_mod, mask):
