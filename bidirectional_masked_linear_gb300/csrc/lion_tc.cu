@@ -399,8 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t lbo_v = (uint32_t)(sOnes - Vt(c));
 #pragma unroll
+          // LIT: both directions weigh every token by 1, so the stacked A is
+          // phi(K_c) twice (second atom at offset 0)
+          const uint8_t* a_tile = MASK == MASK_LIT ? Kt(c) : Wt(2 * c);
+          const uint32_t lbo_a = MASK == MASK_LIT ? 0u : (uint32_t)kTile;
+#pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tbase + kSlot * c, mnmaj(Wt(2 * c), k, kTile), mnmaj(Vt(c), k, lbo_v), idA, k > 0 ? 1u : 0u);
+            mma_bf16(tbase + kSlot * c, mnmaj(a_tile, k, lbo_a), mnmaj(Vt(c), k, lbo_v), idA, k > 0 ? 1u : 0u);
         }
         if (!good) break;
         mma_commit(&bars[BAR_DA]);
@@ -462,8 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // =================== worker warps: CUDA-core stages =======================
-    const int i_row = 16 * quarter + lane;   // M=64 accumulator row of this lane
-    const bool row_thread = lane < 16;
     auto arrive = [&](int b) {   // every worker warp arrives once
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[b]);
@@ -576,20 +579,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint4 kh = pack8_h(x);
         *chunk16(Kt(c), r, c8) = kh;
-        unpack8_h(kh, x);  // the decay weights multiply the fp16 phi(k) that S sees
-        float wf = 1.f, wb = 1.f;
         if (MASK != MASK_LIT) {
+          unpack8_h(kh, x);  // the decay weights multiply the fp16 phi(k) that S sees
           const float pj = sP[c * kC + r];
-          wf = __expf(sP[c * kC + len - 1] - pj);
-          wb = __expf(pj - sP[c * kC]);
+          const float wf = __expf(sP[c * kC + len - 1] - pj);
+          const float wb = __expf(pj - sP[c * kC]);
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = wf * x[e];
+          *chunk16(Wt(2 * c), r, c8) = pack8_h(y);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = wb * x[e];
+          *chunk16(Wt(2 * c + 1), r, c8) = pack8_h(y);
         }
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = wf * x[e];
-        *chunk16(Wt(2 * c), r, c8) = pack8_h(y);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = wb * x[e];
-        *chunk16(Wt(2 * c + 1), r, c8) = pack8_h(y);
         float v8[8];
         unpack8_bf(*chunk16(Vt(c), r, c8), v8);
         *chunk16(Vt(c), r, c8) = pack8_h(v8);
@@ -741,40 +743,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (MASK != MASK_LIT) worker_sync();   // mask factors visible to every worker
           return true;
         };
+        // Epilogues read the M=64 accumulators with the 16x256b shape: this
+        // warp's 16 rows (lane quarter) x its 16 columns, spread over all 32
+        // lanes -- thread t: rows i0 = t/4, i1 = t/4 + 8 of the quarter,
+        // columns j0, j0 + 1, j0 + 8, j0 + 9 with j0 = 16 wg + 2 (t % 4).
+        const int i0 = 16 * quarter + (lane >> 2), i1 = i0 + 8;
+        const int jq = 2 * (lane & 3);
         auto epi1 = [&](int c, int gg) -> bool {
           const int rg = gg & 1;
           if (!waitb(BAR_M1 + rg, (gg >> 1) & 1)) return false;
           tc_fence_after();
           const int len = min(kC, L - bs - c * kC);
           const uint32_t base = tbase + kRegion * rg;
-          float w[16];
-          tmem_ld16(lane_addr(base, warp, R_SI + 16 * wg), w);
+          float w[8];
+          tmem_ld_16x256b_x2(lane_addr(base, warp, R_SI + 16 * wg), w);
           tmem_wait_ld();
-          if (row_thread) {
-            const int i = i_row;
+          const int j0 = 16 * wg + jq;
+          // register r: row (r & 2 ? i1 : i0), column j0 + (r & 1) + (r & 4 ? 8 : 0)
+          if (MASK == MASK_LIT) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const int i = (r & 2) ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
+              if (i >= len || j >= len) w[r] = 0.f;
+            }
+          } else {
             const float* E = sE + (rg * 2) * kC;
             const float* Einv = E + kC;
-            const bool factor = (MASK == MASK_LIT) || (sP[c * kC] - sP[c * kC + len - 1] < kMaxFactorRange);
-            const float Ei = MASK == MASK_LIT ? 1.f : E[i];
-            const float Einvi = MASK == MASK_LIT ? 1.f : Einv[i];
-            const float pi = sP[c * kC + i];
+            const bool factor = sP[c * kC] - sP[c * kC + len - 1] < kMaxFactorRange;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int j = 16 * wg + e;
+            for (int r = 0; r < 8; ++r) {
+              const int i = (r & 2) ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
               float mval;
-              if (MASK == MASK_LIT) {
-                mval = 1.f;
-              } else if (factor) {
-                mval = j <= i ? Ei * Einv[j] : Einvi * E[j];
+              if (factor) {
+                mval = j <= i ? E[i] * Einv[j] : Einv[i] * E[j];
               } else {
-                const float pj = sP[c * kC + j];
+                const float pi = sP[c * kC + i], pj = sP[c * kC + j];
                 mval = __expf(j <= i ? pi - pj : pj - pi);
               }
-              w[e] = (i < len && j < len) ? w[e] * mval : 0.f;
+              w[r] = (i < len && j < len) ? w[r] * mval : 0.f;
             }
-            *chunk16(At(rg), i, 2 * wg) = pack8_h(w);
-            *chunk16(At(rg), i, 2 * wg + 1) = pack8_h(w + 8);
           }
+          uint8_t* at = At(rg);
+          const int cb = 4 * (lane & 3);   // byte offset of (j0, j0+1) inside the 16-byte chunk
+          *reinterpret_cast<uint32_t*>(at + sw128_offset(i0, 2 * wg) + cb) = pack_h2(w[0], w[1]);
+          *reinterpret_cast<uint32_t*>(at + sw128_offset(i1, 2 * wg) + cb) = pack_h2(w[2], w[3]);
+          *reinterpret_cast<uint32_t*>(at + sw128_offset(i0, 2 * wg + 1) + cb) = pack_h2(w[4], w[5]);
+          *reinterpret_cast<uint32_t*>(at + sw128_offset(i1, 2 * wg + 1) + cb) = pack_h2(w[6], w[7]);
           fence_async_smem();
           tc_fence_before();
           arrive(BAR_RE + rg);
@@ -787,38 +801,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = c * kC, len = min(kC, L - bs - s);
           const bool hasF = hf(c), hasG = hg(c);
           const uint32_t base = tbase + kRegion * rg;
-          float oi[16], of[16], og[16];
-          tmem_ld16(lane_addr(base, warp, R_SI + 16 * wg), oi);
-          const float dI = tmem_ld1(lane_addr(base, warp, R_SI + 64));
-          if (hasF) tmem_ld16(lane_addr(base, warp, R_OF + 16 * wg), of);
-          if (hasG) tmem_ld16(lane_addr(base, warp, R_OG + 16 * wg), og);
-          const float dF = tmem_ld1(lane_addr(base, warp, R_Z + 2 * c));
-          const float dG = tmem_ld1(lane_addr(base, warp, R_Z + 2 * c + 1));
+          float oi[8], of[8], og[8], dd[4], zz[4];
+          tmem_ld_16x256b_x2(lane_addr(base, warp, R_SI + 16 * wg), oi);
+          tmem_ld_16x256b(lane_addr(base, warp, R_SI + 64), dd);   // column 64: intra row sums
+          if (hasF) tmem_ld_16x256b_x2(lane_addr(base, warp, R_OF + 16 * wg), of);
+          if (hasG) tmem_ld_16x256b_x2(lane_addr(base, warp, R_OG + 16 * wg), og);
+          tmem_ld_16x256b(lane_addr(base, warp, R_Z), zz);          // columns 2c, 2c+1: z terms
           tmem_wait_ld();
           tc_fence_before();
           arrive(BAR_FR + rg);   // this region (and chunk c's K/V tiles) may be reused
-          if (row_thread && i_row < len) {
-            const int i = i_row;
-            const float pi = sP[s + i];
-            float a = 0.f, bb = 0.f;
-            if (hasF) a = MASK == MASK_LIT ? 1.f : __expf(pi);
-            if (hasG) bb = MASK == MASK_LIT ? 1.f : __expf(sP[s + len - 1] - pi + sMisc[c + 1]);
-            float den = dI;
-            if (hasF) den += a * dF;
-            if (hasG) den += bb * dG;
-            const float inv = 1.f / den;
-            float y[16];
+          // the row sums of rows i0, i1 sit in the quad's first lane (column 64)
+          // and the z terms in the quad lane c (columns 2c, 2c+1)
+          const int qbase = lane & ~3;
+          const float dI0 = __shfl_sync(0xffffffffu, dd[0], qbase);
+          const float dI1 = __shfl_sync(0xffffffffu, dd[2], qbase);
+          const float dF0 = __shfl_sync(0xffffffffu, zz[0], qbase + c);
+          const float dG0 = __shfl_sync(0xffffffffu, zz[1], qbase + c);
+          const float dF1 = __shfl_sync(0xffffffffu, zz[2], qbase + c);
+          const float dG1 = __shfl_sync(0xffffffffu, zz[3], qbase + c);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float acc = oi[e];
-              if (hasF) acc += a * of[e];
-              if (hasG) acc += bb * og[e];
-              y[e] = acc * inv;
+          for (int half = 0; half < 2; ++half) {
+            const int i = half ? i1 : i0;
+            if (i < len) {
+              const float pi = sP[s + i];
+              float a = 0.f, bb = 0.f;
+              if (hasF) a = MASK == MASK_LIT ? 1.f : __expf(pi);
+              if (hasG) bb = MASK == MASK_LIT ? 1.f : __expf(sP[s + len - 1] - pi + sMisc[c + 1]);
+              float den = half ? dI1 : dI0;
+              if (hasF) den += a * (half ? dF1 : dF0);
+              if (hasG) den += bb * (half ? dG1 : dG0);
+              const float inv = 1.f / den;
+              float y[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int r = 2 * half + (e & 1) + ((e & 2) ? 4 : 0);
+                float acc = oi[r];
+                if (hasF) acc += a * of[r];
+                if (hasG) acc += bb * og[r];
+                y[e] = acc * inv;
+              }
+              float* orow = prm.out + ((size_t)bh * L + bs + s + i) * kD + 16 * wg + jq;
+              *reinterpret_cast<float2*>(orow) = make_float2(y[0], y[1]);
+              *reinterpret_cast<float2*>(orow + 8) = make_float2(y[2], y[3]);
             }
-            float* orow = prm.out + ((size_t)bh * L + bs + s + i) * kD + 16 * wg;
-#pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              *reinterpret_cast<float4*>(orow + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
           }
           return true;
         };
