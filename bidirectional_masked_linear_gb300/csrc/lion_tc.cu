@@ -97,8 +97,8 @@ constexpr int OFF_WORK = OFF_ONES + kTile;             // A: Kf/Kb tiles; B/C: F
 constexpr int OFF_A = OFF_WORK + (2 * kMaxChunks + 1) * kTile;  // masked scores, 2 buffers
 constexpr int OFF_Q = OFF_A + 2 * kTile;               // Q ring
 constexpr int OFF_P = OFF_Q + kQSlots * kTile;         // float[256] chunk-local prefix
-constexpr int OFF_E = OFF_P + kBlock * 4;              // float[2][2][64] mask factors per region
-constexpr int OFF_MISC = OFF_E + 2 * 2 * kC * 4;       // float[8]: l at chunk starts
+constexpr int OFF_E = OFF_P + kBlock * 4;              // float[3][2][64] mask factors, by chunk % 3
+constexpr int OFF_MISC = OFF_E + 3 * 2 * kC * 4;       // float[8]: l at chunk starts
 constexpr int OFF_UNI = OFF_MISC + 8 * 4;              // CTA-uniform worker bookkeeping
 constexpr int OFF_BAR = OFF_UNI + 16 * 4;
 constexpr int OFF_TSLOT = OFF_BAR + 24 * 8;
@@ -398,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!good) break;
           tc_fence_after();
           const uint32_t lbo_v = (uint32_t)(sOnes - Vt(c));
-#pragma unroll
           // LIT: both directions weigh every token by 1, so the stacked A is
           // phi(K_c) twice (second atom at offset 0)
           const uint8_t* a_tile = MASK == MASK_LIT ? Kt(c) : Wt(2 * c);
@@ -440,11 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_q_next();
           for (int c = 1; c < NC && good; ++c) {
             const int gc = g + c;
-            good = waitb(BAR_RE + (gc & 1), (gc >> 1) & 1);
-            if (!good) break;
-            tc_fence_after();
-            mma2(c, gc);
-            issue_q_next();
+            // chunk c-1 retired: its TMEM region takes chunk c+1's first MMA group
             good = waitb(BAR_FR + ((gc - 1) & 1), ((gc - 1) >> 1) & 1);
             if (!good) break;
             if (c - 1 < NCn) issue_kv(nxt, c - 1);
@@ -454,6 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               mma1(c + 1, gc + 1, hf(c + 1), hg(c + 1));
             }
+            good = waitb(BAR_RE + (gc & 1), (gc >> 1) & 1);
+            if (!good) break;
+            tc_fence_after();
+            mma2(c, gc);
+            issue_q_next();
           }
           if (!good) break;
           good = waitb(BAR_FR + ((g + NC - 1) & 1), ((g + NC - 1) >> 1) & 1);
@@ -472,6 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[b]);
     };
     auto worker_sync = [&]() { asm volatile("bar.sync 1, %0;" ::"n"(kWorkerWarps * 32) : "memory"); };
+    // row-parallel stages: thread -> (row tid / 8, 16-byte column chunk tid % 8)
+    const uint32_t off_rc = sw128_offset(tid >> 3, tid & 7);
     // CTA-uniform bookkeeping lives in shared memory (register budget):
     // [0..3] K/V loads consumed per slot, [4] rsum, [5] tseg, [6] lseg_after, [7] tcum
     int* uni_i = reinterpret_cast<int*>(smem + OFF_UNI);
@@ -569,32 +571,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         good = waitb(BAR_KV + c, uni_i[c] & 1);
         if (!good) break;
         const int len = min(kC, L - bs - c * kC);
-        const int r = tid >> 3, c8 = tid & 7;
-        float x[8];
-        unpack8_bf(*chunk16(Kt(c), r, c8), x);
-        phi8<PHI>(x);      // every lane: phi8 shuffles within the row's 8 lanes
-        if (r >= len) {    // padding tokens contribute nothing
+        const int r = tid >> 3;
+        uint8_t* kp = Kt(c) + off_rc;
+        uint8_t* vp = Vt(c) + off_rc;
+        uint8_t* fp = Wt(2 * c) + off_rc;
+        uint8_t* bp = Wt(2 * c + 1) + off_rc;
+        if (4 * warp < len) {   // rows of this warp that hold tokens (the rest arrive as zeros)
+          float x[8];
+          unpack8_bf(*reinterpret_cast<const uint4*>(kp), x);
+          phi8<PHI>(x);      // every lane: phi8 shuffles within the row's 8 lanes
+          if (r >= len) {    // padding tokens contribute nothing
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          }
+          const uint4 kh = pack8_h(x);
+          *reinterpret_cast<uint4*>(kp) = kh;
+          if (MASK != MASK_LIT) {
+            unpack8_h(kh, x);  // the decay weights multiply the fp16 phi(k) that S sees
+            const float pj = sP[c * kC + r];
+            const float wf = r < len ? __expf(sP[c * kC + len - 1] - pj) : 0.f;
+            const float wb = r < len ? __expf(pj - sP[c * kC]) : 0.f;
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = wf * x[e];
+            *reinterpret_cast<uint4*>(fp) = pack8_h(y);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = wb * x[e];
+            *reinterpret_cast<uint4*>(bp) = pack8_h(y);
+          }
+          float v8[8];
+          unpack8_bf(*reinterpret_cast<const uint4*>(vp), v8);
+          *reinterpret_cast<uint4*>(vp) = pack8_h(v8);
+        } else if (MASK != MASK_LIT) {
+          // K and V rows past the sequence arrived as zeros (bf16 0 == fp16 0);
+          // the weighted copies still hold an older block's data
+          *reinterpret_cast<uint4*>(fp) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(bp) = make_uint4(0u, 0u, 0u, 0u);
         }
-        const uint4 kh = pack8_h(x);
-        *chunk16(Kt(c), r, c8) = kh;
-        if (MASK != MASK_LIT) {
-          unpack8_h(kh, x);  // the decay weights multiply the fp16 phi(k) that S sees
-          const float pj = sP[c * kC + r];
-          const float wf = __expf(sP[c * kC + len - 1] - pj);
-          const float wb = __expf(pj - sP[c * kC]);
-          float y[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = wf * x[e];
-          *chunk16(Wt(2 * c), r, c8) = pack8_h(y);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = wb * x[e];
-          *chunk16(Wt(2 * c + 1), r, c8) = pack8_h(y);
-        }
-        float v8[8];
-        unpack8_bf(*chunk16(Vt(c), r, c8), v8);
-        *chunk16(Vt(c), r, c8) = pack8_h(v8);
         fence_async_smem();
         arrive(BAR_RA + c);
       }
@@ -720,26 +733,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto hf = [&](int c) { return c > 0 || hasFin; };
         auto hg = [&](int c) { return c < NC - 1 || hasGin; };
         auto prep = [&](int c, int gg) -> bool {
-          const int sl = gg % kQSlots, rg = gg & 1;
+          const int sl = gg % kQSlots;
           if (!waitb(BAR_Q + sl, (gg / kQSlots) & 1)) return false;
           const int len = min(kC, L - bs - c * kC);
-          const int r = tid >> 3, c8 = tid & 7;
-          float x[8];
-          unpack8_bf(*chunk16(Qt(sl), r, c8), x);
-          phi8<PHI>(x);
-          if (r >= len) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          if (4 * warp < len) {   // padding rows arrive as zeros and stay unused
+            uint8_t* qp = Qt(sl) + off_rc;
+            float x[8];
+            unpack8_bf(*reinterpret_cast<const uint4*>(qp), x);
+            phi8<PHI>(x);
+            *reinterpret_cast<uint4*>(qp) = pack8_h(x);
           }
-          *chunk16(Qt(sl), r, c8) = pack8_h(x);
           if (MASK != MASK_LIT && tid < 2 * kC) {
             // E[t] = exp(p_t - p_0), Einv[t] = exp(p_0 - p_t)
             const int t = tid & 63;
             const float d = sP[c * kC + t] - sP[c * kC];
-            sE[(rg * 2 + (tid >> 6)) * kC + t] = tid < 64 ? __expf(d) : __expf(-d);
+            sE[((gg % 3) * 2 + (tid >> 6)) * kC + t] = tid < 64 ? __expf(d) : __expf(-d);
           }
           fence_async_smem();
-          arrive(BAR_RP + rg);
+          arrive(BAR_RP + (gg & 1));
           if (MASK != MASK_LIT) worker_sync();   // mask factors visible to every worker
           return true;
         };
@@ -749,6 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // columns j0, j0 + 1, j0 + 8, j0 + 9 with j0 = 16 wg + 2 (t % 4).
         const int i0 = 16 * quarter + (lane >> 2), i1 = i0 + 8;
         const int jq = 2 * (lane & 3);
+        const uint32_t a_off0 = sw128_offset(i0, 2 * wg) + 4 * (lane & 3);
+        const uint32_t a_off1 = sw128_offset(i1, 2 * wg) + 4 * (lane & 3);
+        const uint32_t a_off2 = sw128_offset(i0, 2 * wg + 1) + 4 * (lane & 3);
+        const uint32_t a_off3 = sw128_offset(i1, 2 * wg + 1) + 4 * (lane & 3);
         auto epi1 = [&](int c, int gg) -> bool {
           const int rg = gg & 1;
           if (!waitb(BAR_M1 + rg, (gg >> 1) & 1)) return false;
@@ -760,35 +775,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           const int j0 = 16 * wg + jq;
           // register r: row (r & 2 ? i1 : i0), column j0 + (r & 1) + (r & 4 ? 8 : 0)
-          if (MASK == MASK_LIT) {
+          if (i0 < len) {
+            if (MASK == MASK_LIT) {
+              if (len < kC) {
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const int i = (r & 2) ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
-              if (i >= len || j >= len) w[r] = 0.f;
-            }
-          } else {
-            const float* E = sE + (rg * 2) * kC;
-            const float* Einv = E + kC;
-            const bool factor = sP[c * kC] - sP[c * kC + len - 1] < kMaxFactorRange;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const int i = (r & 2) ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
-              float mval;
-              if (factor) {
-                mval = j <= i ? E[i] * Einv[j] : Einv[i] * E[j];
-              } else {
-                const float pi = sP[c * kC + i], pj = sP[c * kC + j];
-                mval = __expf(j <= i ? pi - pj : pj - pi);
+                for (int r = 0; r < 8; ++r) {
+                  const int i = (r & 2) ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
+                  if (i >= len || j >= len) w[r] = 0.f;
+                }
               }
-              w[r] = (i < len && j < len) ? w[r] * mval : 0.f;
+            } else {
+              const float* E = sE + ((gg % 3) * 2) * kC;
+              const float* Einv = E + kC;
+              const bool factor = sP[c * kC] - sP[c * kC + len - 1] < kMaxFactorRange;
+              if (factor) {
+                const float2 ej0 = *reinterpret_cast<const float2*>(E + j0);
+                const float2 ej8 = *reinterpret_cast<const float2*>(E + j0 + 8);
+                const float2 nj0 = *reinterpret_cast<const float2*>(Einv + j0);
+                const float2 nj8 = *reinterpret_cast<const float2*>(Einv + j0 + 8);
+                const float Ej[4] = {ej0.x, ej0.y, ej8.x, ej8.y};
+                const float Nj[4] = {nj0.x, nj0.y, nj8.x, nj8.y};
+                const float Ei[2] = {E[i0], E[i1]}, Ni[2] = {Einv[i0], Einv[i1]};
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  const int ri = (r >> 1) & 1, cj = (r & 1) + ((r >> 1) & 2);
+                  const int i = ri ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
+                  w[r] *= j <= i ? Ei[ri] * Nj[cj] : Ni[ri] * Ej[cj];
+                }
+              } else {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  const int i = (r & 2) ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
+                  const float pi = sP[c * kC + i], pj = sP[c * kC + j];
+                  w[r] *= __expf(j <= i ? pi - pj : pj - pi);
+                }
+              }
+              if (len < kC) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                  const int i = (r & 2) ? i1 : i0, j = j0 + (r & 1) + ((r & 4) ? 8 : 0);
+                  if (i >= len || j >= len) w[r] = 0.f;
+                }
+              }
             }
+            uint8_t* at = At(rg);
+            *reinterpret_cast<uint32_t*>(at + a_off0) = pack_h2(w[0], w[1]);
+            *reinterpret_cast<uint32_t*>(at + a_off1) = pack_h2(w[2], w[3]);
+            *reinterpret_cast<uint32_t*>(at + a_off2) = pack_h2(w[4], w[5]);
+            *reinterpret_cast<uint32_t*>(at + a_off3) = pack_h2(w[6], w[7]);
           }
-          uint8_t* at = At(rg);
-          const int cb = 4 * (lane & 3);   // byte offset of (j0, j0+1) inside the 16-byte chunk
-          *reinterpret_cast<uint32_t*>(at + sw128_offset(i0, 2 * wg) + cb) = pack_h2(w[0], w[1]);
-          *reinterpret_cast<uint32_t*>(at + sw128_offset(i1, 2 * wg) + cb) = pack_h2(w[2], w[3]);
-          *reinterpret_cast<uint32_t*>(at + sw128_offset(i0, 2 * wg + 1) + cb) = pack_h2(w[4], w[5]);
-          *reinterpret_cast<uint32_t*>(at + sw128_offset(i1, 2 * wg + 1) + cb) = pack_h2(w[6], w[7]);
           fence_async_smem();
           tc_fence_before();
           arrive(BAR_RE + rg);
@@ -813,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the row sums of rows i0, i1 sit in the quad's first lane (column 64)
           // and the z terms in the quad lane c (columns 2c, 2c+1)
           const int qbase = lane & ~3;
+          float* out_c = prm.out + ((size_t)bh * L + bs + s) * kD + 16 * wg + jq;
           const float dI0 = __shfl_sync(0xffffffffu, dd[0], qbase);
           const float dI1 = __shfl_sync(0xffffffffu, dd[2], qbase);
           const float dF0 = __shfl_sync(0xffffffffu, zz[0], qbase + c);
@@ -840,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (hasG) acc += bb * og[r];
                 y[e] = acc * inv;
               }
-              float* orow = prm.out + ((size_t)bh * L + bs + s + i) * kD + 16 * wg + jq;
+              float* orow = out_c + (size_t)i * kD;
               *reinterpret_cast<float2*>(orow) = make_float2(y[0], y[1]);
               *reinterpret_cast<float2*>(orow + 8) = make_float2(y[2], y[3]);
             }
@@ -848,13 +884,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
 
+        // phi(Q) prep runs two chunks ahead so each MMA group overlaps a full
+        // epilogue: prep c+2 | epi2 c-1, epi1 c | ...
         good = prep(0, g);
         if (good && NC > 1) good = prep(1, g + 1);
         if (good) good = epi1(0, g);
+        if (good && NC > 2) good = prep(2, g + 2);
         for (int c = 1; c < NC && good; ++c) {
-          good = epi1(c, g + c);
-          if (good) good = epi2(c - 1, g + c - 1);
-          if (good && c + 1 < NC) good = prep(c + 1, g + c + 1);
+          good = epi2(c - 1, g + c - 1);
+          if (good) good = epi1(c, g + c);
+          if (good && c + 2 < NC) good = prep(c + 2, g + c + 2);
         }
         if (good) good = epi2(NC - 1, g + NC - 1);
         g += NC;
