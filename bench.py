@@ -32,6 +32,32 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20      # > 129 MB L2
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# kernel, per unit (head) from one ncu capture, keyed by the SHA-256 of the
+# kernel's sources at the time of the capture.  A key that no longer matches
+# the sources reports null: the counters describe another kernel.
+_TC_SOURCES = ("bidirectional_masked_linear_gb300/csrc/lion_tc.cu",
+               "bidirectional_masked_linear_gb300/csrc/tc_ptx.cuh")
+TRAFFIC_PER_HEAD = {
+    # chunk-64 kernel, ViT-B shape at B=128, LION-S: 160.7 MB / 1536 heads
+    ("fc4be66a869d6463b1ad06b8b0948a689343c3e6648cdb380430aac91fcace8c", "vit_b", "s", 64):
+        (117664768 + 43027200) / 1536,
+}
+
+
+def _sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in _TC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_bytes(w, mask, chunk):
+    per_head = TRAFFIC_PER_HEAD.get((_sources_sha(), w.name, mask, chunk))
+    return None if per_head is None else per_head * w.B * w.H
+
 
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -232,26 +258,25 @@ def measure_e2e(w, inp, mask, chunk, form, steps, warmup):
 
 def cpu_baseline(name, mask, chunk, budget_s=10.0):
     """The float64 oracle (chunk form, all host cores) on a bounded sample of
-    heads of the same workload; tokens/s counts B*L tokens per H heads."""
+    the same workload: batch rows (all H heads each) in order, wrapping round
+    to the first row, until `budget_s` of CPU time is spent.  tokens/s counts
+    L tokens per batch row."""
     import oracle
     w = synth.WORKLOADS[name]
     inp = synth.workload_inputs(name, mask)
     q, k, v, ll = (synth.as_f64(inp[x]) for x in ("q", "k", "v", "log_lambda"))
     cores = oracle.threads(0)
-    # one batch row at a time (all H heads) until the budget is spent
-    done_heads, t0 = 0, time.perf_counter()
-    b = 0
-    while b < w.B and (time.perf_counter() - t0) < budget_s:
+    rows, t0 = 0, time.perf_counter()
+    while (time.perf_counter() - t0) < budget_s:
+        b = rows % w.B
         sl = slice(b, b + 1)
         lls = None if ll is None else (ll if mask == "d" else ll[sl])
         oracle.chunk(q[sl], k[sl], v[sl], lls, inp["mask"], chunk, threads=0)
-        done_heads += w.H
-        b += 1
+        rows += 1
     dt = time.perf_counter() - t0
-    tokens = done_heads * w.L / w.H
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{b} of {w.B} batch rows ({done_heads} heads x L={w.L}), float64 chunk form "
-                      f"(chunk {chunk}), OpenMP over heads, {dt:.1f} s"}
+    return {"value": rows * w.L / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} batch rows of {w.B} (wrapping; {rows * w.H} heads x L={w.L}), "
+                      f"float64 chunk form (chunk {chunk}), OpenMP over heads, {dt:.1f} s"}
 
 
 def run_reference(args, dist, ws, rank):
@@ -364,7 +389,7 @@ def main():
             "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": _config(args, w),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None,
+                         "frac": achieved / hbm_peak, "traffic": traffic_bytes(w, args.mask, args.chunk),
                          "peak_source": peak_src, "algorithmic_bytes": abytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
