@@ -183,7 +183,9 @@ def rows(q, k, v, log_lambda, mask_kind, b, h, row_idx, phi_kind=PHI_DEFAULT):
 
 def row_kappa(q, k, log_lambda, mask_kind, b, h, i0, i1, phi_kind=PHI_DEFAULT):
     """Conditioning of rows [i0, i1) of head (b, h):
-    kappa_i = sum_j M_ij |s_ij| / |sum_j M_ij s_ij| (1 for positive features)."""
+    kappa_i = sum_j M_ij (|phi(q_i)| . |phi(k_j)|) / |sum_j M_ij s_ij|: the
+    componentwise condition number of the row sum under relative perturbations
+    of the features (1 for non-negative features)."""
     q, k = _f64(q), _f64(k)
     ll = _f64(log_lambda)
     B, H, L, d = q.shape

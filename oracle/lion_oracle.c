@@ -528,9 +528,15 @@ int oracle_lion_rows(const double* q, const double* k, const double* v,
 
 /* ---------------------------------------------------- conditioning ---- */
 
-/* kappa_i = sum_j M_ij |s_ij| / |sum_j M_ij s_ij| for rows of head (b, h)
- * range [i0, i1).  kappa = 1 when every s_ij >= 0 (elu+1 features); larger
- * values flag rows whose row sum cancels (possible with SiLU features). */
+/* Componentwise condition number of the row sum den_i = sum_j M_ij s_ij
+ * with respect to relative perturbations of the features:
+ *   kappa_i = sum_j M_ij (|phi(q_i)| . |phi(k_j)|) / |sum_j M_ij s_ij|
+ * (|x| . |y| = sum_m |x_m| |y_m|, the quantity that bounds the rounding
+ * error of the dot product s_ij = phi(q_i) . phi(k_j); Higham, "Accuracy
+ * and Stability of Numerical Algorithms", section 3.1), for the rows of head
+ * (b, h) in [i0, i1).  kappa = 1 when every feature is non-negative (elu+1);
+ * larger values flag rows whose scores or row sum cancel (possible with SiLU
+ * features), where any rounding of the features is amplified. */
 int oracle_row_kappa(const double* q, const double* k, const double* log_lambda,
                      int B, int H, int L, int d, int mask_kind, int phi_kind,
                      int b, int h, int i0, int i1, double* kappa) {
@@ -552,10 +558,13 @@ int oracle_row_kappa(const double* q, const double* k, const double* log_lambda,
     phi_row(phi, q + off + (long)i * d, d, fq);
     double sa = 0.0, ss = 0.0;
     for (int j = 0; j < L; ++j) {
-      double s = 0.0;
-      for (int m = 0; m < d; ++m) s += fq[m] * fk[(long)j * d + m];
+      double s = 0.0, a = 0.0;
+      for (int m = 0; m < d; ++m) {
+        s += fq[m] * fk[(long)j * d + m];
+        a += fabs(fq[m]) * fabs(fk[(long)j * d + m]);
+      }
       double Mij = (i >= j) ? exp(P[i] - P[j]) : exp(P[j] - P[i]);
-      sa += Mij * fabs(s);
+      sa += Mij * a;
       ss += Mij * s;
     }
     kappa[i - i0] = sa / fabs(ss);

@@ -5,11 +5,17 @@ Error measure (per output row i of each head):
     err_i = ||y_i - yref_i||_inf / ||yref_i||_inf
 
 must satisfy err_i <= tol * max(1, kappa_i), where
-kappa_i = sum_j M_ij |s_ij| / |sum_j M_ij s_ij| is the conditioning of the row
-sum.  kappa_i = 1 whenever the features are positive (elu+1); with SiLU
-features the row sum can cancel and the bound widens accordingly.  kappa is
-only computed (by the oracle, O(L d) per row) for rows that miss the plain
-bound, which keeps full-size checks fast.
+
+    kappa_i = sum_j M_ij (|phi(q_i)| . |phi(k_j)|) / |sum_j M_ij s_ij|
+
+is the componentwise condition number of the row sum under relative
+perturbations of the features: a tensor-core path rounds phi(q) and phi(k)
+to 16-bit operands, and the error of each score s_ij is bounded by that
+rounding times |phi(q_i)| . |phi(k_j)| (the standard dot-product bound), not
+by |s_ij|.  kappa_i = 1 whenever the features are non-negative (elu+1); with
+SiLU features scores and row sums can cancel and the bound widens
+accordingly.  kappa is only computed (by the oracle, O(L d) per row) for rows
+that miss the plain bound, which keeps full-size checks fast.
 
 Tolerances: 2e-3 for bfloat16 inputs with float32 accumulation, 1e-5 for
 float32 inputs.

@@ -311,6 +311,20 @@ def test_kappa_is_one_for_positive_features(oracle_mod):
     assert np.all(kap2 >= 1.0 - 1e-12)
 
 
+def test_kappa_hand_cases(oracle_mod):
+    """Identity features, LIT mask (M = 1), values worked by hand.
+    One token, q = (2, -1), k = (1, 1): s = 1, |q|.|k| = 3, kappa = 3.
+    Two tokens, q_0 = (1, 1), k_0 = (1, 1), k_1 = (-0.5, 3): s_00 = 2,
+    s_01 = 2.5, |q_0|.|k_1| = 3.5, kappa_0 = (2 + 3.5) / (2 + 2.5) = 11/9."""
+    o = oracle_mod
+    q = np.array([2.0, -1.0]).reshape(1, 1, 1, 2)
+    k = np.array([1.0, 1.0]).reshape(1, 1, 1, 2)
+    assert o.row_kappa(q, k, None, 0, 0, 0, 0, 1, phi_kind=3)[0] == pytest.approx(3.0, rel=1e-15)
+    q = np.array([[1.0, 1.0], [0.3, 0.7]]).reshape(1, 1, 2, 2)
+    k = np.array([[1.0, 1.0], [-0.5, 3.0]]).reshape(1, 1, 2, 2)
+    assert o.row_kappa(q, k, None, 0, 0, 0, 0, 1, phi_kind=3)[0] == pytest.approx(11.0 / 9.0, rel=1e-15)
+
+
 def test_invalid_arguments(oracle_mod):
     o = oracle_mod
     q = np.zeros((1, 1, 4, 2))
