@@ -114,15 +114,18 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
   p.chunk = a->chunk;
   cudaStream_t s = a->stream;
 
-  const bool use_tc = a->form == LION_FORM_CHUNK && lion::chunk_tc_supported(p);
-  if (a->form == LION_FORM_CHUNK && !use_tc && a->chunk > lion::kSimtMaxChunk) return LION_ERR_UNSUPPORTED;
+  const bool use_tc128 = a->form == LION_FORM_CHUNK && lion::chunk128_tc_supported(p);
+  const bool use_tc = !use_tc128 && a->form == LION_FORM_CHUNK && lion::chunk_tc_supported(p);
+  if (a->form == LION_FORM_CHUNK && !use_tc && !use_tc128 && a->chunk > lion::kSimtMaxChunk)
+    return LION_ERR_UNSUPPORTED;
   int* dstatus = nullptr;
-  if (use_tc) {
+  if (use_tc || use_tc128) {
     dstatus = lion::device_status_ptr();
     if (!dstatus) return LION_ERR_CUDA;
   }
-  const size_t need = use_tc ? lion::chunk_tc_workspace_bytes(a->B, a->H, a->L)
-                             : simt_workspace_bytes(a->B, a->H, a->L, a->form);
+  const size_t need = use_tc128 ? 0
+                      : use_tc   ? lion::chunk_tc_workspace_bytes(a->B, a->H, a->L)
+                                 : simt_workspace_bytes(a->B, a->H, a->L, a->form);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
@@ -139,7 +142,9 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
     case LION_FORM_CHUNK:
-      e = use_tc ? lion::launch_chunk_tc(p, ws, dstatus, s) : lion::launch_chunk_simt(p, (float*)ws, s);
+      e = use_tc128 ? lion::launch_chunk128_tc(p, dstatus, s)
+          : use_tc  ? lion::launch_chunk_tc(p, ws, dstatus, s)
+                    : lion::launch_chunk_simt(p, (float*)ws, s);
       break;
   }
   if (owned) {

@@ -35,6 +35,11 @@ size_t chunk_tc_workspace_bytes(int B, int H, int L);
 int chunk_tc_launches(int B, int H, int L);
 cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_t s);
 
+// Tensor-core chunkwise kernel with 128-token chunks: bf16, d = 64,
+// chunk = 128, L <= 256 (one launch, no workspace).
+bool chunk128_tc_supported(const Problem& p);
+cudaError_t launch_chunk128_tc(const Problem& p, int* status, cudaStream_t s);
+
 // Device-side status word that kernels set when a bounded wait gives up
 // (address on the current device; nullptr if it cannot be resolved).
 int* device_status_ptr();

@@ -103,6 +103,42 @@ def test_many_heads_ragged_lengths(oracle_mod, mask):
 
 
 @pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_chunk128_many_heads_ragged_lengths(oracle_mod, mask):
+    """The 128-token-chunk tensor-core kernel: one and two chunks, ragged
+    tails, padding rows inside a warp, more heads than SMs (every persistent
+    CTA cycles its double-buffered head slots several times)."""
+    for L in (1, 2, 31, 100, 127, 128, 129, 160, 197, 224, 225, 255, 256):
+        inp = synth.make_inputs(40, 9, L, 64, mask, "bf16", seed=700 + L)
+        q, k, v, ll = f64(inp)
+        ref = oracle_mod.full(q, k, v, ll, inp["mask"], threads=0)
+        check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 128), ref, inp, TOL_BF16)
+
+
+@pytest.mark.parametrize("phi", (lion.PHI_ELU1, lion.PHI_SILU_L2, lion.PHI_IDENTITY))
+def test_chunk128_feature_maps(oracle_mod, phi):
+    """Every feature map through the 128-token-chunk kernel (bf16)."""
+    inp = synth.make_inputs(3, 4, 197, 64, "s", "bf16", seed=21)
+    if phi == lion.PHI_IDENTITY:   # keep the row sums away from zero
+        for key in ("q", "k"):
+            inp[key] = (inp[key].float().abs() + 0.1).to(torch.bfloat16)
+    q, k, v, ll = f64(inp)
+    ref = oracle_mod.full(q, k, v, ll, 2, phi)
+    check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 128, phi), ref, inp, TOL_BF16, phi)
+
+
+@pytest.mark.parametrize("scale", (1.5, 3.0))
+def test_chunk128_steep_decay_exact_mask(oracle_mod, scale):
+    """Decay ranges above 160 nats inside a 128-token chunk (log lambda around
+    -scale per token): the kernel takes exp(-|p_i - p_j|) per element instead
+    of the factorised mask; M underflows to 0 well inside the chunk."""
+    inp = synth.make_inputs(2, 3, 230, 64, "s", "bf16", seed=int(31 * scale))
+    inp["log_lambda"] = inp["log_lambda"] * (scale / 0.06)
+    q, k, v, ll = f64(inp)
+    ref = oracle_mod.full(q, k, v, ll, 2)
+    check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 128), ref, inp, TOL_BF16)
+
+
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
 def test_long_sequences_blocks_and_segments(oracle_mod, mask):
     """Sequences longer than one 256-token block: the tensor-core path chains
     blocks (and, with few heads, segments of blocks across CTAs) through its
