@@ -18,19 +18,22 @@
 // With two chunks the forward and backward scans are single steps (F_1 is the
 // state of chunk 0, G_0 the state of chunk 1).
 //
-// Design.  One persistent CTA per SM walks heads; the head's Q and V tiles
-// are double-buffered so the next head streams in while this one computes,
-// and the warps are specialised:
-//   warp 0      TMA loads (Q, V per head slot; K single-buffered, refilled as
-//               soon as the score MMAs (LIT: and the state MMAs) have read it);
+// Design.  One persistent CTA per SM walks heads.  Each head's Q and V tiles
+// are double-buffered, so the next head streams in while this one computes.
+// The warps are specialised:
+//   warp 0      TMA loads, polling three streams (V, K, Q) so that none waits
+//               behind another; K is single-buffered and refilled as soon as
+//               the score MMAs (LIT: and the state MMAs) have read it;
 //   warp 1      tcgen05 MMA issue (one thread);
-//   warps 2-9   "prep", one thread per token: decay prefix, phi(k) in place
-//               (fp16), the decay-weighted phi(k) copy for the state MMA,
-//               V -> fp16 in place, phi(q) in place, mask factors;
-//   warps 10-17 "epi", one thread per TMEM lane (= row of a chunk): the decay
+//   warps 2-17  "prep", two threads per token (32 features each): decay
+//               prefix, V -> fp16 in place, phi(k) in place, the
+//               decay-weighted phi(k) copy for the state MMA, phi(q) in
+//               place, mask factors;
+//   warps 18-25 "epi", one thread per TMEM lane (= row of a chunk): the decay
 //               mask on S (P = S * M, fp16, written back into TMEM as the A
 //               operand of P [V | 1]), the state tiles, the decay-scaled
-//               phi(q) for the state product, and the normalised output.
+//               phi(q) for the state product, and the normalised output,
+//               staged per warp in the head's spent Q tile and written by TMA.
 // prep of head h+1 overlaps epi of head h.  MMAs per head:
 //   S_c  = phi(Q_c) phi(K_c)^T                      M=128 N=128 K=64
 //   U_c  = (w_c o phi(K_c))^T [V_c | 1]             M=64  N=80  K=128
@@ -74,15 +77,16 @@ constexpr int kD = 64;                  // head dim
 constexpr int kRows = 2 * kC;           // tokens per head at most
 constexpr int kTile = kC * 128;         // 128 rows x 64 16-bit values, 128-byte swizzle
 constexpr int kStTile = kD * 128;       // 64 x 64 16-bit state tile
-constexpr int kPrepWarps = 8, kEpiWarps = 8;
+constexpr int kPrepWarps = 16, kEpiWarps = 8;
 constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
-constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 576
+constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
 constexpr long long kWaitCycles = 2000000000LL;       // ~1 s at 2 GHz
 constexpr uint32_t kSleepNs = 2000u;
 constexpr float kMaxFactorRange = 80.f;               // exp(80) stays finite in fp32
+constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr int OFF_Q = 0;                          // [slot][chunk] phi(Q) tiles
+constexpr int OFF_Q = 0;                          // [slot][chunk] phi(Q) tiles; output staging
 constexpr int OFF_V = OFF_Q + 4 * kTile;          // [slot][chunk] V tiles
 constexpr int OFF_K = OFF_V + 4 * kTile;          // [chunk] phi(K) tiles
 constexpr int OFF_KW = OFF_K + 2 * kTile;         // [chunk] decay-weighted phi(K)
@@ -91,36 +95,39 @@ constexpr int OFF_ONES = OFF_ST + 2 * kStTile;    // 16 rows, column 0 = 1
 constexpr int OFF_FAC = OFF_ONES + 2048;          // [slot] float alpha[256], rho[256], sig[256], p[256]
 constexpr int OFF_INFO = OFF_FAC + 2 * 4 * kRows * 4;  // [slot] float[8] per-head scalars
 constexpr int OFF_Z = OFF_INFO + 2 * 8 * 4;       // [chunk] float[64] z of the state applied
-constexpr int OFF_RED = OFF_Z + 2 * kD * 4;       // [parity] float[16] prep scan scratch
-constexpr int OFF_BAR = OFF_RED + 2 * 16 * 4;
-constexpr int kNumBars = 16;
+constexpr int OFF_RED = OFF_Z + 2 * kD * 4;       // [parity] float[32] prep scan scratch
+constexpr int OFF_BAR = OFF_RED + 2 * 32 * 4;
+constexpr int kNumBars = 20;
 constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(OFF_ONES % 1024 == 0 && OFF_ST % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
-// per-head scalars (INFO): 0 T_0 (chunk-0 total), 1 l_128, 2/3 p_ref of
-// chunk 0/1, 4/5 exact-mask flag of chunk 0/1
-enum { I_T0 = 0, I_L128 = 1, I_REF0 = 2, I_REF1 = 3, I_EX0 = 4, I_EX1 = 5 };
+// per-head scalars (INFO): exact-mask flag of chunk 0/1
+enum { I_EX0 = 0, I_EX1 = 1 };
 
 // mbarriers
 enum {
-  B_QV0 = 0,      // + slot: Q, V tiles landed (TMA, tx bytes)
-  B_K = 2,        // K tiles landed
-  B_KVR = 3,      // prep: phi(K), weighted phi(K), V written (8 arrivals)
-  B_QR = 4,       // prep: phi(Q) and factors written (8 arrivals)
-  B_S = 5,        // MMA commit: S done
-  B_KE = 6,       // MMA commit: K tiles free
-  B_U = 7,        // MMA commit: states done
-  B_KWE = 8,      // MMA commit: weighted phi(K) free
-  B_PR = 9,       // epi: P, state tiles, scaled phi(Q) written (8 arrivals)
-  B_O = 10,       // MMA commit: O done
-  B_QVE0 = 11,    // + slot: MMA commit: Q, V tiles free
-  B_ED = 13,      // epi: O read (8 arrivals)
-  B_DRAIN = 14,   // MMA commit used when unwinding
+  B_V0 = 0,       // + slot: V tiles landed (TMA, tx bytes)
+  B_Q0 = 2,       // + slot: Q tiles landed
+  B_K = 4,        // K tiles landed
+  B_KVR = 5,      // prep: V, phi(K), weighted phi(K) written (16 arrivals)
+  B_QR = 6,       // prep: phi(Q) and factors written (16 arrivals)
+  B_S = 7,        // MMA commit: S done
+  B_KE = 8,       // MMA commit: K tiles free
+  B_U = 9,        // MMA commit: states done
+  B_KWE = 10,     // MMA commit: weighted phi(K) free
+  B_PR = 11,      // epi: P, state tiles, scaled phi(Q) written (8 arrivals)
+  B_O = 12,       // MMA commit: O done
+  B_VE0 = 13,     // + slot: MMA commit: V tiles free
+  B_QE0 = 15,     // + slot: Q tiles free: every epi warp's output store has read its staging (8)
+  B_ED = 17,      // epi: O read (8 arrivals)
+  B_DRAIN = 18,   // MMA commit used when unwinding
 };
 __host__ __device__ constexpr uint32_t bar_count(int b) {
-  return (b == B_KVR || b == B_QR) ? (uint32_t)kPrepWarps : (b == B_PR || b == B_ED) ? (uint32_t)kEpiWarps : 1u;
+  return (b == B_KVR || b == B_QR)                                  ? (uint32_t)kPrepWarps
+         : (b == B_PR || b == B_ED || b == B_QE0 || b == B_QE0 + 1) ? (uint32_t)kEpiWarps
+                                                                    : 1u;
 }
 
 // TMEM columns
@@ -129,7 +136,6 @@ constexpr uint32_t T_O = 0;       // + 80 c: U_c then O_c
 constexpr uint32_t T_S = 160;     // + 128 c: S_c, P_c in its first 64 columns
 
 struct C128Params {
-  float* out;
   const float* log_lambda;
   int BH, H, L;
   int* status;
@@ -164,23 +170,79 @@ __device__ __forceinline__ uint4 bf8_to_h8(uint4 v) {
   return pack8_h(x);
 }
 
-// phi over the 64 features of one row held by this thread.
+// packed two-lane fp32 arithmetic (one instruction for both lanes)
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// phi over the 32 features (one half row) held by this thread; `pair` is the
+// shuffle mask of this thread and the one holding the other half (SiLU's
+// norm runs over the whole row).
 template <int PHI>
-__device__ __forceinline__ void phi_row(float* x) {
+__device__ __forceinline__ void phi_half(float* x, uint32_t pair) {
   if (PHI == PHI_ELU1) {
 #pragma unroll
-    for (int e = 0; e < kD; ++e) x[e] = x[e] > 0.f ? x[e] + 1.f : __expf(x[e]);
+    for (int e = 0; e < 32; ++e) x[e] = x[e] > 0.f ? x[e] + 1.f : ex2(x[e] * kLog2e);
   } else if (PHI == PHI_SILU_L2) {
-    float ss = 0.f;
+    float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < kD; ++e) {
-      x[e] = __fdividef(x[e], 1.f + __expf(-x[e]));
-      ss = fmaf(x[e], x[e], ss);
+    for (int e = 0; e < 32; e += 2) {
+      const float2 xx = make_float2(x[e], x[e + 1]);
+      const float2 t = mul2(xx, make_float2(-kLog2e, -kLog2e));
+      const float2 d = add2(make_float2(ex2(t.x), ex2(t.y)), make_float2(1.f, 1.f));
+      const float2 u = mul2(xx, make_float2(rcp(d.x), rcp(d.y)));   // silu; -0 when exp overflows
+      ss = fma2(u, u, ss);
+      x[e] = u.x;
+      x[e + 1] = u.y;
     }
-    const float inv = rsqrtf(fmaxf(ss, 1e-24f));
+    float s = ss.x + ss.y;
+    s += __shfl_xor_sync(pair, s, 1);
+    const float inv = rsqrtf(fmaxf(s, 1e-24f));
+    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-    for (int e = 0; e < kD; ++e) x[e] *= inv;
+    for (int e = 0; e < 32; e += 2) {
+      const float2 u = mul2(make_float2(x[e], x[e + 1]), inv2);
+      x[e] = u.x;
+      x[e + 1] = u.y;
+    }
   }
+}
+
+// Orders every later use of v[0..15] after the preceding tcgen05.wait::ld
+// (the TMEM load writes its registers asynchronously).
+__device__ __forceinline__ void reg_fence16(float* v) {
+  asm volatile("" : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+               "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+               "+f"(v[14]), "+f"(v[15]));
 }
 
 __device__ __forceinline__ uint64_t kmaj(const uint8_t* tile, int k) {
@@ -200,10 +262,63 @@ __device__ __forceinline__ float ell_of(const C128Params& p, int bh, int t, floa
   return 0.f;
 }
 
+// One 16-column block of the decay mask on a row of S (row i of its chunk,
+// columns j0..j0+15), in place.  Blocks entirely left (right) of every row
+// of the warp (rows row_lo..row_lo+31) take the lower (upper) factor pair
+// without a select.
+template <int MASK>
+__device__ __forceinline__ void mask_block(float* sv, int j0, int i, int row_lo, bool exact, float ai, float ri,
+                                           float pi, const float* alpha, const float* rho, const float* pp) {
+  if (MASK == MASK_LIT) return;
+  if (exact) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sv[e] *= ex2(-fabsf(pi - pp[j0 + e]) * kLog2e);
+    return;
+  }
+  if (j0 + 15 < row_lo) {
+    const float2 a2 = make_float2(ai, ai);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 r4 = *reinterpret_cast<const float4*>(rho + j0 + 4 * v);
+      const float2 p0 = mul2(mul2(make_float2(sv[4 * v], sv[4 * v + 1]), make_float2(r4.x, r4.y)), a2);
+      const float2 p1 = mul2(mul2(make_float2(sv[4 * v + 2], sv[4 * v + 3]), make_float2(r4.z, r4.w)), a2);
+      sv[4 * v] = p0.x;
+      sv[4 * v + 1] = p0.y;
+      sv[4 * v + 2] = p1.x;
+      sv[4 * v + 3] = p1.y;
+    }
+  } else if (j0 > row_lo + 31) {
+    const float2 r2 = make_float2(ri, ri);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 a4 = *reinterpret_cast<const float4*>(alpha + j0 + 4 * v);
+      const float2 p0 = mul2(mul2(make_float2(sv[4 * v], sv[4 * v + 1]), make_float2(a4.x, a4.y)), r2);
+      const float2 p1 = mul2(mul2(make_float2(sv[4 * v + 2], sv[4 * v + 3]), make_float2(a4.z, a4.w)), r2);
+      sv[4 * v] = p0.x;
+      sv[4 * v + 1] = p0.y;
+      sv[4 * v + 2] = p1.x;
+      sv[4 * v + 3] = p1.y;
+    }
+  } else {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 r4 = *reinterpret_cast<const float4*>(rho + j0 + 4 * v);
+      const float4 a4 = *reinterpret_cast<const float4*>(alpha + j0 + 4 * v);
+      const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + 4 * v + e;
+        sv[4 * v + e] *= j <= i ? ai * rr[e] : ri * aa[e];
+      }
+    }
+  }
+}
+
 template <int MASK, int PHI>
 __global__ void __launch_bounds__(kThreads, 1)
     lion_chunk128_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                            const __grid_constant__ CUtensorMap mapV, C128Params prm) {
+                            const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
+                            C128Params prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -227,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mapQ);
     prefetch_tmap(&mapK);
     prefetch_tmap(&mapV);
+    prefetch_tmap(&mapO);
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b));
     *s_abort = 0;
     fence_mbar_init();
@@ -262,28 +378,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == W_TMA) {
     // =========================== TMA producer ===================================
+    // Three independent streams; each load goes out as soon as its buffer is
+    // free: V(n) after O(n-2), K(n) after S(n-1) (LIT: U(n-1)), Q(n) after
+    // head n-2's output left the Q tiles.
     if (lane == 0) {
-      int issued_qv[2] = {0, 0}, issued_k = 0;
-      for (int n = 0; n < nheads; ++n) {
-        const int bh = head_of(n), s = n & 1;
-        if (n >= 2 && !waitb(B_QVE0 + s, ((n >> 1) - 1) & 1)) break;
-        mbar_arrive_expect_tx(&bars[B_QV0 + s], (uint32_t)(2 * nch * kTile));
-        for (int c = 0; c < nch; ++c) {
-          tma_load_3d(Qt(s, c), &mapQ, &bars[B_QV0 + s], 0, c * kC, bh);
-          tma_load_3d(Vt(s, c), &mapV, &bars[B_QV0 + s], 0, c * kC, bh);
+      int nv = 0, nk = 0, nq = 0;
+      long long idle0 = clock64();
+      while ((nv < nheads || nk < nheads || nq < nheads) && !*s_abort) {
+        bool progress = false;
+        if (nv < nheads && (nv < 2 || mbar_try_wait(&bars[B_VE0 + (nv & 1)], ((nv >> 1) - 1) & 1))) {
+          const int s = nv & 1, bh = head_of(nv);
+          mbar_arrive_expect_tx(&bars[B_V0 + s], (uint32_t)(nch * kTile));
+          for (int c = 0; c < nch; ++c) tma_load_3d(Vt(s, c), &mapV, &bars[B_V0 + s], 0, c * kC, bh);
+          ++nv;
+          progress = true;
         }
-        ++issued_qv[s];
-        if (n >= 1 && !waitb(B_KE, (n - 1) & 1)) break;
-        mbar_arrive_expect_tx(&bars[B_K], (uint32_t)(nch * kTile));
-        for (int c = 0; c < nch; ++c) tma_load_3d(Kt(c), &mapK, &bars[B_K], 0, c * kC, bh);
-        ++issued_k;
+        if (nk < nheads && (nk < 1 || mbar_try_wait(&bars[B_KE], (nk - 1) & 1))) {
+          const int bh = head_of(nk);
+          mbar_arrive_expect_tx(&bars[B_K], (uint32_t)(nch * kTile));
+          for (int c = 0; c < nch; ++c) tma_load_3d(Kt(c), &mapK, &bars[B_K], 0, c * kC, bh);
+          ++nk;
+          progress = true;
+        }
+        if (nq < nheads && (nq < 2 || mbar_try_wait(&bars[B_QE0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
+          const int s = nq & 1, bh = head_of(nq);
+          mbar_arrive_expect_tx(&bars[B_Q0 + s], (uint32_t)(nch * kTile));
+          for (int c = 0; c < nch; ++c) tma_load_3d(Qt(s, c), &mapQ, &bars[B_Q0 + s], 0, c * kC, bh);
+          ++nq;
+          progress = true;
+        }
+        if (progress) {
+          idle0 = clock64();
+        } else {
+          __nanosleep(64);
+          if (clock64() - idle0 > kWaitCycles) *s_abort = 1;
+        }
       }
       if (*s_abort) {
         // let the copies already issued land before the CTA lets go of its memory
         const long long lim = kWaitCycles / 4;
-        for (int s = 0; s < 2; ++s)
-          if (issued_qv[s]) mbar_wait(&bars[B_QV0 + s], (issued_qv[s] - 1) & 1, lim);
-        if (issued_k) mbar_wait(&bars[B_K], (issued_k - 1) & 1, lim);
+        for (int s = 0; s < 2; ++s) {
+          const int v_is = (nv - s + 1) / 2, q_is = (nq - s + 1) / 2;   // loads issued into slot s
+          if (v_is) mbar_wait(&bars[B_V0 + s], (v_is - 1) & 1, lim);
+          if (q_is) mbar_wait(&bars[B_Q0 + s], (q_is - 1) & 1, lim);
+        }
+        if (nk) mbar_wait(&bars[B_K], (nk - 1) & 1, lim);
       }
     }
   } else if (warp == W_MMA) {
@@ -294,6 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idPV = idesc_f16(128, 80, false, true);
       const uint32_t idQX = idesc_f16(128, 64, false, true);
       const uint32_t ones = smem_u32(smem + OFF_ONES);
+      // LIT's state MMA reads phi(K) itself: K stays until the states are done
+      const bool k_after_u = states && MASK == MASK_LIT;
       bool issued = false;
       for (int n = 0; n < nheads; ++n) {
         const int s = n & 1;
@@ -305,8 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k)
             mma_bf16(tbase + T_S + 128 * c, kmaj(Qt(s, c), k), kmaj(Kt(c), k), idS, k > 0 ? 1u : 0u);
         mma_commit(&bars[B_S]);
-        // LIT's state MMA reads phi(K) itself: K stays until the states are done
-        const bool k_after_u = states && MASK == MASK_LIT;
         if (!k_after_u) mma_commit(&bars[B_KE]);
         issued = true;
         if (n >= 1 && !waitb(B_ED, (n - 1) & 1)) break;   // O of the previous head read
@@ -339,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(&bars[B_O]);
-        mma_commit(&bars[B_QVE0 + s]);
+        mma_commit(&bars[B_VE0 + s]);
       }
       if (*s_abort && issued) {
         mma_commit(&bars[B_DRAIN]);
@@ -347,123 +486,133 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < W_EPI) {
-    // =========================== prep: one thread per token ======================
-    const int pw = warp - W_PREP;
-    const int t = 32 * pw + lane;           // token within the head
+    // =========================== prep: two threads per token =====================
+    const int pw = warp - W_PREP;            // 0..15; chunk c = pw / 8
+    const int pt = 32 * pw + lane;
+    const int t = pt >> 1, h = pt & 1;       // token within the head, half row
     const int c = t >> 7, r = t & (kC - 1);
+    const uint32_t pair = 3u << (lane & 30);
     float* red = reinterpret_cast<float*>(smem + OFF_RED);
     bool good = true;
-    float ell_next = 0.f, lh_next = 0.f;
+    float ell_next = 0.f;
     if (nheads > 0) {
       const int bh0 = head_of(0);
-      lh_next = MASK == MASK_D ? __ldg(prm.log_lambda + bh0 % prm.H) : 0.f;
-      ell_next = ell_of<MASK>(prm, bh0, t, lh_next);
+      const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh0 % prm.H) : 0.f;
+      ell_next = ell_of<MASK>(prm, bh0, t, lh);
     }
     for (int n = 0; n < nheads; ++n) {
-      const int bh = head_of(n), s = n & 1;
+      const int s = n & 1;
       const float ell = ell_next;
-      // ---- chunk-local inclusive prefix of l over this thread's chunk
+      // ---- chunk-local inclusive prefix of l (each token's value sits in
+      //      both lanes of its pair, so steps of two lanes)
       float x = ell;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
+      for (int o = 2; o < 32; o <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
       }
-      float* rd = red + 16 * (n & 1);
+      float* rd = red + 32 * (n & 1);
       if (lane == 31) rd[pw] = x;
-      if (t == 0) rd[8] = ell;          // l at the first token of chunk 0
-      if (t == kC) rd[9] = ell;         // l at the first token of chunk 1
+      if (pt == 0) rd[16] = ell;              // l at the first token of chunk 0
+      if (pt == 2 * kC) rd[17] = ell;         // l at the first token of chunk 1
       good = bar_and(1, kPrepWarps * 32, good);
       if (!good) break;
       float pre = 0.f;
-      for (int w = 4 * c; w < pw; ++w) pre += rd[w];
+      for (int w = 8 * c; w < pw; ++w) pre += rd[w];
       const float p = x + pre;                                      // p_t
-      const float T0 = rd[0] + rd[1] + rd[2] + rd[3];               // chunk-0 total
-      const float T1 = rd[4] + rd[5] + rd[6] + rd[7];
-      const float l128 = rd[9];
-      const float pfirst = c == 0 ? rd[8] : rd[9], plast = c == 0 ? T0 : T1;
+      float T0 = 0.f, T1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        T0 += rd[w];
+        T1 += rd[8 + w];
+      }
+      const float l128 = rd[17];
+      const float pfirst = c == 0 ? rd[16] : rd[17], plast = c == 0 ? T0 : T1;
       const float pref = 0.5f * (pfirst + plast);
       const bool exact = (pfirst - plast) > 2.f * kMaxFactorRange;
-      // weight of this token in its chunk's state, and the decay applied to
-      // the state product of this token's query
-      const float w = c == 0 ? __expf(T0 - p) : __expf(p - l128);
-      const float sig = !states ? 0.f : c == 0 ? __expf(T0 + l128 - p) : __expf(p);
+      const bool live = t < L;
+      const int j0 = 4 * h;                   // first 16-byte chunk of this half row
 
+      // ---- V -> fp16 in place
+      if (!waitb(B_V0 + s, (n >> 1) & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);   // pairs must agree before phi's pair shuffle
+      if (good && live) {
+        uint8_t* vt = Vt(s, c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4* a = reinterpret_cast<uint4*>(vt + sw128_offset(r, j0 + j));
+          *a = bf8_to_h8(*a);
+        }
+      }
       // ---- K: phi(k) in place; the decay-weighted copy for the state MMA
       if (!waitb(B_K, n & 1)) good = false;
-      if (good && t < L) {
+      good = __all_sync(0xffffffffu, good);
+      const bool kw = states && MASK != MASK_LIT;
+      if (good && live) {
         uint8_t* kt = Kt(c);
-        float kv[kD];
+        float kv[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) unpack8_bf(*reinterpret_cast<const uint4*>(kt + sw128_offset(r, j)), kv + 8 * j);
-        phi_row<PHI>(kv);
+        for (int j = 0; j < 4; ++j)
+          unpack8_bf(*reinterpret_cast<const uint4*>(kt + sw128_offset(r, j0 + j)), kv + 8 * j);
+        phi_half<PHI>(kv, pair);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(kt + sw128_offset(r, j)) = pack8_h(kv + 8 * j);
-        if (states && MASK != MASK_LIT) {
+        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(kt + sw128_offset(r, j0 + j)) = pack8_h(kv + 8 * j);
+        if (kw) {
           if (n >= 1 && !waitb(B_KWE, (n - 1) & 1)) good = false;
           if (good) {
-            uint8_t* kw = KWt(c);
+            // weight of this token in its chunk's state
+            const float w = c == 0 ? ex2((T0 - p) * kLog2e) : ex2((p - l128) * kLog2e);
+            const float2 w2 = make_float2(w, w);
+            uint8_t* kwt = KWt(c);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
               float y8[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) y8[e] = w * kv[8 * j + e];
-              *reinterpret_cast<uint4*>(kw + sw128_offset(r, j)) = pack8_h(y8);
+              for (int e = 0; e < 8; e += 2) {
+                const float2 u = mul2(make_float2(kv[8 * j + e], kv[8 * j + e + 1]), w2);
+                y8[e] = u.x;
+                y8[e + 1] = u.y;
+              }
+              *reinterpret_cast<uint4*>(kwt + sw128_offset(r, j0 + j)) = pack8_h(y8);
             }
           }
         }
-      } else if (good && states && MASK != MASK_LIT) {
+      } else if (good && kw) {
         // padding token: a zero row in the weighted copy (phi(K) keeps the
         // zeros the copy engine filled in)
         if (n >= 1 && !waitb(B_KWE, (n - 1) & 1)) good = false;
         if (good) {
-          uint8_t* kw = KWt(c);
+          uint8_t* kwt = KWt(c);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(kw + sw128_offset(r, j)) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // ---- V -> fp16 in place
-      if (!waitb(B_QV0 + s, (n >> 1) & 1)) good = false;
-      if (good && t < L) {
-        uint8_t* vt = Vt(s, c);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4* a = reinterpret_cast<uint4*>(vt + sw128_offset(r, j));
-          *a = bf8_to_h8(*a);
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(kwt + sw128_offset(r, j0 + j)) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_KVR]);
       // ---- mask factors and phi(q)
-      if (good) {
+      if (good && h == 0) {
         float* f = fac(s);
-        const float d = p - pref;
-        f[t] = __expf(d);
-        f[kRows + t] = __expf(-d);
-        f[2 * kRows + t] = sig;
+        const float d = (p - pref) * kLog2e;
+        f[t] = ex2(d);
+        f[kRows + t] = ex2(-d);
+        // decay applied to the state product of this token's query
+        f[2 * kRows + t] = !states ? 0.f : c == 0 ? ex2((T0 + l128 - p) * kLog2e) : ex2(p * kLog2e);
         f[3 * kRows + t] = p;
-        if (t == 0) {
-          float* in = info(s);
-          in[I_T0] = T0;
-          in[I_L128] = l128;
-          in[I_REF0] = pref;
-          in[I_EX0] = exact ? 1.f : 0.f;
-        }
-        if (t == kC) {
-          float* in = info(s);
-          in[I_REF1] = pref;
-          in[I_EX1] = exact ? 1.f : 0.f;
-        }
+        if (r == 0) info(s)[I_EX0 + c] = exact ? 1.f : 0.f;
       }
-      if (good && t < L) {
+      if (!waitb(B_Q0 + s, (n >> 1) & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      if (good && live) {
         uint8_t* qt = Qt(s, c);
-        float qv[kD];
+        float qv[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) unpack8_bf(*reinterpret_cast<const uint4*>(qt + sw128_offset(r, j)), qv + 8 * j);
-        phi_row<PHI>(qv);
+        for (int j = 0; j < 4; ++j)
+          unpack8_bf(*reinterpret_cast<const uint4*>(qt + sw128_offset(r, j0 + j)), qv + 8 * j);
+        phi_half<PHI>(qv, pair);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(qt + sw128_offset(r, j)) = pack8_h(qv + 8 * j);
+        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(qt + sw128_offset(r, j0 + j)) = pack8_h(qv + 8 * j);
       }
       fence_async_smem();
       __syncwarp();
@@ -471,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- the next head's decays, loaded while this head is in flight
       if (n + 1 < nheads) {
         const int bhn = head_of(n + 1);
-        lh_next = MASK == MASK_D ? __ldg(prm.log_lambda + bhn % prm.H) : 0.f;
-        ell_next = ell_of<MASK>(prm, bhn, t, lh_next);
+        const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bhn % prm.H) : 0.f;
+        ell_next = ell_of<MASK>(prm, bhn, t, lh);
       }
     }
   } else {
@@ -501,31 +650,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool exact = info(s)[I_EX0 + g] != 0.f;
         const float ai = alpha[i], ri = rho[i], pi = pp[i];
         const uint32_t sa = tbase + lane_off + T_S + 128 * g;
+        float sb0[16], sb1[16];
+        tmem_ld16(sa, sb0);
+        tmem_wait_ld();
+        reg_fence16(sb0);
 #pragma unroll 1
-        for (int jj = 0; jj < 8; ++jj) {
-          float sv[16];
-          tmem_ld16(sa + 16 * jj, sv);
-          tmem_wait_ld();
-          const int j0 = 16 * jj;
-          if (MASK != MASK_LIT) {
-            if (exact) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) sv[e] *= __expf(-fabsf(pi - pp[j0 + e]));
-            } else if (j0 + 15 < 32 * q) {         // whole block left of every row of the warp
-#pragma unroll
-              for (int e = 0; e < 16; ++e) sv[e] *= ai * rho[j0 + e];
-            } else if (j0 > 32 * q + 31) {         // whole block right of every row
-#pragma unroll
-              for (int e = 0; e < 16; ++e) sv[e] *= ri * alpha[j0 + e];
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) sv[e] *= (j0 + e <= i) ? ai * rho[j0 + e] : ri * alpha[j0 + e];
-            }
-          }
+        for (int jj = 0; jj < 8; jj += 2) {
           uint32_t pk[8];
+          tmem_ld16(sa + 16 * (jj + 1), sb1);
+          mask_block<MASK>(sb0, 16 * jj, i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sv[2 * e], sv[2 * e + 1]);
+          for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb0[2 * e], sb0[2 * e + 1]);
           tmem_st8(sa + 8 * jj, pk);
+          tmem_wait_ld();
+          reg_fence16(sb1);
+          if (jj + 2 < 8) tmem_ld16(sa + 16 * (jj + 2), sb0);
+          mask_block<MASK>(sb1, 16 * (jj + 1), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb1[2 * e], sb1[2 * e + 1]);
+          tmem_st8(sa + 8 * (jj + 1), pk);
+          if (jj + 2 < 8) {
+            tmem_wait_ld();
+            reg_fence16(sb0);
+          }
         }
       }
       // ---- state tiles (group g writes the state applied to chunk g) and the
@@ -567,22 +714,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         good = bar_and(2 + g, 128, good);
         if (good && row_ok) {
           const float sg = f[2 * kRows + tok];
+          const float2 sg2 = make_float2(sg, sg);
           uint8_t* qt = Qt(s, g);
           const float* z = sZ + kD * g;
-          float acc = 0.f;
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             uint4* a = reinterpret_cast<uint4*>(qt + sw128_offset(i, j));
             float x8[8];
             unpack8_h(*a, x8);
+            const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * j);
+            const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * j + 4);
+            acc = fma2(make_float2(x8[0], x8[1]), make_float2(z0.x, z0.y), acc);
+            acc = fma2(make_float2(x8[2], x8[3]), make_float2(z0.z, z0.w), acc);
+            acc = fma2(make_float2(x8[4], x8[5]), make_float2(z1.x, z1.y), acc);
+            acc = fma2(make_float2(x8[6], x8[7]), make_float2(z1.z, z1.w), acc);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              acc = fmaf(x8[e], z[8 * j + e], acc);
-              x8[e] *= sg;
+            for (int e = 0; e < 8; e += 2) {
+              const float2 y = mul2(make_float2(x8[e], x8[e + 1]), sg2);
+              x8[e] = y.x;
+              x8[e + 1] = y.y;
             }
             *a = pack8_h(x8);
           }
-          dstate = sg * acc;
+          dstate = sg * (acc.x + acc.y);
         }
       }
       tmem_wait_st();
@@ -590,33 +745,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_PR]);
-      // ---- y = O[0:64] / (O[64] + state normaliser)
+      // ---- y = O[0:64] / (O[64] + state normaliser).  Each warp stages its 32
+      //      rows, 32 columns at a time, with a 128-byte swizzle in its own
+      //      4 KB of this chunk's Q tile (spent once O is done) and writes them
+      //      with a TMA store, which drops the rows past L.
       if (!waitb(B_O, n & 1)) good = false;
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
       if (good && warp_ok) {
         const uint32_t oa = tbase + lane_off + T_O + 80 * g;
-        const float inv = 1.f / (tmem_ld1(oa + 64) + dstate);
-        float4* dst = reinterpret_cast<float4*>(prm.out + ((size_t)bh * L + tok) * kD);
+        uint8_t* stg = Qt(s, g) + 32 * q * 128;
+        float ob0[16], ob1[16];
+        tmem_ld16(oa + 64, ob1);            // column 64: the row sum
+        tmem_ld16(oa, ob0);
+        tmem_wait_ld();
+        reg_fence16(ob0);
+        reg_fence16(ob1);
+        const float inv = 1.f / (ob1[0] + dstate);
+        const float2 inv2 = make_float2(inv, inv);
+        uint8_t* row = stg + lane * 128;
 #pragma unroll 1
-        for (int jb = 0; jb < 4; ++jb) {
-          float o[16];
-          tmem_ld16(oa + 16 * jb, o);
-          tmem_wait_ld();
-          if (row_ok) {
+        for (int half = 0; half < 2; ++half) {
+          if (half == 1) {
+            // the first store has to be done reading the staging
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+          }
+          tmem_ld16(oa + 32 * half + 16, ob1);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              __stcs(dst + 4 * jb + e,
-                     make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv));
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = mul2(make_float2(ob0[4 * e], ob0[4 * e + 1]), inv2);
+            const float2 b = mul2(make_float2(ob0[4 * e + 2], ob0[4 * e + 3]), inv2);
+            *reinterpret_cast<float4*>(row + ((e ^ (lane & 7)) << 4)) = make_float4(a.x, a.y, b.x, b.y);
+          }
+          tmem_wait_ld();
+          reg_fence16(ob1);
+          if (half == 0) tmem_ld16(oa + 32, ob0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = mul2(make_float2(ob1[4 * e], ob1[4 * e + 1]), inv2);
+            const float2 b = mul2(make_float2(ob1[4 * e + 2], ob1[4 * e + 3]), inv2);
+            *reinterpret_cast<float4*>(row + (((4 + e) ^ (lane & 7)) << 4)) = make_float4(a.x, a.y, b.x, b.y);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&mapO, stg, 32 * half, kC * g + 32 * q, bh);
+            bulk_commit();
+          }
+          if (half == 0) {
+            tmem_wait_ld();
+            reg_fence16(ob0);
           }
         }
+        if (lane == 0) bulk_wait_read();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_ED]);
+      if (lane == 0) {
+        mbar_arrive(&bars[B_ED]);
+        mbar_arrive(&bars[B_QE0 + s]);
+      }
       // leave together: the group's named barrier needs all four warps
       if (!bar_and(2 + g, 128, good)) break;
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   __syncthreads();
@@ -660,6 +853,20 @@ bool make_map128(CUtensorMap* m, const void* base, int L, int BH) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// out: [BH][L][64] fp32; box = 32 columns (128 bytes, 128-byte swizzle) x
+// 32 rows x 1 (rows past L are not written).
+bool make_out_map(CUtensorMap* m, float* base, int L, int BH) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)L * kD * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -678,18 +885,18 @@ bool chunk128_tc_supported(const Problem& p) {
 }
 
 cudaError_t launch_chunk128_tc(const Problem& p, int* status, cudaStream_t s) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const int BH = p.B * p.H;
-  if (!make_map128(&mq, p.q, p.L, BH) || !make_map128(&mk, p.k, p.L, BH) || !make_map128(&mv, p.v, p.L, BH))
+  if (!make_map128(&mq, p.q, p.L, BH) || !make_map128(&mk, p.k, p.L, BH) || !make_map128(&mv, p.v, p.L, BH) ||
+      !make_out_map(&mo, p.out, p.L, BH))
     return cudaErrorInvalidValue;
   C128Params prm;
-  prm.out = p.out;
   prm.log_lambda = p.log_lambda;
   prm.BH = BH;
   prm.H = p.H;
   prm.L = p.L;
   prm.status = status;
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, C128Params) = nullptr;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, C128Params) = nullptr;
 #define LION_C128_CASE(M, F) \
   if (p.mask_kind == M && p.phi == F) kern = lion_chunk128_tc_kernel<M, F>;
   LION_C128_CASE(MASK_LIT, PHI_ELU1)
@@ -706,7 +913,7 @@ cudaError_t launch_chunk128_tc(const Problem& p, int* status, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = BH < sm_count() ? BH : sm_count();
-  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, prm);
   return cudaGetLastError();
 }
 
