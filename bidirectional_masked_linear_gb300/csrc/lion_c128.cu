@@ -29,22 +29,31 @@
 //               prefix, V -> fp16 in place, phi(k) in place, the
 //               decay-weighted phi(k) copy for the state MMA, phi(q) in
 //               place, mask factors;
-//   warps 18-25 "epi", one thread per TMEM lane (= row of a chunk): the decay
-//               mask on S (P = S * M, fp16, written back into TMEM as the A
-//               operand of P [V | 1]), the state tiles, the decay-scaled
-//               phi(q) for the state product, and the normalised output,
-//               staged per warp in the head's spent Q tile and written by TMA.
-// prep of head h+1 overlaps epi of head h.  MMAs per head:
-//   S_c  = phi(Q_c) phi(K_c)^T                      M=128 N=128 K=64
-//   U_c  = (w_c o phi(K_c))^T [V_c | 1]             M=64  N=80  K=128
-//   O_c  = P_c [V_c | 1] + (sigma o phi(Q_c)) X_c   M=128 N=80  K=128 (+ N=64 K=64)
-// where X_0 = G_0, X_1 = F_1.  The ones column of [V | 1] comes from a 2 KB
-// constant tile addressed through the descriptor's leading byte offset; the
-// normaliser contribution of the states, sigma_i phi(q_i).z, is a CUDA-core
-// dot product in fp32.
+//   warps 18-25 "epi", one thread per TMEM lane (= row of a chunk), one
+//               group of four warps per chunk: the decay mask on S (P = S * M,
+//               fp16, written back into TMEM as the A operand of P [V | 1]),
+//               the state tile, the decay-scaled phi(q) for the state
+//               product, and the normalised output, staged per warp in the
+//               head's spent Q tile and written by TMA;
+//               the TMA warp also pulls each head's K and Q into L2 when it
+//               loads its V.
+// prep of head h+1 overlaps epi of head h, and the two chunks run as two
+// pipelines (one epi warp group each, per-chunk barriers).  MMAs per head,
+// n_c = columns of chunk c rounded up to 16 (padding beyond is skipped):
+//   S_c   = phi(Q_c) phi(K_c)^T                     M=128 N=n_c K=64
+//   X_c^T = [V_c' | 1]^T (w_c' o phi(K_c'))          M=128 N=64  K=n_c'
+//   O_c   = P_c [V_c | 1] + (sigma o phi(Q_c)) X_c  M=128 N=80  K=n_c (+ K=64)
+// where c' = 1 - c is the chunk whose state chunk c applies (X_0 = G_0 from
+// chunk 1's backward weights, X_1 = F_1 from chunk 0's forward weights).
+// The state comes out transposed (TMEM lane = output column, lane 64 = the
+// normaliser z), so the epi warps write it as a K-major operand tile of 80
+// rows with whole-row 16-byte stores, and the state product's column 64 is
+// the state part of the row sum.  The ones of [V | 1] come from a 2 KB
+// constant tile addressed through the descriptor's leading byte offset.
 //
-// TMEM (512 columns): U_0/O_0 at [0, 80), U_1/O_1 at [80, 160), S_0 at
-// [160, 288), S_1 at [288, 416); P_c overwrites the first 64 columns of S_c.
+// TMEM (512 columns): X_0^T then O_0 at [0, 80), X_1^T then O_1 at [80, 160),
+// S_0 at [160, 288), S_1 at [288, 416); P_c overwrites the first 64 columns
+// of S_c.
 //
 // Mask factors: within a chunk M_ij = alpha_i rho_j (j <= i) or rho_i alpha_j
 // (j > i) with alpha_t = exp(p_t - p_ref), rho_t = 1 / alpha_t and p_ref the
@@ -53,7 +62,8 @@
 //
 // Precision: MMA operands are fp16 (11-bit significand) with fp32
 // accumulation; phi(K), phi(Q), the weighted phi(K), V, P and the two
-// states are each rounded once to fp16, and the decay-scaled phi(q) twice.
+// states (with their z) are each rounded once to fp16, and the decay-scaled
+// phi(q) twice.
 // Precondition: |phi(q)|, |phi(k)|, |v| and the states below 65504.
 //
 // Every mbarrier wait is bounded; on timeout the kernel records an error in
@@ -76,7 +86,8 @@ constexpr int kC = 128;                 // chunk length
 constexpr int kD = 64;                  // head dim
 constexpr int kRows = 2 * kC;           // tokens per head at most
 constexpr int kTile = kC * 128;         // 128 rows x 64 16-bit values, 128-byte swizzle
-constexpr int kStTile = kD * 128;       // 64 x 64 16-bit state tile
+constexpr int kStRows = 80;             // state tile rows: 64 columns of X, z, 15 zero rows
+constexpr int kStTile = kStRows * 128;  // K-major 16-bit state tile
 constexpr int kPrepWarps = 16, kEpiWarps = 8;
 constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
 constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
@@ -94,10 +105,9 @@ constexpr int OFF_ST = OFF_KW + 2 * kTile;        // [chunk] state applied to th
 constexpr int OFF_ONES = OFF_ST + 2 * kStTile;    // 16 rows, column 0 = 1
 constexpr int OFF_FAC = OFF_ONES + 2048;          // [slot] float alpha[256], rho[256], sig[256], p[256]
 constexpr int OFF_INFO = OFF_FAC + 2 * 4 * kRows * 4;  // [slot] float[8] per-head scalars
-constexpr int OFF_Z = OFF_INFO + 2 * 8 * 4;       // [chunk] float[64] z of the state applied
-constexpr int OFF_RED = OFF_Z + 2 * kD * 4;       // [parity] float[32] prep scan scratch
+constexpr int OFF_RED = OFF_INFO + 2 * 8 * 4;     // [parity] float[32] prep scan scratch
 constexpr int OFF_BAR = OFF_RED + 2 * 32 * 4;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 24;
 constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -106,33 +116,34 @@ static_assert(OFF_ONES % 1024 == 0 && OFF_ST % 1024 == 0, "swizzled tiles need 1
 // per-head scalars (INFO): exact-mask flag of chunk 0/1
 enum { I_EX0 = 0, I_EX1 = 1 };
 
-// mbarriers
+// mbarriers ("+ c": one per chunk, "+ slot": one per Q/V slot)
 enum {
   B_V0 = 0,       // + slot: V tiles landed (TMA, tx bytes)
   B_Q0 = 2,       // + slot: Q tiles landed
   B_K = 4,        // K tiles landed
   B_KVR = 5,      // prep: V, phi(K), weighted phi(K) written (16 arrivals)
   B_QR = 6,       // prep: phi(Q) and factors written (16 arrivals)
-  B_S = 7,        // MMA commit: S done
-  B_KE = 8,       // MMA commit: K tiles free
-  B_U = 9,        // MMA commit: states done
-  B_KWE = 10,     // MMA commit: weighted phi(K) free
-  B_PR = 11,      // epi: P, state tiles, scaled phi(Q) written (8 arrivals)
-  B_O = 12,       // MMA commit: O done
-  B_VE0 = 13,     // + slot: MMA commit: V tiles free
-  B_QE0 = 15,     // + slot: Q tiles free: every epi warp's output store has read its staging (8)
-  B_ED = 17,      // epi: O read (8 arrivals)
-  B_DRAIN = 18,   // MMA commit used when unwinding
+  B_S0 = 7,       // + c: MMA commit: S_c done
+  B_KE = 9,       // MMA commit: K tiles free
+  B_U0 = 10,      // + c: MMA commit: the state chunk c applies is done
+  B_KWE = 12,     // MMA commit: weighted phi(K) free
+  B_PR0 = 13,     // + c: epi group c: P_c, state tile, scaled phi(Q_c) written (4 arrivals)
+  B_O0 = 15,      // + c: MMA commit: O_c done
+  B_VE0 = 17,     // + slot: MMA commit: V tiles free
+  B_QE0 = 19,     // + slot: Q tiles free: every epi warp's output store has read its staging
+  B_ED0 = 21,     // + c: epi group c: O_c read (4 arrivals)
+  B_DRAIN = 23,   // MMA commit used when unwinding
 };
-__host__ __device__ constexpr uint32_t bar_count(int b) {
-  return (b == B_KVR || b == B_QR)                                  ? (uint32_t)kPrepWarps
-         : (b == B_PR || b == B_ED || b == B_QE0 || b == B_QE0 + 1) ? (uint32_t)kEpiWarps
-                                                                    : 1u;
+__device__ __forceinline__ uint32_t bar_count(int b, int nch) {
+  if (b == B_KVR || b == B_QR) return kPrepWarps;
+  if (b == B_PR0 || b == B_PR0 + 1 || b == B_ED0 || b == B_ED0 + 1) return 4;
+  if (b == B_QE0 || b == B_QE0 + 1) return 4 * nch;   // the warps of the groups with a chunk
+  return 1;
 }
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t T_O = 0;       // + 80 c: U_c then O_c
+constexpr uint32_t T_O = 0;       // + 80 c: the transposed state chunk c applies, then O_c
 constexpr uint32_t T_S = 160;     // + 128 c: S_c, P_c in its first 64 columns
 
 struct C128Params {
@@ -331,19 +342,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto STt = [&](int c) { return smem + OFF_ST + c * kStTile; };
   auto fac = [&](int s) { return reinterpret_cast<float*>(smem + OFF_FAC) + s * 4 * kRows; };
   auto info = [&](int s) { return reinterpret_cast<float*>(smem + OFF_INFO) + s * 8; };
-  float* sZ = reinterpret_cast<float*>(smem + OFF_Z);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = prm.L;
   const int nch = L > kC ? 2 : 1;
   const bool states = nch == 2;
+  // 16-column steps holding tokens, per chunk (the rest is padding)
+  const int nk0 = nch == 2 ? 8 : (L + 15) >> 4;
+  const int nk1 = nch == 2 ? (L - kC + 15) >> 4 : 0;
 
   if (tid == 0) {
     prefetch_tmap(&mapQ);
     prefetch_tmap(&mapK);
     prefetch_tmap(&mapV);
     prefetch_tmap(&mapO);
-    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b));
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b, nch));
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -390,6 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = nv & 1, bh = head_of(nv);
           mbar_arrive_expect_tx(&bars[B_V0 + s], (uint32_t)(nch * kTile));
           for (int c = 0; c < nch; ++c) tma_load_3d(Vt(s, c), &mapV, &bars[B_V0 + s], 0, c * kC, bh);
+          // K and Q of this head wait for buffers a while longer: start them towards L2
+          for (int c = 0; c < nch; ++c) {
+            tma_prefetch_3d(&mapK, 0, c * kC, bh);
+            tma_prefetch_3d(&mapQ, 0, c * kC, bh);
+          }
           ++nv;
           progress = true;
         }
@@ -428,56 +446,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == W_MMA) {
     // =========================== MMA issuer =====================================
     if (lane == 0) {
-      const uint32_t idS = idesc_f16(128, 128, false, false);
-      const uint32_t idU = idesc_f16(64, 80, true, true);
+      const uint32_t idUT = idesc_f16(128, 64, true, true);
       const uint32_t idPV = idesc_f16(128, 80, false, true);
-      const uint32_t idQX = idesc_f16(128, 64, false, true);
+      const uint32_t idQX = idesc_f16(128, 80, false, false);
       const uint32_t ones = smem_u32(smem + OFF_ONES);
       // LIT's state MMA reads phi(K) itself: K stays until the states are done
       const bool k_after_u = states && MASK == MASK_LIT;
-      bool issued = false;
-      for (int n = 0; n < nheads; ++n) {
+      bool issued = false, ok = true;
+      for (int n = 0; n < nheads && ok; ++n) {
         const int s = n & 1;
         if (!waitb(B_KVR, n & 1) || !waitb(B_QR, n & 1)) break;
-        if (n >= 1 && !waitb(B_O, (n - 1) & 1)) break;   // P of the previous head consumed
-        tc_fence_after();
-        for (int c = 0; c < nch; ++c)
+        for (int c = 0; c < nch && ok; ++c) {
+          if (n >= 1 && !waitb(B_O0 + c, (n - 1) & 1)) ok = false;   // P_c of the previous head consumed
+          if (!ok) break;
+          tc_fence_after();
+          const int nk = c == 0 ? nk0 : nk1;
+          const uint32_t idS = idesc_f16(128, 16 * nk, false, false);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_bf16(tbase + T_S + 128 * c, kmaj(Qt(s, c), k), kmaj(Kt(c), k), idS, k > 0 ? 1u : 0u);
-        mma_commit(&bars[B_S]);
+          mma_commit(&bars[B_S0 + c]);
+          issued = true;
+        }
+        if (!ok) break;
         if (!k_after_u) mma_commit(&bars[B_KE]);
-        issued = true;
-        if (n >= 1 && !waitb(B_ED, (n - 1) & 1)) break;   // O of the previous head read
-        tc_fence_after();
         if (states) {
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t a = smem_u32(MASK == MASK_LIT ? Kt(c) : KWt(c));
-            const uint32_t v = smem_u32(Vt(s, c));
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_bf16(tbase + T_O + 80 * c, mnmaj(a, k, 0), mnmaj(v, k, ones - (v + 2048 * k)), idU,
+          // the state group g applies comes from chunk 1 - g
+          for (int g = 0; g < 2 && ok; ++g) {
+            if (n >= 1 && !waitb(B_ED0 + g, (n - 1) & 1)) ok = false;   // O_g of the previous head read
+            if (!ok) break;
+            tc_fence_after();
+            const int c = 1 - g, nk = c == 0 ? nk0 : nk1;
+            const uint32_t a = smem_u32(Vt(s, c));
+            const uint32_t b = smem_u32(MASK == MASK_LIT ? Kt(c) : KWt(c));
+            for (int k = 0; k < nk; ++k)
+              mma_bf16(tbase + T_O + 80 * g, mnmaj(a, k, ones - (a + 2048 * k)), mnmaj(b, k, 0), idUT,
                        k > 0 ? 1u : 0u);
+            mma_commit(&bars[B_U0 + g]);
           }
-          mma_commit(&bars[B_U]);
+          if (!ok) break;
           mma_commit(&bars[B_KWE]);
           if (k_after_u) mma_commit(&bars[B_KE]);
         }
-        if (!waitb(B_PR, n & 1)) break;
-        tc_fence_after();
-        for (int c = 0; c < nch; ++c) {
+        for (int c = 0; c < nch && ok; ++c) {
+          if (!states && n >= 1 && !waitb(B_ED0 + c, (n - 1) & 1)) ok = false;
+          if (ok && !waitb(B_PR0 + c, n & 1)) ok = false;
+          if (!ok) break;
+          tc_fence_after();
+          const int nk = c == 0 ? nk0 : nk1;
           const uint32_t v = smem_u32(Vt(s, c));
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int k = 0; k < nk; ++k)
             mma_tmem_a(tbase + T_O + 80 * c, tbase + T_S + 128 * c + 8 * k, mnmaj(v, k, ones - (v + 2048 * k)),
                        idPV, k > 0 ? 1u : 0u);
           if (states) {
-            const uint32_t x = smem_u32(STt(c));
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_O + 80 * c, kmaj(Qt(s, c), k), mnmaj(x, k, 0), idQX, 1u);
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(tbase + T_O + 80 * c, kmaj(Qt(s, c), k), kmaj(STt(c), k), idQX, 1u);
           }
+          mma_commit(&bars[B_O0 + c]);
         }
-        mma_commit(&bars[B_O]);
+        if (!ok) break;
         mma_commit(&bars[B_VE0 + s]);
       }
       if (*s_abort && issued) {
@@ -632,18 +660,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = 32 * q + lane;           // row within chunk g
     const int tok = kC * g + i;
     const bool row_ok = tok < L;
-    const bool warp_ok = kC * g + 32 * q < L && g < nch;
+    const bool warp_ok = kC * g + 32 * q < L;
+    const int nk = g == 0 ? nk0 : nk1;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     bool good = true;
-    for (int n = 0; n < nheads; ++n) {
+    for (int n = 0; n < nheads && g < nch; ++n) {
       const int bh = head_of(n), s = n & 1;
       const float* f = fac(s);
       const float* alpha = f + kC * g;
       const float* rho = f + kRows + kC * g;
       const float* pp = f + 3 * kRows + kC * g;
-      float dstate = 0.f;
       // ---- P = S * M, fp16, into the first 64 columns of S
-      if (!waitb(B_S, n & 1)) good = false;
+      if (!waitb(B_S0 + g, n & 1)) good = false;
       good = __all_sync(0xffffffffu, good);   // TMEM loads below are warp-collective
       tc_fence_after();
       if (good && warp_ok) {
@@ -655,80 +683,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence16(sb0);
 #pragma unroll 1
-        for (int jj = 0; jj < 8; jj += 2) {
+        for (int jj = 0; jj < nk; jj += 2) {
           uint32_t pk[8];
-          tmem_ld16(sa + 16 * (jj + 1), sb1);
+          const bool has1 = jj + 1 < nk, has2 = jj + 2 < nk;
+          if (has1) tmem_ld16(sa + 16 * (jj + 1), sb1);
           mask_block<MASK>(sb0, 16 * jj, i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
 #pragma unroll
           for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb0[2 * e], sb0[2 * e + 1]);
           tmem_st8(sa + 8 * jj, pk);
-          tmem_wait_ld();
-          reg_fence16(sb1);
-          if (jj + 2 < 8) tmem_ld16(sa + 16 * (jj + 2), sb0);
-          mask_block<MASK>(sb1, 16 * (jj + 1), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb1[2 * e], sb1[2 * e + 1]);
-          tmem_st8(sa + 8 * (jj + 1), pk);
-          if (jj + 2 < 8) {
+          if (has1) {
             tmem_wait_ld();
-            reg_fence16(sb0);
+            reg_fence16(sb1);
+            if (has2) tmem_ld16(sa + 16 * (jj + 2), sb0);
+            mask_block<MASK>(sb1, 16 * (jj + 1), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb1[2 * e], sb1[2 * e + 1]);
+            tmem_st8(sa + 8 * (jj + 1), pk);
+            if (has2) {
+              tmem_wait_ld();
+              reg_fence16(sb0);
+            }
           }
         }
       }
-      // ---- state tiles (group g writes the state applied to chunk g) and the
-      //      decay-scaled phi(q) for the state product
+      // ---- the state tile this chunk applies (K-major, rows = output
+      //      columns, row 64 = z) and the decay-scaled phi(q)
       if (states) {
-        if (!waitb(B_U, n & 1)) good = false;
+        if (!waitb(B_U0 + g, n & 1)) good = false;
         good = __all_sync(0xffffffffu, good);
         tc_fence_after();
-        if (good) {
-          // U of the other chunk: M=64 rows 16q..16q+15 in lanes 32q..32q+15
-          const uint32_t ua = tbase + lane_off + T_O + 80 * (1 - g);
-          uint8_t* st = STt(g);
-          const int m0 = 16 * q + (lane >> 2), m1 = m0 + 8;
-          const int cc = 2 * (lane & 3);
+        if (good && q < 3) {
+          // transposed state: TMEM lane 32q + lane = tile row, 64 columns
+          const uint32_t ua = tbase + lane_off + T_O + 80 * g;
+          float u0[16], u1[16];
+          tmem_ld16(ua, u0);
+          tmem_ld16(ua + 16, u1);
+          tmem_wait_ld();
+          reg_fence16(u0);
+          reg_fence16(u1);
+          uint8_t* row = STt(g) + i * 128;
+          const bool st_row = i < kStRows;
 #pragma unroll
-          for (int jb = 0; jb < 4; ++jb) {
-            float u[8];
-            tmem_ld_16x256b_x2(ua + 16 * jb, u);
-            tmem_wait_ld();
-            // columns 16jb + cc, +1 (u[0..1] row m0, u[2..3] row m1) and 16jb + 8 + cc, +1 (u[4..7])
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int col = 16 * jb + 8 * hh + cc;
-              *reinterpret_cast<uint32_t*>(st + sw128_offset(m0, col >> 3) + 2 * (col & 7)) =
-                  pack_h2(u[4 * hh], u[4 * hh + 1]);
-              *reinterpret_cast<uint32_t*>(st + sw128_offset(m1, col >> 3) + 2 * (col & 7)) =
-                  pack_h2(u[4 * hh + 2], u[4 * hh + 3]);
+          for (int j = 0; j < 2; ++j) {
+            if (st_row) {
+              *reinterpret_cast<uint4*>(row + ((j ^ (i & 7)) << 4)) = pack8_h(u0 + 8 * j);
+              *reinterpret_cast<uint4*>(row + (((2 + j) ^ (i & 7)) << 4)) = pack8_h(u1 + 8 * j);
             }
           }
-          float zz[4];
-          tmem_ld_16x256b(ua + 64, zz);
+          tmem_ld16(ua + 32, u0);
+          tmem_ld16(ua + 48, u1);
           tmem_wait_ld();
-          if ((lane & 3) == 0) {
-            sZ[kD * g + m0] = zz[0];
-            sZ[kD * g + m1] = zz[2];
+          reg_fence16(u0);
+          reg_fence16(u1);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (st_row) {
+              *reinterpret_cast<uint4*>(row + (((4 + j) ^ (i & 7)) << 4)) = pack8_h(u0 + 8 * j);
+              *reinterpret_cast<uint4*>(row + (((6 + j) ^ (i & 7)) << 4)) = pack8_h(u1 + 8 * j);
+            }
           }
         }
-        fence_async_smem();
-        good = bar_and(2 + g, 128, good);
         if (good && row_ok) {
+          // sigma_i phi(q_i), in place: the A operand of the state product
           const float sg = f[2 * kRows + tok];
           const float2 sg2 = make_float2(sg, sg);
           uint8_t* qt = Qt(s, g);
-          const float* z = sZ + kD * g;
-          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             uint4* a = reinterpret_cast<uint4*>(qt + sw128_offset(i, j));
             float x8[8];
             unpack8_h(*a, x8);
-            const float4 z0 = *reinterpret_cast<const float4*>(z + 8 * j);
-            const float4 z1 = *reinterpret_cast<const float4*>(z + 8 * j + 4);
-            acc = fma2(make_float2(x8[0], x8[1]), make_float2(z0.x, z0.y), acc);
-            acc = fma2(make_float2(x8[2], x8[3]), make_float2(z0.z, z0.w), acc);
-            acc = fma2(make_float2(x8[4], x8[5]), make_float2(z1.x, z1.y), acc);
-            acc = fma2(make_float2(x8[6], x8[7]), make_float2(z1.z, z1.w), acc);
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
               const float2 y = mul2(make_float2(x8[e], x8[e + 1]), sg2);
@@ -737,19 +761,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             *a = pack8_h(x8);
           }
-          dstate = sg * (acc.x + acc.y);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_PR]);
-      // ---- y = O[0:64] / (O[64] + state normaliser).  Each warp stages its 32
-      //      rows, 32 columns at a time, with a 128-byte swizzle in its own
-      //      4 KB of this chunk's Q tile (spent once O is done) and writes them
-      //      with a TMA store, which drops the rows past L.
-      if (!waitb(B_O, n & 1)) good = false;
+      if (lane == 0) mbar_arrive(&bars[B_PR0 + g]);
+      // ---- y = O[0:64] / O[64].  Each warp stages its 32 rows, 32 columns at
+      //      a time, with a 128-byte swizzle in its own 4 KB of this chunk's
+      //      Q tile (spent once O is done) and writes them with a TMA store,
+      //      which drops the rows past L.
+      if (!waitb(B_O0 + g, n & 1)) good = false;
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
       if (good && warp_ok) {
@@ -761,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence16(ob0);
         reg_fence16(ob1);
-        const float inv = 1.f / (ob1[0] + dstate);
+        const float inv = 1.f / ob1[0];
         const float2 inv2 = make_float2(inv, inv);
         uint8_t* row = stg + lane * 128;
 #pragma unroll 1
@@ -803,10 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars[B_ED]);
+        mbar_arrive(&bars[B_ED0 + g]);
         mbar_arrive(&bars[B_QE0 + s]);
       }
-      // leave together: the group's named barrier needs all four warps
+      // leave together (the group's warps vote)
       if (!bar_and(2 + g, 128, good)) break;
     }
     if (lane == 0) bulk_wait_all();
