@@ -36,46 +36,38 @@ L2_FLUSH_BYTES = 256 << 20      # > 129 MB L2
 HIRES_CHUNK = 64                # chunk of the long-sequence tensor-core path
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
-# kernel, per unit (head) from one ncu capture, keyed by the SHA-256 of the
+# kernel, per unit (head) from one ncu capture, keyed by the SHA-256 of that
 # kernel's sources at the time of the capture.  A key that no longer matches
 # the sources reports null: the counters describe another kernel.
-_TC_SOURCES = ("bidirectional_masked_linear_gb300/csrc/lion_tc.cu",
-               "bidirectional_masked_linear_gb300/csrc/tc_ptx.cuh")
+_CSRC = "bidirectional_masked_linear_gb300/csrc/"
+_TC_SOURCES = {
+    64: (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
+    128: (_CSRC + "lion_c128.cu", _CSRC + "tc_ptx.cuh"),
+}
 TRAFFIC_PER_HEAD = {
     # chunk-64 kernel, ViT-B shape at B=128, LION-S: 160.7 MB / 1536 heads
     ("fc4be66a869d6463b1ad06b8b0948a689343c3e6648cdb380430aac91fcace8c", "vit_b", "s", 64):
         (117664768 + 43027200) / 1536,
+    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 153.8 MB / 1536 heads
+    ("e8503bab7d22f45ec730ad5fddb39ae391f7583be09cb0ed15a406c6a0e827a1", "vit_b", "s", 128):
+        (117490944 + 36334336) / 1536,
 }
 
 
-def _sources_sha():
+def _sources_sha(chunk):
     import hashlib
     h = hashlib.sha256()
-    for rel in _TC_SOURCES:
+    for rel in _TC_SOURCES.get(chunk, ()):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
 def traffic_bytes(w, mask, chunk):
-    per_head = TRAFFIC_PER_HEAD.get((_sources_sha(), w.name, mask, chunk))
+    if chunk not in _TC_SOURCES:
+        return None
+    per_head = TRAFFIC_PER_HEAD.get((_sources_sha(chunk), w.name, mask, chunk))
     return None if per_head is None else per_head * w.B * w.H
-
-
-def _peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
-        try:
-            with open(path) as f:
-                d = json.load(f)
-            hbm = next((float(v) for k, v in d.items() if "hbm" in k.lower() and
-                        isinstance(v, (int, float))), None)
-            bf16 = d.get("bf16_tflops")
-            if hbm:
-                return hbm, float(bf16) if bf16 else FALLBACK_BF16_TFLOPS, "measured"
-        except (OSError, ValueError):
-            pass
-    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def algorithmic_bytes(w, mask: str) -> int:

@@ -311,15 +311,20 @@ __device__ __forceinline__ void mask_block(float* sv, int j0, int i, int row_lo,
       sv[4 * v + 3] = p1.y;
     }
   } else {
+    const float2 a2 = make_float2(ai, ai), r2 = make_float2(ri, ri);
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       const float4 r4 = *reinterpret_cast<const float4*>(rho + j0 + 4 * v);
       const float4 a4 = *reinterpret_cast<const float4*>(alpha + j0 + 4 * v);
-      const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 4; e += 2) {
         const int j = j0 + 4 * v + e;
-        sv[4 * v + e] *= j <= i ? ai * rr[e] : ri * aa[e];
+        const float2 lo = mul2(a2, e == 0 ? make_float2(r4.x, r4.y) : make_float2(r4.z, r4.w));
+        const float2 up = mul2(r2, e == 0 ? make_float2(a4.x, a4.y) : make_float2(a4.z, a4.w));
+        const float2 fct = make_float2(j <= i ? lo.x : up.x, j + 1 <= i ? lo.y : up.y);
+        const float2 pv = mul2(make_float2(sv[4 * v + e], sv[4 * v + e + 1]), fct);
+        sv[4 * v + e] = pv.x;
+        sv[4 * v + e + 1] = pv.y;
       }
     }
   }
