@@ -70,6 +70,22 @@ def traffic_bytes(w, mask, chunk):
     return None if per_head is None else per_head * w.B * w.H
 
 
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            hbm = next((float(v) for k, v in d.items() if "hbm" in k.lower() and
+                        isinstance(v, (int, float))), None)
+            bf16 = d.get("bf16_tflops")
+            if hbm:
+                return hbm, float(bf16) if bf16 else FALLBACK_BF16_TFLOPS, "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def algorithmic_bytes(w, mask: str) -> int:
     """Bytes the operator must move per call: q, k, v read once, y (fp32)
     written once, plus the decays (per token for LION-S, per head for D)."""

@@ -1,0 +1,37 @@
+"""CPU checks of bench.py's bookkeeping: peaks, algorithmic bytes, traffic
+lookup and launch counts (no GPU, no timing)."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from bidirectional_masked_linear_gb300 import synth  # noqa: E402
+
+
+def test_peaks_fall_back_without_measurements():
+    hbm, bf16, src = bench._peaks()
+    assert hbm > 0 and bf16 > 0 and src in ("measured", "fallback")
+
+
+def test_algorithmic_bytes_vit_b():
+    w = synth.WORKLOADS["vit_b"]
+    # 3 bf16 inputs + fp32 output per (token, head, feature), plus the LION-S decays
+    assert bench.algorithmic_bytes(w, "s") == w.B * w.H * w.L * (644)
+    assert bench.algorithmic_bytes(w, "lit") == w.B * w.H * w.L * 640
+
+
+def test_traffic_is_null_for_unknown_kernels():
+    w = synth.WORKLOADS["vit_b"]
+    assert bench.traffic_bytes(w, "s", 32) is None
+    t = bench.traffic_bytes(w, "s", 128)
+    assert t is None or t > 0
+
+
+def test_launch_counts():
+    vit = synth.WORKLOADS["vit_b"]
+    hires = synth.WORKLOADS["hires_2496"]
+    assert bench.kernels_per_call("chunk", 128, vit) == 1
+    assert bench.kernels_per_call("chunk", 64, vit) == 1
+    assert bench.kernels_per_call("chunk", 64, hires) == 3
