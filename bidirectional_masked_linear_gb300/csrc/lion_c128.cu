@@ -826,12 +826,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_fence16(ob0);
           }
         }
-        if (lane == 0) bulk_wait_read();
       }
+      // O_c is read: the next head's state MMA may use these TMEM columns
+      // while the second store is still reading the staging
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[B_ED0 + g]);
+        bulk_wait_read();
         mbar_arrive(&bars[B_QE0 + s]);
       }
       // leave together (the group's warps vote)
