@@ -918,25 +918,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Chains segment summaries into the states entering each segment:
 //   F_in(s+1) = exp(T_seg(s)) F_in(s) + U^F_seg(s),            F_in(0) = 0
 //   G_in(s-1) = exp(P_{s_seg(s+1)} - P_{s_seg(s)}) G_in(s) + U^B_seg(s), G_in(last) = 0
+// One thread per (head, state element, direction); the summaries it reads do
+// not depend on the running state, so their loads go out ahead of the chain.
+constexpr int kScanThreads = 128;
 template <int MASK>
-__global__ void __launch_bounds__(256) lion_segment_scan_kernel(TcParams prm, float* segin) {
-  const int bh = blockIdx.x, h = bh % prm.H;
+__global__ void __launch_bounds__(kScanThreads) lion_segment_scan_kernel(TcParams prm, float* segin) {
+  const int bh = blockIdx.y, h = bh % prm.H;
+  const int x = blockIdx.x * kScanThreads + threadIdx.x;     // [0, 2 * kD * kStateCols)
+  if (x >= 2 * kD * kStateCols) return;
+  const bool fwd = x < kD * kStateCols;
+  const int e = fwd ? x : x - kD * kStateCols;
   const float lh = MASK == MASK_D ? prm.log_lambda[h] : 0.f;
   const int segtok = prm.SEGB * kBlock;
-  for (int e = threadIdx.x; e < kD * kStateCols; e += blockDim.x) {
-    float F = 0.f;
-    for (int s = 0; s < prm.nseg; ++s) {
-      const float* ss = prm.segsum + ((size_t)bh * prm.nseg + s) * kSegSumFloats;
-      segin[((size_t)bh * prm.nseg + s) * kSegInFloats + e] = F;
-      F = __expf(ss[2 * kD * kStateCols]) * F + ss[e];
+  const size_t base = (size_t)bh * prm.nseg;
+  float st = 0.f;
+  if (fwd) {
+#pragma unroll 4
+    for (int sg = 0; sg < prm.nseg; ++sg) {
+      const float* ss = prm.segsum + (base + sg) * kSegSumFloats;
+      const float t = __ldg(ss + 2 * kD * kStateCols), u = __ldg(ss + e);
+      segin[(base + sg) * kSegInFloats + e] = st;
+      st = __expf(t) * st + u;
     }
-    float G = 0.f;
-    for (int s = prm.nseg - 1; s >= 0; --s) {
-      const float* ss = prm.segsum + ((size_t)bh * prm.nseg + s) * kSegSumFloats;
-      segin[((size_t)bh * prm.nseg + s) * kSegInFloats + kD * kStateCols + e] = G;
-      const float lfirst = ell_at<MASK>(prm, bh, s * segtok, lh);
-      const float lnext = ell_at<MASK>(prm, bh, (s + 1) * segtok, lh);
-      G = __expf(ss[2 * kD * kStateCols] - lfirst + lnext) * G + ss[kD * kStateCols + e];
+  } else {
+#pragma unroll 4
+    for (int sg = prm.nseg - 1; sg >= 0; --sg) {
+      const float* ss = prm.segsum + (base + sg) * kSegSumFloats;
+      const float t = __ldg(ss + 2 * kD * kStateCols), u = __ldg(ss + kD * kStateCols + e);
+      const float lfirst = ell_at<MASK>(prm, bh, sg * segtok, lh);
+      const float lnext = ell_at<MASK>(prm, bh, (sg + 1) * segtok, lh);
+      segin[(base + sg) * kSegInFloats + kD * kStateCols + e] = st;
+      st = __expf(t - lfirst + lnext) * st + u;
     }
   }
 }
@@ -1089,9 +1101,10 @@ cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_
     prm.segin = segin;
     cudaError_t e = launch_mode<MODE_PRE>(p, mq, mk, mv, prm, grid, s);
     if (e != cudaSuccess) return e;
-    if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<BH, 256, 0, s>>>(prm, segin);
-    else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<BH, 256, 0, s>>>(prm, segin);
-    else lion_segment_scan_kernel<MASK_S><<<BH, 256, 0, s>>>(prm, segin);
+    const dim3 sgrid((2 * kD * kStateCols + kScanThreads - 1) / kScanThreads, BH);
+    if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
+    else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
+    else lion_segment_scan_kernel<MASK_S><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
