@@ -33,40 +33,49 @@ from bidirectional_masked_linear_gb300 import lion, synth  # noqa: E402
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20      # > 129 MB L2
-HIRES_CHUNK = 64                # chunk of the long-sequence tensor-core path
+HIRES_CHUNK = 128               # chunk of the long-sequence tensor-core path
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
 # kernel, per unit (head) from one ncu capture, keyed by the SHA-256 of that
 # kernel's sources at the time of the capture.  A key that no longer matches
-# the sources reports null: the counters describe another kernel.
+# the sources reports null: the counters describe another kernel.  Keys are
+# (chunk, sequence longer than 256 tokens): the long chunk-128 path has its
+# own main pass.
 _CSRC = "bidirectional_masked_linear_gb300/csrc/"
 _TC_SOURCES = {
-    64: (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
-    128: (_CSRC + "lion_c128.cu", _CSRC + "tc_ptx.cuh"),
+    (64, False): (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
+    (64, True): (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
+    (128, False): (_CSRC + "lion_c128.cu", _CSRC + "c128_common.cuh", _CSRC + "tc_ptx.cuh"),
+    (128, True): (_CSRC + "lion_c128L.cu", _CSRC + "c128_common.cuh", _CSRC + "tc_ptx.cuh"),
 }
 TRAFFIC_PER_HEAD = {
     # chunk-64 kernel, ViT-B shape at B=128, LION-S: 160.7 MB / 1536 heads
     ("fc4be66a869d6463b1ad06b8b0948a689343c3e6648cdb380430aac91fcace8c", "vit_b", "s", 64):
         (117664768 + 43027200) / 1536,
-    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 153.8 MB / 1536 heads
-    ("e8503bab7d22f45ec730ad5fddb39ae391f7583be09cb0ed15a406c6a0e827a1", "vit_b", "s", 128):
-        (117490944 + 36334336) / 1536,
+    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 154.5 MB / 1536 heads
+    ("6693686b17732376e16c6633cd5a38da8782169cbf771b1894f7f78eaa7b640c", "vit_b", "s", 128):
+        (117491712 + 37051648) / 1536,
+    # chunk-128 main pass for long sequences, L=24337 (B=2, H=12), LION-S:
+    # 387.8 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
+    ("81c6b55ae02d78fac6e46083f9ea1ef872d35a3a898b5c1c394ec238906b64d0", "hires_2496", "s", 128):
+        (271664896 + 116118528) / 24,
 }
 
 
-def _sources_sha(chunk):
+def _sources_sha(key):
     import hashlib
     h = hashlib.sha256()
-    for rel in _TC_SOURCES.get(chunk, ()):
+    for rel in _TC_SOURCES.get(key, ()):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
 def traffic_bytes(w, mask, chunk):
-    if chunk not in _TC_SOURCES:
+    key = (chunk, w.L > 256)
+    if key not in _TC_SOURCES:
         return None
-    per_head = TRAFFIC_PER_HEAD.get((_sources_sha(chunk), w.name, mask, chunk))
+    per_head = TRAFFIC_PER_HEAD.get((_sources_sha(key), w.name, mask, chunk))
     return None if per_head is None else per_head * w.B * w.H
 
 
@@ -100,10 +109,10 @@ def algorithmic_bytes(w, mask: str) -> int:
 
 
 def kernels_per_call(form: str, chunk: int, w) -> int:
-    """Kernel launches one operator call makes: the tensor-core chunk path
-    (bf16, d=64, chunk 64) takes one launch up to 256 tokens and three
+    """Kernel launches one operator call makes: the tensor-core chunk paths
+    (bf16, d=64, chunk 64 or 128) take one launch up to 256 tokens and three
     (pre-pass, segment scan, main pass) beyond; every other path one."""
-    tc = form == "chunk" and chunk == 64 and w.d == 64 and w.dtype == "bf16"
+    tc = form == "chunk" and chunk in (64, 128) and w.d == 64 and w.dtype == "bf16"
     return 3 if tc and w.L > 256 else 1
 
 

@@ -92,6 +92,10 @@ size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk
     const size_t tc = lion::chunk_tc_workspace_bytes(B, H, L);
     if (tc > need) need = tc;
   }
+  if (form == LION_FORM_CHUNK && d == 64 && chunk == 128 && L > 256) {
+    const size_t tc = lion::chunk128_long_workspace_bytes(B, H, L);
+    if (tc > need) need = tc;
+  }
   return need;
 }
 
@@ -115,17 +119,19 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
   cudaStream_t s = a->stream;
 
   const bool use_tc128 = a->form == LION_FORM_CHUNK && lion::chunk128_tc_supported(p);
-  const bool use_tc = !use_tc128 && a->form == LION_FORM_CHUNK && lion::chunk_tc_supported(p);
-  if (a->form == LION_FORM_CHUNK && !use_tc && !use_tc128 && a->chunk > lion::kSimtMaxChunk)
+  const bool use_tc128l = a->form == LION_FORM_CHUNK && lion::chunk128_long_supported(p);
+  const bool use_tc = !use_tc128 && !use_tc128l && a->form == LION_FORM_CHUNK && lion::chunk_tc_supported(p);
+  if (a->form == LION_FORM_CHUNK && !use_tc && !use_tc128 && !use_tc128l && a->chunk > lion::kSimtMaxChunk)
     return LION_ERR_UNSUPPORTED;
   int* dstatus = nullptr;
-  if (use_tc || use_tc128) {
+  if (use_tc || use_tc128 || use_tc128l) {
     dstatus = lion::device_status_ptr();
     if (!dstatus) return LION_ERR_CUDA;
   }
-  const size_t need = use_tc128 ? 0
-                      : use_tc   ? lion::chunk_tc_workspace_bytes(a->B, a->H, a->L)
-                                 : simt_workspace_bytes(a->B, a->H, a->L, a->form);
+  const size_t need = use_tc128   ? 0
+                      : use_tc128l ? lion::chunk128_long_workspace_bytes(a->B, a->H, a->L)
+                      : use_tc     ? lion::chunk_tc_workspace_bytes(a->B, a->H, a->L)
+                                   : simt_workspace_bytes(a->B, a->H, a->L, a->form);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
@@ -142,9 +148,10 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
     case LION_FORM_CHUNK:
-      e = use_tc128 ? lion::launch_chunk128_tc(p, dstatus, s)
-          : use_tc  ? lion::launch_chunk_tc(p, ws, dstatus, s)
-                    : lion::launch_chunk_simt(p, (float*)ws, s);
+      e = use_tc128    ? lion::launch_chunk128_tc(p, dstatus, s)
+          : use_tc128l ? lion::launch_chunk128_long(p, ws, dstatus, s)
+          : use_tc     ? lion::launch_chunk_tc(p, ws, dstatus, s)
+                       : lion::launch_chunk_simt(p, (float*)ws, s);
       break;
   }
   if (owned) {

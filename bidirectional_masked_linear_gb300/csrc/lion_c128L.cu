@@ -1,0 +1,785 @@
+// lion_c128L.cu -- main pass of the chunkwise LION forward with 128-token
+// chunks for sequences longer than 256 tokens, on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA), bfloat16 inputs, head dim 64.
+//
+// Chunkwise form ("LION Part IV - Results", "LION Chunk"; rebuttal page
+// "LION: A bidirectional framework ...", reply "4: Practicality of Recurrent
+// Inference").  With P the inclusive prefix of l = log(lambda), chunk c =
+// tokens [s_c, e_c] and p the chunk-local prefix, row i of chunk c is
+//
+//   y_i = (O_i + a_i T_i + b_i R_i)[0:64] / (O_i + a_i T_i + b_i R_i)[64]
+//   O_i = sum_{j in c} M_ij s_ij [v_j; 1]               (intra-chunk)
+//   T_i = phi(q_i) F_c,  a_i = exp(P_i - P_{e_{c-1}}) = exp(p_i)
+//   R_i = phi(q_i) G_c,  b_i = exp(P_{s_{c+1}} - P_i)
+//
+// F_c is the forward state entering chunk c from the left (anchored at
+// e_{c-1}) and G_c the backward state entering it from the right (anchored
+// at s_{c+1}), both [phi(k) (x) [v; 1]] sums weighted by the decay.
+//
+// The sequence is cut into segments of 256-token blocks.  A pre-pass (the
+// chunk-64 kernel's, run right to left over each segment) and a segment scan
+// provide, per block, the backward state at its end and at its token 128, and
+// per segment the states entering it from both sides.  This pass walks one
+// segment left to right, one chunk at a time:
+//   F_c     carried in TMEM (fp32, transposed: lane = output column, lane 64
+//           = z), starting from the segment's entering state, and advanced
+//           after every chunk: F_{c+1} = exp(T_c) F_c + U_c with
+//           U_c^T = [V_c | 1]^T (w_c o phi(K_c)), w_j = exp(p_e - p_j);
+//   G_c     the pre-pass state at the chunk's right edge plus the segment's
+//           entering backward state decayed to it;
+// both written each chunk as K-major fp16 operand tiles of 80 rows (row 64 =
+// z).  MMAs per chunk (n = columns with tokens, rounded up to 16):
+//   S   = phi(Q) phi(K)^T            M=128 N=n  K=64
+//   U^T = [V | 1]^T (w o phi(K))     M=128 N=64 K=n
+//   T   = phi(Q) X_F,  R = phi(Q) X_G  M=128 N=80 K=64
+//   O   = P [V | 1]                  M=128 N=80 K=n  (A operand P in TMEM)
+// with the decay mask applied to S on the CUDA cores as in lion_c128.cu.
+//
+// Warps: 0 TMA (Q, K, V and the pre-pass state of a chunk into one of two
+// slots; the segment's entering backward state), 1 MMA issue, 2-17 "prep"
+// (four threads per token: prefix, V -> fp16, phi(k) and its weighted copy,
+// phi(q), factors), 18-25 "epi" (two warps per TMEM lane quarter, each one
+// column half: state tiles, carried state, mask, output through TMA).
+// Prep of chunk c+1 overlaps the epilogue of chunk c.
+//
+// TMEM (512 columns): S [0,128) (P in columns 0-31 and 64-95), O [128,208),
+// T [208,288), R [288,368), F^T [368,432), U^T [432,496).
+//
+// Precision as lion_c128.cu: fp16 operands, fp32 accumulation, the states
+// rounded once to fp16 per use.  Every mbarrier wait is bounded; on timeout
+// the kernel records an error in `status`, waits (bounded) for its own copies
+// and MMAs in flight, releases its TMEM and returns.
+#include "c128_common.cuh"
+#include "lion_common.cuh"
+#include "lion_internal.h"
+#include "tc_ptx.cuh"
+
+namespace lion {
+namespace {
+
+using namespace tc;
+using namespace c128;
+
+constexpr int kStRows = 80;                 // state tile rows: 64 columns, z, 15 zero rows
+constexpr int kStTile = kStRows * 128;
+constexpr int kPrepWarps = 16, kEpiWarps = 8;
+constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
+constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
+constexpr long long kWaitCycles = 2000000000LL;       // ~1 s at 2 GHz
+constexpr uint32_t kSleepNs = 2000u;
+constexpr int kGsegBytes = 64 * kLongStateCols * 4;  // one fp32 [64][80] state
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr int kSlotG = 9 * 1024;                      // pre-pass state (kGlocBytes) of a chunk
+constexpr int kSlotBytes = 3 * kTile + kSlotG;        // Q, K, V, pre-pass state
+constexpr int OFF_SLOT = 0;                           // [2] slots
+constexpr int OFF_KW = OFF_SLOT + 2 * kSlotBytes;     // weighted phi(K)
+constexpr int OFF_XF = OFF_KW + kTile;                // X_F operand tile
+constexpr int OFF_XG = OFF_XF + kStTile;              // X_G operand tile
+constexpr int OFF_ONES = OFF_XG + kStTile;            // 16 rows, column 0 = 1
+constexpr int OFF_GSEG = OFF_ONES + 2048;             // the segment's entering backward state (fp32 [64][80])
+constexpr int OFF_FAC = OFF_GSEG + kGsegBytes;        // [slot] alpha, rho, a, b, p [128] each
+constexpr int OFF_INFO = OFF_FAC + 2 * 5 * kC * 4;    // [slot] float[8] per-chunk scalars
+constexpr int OFF_RED = OFF_INFO + 2 * 8 * 4;         // [parity] float[32] prep scan scratch
+constexpr int OFF_BAR = OFF_RED + 2 * 32 * 4;
+constexpr int kNumBars = 24;
+constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
+constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;     // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kSlotBytes % 1024 == 0 && OFF_KW % 1024 == 0 && OFF_XF % 1024 == 0 && OFF_XG % 1024 == 0 &&
+                  OFF_ONES % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
+static_assert(kGlocBytes <= kSlotG && kGlocBytes % 16 == 0 && kGsegBytes % 16 == 0, "bulk copies");
+
+// per-chunk scalars (INFO)
+enum { I_EXACT = 0, I_T = 1, I_LNEXT = 2 };
+
+// mbarriers
+enum {
+  B_LD0 = 0,     // + slot: Q, K, V, pre-pass state landed (TMA, tx bytes)
+  B_GS = 2,      // segment's entering backward state landed (tx bytes)
+  B_KVR = 3,     // prep: V, phi(K), weighted phi(K) written (16 arrivals)
+  B_QR = 4,      // prep: phi(Q), factors written (16 arrivals)
+  B_S = 5,       // MMA commit: S done
+  B_U = 6,       // MMA commit: U^T done
+  B_PVD = 7,     // MMA commit: P [V | 1] done (S's columns free)
+  B_O = 8,       // MMA commit: O, T, R done
+  B_KE0 = 9,     // + slot: MMA commit: K tile of the slot read
+  B_KWE = 11,    // MMA commit: weighted phi(K) read
+  B_XF = 12,     // epi: X_F written (8 arrivals)
+  B_XG = 13,     // epi: X_G written (8 arrivals)
+  B_CU = 14,     // epi: carried state advanced, U^T read (8 arrivals)
+  B_PM = 15,     // epi: P written (8 arrivals)
+  B_ED = 16,     // epi: O, T, R read (8 arrivals)
+  B_QVE0 = 17,   // + slot: epi: output stores have read the slot's Q and V tiles (8 arrivals)
+  B_DRAIN = 19,  // MMA commit used when unwinding
+  B_GF = 20,     // epi: the item's last X_G written, the segment state may be replaced (8 arrivals)
+};
+__device__ __forceinline__ uint32_t bar_count(int b) {
+  if (b == B_KVR || b == B_QR) return kPrepWarps;
+  if ((b >= B_XF && b <= B_QVE0 + 1) || b == B_GF) return kEpiWarps;
+  return 1;
+}
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t T_S = 0, T_O = 128, T_T = 208, T_R = 288, T_F = 368, T_U = 432;
+// P (fp16, two per column) over S: each of the two epi warps of a lane
+// quarter packs its own half of the keys into the start of its own half of
+// S's columns, so neither overwrites columns the other has still to read
+// (keys 16j..16j+15 at columns 8j, or 32 + 8j for the second half).
+__host__ __device__ constexpr uint32_t p_col(int j) { return 8u * j + (j >= 4 ? 32u : 0u); }
+
+struct LongParams {
+  const float* log_lambda;
+  int BH, H, L;
+  int NBL, SEGB, nseg;
+  const uint8_t* gloc;
+  const uint8_t* gmid;
+  const float* segsum;
+  const float* segin;
+  int* status;
+};
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int MASK>
+__device__ __forceinline__ float ell_at(const LongParams& p, int bh, int t, float lh) {
+  if (t >= p.L || t < 0) return 0.f;
+  if (MASK == MASK_S) return __ldg(p.log_lambda + (size_t)bh * p.L + t);
+  if (MASK == MASK_D) return lh;
+  return 0.f;
+}
+
+// The per-CTA sequence of steps: work items (segments of heads) blockIdx.x,
+// + gridDim.x, ...; the 128-token chunks of each item left to right.
+struct Step {
+  int item, c, c_lo, c_hi;   // chunk c of [c_lo, c_hi)
+  __device__ void set_item(const LongParams& p, int it) {
+    item = it;
+    const int nch = (p.L + kC - 1) / kC;
+    const int seg = it % p.nseg;
+    c_lo = 2 * seg * p.SEGB;
+    c_hi = min(nch, 2 * (seg + 1) * p.SEGB);
+    c = c_lo;
+  }
+  __device__ bool valid(const LongParams& p) const { return item < p.BH * p.nseg; }
+  __device__ void next(const LongParams& p) {
+    if (++c == c_hi) {
+      item += gridDim.x;
+      if (valid(p)) set_item(p, item);
+    }
+  }
+};
+
+template <int MASK, int PHI>
+__global__ void __launch_bounds__(kThreads, 1)
+    lion_chunk128_long_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                              const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
+                              LongParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 8);
+  auto Qt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes; };
+  auto Kt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes + kTile; };
+  auto Vt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes + 2 * kTile; };
+  auto Gt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes + 3 * kTile; };
+  uint8_t* KWt = smem + OFF_KW;
+  uint8_t* XFt = smem + OFF_XF;
+  uint8_t* XGt = smem + OFF_XG;
+  const float* gseg = reinterpret_cast<const float*>(smem + OFF_GSEG);
+  auto fac = [&](int s) { return reinterpret_cast<float*>(smem + OFF_FAC) + s * 5 * kC; };
+  auto info = [&](int s) { return reinterpret_cast<float*>(smem + OFF_INFO) + s * 8; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = prm.L;
+
+  if (tid == 0) {
+    prefetch_tmap(&mapQ);
+    prefetch_tmap(&mapK);
+    prefetch_tmap(&mapV);
+    prefetch_tmap(&mapO);
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b));
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  for (int x = tid; x < 16 * 8; x += kThreads) {
+    const int r = x >> 3, c8 = x & 7;
+    *reinterpret_cast<uint4*>(smem + OFF_ONES + sw128_offset(r, c8)) =
+        make_uint4(c8 == 0 ? pack_h2(1.f, 0.f) : 0u, 0u, 0u, 0u);
+  }
+  // rows 65..79 of the state tiles stay zero
+  for (int x = tid; x < 2 * 15 * 8; x += kThreads) {
+    uint8_t* t = x < 15 * 8 ? XFt : XGt;
+    const int y = x % (15 * 8), r = 65 + y / 8, c8 = y % 8;
+    *reinterpret_cast<uint4*>(t + sw128_offset(r, c8)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (warp == W_TMA) tmem_alloc(tslot, kTmemCols);
+  fence_async_smem();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  auto waitb = [&](int b, uint32_t parity) -> bool {
+    if (*s_abort) return false;
+    if (mbar_try_wait(&bars[b], parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_sleep(&bars[b], parity, kSleepNs)) {
+      if (*s_abort) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        *s_abort = 1;
+        return false;
+      }
+    }
+    return true;
+  };
+  auto nk_of = [&](int c) { return (min(kC, L - kC * c) + 15) >> 4; };
+  // pre-pass state at the right edge of chunk c
+  auto gsrc = [&](int bh, int c) {
+    const int b = c >> 1;
+    const bool mid = (c & 1) == 0 && L - 256 * b > kC;
+    return (mid ? prm.gmid : prm.gloc) + ((size_t)bh * prm.NBL + b) * kGlocBytes;
+  };
+
+  if (warp == W_TMA) {
+    // =========================== TMA producer ===================================
+    // Step n's Q, K, V and pre-pass state go into slot n & 1 once step n-2's
+    // MMAs have read K and its output stores Q and V; the segment's entering
+    // backward state once the previous item's last state tile is written
+    // (a barrier that completes once per item, so that its phases cannot be
+    // confused while polling).
+    if (lane == 0) {
+      Step ld, gs;
+      ld.item = gs.item = blockIdx.x;
+      if (ld.valid(prm)) {
+        ld.set_item(prm, ld.item);
+        gs.set_item(prm, gs.item);
+      }
+      int n = 0, ng = 0;   // steps issued; segment states issued
+      int issued_ld[2] = {0, 0};
+      long long idle0 = clock64();
+      while ((ld.valid(prm) || gs.valid(prm)) && !*s_abort) {
+        bool progress = false;
+        if (gs.valid(prm) && (ng == 0 || mbar_try_wait(&bars[B_GF], (ng - 1) & 1))) {
+          mbar_arrive_expect_tx(&bars[B_GS], (uint32_t)kGsegBytes);
+          bulk_load(smem + OFF_GSEG, prm.segin + (size_t)gs.item * kSegInFloats + 64 * kLongStateCols,
+                    (uint32_t)kGsegBytes, &bars[B_GS]);
+          ++ng;
+          gs.item += gridDim.x;
+          if (gs.valid(prm)) gs.set_item(prm, gs.item);
+          progress = true;
+        }
+        const int s = n & 1;
+        if (ld.valid(prm) && (n < 2 || (mbar_try_wait(&bars[B_KE0 + s], ((n >> 1) - 1) & 1) &&
+                                        mbar_try_wait(&bars[B_QVE0 + s], ((n >> 1) - 1) & 1)))) {
+          const int bh = ld.item / prm.nseg;
+          mbar_arrive_expect_tx(&bars[B_LD0 + s], (uint32_t)(3 * kTile + kGlocBytes));
+          tma_load_3d(Vt(s), &mapV, &bars[B_LD0 + s], 0, kC * ld.c, bh);
+          tma_load_3d(Kt(s), &mapK, &bars[B_LD0 + s], 0, kC * ld.c, bh);
+          tma_load_3d(Qt(s), &mapQ, &bars[B_LD0 + s], 0, kC * ld.c, bh);
+          bulk_load(Gt(s), gsrc(bh, ld.c), (uint32_t)kGlocBytes, &bars[B_LD0 + s]);
+          ++issued_ld[s];
+          ++n;
+          ld.next(prm);
+          progress = true;
+        }
+        if (progress) {
+          idle0 = clock64();
+        } else {
+          __nanosleep(64);
+          if (clock64() - idle0 > kWaitCycles) *s_abort = 1;
+        }
+      }
+      if (*s_abort) {
+        const long long lim = kWaitCycles / 4;
+        for (int s = 0; s < 2; ++s)
+          if (issued_ld[s]) mbar_wait(&bars[B_LD0 + s], (issued_ld[s] - 1) & 1, lim);
+        if (ng) mbar_wait(&bars[B_GS], (ng - 1) & 1, lim);
+      }
+    }
+  } else if (warp == W_MMA) {
+    // =========================== MMA issuer =====================================
+    if (lane == 0) {
+      const uint32_t idUT = idesc_f16(128, 64, true, true);
+      const uint32_t idPV = idesc_f16(128, 80, false, true);
+      const uint32_t idX = idesc_f16(128, 80, false, false);
+      const uint32_t ones = smem_u32(smem + OFF_ONES);
+      bool issued = false;
+      Step st;
+      st.item = blockIdx.x;
+      if (st.valid(prm)) st.set_item(prm, st.item);
+      for (int n = 0; st.valid(prm); ++n, st.next(prm)) {
+        const int s = n & 1, nk = nk_of(st.c);
+        if (!waitb(B_KVR, n & 1) || !waitb(B_QR, n & 1)) break;
+        if (n >= 1 && !waitb(B_PVD, (n - 1) & 1)) break;   // S's columns: P of the previous chunk read
+        tc_fence_after();
+        const uint32_t idS = idesc_f16(128, 16 * nk, false, false);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_S, kmaj(Qt(s), k), kmaj(Kt(s), k), idS, k > 0 ? 1u : 0u);
+        mma_commit(&bars[B_S]);
+        issued = true;
+        if (n >= 1 && !waitb(B_CU, (n - 1) & 1)) break;    // U^T of the previous chunk read
+        tc_fence_after();
+        {
+          const uint32_t a = smem_u32(Vt(s));
+          const uint32_t b = smem_u32(MASK == MASK_LIT ? Kt(s) : KWt);
+          for (int k = 0; k < nk; ++k)
+            mma_bf16(tbase + T_U, mnmaj(a, k, ones - (a + 2048 * k)), mnmaj(b, k, 0), idUT, k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[B_U]);
+        mma_commit(&bars[B_KWE]);
+        mma_commit(&bars[B_KE0 + s]);
+        if (n >= 1 && !waitb(B_ED, (n - 1) & 1)) break;    // O, T, R of the previous chunk read
+        if (!waitb(B_XF, n & 1)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_T, kmaj(Qt(s), k), kmaj(XFt, k), idX, k > 0 ? 1u : 0u);
+        if (!waitb(B_XG, n & 1)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_R, kmaj(Qt(s), k), kmaj(XGt, k), idX, k > 0 ? 1u : 0u);
+        if (!waitb(B_PM, n & 1)) break;
+        tc_fence_after();
+        {
+          const uint32_t v = smem_u32(Vt(s));
+          for (int k = 0; k < nk; ++k)
+            mma_tmem_a(tbase + T_O, tbase + T_S + p_col(k), mnmaj(v, k, ones - (v + 2048 * k)), idPV,
+                       k > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars[B_PVD]);
+        mma_commit(&bars[B_O]);
+      }
+      if (*s_abort && issued) {
+        mma_commit(&bars[B_DRAIN]);
+        mbar_wait(&bars[B_DRAIN], 0, kWaitCycles / 4);
+      }
+    }
+  } else if (warp < W_EPI) {
+    // =========================== prep: four threads per token ====================
+    const int pw = warp - W_PREP;            // 0..15: tokens 8 pw .. 8 pw + 7
+    const int pt = 32 * pw + lane;
+    const int t = pt >> 2, qq = pt & 3;      // token within the chunk, quarter row
+    const int j0 = 2 * qq;                   // first 16-byte chunk of this quarter row
+    const uint32_t peers = 0xfu << (lane & 28);
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);
+    bool good = true;
+    Step st;
+    st.item = blockIdx.x;
+    if (st.valid(prm)) st.set_item(prm, st.item);
+    float ell_next = 0.f, lnext_next = 0.f;
+    auto load_ell = [&](const Step& x, float* e, float* en) {
+      const int bh = x.item / prm.nseg;
+      const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
+      *e = ell_at<MASK>(prm, bh, kC * x.c + t, lh);
+      *en = ell_at<MASK>(prm, bh, kC * x.c + kC, lh);   // first token after the chunk
+    };
+    if (st.valid(prm)) load_ell(st, &ell_next, &lnext_next);
+    for (int n = 0; st.valid(prm); ++n) {
+      const int s = n & 1, tok = kC * st.c + t;
+      const float ell = ell_next, lnext = lnext_next;
+      // ---- chunk-local inclusive prefix (each token's value sits in its four lanes)
+      float x = ell;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      float* rd = red + 32 * (n & 1);
+      if (lane == 31) rd[pw] = x;
+      if (pt == 0) rd[16] = ell;
+      good = bar_and(1, kPrepWarps * 32, good);
+      if (!good) break;
+      float pre = 0.f;
+      for (int w = 0; w < pw; ++w) pre += rd[w];
+      float T = 0.f;
+#pragma unroll
+      for (int w = 0; w < 16; ++w) T += rd[w];
+      const float p = x + pre;
+      const float pfirst = rd[16];
+      const float pref = 0.5f * (pfirst + T);
+      const bool exact = (pfirst - T) > 2.f * kMaxFactorRange;
+      const bool live = tok < L;
+
+      if (!waitb(B_LD0 + s, (n >> 1) & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      // ---- V -> fp16 in place
+      if (good && live) {
+        uint8_t* vt = Vt(s);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint4* a = reinterpret_cast<uint4*>(vt + sw128_offset(t, j0 + j));
+          *a = bf8_to_h8(*a);
+        }
+      }
+      // ---- phi(k) in place and its weighted copy w_j phi(k_j), w_j = exp(p_e - p_j)
+      if (good && live) {
+        uint8_t* kt = Kt(s);
+        float kv[16];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          unpack8_bf(*reinterpret_cast<const uint4*>(kt + sw128_offset(t, j0 + j)), kv + 8 * j);
+        phi_part<PHI, 16, 4>(kv, peers);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) *reinterpret_cast<uint4*>(kt + sw128_offset(t, j0 + j)) = pack8_h(kv + 8 * j);
+        if (MASK != MASK_LIT) {
+          if (n >= 1 && !waitb(B_KWE, (n - 1) & 1)) good = false;
+          if (good) {
+            const float w = ex2((T - p) * kLog2e);
+            const float2 w2 = make_float2(w, w);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              float y8[8];
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                const float2 u = mul2(make_float2(kv[8 * j + e], kv[8 * j + e + 1]), w2);
+                y8[e] = u.x;
+                y8[e + 1] = u.y;
+              }
+              *reinterpret_cast<uint4*>(KWt + sw128_offset(t, j0 + j)) = pack8_h(y8);
+            }
+          }
+        }
+      } else if (good && MASK != MASK_LIT) {
+        if (n >= 1 && !waitb(B_KWE, (n - 1) & 1)) good = false;
+        if (good) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<uint4*>(KWt + sw128_offset(t, j0 + j)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_KVR]);
+      // ---- factors and phi(q)
+      if (good && qq == 0) {
+        float* f = fac(s);
+        const float d = (p - pref) * kLog2e;
+        f[t] = ex2(d);
+        f[kC + t] = ex2(-d);
+        f[2 * kC + t] = ex2(p * kLog2e);                       // a_i
+        f[3 * kC + t] = ex2((T + lnext - p) * kLog2e);         // b_i
+        f[4 * kC + t] = p;
+        if (t == 0) {
+          float* in = info(s);
+          in[I_EXACT] = exact ? 1.f : 0.f;
+          in[I_T] = T;
+          in[I_LNEXT] = lnext;
+        }
+      }
+      if (good && live) {
+        uint8_t* qt = Qt(s);
+        float qv[16];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          unpack8_bf(*reinterpret_cast<const uint4*>(qt + sw128_offset(t, j0 + j)), qv + 8 * j);
+        phi_part<PHI, 16, 4>(qv, peers);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) *reinterpret_cast<uint4*>(qt + sw128_offset(t, j0 + j)) = pack8_h(qv + 8 * j);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_QR]);
+      st.next(prm);
+      if (st.valid(prm)) load_ell(st, &ell_next, &lnext_next);
+    }
+  } else {
+    // =========================== epi: two warps per TMEM lane quarter =============
+    const int ew = warp - W_EPI;
+    const int q = warp & 3;                  // TMEM lane quarter: rows 32q..32q+31
+    const int hc = ew >> 2;                  // column half
+    const int i = 32 * q + lane;             // row (and state-tile row)
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const bool st_row = i < kStRows;         // lanes holding a state-tile row
+    bool good = true;
+    Step st;
+    st.item = blockIdx.x;
+    if (st.valid(prm)) st.set_item(prm, st.item);
+    int ng = 0;                // items started
+    float cum = 0.f, tseg = 0.f, lafter = 0.f;
+    for (int n = 0; st.valid(prm); ++n) {
+      const int s = n & 1, c = st.c, nk = nk_of(c), bh = st.item / prm.nseg;
+      const int tok = kC * c + i;
+      const bool first = c == st.c_lo, row_ok = tok < L, warp_ok = kC * c + 32 * q < L;
+      const float* f = fac(s);
+      const float* alpha = f;
+      const float* rho = f + kC;
+      const float* pp = f + 4 * kC;
+      if (first) {
+        // a new segment: its forward entering state into the carried TMEM
+        // state, and the bookkeeping for its backward entering state
+        const int seg = st.item % prm.nseg;
+        const float* fin = prm.segin + (size_t)st.item * kSegInFloats;   // [64 m][80]
+        tseg = prm.segsum[(size_t)st.item * kSegSumFloats + 2 * 64 * kLongStateCols];
+        const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
+        lafter = ell_at<MASK>(prm, bh, 256 * min(prm.NBL, (seg + 1) * prm.SEGB), lh);
+        cum = 0.f;
+        if (q < 3) {
+          float v[16];
+#pragma unroll 1
+          for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = st_row ? __ldg(fin + (32 * hc + 16 * h2 + e) * kLongStateCols + i) : 0.f;
+            tmem_st16(tbase + lane_off + T_F + 32 * hc + 16 * h2, v);
+          }
+          tmem_wait_st();
+        }
+        ++ng;
+      }
+      // ---- X_F = the carried state, transposed, K-major fp16 (rows = output columns)
+      if (good && q < 3) {
+        float u0[16], u1[16];
+        const uint32_t fa = tbase + lane_off + T_F + 32 * hc;
+        tmem_ld16(fa, u0);
+        tmem_ld16(fa + 16, u1);
+        tmem_wait_ld();
+        reg_fence16(u0);
+        reg_fence16(u1);
+        if (st_row) {
+          uint8_t* row = XFt + i * 128;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            *reinterpret_cast<uint4*>(row + (((4 * hc + j) ^ (i & 7)) << 4)) = pack8_h(u0 + 8 * j);
+            *reinterpret_cast<uint4*>(row + (((4 * hc + 2 + j) ^ (i & 7)) << 4)) = pack8_h(u1 + 8 * j);
+          }
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_XF]);
+      // ---- advance the carried state: F <- exp(T_c) F + U^T (the U commit
+      //      also means prep's per-chunk scalars of this step are written)
+      if (!waitb(B_U, n & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      tc_fence_after();
+      if (good && q < 3) {
+        const float dec = MASK == MASK_LIT ? 1.f : __expf(info(s)[I_T]);
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float fv[16], uv[16];
+          const uint32_t off = lane_off + 32 * hc + 16 * h2;
+          tmem_ld16(tbase + off + T_F, fv);
+          tmem_ld16(tbase + off + T_U, uv);
+          tmem_wait_ld();
+          reg_fence16(fv);
+          reg_fence16(uv);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) fv[e] = fmaf(dec, fv[e], uv[e]);
+          tmem_st16(tbase + off + T_F, fv);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_CU]);
+      // ---- X_G = pre-pass state + decay * segment's backward entering state, transposed
+      if (!waitb(B_LD0 + s, (n >> 1) & 1)) good = false;
+      if (first && !waitb(B_GS, (ng - 1) & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      if (good && st_row) {
+        const float Tc = info(s)[I_T], lnext = info(s)[I_LNEXT];
+        // exp(P at the first token after the segment - P at the first token after chunk c)
+        const float fdec = __expf(tseg - (cum + Tc) - lnext + lafter);
+        const uint8_t* g = Gt(s);
+        uint8_t* row = XGt + i * 128;
+        if (i < 64) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float y8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int m = 32 * hc + 8 * j + e;
+              y8[e] = __half2float(reinterpret_cast<const __half*>(g)[m * 64 + i]) + fdec * gseg[m * kLongStateCols + i];
+            }
+            *reinterpret_cast<uint4*>(row + (((4 * hc + j) ^ (i & 7)) << 4)) = pack8_h(y8);
+          }
+        } else if (i == 64) {
+          const float* gz = reinterpret_cast<const float*>(g + 64 * 64 * 2);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float y8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int m = 32 * hc + 8 * j + e;
+              y8[e] = gz[m] + fdec * gseg[m * kLongStateCols + 64];
+            }
+            *reinterpret_cast<uint4*>(row + (((4 * hc + j) ^ (i & 7)) << 4)) = pack8_h(y8);
+          }
+        }
+      }
+      cum += info(s)[I_T];
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[B_XG]);
+        if (c + 1 == st.c_hi) mbar_arrive(&bars[B_GF]);   // done with this segment's state
+      }
+      // ---- P = S * M, fp16, into the first 64 columns of S (this warp's column half)
+      if (!waitb(B_S, n & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      tc_fence_after();
+      if (good && warp_ok && 4 * hc < nk) {
+        const bool exact = info(s)[I_EXACT] != 0.f;
+        const float ai = alpha[i], ri = rho[i], pi = pp[i];
+        const uint32_t sa = tbase + lane_off + T_S;
+        const int jend = min(nk, 4 * hc + 4);
+        float sb0[16], sb1[16];
+#pragma unroll 1
+        for (int jj = 4 * hc; jj < jend; jj += 2) {
+          uint32_t pk[8];
+          const bool has1 = jj + 1 < jend;
+          tmem_ld16(sa + 16 * jj, sb0);
+          if (has1) tmem_ld16(sa + 16 * (jj + 1), sb1);
+          tmem_wait_ld();
+          reg_fence16(sb0);
+          reg_fence16(sb1);
+          mask_block<MASK>(sb0, 16 * jj, i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb0[2 * e], sb0[2 * e + 1]);
+          tmem_st8(sa + p_col(jj), pk);
+          if (has1) {
+            mask_block<MASK>(sb1, 16 * (jj + 1), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb1[2 * e], sb1[2 * e + 1]);
+            tmem_st8(sa + p_col(jj + 1), pk);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_PM]);
+      // ---- y = (O + a T + b R)[0:64] / (O + a T + b R)[64], this warp's 32
+      //      columns, staged (128-byte swizzle) in its 4 KB of the slot's
+      //      spent Q (first half) or V (second half) tile, written by TMA
+      if (!waitb(B_O, n & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      tc_fence_after();
+      if (good && warp_ok) {
+        const float ai = f[2 * kC + i], bi = f[3 * kC + i];
+        const float2 a2 = make_float2(ai, ai), b2 = make_float2(bi, bi);
+        const uint32_t base = tbase + lane_off;
+        uint8_t* stg = (hc == 0 ? Qt(s) : Vt(s)) + 32 * q * 128;
+        uint8_t* row = stg + lane * 128;
+        float o[16], tt[16], rr[16];
+        tmem_ld16(base + T_O + 64, o);
+        tmem_ld16(base + T_T + 64, tt);
+        tmem_ld16(base + T_R + 64, rr);
+        tmem_wait_ld();
+        reg_fence16(o);
+        reg_fence16(tt);
+        reg_fence16(rr);
+        const float inv = 1.f / (o[0] + ai * tt[0] + bi * rr[0]);
+        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int col = 32 * hc + 16 * h2;
+          tmem_ld16(base + T_O + col, o);
+          tmem_ld16(base + T_T + col, tt);
+          tmem_ld16(base + T_R + col, rr);
+          tmem_wait_ld();
+          reg_fence16(o);
+          reg_fence16(tt);
+          reg_fence16(rr);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 x0 = make_float2(o[4 * e], o[4 * e + 1]), x1 = make_float2(o[4 * e + 2], o[4 * e + 3]);
+            x0 = fma2(a2, make_float2(tt[4 * e], tt[4 * e + 1]), x0);
+            x1 = fma2(a2, make_float2(tt[4 * e + 2], tt[4 * e + 3]), x1);
+            x0 = fma2(b2, make_float2(rr[4 * e], rr[4 * e + 1]), x0);
+            x1 = fma2(b2, make_float2(rr[4 * e + 2], rr[4 * e + 3]), x1);
+            x0 = mul2(x0, inv2);
+            x1 = mul2(x1, inv2);
+            *reinterpret_cast<float4*>(row + (((4 * h2 + e) ^ (lane & 7)) << 4)) = make_float4(x0.x, x0.y, x1.x, x1.y);
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&mapO, stg, 32 * hc, kC * c + 32 * q, bh);
+          bulk_commit();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[B_ED]);
+        bulk_wait_read();
+        mbar_arrive(&bars[B_QVE0 + s]);
+      }
+      (void)row_ok;
+      // leave together
+      if (!bar_and(2, kEpiWarps * 32, good)) break;
+      st.next(prm);
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  __syncthreads();
+  if (tid == 0 && *s_abort) atomicExch(prm.status, 1);
+  if (warp == W_TMA) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+    tmem_relinquish();
+  }
+}
+
+}  // namespace
+
+bool chunk128_long_supported(const Problem& p) {
+  return p.dtype == DT_BF16 && p.d == kD && p.chunk == kC && p.L > 2 * kC;
+}
+
+size_t chunk128_long_workspace_bytes(int B, int H, int L) { return long_states_workspace_bytes(B, H, L); }
+
+cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaStream_t s) {
+  LongStates ls;
+  cudaError_t e = launch_long_states(p, ws, status, s, &ls);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv, mo;
+  const int BH = p.B * p.H;
+  if (!make_map128(&mq, p.q, p.L, BH) || !make_map128(&mk, p.k, p.L, BH) || !make_map128(&mv, p.v, p.L, BH) ||
+      !make_out_map(&mo, p.out, p.L, BH))
+    return cudaErrorInvalidValue;
+  LongParams prm;
+  prm.log_lambda = p.log_lambda;
+  prm.BH = BH;
+  prm.H = p.H;
+  prm.L = p.L;
+  prm.NBL = ls.NBL;
+  prm.SEGB = ls.SEGB;
+  prm.nseg = ls.nseg;
+  prm.gloc = ls.gloc;
+  prm.gmid = ls.gmid;
+  prm.segsum = ls.segsum;
+  prm.segin = ls.segin;
+  prm.status = status;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, LongParams) = nullptr;
+#define LION_C128L_CASE(M, F) \
+  if (p.mask_kind == M && p.phi == F) kern = lion_chunk128_long_kernel<M, F>;
+  LION_C128L_CASE(MASK_LIT, PHI_ELU1)
+  LION_C128L_CASE(MASK_LIT, PHI_SILU_L2)
+  LION_C128L_CASE(MASK_LIT, PHI_IDENTITY)
+  LION_C128L_CASE(MASK_D, PHI_ELU1)
+  LION_C128L_CASE(MASK_D, PHI_SILU_L2)
+  LION_C128L_CASE(MASK_D, PHI_IDENTITY)
+  LION_C128L_CASE(MASK_S, PHI_ELU1)
+  LION_C128L_CASE(MASK_S, PHI_SILU_L2)
+  LION_C128L_CASE(MASK_S, PHI_IDENTITY)
+#undef LION_C128L_CASE
+  if (!kern) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int items = BH * ls.nseg;
+  const int grid = items < sm_count() ? items : sm_count();
+  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace lion

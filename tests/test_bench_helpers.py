@@ -35,3 +35,13 @@ def test_launch_counts():
     assert bench.kernels_per_call("chunk", 128, vit) == 1
     assert bench.kernels_per_call("chunk", 64, vit) == 1
     assert bench.kernels_per_call("chunk", 64, hires) == 3
+    assert bench.kernels_per_call("chunk", 128, hires) == 3
+    assert bench.kernels_per_call("chunk", 32, hires) == 1
+
+
+def test_traffic_keys_follow_the_kernel_that_runs():
+    # every sources list names files that exist, so a hash can be taken
+    for key, files in bench._TC_SOURCES.items():
+        for rel in files:
+            assert os.path.exists(os.path.join(ROOT, rel)), (key, rel)
+    assert bench._sources_sha((128, False)) != bench._sources_sha((128, True))

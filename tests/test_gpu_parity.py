@@ -139,6 +139,20 @@ def test_chunk128_steep_decay_exact_mask(oracle_mod, scale):
 
 
 @pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_chunk128_long_sequences(oracle_mod, mask):
+    """Sequences longer than 256 tokens at chunk 128: the pre-pass and segment
+    scan, then the chunk-sequential main pass carrying the forward state,
+    with ragged last chunks, blocks with one or two chunks, one or several
+    segments per head and several heads per CTA."""
+    for B, H, L in ((1, 2, 257), (1, 2, 384), (1, 3, 700), (2, 1, 2000), (8, 5, 1000), (1, 6, 3000),
+                    (40, 9, 300)):
+        inp = synth.make_inputs(B, H, L, 64, mask, "bf16", seed=900 + L + B)
+        q, k, v, ll = f64(inp)
+        ref = oracle_mod.rnn(q, k, v, ll, inp["mask"], threads=0)
+        check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 128), ref, inp, TOL_BF16)
+
+
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
 def test_long_sequences_blocks_and_segments(oracle_mod, mask):
     """Sequences longer than one 256-token block: the tensor-core path chains
     blocks (and, with few heads, segments of blocks across CTAs) through its
