@@ -16,11 +16,11 @@
 // e_{c-1}) and G_c the backward state entering it from the right (anchored
 // at s_{c+1}), both [phi(k) (x) [v; 1]] sums weighted by the decay.
 //
-// The sequence is cut into segments of 256-token blocks.  A pre-pass (the
-// chunk-64 kernel's, run right to left over each segment) and a segment scan
-// provide, per block, the backward state at its end and at its token 128, and
-// per segment the states entering it from both sides.  This pass walks one
-// segment left to right, one chunk at a time:
+// The sequence is cut into segments of 256-token blocks.  A pre-pass (run
+// right to left over each segment, lion_c128P.cu) and a segment scan provide,
+// per chunk, the backward state entering it from the right within its
+// segment, and per segment the states entering it from both sides.  This pass
+// walks one segment left to right, one chunk at a time:
 //   F_c     carried in TMEM (fp32, transposed: lane = output column, lane 64
 //           = z), starting from the segment's entering state, and advanced
 //           after every chunk: F_{c+1} = exp(T_c) F_c + U_c with
@@ -70,7 +70,7 @@ constexpr uint32_t kSleepNs = 2000u;
 constexpr int kGsegBytes = 64 * kLongStateCols * 4;  // one fp32 [64][80] state
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr int kSlotG = 9 * 1024;                      // pre-pass state (kGlocBytes) of a chunk
+constexpr int kSlotG = 9 * 1024;                      // pre-pass state (kGstBytes) of a chunk
 constexpr int kSlotBytes = 3 * kTile + kSlotG;        // Q, K, V, pre-pass state
 constexpr int OFF_SLOT = 0;                           // [2] slots
 constexpr int OFF_KW = OFF_SLOT + 2 * kSlotBytes;     // weighted phi(K)
@@ -89,7 +89,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kSlotBytes % 1024 == 0 && OFF_KW % 1024 == 0 && OFF_XF % 1024 == 0 && OFF_XG % 1024 == 0 &&
                   OFF_ONES % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
-static_assert(kGlocBytes <= kSlotG && kGlocBytes % 16 == 0 && kGsegBytes % 16 == 0, "bulk copies");
+static_assert(kGstBytes <= kSlotG && kGstBytes % 16 == 0 && kGsegBytes % 16 == 0, "bulk copies");
 
 // per-chunk scalars (INFO)
 enum { I_EXACT = 0, I_T = 1, I_LNEXT = 2 };
@@ -133,8 +133,7 @@ struct LongParams {
   const float* log_lambda;
   int BH, H, L;
   int NBL, SEGB, nseg;
-  const uint8_t* gloc;
-  const uint8_t* gmid;
+  const uint8_t* gst;       // [BH][chunks] pre-pass states (kGstBytes each)
   const float* segsum;
   const float* segin;
   int* status;
@@ -242,11 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto nk_of = [&](int c) { return (min(kC, L - kC * c) + 15) >> 4; };
   // pre-pass state at the right edge of chunk c
-  auto gsrc = [&](int bh, int c) {
-    const int b = c >> 1;
-    const bool mid = (c & 1) == 0 && L - 256 * b > kC;
-    return (mid ? prm.gmid : prm.gloc) + ((size_t)bh * prm.NBL + b) * kGlocBytes;
-  };
+  const int nch_all = (L + kC - 1) / kC;
+  auto gsrc = [&](int bh, int c) { return prm.gst + ((size_t)bh * nch_all + c) * kGstBytes; };
 
   if (warp == W_TMA) {
     // =========================== TMA producer ===================================
@@ -280,11 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ld.valid(prm) && (n < 2 || (mbar_try_wait(&bars[B_KE0 + s], ((n >> 1) - 1) & 1) &&
                                         mbar_try_wait(&bars[B_QVE0 + s], ((n >> 1) - 1) & 1)))) {
           const int bh = ld.item / prm.nseg;
-          mbar_arrive_expect_tx(&bars[B_LD0 + s], (uint32_t)(3 * kTile + kGlocBytes));
+          mbar_arrive_expect_tx(&bars[B_LD0 + s], (uint32_t)(3 * kTile + kGstBytes));
           tma_load_3d(Vt(s), &mapV, &bars[B_LD0 + s], 0, kC * ld.c, bh);
           tma_load_3d(Kt(s), &mapK, &bars[B_LD0 + s], 0, kC * ld.c, bh);
           tma_load_3d(Qt(s), &mapQ, &bars[B_LD0 + s], 0, kC * ld.c, bh);
-          bulk_load(Gt(s), gsrc(bh, ld.c), (uint32_t)kGlocBytes, &bars[B_LD0 + s]);
+          bulk_load(Gt(s), gsrc(bh, ld.c), (uint32_t)kGstBytes, &bars[B_LD0 + s]);
           ++issued_ld[s];
           ++n;
           ld.next(prm);
@@ -586,30 +582,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float Tc = info(s)[I_T], lnext = info(s)[I_LNEXT];
         // exp(P at the first token after the segment - P at the first token after chunk c)
         const float fdec = __expf(tseg - (cum + Tc) - lnext + lafter);
-        const uint8_t* g = Gt(s);
-        uint8_t* row = XGt + i * 128;
-        if (i < 64) {
+        // the pre-pass tile has the operand tile's row order and swizzle: row i
+        // (state column i, 64 = z) over m, 16-byte piece j at j ^ (i & 7)
+        if (i < 65) {
+          const uint8_t* grow = Gt(s) + i * 128;
+          uint8_t* row = XGt + i * 128;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
+            const int off = ((4 * hc + j) ^ (i & 7)) << 4;
             float y8[8];
+            unpack8_h(*reinterpret_cast<const uint4*>(grow + off), y8);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int m = 32 * hc + 8 * j + e;
-              y8[e] = __half2float(reinterpret_cast<const __half*>(g)[m * 64 + i]) + fdec * gseg[m * kLongStateCols + i];
-            }
-            *reinterpret_cast<uint4*>(row + (((4 * hc + j) ^ (i & 7)) << 4)) = pack8_h(y8);
-          }
-        } else if (i == 64) {
-          const float* gz = reinterpret_cast<const float*>(g + 64 * 64 * 2);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float y8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int m = 32 * hc + 8 * j + e;
-              y8[e] = gz[m] + fdec * gseg[m * kLongStateCols + 64];
-            }
-            *reinterpret_cast<uint4*>(row + (((4 * hc + j) ^ (i & 7)) << 4)) = pack8_h(y8);
+            for (int e = 0; e < 8; ++e) y8[e] = fmaf(fdec, gseg[(32 * hc + 8 * j + e) * kLongStateCols + i], y8[e]);
+            *reinterpret_cast<uint4*>(row + off) = pack8_h(y8);
           }
         }
       }
@@ -736,11 +721,34 @@ bool chunk128_long_supported(const Problem& p) {
   return p.dtype == DT_BF16 && p.d == kD && p.chunk == kC && p.L > 2 * kC;
 }
 
-size_t chunk128_long_workspace_bytes(int B, int H, int L) { return long_states_workspace_bytes(B, H, L); }
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+struct LongWs {
+  size_t gst, segsum, segin;
+};
+LongWs long_ws(int B, int H, int L, const LongPlan& plan) {
+  const size_t BH = (size_t)B * H, nch = (size_t)(L + kC - 1) / kC;
+  return {align256(BH * nch * kGstBytes), align256(BH * plan.nseg * kSegSumFloats * 4),
+          align256(BH * plan.nseg * kSegInFloats * 4)};
+}
+}  // namespace
+
+size_t chunk128_long_workspace_bytes(int B, int H, int L) {
+  if (L <= 2 * kC) return 0;
+  const LongWs w = long_ws(B, H, L, long_plan(B, H, L));
+  return w.gst + w.segsum + w.segin;
+}
 
 cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaStream_t s) {
-  LongStates ls;
-  cudaError_t e = launch_long_states(p, ws, status, s, &ls);
+  if (!ws) return cudaErrorInvalidValue;
+  const LongPlan plan = long_plan(p.B, p.H, p.L);
+  const LongWs w = long_ws(p.B, p.H, p.L, plan);
+  uint8_t* gst = static_cast<uint8_t*>(ws);
+  float* segsum = reinterpret_cast<float*>(gst + w.gst);
+  float* segin = reinterpret_cast<float*>(gst + w.gst + w.segsum);
+  cudaError_t e = launch_chunk128_pre(p, plan, gst, segsum, status, s);
+  if (e != cudaSuccess) return e;
+  e = launch_segment_scan(p, plan, segsum, segin, s);
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mo;
   const int BH = p.B * p.H;
@@ -752,13 +760,12 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   prm.BH = BH;
   prm.H = p.H;
   prm.L = p.L;
-  prm.NBL = ls.NBL;
-  prm.SEGB = ls.SEGB;
-  prm.nseg = ls.nseg;
-  prm.gloc = ls.gloc;
-  prm.gmid = ls.gmid;
-  prm.segsum = ls.segsum;
-  prm.segin = ls.segin;
+  prm.NBL = plan.NBL;
+  prm.SEGB = plan.SEGB;
+  prm.nseg = plan.nseg;
+  prm.gst = gst;
+  prm.segsum = segsum;
+  prm.segin = segin;
   prm.status = status;
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, LongParams) = nullptr;
 #define LION_C128L_CASE(M, F) \
@@ -776,7 +783,7 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   if (!kern) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int items = BH * ls.nseg;
+  const int items = BH * plan.nseg;
   const int grid = items < sm_count() ? items : sm_count();
   kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, prm);
   return cudaGetLastError();

@@ -36,43 +36,49 @@ size_t chunk_tc_workspace_bytes(int B, int H, int L);
 int chunk_tc_launches(int B, int H, int L);
 cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_t s);
 
-// Backward pre-pass and segment scan of the chunk-64 kernel, run for the
-// 128-token-chunk main pass of sequences longer than 256 tokens.  Per head the
-// sequence is cut into 256-token blocks and segments of `SEGB` blocks:
-//   gloc[bh][b]  backward state entering block b from the right, from the
-//                blocks after it within its segment (anchored at the first
-//                token after the block);
-//   gmid[bh][b]  the same at the block's token 128 (anchored there), also
-//                taking in the block's own tokens 128..255;
-// both fp16 [64 rows m][64 columns n] followed by fp32 z[64];
-//   segsum[bh][s] (fp32): forward summary [64][80], backward summary
-//                [64][80], then the sum of log(lambda) over the segment;
+// Segment plan and segment scan of the long-sequence tensor-core paths.  Per
+// head the sequence is cut into 256-token blocks and segments of `SEGB`
+// blocks (`nseg` of them, so that B*H*nseg fills the SMs).  A pre-pass
+// writes per segment
+//   segsum[bh][s] (fp32): forward summary [64 m][80] (sum over the segment of
+//                 exp(P_last - P_j) phi(k_j) [v_j; 1]^T, anchored at its last
+//                 token), backward summary [64][80] (exp(P_j - P_first) ...,
+//                 anchored at its first token), then the sum of log(lambda)
+//                 over the segment;
+// and the scan chains them into
 //   segin[bh][s]  (fp32): forward state entering segment s from the left
-//                [64][80], backward state entering it from the right [64][80]
+//                 [64][80], backward state entering it from the right [64][80]
 // (column 64 of a [64][80] state is z; 65..79 are zero).
 constexpr int kLongStateCols = 80;
-constexpr int kGlocBytes = 64 * 64 * 2 + 64 * 4;
 constexpr int kSegSumFloats = 2 * 64 * kLongStateCols + 4;
 constexpr int kSegInFloats = 2 * 64 * kLongStateCols;
-struct LongStates {
+struct LongPlan {
   int NBL, SEGB, nseg;
-  const uint8_t* gloc;
-  const uint8_t* gmid;
-  const float* segsum;
-  const float* segin;
 };
-size_t long_states_workspace_bytes(int B, int H, int L);
-cudaError_t launch_long_states(const Problem& p, void* ws, int* status, cudaStream_t s, LongStates* out);
+LongPlan long_plan(int B, int H, int L);
+cudaError_t launch_segment_scan(const Problem& p, const LongPlan& plan, const float* segsum, float* segin,
+                                cudaStream_t s);
+
+// Per-chunk backward states of the 128-token-chunk path: for chunk c of a
+// head, the backward state entering it from the right, from the tokens after
+// it within its segment, anchored at the first token after the chunk, stored
+// transposed as 65 rows (row n < 64: column n of the state over the 64 key
+// features m; row 64: z) of 64 fp16 values, the 16-byte pieces of row r in
+// the order j ^ (r & 7) (the 128-byte swizzle of the operand tiles).
+constexpr int kGstBytes = 65 * 128;
 
 // Tensor-core chunkwise kernel with 128-token chunks: bf16, d = 64,
 // chunk = 128.  L <= 256: one launch, no workspace.
 bool chunk128_tc_supported(const Problem& p);
 cudaError_t launch_chunk128_tc(const Problem& p, int* status, cudaStream_t s);
-// The same for L > 256: the chunk-64 pre-pass and segment scan above, then a
-// 128-token-chunk main pass (three launches; workspace as returned).
+// The same for L > 256: a backward pre-pass over 128-token chunks (per-chunk
+// states and segment summaries), the segment scan, and the main pass (three
+// launches; workspace as returned).
 bool chunk128_long_supported(const Problem& p);
 size_t chunk128_long_workspace_bytes(int B, int H, int L);
 cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaStream_t s);
+cudaError_t launch_chunk128_pre(const Problem& p, const LongPlan& plan, uint8_t* gst, float* segsum, int* status,
+                                cudaStream_t s);
 
 // Device-side status word that kernels set when a bounded wait gives up
 // (address on the current device; nullptr if it cannot be resolved).

@@ -139,10 +139,12 @@ constexpr uint32_t R_SI = 0, R_OF = 80, R_OG = 144, R_Z = 208;
 //   pre:  the segment's forward summary / backward state entering the next block
 constexpr uint32_t TM_KEEP = 2 * kRegion;   // 432
 
-// long-sequence exchange buffers (global, per block / per segment)
-// (kGlocBytes, kSegSumFloats, kSegInFloats: lion_internal.h)
-static_assert(kGlocBytes == kD * kD * 2 + kD * 4 && kLongStateCols == kStateCols &&
-                  kSegSumFloats == 2 * kD * kStateCols + 4 && kSegInFloats == 2 * kD * kStateCols,
+// long-sequence exchange buffers (global, per block / per segment): the
+// backward state entering each block, fp16 [64 m][64 n] then fp32 z[64];
+// segment summaries and entering states as declared in lion_internal.h
+constexpr int kGlocBytes = kD * kD * 2 + kD * 4;
+static_assert(kLongStateCols == kStateCols && kSegSumFloats == 2 * kD * kStateCols + 4 &&
+                  kSegInFloats == 2 * kD * kStateCols,
               "exchange-buffer layout");
 
 struct TcParams {
@@ -153,7 +155,6 @@ struct TcParams {
   int SEGB;       // blocks per segment
   int nseg;       // segments per head
   uint8_t* gloc;       // [BH][NBL] backward state entering each block (within its segment)
-  uint8_t* gmid;       // [BH][NBL] or null: the same at the block's token 128 (pre-pass only)
   float* segsum;       // [BH][nseg] segment summaries (pre-pass output)
   const float* segin;  // [BH][nseg] states entering each segment (scan output)
   int* status;
@@ -687,16 +688,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) st[e] = decay * st[e] + u[e];
           stz = decay * stz + uz;
-          if (MODE == MODE_PRE && !fwd && c == 2 && prm.gmid) {
-            // backward state at the block's token 128 (chunks 2 and 3 of 64
-            // taken in): the right-hand state of its first 128-token chunk
-            uint8_t* gl = prm.gmid + ((size_t)bh * prm.NBL + b) * kGlocBytes;
-            __half* gv = reinterpret_cast<__half*>(gl) + m * kD + 16 * wg;
-#pragma unroll
-            for (int e = 0; e < 16; e += 2)
-              *reinterpret_cast<__half2*>(gv + e) = __floats2half2_rn(st[e], st[e + 1]);
-            if (wg == 3) reinterpret_cast<float*>(gl + kD * kD * 2)[m] = stz;
-          }
         }
         // states leaving the block
         if (MODE == MODE_MAIN) {
@@ -1075,53 +1066,31 @@ cudaError_t launch_mode(const Problem& p, const CUtensorMap& mq, const CUtensorM
 
 }  // namespace
 
-size_t long_states_workspace_bytes(int B, int H, int L) {
+LongPlan long_plan(int B, int H, int L) {
   const TcPlan t = plan_tc(B, H, L);
-  if (t.NBL == 1) return 0;
-  return 2 * align256(t.gloc_bytes) + align256(t.segsum_bytes) + align256(t.segin_bytes);
+  LongPlan lp;
+  lp.NBL = t.NBL;
+  lp.SEGB = t.SEGB;
+  lp.nseg = t.nseg;
+  return lp;
 }
 
-cudaError_t launch_long_states(const Problem& p, void* ws, int* status, cudaStream_t s, LongStates* out) {
-  CUtensorMap mq, mk, mv;
-  const int BH = p.B * p.H;
-  const TcPlan t = plan_tc(p.B, p.H, p.L);
-  if (t.NBL == 1 || !ws) return cudaErrorInvalidValue;
-  if (!make_map(&mq, p.q, p.L, BH) || !make_map(&mk, p.k, p.L, BH) || !make_map(&mv, p.v, p.L, BH))
-    return cudaErrorInvalidValue;
-  TcParams prm;
-  prm.out = p.out;
+cudaError_t launch_segment_scan(const Problem& p, const LongPlan& plan, const float* segsum, float* segin,
+                                cudaStream_t s) {
+  TcParams prm = {};
   prm.log_lambda = p.log_lambda;
-  prm.BH = BH;
+  prm.BH = p.B * p.H;
   prm.H = p.H;
   prm.L = p.L;
-  prm.NBL = t.NBL;
-  prm.SEGB = t.SEGB;
-  prm.nseg = t.nseg;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  prm.gloc = w;
-  prm.gmid = w + align256(t.gloc_bytes);
-  prm.segsum = reinterpret_cast<float*>(w + 2 * align256(t.gloc_bytes));
-  float* segin = reinterpret_cast<float*>(w + 2 * align256(t.gloc_bytes) + align256(t.segsum_bytes));
-  prm.segin = segin;
-  prm.status = status;
-  const int items = BH * t.nseg;
-  const int grid = items < num_sms() ? items : num_sms();
-  cudaError_t e = launch_mode<MODE_PRE>(p, mq, mk, mv, prm, grid, s);
-  if (e != cudaSuccess) return e;
-  const dim3 sgrid((2 * kD * kStateCols + kScanThreads - 1) / kScanThreads, BH);
+  prm.NBL = plan.NBL;
+  prm.SEGB = plan.SEGB;
+  prm.nseg = plan.nseg;
+  prm.segsum = const_cast<float*>(segsum);
+  const dim3 sgrid((2 * kD * kStateCols + kScanThreads - 1) / kScanThreads, prm.BH);
   if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
   else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
   else lion_segment_scan_kernel<MASK_S><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  out->NBL = t.NBL;
-  out->SEGB = t.SEGB;
-  out->nseg = t.nseg;
-  out->gloc = prm.gloc;
-  out->gmid = prm.gmid;
-  out->segsum = prm.segsum;
-  out->segin = segin;
-  return cudaSuccess;
+  return cudaGetLastError();
 }
 
 size_t chunk_tc_workspace_bytes(int B, int H, int L) {
@@ -1148,7 +1117,6 @@ cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_
   prm.SEGB = t.SEGB;
   prm.nseg = t.nseg;
   prm.gloc = nullptr;
-  prm.gmid = nullptr;
   prm.segsum = nullptr;
   prm.segin = nullptr;
   prm.status = status;
