@@ -26,9 +26,11 @@
 //           after every chunk: F_{c+1} = exp(T_c) F_c + U_c with
 //           U_c^T = [V_c | 1]^T (w_c o phi(K_c)), w_j = exp(p_e - p_j);
 //   G_c     the pre-pass state at the chunk's right edge plus the segment's
-//           entering backward state decayed to it;
-// both written each chunk as K-major fp16 operand tiles of 80 rows (row 64 =
-// z).  MMAs per chunk (n = columns with tokens, rounded up to 16):
+//           entering backward state decayed to it, built by prep in place in
+//           the chunk's copy of the pre-pass tile (which has the operand
+//           tile's layout);
+// both as K-major fp16 operand tiles of 80 rows (row 64 = z).  MMAs per chunk
+// (n = columns with tokens, rounded up to 16):
 //   S   = phi(Q) phi(K)^T            M=128 N=n  K=64
 //   U^T = [V | 1]^T (w o phi(K))     M=128 N=64 K=n
 //   T   = phi(Q) X_F,  R = phi(Q) X_G  M=128 N=80 K=64
@@ -38,8 +40,9 @@
 // Warps: 0 TMA (Q, K, V and the pre-pass state of a chunk into one of two
 // slots; the segment's entering backward state), 1 MMA issue, 2-17 "prep"
 // (four threads per token: prefix, V -> fp16, phi(k) and its weighted copy,
-// phi(q), factors), 18-25 "epi" (two warps per TMEM lane quarter, each one
-// column half: state tiles, carried state, mask, output through TMA).
+// phi(q), factors, the X_G tile), 18-25 "epi" (two warps per TMEM lane
+// quarter, each one column half: mask, carried state and the next chunk's
+// X_F while the chunk's output product runs, then the output through TMA).
 // Prep of chunk c+1 overlaps the epilogue of chunk c.
 //
 // TMEM (512 columns): S [0,128) (P in columns 0-31 and 64-95), O [128,208),
@@ -70,13 +73,12 @@ constexpr uint32_t kSleepNs = 2000u;
 constexpr int kGsegBytes = 64 * kLongStateCols * 4;  // one fp32 [64][80] state
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr int kSlotG = 9 * 1024;                      // pre-pass state (kGstBytes) of a chunk
+constexpr int kSlotG = kStTile;                       // pre-pass state of a chunk, then its X_G tile
 constexpr int kSlotBytes = 3 * kTile + kSlotG;        // Q, K, V, pre-pass state
 constexpr int OFF_SLOT = 0;                           // [2] slots
 constexpr int OFF_KW = OFF_SLOT + 2 * kSlotBytes;     // weighted phi(K)
 constexpr int OFF_XF = OFF_KW + kTile;                // X_F operand tile
-constexpr int OFF_XG = OFF_XF + kStTile;              // X_G operand tile
-constexpr int OFF_ONES = OFF_XG + kStTile;            // 16 rows, column 0 = 1
+constexpr int OFF_ONES = OFF_XF + kStTile;            // 16 rows, column 0 = 1
 constexpr int OFF_GSEG = OFF_ONES + 2048;             // the segment's entering backward state (fp32 [64][80])
 constexpr int OFF_FAC = OFF_GSEG + kGsegBytes;        // [slot] alpha, rho, a, b, p [128] each
 constexpr int OFF_INFO = OFF_FAC + 2 * 5 * kC * 4;    // [slot] float[8] per-chunk scalars
@@ -86,8 +88,8 @@ constexpr int kNumBars = 24;
 constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kSlotBytes % 1024 == 0 && OFF_KW % 1024 == 0 && OFF_XF % 1024 == 0 && OFF_XG % 1024 == 0 &&
-                  OFF_ONES % 1024 == 0,
+static_assert(kSlotBytes % 1024 == 0 && OFF_KW % 1024 == 0 && OFF_XF % 1024 == 0 && OFF_ONES % 1024 == 0 &&
+                  (3 * kTile) % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(kGstBytes <= kSlotG && kGstBytes % 16 == 0 && kGsegBytes % 16 == 0, "bulk copies");
 
@@ -107,17 +109,18 @@ enum {
   B_KE0 = 9,     // + slot: MMA commit: K tile of the slot read
   B_KWE = 11,    // MMA commit: weighted phi(K) read
   B_XF = 12,     // epi: X_F written (8 arrivals)
-  B_XG = 13,     // epi: X_G written (8 arrivals)
+  B_XG = 13,     // prep: X_G written (16 arrivals)
   B_CU = 14,     // epi: carried state advanced, U^T read (8 arrivals)
   B_PM = 15,     // epi: P written (8 arrivals)
   B_ED = 16,     // epi: O, T, R read (8 arrivals)
   B_QVE0 = 17,   // + slot: epi: output stores have read the slot's Q and V tiles (8 arrivals)
   B_DRAIN = 19,  // MMA commit used when unwinding
-  B_GF = 20,     // epi: the item's last X_G written, the segment state may be replaced (8 arrivals)
+  B_GF = 20,     // prep: the item's last X_G written, the segment state may be replaced (16 arrivals)
+  B_TD = 21,     // MMA commit: T done (X_F read)
 };
 __device__ __forceinline__ uint32_t bar_count(int b) {
-  if (b == B_KVR || b == B_QR) return kPrepWarps;
-  if ((b >= B_XF && b <= B_QVE0 + 1) || b == B_GF) return kEpiWarps;
+  if (b == B_KVR || b == B_QR || b == B_XG || b == B_GF) return kPrepWarps;
+  if (b == B_XF || b == B_CU || b == B_PM || b == B_ED || b == B_QVE0 || b == B_QVE0 + 1) return kEpiWarps;
   return 1;
 }
 
@@ -192,7 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto Gt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes + 3 * kTile; };
   uint8_t* KWt = smem + OFF_KW;
   uint8_t* XFt = smem + OFF_XF;
-  uint8_t* XGt = smem + OFF_XG;
   const float* gseg = reinterpret_cast<const float*>(smem + OFF_GSEG);
   auto fac = [&](int s) { return reinterpret_cast<float*>(smem + OFF_FAC) + s * 5 * kC; };
   auto info = [&](int s) { return reinterpret_cast<float*>(smem + OFF_INFO) + s * 8; };
@@ -214,9 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *reinterpret_cast<uint4*>(smem + OFF_ONES + sw128_offset(r, c8)) =
         make_uint4(c8 == 0 ? pack_h2(1.f, 0.f) : 0u, 0u, 0u, 0u);
   }
-  // rows 65..79 of the state tiles stay zero
-  for (int x = tid; x < 2 * 15 * 8; x += kThreads) {
-    uint8_t* t = x < 15 * 8 ? XFt : XGt;
+  // rows 65..79 of the state tiles (X_F, and X_G in each slot past the
+  // 65 rows its copy brings) stay zero
+  for (int x = tid; x < 3 * 15 * 8; x += kThreads) {
+    const int w = x / (15 * 8);
+    uint8_t* t = w == 0 ? XFt : Gt(w - 1);
     const int y = x % (15 * 8), r = 65 + y / 8, c8 = y % 8;
     *reinterpret_cast<uint4*>(t + sw128_offset(r, c8)) = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -337,10 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_T, kmaj(Qt(s), k), kmaj(XFt, k), idX, k > 0 ? 1u : 0u);
+        mma_commit(&bars[B_TD]);
         if (!waitb(B_XG, n & 1)) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_R, kmaj(Qt(s), k), kmaj(XGt, k), idX, k > 0 ? 1u : 0u);
+        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_R, kmaj(Qt(s), k), kmaj(Gt(s), k), idX, k > 0 ? 1u : 0u);
         if (!waitb(B_PM, n & 1)) break;
         tc_fence_after();
         {
@@ -377,9 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       *en = ell_at<MASK>(prm, bh, kC * x.c + kC, lh);   // first token after the chunk
     };
     if (st.valid(prm)) load_ell(st, &ell_next, &lnext_next);
+    int ng = 0;                               // items started
+    float cum = 0.f, tseg = 0.f, lafter = 0.f;
     for (int n = 0; st.valid(prm); ++n) {
       const int s = n & 1, tok = kC * st.c + t;
       const float ell = ell_next, lnext = lnext_next;
+      const bool first = st.c == st.c_lo, last = st.c + 1 == st.c_hi;
+      if (first) {
+        // a new segment: bookkeeping for its backward entering state
+        const int bh = st.item / prm.nseg, seg = st.item % prm.nseg;
+        tseg = __ldg(prm.segsum + (size_t)st.item * kSegSumFloats + 2 * 64 * kLongStateCols);
+        const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
+        lafter = ell_at<MASK>(prm, bh, 256 * min(prm.NBL, (seg + 1) * prm.SEGB), lh);
+        cum = 0.f;
+        ++ng;
+      }
       // ---- chunk-local inclusive prefix (each token's value sits in its four lanes)
       float x = ell;
 #pragma unroll
@@ -450,6 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(KWt + sw128_offset(t, j0 + j)) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
+      // Arrivals on KVR and QR wait for the previous chunk's state MMA (issued
+      // after the MMA thread's own waits on them) and on XG for its output
+      // product, so that no barrier the MMA thread polls runs two phases ahead
+      // of its wait.  LION-S and -D already waited above for the weighted copy.
+      if (MASK == MASK_LIT && n >= 1 && !waitb(B_KWE, (n - 1) & 1)) good = false;
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_KVR]);
@@ -482,6 +504,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_QR]);
+      // ---- X_G = pre-pass state + decay * the segment's backward entering
+      //      state, in place in the slot's pre-pass tile (row i = state column
+      //      i, 64 = z; this thread: row t, state rows m = 16 qq .. 16 qq + 15)
+      if (first && !waitb(B_GS, (ng - 1) & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      if (good && t < 65) {
+        // exp(P at the first token after the segment - P at the first token after the chunk)
+        const float fdec = __expf(tseg - (cum + T) - lnext + lafter);
+        uint8_t* grow = Gt(s) + t * 128;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int off = ((j0 + j) ^ (t & 7)) << 4;
+          float y8[8];
+          unpack8_h(*reinterpret_cast<const uint4*>(grow + off), y8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y8[e] = fmaf(fdec, gseg[(8 * (j0 + j) + e) * kLongStateCols + t], y8[e]);
+          *reinterpret_cast<uint4*>(grow + off) = pack8_h(y8);
+        }
+      }
+      cum += T;
+      if (n >= 1 && !waitb(B_O, (n - 1) & 1)) good = false;
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[B_XG]);
+        if (last) mbar_arrive(&bars[B_GF]);   // done with this segment's state
+      }
       st.next(prm);
       if (st.valid(prm)) load_ell(st, &ell_next, &lnext_next);
     }
@@ -494,42 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const bool st_row = i < kStRows;         // lanes holding a state-tile row
     bool good = true;
-    Step st;
-    st.item = blockIdx.x;
-    if (st.valid(prm)) st.set_item(prm, st.item);
-    int ng = 0;                // items started
-    float cum = 0.f, tseg = 0.f, lafter = 0.f;
-    for (int n = 0; st.valid(prm); ++n) {
-      const int s = n & 1, c = st.c, nk = nk_of(c), bh = st.item / prm.nseg;
-      const int tok = kC * c + i;
-      const bool first = c == st.c_lo, row_ok = tok < L, warp_ok = kC * c + 32 * q < L;
-      const float* f = fac(s);
-      const float* alpha = f;
-      const float* rho = f + kC;
-      const float* pp = f + 4 * kC;
-      if (first) {
-        // a new segment: its forward entering state into the carried TMEM
-        // state, and the bookkeeping for its backward entering state
-        const int seg = st.item % prm.nseg;
-        const float* fin = prm.segin + (size_t)st.item * kSegInFloats;   // [64 m][80]
-        tseg = prm.segsum[(size_t)st.item * kSegSumFloats + 2 * 64 * kLongStateCols];
-        const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
-        lafter = ell_at<MASK>(prm, bh, 256 * min(prm.NBL, (seg + 1) * prm.SEGB), lh);
-        cum = 0.f;
-        if (q < 3) {
-          float v[16];
-#pragma unroll 1
-          for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = st_row ? __ldg(fin + (32 * hc + 16 * h2 + e) * kLongStateCols + i) : 0.f;
-            tmem_st16(tbase + lane_off + T_F + 32 * hc + 16 * h2, v);
-          }
-          tmem_wait_st();
-        }
-        ++ng;
-      }
-      // ---- X_F = the carried state, transposed, K-major fp16 (rows = output columns)
-      if (good && q < 3) {
+    // X_F = the carried state, transposed, K-major fp16 (rows = output columns)
+    auto write_xf = [&]() {
+      if (q < 3) {
         float u0[16], u1[16];
         const uint32_t fa = tbase + lane_off + T_F + 32 * hc;
         tmem_ld16(fa, u0);
@@ -549,61 +565,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_XF]);
-      // ---- advance the carried state: F <- exp(T_c) F + U^T (the U commit
-      //      also means prep's per-chunk scalars of this step are written)
-      if (!waitb(B_U, n & 1)) good = false;
-      good = __all_sync(0xffffffffu, good);
-      tc_fence_after();
-      if (good && q < 3) {
-        const float dec = MASK == MASK_LIT ? 1.f : __expf(info(s)[I_T]);
+    };
+    Step st;
+    st.item = blockIdx.x;
+    if (st.valid(prm)) st.set_item(prm, st.item);
+    for (int n = 0; st.valid(prm) && good; ++n) {
+      const int s = n & 1, c = st.c, nk = nk_of(c), bh = st.item / prm.nseg;
+      const bool first = c == st.c_lo, last = c + 1 == st.c_hi, warp_ok = kC * c + 32 * q < L;
+      const float* f = fac(s);
+      const float* alpha = f;
+      const float* rho = f + kC;
+      const float* pp = f + 4 * kC;
+      if (first) {
+        // a new segment: its forward entering state into the carried TMEM
+        // state, then X_F once the previous chunk's T has read the tile
+        const float* fin = prm.segin + (size_t)st.item * kSegInFloats;   // [64 m][80]
+        if (q < 3) {
+          float v[16];
 #pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float fv[16], uv[16];
-          const uint32_t off = lane_off + 32 * hc + 16 * h2;
-          tmem_ld16(tbase + off + T_F, fv);
-          tmem_ld16(tbase + off + T_U, uv);
-          tmem_wait_ld();
-          reg_fence16(fv);
-          reg_fence16(uv);
+          for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) fv[e] = fmaf(dec, fv[e], uv[e]);
-          tmem_st16(tbase + off + T_F, fv);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_CU]);
-      // ---- X_G = pre-pass state + decay * segment's backward entering state, transposed
-      if (!waitb(B_LD0 + s, (n >> 1) & 1)) good = false;
-      if (first && !waitb(B_GS, (ng - 1) & 1)) good = false;
-      good = __all_sync(0xffffffffu, good);
-      if (good && st_row) {
-        const float Tc = info(s)[I_T], lnext = info(s)[I_LNEXT];
-        // exp(P at the first token after the segment - P at the first token after chunk c)
-        const float fdec = __expf(tseg - (cum + Tc) - lnext + lafter);
-        // the pre-pass tile has the operand tile's row order and swizzle: row i
-        // (state column i, 64 = z) over m, 16-byte piece j at j ^ (i & 7)
-        if (i < 65) {
-          const uint8_t* grow = Gt(s) + i * 128;
-          uint8_t* row = XGt + i * 128;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int off = ((4 * hc + j) ^ (i & 7)) << 4;
-            float y8[8];
-            unpack8_h(*reinterpret_cast<const uint4*>(grow + off), y8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y8[e] = fmaf(fdec, gseg[(32 * hc + 8 * j + e) * kLongStateCols + i], y8[e]);
-            *reinterpret_cast<uint4*>(row + off) = pack8_h(y8);
+            for (int e = 0; e < 16; ++e) v[e] = st_row ? __ldg(fin + (32 * hc + 16 * h2 + e) * kLongStateCols + i) : 0.f;
+            tmem_st16(tbase + lane_off + T_F + 32 * hc + 16 * h2, v);
           }
+          tmem_wait_st();
         }
-      }
-      cum += info(s)[I_T];
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[B_XG]);
-        if (c + 1 == st.c_hi) mbar_arrive(&bars[B_GF]);   // done with this segment's state
+        if (n >= 1 && !waitb(B_TD, (n - 1) & 1)) good = false;
+        good = __all_sync(0xffffffffu, good);
+        if (!good) break;
+        write_xf();
       }
       // ---- P = S * M, fp16, into the first 64 columns of S (this warp's column half)
       if (!waitb(B_S, n & 1)) good = false;
@@ -640,6 +630,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_PM]);
+      // ---- advance the carried state: F <- exp(T_c) F + U^T (the U commit
+      //      also means prep's per-chunk scalars of this step are written),
+      //      then the next chunk's X_F once this chunk's T has read the tile;
+      //      the output product runs meanwhile
+      if (!waitb(B_U, n & 1)) good = false;
+      good = __all_sync(0xffffffffu, good);
+      tc_fence_after();
+      if (good && q < 3) {
+        const float dec = MASK == MASK_LIT ? 1.f : __expf(info(s)[I_T]);
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float fv[16], uv[16];
+          const uint32_t off = lane_off + 32 * hc + 16 * h2;
+          tmem_ld16(tbase + off + T_F, fv);
+          tmem_ld16(tbase + off + T_U, uv);
+          tmem_wait_ld();
+          reg_fence16(fv);
+          reg_fence16(uv);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) fv[e] = fmaf(dec, fv[e], uv[e]);
+          tmem_st16(tbase + off + T_F, fv);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_CU]);
+      if (!last) {
+        if (!waitb(B_TD, n & 1)) good = false;
+        good = __all_sync(0xffffffffu, good);
+        if (good) {
+          tc_fence_after();
+          write_xf();
+        }
+      }
       // ---- y = (O + a T + b R)[0:64] / (O + a T + b R)[64], this warp's 32
       //      columns, staged (128-byte swizzle) in its 4 KB of the slot's
       //      spent Q (first half) or V (second half) tile, written by TMA
@@ -698,9 +723,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_wait_read();
         mbar_arrive(&bars[B_QVE0 + s]);
       }
-      (void)row_ok;
-      // leave together
-      if (!bar_and(2, kEpiWarps * 32, good)) break;
       st.next(prm);
     }
     if (lane == 0) bulk_wait_all();
