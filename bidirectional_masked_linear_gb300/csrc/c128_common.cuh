@@ -136,6 +136,14 @@ __device__ __forceinline__ uint64_t kmaj(const uint8_t* tile, int k) {
 __device__ __forceinline__ uint64_t mnmaj(uint32_t addr, int k, uint32_t lbo) {
   return desc_sw128(addr + 2048 * k, lbo, 1024);
 }
+// One K step (16 rows of K) is a constant added to a descriptor, whose fields
+// count 16-byte units: 32 bytes of a K-major tile, one 2048-byte block of an
+// MN-major one, and for the [V | 1] operand (second MN atom = the ones tile,
+// reached through the leading byte offset) the offset shrinks by as much.
+// The ones tile lies above every V block, so the offset stays positive.
+constexpr uint64_t kKmajStep = 32 >> 4;
+constexpr uint64_t kMnmajStep = 2048 >> 4;
+constexpr uint64_t kMnmajOnesStep = (2048 >> 4) - ((uint64_t)(2048 >> 4) << 16);
 
 // One 16-column block of the decay mask on a row of S (row i of its chunk,
 // columns j0..j0+15), in place.  Blocks entirely left (right) of every row

@@ -294,9 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int nk = c == 0 ? nk0 : nk1;
           const uint32_t idS = idesc_f16(128, 16 * nk, false, false);
+          {
+            uint64_t da = kmaj(Qt(s, c), 0), db = kmaj(Kt(c), 0);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tbase + T_S + 128 * c, kmaj(Qt(s, c), k), kmaj(Kt(c), k), idS, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 4; ++k, da += kKmajStep, db += kKmajStep)
+              mma_bf16(tbase + T_S + 128 * c, da, db, idS, k > 0 ? 1u : 0u);
+          }
           mma_commit(&bars[B_S0 + c]);
           issued = true;
         }
@@ -311,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c = 1 - g, nk = c == 0 ? nk0 : nk1;
             const uint32_t a = smem_u32(Vt(s, c));
             const uint32_t b = smem_u32(MASK == MASK_LIT ? Kt(c) : KWt(c));
-            for (int k = 0; k < nk; ++k)
-              mma_bf16(tbase + T_O + 80 * g, mnmaj(a, k, ones - (a + 2048 * k)), mnmaj(b, k, 0), idUT,
-                       k > 0 ? 1u : 0u);
+            uint64_t da = mnmaj(a, 0, ones - a), db = mnmaj(b, 0, 0);
+            for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
+              mma_bf16(tbase + T_O + 80 * g, da, db, idUT, k > 0 ? 1u : 0u);
             mma_commit(&bars[B_U0 + g]);
           }
           if (!ok) break;
@@ -327,13 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int nk = c == 0 ? nk0 : nk1;
           const uint32_t v = smem_u32(Vt(s, c));
-          for (int k = 0; k < nk; ++k)
-            mma_tmem_a(tbase + T_O + 80 * c, tbase + T_S + 128 * c + 8 * k, mnmaj(v, k, ones - (v + 2048 * k)),
-                       idPV, k > 0 ? 1u : 0u);
+          uint64_t dv = mnmaj(v, 0, ones - v);
+          for (int k = 0; k < nk; ++k, dv += kMnmajOnesStep)
+            mma_tmem_a(tbase + T_O + 80 * c, tbase + T_S + 128 * c + 8 * k, dv, idPV, k > 0 ? 1u : 0u);
           if (states) {
+            uint64_t dq = kmaj(Qt(s, c), 0), dx = kmaj(STt(c), 0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16(tbase + T_O + 80 * c, kmaj(Qt(s, c), k), kmaj(STt(c), k), idQX, 1u);
+            for (int k = 0; k < 4; ++k, dq += kKmajStep, dx += kKmajStep)
+              mma_bf16(tbase + T_O + 80 * c, dq, dx, idQX, 1u);
           }
           mma_commit(&bars[B_O0 + c]);
         }

@@ -79,7 +79,8 @@ constexpr int OFF_SLOT = 0;                           // [2] slots
 constexpr int OFF_KW = OFF_SLOT + 2 * kSlotBytes;     // weighted phi(K)
 constexpr int OFF_XF = OFF_KW + kTile;                // X_F operand tile
 constexpr int OFF_ONES = OFF_XF + kStTile;            // 16 rows, column 0 = 1
-constexpr int OFF_GSEG = OFF_ONES + 2048;             // the segment's entering backward state (fp32 [64][80])
+constexpr int OFF_STG = OFF_ONES + 2048;              // [8 epi warps] 4 KB output staging
+constexpr int OFF_GSEG = OFF_STG + kEpiWarps * 4096;  // the segment's entering backward state (fp32 [64][80])
 constexpr int OFF_FAC = OFF_GSEG + kGsegBytes;        // [slot] alpha, rho, a, b, p [128] each
 constexpr int OFF_INFO = OFF_FAC + 2 * 5 * kC * 4;    // [slot] float[8] per-chunk scalars
 constexpr int OFF_RED = OFF_INFO + 2 * 8 * 4;         // [parity] float[32] prep scan scratch
@@ -89,6 +90,7 @@ constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kSlotBytes % 1024 == 0 && OFF_KW % 1024 == 0 && OFF_XF % 1024 == 0 && OFF_ONES % 1024 == 0 &&
+                  OFF_STG % 1024 == 0 &&
                   (3 * kTile) % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(kGstBytes <= kSlotG && kGstBytes % 16 == 0 && kGsegBytes % 16 == 0, "bulk copies");
@@ -106,31 +108,30 @@ enum {
   B_U = 6,       // MMA commit: U^T done
   B_PVD = 7,     // MMA commit: P [V | 1] done (S's columns free)
   B_O = 8,       // MMA commit: O, T, R done
-  B_KE0 = 9,     // + slot: MMA commit: K tile of the slot read
+  B_KE0 = 9,     // + slot: MMA commit: every MMA of the step read the slot (Q, K, V, X_G)
   B_KWE = 11,    // MMA commit: weighted phi(K) read
   B_XF = 12,     // epi: X_F written (8 arrivals)
   B_XG = 13,     // prep: X_G written (16 arrivals)
   B_CU = 14,     // epi: carried state advanced, U^T read (8 arrivals)
   B_PM = 15,     // epi: P written (8 arrivals)
   B_ED = 16,     // epi: O, T, R read (8 arrivals)
-  B_QVE0 = 17,   // + slot: epi: output stores have read the slot's Q and V tiles (8 arrivals)
   B_DRAIN = 19,  // MMA commit used when unwinding
   B_GF = 20,     // prep: the item's last X_G written, the segment state may be replaced (16 arrivals)
   B_TD = 21,     // MMA commit: T done (X_F read)
 };
 __device__ __forceinline__ uint32_t bar_count(int b) {
   if (b == B_KVR || b == B_QR || b == B_XG || b == B_GF) return kPrepWarps;
-  if (b == B_XF || b == B_CU || b == B_PM || b == B_ED || b == B_QVE0 || b == B_QVE0 + 1) return kEpiWarps;
+  if (b == B_XF || b == B_CU || b == B_PM || b == B_ED) return kEpiWarps;
   return 1;
 }
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t T_S = 0, T_O = 128, T_T = 208, T_R = 288, T_F = 368, T_U = 432;
-// P (fp16, two per column) over S: each of the two epi warps of a lane
-// quarter packs its own half of the keys into the start of its own half of
-// S's columns, so neither overwrites columns the other has still to read
-// (keys 16j..16j+15 at columns 8j, or 32 + 8j for the second half).
-__host__ __device__ constexpr uint32_t p_col(int j) { return 8u * j + (j >= 4 ? 32u : 0u); }
+// P (fp16, two per column) over S: keys 16j..16j+15 are packed into the
+// first 8 of the 16 columns that held their scores, which the warp writing
+// them has just read, so any split of the key blocks between the two epi
+// warps of a lane quarter is safe.  The split is by parity of the block, so
+// that each warp takes one of its quarter's two diagonal blocks.
 
 struct LongParams {
   const float* log_lambda;
@@ -277,8 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           progress = true;
         }
         const int s = n & 1;
-        if (ld.valid(prm) && (n < 2 || (mbar_try_wait(&bars[B_KE0 + s], ((n >> 1) - 1) & 1) &&
-                                        mbar_try_wait(&bars[B_QVE0 + s], ((n >> 1) - 1) & 1)))) {
+        if (ld.valid(prm) && (n < 2 || mbar_try_wait(&bars[B_KE0 + s], ((n >> 1) - 1) & 1))) {
           const int bh = ld.item / prm.nseg;
           mbar_arrive_expect_tx(&bars[B_LD0 + s], (uint32_t)(3 * kTile + kGstBytes));
           tma_load_3d(Vt(s), &mapV, &bars[B_LD0 + s], 0, kC * ld.c, bh);
@@ -288,6 +288,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++issued_ld[s];
           ++n;
           ld.next(prm);
+          {
+            // the step after next waits for this slot's successor: start its
+            // tiles towards L2 now
+            Step pf = ld;
+            pf.next(prm);
+            if (pf.valid(prm)) {
+              const int bhp = pf.item / prm.nseg;
+              tma_prefetch_3d(&mapV, 0, kC * pf.c, bhp);
+              tma_prefetch_3d(&mapK, 0, kC * pf.c, bhp);
+              tma_prefetch_3d(&mapQ, 0, kC * pf.c, bhp);
+            }
+          }
           progress = true;
         }
         if (progress) {
@@ -322,7 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t idS = idesc_f16(128, 16 * nk, false, false);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_S, kmaj(Qt(s), k), kmaj(Kt(s), k), idS, k > 0 ? 1u : 0u);
+        {
+          uint64_t da = kmaj(Qt(s), 0), db = kmaj(Kt(s), 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k, da += kKmajStep, db += kKmajStep)
+            mma_bf16(tbase + T_S, da, db, idS, k > 0 ? 1u : 0u);
+        }
         mma_commit(&bars[B_S]);
         issued = true;
         if (n >= 1 && !waitb(B_CU, (n - 1) & 1)) break;    // U^T of the previous chunk read
@@ -330,32 +347,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint32_t a = smem_u32(Vt(s));
           const uint32_t b = smem_u32(MASK == MASK_LIT ? Kt(s) : KWt);
-          for (int k = 0; k < nk; ++k)
-            mma_bf16(tbase + T_U, mnmaj(a, k, ones - (a + 2048 * k)), mnmaj(b, k, 0), idUT, k > 0 ? 1u : 0u);
+          uint64_t da = mnmaj(a, 0, ones - a), db = mnmaj(b, 0, 0);
+          for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
+            mma_bf16(tbase + T_U, da, db, idUT, k > 0 ? 1u : 0u);
         }
         mma_commit(&bars[B_U]);
         mma_commit(&bars[B_KWE]);
-        mma_commit(&bars[B_KE0 + s]);
         if (n >= 1 && !waitb(B_ED, (n - 1) & 1)) break;    // O, T, R of the previous chunk read
         if (!waitb(B_XF, n & 1)) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_T, kmaj(Qt(s), k), kmaj(XFt, k), idX, k > 0 ? 1u : 0u);
+        {
+          uint64_t da = kmaj(Qt(s), 0), db = kmaj(XFt, 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k, da += kKmajStep, db += kKmajStep)
+            mma_bf16(tbase + T_T, da, db, idX, k > 0 ? 1u : 0u);
+        }
         mma_commit(&bars[B_TD]);
         if (!waitb(B_XG, n & 1)) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mma_bf16(tbase + T_R, kmaj(Qt(s), k), kmaj(Gt(s), k), idX, k > 0 ? 1u : 0u);
+        {
+          uint64_t da = kmaj(Qt(s), 0), db = kmaj(Gt(s), 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k, da += kKmajStep, db += kKmajStep)
+            mma_bf16(tbase + T_R, da, db, idX, k > 0 ? 1u : 0u);
+        }
         if (!waitb(B_PM, n & 1)) break;
         tc_fence_after();
         {
           const uint32_t v = smem_u32(Vt(s));
-          for (int k = 0; k < nk; ++k)
-            mma_tmem_a(tbase + T_O, tbase + T_S + p_col(k), mnmaj(v, k, ones - (v + 2048 * k)), idPV,
-                       k > 0 ? 1u : 0u);
+          uint64_t dv = mnmaj(v, 0, ones - v);
+          for (int k = 0; k < nk; ++k, dv += kMnmajOnesStep)
+            mma_tmem_a(tbase + T_O, tbase + T_S + 16 * k, dv, idPV, k > 0 ? 1u : 0u);
         }
         mma_commit(&bars[B_PVD]);
         mma_commit(&bars[B_O]);
+        mma_commit(&bars[B_KE0 + s]);
       }
       if (*s_abort && issued) {
         mma_commit(&bars[B_DRAIN]);
@@ -409,6 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pt == 0) rd[16] = ell;
       good = bar_and(1, kPrepWarps * 32, good);
       if (!good) break;
+      {
+        // the next step's decays, loaded a whole step ahead of their use
+        Step nx = st;
+        nx.next(prm);
+        if (nx.valid(prm)) load_ell(nx, &ell_next, &lnext_next);
+      }
       float pre = 0.f;
       for (int w = 0; w < pw; ++w) pre += rd[w];
       float T = 0.f;
@@ -532,7 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last) mbar_arrive(&bars[B_GF]);   // done with this segment's state
       }
       st.next(prm);
-      if (st.valid(prm)) load_ell(st, &ell_next, &lnext_next);
     }
   } else {
     // =========================== epi: two warps per TMEM lane quarter =============
@@ -595,34 +628,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!good) break;
         write_xf();
       }
-      // ---- P = S * M, fp16, into the first 64 columns of S (this warp's column half)
+      // ---- P = S * M, fp16, over S (this warp's key blocks: those of parity hc)
       if (!waitb(B_S, n & 1)) good = false;
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
-      if (good && warp_ok && 4 * hc < nk) {
+      // this step's scalars, read now: once its output product is done the
+      // slot (and with it these factors) may be refilled for step n + 2
+      const float dec = MASK == MASK_LIT ? 1.f : __expf(info(s)[I_T]);
+      const float a_out = f[2 * kC + i], b_out = f[3 * kC + i];
+      if (good && warp_ok && hc < nk) {
         const bool exact = info(s)[I_EXACT] != 0.f;
         const float ai = alpha[i], ri = rho[i], pi = pp[i];
         const uint32_t sa = tbase + lane_off + T_S;
-        const int jend = min(nk, 4 * hc + 4);
         float sb0[16], sb1[16];
 #pragma unroll 1
-        for (int jj = 4 * hc; jj < jend; jj += 2) {
+        for (int jj = hc; jj < nk; jj += 4) {
           uint32_t pk[8];
-          const bool has1 = jj + 1 < jend;
+          const bool has1 = jj + 2 < nk;
           tmem_ld16(sa + 16 * jj, sb0);
-          if (has1) tmem_ld16(sa + 16 * (jj + 1), sb1);
+          if (has1) tmem_ld16(sa + 16 * (jj + 2), sb1);
           tmem_wait_ld();
           reg_fence16(sb0);
           reg_fence16(sb1);
           mask_block<MASK>(sb0, 16 * jj, i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
 #pragma unroll
           for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb0[2 * e], sb0[2 * e + 1]);
-          tmem_st8(sa + p_col(jj), pk);
+          tmem_st8(sa + 16 * jj, pk);
           if (has1) {
-            mask_block<MASK>(sb1, 16 * (jj + 1), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
+            mask_block<MASK>(sb1, 16 * (jj + 2), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb1[2 * e], sb1[2 * e + 1]);
-            tmem_st8(sa + p_col(jj + 1), pk);
+            tmem_st8(sa + 16 * (jj + 2), pk);
           }
         }
       }
@@ -638,7 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
       if (good && q < 3) {
-        const float dec = MASK == MASK_LIT ? 1.f : __expf(info(s)[I_T]);
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
           float fv[16], uv[16];
@@ -666,34 +701,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ---- y = (O + a T + b R)[0:64] / (O + a T + b R)[64], this warp's 32
-      //      columns, staged (128-byte swizzle) in its 4 KB of the slot's
-      //      spent Q (first half) or V (second half) tile, written by TMA
+      //      columns, staged (128-byte swizzle) in its own 4 KB once its
+      //      previous store has read them, written by TMA
       if (!waitb(B_O, n & 1)) good = false;
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
       if (good && warp_ok) {
-        const float ai = f[2 * kC + i], bi = f[3 * kC + i];
-        const float2 a2 = make_float2(ai, ai), b2 = make_float2(bi, bi);
+        const float2 a2 = make_float2(a_out, a_out), b2 = make_float2(b_out, b_out);
         const uint32_t base = tbase + lane_off;
-        uint8_t* stg = (hc == 0 ? Qt(s) : Vt(s)) + 32 * q * 128;
+        uint8_t* stg = smem + OFF_STG + ew * 4096;
         uint8_t* row = stg + lane * 128;
         float o[16], tt[16], rr[16];
-        tmem_ld16(base + T_O + 64, o);
-        tmem_ld16(base + T_T + 64, tt);
-        tmem_ld16(base + T_R + 64, rr);
-        tmem_wait_ld();
-        reg_fence16(o);
-        reg_fence16(tt);
-        reg_fence16(rr);
-        const float inv = 1.f / (o[0] + ai * tt[0] + bi * rr[0]);
-        const float2 inv2 = make_float2(inv, inv);
+        float2 inv2 = make_float2(0.f, 0.f);
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
           const int col = 32 * hc + 16 * h2;
           tmem_ld16(base + T_O + col, o);
           tmem_ld16(base + T_T + col, tt);
           tmem_ld16(base + T_R + col, rr);
-          tmem_wait_ld();
+          if (h2 == 0) {
+            // column 64, the row sums, with the first block
+            float z[3];
+            z[0] = tmem_ld1(base + T_O + 64);
+            z[1] = tmem_ld1(base + T_T + 64);
+            z[2] = tmem_ld1(base + T_R + 64);
+            tmem_wait_ld();
+            asm volatile("" : "+f"(z[0]), "+f"(z[1]), "+f"(z[2]));
+            const float inv = 1.f / (z[0] + a_out * z[1] + b_out * z[2]);
+            inv2 = make_float2(inv, inv);
+          } else {
+            tmem_wait_ld();
+          }
           reg_fence16(o);
           reg_fence16(tt);
           reg_fence16(rr);
@@ -718,11 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[B_ED]);
-        bulk_wait_read();
-        mbar_arrive(&bars[B_QVE0 + s]);
-      }
+      if (lane == 0) mbar_arrive(&bars[B_ED]);
       st.next(prm);
     }
     if (lane == 0) bulk_wait_all();

@@ -210,6 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++issued[s];
           ++n;
           ld.next(prm);
+          {
+            // the step after next waits for this slot's successor: start its
+            // tiles towards L2 now
+            Step pf = ld;
+            pf.next(prm);
+            if (pf.valid(prm)) {
+              tma_prefetch_3d(&mapK, 0, kC * pf.c, pf.item / prm.nseg);
+              tma_prefetch_3d(&mapV, 0, kC * pf.c, pf.item / prm.nseg);
+            }
+          }
           idle0 = clock64();
         } else {
           __nanosleep(64);
@@ -240,11 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a = smem_u32(Vt(s));
         const uint32_t bb = smem_u32(MASK == MASK_LIT ? Kt(s) : KBt);
         const uint32_t bf = smem_u32(MASK == MASK_LIT ? Kt(s) : KFt);
-        for (int k = 0; k < nk; ++k)
-          mma_bf16(tbase + T_U, mnmaj(a, k, ones - (a + 2048 * k)), mnmaj(bb, k, 0), idUT, k > 0 ? 1u : 0u);
-        for (int k = 0; k < nk; ++k)
-          mma_bf16(tbase + T_FA, mnmaj(a, k, ones - (a + 2048 * k)), mnmaj(bf, k, 0), idUT,
-                   (k > 0 || !first) ? 1u : 0u);
+        const uint64_t da0 = mnmaj(a, 0, ones - a);
+        uint64_t da = da0, db = mnmaj(bb, 0, 0);
+        for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
+          mma_bf16(tbase + T_U, da, db, idUT, k > 0 ? 1u : 0u);
+        da = da0;
+        db = mnmaj(bf, 0, 0);
+        for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
+          mma_bf16(tbase + T_FA, da, db, idUT, (k > 0 || !first) ? 1u : 0u);
         mma_commit(&bars[B_U]);
         mma_commit(&bars[B_KWE]);
         mma_commit(&bars[B_KVE0 + s]);
@@ -292,6 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pt == 0) rd[16] = ell;
       good = bar_and(1, kPrepWarps * 32, good);
       if (!good) break;
+      {
+        // the next step's decays, loaded a whole step ahead of their use
+        Step nx = st;
+        nx.next(prm);
+        if (nx.valid(prm)) load_ell(nx, &ell_next, &lnext_next);
+      }
       float pre = 0.f;
       for (int w = 0; w < pw; ++w) pre += rd[w];
       float T = 0.f;
@@ -364,7 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[B_KVR]);
       D += T;
       st.next(prm);
-      if (st.valid(prm)) load_ell(st, &ell_next, &lnext_next);
     }
   } else {
     // =========================== epi: two warps per TMEM lane quarter =============
