@@ -52,13 +52,13 @@ TRAFFIC_PER_HEAD = {
     # chunk-64 kernel, ViT-B shape at B=128, LION-S: 160.7 MB / 1536 heads
     ("fc4be66a869d6463b1ad06b8b0948a689343c3e6648cdb380430aac91fcace8c", "vit_b", "s", 64):
         (117664768 + 43027200) / 1536,
-    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 154.5 MB / 1536 heads
-    ("6693686b17732376e16c6633cd5a38da8782169cbf771b1894f7f78eaa7b640c", "vit_b", "s", 128):
-        (117491712 + 37051648) / 1536,
+    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 154.2 MB / 1536 heads
+    ("cd7374c887e34b93d59863825085e6318b533036691eec3187d21c51d5ee0c8b", "vit_b", "s", 128):
+        (117489408 + 36713728) / 1536,
     # chunk-128 main pass for long sequences, L=24337 (B=2, H=12), LION-S:
-    # 387.8 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
-    ("81c6b55ae02d78fac6e46083f9ea1ef872d35a3a898b5c1c394ec238906b64d0", "hires_2496", "s", 128):
-        (271664896 + 116118528) / 24,
+    # 386.1 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
+    ("d0529b6a1e41d23db5587530f8467479ac0c1f5de05919565d16e6064169c60f", "hires_2496", "s", 128):
+        (271412992 + 114661376) / 24,
 }
 
 
