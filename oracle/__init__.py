@@ -68,9 +68,10 @@ def _load():
         lib.oracle_row_kappa.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, i, i, i, dp]
         lib.oracle_threads.argtypes = [i]
         lib.oracle_rnn_forward_half.argtypes = form + [dp, dp]
+        lib.oracle_lion_full_bwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, dp, dp, dp, i]
         for f in (lib.oracle_phi, lib.oracle_mask, lib.oracle_lion_full, lib.oracle_lion_rnn,
                   lib.oracle_lion_chunk, lib.oracle_lion_rows, lib.oracle_row_kappa,
-                  lib.oracle_threads, lib.oracle_rnn_forward_half):
+                  lib.oracle_threads, lib.oracle_rnn_forward_half, lib.oracle_lion_full_bwd):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -149,6 +150,26 @@ def rnn(q, k, v, log_lambda, mask_kind, phi_kind=PHI_DEFAULT, threads=1):
 def chunk(q, k, v, log_lambda, mask_kind, chunk, phi_kind=PHI_DEFAULT, threads=1):
     return _run(_load().oracle_lion_chunk, q, k, v, log_lambda, mask_kind, phi_kind,
                 extra_before_y=(int(chunk),), threads=threads)
+
+
+def full_bwd(q, k, v, log_lambda, dy, mask_kind, phi_kind=PHI_DEFAULT, threads=1):
+    """Gradients of sum(dy * y) for the full form: ``(dq, dk, dv, dlog_lambda)``.
+    ``dlog_lambda`` is None for LIT, [H] for D (summed over batch and
+    positions), [B, H, L] for S (position 0 never enters the mask: 0)."""
+    q, k, v, ll = _prep(q, k, v, log_lambda)
+    B, H, L, d = q.shape
+    _check_ll(mask_kind, ll, B, H, L)
+    dy = _f64(dy)
+    if dy.shape != q.shape:
+        raise ValueError("dy must have the shape of q")
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    dll = None if mask_kind == MASK_LIT else np.empty((H,) if mask_kind == MASK_D else (B, H, L))
+    rc = _load().oracle_lion_full_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(ll), _ptr(dy), B, H, L, d,
+                                      mask_kind, phi_kind, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dll),
+                                      threads)
+    if rc:
+        raise ValueError(f"oracle_lion_full_bwd failed ({rc})")
+    return dq, dk, dv, dll
 
 
 def rnn_forward_half(q, k, v, log_lambda, mask_kind, phi_kind=PHI_DEFAULT):

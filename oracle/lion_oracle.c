@@ -222,6 +222,160 @@ int oracle_lion_full(const double* q, const double* k, const double* v,
   return err;
 }
 
+/* ------------------------------------------------ full-form backward -- */
+
+/* d phi / d x applied to an upstream gradient dphi of one row (the chain rule
+ * written out from each feature map's definition):
+ *   elu+1     phi = x + 1 (x > 0), e^x otherwise: dx = dphi or e^x dphi;
+ *   SiLU, L2  u = x sigmoid(x), phi = u / max(|u|, 1e-12):
+ *             du = (dphi - phi (phi . dphi)) / |u| when |u| >= 1e-12, else
+ *             dphi / 1e-12; dx = du sigmoid(x) (1 + x (1 - sigmoid(x)));
+ *   identity  dx = dphi. */
+static void phi_row_bwd(int phi, const double* x, const double* dphi, int d, double* dx) {
+  if (phi == ORC_PHI_ELU1) {
+    for (int m = 0; m < d; ++m) dx[m] = x[m] > 0.0 ? dphi[m] : exp(x[m]) * dphi[m];
+  } else if (phi == ORC_PHI_SILU_L2) {
+    double ss = 0.0;
+    for (int m = 0; m < d; ++m) {
+      double u = x[m] / (1.0 + exp(-x[m]));
+      ss += u * u;
+    }
+    double nrm = sqrt(ss);
+    if (nrm >= 1e-12) {
+      double dot = 0.0;
+      for (int m = 0; m < d; ++m) dot += (x[m] / (1.0 + exp(-x[m]))) / nrm * dphi[m];
+      for (int m = 0; m < d; ++m) {
+        double sg = 1.0 / (1.0 + exp(-x[m]));
+        double fm = x[m] * sg / nrm;
+        double du = (dphi[m] - fm * dot) / nrm;
+        dx[m] = du * sg * (1.0 + x[m] * (1.0 - sg));
+      }
+    } else {
+      for (int m = 0; m < d; ++m) {
+        double sg = 1.0 / (1.0 + exp(-x[m]));
+        dx[m] = dphi[m] / 1e-12 * sg * (1.0 + x[m] * (1.0 - sg));
+      }
+    }
+  } else {
+    for (int m = 0; m < d; ++m) dx[m] = dphi[m];
+  }
+}
+
+/* Gradients of a scalar loss through y = SCALE((phi(Q) phi(K)^T (.) M) V)
+ * for one head, given dy = dLoss/dy.  With A_ij = M_ij s_ij, num_i =
+ * sum_j A_ij v_j, den_i = sum_j A_ij and y_i = num_i / den_i:
+ *   dnum_i = dy_i / den_i,  dden_i = -(dy_i . y_i) / den_i,
+ *   dA_ij = dnum_i . v_j + dden_i,
+ *   dv_j = sum_i A_ij dnum_i,
+ *   dphi(q_i) = sum_j M_ij dA_ij phi(k_j),  dphi(k_j) = sum_i M_ij dA_ij phi(q_i),
+ *   and, since M_ij = exp(sum of l_u over u in (min(i,j), max(i,j)]),
+ *   dl_u = sum over the pairs (i, j) whose interval holds u of A_ij dA_ij.
+ * l_0 never enters M, so dl_0 = 0. */
+static void full_head_bwd(const double* q, const double* k, const double* v,
+                          const double* l, const double* dy, int L, int d, int phi,
+                          double* dq, double* dk, double* dv, double* dl,
+                          double* fq, double* fk, double* M, double* y, double* g,
+                          double* hh, double* dfq, double* dfk) {
+  for (int t = 0; t < L; ++t) {
+    phi_row(phi, q + (long)t * d, d, fq + (long)t * d);
+    phi_row(phi, k + (long)t * d, d, fk + (long)t * d);
+  }
+  mask_of_head(l, L, M);
+  for (int i = 0; i < L; ++i) {
+    double den = 0.0;
+    for (int n = 0; n < d; ++n) y[(long)i * d + n] = 0.0;
+    for (int j = 0; j < L; ++j) {
+      double s = 0.0;
+      for (int m = 0; m < d; ++m) s += fq[(long)i * d + m] * fk[(long)j * d + m];
+      double a = M[(long)i * L + j] * s;
+      den += a;
+      for (int n = 0; n < d; ++n) y[(long)i * d + n] += a * v[(long)j * d + n];
+    }
+    double dyy = 0.0;
+    for (int n = 0; n < d; ++n) {
+      y[(long)i * d + n] /= den;
+      dyy += dy[(long)i * d + n] * y[(long)i * d + n];
+    }
+    for (int n = 0; n < d; ++n) g[(long)i * d + n] = dy[(long)i * d + n] / den;
+    hh[i] = -dyy / den;
+  }
+  for (long t = 0; t < (long)L * d; ++t) dv[t] = dfq[t] = dfk[t] = 0.0;
+  for (int u = 0; u < L; ++u) dl[u] = 0.0;
+  for (int i = 0; i < L; ++i) {
+    for (int j = 0; j < L; ++j) {
+      double s = 0.0, gv = 0.0;
+      for (int m = 0; m < d; ++m) s += fq[(long)i * d + m] * fk[(long)j * d + m];
+      for (int n = 0; n < d; ++n) gv += g[(long)i * d + n] * v[(long)j * d + n];
+      double mij = M[(long)i * L + j];
+      double a = mij * s;
+      double da = gv + hh[i];
+      for (int n = 0; n < d; ++n) dv[(long)j * d + n] += a * g[(long)i * d + n];
+      double ds = mij * da;
+      for (int m = 0; m < d; ++m) {
+        dfq[(long)i * d + m] += ds * fk[(long)j * d + m];
+        dfk[(long)j * d + m] += ds * fq[(long)i * d + m];
+      }
+      int lo = i < j ? i : j, hi = i < j ? j : i;
+      for (int u = lo + 1; u <= hi; ++u) dl[u] += a * da;
+    }
+  }
+  for (int t = 0; t < L; ++t) {
+    phi_row_bwd(phi, q + (long)t * d, dfq + (long)t * d, d, dq + (long)t * d);
+    phi_row_bwd(phi, k + (long)t * d, dfk + (long)t * d, d, dk + (long)t * d);
+  }
+}
+
+/* Full-form backward over all heads.  dy, dq, dk, dv: [B][H][L][d].
+ * dlog_lambda: LIT ignored (may be NULL); D [H] (summed over batch and
+ * positions: every position of head h carries the same log lambda_h);
+ * S [B][H][L]. */
+int oracle_lion_full_bwd(const double* q, const double* k, const double* v,
+                         const double* log_lambda, const double* dy, int B, int H,
+                         int L, int d, int mask_kind, int phi_kind, double* dq,
+                         double* dk, double* dv, double* dlog_lambda, int nthreads) {
+  if (check_args(q, k, v, log_lambda, B, H, L, d, mask_kind, phi_kind, dq)) return 1;
+  if (!dy || !dk || !dv) return 1;
+  if (mask_kind != ORC_MASK_LIT && !dlog_lambda) return 1;
+  int phi = resolve_phi(mask_kind, phi_kind);
+  int nt = set_threads(nthreads);
+  int err = 0;
+  long heads = (long)B * H;
+  double* dl_all = (double*)malloc(sizeof(double) * (size_t)heads * L);
+  if (!dl_all) return 2;
+#pragma omp parallel for schedule(dynamic) num_threads(nt) reduction(| : err)
+  for (long bh = 0; bh < heads; ++bh) {
+    int b = (int)(bh / H), h = (int)(bh % H);
+    size_t Ld = (size_t)L * d;
+    double* l = (double*)malloc(sizeof(double) * L);
+    double* fq = (double*)malloc(sizeof(double) * Ld);
+    double* fk = (double*)malloc(sizeof(double) * Ld);
+    double* M = (double*)malloc(sizeof(double) * (size_t)L * L);
+    double* y = (double*)malloc(sizeof(double) * Ld);
+    double* g = (double*)malloc(sizeof(double) * Ld);
+    double* hh = (double*)malloc(sizeof(double) * L);
+    double* dfq = (double*)malloc(sizeof(double) * Ld);
+    double* dfk = (double*)malloc(sizeof(double) * Ld);
+    if (!l || !fq || !fk || !M || !y || !g || !hh || !dfq || !dfk) {
+      err |= 2;
+    } else {
+      long off = bh * (long)Ld;
+      head_log_lambda(mask_kind, log_lambda, b, h, H, L, l);
+      full_head_bwd(q + off, k + off, v + off, l, dy + off, L, d, phi, dq + off, dk + off,
+                    dv + off, dl_all + bh * L, fq, fk, M, y, g, hh, dfq, dfk);
+    }
+    free(l); free(fq); free(fk); free(M); free(y); free(g); free(hh); free(dfq); free(dfk);
+  }
+  if (!err && mask_kind == ORC_MASK_S) {
+    memcpy(dlog_lambda, dl_all, sizeof(double) * (size_t)heads * L);
+  } else if (!err && mask_kind == ORC_MASK_D) {
+    for (int h = 0; h < H; ++h) dlog_lambda[h] = 0.0;
+    for (long bh = 0; bh < heads; ++bh)
+      for (int u = 0; u < L; ++u) dlog_lambda[bh % H] += dl_all[bh * L + u];
+  }
+  free(dl_all);
+  return err;
+}
+
 /* -------------------------------------------------------- RNN form ----- */
 
 /* Forward recurrence S^F_i = lambda_i S^F_{i-1} + phi(k_i) v_i^T,

@@ -332,3 +332,81 @@ def test_invalid_arguments(oracle_mod):
         o.full(q, q, q, None, 1)                      # LION-D without decays
     with pytest.raises(ValueError):
         o.chunk(q, q, q, None, 0, 0)                  # chunk < 1
+
+
+# ------------------------------------------------------ backward (full form) --
+# The gradients of sum(dy * y) with respect to q, k, v and log lambda: the
+# operator is the pages' training path (the full form trains like a
+# Transformer, rebuttal page reply "Concern 1", Theorem 3.3 Eq 25).
+
+def _fd_loss(oracle_mod, q, k, v, ll, dy, mask_kind, phi_kind):
+    return float((oracle_mod.full(q, k, v, ll, mask_kind, phi_kind) * dy).sum())
+
+
+@pytest.mark.parametrize("mask_kind", MASKS)
+@pytest.mark.parametrize("phi_kind", (1, 2, 3))
+def test_full_bwd_matches_finite_differences(oracle_mod, mask_kind, phi_kind):
+    """Every element of dq, dk, dv (and dlog_lambda) against central
+    differences of the forward oracle (step 1e-6, float64)."""
+    rng = np.random.default_rng(40 + 3 * mask_kind + phi_kind)
+    q, k, v, ll = _inputs(rng, 1, 2, 6, 4, mask_kind, lam_lo=0.5)
+    if phi_kind == 3:   # identity features: keep the row sums away from zero
+        q, k = np.abs(q) + 0.3, np.abs(k) + 0.3
+    dy = rng.standard_normal(q.shape)
+    dq, dk, dv, dll = oracle_mod.full_bwd(q, k, v, ll, dy, mask_kind, phi_kind)
+    eps = 1e-6
+    named = {"q": (q, dq), "k": (k, dk), "v": (v, dv)}
+    if ll is not None:
+        named["ll"] = (ll, dll)
+    for name, (arr, grad) in named.items():
+        for idx in np.ndindex(arr.shape):
+            args = {"q": q, "k": k, "v": v, "ll": ll}
+            a = arr.copy()
+            a[idx] += eps
+            args[name] = a
+            fp = _fd_loss(oracle_mod, args["q"], args["k"], args["v"], args["ll"], dy, mask_kind, phi_kind)
+            a[idx] -= 2 * eps
+            fm = _fd_loss(oracle_mod, args["q"], args["k"], args["v"], args["ll"], dy, mask_kind, phi_kind)
+            fd = (fp - fm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 2e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+    if mask_kind == 2:
+        assert np.all(dll[..., 0] == 0.0)   # l_0 never enters the mask
+
+
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_full_bwd_euler_identity_in_v(oracle_mod, mask_kind):
+    """y is homogeneous of degree 1 in v, so <dy, y> = <dv, v>."""
+    rng = np.random.default_rng(50 + mask_kind)
+    q, k, v, ll = _inputs(rng, 2, 2, 13, 5, mask_kind)
+    dy = rng.standard_normal(q.shape)
+    _, _, dv, _ = oracle_mod.full_bwd(q, k, v, ll, dy, mask_kind)
+    y = oracle_mod.full(q, k, v, ll, mask_kind)
+    assert abs((dy * y).sum() - (dv * v).sum()) <= 1e-10 * max(1.0, abs((dy * y).sum()))
+
+
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_full_bwd_query_scale_invariance(oracle_mod, mask_kind):
+    """With identity features y_i does not change when q_i is scaled, so the
+    gradient with respect to q_i is orthogonal to q_i."""
+    rng = np.random.default_rng(60 + mask_kind)
+    q, k, v, ll = _inputs(rng, 1, 3, 11, 6, mask_kind)
+    q, k = np.abs(q) + 0.2, np.abs(k) + 0.2
+    dy = rng.standard_normal(q.shape)
+    dq, _, _, _ = oracle_mod.full_bwd(q, k, v, ll, dy, mask_kind, 3)
+    dots = (dq * q).sum(-1)
+    assert np.abs(dots).max() <= 1e-10 * max(1.0, np.abs(dq).max() * np.abs(q).max())
+
+
+def test_full_bwd_d_is_the_sum_of_s(oracle_mod):
+    """LION-D is LION-S with every position carrying log lambda_h: its
+    gradient is the sum over batch and positions of the per-token ones, and
+    the other gradients coincide."""
+    rng = np.random.default_rng(70)
+    q, k, v, ll_d = _inputs(rng, 2, 3, 9, 4, 1)
+    ll_s = np.broadcast_to(ll_d[None, :, None], (2, 3, 9)).copy()
+    dy = rng.standard_normal(q.shape)
+    gd = oracle_mod.full_bwd(q, k, v, ll_d, dy, 1, 1)
+    gs = oracle_mod.full_bwd(q, k, v, ll_s, dy, 2, 1)
+    for a, b in zip(gd[:3], gs[:3]):
+        assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(a).max())
+    assert np.abs(gd[3] - gs[3].sum(axis=(0, 2))).max() <= 1e-10 * max(1.0, np.abs(gd[3]).max())
