@@ -34,6 +34,9 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20      # > 129 MB L2
 HIRES_CHUNK = 128               # chunk of the long-sequence tensor-core path
+# fp32 arithmetic peak of the CUDA cores, from unit counts and the clock:
+# 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2.07 GHz
+FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
 # kernel, per unit (head) from one ncu capture, keyed by the SHA-256 of that
@@ -276,6 +279,44 @@ def measure_e2e(w, inp, mask, chunk, form, steps, warmup):
     return ms, h2d, d2h
 
 
+def bwd_flops(w) -> int:
+    """Algorithmic flops of the gradients through the full form per call: the
+    six L x L x d products they need (S = phi(Q) phi(K)^T, the recomputed
+    A V, G V^T, dS phi(K), dS^T phi(Q), A^T G), 2 L^2 d flops each, per head."""
+    return 12 * w.B * w.H * w.L * w.L * w.d
+
+
+def measure_bwd(w, mask, steps, warmup, flush):
+    """CUDA-event time of one gradient call (lion_attn_bwd, all its kernels)
+    through the C entry point with preallocated outputs and workspace."""
+    import ctypes
+    inp = synth.make_inputs(w.B, w.H, w.L, w.d, mask, w.dtype, w.seed, w.lam)
+    dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
+    dy = torch.randn((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    grads = [torch.empty_like(dy) for _ in range(3)]
+    dll = None
+    if inp["mask"] == lion.MASK_D:
+        dll = torch.empty((w.H,), dtype=torch.float32, device="cuda")
+    elif inp["mask"] == lion.MASK_S:
+        dll = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device="cuda")
+    wsb = lion.bwd_workspace_bytes(w.B, w.H, w.L, w.d)
+    wsp = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    p = lambda t: None if t is None else t.data_ptr()
+    a = lion._BwdArgs(p(dev["q"]), p(dev["k"]), p(dev["v"]), p(dev["log_lambda"]), p(dy),
+                      p(grads[0]), p(grads[1]), p(grads[2]), p(dll), w.B, w.H, w.L, w.d,
+                      inp["mask"], lion.DTYPE_BF16 if w.dtype == "bf16" else lion.DTYPE_FP32,
+                      lion.PHI_DEFAULT, wsp.data_ptr(), wsb, stream.cuda_stream)
+    lib = lion.load()
+
+    def call():
+        st = lib.lion_attn_bwd(ctypes.byref(a))
+        if st:
+            raise RuntimeError(f"lion_attn_bwd failed ({st})")
+
+    return time_device(call, steps, warmup, flush, stream)
+
+
 def cpu_baseline(name, mask, chunk, budget_s=10.0):
     """The float64 oracle (chunk form, all host cores) on a bounded sample of
     the same workload: batch rows (all H heads each) in order, wrapping round
@@ -343,6 +384,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling captures)")
     args = ap.parse_args()
@@ -397,6 +439,19 @@ def main():
                                   "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak}}
         del _k2
 
+    backward = None
+    if not args.no_backward and w.L <= lion.FULL_MAX_L:
+        tb = measure_bwd(w, args.mask, 20, 3, flush)
+        msb = statistics.mean(tb)
+        fl = bwd_flops(w)
+        backward = {"form": "full", "value": w.B * w.L / (msb * 1e-3), "unit": "tokens/s", "ms_per_call": msb,
+                    "launches_per_call": 4 if args.mask != "d" else 5,
+                    "roofline": {"bound": "alu", "achieved": fl / (msb * 1e-3) / 1e12,
+                                 "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
+                                 "frac": fl / (msb * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
+                                 "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
+                                 "algorithmic_flops": fl}}
+
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(args.workload, args.mask, args.chunk)
@@ -417,6 +472,7 @@ def main():
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
             "secondary": secondary,
+            "backward": backward,
         }
         print(json.dumps(line))
     if dist is not None:

@@ -1,0 +1,503 @@
+// lion_bwd.cu -- gradients of the LION operator through its full form, on
+// the CUDA cores in fp32, for any d in {16, 32, 64, 128} and bfloat16 or
+// float32 inputs.
+//
+// Full form (rebuttal page "LION: A bidirectional framework that trains like
+// a Transformer and infers like an RNN", reply "Concern 1", Theorem 3.3
+// Eq 25): per head, with A_ij = M_ij s_ij, s_ij = phi(q_i) . phi(k_j),
+// num_i = sum_j A_ij v_j, den_i = sum_j A_ij and y_i = num_i / den_i.  Given
+// dy = dLoss/dy, with dnum_i = dy_i / den_i and dden_i = -(dy_i . y_i) / den_i:
+//   dA_ij     = dnum_i . v_j + dden_i
+//   dv_j      = sum_i A_ij dnum_i
+//   dphi(q_i) = sum_j M_ij dA_ij phi(k_j),   dphi(k_j) = sum_i M_ij dA_ij phi(q_i)
+// and, M_ij being exp(P_max(i,j) - P_min(i,j)) with P the inclusive prefix of
+// l = log(lambda), dLoss/dP_m = sum_{j<m} c_mj - sum_{i>m} c_im
+// + sum_{i<m} c_im - sum_{j>m} c_mj with c_ij = A_ij dA_ij, so that
+// dl_u = sum_{m >= u} dLoss/dP_m (l_0 never enters M: dl_0 = 0).  The
+// feature maps' derivatives follow by the chain rule.
+//
+// Kernels: (1) phi(q), phi(k) into the workspace; (2) one pass per block of
+// 32 query rows: y, dnum, dden (stored), then dphi(q), dq and the row terms
+// of dLoss/dP; (3) one pass per block of 32 key rows: dphi(k), dk, dv and the
+// column terms; (4) per head, dl (LION-S: suffix sums; LION-D: the sum over
+// positions, sum_m m dLoss/dP_m) in double, and for LION-D the sum over the
+// batch.  The mask value is generated per (i, j) as in the forward full form.
+#include "lion_common.cuh"
+#include "lion_internal.h"
+
+namespace lion {
+namespace {
+
+constexpr int kRows = 32;    // rows of a block (queries in pass 2, keys in pass 3)
+constexpr int kGroup = 8;    // threads per row
+constexpr int kTile = 32;    // tokens per staged tile of the other side
+
+template <typename T>
+__device__ __forceinline__ const T* head_of(const void* base, int bh, int L, int D) {
+  return reinterpret_cast<const T*>(base) + (size_t)bh * L * D;
+}
+
+__device__ __forceinline__ float group_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  return x;
+}
+
+// Inclusive prefix of l over the head into sP[0..L) (LION-S), whole block.
+__device__ void prefix_log_lambda(const float* ll, int L, float* sP, float* scratch) {
+  const int T = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int i = t; i < L; i += T) sP[i] = ll[i];
+  __syncthreads();
+  const int per = (L + T - 1) / T;
+  const int lo = min(L, t * per), hi = min(L, lo + per);
+  float run = 0.f;
+  for (int i = lo; i < hi; ++i) { run += sP[i]; sP[i] = run; }
+  float x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < (T >> 5) ? scratch[lane] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  const float excl = x - run + (warp > 0 ? scratch[warp - 1] : 0.f);
+  for (int i = lo; i < hi; ++i) sP[i] += excl;
+  __syncthreads();
+}
+
+// log M_ij for the head's decay kind.
+__device__ __forceinline__ float log_mask(int mask_kind, int i, int j, float lh, const float* sP) {
+  if (mask_kind == MASK_D) return fabsf((float)(i - j)) * lh;
+  if (mask_kind == MASK_S) return i >= j ? sP[i] - sP[j] : sP[j] - sP[i];
+  return 0.f;
+}
+
+// dphi -> dx for this thread's NC features of one row (features g + c*8),
+// the row's 8 threads cooperating on the SiLU + L2 norm.
+template <int NC>
+__device__ __forceinline__ void phi_backward(int phi, const float* x, const float* dphi, float* dx) {
+  if (phi == PHI_ELU1) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) dx[c] = x[c] > 0.f ? dphi[c] : expf(x[c]) * dphi[c];
+  } else if (phi == PHI_SILU_L2) {
+    float u[NC], sg[NC], ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      sg[c] = 1.f / (1.f + expf(-x[c]));
+      u[c] = x[c] * sg[c];
+      ss += u[c] * u[c];
+    }
+    const float nrm = sqrtf(group_sum(ss));
+    float dx_scale, dot = 0.f;
+    if (nrm >= 1e-12f) {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) dot += u[c] / nrm * dphi[c];
+      dot = group_sum(dot);
+      dx_scale = 1.f / nrm;
+    } else {
+      dx_scale = 1e12f;
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const float f = nrm >= 1e-12f ? u[c] / nrm : 0.f;
+      const float du = (dphi[c] - f * dot) * dx_scale;
+      dx[c] = du * sg[c] * (1.f + x[c] * (1.f - sg[c]));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) dx[c] = dphi[c];
+  }
+}
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* log_lambda;
+  const float* dy;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dll;
+  int B, H, L;
+  int mask_kind, phi;
+  // workspace
+  float* fq;     // [BH][L][D] phi(q)
+  float* fk;     // [BH][L][D] phi(k)
+  float* g;      // [BH][L][D] dnum
+  float* hd;     // [BH][L]    dden
+  float* rowd;   // [BH][L]    row terms of dLoss/dP
+  float* cold;   // [BH][L]    column terms of dLoss/dP
+  double* dsum;  // [BH]       LION-D: sum over positions of dl
+};
+
+// (1) phi(q), phi(k): one warp per row.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_phi_kernel(BwdParams p) {
+  const long warp = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long rows = (long)p.B * p.H * p.L;
+  if (warp >= 2 * rows) return;
+  const bool isq = warp < rows;
+  const long r = isq ? warp : warp - rows;
+  const T* src = reinterpret_cast<const T*>(isq ? p.q : p.k) + (size_t)r * D;
+  float* dst = (isq ? p.fq : p.fk) + (size_t)r * D;
+  constexpr int NL = (D + 31) / 32;
+  float x[NL];
+#pragma unroll
+  for (int c = 0; c < NL; ++c) {
+    const int m = lane + 32 * c;
+    x[c] = m < D ? to_f32(src[m]) : 0.f;
+  }
+  if (p.phi == PHI_ELU1) {
+#pragma unroll
+    for (int c = 0; c < NL; ++c) x[c] = elu1(x[c]);
+  } else if (p.phi == PHI_SILU_L2) {
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < NL; ++c) {
+      const int m = lane + 32 * c;
+      x[c] = m < D ? silu(x[c]) : 0.f;
+      ss += x[c] * x[c];
+    }
+    const float inv = 1.f / fmaxf(sqrtf(warp_sum(ss)), 1e-12f);
+#pragma unroll
+    for (int c = 0; c < NL; ++c) x[c] *= inv;
+  }
+#pragma unroll
+  for (int c = 0; c < NL; ++c) {
+    const int m = lane + 32 * c;
+    if (m < D) dst[m] = x[c];
+  }
+}
+
+__device__ __forceinline__ void load_tile(float* dst, int ld, const float* src, int row0, int rows, int L, int D) {
+  for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+    const int r = idx / D, m = idx - r * D, i = row0 + r;
+    dst[r * ld + m] = i < L ? src[(size_t)i * D + m] : 0.f;
+  }
+}
+template <typename T>
+__device__ __forceinline__ void load_tile_in(float* dst, int ld, const T* src, int row0, int rows, int L, int D) {
+  for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+    const int r = idx / D, m = idx - r * D, i = row0 + r;
+    dst[r * ld + m] = i < L ? to_f32(src[(size_t)i * D + m]) : 0.f;
+  }
+}
+
+// (2) rows: 32 queries per CTA, 8 threads per query.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_rows_kernel(BwdParams p) {
+  constexpr int LD = D + 8, NC = D / kGroup;
+  extern __shared__ float smem[];
+  float* sQ = smem;                   // [kRows][LD] phi(q)
+  float* sK = sQ + kRows * LD;        // [kTile][D]  phi(k)
+  float* sV = sK + kTile * D;         // [kTile][D]  v
+  float* sP = sV + kTile * D;         // [L] prefix (LION-S)
+  __shared__ float scratch[32];
+  const int L = p.L, bh = blockIdx.x, h = bh % p.H, i0 = blockIdx.y * kRows;
+  const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
+  if (p.mask_kind == MASK_S) prefix_log_lambda(p.log_lambda + (size_t)bh * L, L, sP, scratch);
+  load_tile(sQ, LD, p.fq + (size_t)bh * L * D, i0, kRows, L, D);
+  __syncthreads();
+  const int r = threadIdx.x / kGroup, g = threadIdx.x % kGroup, i0r = i0 + r;
+  const bool live = i0r < L;
+  // rows past L run on row L-1's mask values (in bounds) and store nothing;
+  // every thread takes part in its group's shuffles
+  const int i = live ? i0r : L - 1;
+  const T* vh = head_of<T>(p.v, bh, L, D);
+  // ---- pass A: y_i, then dnum_i and dden_i
+  float acc[NC], den = 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+  for (int j0 = 0; j0 < L; j0 += kTile) {
+    const int nj = min(kTile, L - j0);
+    load_tile(sK, D, p.fk + (size_t)bh * L * D, j0, kTile, L, D);
+    load_tile_in<T>(sV, D, vh, j0, kTile, L, D);
+    __syncthreads();
+    for (int jj = 0; jj < nj; ++jj) {
+      float s = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) s += sQ[r * LD + g + c * kGroup] * sK[jj * D + g + c * kGroup];
+      s = group_sum(s);
+      const float a = s * expf(log_mask(p.mask_kind, i, j0 + jj, lh, sP));
+      den += a;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) acc[c] += a * sV[jj * D + g + c * kGroup];
+    }
+    __syncthreads();
+  }
+  float gi[NC], hi = 0.f;
+  {
+    const float* dy = p.dy + ((size_t)bh * L + (live ? i : 0)) * D;
+    float dyy = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const float d = live ? dy[g + c * kGroup] : 0.f;
+      dyy += d * (acc[c] / den);
+      gi[c] = live ? d / den : 0.f;
+    }
+    const float gs = group_sum(dyy);
+    hi = live ? -gs / den : 0.f;
+    if (live) {
+      float* gw = p.g + ((size_t)bh * L + i) * D;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) gw[g + c * kGroup] = gi[c];
+      if (g == 0) p.hd[(size_t)bh * L + i] = hi;
+    }
+  }
+  // ---- pass B: dphi(q_i) and the row terms of dLoss/dP
+  float dfq[NC], rowl = 0.f, rowu = 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) dfq[c] = 0.f;
+  for (int j0 = 0; j0 < L; j0 += kTile) {
+    const int nj = min(kTile, L - j0);
+    load_tile(sK, D, p.fk + (size_t)bh * L * D, j0, kTile, L, D);
+    load_tile_in<T>(sV, D, vh, j0, kTile, L, D);
+    __syncthreads();
+    for (int jj = 0; jj < nj; ++jj) {
+      float s = 0.f, gv = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        s += sQ[r * LD + g + c * kGroup] * sK[jj * D + g + c * kGroup];
+        gv += gi[c] * sV[jj * D + g + c * kGroup];
+      }
+      s = group_sum(s);
+      gv = group_sum(gv);
+      const int j = j0 + jj;
+      const float m = expf(log_mask(p.mask_kind, i, j, lh, sP));
+      const float da = gv + hi, ds = m * da, cij = m * s * da;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) dfq[c] += ds * sK[jj * D + g + c * kGroup];
+      if (j < i) rowl += cij;
+      else if (j > i) rowu += cij;
+    }
+    __syncthreads();
+  }
+  {
+    const T* qr = head_of<T>(p.q, bh, L, D) + (size_t)i * D;
+    float x[NC], dx[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) x[c] = to_f32(qr[g + c * kGroup]);
+    phi_backward<NC>(p.phi, x, dfq, dx);   // gi = 0 on dead rows: dfq = 0
+    if (live) {
+      float* dq = p.dq + ((size_t)bh * L + i) * D;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) dq[g + c * kGroup] = dx[c];
+      if (g == 0) p.rowd[(size_t)bh * L + i] = rowl - rowu;
+    }
+  }
+}
+
+// (3) columns: 32 keys per CTA, 8 threads per key.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_cols_kernel(BwdParams p) {
+  constexpr int LD = D + 8, NC = D / kGroup;
+  extern __shared__ float smem[];
+  float* sK = smem;                   // [kRows][LD] phi(k) of this block's keys
+  float* sVc = sK + kRows * LD;       // [kRows][LD] v of this block's keys
+  float* sQ = sVc + kRows * LD;       // [kTile][D]  phi(q)
+  float* sG = sQ + kTile * D;         // [kTile][D]  dnum
+  float* sH = sG + kTile * D;         // [kTile]     dden
+  float* sP = sH + kTile;             // [L] prefix (LION-S)
+  __shared__ float scratch[32];
+  const int L = p.L, bh = blockIdx.x, h = bh % p.H, j0b = blockIdx.y * kRows;
+  const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
+  if (p.mask_kind == MASK_S) prefix_log_lambda(p.log_lambda + (size_t)bh * L, L, sP, scratch);
+  load_tile(sK, LD, p.fk + (size_t)bh * L * D, j0b, kRows, L, D);
+  load_tile_in<T>(sVc, LD, head_of<T>(p.v, bh, L, D), j0b, kRows, L, D);
+  __syncthreads();
+  const int r = threadIdx.x / kGroup, g = threadIdx.x % kGroup, j0r = j0b + r;
+  const bool live = j0r < L;
+  const int j = live ? j0r : L - 1;   // in-bounds mask values; stores only when live
+  float dfk[NC], dvj[NC], coll = 0.f, colu = 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) dfk[c] = dvj[c] = 0.f;
+  for (int i0 = 0; i0 < L; i0 += kTile) {
+    const int ni = min(kTile, L - i0);
+    load_tile(sQ, D, p.fq + (size_t)bh * L * D, i0, kTile, L, D);
+    load_tile(sG, D, p.g + (size_t)bh * L * D, i0, kTile, L, D);
+    for (int t = threadIdx.x; t < kTile; t += blockDim.x) sH[t] = i0 + t < L ? p.hd[(size_t)bh * L + i0 + t] : 0.f;
+    __syncthreads();
+    for (int ii = 0; ii < ni; ++ii) {
+      float s = 0.f, gv = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        s += sQ[ii * D + g + c * kGroup] * sK[r * LD + g + c * kGroup];
+        gv += sG[ii * D + g + c * kGroup] * sVc[r * LD + g + c * kGroup];
+      }
+      s = group_sum(s);
+      gv = group_sum(gv);
+      const int i = i0 + ii;
+      const float m = expf(log_mask(p.mask_kind, i, j, lh, sP));
+      const float a = m * s, da = gv + sH[ii], ds = m * da, cij = a * da;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        dfk[c] += ds * sQ[ii * D + g + c * kGroup];
+        dvj[c] += a * sG[ii * D + g + c * kGroup];
+      }
+      if (i > j) coll += cij;
+      else if (i < j) colu += cij;
+    }
+    __syncthreads();
+  }
+  {
+    const T* kr = head_of<T>(p.k, bh, L, D) + (size_t)j * D;
+    float x[NC], dx[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) x[c] = to_f32(kr[g + c * kGroup]);
+    phi_backward<NC>(p.phi, x, dfk, dx);
+    if (live) {
+      float* dk = p.dk + ((size_t)bh * L + j) * D;
+      float* dv = p.dv + ((size_t)bh * L + j) * D;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        dk[g + c * kGroup] = dx[c];
+        dv[g + c * kGroup] = dvj[c];
+      }
+      if (g == 0) p.cold[(size_t)bh * L + j] = colu - coll;
+    }
+  }
+}
+
+// (4) dl of one head (one CTA): dLoss/dP_m = rowd_m + cold_m; LION-S writes
+// the suffix sums (position 0: 0), LION-D the total sum_m m dLoss/dP_m.
+constexpr int kDlThreads = 256;
+__global__ void __launch_bounds__(kDlThreads) bwd_dl_kernel(BwdParams p) {
+  __shared__ double part[kDlThreads];
+  const int L = p.L, bh = blockIdx.x, t = threadIdx.x;
+  const float* rd = p.rowd + (size_t)bh * L;
+  const float* cd = p.cold + (size_t)bh * L;
+  const int per = (L + kDlThreads - 1) / kDlThreads;
+  const int lo = min(L, t * per), hi = min(L, lo + per);
+  if (p.mask_kind == MASK_D) {
+    double acc = 0.0;
+    for (int m = lo; m < hi; ++m) acc += (double)m * ((double)rd[m] + (double)cd[m]);
+    part[t] = acc;
+    __syncthreads();
+    for (int o = kDlThreads / 2; o > 0; o >>= 1) {
+      if (t < o) part[t] += part[t + o];
+      __syncthreads();
+    }
+    if (t == 0) p.dsum[bh] = part[0];
+    return;
+  }
+  // suffix sums: this thread's chunk total, then the totals of the chunks to its right
+  double run = 0.0;
+  for (int m = lo; m < hi; ++m) run += (double)rd[m] + (double)cd[m];
+  part[t] = run;
+  __syncthreads();
+  double right = 0.0;
+  for (int u = t + 1; u < kDlThreads; ++u) right += part[u];
+  float* out = p.dll + (size_t)bh * L;
+  for (int m = hi - 1; m >= lo; --m) {
+    right += (double)rd[m] + (double)cd[m];
+    out[m] = m == 0 ? 0.f : (float)right;
+  }
+}
+
+// LION-D: dlog_lambda[h] = sum over the batch of the per-head totals.
+__global__ void bwd_dl_heads_kernel(BwdParams p) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= p.H) return;
+  double acc = 0.0;
+  for (int b = 0; b < p.B; ++b) acc += p.dsum[(size_t)b * p.H + h];
+  p.dll[h] = (float)acc;
+}
+
+template <typename Kern>
+cudaError_t allow(Kern kern, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename T, int D>
+cudaError_t bwd_launch(const BwdParams& p, cudaStream_t s) {
+  const long rows = (long)p.B * p.H * p.L;
+  bwd_phi_kernel<T, D><<<(unsigned)((2 * rows * 32 + 255) / 256), 256, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t sp = p.mask_kind == MASK_S ? (size_t)p.L : 0;
+  const size_t smem_r = sizeof(float) * ((size_t)kRows * (D + 8) + 2 * kTile * D + sp);
+  const size_t smem_c = sizeof(float) * (2 * (size_t)kRows * (D + 8) + 2 * kTile * D + kTile + sp);
+  if ((e = allow(bwd_rows_kernel<T, D>, smem_r)) != cudaSuccess) return e;
+  if ((e = allow(bwd_cols_kernel<T, D>, smem_c)) != cudaSuccess) return e;
+  const dim3 grid(p.B * p.H, (p.L + kRows - 1) / kRows);
+  bwd_rows_kernel<T, D><<<grid, 256, smem_r, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_cols_kernel<T, D><<<grid, 256, smem_c, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.mask_kind != MASK_LIT) {
+    bwd_dl_kernel<<<p.B * p.H, kDlThreads, 0, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (p.mask_kind == MASK_D) {
+      bwd_dl_heads_kernel<<<(p.H + 127) / 128, 128, 0, s>>>(p);
+      e = cudaGetLastError();
+    }
+  }
+  return e;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int H, int L, int d) {
+  const size_t BH = (size_t)B * H, n = BH * L;
+  return 3 * align256(sizeof(float) * n * d) + 3 * align256(sizeof(float) * n) + align256(sizeof(double) * BH);
+}
+
+cudaError_t launch_bwd(const Problem& pr, const float* dy, float* dq, float* dk, float* dv, float* dll, void* ws,
+                       cudaStream_t s) {
+  BwdParams p;
+  p.q = pr.q;
+  p.k = pr.k;
+  p.v = pr.v;
+  p.log_lambda = pr.log_lambda;
+  p.dy = dy;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dll = dll;
+  p.B = pr.B;
+  p.H = pr.H;
+  p.L = pr.L;
+  p.mask_kind = pr.mask_kind;
+  p.phi = pr.phi;
+  const size_t BH = (size_t)pr.B * pr.H, n = BH * pr.L;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.fq = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n * pr.d);
+  p.fk = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n * pr.d);
+  p.g = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n * pr.d);
+  p.hd = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n);
+  p.rowd = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n);
+  p.cold = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n);
+  p.dsum = reinterpret_cast<double*>(w);
+  const bool bf = pr.dtype == DT_BF16;
+  switch (pr.d) {
+    case 16: return bf ? bwd_launch<__nv_bfloat16, 16>(p, s) : bwd_launch<float, 16>(p, s);
+    case 32: return bf ? bwd_launch<__nv_bfloat16, 32>(p, s) : bwd_launch<float, 32>(p, s);
+    case 64: return bf ? bwd_launch<__nv_bfloat16, 64>(p, s) : bwd_launch<float, 64>(p, s);
+    case 128: return bf ? bwd_launch<__nv_bfloat16, 128>(p, s) : bwd_launch<float, 128>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lion

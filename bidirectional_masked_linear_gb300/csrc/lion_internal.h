@@ -80,6 +80,12 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
 cudaError_t launch_chunk128_pre(const Problem& p, const LongPlan& plan, uint8_t* gst, float* segsum, int* status,
                                 cudaStream_t s);
 
+// Gradients through the full form (fp32, CUDA cores): dq, dk, dv [B][H][L][d],
+// dll as the public entry point describes; workspace of bwd_workspace_bytes.
+size_t bwd_workspace_bytes(int B, int H, int L, int d);
+cudaError_t launch_bwd(const Problem& p, const float* dy, float* dq, float* dk, float* dv, float* dll, void* ws,
+                       cudaStream_t s);
+
 // Device-side status word that kernels set when a bounded wait gives up
 // (address on the current device; nullptr if it cannot be resolved).
 int* device_status_ptr();

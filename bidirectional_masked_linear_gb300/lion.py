@@ -46,11 +46,24 @@ class _Args(ctypes.Structure):
     ]
 
 
+class _BwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_lambda", ctypes.c_void_p), ("dy", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dlog_lambda", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int),
+        ("mask_kind", ctypes.c_int), ("dtype", ctypes.c_int), ("phi", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "lion_rnn_step",
            "lion_status_string", "lion_abi_version", "lion_sync_status",
-           "lion_attn_fwd_rnn_noalloc")
+           "lion_attn_fwd_rnn_noalloc", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes")
 NOALLOC_MAX_HEAD_TOKENS = 1 << 20
 
 
@@ -80,6 +93,10 @@ def load(path: str = LIB_PATH):
     lib.lion_sync_status.restype = i
     lib.lion_abi_version.argtypes = []
     lib.lion_abi_version.restype = i
+    lib.lion_attn_bwd.argtypes = [ctypes.POINTER(_BwdArgs)]
+    lib.lion_attn_bwd.restype = i
+    lib.lion_attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.lion_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     _lib = lib
     return lib
 
@@ -182,3 +199,57 @@ def rnn_step(q, k, v, log_lambda, S, z, y_part, c_part, mask_kind, stream=None):
                            _stream_handle(stream))
     _check(st)
     return y_part, c_part
+
+
+def bwd_workspace_bytes(B, H, L, d) -> int:
+    return int(load().lion_attn_bwd_workspace_bytes(B, H, L, d))
+
+
+def attn_bwd(q, k, v, log_lambda, dy, mask_kind, phi=PHI_DEFAULT, workspace=None, stream=None):
+    """Gradients of a loss through Y = SCALE((phi(Q) phi(K)^T (.) M) V), given
+    ``dy`` = dLoss/dY ([B, H, L, d] float32).  Returns ``(dq, dk, dv,
+    dlog_lambda)`` as float32 tensors; ``dlog_lambda`` is None for LIT, [H]
+    for D and [B, H, L] for S."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    B, H, L, d = q.shape
+    dt = _dtype_code(q)
+    for t in (q, k, v, dy) + ((log_lambda,) if log_lambda is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if dy.dtype != torch.float32 or dy.shape != q.shape:
+        raise ValueError("dy must be float32 with the shape of q")
+    dq = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    dll = None
+    if mask_kind == MASK_D:
+        dll = torch.empty((H,), dtype=torch.float32, device=q.device)
+    elif mask_kind == MASK_S:
+        dll = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    a = _BwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv),
+                 _ptr(dll), B, H, L, d, mask_kind, dt, phi, _ptr(workspace),
+                 0 if workspace is None else workspace.numel() * workspace.element_size(),
+                 _stream_handle(stream))
+    _check(lib.lion_attn_bwd(ctypes.byref(a)))
+    return dq, dk, dv, dll
+
+
+class LionAttention(torch.autograd.Function):
+    """Y = SCALE((phi(Q) phi(K)^T (.) M) V) as a differentiable op: the
+    forward runs the library's forward in the given form, the backward its
+    gradient kernels (the forms agree, so the gradient is the same)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=128, phi=PHI_DEFAULT):
+        ctx.save_for_backward(q, k, v, log_lambda)
+        ctx.mask_kind, ctx.phi = mask_kind, phi
+        return attn_fwd(q, k, v, log_lambda, mask_kind, form, chunk, phi=phi)
+
+    @staticmethod
+    def backward(ctx, dy):
+        q, k, v, log_lambda = ctx.saved_tensors
+        dq, dk, dv, dll = attn_bwd(q, k, v, log_lambda, dy.contiguous().float(), ctx.mask_kind, ctx.phi)
+        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype),
+                None if log_lambda is None else dll, None, None, None, None)

@@ -177,6 +177,51 @@ lion_status lion_attn_fwd_rnn_noalloc(const void* q, const void* k, const void* 
                                       int mask_kind, int dtype, float* out,
                                       cudaStream_t stream);
 
+/*
+ * lion_attn_bwd -- gradients of a scalar loss through the operator, given
+ * dy = dLoss/dY (the training path: the full form trains like a Transformer,
+ * rebuttal page reply "Concern 1", Theorem 3.3 Eq 25).  With A = (phi(Q)
+ * phi(K)^T) (.) M, num = A V, den = A 1 and Y = num / den row by row:
+ *     dnum_i = dy_i / den_i,   dden_i = -(dy_i . y_i) / den_i,
+ *     dA_ij = dnum_i . v_j + dden_i,   dV = A^T dnum,
+ *     dphi(Q) = (M (.) dA) phi(K),     dphi(K) = (M (.) dA)^T phi(Q),
+ *     dlog(lambda_u) = sum of A_ij dA_ij over the pairs (i, j) with
+ *                      min(i,j) < u <= max(i,j)   (the factors of M_ij),
+ * then through the feature map by the chain rule.  The result does not
+ * depend on which form produced Y (they agree, Theorem 3.3).
+ *   q, k, v      [B][H][L][d] in `dtype`, device; log_lambda as for the forward.
+ *   dy           [B][H][L][d] float32, device.
+ *   dq, dk, dv   [B][H][L][d] float32, device, written entirely.
+ *   dlog_lambda  LIT: unused (NULL allowed); D: [H] (summed over the batch
+ *                and the positions, which share lambda_h); S: [B][H][L]
+ *                (position 0 never enters the mask: 0).  float32, device.
+ * Computed in fp32 on the CUDA cores, O(L^2 d) per head like the full form
+ * (L <= LION_FULL_MAX_L, else LION_ERR_UNSUPPORTED).  Workspace: as
+ * lion_attn_fwd_ex (NULL: stream-ordered allocation).
+ */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* log_lambda;
+  const float* dy;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dlog_lambda;
+  int B, H, L, d;
+  int mask_kind;             /* lion_mask_kind                             */
+  int dtype;                 /* lion_dtype of q, k, v                      */
+  int phi;                   /* lion_phi                                   */
+  void* workspace;           /* device, 256-byte aligned, or NULL          */
+  size_t workspace_bytes;    /* >= lion_attn_bwd_workspace_bytes(...)      */
+  cudaStream_t stream;
+} lion_bwd_args;
+lion_status lion_attn_bwd(const lion_bwd_args* a);
+
+/* Workspace bytes lion_attn_bwd needs for this problem. */
+size_t lion_attn_bwd_workspace_bytes(int B, int H, int L, int d);
+
 /* Static, human-readable text for a status. */
 const char* lion_status_string(lion_status s);
 

@@ -28,7 +28,7 @@ def _declared():
 def test_header_declares_the_abi():
     names = _declared()
     for want in ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_rnn_step", "lion_status_string",
-                 "lion_attn_workspace_bytes"):
+                 "lion_attn_workspace_bytes", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes"):
         assert want in names
 
 
@@ -56,6 +56,38 @@ def test_workspace_query(lib):
     assert lion.workspace_bytes(2, 3, 10, 64, lion.FORM_RNN) >= 2 * 3 * 10 * 4
     assert lion.workspace_bytes(0, 3, 10, 64, lion.FORM_RNN) == 0
     assert lion.workspace_bytes(1, 1, 10, 48, lion.FORM_RNN) == 0      # d unsupported
+
+
+def test_bwd_workspace_query(lib):
+    from bidirectional_masked_linear_gb300 import lion
+    # phi(q), phi(k) and dnum (L*d floats each), three per-token floats, a double per head
+    need = lion.bwd_workspace_bytes(2, 3, 10, 64)
+    assert need >= 2 * 3 * 10 * (3 * 64 + 3) * 4 + 2 * 3 * 8
+    assert lion.bwd_workspace_bytes(0, 3, 10, 64) == 0
+    assert lion.bwd_workspace_bytes(1, 1, 10, 48) == 0
+
+
+def _bwd(lib, **kw):
+    from bidirectional_masked_linear_gb300 import lion
+    f = dict(q=4096, k=8192, v=12288, log_lambda=0, dy=16384, dq=20480, dk=24576, dv=28672,
+             dlog_lambda=0, B=1, H=1, L=8, d=64, mask_kind=0, dtype=0, phi=0, workspace=0,
+             workspace_bytes=0, stream=0)
+    f.update(kw)
+    a = lion._BwdArgs(**f)
+    return lib.lion_attn_bwd(ctypes.byref(a))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(k=0), dict(v=0), dict(dy=0), dict(dq=0), dict(dk=0), dict(dv=0),
+    dict(B=0), dict(H=0), dict(L=0), dict(d=48), dict(mask_kind=3), dict(dtype=2), dict(phi=4),
+    dict(mask_kind=1, log_lambda=32768, dlog_lambda=0), dict(mask_kind=2, log_lambda=0, dlog_lambda=32768),
+    dict(),   # pointers that are not device memory
+])
+def test_bwd_invalid_arguments_rejected_before_launch(lib, kw):
+    from bidirectional_masked_linear_gb300 import lion
+    lib.lion_attn_bwd.argtypes = [ctypes.POINTER(lion._BwdArgs)]
+    assert _bwd(lib, **kw) == 1
+    assert lib.lion_attn_bwd(None) == 1
 
 
 def _fwd(lib, q=1, k=1, v=1, ll=None, B=1, H=1, L=8, d=64, mask=0, form=2, chunk=64, out=1):

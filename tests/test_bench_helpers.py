@@ -45,3 +45,10 @@ def test_traffic_keys_follow_the_kernel_that_runs():
         for rel in files:
             assert os.path.exists(os.path.join(ROOT, rel)), (key, rel)
     assert bench._sources_sha((128, False)) != bench._sources_sha((128, True))
+
+
+def test_backward_flops_and_peak():
+    w = synth.WORKLOADS["vit_b"]
+    # six L x L x d products of 2 L^2 d flops per head
+    assert bench.bwd_flops(w) == 6 * 2 * w.B * w.H * w.L ** 2 * w.d
+    assert abs(bench.FP32_ALU_PEAK_TFLOPS - 80.54) < 0.01

@@ -297,3 +297,102 @@ def test_full_workload(oracle_mod, name, mask, form, chunk):
     ref = _reference(name, mask)
     y = run_gpu(inp, form, chunk)
     check(oracle_mod, y, ref, inp, TOL_BF16)
+
+
+# ------------------------------------------------------------- backward ---
+# Gradients through the full form (the training path, rebuttal page reply
+# "Concern 1", Theorem 3.3 Eq 25) against the float64 oracle's gradients,
+# which finite differences of the forward pin.  The GPU path computes in
+# fp32; each gradient tensor is compared relative to its largest entry.
+TOL_BWD = 2e-4
+
+
+def _bwd_check(oracle_mod, B, H, L, d, mask, dtype, phi=0, seed=0, positive=False):
+    inp = synth.make_inputs(B, H, L, d, mask, dtype, seed=seed)
+    if positive:   # identity features need row sums away from zero
+        for key in ("q", "k"):
+            inp[key] = (inp[key].float().abs() + 0.25).to(inp[key].dtype)
+    q64, k64, v64, ll64 = f64(inp)
+    dy = np.random.default_rng(seed + 1).standard_normal((B, H, L, d)).astype(np.float32)
+    ref = oracle_mod.full_bwd(q64, k64, v64, ll64, dy.astype(np.float64), inp["mask"], phi)
+    g = _cuda(inp)
+    got = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], torch.from_numpy(dy).cuda(),
+                        inp["mask"], phi)
+    torch.cuda.synchronize()
+    # a tensor whose exact value is 0 (dq and dk at L = 1) is measured against
+    # the scale of the case's other gradients
+    floor = 1e-2 * max(float(np.abs(r).max()) for r in ref if r is not None)
+    for name, r, x in zip(("dq", "dk", "dv", "dlog_lambda"), ref, got):
+        if r is None:
+            assert x is None
+            continue
+        x = x.cpu().numpy().astype(np.float64)
+        assert x.shape == r.shape, name
+        err = float(np.abs(x - r).max() / max(np.abs(r).max(), floor))
+        assert err <= TOL_BWD, (name, B, H, L, d, dtype, err)
+    return got
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+@pytest.mark.parametrize("dtype", ("bf16", "fp32"))
+def test_backward_matches_oracle(oracle_mod, mask, dtype):
+    for n, (B, H, L, d) in enumerate(((1, 2, 64, 16), (2, 3, 197, 64), (1, 2, 33, 32), (1, 1, 300, 128))):
+        _bwd_check(oracle_mod, B, H, L, d, mask, dtype, seed=700 + 10 * n)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_backward_single_token(mask):
+    """L = 1: y = v whatever q and k are, so dv = dy and dq = dk = 0 up to the
+    fp32 rounding of v - y; the decay never enters (dlog_lambda = 0)."""
+    inp = synth.make_inputs(3, 2, 1, 64, mask, "bf16", seed=760)
+    g = _cuda(inp)
+    dy = torch.randn(3, 2, 1, 64, device="cuda")
+    dq, dk, dv, dll = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], dy, inp["mask"])
+    scale = float(dy.abs().max())
+    assert float((dv - dy).abs().max()) <= 1e-5 * scale
+    assert float(dq.abs().max()) <= 1e-3 * scale and float(dk.abs().max()) <= 1e-3 * scale
+    if dll is not None:
+        assert float(dll.abs().max()) == 0.0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask,phi,positive", (("lit", 2, False), ("d", 2, False), ("s", 1, False),
+                                               ("s", 3, True), ("lit", 3, True)))
+def test_backward_feature_maps(oracle_mod, mask, phi, positive):
+    _bwd_check(oracle_mod, 2, 2, 150, 64, mask, "bf16", phi=phi, seed=800, positive=positive)
+
+
+@pytest.mark.gpu
+def test_backward_steep_decay(oracle_mod):
+    """Fast-decaying LION-S (log lambda scaled by 40): most of M underflows.
+    elu+1 features keep the row sums (here about s_ii) away from zero, so the
+    case measures the mask, not a near-zero denominator's conditioning."""
+    inp = synth.make_inputs(2, 2, 120, 64, "s", "bf16", seed=810)
+    inp["log_lambda"] = inp["log_lambda"] * 40.0
+    q64, k64, v64, ll64 = f64(inp)
+    dy = np.random.default_rng(811).standard_normal(q64.shape).astype(np.float32)
+    ref = oracle_mod.full_bwd(q64, k64, v64, ll64, dy.astype(np.float64), inp["mask"], 1)
+    g = _cuda(inp)
+    got = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], torch.from_numpy(dy).cuda(), inp["mask"], 1)
+    for r, x in zip(ref, got):
+        x = x.cpu().numpy().astype(np.float64)
+        assert np.abs(x - r).max() <= TOL_BWD * max(np.abs(r).max(), 1e-30)
+
+
+@pytest.mark.gpu
+def test_autograd_function_uses_the_backward():
+    """LionAttention: forward by the chunk form, backward by attn_bwd."""
+    inp = synth.make_inputs(2, 3, 197, 64, "s", "bf16", seed=820)
+    g = _cuda(inp)
+    q = g["q"].clone().requires_grad_(True)
+    k = g["k"].clone().requires_grad_(True)
+    v = g["v"].clone().requires_grad_(True)
+    ll = g["log_lambda"].clone().requires_grad_(True)
+    y = lion.LionAttention.apply(q, k, v, ll, lion.MASK_S, lion.FORM_CHUNK, 128)
+    dy = torch.randn_like(y)
+    y.backward(dy)
+    dq, dk, dv, dll = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], dy, lion.MASK_S)
+    assert torch.equal(q.grad, dq.to(q.dtype)) and torch.equal(k.grad, dk.to(k.dtype))
+    assert torch.equal(v.grad, dv.to(v.dtype)) and torch.equal(ll.grad, dll)
