@@ -234,6 +234,51 @@ lion_status lion_sync_status(cudaStream_t stream) {
   return LION_OK;
 }
 
+lion_status lion_attn_fwd_causal(const lion_args* a) {
+  lion_status st = validate(a);
+  if (st != LION_OK) return st;
+  if (a->form == LION_FORM_CHUNK && a->chunk > lion::kSimtMaxChunk) return LION_ERR_UNSUPPORTED;
+  Problem p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.log_lambda = a->log_lambda;
+  p.out = a->out;
+  p.B = a->B;
+  p.H = a->H;
+  p.L = a->L;
+  p.d = a->d;
+  p.mask_kind = a->mask_kind;
+  p.phi = lion::resolve_phi(a->mask_kind, a->phi);
+  p.dtype = a->dtype;
+  p.chunk = a->chunk;
+  p.causal = 1;
+  cudaStream_t s = a->stream;
+  const size_t need = simt_workspace_bytes(a->B, a->H, a->L, a->form);
+  void* ws = a->workspace;
+  bool owned = false;
+  if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
+  if (need > 0 && !ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
+    }
+    owned = true;
+  }
+  cudaError_t e = cudaSuccess;
+  switch (a->form) {
+    case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
+    case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
+    case LION_FORM_CHUNK: e = lion::launch_chunk_simt(p, (float*)ws, s); break;
+  }
+  if (owned) {
+    cudaError_t f = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = f;
+  }
+  return from_cuda(e);
+}
+
 lion_status lion_attn_fwd(const void* q, const void* k, const void* v, const float* log_lambda,
                           int B, int H, int L, int d, int mask_kind, int form, int chunk,
                           float* out, cudaStream_t stream) {

@@ -18,6 +18,7 @@ struct Problem {
   int phi;     // resolved (never PHI_DEFAULT)
   int dtype;   // DT_BF16 / DT_FP32
   int chunk;
+  int causal = 0;   // 1: only j <= i (the forward half), SIMT kernels only
 };
 
 // SIMT (CUDA-core) kernels: any d in {16,32,64,128}, both dtypes.

@@ -18,6 +18,10 @@
 //                      Chunk"): a right-to-left sweep applies the backward
 //                      chunk state, then a left-to-right sweep adds the
 //                      intra-chunk masked attention and the forward state.
+// With Problem::causal each computes the forward half alone, y_i =
+// sum_{j<=i} M_ij s_ij v_j / sum_{j<=i} M_ij s_ij: the causal recurrence of the
+// Linear Transformer with the decay (rebuttal page reply "1: Recurrence Form";
+// the unidirectional LION-S of reply "Q5").
 #include "lion_common.cuh"
 #include "lion_internal.h"
 
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(256) full_simt_kernel(Problem p) {
 #pragma unroll
   for (int c = 0; c < NC; ++c) acc[c] = 0.f;
   float den = 0.f;
-  for (int j0 = 0; j0 < L; j0 += kFullTile) {
+  const int jend = p.causal ? min(L, i0 + kFullRows) : L;   // causal: keys up to the block's last row
+  for (int j0 = 0; j0 < jend; j0 += kFullTile) {
     const int nj = min(kFullTile, L - j0);
     load_rows<T>(sK, D, k, j0, kFullTile, L, D);
     load_rows<T>(sV, D, v, j0, kFullTile, L, D);
@@ -123,7 +128,7 @@ __global__ void __launch_bounds__(256) full_simt_kernel(Problem p) {
       s += __shfl_xor_sync(0xffffffffu, s, 2);
       s += __shfl_xor_sync(0xffffffffu, s, 4);
       const int j = j0 + jj;
-      float w = s;
+      float w = (p.causal && j > i) ? 0.f : s;
       if (p.mask_kind == MASK_D) w *= expf(fabsf((float)(i - j)) * lh);
       else if (p.mask_kind == MASK_S) w *= expf(mask_exponent(i, j, Pi, sP[j]));
       den += w;
@@ -199,12 +204,17 @@ __global__ void __launch_bounds__(D * kRnnSplit) rnn_simt_kernel(Problem p, floa
       c += __shfl_xor_sync(0xffffffffu, c, 1);
       c += __shfl_xor_sync(0xffffffffu, c, 2);
       if (r == 0) {
-        out[(size_t)(t0 + tt) * D + n] = y;
-        if (n == 0) cF[t0 + tt] = c;
+        if (p.causal) {
+          out[(size_t)(t0 + tt) * D + n] = y / c;   // the forward half is the whole result
+        } else {
+          out[(size_t)(t0 + tt) * D + n] = y;
+          if (n == 0) cF[t0 + tt] = c;
+        }
       }
     }
     __syncthreads();
   }
+  if (p.causal) return;
 #pragma unroll
   for (int a = 0; a < MS; ++a) { S[a] = 0.f; z[a] = 0.f; }
 
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(256) chunk_simt_kernel(Problem p, float* den_a
   const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
   auto ell = [&](int t) -> float { return p.mask_kind == MASK_S ? ll[t] : lh; };
 
-  for (int sweep = 0; sweep < 2; ++sweep) {
+  for (int sweep = p.causal ? 1 : 0; sweep < 2; ++sweep) {
     const bool fwd = sweep == 1;
     for (int x = threadIdx.x; x < D * W; x += blockDim.x) sSt[x] = 0.f;
     __syncthreads();
@@ -335,7 +345,7 @@ __global__ void __launch_bounds__(256) chunk_simt_kernel(Problem p, float* den_a
             for (int idx = threadIdx.x; idx < kPanel * kPanel; idx += blockDim.x) {
               const int r = idx / kPanel, jj = idx - r * kPanel;
               float w = 0.f;
-              if (r < nq && jj < nk) {
+              if (r < nq && jj < nk && (!p.causal || ka + jj <= qa + r)) {
                 const int i = qa + r, j = ka + jj;
                 float dot = 0.f;
                 for (int m = 0; m < D; ++m) dot += sQ[r * LDQ + m] * sK[jj * D + m];
@@ -366,8 +376,9 @@ __global__ void __launch_bounds__(256) chunk_simt_kernel(Problem p, float* den_a
           __syncthreads();
           for (int idx = threadIdx.x; idx < nq * D; idx += blockDim.x) {
             const int r = idx / D, n = idx - r * D, i = qa + r;
-            const float dn = sAcc[r * W + D] + den[i];
-            out[(size_t)i * D + n] = (sAcc[r * W + n] + out[(size_t)i * D + n]) / dn;
+            // (causal: no backward sweep parked anything)
+            const float dn = sAcc[r * W + D] + (p.causal ? 0.f : den[i]);
+            out[(size_t)i * D + n] = (sAcc[r * W + n] + (p.causal ? 0.f : out[(size_t)i * D + n])) / dn;
           }
         }
         __syncthreads();

@@ -63,7 +63,8 @@ _lib = None
 
 EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "lion_rnn_step",
            "lion_status_string", "lion_abi_version", "lion_sync_status",
-           "lion_attn_fwd_rnn_noalloc", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes")
+           "lion_attn_fwd_rnn_noalloc", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
+           "lion_attn_fwd_causal")
 NOALLOC_MAX_HEAD_TOKENS = 1 << 20
 
 
@@ -93,6 +94,8 @@ def load(path: str = LIB_PATH):
     lib.lion_sync_status.restype = i
     lib.lion_abi_version.argtypes = []
     lib.lion_abi_version.restype = i
+    lib.lion_attn_fwd_causal.argtypes = [ctypes.POINTER(_Args)]
+    lib.lion_attn_fwd_causal.restype = i
     lib.lion_attn_bwd.argtypes = [ctypes.POINTER(_BwdArgs)]
     lib.lion_attn_bwd.restype = i
     lib.lion_attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
@@ -253,3 +256,26 @@ class LionAttention(torch.autograd.Function):
         dq, dk, dv, dll = attn_bwd(q, k, v, log_lambda, dy.contiguous().float(), ctx.mask_kind, ctx.phi)
         return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype),
                 None if log_lambda is None else dll, None, None, None, None)
+
+
+def attn_fwd_causal(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None,
+                    phi=PHI_DEFAULT, workspace=None, stream=None):
+    """The forward half alone (a unidirectional model): y_i = sum_{j<=i}
+    M_ij s_ij v_j / sum_{j<=i} M_ij s_ij, in any form."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    if isinstance(form, str):
+        form = FORMS[form]
+    B, H, L, d = q.shape
+    if out is None:
+        out = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    for t in (q, k, v, out) + ((log_lambda,) if log_lambda is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(out), B, H, L, d, mask_kind,
+              form, chunk, _dtype_code(q), phi, _ptr(workspace),
+              0 if workspace is None else workspace.numel() * workspace.element_size(),
+              _stream_handle(stream))
+    _check(lib.lion_attn_fwd_causal(ctypes.byref(a)))
+    return out

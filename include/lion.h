@@ -124,6 +124,19 @@ lion_status lion_attn_fwd_ex(const lion_args* a);
 size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk);
 
 /*
+ * lion_attn_fwd_causal -- the forward half alone, for a unidirectional
+ * (generative) model: y_i = sum_{j<=i} M_ij s_ij v_j / sum_{j<=i} M_ij s_ij.
+ * This is the causal Linear-Transformer recurrence with the decay (rebuttal
+ * page reply "1: Recurrence Form"; the unidirectional LION-S of reply
+ * "Q5").  Arguments as lion_attn_fwd_ex, in every form (FULL: keys up to the
+ * row; RNN: the forward recurrence alone; CHUNK: the forward chunk scan and
+ * the lower triangle of each chunk).  Computed on the CUDA cores in fp32,
+ * chunk <= 1024.  Workspace: B*H*L floats for RNN and CHUNK, none for FULL
+ * (NULL: stream-ordered allocation).
+ */
+lion_status lion_attn_fwd_causal(const lion_args* a);
+
+/*
  * lion_rnn_step -- one token of one direction of the recurrent form, for
  * B*H heads at once (Theorem 3.3 Eq 20-24; the causal Linear-Transformer
  * recurrence of reply "1: Recurrence Form" with a decay):

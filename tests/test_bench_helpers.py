@@ -52,3 +52,8 @@ def test_backward_flops_and_peak():
     # six L x L x d products of 2 L^2 d flops per head
     assert bench.bwd_flops(w) == 6 * 2 * w.B * w.H * w.L ** 2 * w.d
     assert abs(bench.FP32_ALU_PEAK_TFLOPS - 80.54) < 0.01
+
+
+def test_stream_bytes():
+    # ViT-B heads, d = 64: S and z read and written in fp32, bf16 q, k, v in
+    assert bench.stream_bytes(64, 12, 64) == 64 * 12 * (2 * (64 * 64 + 64) * 4 + 3 * 64 * 2 + 4 + 64 * 4 + 4)

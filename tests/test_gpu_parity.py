@@ -396,3 +396,56 @@ def test_autograd_function_uses_the_backward():
     dq, dk, dv, dll = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], dy, lion.MASK_S)
     assert torch.equal(q.grad, dq.to(q.dtype)) and torch.equal(k.grad, dk.to(k.dtype))
     assert torch.equal(v.grad, dv.to(v.dtype)) and torch.equal(ll.grad, dll)
+
+
+# --------------------------------------------------------- causal (f3) ---
+# The forward half alone, y_i = sum_{j<=i} M_ij s_ij v_j / sum_{j<=i} M_ij s_ij
+# (rebuttal page reply "1: Recurrence Form"; the unidirectional LION-S of reply
+# "Q5"), against the oracle's forward recurrence (pinned to the causal Linear
+# Transformer at lambda = 1).  fp32 arithmetic on the CUDA cores.
+TOL_CAUSAL = 1e-4
+
+
+def _causal_check(oracle_mod, inp, form, chunk, phi=0):
+    q, k, v, ll = f64(inp)
+    B, H, L, d = q.shape
+    yF, cF = oracle_mod.rnn_forward_half(q, k, v, ll, inp["mask"], phi)
+    ref = yF / cF[..., None]
+    g = _cuda(inp)
+    y = lion.attn_fwd_causal(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], form, chunk, phi=phi)
+    y = y.cpu().numpy().astype(np.float64)
+    kind = phi or (2 if inp["mask"] == lion.MASK_S else 1)
+    err = row_errors(y, ref)
+    for b in range(B):
+        for h in range(H):
+            M = np.tril(oracle_mod.mask(inp["mask"], ll, L, b, h, H))
+            fq, fk = oracle_mod.phi(kind, q[b, h]), oracle_mod.phi(kind, k[b, h])
+            den = (M * (fq @ fk.T)).sum(1)
+            kap = (M * (np.abs(fq) @ np.abs(fk).T)).sum(1) / np.abs(den)
+            bad = err[b, h] > TOL_CAUSAL * np.maximum(1.0, kap)
+            assert not bad.any(), (form, chunk, b, h, np.argwhere(bad)[:3], err[b, h][bad][:3])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+@pytest.mark.parametrize("dtype", ("bf16", "fp32"))
+def test_causal_matches_forward_half(oracle_mod, mask, dtype):
+    for n, (B, H, L, d) in enumerate(((1, 2, 64, 16), (2, 3, 197, 64), (1, 2, 300, 32), (1, 1, 77, 128))):
+        inp = synth.make_inputs(B, H, L, d, mask, dtype, seed=900 + 10 * n)
+        for form, chunk in ((lion.FORM_FULL, 0), (lion.FORM_RNN, 0), (lion.FORM_CHUNK, 16),
+                            (lion.FORM_CHUNK, 64), (lion.FORM_CHUNK, 100)):
+            _causal_check(oracle_mod, inp, form, max(chunk, 1))
+
+
+@pytest.mark.gpu
+def test_causal_feature_maps_and_single_token(oracle_mod):
+    inp = synth.make_inputs(2, 2, 130, 64, "lit", "bf16", seed=950)
+    _causal_check(oracle_mod, inp, lion.FORM_CHUNK, 64, phi=2)
+    inp = synth.make_inputs(2, 2, 130, 64, "s", "bf16", seed=951)
+    _causal_check(oracle_mod, inp, lion.FORM_RNN, 1, phi=1)
+    # L = 1: y_0 = v_0
+    inp = synth.make_inputs(3, 2, 1, 64, "s", "bf16", seed=952)
+    g = _cuda(inp)
+    for form in (lion.FORM_FULL, lion.FORM_RNN, lion.FORM_CHUNK):
+        y = lion.attn_fwd_causal(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], form, 8)
+        assert torch.allclose(y, g["v"].float(), rtol=1e-5, atol=1e-6)   # (s v) / s, rounded
