@@ -491,6 +491,17 @@ def main():
                                   "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak}}
         del _k2
 
+    lra = None
+    if not args.no_secondary and args.workload != "lra_4096":
+        w3, _, t3, _k3 = measure("lra_4096", args.mask if args.mask != "lit" else "s", 128, "chunk", 50, 3, flush)
+        ms3 = statistics.mean(t3)
+        b3 = algorithmic_bytes(w3, args.mask if args.mask != "lit" else "s")
+        lra = {"workload": f"{w3.name} B={w3.B} H={w3.H} L={w3.L} d={w3.d}", "chunk": 128,
+               "value": w3.B * w3.L / (ms3 * 1e-3), "unit": "tokens/s", "ms_per_step": ms3,
+               "roofline": {"bound": "hbm", "achieved": b3 / (ms3 * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                            "frac": b3 / (ms3 * 1e-3) / 1e9 / hbm_peak}}
+        del _k3
+
     backward = None
     if not args.no_backward and w.L <= lion.FULL_MAX_L:
         tb = measure_bwd(w, args.mask, 20, 3, flush)
@@ -536,6 +547,7 @@ def main():
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
             "secondary": secondary,
+            "lra": lra,
             "backward": backward,
             "streaming": streaming,
         }

@@ -20,7 +20,8 @@ Recipe (every workload):
   as float32.
 
 The shapes stand in for the pages' ImageNet (ViT-T / ViT-B patch sequences),
-C4 MLM (BERT-large) and 2496-px image workloads, whose data are not available.
+C4 MLM (BERT-large), 2496-px image and Long-Range-Arena text (length 4096)
+workloads, whose data are not available.
 """
 from __future__ import annotations
 
@@ -52,6 +53,7 @@ WORKLOADS = {
     "vit_b": Workload("vit_b", 64, 12, 197, 64, "bf16", ("lit", "d", "s"), (32, 64, 128), "u09", 1003),
     "bert_large": Workload("bert_large", 32, 16, 512, 64, "bf16", ("d", "s"), (64, 128), "u09", 1004),
     "hires_2496": Workload("hires_2496", 2, 12, 24337, 64, "bf16", ("d", "s"), (64, 128), "u09", 1005),
+    "lra_4096": Workload("lra_4096", 16, 8, 4096, 64, "bf16", ("d", "s"), (64, 128), "u09", 1006),
 }
 
 

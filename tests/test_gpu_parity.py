@@ -288,6 +288,8 @@ FULL_CASES = [
     ("hires_2496", "d", lion.FORM_RNN, 64),
     ("hires_2496", "s", lion.FORM_CHUNK, 64), ("hires_2496", "s", lion.FORM_CHUNK, 128),
     ("hires_2496", "s", lion.FORM_RNN, 64),
+    ("lra_4096", "s", lion.FORM_CHUNK, 128), ("lra_4096", "d", lion.FORM_CHUNK, 128),
+    ("lra_4096", "s", lion.FORM_CHUNK, 64), ("lra_4096", "s", lion.FORM_RNN, 64),
 ]
 
 
