@@ -311,11 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         nx.next(prm);
         if (nx.valid(prm)) load_ell(nx, &ell_next, &lnext_next);
       }
-      float pre = 0.f;
-      for (int w = 0; w < pw; ++w) pre += rd[w];
-      float T = 0.f;
+      // the warps' totals, one per lane, scanned: the chunk total and this
+      // warp's offset
+      float sc = lane < 16 ? rd[lane] : 0.f;
 #pragma unroll
-      for (int w = 0; w < 16; ++w) T += rd[w];
+      for (int o = 1; o < 16; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, sc, o);
+        if (lane >= o) sc += y;
+      }
+      const float T = __shfl_sync(0xffffffffu, sc, 15);
+      const float pre_l = __shfl_sync(0xffffffffu, sc, (pw + 15) & 15);   // lane pw - 1 (warp-uniform)
+      const float pre = pw == 0 ? 0.f : pre_l;
       const float p = x + pre;
       const float pfirst = rd[16];
       const bool live = tok < L;
