@@ -286,6 +286,13 @@ def bwd_flops(w) -> int:
     return 12 * w.B * w.H * w.L * w.L * w.d
 
 
+def bwd_launches(mask, d) -> int:
+    """Kernels one lion_attn_bwd call launches: phi, rows and columns passes;
+    the dl pass for LION-D and LION-S; the batch sum for LION-D; the prefix of
+    log-lambda for LION-S when d >= 64 (the register-tiled passes)."""
+    return 3 + (mask != "lit") + (mask == "d") + (mask == "s" and d >= 64)
+
+
 def measure_bwd(w, mask, steps, warmup, flush):
     """CUDA-event time of one gradient call (lion_attn_bwd, all its kernels)
     through the C entry point with preallocated outputs and workspace."""
@@ -508,7 +515,7 @@ def main():
         msb = statistics.mean(tb)
         fl = bwd_flops(w)
         backward = {"form": "full", "value": w.B * w.L / (msb * 1e-3), "unit": "tokens/s", "ms_per_call": msb,
-                    "launches_per_call": 4 if args.mask != "d" else 5,
+                    "launches_per_call": bwd_launches(args.mask, w.d),
                     "roofline": {"bound": "alu", "achieved": fl / (msb * 1e-3) / 1e12,
                                  "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
                                  "frac": fl / (msb * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,

@@ -22,6 +22,10 @@
 // column terms; (4) per head, dl (LION-S: suffix sums; LION-D: the sum over
 // positions, sum_m m dLoss/dP_m) in double, and for LION-D the sum over the
 // batch.  The mask value is generated per (i, j) as in the forward full form.
+// Passes (2) and (3) come in two builds: for d = 16 and 32, 8 threads share a
+// row and reduce each dot product by shuffles; for d = 64 and 128 a thread
+// holds a 4 x 4 tile of scores and whole dot products (register tiling, with
+// LION-S reading a per-head prefix of l that a small kernel writes first).
 #include "lion_common.cuh"
 #include "lion_internal.h"
 
@@ -37,10 +41,11 @@ __device__ __forceinline__ const T* head_of(const void* base, int bh, int L, int
   return reinterpret_cast<const T*>(base) + (size_t)bh * L * D;
 }
 
+// sum over W adjacent lanes (W a power of two, the group aligned to W)
+template <int W = kGroup>
 __device__ __forceinline__ float group_sum(float x) {
-  x += __shfl_xor_sync(0xffffffffu, x, 1);
-  x += __shfl_xor_sync(0xffffffffu, x, 2);
-  x += __shfl_xor_sync(0xffffffffu, x, 4);
+#pragma unroll
+  for (int o = 1; o < W; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
 
@@ -83,9 +88,10 @@ __device__ __forceinline__ float log_mask(int mask_kind, int i, int j, float lh,
   return 0.f;
 }
 
-// dphi -> dx for this thread's NC features of one row (features g + c*8),
-// the row's 8 threads cooperating on the SiLU + L2 norm.
-template <int NC>
+// dphi -> dx for this thread's NC features of one row, the row's W threads
+// (adjacent lanes) together holding all of its features and cooperating on
+// the SiLU + L2 norm.
+template <int NC, int W = kGroup>
 __device__ __forceinline__ void phi_backward(int phi, const float* x, const float* dphi, float* dx) {
   if (phi == PHI_ELU1) {
 #pragma unroll
@@ -98,12 +104,12 @@ __device__ __forceinline__ void phi_backward(int phi, const float* x, const floa
       u[c] = x[c] * sg[c];
       ss += u[c] * u[c];
     }
-    const float nrm = sqrtf(group_sum(ss));
+    const float nrm = sqrtf(group_sum<W>(ss));
     float dx_scale, dot = 0.f;
     if (nrm >= 1e-12f) {
 #pragma unroll
       for (int c = 0; c < NC; ++c) dot += u[c] / nrm * dphi[c];
-      dot = group_sum(dot);
+      dot = group_sum<W>(dot);
       dx_scale = 1.f / nrm;
     } else {
       dx_scale = 1e12f;
@@ -140,6 +146,7 @@ struct BwdParams {
   float* rowd;   // [BH][L]    row terms of dLoss/dP
   float* cold;   // [BH][L]    column terms of dLoss/dP
   double* dsum;  // [BH]       LION-D: sum over positions of dl
+  float* P;      // [BH][L]    LION-S: inclusive prefix of l (tiled passes)
 };
 
 // (1) phi(q), phi(k): one warp per row.
@@ -371,6 +378,378 @@ __global__ void __launch_bounds__(256) bwd_cols_kernel(BwdParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Register-tiled passes (2) and (3) for d in {64, 128}.  A CTA of 128 threads
+// (an 8 x 16 grid: ty = 0..7, tx = 0..15) holds a block of 32 rows of its own
+// side and walks the other side in tiles of 64 tokens.  Each thread computes
+// the 4 x 4 piece (rows ty + 8a, columns tx + 16b) of a 32 x 64 tile of
+// scores with whole dot products over the features in its own registers, and
+// accumulates the block's outputs for its 4 rows and the d/16 features
+// 4tx + 64u + e.  Operand rows sit in shared memory with a stride of d + 4
+// floats and are read as float4 along the features: consecutive column
+// threads read consecutive rows (4 banks apart: no conflicts) and the row
+// threads of a quarter warp read one address (a broadcast).  The mask value is
+// generated per (i, j) exactly as in the one-row-per-group passes.
+constexpr int kTR = 32;            // rows of a block
+constexpr int kTC = 64;            // tokens of a tile of the other side
+constexpr int kTAL = kTC + 16;     // row stride of the staged score tiles (floats)
+constexpr int kTThreads = 128;
+
+__device__ __forceinline__ float4 load4(const float* src) { return *reinterpret_cast<const float4*>(src); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* src) {
+  const uint2 u = *reinterpret_cast<const uint2*>(src);
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ float elem(const float4& x, int e) {
+  return e == 0 ? x.x : e == 1 ? x.y : e == 2 ? x.z : x.w;
+}
+
+// Rows [row0, row0 + nrows) of a [L][D] head array into dst (row stride
+// D + 4 floats), zero past L.  Whole block.
+template <int D, typename T>
+__device__ __forceinline__ void stage_rows(float* dst, const T* src, int row0, int nrows, int L) {
+  constexpr int V = D / 4, LD = D + 4;
+  for (int idx = threadIdx.x; idx < nrows * V; idx += blockDim.x) {
+    const int r = idx / V, c = (idx - r * V) * 4, i = row0 + r;
+    const float4 x = i < L ? load4(src + (size_t)i * D + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(dst + r * LD + c) = x;
+  }
+}
+__device__ __forceinline__ void stage_vec(float* dst, const float* src, int row0, int n, int L) {
+  for (int t = threadIdx.x; t < n; t += blockDim.x) dst[t] = row0 + t < L ? src[row0 + t] : 0.f;
+}
+
+// acc[a][b] = sum_m X[ty + 8a][m] Y[tx + 16b][m]
+template <int D>
+__device__ __forceinline__ void tile_scores(const float* X, const float* Y, int ty, int tx, float (&acc)[4][4]) {
+  constexpr int LD = D + 4;
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+  for (int m = 0; m < D; m += 4) {
+    float4 x[4], y[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) x[a] = *reinterpret_cast<const float4*>(X + (ty + 8 * a) * LD + m);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) y[b] = *reinterpret_cast<const float4*>(Y + (tx + 16 * b) * LD + m);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float t = acc[a][b];
+        t = fmaf(x[a].x, y[b].x, t);
+        t = fmaf(x[a].y, y[b].y, t);
+        t = fmaf(x[a].z, y[b].z, t);
+        acc[a][b] = fmaf(x[a].w, y[b].w, t);
+      }
+  }
+}
+
+// out[a][4u + e] += sum_{t < n} S[ty + 8a][t] Z[t][4tx + 64u + e]; n is a
+// multiple of 4 and S is zero from the last real token to n.
+template <int D>
+__device__ __forceinline__ void tile_apply(const float* S, const float* Z, int n, int ty, int tx,
+                                           float (&out)[4][D / 16]) {
+  constexpr int LD = D + 4, U = D / 64;
+#pragma unroll 2
+  for (int t = 0; t < n; t += 4) {
+    float4 s[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) s[a] = *reinterpret_cast<const float4*>(S + (ty + 8 * a) * kTAL + t);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float4 z = *reinterpret_cast<const float4*>(Z + (t + e) * LD + 4 * tx + 64 * u);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float w = elem(s[a], e);
+          out[a][4 * u + 0] = fmaf(w, z.x, out[a][4 * u + 0]);
+          out[a][4 * u + 1] = fmaf(w, z.y, out[a][4 * u + 1]);
+          out[a][4 * u + 2] = fmaf(w, z.z, out[a][4 * u + 2]);
+          out[a][4 * u + 3] = fmaf(w, z.w, out[a][4 * u + 3]);
+        }
+      }
+  }
+}
+
+// M_ij of query i and key j (Pi, Pj: the prefix at i and j for LION-S).
+__device__ __forceinline__ float mask_value(int mask_kind, int i, int j, float Pi, float Pj, float lh) {
+  if (mask_kind == MASK_D) return expf(fabsf((float)(i - j)) * lh);
+  if (mask_kind == MASK_S) return expf(i >= j ? Pi - Pj : Pj - Pi);
+  return 1.f;
+}
+
+// LION-S: the inclusive prefix of l per head into P (one CTA per head),
+// accumulated in double and stored in fp32.
+constexpr int kPrefixThreads = 256;
+__global__ void __launch_bounds__(kPrefixThreads) bwd_prefix_kernel(BwdParams p) {
+  __shared__ double tot[kPrefixThreads];
+  const int L = p.L, bh = blockIdx.x, t = threadIdx.x;
+  const float* ll = p.log_lambda + (size_t)bh * L;
+  float* P = p.P + (size_t)bh * L;
+  const int per = (L + kPrefixThreads - 1) / kPrefixThreads;
+  const int lo = min(L, t * per), hi = min(L, lo + per);
+  double run = 0.0;
+  for (int m = lo; m < hi; ++m) run += (double)ll[m];
+  tot[t] = run;
+  __syncthreads();
+  double off = 0.0;
+  for (int u = 0; u < t; ++u) off += tot[u];
+  for (int m = lo; m < hi; ++m) {
+    off += (double)ll[m];
+    P[m] = (float)off;
+  }
+}
+
+template <int D>
+constexpr size_t rows_tiled_smem() {
+  return sizeof(float) * ((size_t)(2 * kTR + 2 * kTC) * (D + 4) + kTR * kTAL + kTC);
+}
+template <int D>
+constexpr size_t cols_tiled_smem() {
+  return sizeof(float) * ((size_t)(2 * kTR + 2 * kTC) * (D + 4) + 2 * kTR * kTAL + 2 * kTC);
+}
+
+// (2) rows, tiled: 32 queries per CTA.
+template <typename T, int D>
+__global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
+  constexpr int LD = D + 4, MF = D / 16, U = D / 64;
+  extern __shared__ __align__(16) float smem[];
+  float* sQ = smem;                  // [kTR][LD]   phi(q) of the block
+  float* sG = sQ + kTR * LD;         // [kTR][LD]   dnum of the block
+  float* sK = sG + kTR * LD;         // [kTC][LD]   phi(k) of the tile
+  float* sV = sK + kTC * LD;         // [kTC][LD]   v of the tile
+  float* sA = sV + kTC * LD;         // [kTR][kTAL] A (pass A), M (.) dA (pass B)
+  float* sPt = sA + kTR * kTAL;      // [kTC]       P of the tile (LION-S)
+  const int L = p.L, bh = blockIdx.x, h = bh % p.H, i0 = blockIdx.y * kTR;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const bool ms = p.mask_kind == MASK_S;
+  const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
+  const float* Ph = ms ? p.P + (size_t)bh * L : nullptr;
+  const float* fkh = p.fk + (size_t)bh * L * D;
+  const T* vh = head_of<T>(p.v, bh, L, D);
+  stage_rows<D>(sQ, p.fq + (size_t)bh * L * D, i0, kTR, L);
+  int ia[4];
+  bool live[4];
+  float Pi[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    ia[a] = i0 + ty + 8 * a;
+    live[a] = ia[a] < L;
+    Pi[a] = ms && live[a] ? Ph[ia[a]] : 0.f;
+  }
+  // ---- pass A: den_i and num_i
+  float den[4], num[4][MF];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    den[a] = 0.f;
+#pragma unroll
+    for (int f = 0; f < MF; ++f) num[a][f] = 0.f;
+  }
+  for (int j0 = 0; j0 < L; j0 += kTC) {
+    stage_rows<D>(sK, fkh, j0, kTC, L);
+    stage_rows<D>(sV, vh, j0, kTC, L);
+    if (ms) stage_vec(sPt, Ph, j0, kTC, L);
+    __syncthreads();
+    float s[4][4];
+    tile_scores<D>(sQ, sK, ty, tx, s);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int jl = tx + 16 * b, j = j0 + jl;
+        const float m = live[a] && j < L ? mask_value(p.mask_kind, ia[a], j, Pi[a], sPt[jl], lh) : 0.f;
+        const float x = m * s[a][b];
+        den[a] += x;
+        sA[(ty + 8 * a) * kTAL + jl] = x;
+      }
+    __syncthreads();
+    tile_apply<D>(sA, sV, (min(kTC, L - j0) + 3) & ~3, ty, tx, num);
+    __syncthreads();
+  }
+  // ---- y_i, dnum_i = dy_i / den_i, dden_i = -(dy_i . y_i) / den_i
+  float hi[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const float dn = group_sum<16>(den[a]);
+    const float* dyr = p.dy + ((size_t)bh * L + (live[a] ? ia[a] : 0)) * D;
+    float dyy = 0.f, gi[MF];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 d4 = live[a] ? load4(dyr + 4 * tx + 64 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float d = elem(d4, e);
+        dyy += d * (num[a][4 * u + e] / dn);
+        gi[4 * u + e] = live[a] ? d / dn : 0.f;
+      }
+    }
+    dyy = group_sum<16>(dyy);
+    hi[a] = live[a] ? -dyy / dn : 0.f;
+    float* gs = sG + (ty + 8 * a) * LD;
+    float* gw = p.g + ((size_t)bh * L + (live[a] ? ia[a] : 0)) * D;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 g4 = make_float4(gi[4 * u], gi[4 * u + 1], gi[4 * u + 2], gi[4 * u + 3]);
+      *reinterpret_cast<float4*>(gs + 4 * tx + 64 * u) = g4;
+      if (live[a]) *reinterpret_cast<float4*>(gw + 4 * tx + 64 * u) = g4;
+    }
+    if (live[a] && tx == 0) p.hd[(size_t)bh * L + ia[a]] = hi[a];
+  }
+  // ---- pass B: dphi(q_i) and the row terms of dLoss/dP
+  float dfq[4][MF], rowl[4], rowu[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    rowl[a] = rowu[a] = 0.f;
+#pragma unroll
+    for (int f = 0; f < MF; ++f) dfq[a][f] = 0.f;
+  }
+  for (int j0 = 0; j0 < L; j0 += kTC) {
+    stage_rows<D>(sK, fkh, j0, kTC, L);
+    stage_rows<D>(sV, vh, j0, kTC, L);
+    if (ms) stage_vec(sPt, Ph, j0, kTC, L);
+    __syncthreads();
+    float s[4][4], gv[4][4];
+    tile_scores<D>(sQ, sK, ty, tx, s);
+    tile_scores<D>(sG, sV, ty, tx, gv);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int jl = tx + 16 * b, j = j0 + jl;
+        const float m = live[a] && j < L ? mask_value(p.mask_kind, ia[a], j, Pi[a], sPt[jl], lh) : 0.f;
+        const float da = gv[a][b] + hi[a], c = m * s[a][b] * da;
+        sA[(ty + 8 * a) * kTAL + jl] = m * da;
+        if (j < ia[a]) rowl[a] += c;
+        else if (j > ia[a]) rowu[a] += c;
+      }
+    __syncthreads();
+    tile_apply<D>(sA, sK, (min(kTC, L - j0) + 3) & ~3, ty, tx, dfq);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const float rl = group_sum<16>(rowl[a]), ru = group_sum<16>(rowu[a]);
+    // dead rows run on row L-1's inputs with dfq = 0 and store nothing; every
+    // thread takes part in its group's shuffles
+    const T* qr = head_of<T>(p.q, bh, L, D) + (size_t)(live[a] ? ia[a] : L - 1) * D;
+    float x[MF], dx[MF];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 x4 = load4(qr + 4 * tx + 64 * u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[4 * u + e] = elem(x4, e);
+    }
+    phi_backward<MF, 16>(p.phi, x, dfq[a], dx);
+    if (live[a]) {
+      float* dq = p.dq + ((size_t)bh * L + ia[a]) * D;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        *reinterpret_cast<float4*>(dq + 4 * tx + 64 * u) =
+            make_float4(dx[4 * u], dx[4 * u + 1], dx[4 * u + 2], dx[4 * u + 3]);
+      if (tx == 0) p.rowd[(size_t)bh * L + ia[a]] = rl - ru;
+    }
+  }
+}
+
+// (3) columns, tiled: 32 keys per CTA.
+template <typename T, int D>
+__global__ void __launch_bounds__(kTThreads) bwd_cols_tiled(BwdParams p) {
+  constexpr int LD = D + 4, MF = D / 16, U = D / 64;
+  extern __shared__ __align__(16) float smem[];
+  float* sK = smem;                  // [kTR][LD]   phi(k) of the block
+  float* sVb = sK + kTR * LD;        // [kTR][LD]   v of the block
+  float* sQ = sVb + kTR * LD;        // [kTC][LD]   phi(q) of the tile
+  float* sG = sQ + kTC * LD;         // [kTC][LD]   dnum of the tile
+  float* sA = sG + kTC * LD;         // [kTR][kTAL] A^T
+  float* sD = sA + kTR * kTAL;       // [kTR][kTAL] (M (.) dA)^T
+  float* sHt = sD + kTR * kTAL;      // [kTC]       dden of the tile
+  float* sPt = sHt + kTC;            // [kTC]       P of the tile (LION-S)
+  const int L = p.L, bh = blockIdx.x, h = bh % p.H, j0b = blockIdx.y * kTR;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const bool ms = p.mask_kind == MASK_S;
+  const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
+  const float* Ph = ms ? p.P + (size_t)bh * L : nullptr;
+  const float* fqh = p.fq + (size_t)bh * L * D;
+  const float* gh = p.g + (size_t)bh * L * D;
+  const float* hh = p.hd + (size_t)bh * L;
+  stage_rows<D>(sK, p.fk + (size_t)bh * L * D, j0b, kTR, L);
+  stage_rows<D>(sVb, head_of<T>(p.v, bh, L, D), j0b, kTR, L);
+  int ja[4];
+  bool live[4];
+  float Pj[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    ja[a] = j0b + ty + 8 * a;
+    live[a] = ja[a] < L;
+    Pj[a] = ms && live[a] ? Ph[ja[a]] : 0.f;
+  }
+  float dfk[4][MF], dvj[4][MF], coll[4], colu[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    coll[a] = colu[a] = 0.f;
+#pragma unroll
+    for (int f = 0; f < MF; ++f) dfk[a][f] = dvj[a][f] = 0.f;
+  }
+  for (int i0 = 0; i0 < L; i0 += kTC) {
+    stage_rows<D>(sQ, fqh, i0, kTC, L);
+    stage_rows<D>(sG, gh, i0, kTC, L);
+    stage_vec(sHt, hh, i0, kTC, L);
+    if (ms) stage_vec(sPt, Ph, i0, kTC, L);
+    __syncthreads();
+    float s[4][4], gv[4][4];
+    tile_scores<D>(sK, sQ, ty, tx, s);
+    tile_scores<D>(sVb, sG, ty, tx, gv);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int il = tx + 16 * b, i = i0 + il;
+        const float m = live[a] && i < L ? mask_value(p.mask_kind, i, ja[a], sPt[il], Pj[a], lh) : 0.f;
+        const float x = m * s[a][b], da = gv[a][b] + sHt[il], c = x * da;
+        sA[(ty + 8 * a) * kTAL + il] = x;
+        sD[(ty + 8 * a) * kTAL + il] = m * da;
+        if (i > ja[a]) coll[a] += c;
+        else if (i < ja[a]) colu[a] += c;
+      }
+    __syncthreads();
+    const int n4 = (min(kTC, L - i0) + 3) & ~3;
+    tile_apply<D>(sD, sQ, n4, ty, tx, dfk);
+    tile_apply<D>(sA, sG, n4, ty, tx, dvj);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const float cl = group_sum<16>(coll[a]), cu = group_sum<16>(colu[a]);
+    const T* kr = head_of<T>(p.k, bh, L, D) + (size_t)(live[a] ? ja[a] : L - 1) * D;
+    float x[MF], dx[MF];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 x4 = load4(kr + 4 * tx + 64 * u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[4 * u + e] = elem(x4, e);
+    }
+    phi_backward<MF, 16>(p.phi, x, dfk[a], dx);
+    if (live[a]) {
+      float* dk = p.dk + ((size_t)bh * L + ja[a]) * D;
+      float* dv = p.dv + ((size_t)bh * L + ja[a]) * D;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        *reinterpret_cast<float4*>(dk + 4 * tx + 64 * u) =
+            make_float4(dx[4 * u], dx[4 * u + 1], dx[4 * u + 2], dx[4 * u + 3]);
+        *reinterpret_cast<float4*>(dv + 4 * tx + 64 * u) =
+            make_float4(dvj[a][4 * u], dvj[a][4 * u + 1], dvj[a][4 * u + 2], dvj[a][4 * u + 3]);
+      }
+      if (tx == 0) p.cold[(size_t)bh * L + ja[a]] = cu - cl;
+    }
+  }
+}
+
 // (4) dl of one head (one CTA): dLoss/dP_m = rowd_m + cold_m; LION-S writes
 // the suffix sums (position 0: 0), LION-D the total sum_m m dLoss/dP_m.
 constexpr int kDlThreads = 256;
@@ -428,16 +807,31 @@ cudaError_t bwd_launch(const BwdParams& p, cudaStream_t s) {
   bwd_phi_kernel<T, D><<<(unsigned)((2 * rows * 32 + 255) / 256), 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t sp = p.mask_kind == MASK_S ? (size_t)p.L : 0;
-  const size_t smem_r = sizeof(float) * ((size_t)kRows * (D + 8) + 2 * kTile * D + sp);
-  const size_t smem_c = sizeof(float) * (2 * (size_t)kRows * (D + 8) + 2 * kTile * D + kTile + sp);
-  if ((e = allow(bwd_rows_kernel<T, D>, smem_r)) != cudaSuccess) return e;
-  if ((e = allow(bwd_cols_kernel<T, D>, smem_c)) != cudaSuccess) return e;
-  const dim3 grid(p.B * p.H, (p.L + kRows - 1) / kRows);
-  bwd_rows_kernel<T, D><<<grid, 256, smem_r, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_cols_kernel<T, D><<<grid, 256, smem_c, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if constexpr (D >= 64) {
+    if (p.mask_kind == MASK_S) {
+      bwd_prefix_kernel<<<p.B * p.H, kPrefixThreads, 0, s>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    constexpr size_t smem_r = rows_tiled_smem<D>(), smem_c = cols_tiled_smem<D>();
+    if ((e = allow(bwd_rows_tiled<T, D>, smem_r)) != cudaSuccess) return e;
+    if ((e = allow(bwd_cols_tiled<T, D>, smem_c)) != cudaSuccess) return e;
+    const dim3 grid(p.B * p.H, (p.L + kTR - 1) / kTR);
+    bwd_rows_tiled<T, D><<<grid, kTThreads, smem_r, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_cols_tiled<T, D><<<grid, kTThreads, smem_c, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
+    const size_t sp = p.mask_kind == MASK_S ? (size_t)p.L : 0;
+    const size_t smem_r = sizeof(float) * ((size_t)kRows * (D + 8) + 2 * kTile * D + sp);
+    const size_t smem_c = sizeof(float) * (2 * (size_t)kRows * (D + 8) + 2 * kTile * D + kTile + sp);
+    if ((e = allow(bwd_rows_kernel<T, D>, smem_r)) != cudaSuccess) return e;
+    if ((e = allow(bwd_cols_kernel<T, D>, smem_c)) != cudaSuccess) return e;
+    const dim3 grid(p.B * p.H, (p.L + kRows - 1) / kRows);
+    bwd_rows_kernel<T, D><<<grid, 256, smem_r, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_cols_kernel<T, D><<<grid, 256, smem_c, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (p.mask_kind != MASK_LIT) {
     bwd_dl_kernel<<<p.B * p.H, kDlThreads, 0, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -455,7 +849,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 size_t bwd_workspace_bytes(int B, int H, int L, int d) {
   const size_t BH = (size_t)B * H, n = BH * L;
-  return 3 * align256(sizeof(float) * n * d) + 3 * align256(sizeof(float) * n) + align256(sizeof(double) * BH);
+  return 3 * align256(sizeof(float) * n * d) + 4 * align256(sizeof(float) * n) + align256(sizeof(double) * BH);
 }
 
 cudaError_t launch_bwd(const Problem& pr, const float* dy, float* dq, float* dk, float* dv, float* dll, void* ws,
@@ -490,6 +884,8 @@ cudaError_t launch_bwd(const Problem& pr, const float* dy, float* dq, float* dk,
   p.cold = reinterpret_cast<float*>(w);
   w += align256(sizeof(float) * n);
   p.dsum = reinterpret_cast<double*>(w);
+  w += align256(sizeof(double) * BH);
+  p.P = reinterpret_cast<float*>(w);
   const bool bf = pr.dtype == DT_BF16;
   switch (pr.d) {
     case 16: return bf ? bwd_launch<__nv_bfloat16, 16>(p, s) : bwd_launch<float, 16>(p, s);

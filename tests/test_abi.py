@@ -60,9 +60,9 @@ def test_workspace_query(lib):
 
 def test_bwd_workspace_query(lib):
     from bidirectional_masked_linear_gb300 import lion
-    # phi(q), phi(k) and dnum (L*d floats each), three per-token floats, a double per head
+    # phi(q), phi(k) and dnum (L*d floats each), four per-token floats, a double per head
     need = lion.bwd_workspace_bytes(2, 3, 10, 64)
-    assert need >= 2 * 3 * 10 * (3 * 64 + 3) * 4 + 2 * 3 * 8
+    assert need >= 2 * 3 * 10 * (3 * 64 + 4) * 4 + 2 * 3 * 8
     assert lion.bwd_workspace_bytes(0, 3, 10, 64) == 0
     assert lion.bwd_workspace_bytes(1, 1, 10, 48) == 0
 

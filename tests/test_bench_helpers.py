@@ -54,6 +54,15 @@ def test_backward_flops_and_peak():
     assert abs(bench.FP32_ALU_PEAK_TFLOPS - 80.54) < 0.01
 
 
+def test_backward_launch_counts():
+    # phi, rows, columns; + dl (D, S); + batch sum (D); + prefix (S, tiled d >= 64)
+    assert bench.bwd_launches("lit", 64) == 3
+    assert bench.bwd_launches("d", 64) == 5
+    assert bench.bwd_launches("s", 64) == 5
+    assert bench.bwd_launches("s", 32) == 4
+    assert bench.bwd_launches("d", 16) == 5
+
+
 def test_stream_bytes():
     # ViT-B heads, d = 64: S and z read and written in fp32, bf16 q, k, v in
     assert bench.stream_bytes(64, 12, 64) == 64 * 12 * (2 * (64 * 64 + 64) * 4 + 3 * 64 * 2 + 4 + 64 * 4 + 4)
