@@ -49,6 +49,18 @@ __device__ __forceinline__ float group_sum(float x) {
   return x;
 }
 
+// Four consecutive features as fp32 (16-byte aligned for fp32, 8 for bf16).
+__device__ __forceinline__ float4 load4(const float* src) { return *reinterpret_cast<const float4*>(src); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* src) {
+  const uint2 u = *reinterpret_cast<const uint2*>(src);
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ float elem(const float4& x, int e) {
+  return e == 0 ? x.x : e == 1 ? x.y : e == 2 ? x.z : x.w;
+}
+
 // Inclusive prefix of l over the head into sP[0..L) (LION-S), whole block.
 __device__ void prefix_log_lambda(const float* ll, int L, float* sP, float* scratch) {
   const int T = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -147,46 +159,37 @@ struct BwdParams {
   float* cold;   // [BH][L]    column terms of dLoss/dP
   double* dsum;  // [BH]       LION-D: sum over positions of dl
   float* P;      // [BH][L]    LION-S: inclusive prefix of l (tiled passes)
+  // stored-tile build (L <= kBwdStoreMaxL): A_ij and M_ij dA_ij transposed,
+  // [BH][L (j)][LP (i)], and the rows pass's column terms per block of 32 rows
+  float* At;
+  float* Dt;
+  float* colpart;  // [BH][nblk][L]
+  int LP, nblk;
 };
 
-// (1) phi(q), phi(k): one warp per row.
+// (1) phi(q), phi(k): D/4 adjacent lanes per row, four features a lane.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_phi_kernel(BwdParams p) {
-  const long warp = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  constexpr int W = D / 4;   // divides 32: a row's lanes never straddle a warp
+  const long t = (long)blockIdx.x * blockDim.x + threadIdx.x;
   const long rows = (long)p.B * p.H * p.L;
-  if (warp >= 2 * rows) return;
-  const bool isq = warp < rows;
-  const long r = isq ? warp : warp - rows;
-  const T* src = reinterpret_cast<const T*>(isq ? p.q : p.k) + (size_t)r * D;
-  float* dst = (isq ? p.fq : p.fk) + (size_t)r * D;
-  constexpr int NL = (D + 31) / 32;
-  float x[NL];
-#pragma unroll
-  for (int c = 0; c < NL; ++c) {
-    const int m = lane + 32 * c;
-    x[c] = m < D ? to_f32(src[m]) : 0.f;
-  }
+  // lanes past the last row work on it without storing, so that every lane
+  // takes part in its group's shuffles
+  const bool ok = t / W < 2 * rows;
+  const long r = ok ? t / W : 2 * rows - 1;
+  const int c = (int)(t % W) * 4;
+  const bool isq = r < rows;
+  const long rr = isq ? r : r - rows;
+  float4 x = load4(reinterpret_cast<const T*>(isq ? p.q : p.k) + (size_t)rr * D + c);
   if (p.phi == PHI_ELU1) {
-#pragma unroll
-    for (int c = 0; c < NL; ++c) x[c] = elu1(x[c]);
+    x = make_float4(elu1(x.x), elu1(x.y), elu1(x.z), elu1(x.w));
   } else if (p.phi == PHI_SILU_L2) {
-    float ss = 0.f;
-#pragma unroll
-    for (int c = 0; c < NL; ++c) {
-      const int m = lane + 32 * c;
-      x[c] = m < D ? silu(x[c]) : 0.f;
-      ss += x[c] * x[c];
-    }
-    const float inv = 1.f / fmaxf(sqrtf(warp_sum(ss)), 1e-12f);
-#pragma unroll
-    for (int c = 0; c < NL; ++c) x[c] *= inv;
+    x = make_float4(silu(x.x), silu(x.y), silu(x.z), silu(x.w));
+    const float ss = group_sum<W>(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
+    const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+    x = make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
   }
-#pragma unroll
-  for (int c = 0; c < NL; ++c) {
-    const int m = lane + 32 * c;
-    if (m < D) dst[m] = x[c];
-  }
+  if (ok) *reinterpret_cast<float4*>((isq ? p.fq : p.fk) + (size_t)rr * D + c) = x;
 }
 
 __device__ __forceinline__ void load_tile(float* dst, int ld, const float* src, int row0, int rows, int L, int D) {
@@ -395,16 +398,6 @@ constexpr int kTC = 64;            // tokens of a tile of the other side
 constexpr int kTAL = kTC + 16;     // row stride of the staged score tiles (floats)
 constexpr int kTThreads = 128;
 
-__device__ __forceinline__ float4 load4(const float* src) { return *reinterpret_cast<const float4*>(src); }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16* src) {
-  const uint2 u = *reinterpret_cast<const uint2*>(src);
-  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-  return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
-__device__ __forceinline__ float elem(const float4& x, int e) {
-  return e == 0 ? x.x : e == 1 ? x.y : e == 2 ? x.z : x.w;
-}
 
 // Rows [row0, row0 + nrows) of a [L][D] head array into dst (row stride
 // D + 4 floats), zero past L.  Whole block.
@@ -421,25 +414,22 @@ __device__ __forceinline__ void stage_vec(float* dst, const float* src, int row0
   for (int t = threadIdx.x; t < n; t += blockDim.x) dst[t] = row0 + t < L ? src[row0 + t] : 0.f;
 }
 
-// acc[a][b] = sum_m X[ty + 8a][m] Y[tx + 16b][m]
-template <int D>
-__device__ __forceinline__ void tile_scores(const float* X, const float* Y, int ty, int tx, float (&acc)[4][4]) {
+// acc[a][b] = sum_m X[ty + 8a][m] Y[tx + 16b][m] for a < NA, b < NB (the
+// caller zeroes acc)
+template <int D, int NA, int NB>
+__device__ __forceinline__ void tile_scores_n(const float* X, const float* Y, int ty, int tx, float (&acc)[4][4]) {
   constexpr int LD = D + 4;
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 #pragma unroll 4
   for (int m = 0; m < D; m += 4) {
-    float4 x[4], y[4];
+    float4 x[NA], y[NB];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) x[a] = *reinterpret_cast<const float4*>(X + (ty + 8 * a) * LD + m);
+    for (int a = 0; a < NA; ++a) x[a] = *reinterpret_cast<const float4*>(X + (ty + 8 * a) * LD + m);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) y[b] = *reinterpret_cast<const float4*>(Y + (tx + 16 * b) * LD + m);
+    for (int b = 0; b < NB; ++b) y[b] = *reinterpret_cast<const float4*>(Y + (tx + 16 * b) * LD + m);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < NA; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
+      for (int b = 0; b < NB; ++b) {
         float t = acc[a][b];
         t = fmaf(x[a].x, y[b].x, t);
         t = fmaf(x[a].y, y[b].y, t);
@@ -449,24 +439,53 @@ __device__ __forceinline__ void tile_scores(const float* X, const float* Y, int 
   }
 }
 
-// out[a][4u + e] += sum_{t < n} S[ty + 8a][t] Z[t][4tx + 64u + e]; n is a
-// multiple of 4 and S is zero from the last real token to n.
+// Row (column) slices a thread needs when only the first nr rows of X (nc of
+// Y) are real tokens: 1, 2 or all 4 (uniform over the CTA).
+__device__ __forceinline__ int slices(int n, int step) { return n > 2 * step ? 4 : n > step ? 2 : 1; }
+
+// acc[a][b] = sum_m X[ty + 8a][m] Y[tx + 16b][m]; entries whose row is past
+// nr or whose column is past nc are left 0.
 template <int D>
-__device__ __forceinline__ void tile_apply(const float* S, const float* Z, int n, int ty, int tx,
-                                           float (&out)[4][D / 16]) {
+__device__ __forceinline__ void tile_scores(const float* X, const float* Y, int ty, int tx, int nr, int nc,
+                                            float (&acc)[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+  const int na = slices(nr, 8), nb = slices(nc, 16);
+  if (na == 4) {
+    if (nb == 4) tile_scores_n<D, 4, 4>(X, Y, ty, tx, acc);
+    else if (nb == 2) tile_scores_n<D, 4, 2>(X, Y, ty, tx, acc);
+    else tile_scores_n<D, 4, 1>(X, Y, ty, tx, acc);
+  } else if (na == 2) {
+    if (nb == 4) tile_scores_n<D, 2, 4>(X, Y, ty, tx, acc);
+    else if (nb == 2) tile_scores_n<D, 2, 2>(X, Y, ty, tx, acc);
+    else tile_scores_n<D, 2, 1>(X, Y, ty, tx, acc);
+  } else {
+    if (nb == 4) tile_scores_n<D, 1, 4>(X, Y, ty, tx, acc);
+    else if (nb == 2) tile_scores_n<D, 1, 2>(X, Y, ty, tx, acc);
+    else tile_scores_n<D, 1, 1>(X, Y, ty, tx, acc);
+  }
+}
+
+// out[a][4u + e] += sum_{t < n} S[ty + 8a][t] Z[t][4tx + 64u + e] for a < NA;
+// n is a multiple of 4 and S is zero from the last real token to n.
+template <int D, int NA>
+__device__ __forceinline__ void tile_apply_n(const float* S, const float* Z, int n, int ty, int tx,
+                                             float (&out)[4][D / 16]) {
   constexpr int LD = D + 4, U = D / 64;
 #pragma unroll 2
   for (int t = 0; t < n; t += 4) {
-    float4 s[4];
+    float4 s[NA];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) s[a] = *reinterpret_cast<const float4*>(S + (ty + 8 * a) * kTAL + t);
+    for (int a = 0; a < NA; ++a) s[a] = *reinterpret_cast<const float4*>(S + (ty + 8 * a) * kTAL + t);
 #pragma unroll
     for (int e = 0; e < 4; ++e)
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float4 z = *reinterpret_cast<const float4*>(Z + (t + e) * LD + 4 * tx + 64 * u);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < NA; ++a) {
           const float w = elem(s[a], e);
           out[a][4 * u + 0] = fmaf(w, z.x, out[a][4 * u + 0]);
           out[a][4 * u + 1] = fmaf(w, z.y, out[a][4 * u + 1]);
@@ -476,6 +495,15 @@ __device__ __forceinline__ void tile_apply(const float* S, const float* Z, int n
       }
   }
 }
+// The same for the first nr rows of S (the rows past nr keep their values).
+template <int D>
+__device__ __forceinline__ void tile_apply(const float* S, const float* Z, int n, int ty, int tx, int nr,
+                                           float (&out)[4][D / 16]) {
+  const int na = slices(nr, 8);
+  if (na == 4) tile_apply_n<D, 4>(S, Z, n, ty, tx, out);
+  else if (na == 2) tile_apply_n<D, 2>(S, Z, n, ty, tx, out);
+  else tile_apply_n<D, 1>(S, Z, n, ty, tx, out);
+}
 
 // M_ij of query i and key j (Pi, Pj: the prefix at i and j for LION-S).
 __device__ __forceinline__ float mask_value(int mask_kind, int i, int j, float Pi, float Pj, float lh) {
@@ -484,22 +512,41 @@ __device__ __forceinline__ float mask_value(int mask_kind, int i, int j, float P
   return 1.f;
 }
 
+// Inclusive scan of x over a block of kScanThreads threads in double (lane
+// shuffles, then the warp totals); *total receives the block's sum.
+constexpr int kScanThreads = 256;
+__device__ __forceinline__ double block_scan(double x, double* total) {
+  __shared__ double warp_tot[kScanThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  double off = 0.0, all = 0.0;
+#pragma unroll
+  for (int u = 0; u < kScanThreads / 32; ++u) {
+    off += u < warp ? warp_tot[u] : 0.0;
+    all += warp_tot[u];
+  }
+  *total = all;
+  return x + off;
+}
+
 // LION-S: the inclusive prefix of l per head into P (one CTA per head),
 // accumulated in double and stored in fp32.
-constexpr int kPrefixThreads = 256;
+constexpr int kPrefixThreads = kScanThreads;
 __global__ void __launch_bounds__(kPrefixThreads) bwd_prefix_kernel(BwdParams p) {
-  __shared__ double tot[kPrefixThreads];
   const int L = p.L, bh = blockIdx.x, t = threadIdx.x;
   const float* ll = p.log_lambda + (size_t)bh * L;
   float* P = p.P + (size_t)bh * L;
   const int per = (L + kPrefixThreads - 1) / kPrefixThreads;
   const int lo = min(L, t * per), hi = min(L, lo + per);
-  double run = 0.0;
+  double run = 0.0, all;
   for (int m = lo; m < hi; ++m) run += (double)ll[m];
-  tot[t] = run;
-  __syncthreads();
-  double off = 0.0;
-  for (int u = 0; u < t; ++u) off += tot[u];
+  double off = block_scan(run, &all) - run;
   for (int m = lo; m < hi; ++m) {
     off += (double)ll[m];
     P[m] = (float)off;
@@ -507,16 +554,19 @@ __global__ void __launch_bounds__(kPrefixThreads) bwd_prefix_kernel(BwdParams p)
 }
 
 template <int D>
-constexpr size_t rows_tiled_smem() {
-  return sizeof(float) * ((size_t)(2 * kTR + 2 * kTC) * (D + 4) + kTR * kTAL + kTC);
+constexpr size_t rows_tiled_smem(bool store) {
+  return sizeof(float) * ((size_t)(2 * kTR + 2 * kTC) * (D + 4) + (store ? 2 : 1) * kTR * kTAL + kTC);
 }
 template <int D>
 constexpr size_t cols_tiled_smem() {
   return sizeof(float) * ((size_t)(2 * kTR + 2 * kTC) * (D + 4) + 2 * kTR * kTAL + 2 * kTC);
 }
 
-// (2) rows, tiled: 32 queries per CTA.
-template <typename T, int D>
+// (2) rows, tiled: 32 queries per CTA.  STORE: pass A writes A_ij and pass
+// B reads it back instead of recomputing the scores, writes M_ij dA_ij, and
+// sums the column terms of its 32 rows per key (the columns pass then needs
+// no scores of its own).
+template <typename T, int D, bool STORE>
 __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
   constexpr int LD = D + 4, MF = D / 16, U = D / 64;
   extern __shared__ __align__(16) float smem[];
@@ -526,7 +576,10 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
   float* sV = sK + kTC * LD;         // [kTC][LD]   v of the tile
   float* sA = sV + kTC * LD;         // [kTR][kTAL] A (pass A), M (.) dA (pass B)
   float* sPt = sA + kTR * kTAL;      // [kTC]       P of the tile (LION-S)
-  const int L = p.L, bh = blockIdx.x, h = bh % p.H, i0 = blockIdx.y * kTR;
+  float* sC = sPt + kTC;             // [kTR][kTAL] signed c_ij (STORE)
+  const int L = p.L, bh = blockIdx.x, h = bh % p.H, i0 = blockIdx.y * kTR, nr = min(kTR, L - i0);
+  float* At = STORE ? p.At + (size_t)bh * L * p.LP : nullptr;
+  float* Dt = STORE ? p.Dt + (size_t)bh * L * p.LP : nullptr;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const bool ms = p.mask_kind == MASK_S;
   const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
@@ -556,8 +609,9 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
     stage_rows<D>(sV, vh, j0, kTC, L);
     if (ms) stage_vec(sPt, Ph, j0, kTC, L);
     __syncthreads();
+    const int nc = min(kTC, L - j0);
     float s[4][4];
-    tile_scores<D>(sQ, sK, ty, tx, s);
+    tile_scores<D>(sQ, sK, ty, tx, nr, nc, s);
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -567,9 +621,10 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
         const float x = m * s[a][b];
         den[a] += x;
         sA[(ty + 8 * a) * kTAL + jl] = x;
+        if (STORE && live[a] && j < L) At[(size_t)j * p.LP + ia[a]] = x;
       }
     __syncthreads();
-    tile_apply<D>(sA, sV, (min(kTC, L - j0) + 3) & ~3, ty, tx, num);
+    tile_apply<D>(sA, sV, (nc + 3) & ~3, ty, tx, nr, num);
     __syncthreads();
   }
   // ---- y_i, dnum_i = dy_i / den_i, dden_i = -(dy_i . y_i) / den_i
@@ -614,22 +669,45 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
     stage_rows<D>(sV, vh, j0, kTC, L);
     if (ms) stage_vec(sPt, Ph, j0, kTC, L);
     __syncthreads();
+    const int nc = min(kTC, L - j0);
     float s[4][4], gv[4][4];
-    tile_scores<D>(sQ, sK, ty, tx, s);
-    tile_scores<D>(sG, sV, ty, tx, gv);
+    if (STORE) {   // A_ij as this thread wrote it in pass A
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int j = j0 + tx + 16 * b;
+          s[a][b] = live[a] && j < L ? At[(size_t)j * p.LP + ia[a]] : 0.f;
+        }
+    } else {
+      tile_scores<D>(sQ, sK, ty, tx, nr, nc, s);
+    }
+    tile_scores<D>(sG, sV, ty, tx, nr, nc, gv);
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int jl = tx + 16 * b, j = j0 + jl;
         const float m = live[a] && j < L ? mask_value(p.mask_kind, ia[a], j, Pi[a], sPt[jl], lh) : 0.f;
-        const float da = gv[a][b] + hi[a], c = m * s[a][b] * da;
-        sA[(ty + 8 * a) * kTAL + jl] = m * da;
+        const float x = STORE ? s[a][b] : m * s[a][b];
+        const float da = gv[a][b] + hi[a], c = x * da, ds = m * da;
+        sA[(ty + 8 * a) * kTAL + jl] = ds;
+        if (STORE) {
+          sC[(ty + 8 * a) * kTAL + jl] = j > ia[a] ? c : j < ia[a] ? -c : 0.f;
+          if (live[a] && j < L) Dt[(size_t)j * p.LP + ia[a]] = ds;
+        }
         if (j < ia[a]) rowl[a] += c;
         else if (j > ia[a]) rowu[a] += c;
       }
     __syncthreads();
-    tile_apply<D>(sA, sK, (min(kTC, L - j0) + 3) & ~3, ty, tx, dfq);
+    tile_apply<D>(sA, sK, (nc + 3) & ~3, ty, tx, nr, dfq);
+    if (STORE) {   // sum over this block's rows of the signed column terms
+      for (int t = threadIdx.x; t < nc; t += kTThreads) {
+        float cs = 0.f;
+        for (int r = 0; r < nr; ++r) cs += sC[r * kTAL + t];
+        p.colpart[((size_t)bh * p.nblk + blockIdx.y) * L + j0 + t] = cs;
+      }
+    }
     __syncthreads();
   }
 #pragma unroll
@@ -670,7 +748,7 @@ __global__ void __launch_bounds__(kTThreads) bwd_cols_tiled(BwdParams p) {
   float* sD = sA + kTR * kTAL;       // [kTR][kTAL] (M (.) dA)^T
   float* sHt = sD + kTR * kTAL;      // [kTC]       dden of the tile
   float* sPt = sHt + kTC;            // [kTC]       P of the tile (LION-S)
-  const int L = p.L, bh = blockIdx.x, h = bh % p.H, j0b = blockIdx.y * kTR;
+  const int L = p.L, bh = blockIdx.x, h = bh % p.H, j0b = blockIdx.y * kTR, nr = min(kTR, L - j0b);
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const bool ms = p.mask_kind == MASK_S;
   const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
@@ -702,9 +780,10 @@ __global__ void __launch_bounds__(kTThreads) bwd_cols_tiled(BwdParams p) {
     stage_vec(sHt, hh, i0, kTC, L);
     if (ms) stage_vec(sPt, Ph, i0, kTC, L);
     __syncthreads();
+    const int nc = min(kTC, L - i0);
     float s[4][4], gv[4][4];
-    tile_scores<D>(sK, sQ, ty, tx, s);
-    tile_scores<D>(sVb, sG, ty, tx, gv);
+    tile_scores<D>(sK, sQ, ty, tx, nr, nc, s);
+    tile_scores<D>(sVb, sG, ty, tx, nr, nc, gv);
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -718,9 +797,9 @@ __global__ void __launch_bounds__(kTThreads) bwd_cols_tiled(BwdParams p) {
         else if (i < ja[a]) colu[a] += c;
       }
     __syncthreads();
-    const int n4 = (min(kTC, L - i0) + 3) & ~3;
-    tile_apply<D>(sD, sQ, n4, ty, tx, dfk);
-    tile_apply<D>(sA, sG, n4, ty, tx, dvj);
+    const int n4 = (nc + 3) & ~3;
+    tile_apply<D>(sD, sQ, n4, ty, tx, nr, dfk);
+    tile_apply<D>(sA, sG, n4, ty, tx, nr, dvj);
     __syncthreads();
   }
 #pragma unroll
@@ -750,9 +829,92 @@ __global__ void __launch_bounds__(kTThreads) bwd_cols_tiled(BwdParams p) {
   }
 }
 
+template <int D>
+constexpr size_t cols_stored_smem() {
+  return sizeof(float) * ((size_t)2 * kTC * (D + 4) + 2 * kTR * kTAL);
+}
+
+// (3) columns from the stored A_ij and M_ij dA_ij: 32 keys per CTA,
+// dphi(k_j) = sum_i M_ij dA_ij phi(q_i) and dv_j = sum_i A_ij dnum_i; the
+// column terms are the sums of the rows pass's per-block partials.
+template <typename T, int D>
+__global__ void __launch_bounds__(kTThreads) bwd_cols_stored(BwdParams p) {
+  constexpr int LD = D + 4, MF = D / 16, U = D / 64, Q4 = kTC / 4;
+  extern __shared__ __align__(16) float smem[];
+  float* sQ = smem;                  // [kTC][LD]   phi(q) of the tile
+  float* sG = sQ + kTC * LD;         // [kTC][LD]   dnum of the tile
+  float* sA = sG + kTC * LD;         // [kTR][kTAL] A^T
+  float* sD = sA + kTR * kTAL;       // [kTR][kTAL] (M (.) dA)^T
+  const int L = p.L, LP = p.LP, bh = blockIdx.x, j0b = blockIdx.y * kTR, nr = min(kTR, L - j0b);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const float* fqh = p.fq + (size_t)bh * L * D;
+  const float* gh = p.g + (size_t)bh * L * D;
+  const float* At = p.At + (size_t)bh * L * LP;
+  const float* Dt = p.Dt + (size_t)bh * L * LP;
+  float dfk[4][MF], dvj[4][MF];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int f = 0; f < MF; ++f) dfk[a][f] = dvj[a][f] = 0.f;
+  for (int i0 = 0; i0 < L; i0 += kTC) {
+    stage_rows<D>(sQ, fqh, i0, kTC, L);
+    stage_rows<D>(sG, gh, i0, kTC, L);
+    // rows j0b.. of A^T and (M (.) dA)^T over the tile's queries; entries
+    // past L (the row padding up to LP, never written) read as 0
+    for (int idx = threadIdx.x; idx < kTR * Q4; idx += kTThreads) {
+      const int r = idx / Q4, c = (idx - r * Q4) * 4, j = j0b + r, i = i0 + c;
+      float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = a4;
+      if (j < L && i < L) {
+        a4 = load4(At + (size_t)j * LP + i);
+        d4 = load4(Dt + (size_t)j * LP + i);
+        if (i + 1 >= L) a4.y = d4.y = 0.f;
+        if (i + 2 >= L) a4.z = d4.z = 0.f;
+        if (i + 3 >= L) a4.w = d4.w = 0.f;
+      }
+      *reinterpret_cast<float4*>(sA + r * kTAL + c) = a4;
+      *reinterpret_cast<float4*>(sD + r * kTAL + c) = d4;
+    }
+    __syncthreads();
+    const int n4 = (min(kTC, L - i0) + 3) & ~3;
+    tile_apply<D>(sD, sQ, n4, ty, tx, nr, dfk);
+    tile_apply<D>(sA, sG, n4, ty, tx, nr, dvj);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int ja = j0b + ty + 8 * a;
+    const bool live = ja < L;
+    const T* kr = head_of<T>(p.k, bh, L, D) + (size_t)(live ? ja : L - 1) * D;
+    float x[MF], dx[MF];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 x4 = load4(kr + 4 * tx + 64 * u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[4 * u + e] = elem(x4, e);
+    }
+    phi_backward<MF, 16>(p.phi, x, dfk[a], dx);
+    if (live) {
+      float* dk = p.dk + ((size_t)bh * L + ja) * D;
+      float* dv = p.dv + ((size_t)bh * L + ja) * D;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        *reinterpret_cast<float4*>(dk + 4 * tx + 64 * u) =
+            make_float4(dx[4 * u], dx[4 * u + 1], dx[4 * u + 2], dx[4 * u + 3]);
+        *reinterpret_cast<float4*>(dv + 4 * tx + 64 * u) =
+            make_float4(dvj[a][4 * u], dvj[a][4 * u + 1], dvj[a][4 * u + 2], dvj[a][4 * u + 3]);
+      }
+      if (tx == 0) {
+        float cs = 0.f;
+        for (int blk = 0; blk < p.nblk; ++blk) cs += p.colpart[((size_t)bh * p.nblk + blk) * L + ja];
+        p.cold[(size_t)bh * L + ja] = cs;
+      }
+    }
+  }
+}
+
 // (4) dl of one head (one CTA): dLoss/dP_m = rowd_m + cold_m; LION-S writes
 // the suffix sums (position 0: 0), LION-D the total sum_m m dLoss/dP_m.
-constexpr int kDlThreads = 256;
+constexpr int kDlThreads = kScanThreads;
 __global__ void __launch_bounds__(kDlThreads) bwd_dl_kernel(BwdParams p) {
   __shared__ double part[kDlThreads];
   const int L = p.L, bh = blockIdx.x, t = threadIdx.x;
@@ -773,12 +935,10 @@ __global__ void __launch_bounds__(kDlThreads) bwd_dl_kernel(BwdParams p) {
     return;
   }
   // suffix sums: this thread's chunk total, then the totals of the chunks to its right
-  double run = 0.0;
+  double run = 0.0, all;
   for (int m = lo; m < hi; ++m) run += (double)rd[m] + (double)cd[m];
-  part[t] = run;
-  __syncthreads();
-  double right = 0.0;
-  for (int u = t + 1; u < kDlThreads; ++u) right += part[u];
+  double right = block_scan(run, &all);
+  right = all - right;
   float* out = p.dll + (size_t)bh * L;
   for (int m = hi - 1; m >= lo; --m) {
     right += (double)rd[m] + (double)cd[m];
@@ -804,7 +964,7 @@ cudaError_t allow(Kern kern, size_t bytes) {
 template <typename T, int D>
 cudaError_t bwd_launch(const BwdParams& p, cudaStream_t s) {
   const long rows = (long)p.B * p.H * p.L;
-  bwd_phi_kernel<T, D><<<(unsigned)((2 * rows * 32 + 255) / 256), 256, 0, s>>>(p);
+  bwd_phi_kernel<T, D><<<(unsigned)((2 * rows * (D / 4) + 255) / 256), 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if constexpr (D >= 64) {
@@ -812,13 +972,22 @@ cudaError_t bwd_launch(const BwdParams& p, cudaStream_t s) {
       bwd_prefix_kernel<<<p.B * p.H, kPrefixThreads, 0, s>>>(p);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    constexpr size_t smem_r = rows_tiled_smem<D>(), smem_c = cols_tiled_smem<D>();
-    if ((e = allow(bwd_rows_tiled<T, D>, smem_r)) != cudaSuccess) return e;
-    if ((e = allow(bwd_cols_tiled<T, D>, smem_c)) != cudaSuccess) return e;
     const dim3 grid(p.B * p.H, (p.L + kTR - 1) / kTR);
-    bwd_rows_tiled<T, D><<<grid, kTThreads, smem_r, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_cols_tiled<T, D><<<grid, kTThreads, smem_c, s>>>(p);
+    if (p.At) {
+      constexpr size_t smem_r = rows_tiled_smem<D>(true), smem_c = cols_stored_smem<D>();
+      if ((e = allow(bwd_rows_tiled<T, D, true>, smem_r)) != cudaSuccess) return e;
+      if ((e = allow(bwd_cols_stored<T, D>, smem_c)) != cudaSuccess) return e;
+      bwd_rows_tiled<T, D, true><<<grid, kTThreads, smem_r, s>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      bwd_cols_stored<T, D><<<grid, kTThreads, smem_c, s>>>(p);
+    } else {
+      constexpr size_t smem_r = rows_tiled_smem<D>(false), smem_c = cols_tiled_smem<D>();
+      if ((e = allow(bwd_rows_tiled<T, D, false>, smem_r)) != cudaSuccess) return e;
+      if ((e = allow(bwd_cols_tiled<T, D>, smem_c)) != cudaSuccess) return e;
+      bwd_rows_tiled<T, D, false><<<grid, kTThreads, smem_r, s>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      bwd_cols_tiled<T, D><<<grid, kTThreads, smem_c, s>>>(p);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else {
     const size_t sp = p.mask_kind == MASK_S ? (size_t)p.L : 0;
@@ -845,11 +1014,21 @@ cudaError_t bwd_launch(const BwdParams& p, cudaStream_t s) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Sequences up to this length keep A and M (.) dA in the workspace (8 L^2
+// bytes a head) instead of recomputing the scores in two more passes.
+constexpr int kBwdStoreMaxL = 1024;
+bool bwd_stores(int L, int d) { return d >= 64 && L <= kBwdStoreMaxL; }
+size_t stored_bytes(size_t BH, int L) {
+  const size_t LP = ((size_t)L + 3) & ~(size_t)3, nblk = ((size_t)L + kTR - 1) / kTR;
+  return 2 * align256(sizeof(float) * BH * L * LP) + align256(sizeof(float) * BH * nblk * L);
+}
+
 }  // namespace
 
 size_t bwd_workspace_bytes(int B, int H, int L, int d) {
   const size_t BH = (size_t)B * H, n = BH * L;
-  return 3 * align256(sizeof(float) * n * d) + 4 * align256(sizeof(float) * n) + align256(sizeof(double) * BH);
+  return 3 * align256(sizeof(float) * n * d) + 4 * align256(sizeof(float) * n) + align256(sizeof(double) * BH) +
+         (bwd_stores(L, d) ? stored_bytes(BH, L) : 0);
 }
 
 cudaError_t launch_bwd(const Problem& pr, const float* dy, float* dq, float* dk, float* dv, float* dll, void* ws,
@@ -886,6 +1065,17 @@ cudaError_t launch_bwd(const Problem& pr, const float* dy, float* dq, float* dk,
   p.dsum = reinterpret_cast<double*>(w);
   w += align256(sizeof(double) * BH);
   p.P = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n);
+  p.LP = (pr.L + 3) & ~3;
+  p.nblk = (pr.L + kTR - 1) / kTR;
+  p.At = p.Dt = p.colpart = nullptr;
+  if (bwd_stores(pr.L, pr.d)) {
+    p.At = reinterpret_cast<float*>(w);
+    w += align256(sizeof(float) * BH * pr.L * p.LP);
+    p.Dt = reinterpret_cast<float*>(w);
+    w += align256(sizeof(float) * BH * pr.L * p.LP);
+    p.colpart = reinterpret_cast<float*>(w);
+  }
   const bool bf = pr.dtype == DT_BF16;
   switch (pr.d) {
     case 16: return bf ? bwd_launch<__nv_bfloat16, 16>(p, s) : bwd_launch<float, 16>(p, s);

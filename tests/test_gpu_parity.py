@@ -340,7 +340,7 @@ def _bwd_check(oracle_mod, B, H, L, d, mask, dtype, phi=0, seed=0, positive=Fals
 @pytest.mark.parametrize("dtype", ("bf16", "fp32"))
 def test_backward_matches_oracle(oracle_mod, mask, dtype):
     for n, (B, H, L, d) in enumerate(((1, 2, 64, 16), (2, 3, 197, 64), (1, 2, 33, 32), (1, 1, 300, 128),
-                                      (1, 2, 515, 64), (2, 1, 7, 64))):
+                                      (1, 2, 515, 64), (2, 1, 7, 64), (1, 1, 1100, 64))):
         _bwd_check(oracle_mod, B, H, L, d, mask, dtype, seed=700 + 10 * n)
 
 
