@@ -159,8 +159,8 @@ struct BwdParams {
   float* cold;   // [BH][L]    column terms of dLoss/dP
   double* dsum;  // [BH]       LION-D: sum over positions of dl
   float* P;      // [BH][L]    LION-S: inclusive prefix of l (tiled passes)
-  // stored-tile build (L <= kBwdStoreMaxL): A_ij and M_ij dA_ij transposed,
-  // [BH][L (j)][LP (i)], and the rows pass's column terms per block of 32 rows
+  // stored-tile build (L <= kBwdStoreMaxL): A_ij and M_ij dA_ij, [BH][L (i)]
+  // [LP (j)], and the rows pass's column terms per block of 32 rows
   float* At;
   float* Dt;
   float* colpart;  // [BH][nblk][L]
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(kPrefixThreads) bwd_prefix_kernel(BwdParams p)
 
 template <int D>
 constexpr size_t rows_tiled_smem(bool store) {
-  return sizeof(float) * ((size_t)(2 * kTR + 2 * kTC) * (D + 4) + (store ? 2 : 1) * kTR * kTAL + kTC);
+  return sizeof(float) * ((size_t)(2 * kTR + 2 * kTC) * (D + 4) + kTR * kTAL + kTC + (store ? 4 * kTC : 0));
 }
 template <int D>
 constexpr size_t cols_tiled_smem() {
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
   float* sV = sK + kTC * LD;         // [kTC][LD]   v of the tile
   float* sA = sV + kTC * LD;         // [kTR][kTAL] A (pass A), M (.) dA (pass B)
   float* sPt = sA + kTR * kTAL;      // [kTC]       P of the tile (LION-S)
-  float* sC = sPt + kTC;             // [kTR][kTAL] signed c_ij (STORE)
+  float* sCol = sPt + kTC;           // [4][kTC]    column terms per warp (STORE)
   const int L = p.L, bh = blockIdx.x, h = bh % p.H, i0 = blockIdx.y * kTR, nr = min(kTR, L - i0);
   float* At = STORE ? p.At + (size_t)bh * L * p.LP : nullptr;
   float* Dt = STORE ? p.Dt + (size_t)bh * L * p.LP : nullptr;
@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
         const float x = m * s[a][b];
         den[a] += x;
         sA[(ty + 8 * a) * kTAL + jl] = x;
-        if (STORE && live[a] && j < L) At[(size_t)j * p.LP + ia[a]] = x;
+        if (STORE && live[a] && j < L) At[(size_t)ia[a] * p.LP + j] = x;
       }
     __syncthreads();
     tile_apply<D>(sA, sV, (nc + 3) & ~3, ty, tx, nr, num);
@@ -665,24 +665,24 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
     for (int f = 0; f < MF; ++f) dfq[a][f] = 0.f;
   }
   for (int j0 = 0; j0 < L; j0 += kTC) {
-    stage_rows<D>(sK, fkh, j0, kTC, L);
-    stage_rows<D>(sV, vh, j0, kTC, L);
-    if (ms) stage_vec(sPt, Ph, j0, kTC, L);
-    __syncthreads();
-    const int nc = min(kTC, L - j0);
     float s[4][4], gv[4][4];
-    if (STORE) {   // A_ij as this thread wrote it in pass A
+    if (STORE) {   // A_ij as this thread wrote it in pass A, in flight during the staging
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const int j = j0 + tx + 16 * b;
-          s[a][b] = live[a] && j < L ? At[(size_t)j * p.LP + ia[a]] : 0.f;
+          s[a][b] = live[a] && j < L ? At[(size_t)ia[a] * p.LP + j] : 0.f;
         }
-    } else {
-      tile_scores<D>(sQ, sK, ty, tx, nr, nc, s);
     }
+    stage_rows<D>(sK, fkh, j0, kTC, L);
+    stage_rows<D>(sV, vh, j0, kTC, L);
+    if (ms) stage_vec(sPt, Ph, j0, kTC, L);
+    __syncthreads();
+    const int nc = min(kTC, L - j0);
+    if (!STORE) tile_scores<D>(sQ, sK, ty, tx, nr, nc, s);
     tile_scores<D>(sG, sV, ty, tx, nr, nc, gv);
+    float cs[4] = {0.f, 0.f, 0.f, 0.f};   // signed column terms of this thread's rows
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -693,21 +693,24 @@ __global__ void __launch_bounds__(kTThreads) bwd_rows_tiled(BwdParams p) {
         const float da = gv[a][b] + hi[a], c = x * da, ds = m * da;
         sA[(ty + 8 * a) * kTAL + jl] = ds;
         if (STORE) {
-          sC[(ty + 8 * a) * kTAL + jl] = j > ia[a] ? c : j < ia[a] ? -c : 0.f;
-          if (live[a] && j < L) Dt[(size_t)j * p.LP + ia[a]] = ds;
+          cs[b] += j > ia[a] ? c : j < ia[a] ? -c : 0.f;
+          if (live[a] && j < L) Dt[(size_t)ia[a] * p.LP + j] = ds;
         }
         if (j < ia[a]) rowl[a] += c;
         else if (j > ia[a]) rowu[a] += c;
       }
-    __syncthreads();
-    tile_apply<D>(sA, sK, (nc + 3) & ~3, ty, tx, nr, dfq);
-    if (STORE) {   // sum over this block's rows of the signed column terms
-      for (int t = threadIdx.x; t < nc; t += kTThreads) {
-        float cs = 0.f;
-        for (int r = 0; r < nr; ++r) cs += sC[r * kTAL + t];
-        p.colpart[((size_t)bh * p.nblk + blockIdx.y) * L + j0 + t] = cs;
+    if (STORE) {   // the two row threads of a column in a warp, then one slot per warp
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        cs[b] += __shfl_xor_sync(0xffffffffu, cs[b], 16);
+        if ((ty & 1) == 0) sCol[(ty >> 1) * kTC + tx + 16 * b] = cs[b];
       }
     }
+    __syncthreads();
+    tile_apply<D>(sA, sK, (nc + 3) & ~3, ty, tx, nr, dfq);
+    if (STORE && threadIdx.x < nc)
+      p.colpart[((size_t)bh * p.nblk + blockIdx.y) * L + j0 + threadIdx.x] =
+          sCol[threadIdx.x] + sCol[kTC + threadIdx.x] + sCol[2 * kTC + threadIdx.x] + sCol[3 * kTC + threadIdx.x];
     __syncthreads();
   }
 #pragma unroll
@@ -829,23 +832,49 @@ __global__ void __launch_bounds__(kTThreads) bwd_cols_tiled(BwdParams p) {
   }
 }
 
+// out[a][4u + e] += sum_{t < n} S[t][4ty + a] Z[t][4tx + 64u + e] (S with
+// row stride lds, its rows read as one float4 a thread: a broadcast)
 template <int D>
-constexpr size_t cols_stored_smem() {
-  return sizeof(float) * ((size_t)2 * kTC * (D + 4) + 2 * kTR * kTAL);
+__device__ __forceinline__ void tile_apply_t(const float* S, int lds, const float* Z, int n, int ty, int tx,
+                                             float (&out)[4][D / 16]) {
+  constexpr int LD = D + 4, U = D / 64;
+#pragma unroll 4
+  for (int t = 0; t < n; ++t) {
+    const float4 s = *reinterpret_cast<const float4*>(S + t * lds + 4 * ty);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 z = *reinterpret_cast<const float4*>(Z + t * LD + 4 * tx + 64 * u);
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const float w = elem(s, a);
+        out[a][4 * u + 0] = fmaf(w, z.x, out[a][4 * u + 0]);
+        out[a][4 * u + 1] = fmaf(w, z.y, out[a][4 * u + 1]);
+        out[a][4 * u + 2] = fmaf(w, z.z, out[a][4 * u + 2]);
+        out[a][4 * u + 3] = fmaf(w, z.w, out[a][4 * u + 3]);
+      }
+    }
+  }
 }
 
-// (3) columns from the stored A_ij and M_ij dA_ij: 32 keys per CTA,
-// dphi(k_j) = sum_i M_ij dA_ij phi(q_i) and dv_j = sum_i A_ij dnum_i; the
-// column terms are the sums of the rows pass's per-block partials.
+constexpr int kTSL = kTR + 4;   // row stride of the stored-tile slices (floats)
+template <int D>
+constexpr size_t cols_stored_smem() {
+  return sizeof(float) * ((size_t)2 * kTC * (D + 4) + 2 * kTC * kTSL);
+}
+
+// (3) columns from the stored A_ij and M_ij dA_ij: 32 keys per CTA, thread
+// (ty, tx) holding keys 4ty + a; dphi(k_j) = sum_i M_ij dA_ij phi(q_i) and
+// dv_j = sum_i A_ij dnum_i; the column terms are the sums of the rows pass's
+// per-block partials.
 template <typename T, int D>
 __global__ void __launch_bounds__(kTThreads) bwd_cols_stored(BwdParams p) {
-  constexpr int LD = D + 4, MF = D / 16, U = D / 64, Q4 = kTC / 4;
+  constexpr int LD = D + 4, MF = D / 16, U = D / 64, J4 = kTR / 4;
   extern __shared__ __align__(16) float smem[];
   float* sQ = smem;                  // [kTC][LD]   phi(q) of the tile
   float* sG = sQ + kTC * LD;         // [kTC][LD]   dnum of the tile
-  float* sA = sG + kTC * LD;         // [kTR][kTAL] A^T
-  float* sD = sA + kTR * kTAL;       // [kTR][kTAL] (M (.) dA)^T
-  const int L = p.L, LP = p.LP, bh = blockIdx.x, j0b = blockIdx.y * kTR, nr = min(kTR, L - j0b);
+  float* sA = sG + kTC * LD;         // [kTC][kTSL] A over the tile's queries x the block's keys
+  float* sD = sA + kTC * kTSL;       // [kTC][kTSL] M (.) dA, the same
+  const int L = p.L, LP = p.LP, bh = blockIdx.x, j0b = blockIdx.y * kTR;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const float* fqh = p.fq + (size_t)bh * L * D;
   const float* gh = p.g + (size_t)bh * L * D;
@@ -859,30 +888,30 @@ __global__ void __launch_bounds__(kTThreads) bwd_cols_stored(BwdParams p) {
   for (int i0 = 0; i0 < L; i0 += kTC) {
     stage_rows<D>(sQ, fqh, i0, kTC, L);
     stage_rows<D>(sG, gh, i0, kTC, L);
-    // rows j0b.. of A^T and (M (.) dA)^T over the tile's queries; entries
-    // past L (the row padding up to LP, never written) read as 0
-    for (int idx = threadIdx.x; idx < kTR * Q4; idx += kTThreads) {
-      const int r = idx / Q4, c = (idx - r * Q4) * 4, j = j0b + r, i = i0 + c;
+    // the block's 32 columns of A and M (.) dA over the tile's rows; entries
+    // past L (rows, and the row padding up to LP that is never written) read as 0
+    for (int idx = threadIdx.x; idx < kTC * J4; idx += kTThreads) {
+      const int r = idx / J4, c = (idx - r * J4) * 4, i = i0 + r, j = j0b + c;
       float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = a4;
-      if (j < L && i < L) {
-        a4 = load4(At + (size_t)j * LP + i);
-        d4 = load4(Dt + (size_t)j * LP + i);
-        if (i + 1 >= L) a4.y = d4.y = 0.f;
-        if (i + 2 >= L) a4.z = d4.z = 0.f;
-        if (i + 3 >= L) a4.w = d4.w = 0.f;
+      if (i < L && j < L) {
+        a4 = load4(At + (size_t)i * LP + j);
+        d4 = load4(Dt + (size_t)i * LP + j);
+        if (j + 1 >= L) a4.y = d4.y = 0.f;
+        if (j + 2 >= L) a4.z = d4.z = 0.f;
+        if (j + 3 >= L) a4.w = d4.w = 0.f;
       }
-      *reinterpret_cast<float4*>(sA + r * kTAL + c) = a4;
-      *reinterpret_cast<float4*>(sD + r * kTAL + c) = d4;
+      *reinterpret_cast<float4*>(sA + r * kTSL + c) = a4;
+      *reinterpret_cast<float4*>(sD + r * kTSL + c) = d4;
     }
     __syncthreads();
     const int n4 = (min(kTC, L - i0) + 3) & ~3;
-    tile_apply<D>(sD, sQ, n4, ty, tx, nr, dfk);
-    tile_apply<D>(sA, sG, n4, ty, tx, nr, dvj);
+    tile_apply_t<D>(sD, kTSL, sQ, n4, ty, tx, dfk);
+    tile_apply_t<D>(sA, kTSL, sG, n4, ty, tx, dvj);
     __syncthreads();
   }
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
-    const int ja = j0b + ty + 8 * a;
+    const int ja = j0b + 4 * ty + a;
     const bool live = ja < L;
     const T* kr = head_of<T>(p.k, bh, L, D) + (size_t)(live ? ja : L - 1) * D;
     float x[MF], dx[MF];
