@@ -59,9 +59,9 @@ TRAFFIC_PER_HEAD = {
     ("cd7374c887e34b93d59863825085e6318b533036691eec3187d21c51d5ee0c8b", "vit_b", "s", 128):
         (117489408 + 36713728) / 1536,
     # chunk-128 main pass for long sequences, L=24337 (B=2, H=12), LION-S:
-    # 386.1 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
-    ("d0529b6a1e41d23db5587530f8467479ac0c1f5de05919565d16e6064169c60f", "hires_2496", "s", 128):
-        (271412992 + 114661376) / 24,
+    # 386.4 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
+    ("f5392832814fe3f453e48183bf94befb7eaf5f8eef334cc21c56b81c2d242666", "hires_2496", "s", 128):
+        (271398656 + 114964992) / 24,
 }
 
 
@@ -495,7 +495,9 @@ def main():
                      "value": w2.B * w2.L / (ms2 * 1e-3), "unit": "tokens/s", "ms_per_step": ms2,
                      "roofline": {"bound": "hbm", "achieved": b2 / (ms2 * 1e-3) / 1e9,
                                   "peak": hbm_peak, "unit": "GB/s",
-                                  "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak}}
+                                  "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak,
+                                  "traffic": traffic_bytes(w2, args.mask if args.mask != "lit" else "s",
+                                                           HIRES_CHUNK)}}
         del _k2
 
     lra = None
