@@ -15,6 +15,9 @@ follow):
 * :func:`rnn`   -- forward and backward recurrences, diagonal removed once
   (rebuttal page, Theorem 3.3 Eq 20-24 and reply "1: Recurrence Form").
 * :func:`chunk` -- chunkwise form ("LION Part IV - Results", "LION Chunk").
+* :func:`full_reordered` -- the full form with the mask averaged over two
+  traversal orders of the tokens (rebuttal page, "P2: Comparison against
+  vision SSMs", item 1; the results page's reordered-patch models).
 * :func:`rows`  -- brute force for a sample of rows of one head.
 * :func:`mask`  -- the explicit mask of one head.
 * :func:`phi`   -- the feature maps.
@@ -69,9 +72,12 @@ def _load():
         lib.oracle_threads.argtypes = [i]
         lib.oracle_rnn_forward_half.argtypes = form + [dp, dp]
         lib.oracle_lion_full_bwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, dp, dp, dp, i]
+        lib.oracle_lion_full_reordered.argtypes = [dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int),
+                                                   i, i, i, i, i, i, dp, i]
         for f in (lib.oracle_phi, lib.oracle_mask, lib.oracle_lion_full, lib.oracle_lion_rnn,
                   lib.oracle_lion_chunk, lib.oracle_lion_rows, lib.oracle_row_kappa,
-                  lib.oracle_threads, lib.oracle_rnn_forward_half, lib.oracle_lion_full_bwd):
+                  lib.oracle_threads, lib.oracle_rnn_forward_half, lib.oracle_lion_full_bwd,
+                  lib.oracle_lion_full_reordered):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -150,6 +156,25 @@ def rnn(q, k, v, log_lambda, mask_kind, phi_kind=PHI_DEFAULT, threads=1):
 def chunk(q, k, v, log_lambda, mask_kind, chunk, phi_kind=PHI_DEFAULT, threads=1):
     return _run(_load().oracle_lion_chunk, q, k, v, log_lambda, mask_kind, phi_kind,
                 extra_before_y=(int(chunk),), threads=threads)
+
+
+def full_reordered(q, k, v, log_lambda, orders, mask_kind, phi_kind=PHI_DEFAULT, threads=1):
+    """Full form with the mask averaged over two traversal orders of the
+    tokens: ``orders`` is [2][L] (each row a permutation; position t of order
+    p holds token orders[p][t]), the same for every (b, h)."""
+    q, k, v, ll = _prep(q, k, v, log_lambda)
+    B, H, L, d = q.shape
+    _check_ll(mask_kind, ll, B, H, L)
+    o = np.ascontiguousarray(np.asarray(orders, dtype=np.int32))
+    if o.shape != (2, L):
+        raise ValueError("orders must be [2][L]")
+    y = np.empty_like(q)
+    rc = _load().oracle_lion_full_reordered(_ptr(q), _ptr(k), _ptr(v), _ptr(ll),
+                                            o.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                            B, H, L, d, mask_kind, phi_kind, _ptr(y), threads)
+    if rc:
+        raise ValueError(f"oracle call failed ({rc})")
+    return y
 
 
 def full_bwd(q, k, v, log_lambda, dy, mask_kind, phi_kind=PHI_DEFAULT, threads=1):

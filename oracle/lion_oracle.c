@@ -48,6 +48,16 @@
  *                      per-chunk states carried by a forward and a backward
  *                      scan over chunks ([P4] "LION Chunk"; [RB] reply "4:
  *                      Practicality of Recurrent Inference", chunking).
+ *   oracle_lion_full_reordered
+ *                      the full form with the mask averaged over two traversal
+ *                      orders of the tokens (LION-S (v2), LION-D / LION-S with
+ *                      reordered patches: [RB] "P2: Comparison against vision
+ *                      SSMs", item 1, which averages the two masks of its
+ *                      Figure 7 b and c; [P4] "Model Comparisons", the rows
+ *                      marked natural).  The figure is not on the pages, so
+ *                      the two orders are inputs.  Reading: along an order the
+ *                      mask is LION's mask of the reordered sequence, and the
+ *                      two masks are averaged inside the row-sum normaliser.
  *
  * Layouts: q, k, v, y are [B][H][L][d] row-major float64.  log_lambda:
  * LIT ignored (may be NULL), D [H], S [B][H][L].  Return 0 on success,
@@ -171,15 +181,10 @@ int oracle_threads(int nthreads) { return set_threads(nthreads); }
 
 /* ------------------------------------------------------- full form ----- */
 
-/* Brute force, Y = SCALE(QK^T (.) M) V ([RB] Theorem 3.3 Eq 25). */
-static void full_head(const double* q, const double* k, const double* v,
-                      const double* l, int L, int d, int phi, double* y,
-                      double* fq, double* fk, double* M, double* num) {
-  for (int t = 0; t < L; ++t) {
-    phi_row(phi, q + (long)t * d, d, fq + (long)t * d);
-    phi_row(phi, k + (long)t * d, d, fk + (long)t * d);
-  }
-  mask_of_head(l, L, M);
+/* Y = SCALE(QK^T (.) M) V for a given explicit mask M ([RB] Theorem 3.3
+ * Eq 25); fq, fk hold phi(q), phi(k). */
+static void masked_attention(const double* fq, const double* fk, const double* v,
+                             const double* M, int L, int d, double* y, double* num) {
   for (int i = 0; i < L; ++i) {
     double den = 0.0;
     for (int n = 0; n < d; ++n) num[n] = 0.0;
@@ -192,6 +197,22 @@ static void full_head(const double* q, const double* k, const double* v,
     }
     for (int n = 0; n < d; ++n) y[(long)i * d + n] = num[n] / den;
   }
+}
+
+static void phi_rows(int phi, const double* q, const double* k, int L, int d, double* fq, double* fk) {
+  for (int t = 0; t < L; ++t) {
+    phi_row(phi, q + (long)t * d, d, fq + (long)t * d);
+    phi_row(phi, k + (long)t * d, d, fk + (long)t * d);
+  }
+}
+
+/* Brute force, Y = SCALE(QK^T (.) M) V ([RB] Theorem 3.3 Eq 25). */
+static void full_head(const double* q, const double* k, const double* v,
+                      const double* l, int L, int d, int phi, double* y,
+                      double* fq, double* fk, double* M, double* num) {
+  phi_rows(phi, q, k, L, d, fq, fk);
+  mask_of_head(l, L, M);
+  masked_attention(fq, fk, v, M, L, d, y, num);
 }
 
 int oracle_lion_full(const double* q, const double* k, const double* v,
@@ -218,6 +239,72 @@ int oracle_lion_full(const double* q, const double* k, const double* v,
       full_head(q + off, k + off, v + off, l, L, d, phi, y + off, fq, fk, M, num);
     }
     free(l); free(fq); free(fk); free(M); free(num);
+  }
+  return err;
+}
+
+/* ------------------------------------------ reordered full form -------- */
+
+/* The mask of one head taken along a traversal order: position t of the
+ * order holds token order[t].  Between the tokens at positions t and u the
+ * mask is LION's mask of the reordered sequence, the product of
+ * lambda_{order[w]} over the positions w in (min(t,u), max(t,u)].  It is
+ * accumulated into Macc[a*L + b] (token indices) with weight `wgt`.
+ * lo and Mo are scratch of L and L*L doubles. */
+static void add_mask_along_order(const double* l, const int* order, int L, double wgt, double* Macc,
+                                 double* lo, double* Mo) {
+  for (int t = 0; t < L; ++t) lo[t] = l[order[t]];
+  mask_of_head(lo, L, Mo);
+  for (int t = 0; t < L; ++t)
+    for (int u = 0; u < L; ++u) Macc[(long)order[t] * L + order[u]] += wgt * Mo[(long)t * L + u];
+}
+
+/* 1 unless order[0..L) is a permutation of 0..L-1. */
+static int not_a_permutation(const int* order, int L) {
+  char* seen = (char*)calloc((size_t)L, 1);
+  if (!seen) return 1;
+  int bad = 0;
+  for (int t = 0; t < L && !bad; ++t) {
+    if (order[t] < 0 || order[t] >= L || seen[order[t]]) bad = 1;
+    else seen[order[t]] = 1;
+  }
+  free(seen);
+  return bad;
+}
+
+/* orders: [2][L], each a permutation of the tokens, the same for every
+ * (b, h).  Y = SCALE(QK^T (.) (M1 + M2) / 2) V with Mp the mask along
+ * order p. */
+int oracle_lion_full_reordered(const double* q, const double* k, const double* v,
+                               const double* log_lambda, const int* orders, int B, int H, int L,
+                               int d, int mask_kind, int phi_kind, double* y, int nthreads) {
+  if (check_args(q, k, v, log_lambda, B, H, L, d, mask_kind, phi_kind, y)) return 1;
+  if (!orders || not_a_permutation(orders, L) || not_a_permutation(orders + L, L)) return 1;
+  int phi = resolve_phi(mask_kind, phi_kind);
+  int nt = set_threads(nthreads);
+  int err = 0;
+  long heads = (long)B * H;
+#pragma omp parallel for schedule(dynamic) num_threads(nt) reduction(| : err)
+  for (long bh = 0; bh < heads; ++bh) {
+    int b = (int)(bh / H), h = (int)(bh % H);
+    double* l = (double*)malloc(sizeof(double) * L);
+    double* lo = (double*)malloc(sizeof(double) * L);
+    double* fq = (double*)malloc(sizeof(double) * (size_t)L * d);
+    double* fk = (double*)malloc(sizeof(double) * (size_t)L * d);
+    double* M = (double*)calloc((size_t)L * L, sizeof(double));
+    double* Mo = (double*)malloc(sizeof(double) * (size_t)L * L);
+    double* num = (double*)malloc(sizeof(double) * d);
+    if (!l || !lo || !fq || !fk || !M || !Mo || !num) {
+      err |= 2;
+    } else {
+      long off = bh * (long)L * d;
+      head_log_lambda(mask_kind, log_lambda, b, h, H, L, l);
+      add_mask_along_order(l, orders, L, 0.5, M, lo, Mo);
+      add_mask_along_order(l, orders + L, L, 0.5, M, lo, Mo);
+      phi_rows(phi, q + off, k + off, L, d, fq, fk);
+      masked_attention(fq, fk, v + off, M, L, d, y + off, num);
+    }
+    free(l); free(lo); free(fq); free(fk); free(M); free(Mo); free(num);
   }
   return err;
 }

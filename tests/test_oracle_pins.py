@@ -410,3 +410,124 @@ def test_full_bwd_d_is_the_sum_of_s(oracle_mod):
     for a, b in zip(gd[:3], gs[:3]):
         assert np.abs(a - b).max() <= 1e-12 * max(1.0, np.abs(a).max())
     assert np.abs(gd[3] - gs[3].sum(axis=(0, 2))).max() <= 1e-10 * max(1.0, np.abs(gd[3]).max())
+
+
+# ------------------------------------------------- reordered full form ----
+# The mask averaged over two traversal orders of the tokens (rebuttal page,
+# reply "P2: Comparison against vision SSMs", item 1: the two masks of its
+# Figure 7 b and c are averaged; results page "LION Part IV - Results",
+# "Model Comparisons", the reordered-patch models).  Along an order the mask
+# is LION's mask of the reordered sequence.
+
+def _non_involution(rng, L):
+    while True:
+        p = rng.permutation(L)
+        if np.any(p[p] != np.arange(L)):
+            return p
+
+
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_reordered_one_order_twice_is_lion_on_the_reordered_sequence(oracle_mod, mask_kind):
+    """Both orders equal to pi: the plain operator run on the tokens (with
+    their decays) taken in the order pi, its output put back in place."""
+    rng = np.random.default_rng(900 + mask_kind)
+    B, H, L, d = 2, 2, 11, 5
+    q, k, v, ll = _inputs(rng, B, H, L, d, mask_kind)
+    pi = _non_involution(rng, L)
+    got = oracle_mod.full_reordered(q, k, v, ll, np.stack([pi, pi]), mask_kind)
+    llp = ll[..., pi] if mask_kind == 2 else ll
+    yp = oracle_mod.full(q[:, :, pi], k[:, :, pi], v[:, :, pi], llp, mask_kind)
+    want = np.empty_like(yp)
+    want[:, :, pi] = yp
+    assert _rel(got, want) < 1e-12
+
+
+def test_reordered_order_swap_and_lit(oracle_mod):
+    rng = np.random.default_rng(910)
+    L = 13
+    o1, o2 = rng.permutation(L), rng.permutation(L)
+    q, k, v, ll = _inputs(rng, 1, 2, L, 4, 2)
+    a = oracle_mod.full_reordered(q, k, v, ll, np.stack([o1, o2]), 2)
+    b = oracle_mod.full_reordered(q, k, v, ll, np.stack([o2, o1]), 2)
+    assert _rel(a, b) < 1e-14
+    # LIT: every order gives the all-ones mask
+    got = oracle_mod.full_reordered(q, k, v, None, np.stack([o1, o2]), 0)
+    assert _rel(got, oracle_mod.full(q, k, v, None, 0)) < 1e-13
+
+
+def test_reordered_d_with_reversal_is_plain_d(oracle_mod):
+    """LION-D along the reversed order keeps every distance |i - j|."""
+    rng = np.random.default_rng(920)
+    L = 12
+    q, k, v, ll = _inputs(rng, 2, 3, L, 4, 1)
+    orders = np.stack([np.arange(L), np.arange(L)[::-1]])
+    got = oracle_mod.full_reordered(q, k, v, ll, orders, 1)
+    assert _rel(got, oracle_mod.full(q, k, v, ll, 1)) < 1e-13
+
+
+def test_reordered_s_with_reversal_closed_form(oracle_mod):
+    """LION-S, orders (identity, reversal): for i < j the reversed traversal
+    multiplies lambda_i .. lambda_{j-1} instead of lambda_{i+1} .. lambda_j,
+    so M_ij = (prod_{i<t<=j} lambda_t + prod_{i<=t<j} lambda_t) / 2 (and
+    symmetric).  Identity features, written out with explicit products."""
+    rng = np.random.default_rng(930)
+    B, H, L, d = 1, 2, 10, 3
+    q, k, v, ll = _inputs(rng, B, H, L, d, 2)
+    q, k = np.abs(q) + 0.25, np.abs(k) + 0.25
+    orders = np.stack([np.arange(L), np.arange(L)[::-1]])
+    got = oracle_mod.full_reordered(q, k, v, ll, orders, 2, phi_kind=3)
+    lam = np.exp(ll)
+    for b in range(B):
+        for h in range(H):
+            M = np.ones((L, L))
+            for i in range(L):
+                for j in range(i + 1, L):
+                    fwd = np.prod(lam[b, h, i + 1:j + 1])
+                    rev = np.prod(lam[b, h, i:j])
+                    M[i, j] = M[j, i] = 0.5 * (fwd + rev)
+            A = (q[b, h] @ k[b, h].T) * M
+            want = (A @ v[b, h]) / A.sum(axis=1, keepdims=True)
+            assert _rel(got[b, h], want) < 1e-12
+
+
+def test_reordered_s_matches_cumsum_route(oracle_mod):
+    """General orders, LION-S: the mask along an order from the cumulative
+    sum of the reordered log-decays (M = exp(-|C_{r(a)} - C_{r(b)}|), r the
+    position of a token in the order), against the oracle's products."""
+    rng = np.random.default_rng(940)
+    B, H, L, d = 2, 1, 14, 4
+    q, k, v, ll = _inputs(rng, B, H, L, d, 2)
+    q, k = np.abs(q) + 0.25, np.abs(k) + 0.25
+    orders = np.stack([rng.permutation(L), rng.permutation(L)])
+    got = oracle_mod.full_reordered(q, k, v, ll, orders, 2, phi_kind=3)
+    for b in range(B):
+        M = np.zeros((L, L))
+        for o in orders:
+            rank = np.empty(L, dtype=int)
+            rank[o] = np.arange(L)
+            C = np.cumsum(ll[b, 0][o])
+            Cr = C[rank]
+            M += 0.5 * np.exp(-np.abs(Cr[:, None] - Cr[None, :]))
+        A = (q[b, 0] @ k[b, 0].T) * M
+        want = (A @ v[b, 0]) / A.sum(axis=1, keepdims=True)
+        assert _rel(got[b, 0], want) < 1e-12
+
+
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_reordered_convex_hull(oracle_mod, mask_kind):
+    rng = np.random.default_rng(950 + mask_kind)
+    L = 15
+    q, k, v, ll = _inputs(rng, 1, 2, L, 6, mask_kind)
+    y = oracle_mod.full_reordered(q, k, v, ll, np.stack([rng.permutation(L), rng.permutation(L)]),
+                                  mask_kind, phi_kind=1)
+    assert np.all(y >= v.min(axis=2, keepdims=True) - 1e-12)
+    assert np.all(y <= v.max(axis=2, keepdims=True) + 1e-12)
+
+
+def test_reordered_rejects_non_permutations(oracle_mod):
+    rng = np.random.default_rng(960)
+    q, k, v, ll = _inputs(rng, 1, 1, 5, 2, 2)
+    good = np.arange(5)
+    for bad in (np.array([0, 1, 2, 3, 3]), np.array([0, 1, 2, 3, 5]), np.array([-1, 1, 2, 3, 4])):
+        with pytest.raises(ValueError):
+            oracle_mod.full_reordered(q, k, v, ll, np.stack([good, bad]), 2)
