@@ -324,6 +324,61 @@ def measure_bwd(w, mask, steps, warmup, flush):
     return time_device(call, steps, warmup, flush, stream)
 
 
+def reorder_flops(w) -> int:
+    """Algorithmic flops of the full form per call: phi(Q) phi(K)^T and the
+    masked product with V, 2 L^2 d flops each, per head."""
+    return 4 * w.B * w.H * w.L * w.L * w.d
+
+
+def reorder_launches(mask) -> int:
+    """Kernels one lion_attn_fwd_reordered call launches: the order check,
+    phi and the full form; LION-S adds the prefix along each order."""
+    return 3 + (mask == "s")
+
+
+def vit_grid_orders(L):
+    """Two traversals of a ViT token sequence (class token first, then a
+    square patch grid): the patches row by row, and column by column.  Any
+    permutation costs the same; these stand in for the pages' two orders."""
+    side = int(round((L - 1) ** 0.5))
+    if side * side != L - 1:
+        rows = torch.arange(L, dtype=torch.int32)
+        return torch.stack([rows, rows.flip(0)])
+    rows = torch.arange(L, dtype=torch.int32)
+    cols = torch.cat([torch.zeros(1, dtype=torch.int32),
+                      1 + torch.arange(side * side, dtype=torch.int32).reshape(side, side).t().reshape(-1)])
+    return torch.stack([rows, cols])
+
+
+def measure_reordered(w, mask, steps, warmup, flush):
+    """CUDA-event time of one lion_attn_fwd_reordered call through the C
+    entry point with a preallocated output and workspace."""
+    import ctypes
+    inp = synth.make_inputs(w.B, w.H, w.L, w.d, mask, w.dtype, w.seed, w.lam)
+    dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
+    orders = vit_grid_orders(w.L).cuda()
+    out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    wsb = lion.reordered_workspace_bytes(w.B, w.H, w.L, w.d)
+    wsp = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    p = lambda t: None if t is None else t.data_ptr()
+    a = lion._ReorderArgs(p(dev["q"]), p(dev["k"]), p(dev["v"]), p(dev["log_lambda"]), orders.data_ptr(),
+                          out.data_ptr(), w.B, w.H, w.L, w.d, inp["mask"],
+                          lion.DTYPE_BF16 if w.dtype == "bf16" else lion.DTYPE_FP32, lion.PHI_DEFAULT,
+                          wsp.data_ptr(), wsb, stream.cuda_stream)
+    lib = lion.load()
+
+    def call():
+        st = lib.lion_attn_fwd_reordered(ctypes.byref(a))
+        if st:
+            raise RuntimeError(f"lion_attn_fwd_reordered failed ({st})")
+
+    t = time_device(call, steps, warmup, flush, stream)
+    if lion.sync_status() != lion.OK:
+        raise RuntimeError("traversal order rejected on the device")
+    return t
+
+
 def stream_bytes(B, H, d, in_bytes=2) -> int:
     """Bytes one decode step must move: the fp32 state S (d x d) and z read
     and written, the token's q, k, v and log-lambda read, y_part and c_part
@@ -444,6 +499,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-streaming", action="store_true")
+    ap.add_argument("--no-reordered", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling captures)")
     args = ap.parse_args()
@@ -524,6 +580,21 @@ def main():
                                  "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
                                  "algorithmic_flops": fl}}
 
+    reordered = None
+    if not args.no_reordered and w.L <= lion.FULL_MAX_L and w.d in (64, 128):
+        tr = measure_reordered(w, args.mask, 20, 3, flush)
+        msr = statistics.mean(tr)
+        flr = reorder_flops(w)
+        reordered = {"form": "full, mask averaged over two traversal orders",
+                     "orders": "class token, then the patch grid by rows / by columns",
+                     "value": w.B * w.L / (msr * 1e-3), "unit": "tokens/s", "ms_per_call": msr,
+                     "launches_per_call": reorder_launches(args.mask),
+                     "roofline": {"bound": "alu", "achieved": flr / (msr * 1e-3) / 1e12,
+                                  "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
+                                  "frac": flr / (msr * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
+                                  "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
+                                  "algorithmic_flops": flr}}
+
     streaming = None
     if not args.no_streaming:
         ms_s = measure_stream(w.B, w.H, w.d, args.mask, 200, 10)
@@ -558,6 +629,7 @@ def main():
             "secondary": secondary,
             "lra": lra,
             "backward": backward,
+            "reordered": reordered,
             "streaming": streaming,
         }
         print(json.dumps(line))

@@ -229,7 +229,7 @@ lion_status lion_sync_status(cudaStream_t stream) {
   if (v != 0) {
     const int zero = 0;
     if (cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return LION_ERR_CUDA;
-    return LION_ERR_TIMEOUT;
+    return v == lion::kStatusBadOrder ? LION_ERR_INVALID_ARG : LION_ERR_TIMEOUT;
   }
   return LION_OK;
 }
@@ -272,6 +272,72 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
     case LION_FORM_CHUNK: e = lion::launch_chunk_simt(p, (float*)ws, s); break;
   }
+  if (owned) {
+    cudaError_t f = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = f;
+  }
+  return from_cuda(e);
+}
+
+size_t lion_attn_reordered_workspace_bytes(int B, int H, int L, int d) {
+  if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128)) return 0;
+  return lion::reorder_workspace_bytes(B, H, L, d);
+}
+
+lion_status lion_attn_fwd_reordered(const lion_reorder_args* a) {
+  if (!a) return LION_ERR_INVALID_ARG;
+  lion_args g;
+  memset(&g, 0, sizeof(g));
+  g.q = a->q;
+  g.k = a->k;
+  g.v = a->v;
+  g.log_lambda = a->log_lambda;
+  g.out = a->out;
+  g.B = a->B;
+  g.H = a->H;
+  g.L = a->L;
+  g.d = a->d;
+  g.mask_kind = a->mask_kind;
+  g.form = LION_FORM_FULL;
+  g.dtype = a->dtype;
+  g.phi = a->phi;
+  g.workspace = a->workspace;
+  g.workspace_bytes = a->workspace_bytes;
+  g.stream = a->stream;
+  lion_status st = validate(&g);
+  if (st != LION_OK) return st;
+  if (!a->order || !aligned(a->order, 4) || !device_accessible(a->order)) return LION_ERR_INVALID_ARG;
+  if (a->d != 64 && a->d != 128) return LION_ERR_UNSUPPORTED;
+  const size_t need = lion::reorder_workspace_bytes(a->B, a->H, a->L, a->d);
+  if (a->workspace && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
+  int* dstatus = lion::device_status_ptr();
+  if (!dstatus) return LION_ERR_CUDA;
+  Problem p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.log_lambda = a->log_lambda;
+  p.out = a->out;
+  p.B = a->B;
+  p.H = a->H;
+  p.L = a->L;
+  p.d = a->d;
+  p.mask_kind = a->mask_kind;
+  p.phi = lion::resolve_phi(a->mask_kind, a->phi);
+  p.dtype = a->dtype;
+  p.chunk = 0;
+  cudaStream_t s = a->stream;
+  void* ws = a->workspace;
+  bool owned = false;
+  if (!ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
+    }
+    owned = true;
+  }
+  cudaError_t e = lion::launch_reordered(p, a->order, ws, dstatus, s);
   if (owned) {
     cudaError_t f = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = f;

@@ -87,8 +87,19 @@ size_t bwd_workspace_bytes(int B, int H, int L, int d);
 cudaError_t launch_bwd(const Problem& p, const float* dy, float* dq, float* dk, float* dv, float* dll, void* ws,
                        cudaStream_t s);
 
+// Full form with the mask averaged over two traversal orders (order: device
+// int32 [2][L]); fp32 on the CUDA cores, d in {64, 128}; workspace of
+// reorder_workspace_bytes; reorder_launches kernels a call.
+size_t reorder_workspace_bytes(int B, int H, int L, int d);
+int reorder_launches(int mask_kind);
+cudaError_t launch_reordered(const Problem& p, const int* order, void* ws, int* status, cudaStream_t s);
+
 // Device-side status word that kernels set when a bounded wait gives up
-// (address on the current device; nullptr if it cannot be resolved).
+// (kStatusTimeout) or a traversal order is not a permutation
+// (kStatusBadOrder); address on the current device, nullptr if it cannot be
+// resolved.
+constexpr int kStatusTimeout = 1;
+constexpr int kStatusBadOrder = 2;
 int* device_status_ptr();
 
 // Largest chunk the SIMT chunk kernel takes (its chunk-local prefix lives in

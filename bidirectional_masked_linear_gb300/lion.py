@@ -59,12 +59,23 @@ class _BwdArgs(ctypes.Structure):
     ]
 
 
+class _ReorderArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_lambda", ctypes.c_void_p), ("order", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int),
+        ("mask_kind", ctypes.c_int), ("dtype", ctypes.c_int), ("phi", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "lion_rnn_step",
            "lion_status_string", "lion_abi_version", "lion_sync_status",
            "lion_attn_fwd_rnn_noalloc", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
-           "lion_attn_fwd_causal")
+           "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes")
 NOALLOC_MAX_HEAD_TOKENS = 1 << 20
 
 
@@ -100,6 +111,10 @@ def load(path: str = LIB_PATH):
     lib.lion_attn_bwd.restype = i
     lib.lion_attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.lion_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.lion_attn_fwd_reordered.argtypes = [ctypes.POINTER(_ReorderArgs)]
+    lib.lion_attn_fwd_reordered.restype = i
+    lib.lion_attn_reordered_workspace_bytes.argtypes = [i, i, i, i]
+    lib.lion_attn_reordered_workspace_bytes.restype = ctypes.c_size_t
     _lib = lib
     return lib
 
@@ -131,8 +146,9 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def sync_status(stream=None) -> int:
-    """Synchronise the stream and return the library's device status
-    (OK, or ERR_TIMEOUT if a kernel gave up on a bounded wait)."""
+    """Synchronise the stream and return the library's device status (OK;
+    ERR_TIMEOUT if a kernel gave up on a bounded wait; ERR_INVALID_ARG if a
+    traversal order given to attn_fwd_reordered was not a permutation)."""
     return int(load().lion_sync_status(_stream_handle(stream)))
 
 
@@ -278,4 +294,32 @@ def attn_fwd_causal(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, o
               0 if workspace is None else workspace.numel() * workspace.element_size(),
               _stream_handle(stream))
     _check(lib.lion_attn_fwd_causal(ctypes.byref(a)))
+    return out
+
+
+def reordered_workspace_bytes(B, H, L, d) -> int:
+    return int(load().lion_attn_reordered_workspace_bytes(B, H, L, d))
+
+
+def attn_fwd_reordered(q, k, v, log_lambda, orders, mask_kind, out=None, phi=PHI_DEFAULT, workspace=None,
+                       stream=None):
+    """Full form with the mask averaged over two traversal orders of the
+    tokens: ``orders`` is an int32 device tensor [2, L] (row p: the token at
+    each position of traversal p), the same for every (b, h).  fp32 output."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    B, H, L, d = q.shape
+    if orders.dtype != torch.int32 or tuple(orders.shape) != (2, L):
+        raise ValueError("orders must be int32 of shape [2, L]")
+    if out is None:
+        out = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    for t in (q, k, v, out, orders) + ((log_lambda,) if log_lambda is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    a = _ReorderArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(orders), _ptr(out), B, H, L, d,
+                     mask_kind, _dtype_code(q), phi, _ptr(workspace),
+                     0 if workspace is None else workspace.numel() * workspace.element_size(),
+                     _stream_handle(stream))
+    _check(lib.lion_attn_fwd_reordered(ctypes.byref(a)))
     return out

@@ -159,7 +159,8 @@ lion_status lion_rnn_step(const void* q, const void* k, const void* v,
 /*
  * lion_sync_status -- synchronise `stream`, then report whether any kernel
  * of this library on the current device gave up on a bounded device-side
- * wait since the last call (LION_ERR_TIMEOUT; the flag is then cleared).
+ * wait since the last call (LION_ERR_TIMEOUT), or was given a traversal order
+ * that is not a permutation (LION_ERR_INVALID_ARG); the flag is then cleared.
  * Kernels never spin unboundedly: a wait that runs out records the error,
  * releases its tensor memory and returns.  LION_ERR_CUDA if the
  * synchronisation itself fails.
@@ -234,6 +235,50 @@ lion_status lion_attn_bwd(const lion_bwd_args* a);
 
 /* Workspace bytes lion_attn_bwd needs for this problem. */
 size_t lion_attn_bwd_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * lion_attn_fwd_reordered -- the full form with the mask averaged over two
+ * traversal orders of the tokens: LION-S (v2) and the reordered-patch LION-D
+ * and LION-S (rebuttal page reply "P2: Comparison against vision SSMs",
+ * item 1: the masks of two traversals of the patch grid are averaged; results
+ * page "LION Part IV - Results", "Model Comparisons").
+ *   Along order p, position t holds token order[p*L + t]; the mask between
+ *   two tokens is the operator's mask of the sequence taken in that order
+ *   (the product of the decays at the positions after the earlier token, up
+ *   to and including the later one; LION-D: lambda to the distance between
+ *   the positions).  y_i = sum_j M_ij s_ij v_j / sum_j M_ij s_ij with
+ *   M = (M^1 + M^2) / 2.  Identical orders give the plain operator run on the
+ *   reordered sequence; LIT ignores the orders.
+ *   q, k, v, log_lambda, out, B, H, L, dtype, phi, workspace, stream: as
+ *   lion_args (form and chunk are not used).
+ *   order   device int32 [2][L], each row a permutation of 0..L-1, the same
+ *           for every (b, h); 4-byte aligned.  A row that is not a
+ *           permutation is detected on the device: the call still returns
+ *           LION_OK, every access stays in bounds, out is undefined, and the
+ *           next lion_sync_status returns LION_ERR_INVALID_ARG.
+ *   Computed in fp32 on the CUDA cores; d in {64, 128} (else
+ *   LION_ERR_UNSUPPORTED) and L <= LION_FULL_MAX_L.  Workspace as returned
+ *   by lion_attn_reordered_workspace_bytes (NULL: stream-ordered allocation).
+ */
+typedef struct {
+  const void* q;             /* [B][H][L][d], dtype below                  */
+  const void* k;
+  const void* v;
+  const float* log_lambda;   /* as lion_args                               */
+  const int* order;          /* [2][L] device int32                        */
+  float* out;                /* [B][H][L][d] float32                       */
+  int B, H, L, d;
+  int mask_kind;             /* lion_mask_kind                             */
+  int dtype;                 /* lion_dtype of q, k, v                      */
+  int phi;                   /* lion_phi                                   */
+  void* workspace;           /* device, 256-byte aligned, or NULL          */
+  size_t workspace_bytes;
+  cudaStream_t stream;
+} lion_reorder_args;
+lion_status lion_attn_fwd_reordered(const lion_reorder_args* a);
+
+/* Workspace bytes lion_attn_fwd_reordered needs (0 if d is not 64 or 128). */
+size_t lion_attn_reordered_workspace_bytes(int B, int H, int L, int d);
 
 /* Static, human-readable text for a status. */
 const char* lion_status_string(lion_status s);

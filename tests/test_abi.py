@@ -28,7 +28,8 @@ def _declared():
 def test_header_declares_the_abi():
     names = _declared()
     for want in ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_rnn_step", "lion_status_string",
-                 "lion_attn_workspace_bytes", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes"):
+                 "lion_attn_workspace_bytes", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
+                 "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes"):
         assert want in names
 
 
@@ -65,6 +66,38 @@ def test_bwd_workspace_query(lib):
     assert need >= 2 * 3 * 10 * (3 * 64 + 4) * 4 + 2 * 3 * 8
     assert lion.bwd_workspace_bytes(0, 3, 10, 64) == 0
     assert lion.bwd_workspace_bytes(1, 1, 10, 48) == 0
+
+
+def test_reordered_workspace_query(lib):
+    from bidirectional_masked_linear_gb300 import lion
+    # phi(q), phi(k) (L*d floats each), two positions per token of the order,
+    # two coordinates per head-token
+    need = lion.reordered_workspace_bytes(2, 3, 10, 64)
+    assert need >= 2 * 3 * 10 * (2 * 64 + 2) * 4 + 2 * 10 * 4
+    assert lion.reordered_workspace_bytes(0, 3, 10, 64) == 0
+    assert lion.reordered_workspace_bytes(1, 1, 10, 32) == 0    # d = 64 and 128 only
+
+
+def _reorder(lib, **kw):
+    from bidirectional_masked_linear_gb300 import lion
+    f = dict(q=4096, k=8192, v=12288, log_lambda=0, order=16384, out=20480, B=1, H=1, L=8, d=64,
+             mask_kind=0, dtype=0, phi=0, workspace=0, workspace_bytes=0, stream=0)
+    f.update(kw)
+    a = lion._ReorderArgs(**f)
+    return lib.lion_attn_fwd_reordered(ctypes.byref(a))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(k=0), dict(v=0), dict(out=0), dict(order=0), dict(order=16386),
+    dict(B=0), dict(H=0), dict(L=0), dict(d=48), dict(mask_kind=3), dict(dtype=2), dict(phi=4),
+    dict(mask_kind=1, log_lambda=0), dict(mask_kind=2, log_lambda=0),
+    dict(),   # pointers that are not device memory
+])
+def test_reordered_invalid_arguments_rejected_before_launch(lib, kw):
+    from bidirectional_masked_linear_gb300 import lion
+    lib.lion_attn_fwd_reordered.argtypes = [ctypes.POINTER(lion._ReorderArgs)]
+    assert _reorder(lib, **kw) == 1
+    assert lib.lion_attn_fwd_reordered(None) == 1
 
 
 def _bwd(lib, **kw):

@@ -66,3 +66,17 @@ def test_backward_launch_counts():
 def test_stream_bytes():
     # ViT-B heads, d = 64: S and z read and written in fp32, bf16 q, k, v in
     assert bench.stream_bytes(64, 12, 64) == 64 * 12 * (2 * (64 * 64 + 64) * 4 + 3 * 64 * 2 + 4 + 64 * 4 + 4)
+
+
+def test_reordered_flops_launches_and_orders():
+    w = synth.WORKLOADS["vit_b"]
+    assert bench.reorder_flops(w) == 2 * 2 * w.B * w.H * w.L ** 2 * w.d
+    assert bench.reorder_launches("s") == 4 and bench.reorder_launches("d") == 3
+    o = bench.vit_grid_orders(197)
+    assert tuple(o.shape) == (2, 197)
+    for row in o:   # permutations, class token first
+        assert sorted(row.tolist()) == list(range(197)) and int(row[0]) == 0
+    assert o[1, 1:15].tolist() == [1 + 14 * r for r in range(14)]   # first column of the grid
+    r = bench.vit_grid_orders(11)   # not 1 + a square: identity and reversal
+    assert r[1].tolist() == list(range(10, -1, -1))
+

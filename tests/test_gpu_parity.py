@@ -452,3 +452,92 @@ def test_causal_feature_maps_and_single_token(oracle_mod):
     for form in (lion.FORM_FULL, lion.FORM_RNN, lion.FORM_CHUNK):
         y = lion.attn_fwd_causal(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], form, 8)
         assert torch.allclose(y, g["v"].float(), rtol=1e-5, atol=1e-6)   # (s v) / s, rounded
+
+
+# ------------------------------------------------- patch reordering (f2) --
+# The full form with the mask averaged over two traversal orders of the tokens
+# (rebuttal page, reply "P2: Comparison against vision SSMs", item 1; results
+# page "LION Part IV - Results", the reordered-patch models), against the
+# oracle's brute force (pinned by the one-order, reversal and cumulative-sum
+# cases).  fp32 arithmetic on the CUDA cores; rows are measured against the
+# averaged mask's conditioning like every other SiLU case.
+TOL_REORDER = 1e-4
+
+
+def _vit_grid_orders(side=14):
+    """Class token first, then the patch grid row by row, or column by column."""
+    rows = np.arange(1 + side * side)
+    cols = np.concatenate([[0], 1 + np.arange(side * side).reshape(side, side).T.ravel()])
+    return np.stack([rows, cols]).astype(np.int32)
+
+
+def _avg_mask(oracle_mod, mask, ll, orders, b, h, H, L):
+    M = np.zeros((L, L))
+    for o in orders:
+        llo = ll[:, :, o] if mask == lion.MASK_S else ll
+        M[np.ix_(o, o)] += 0.5 * oracle_mod.mask(mask, llo, L, b, h, H)
+    return M
+
+
+def _reorder_check(oracle_mod, inp, orders, phi=0):
+    q, k, v, ll = f64(inp)
+    B, H, L, d = q.shape
+    ref = oracle_mod.full_reordered(q, k, v, ll, orders, inp["mask"], phi)
+    g = _cuda(inp)
+    o = torch.from_numpy(np.ascontiguousarray(orders, dtype=np.int32)).cuda()
+    y = lion.attn_fwd_reordered(g["q"], g["k"], g["v"], g["log_lambda"], o, inp["mask"], phi=phi)
+    assert lion.sync_status() == lion.OK
+    y = y.cpu().numpy().astype(np.float64)
+    kind = phi or (2 if inp["mask"] == lion.MASK_S else 1)
+    err = row_errors(y, ref)
+    for b in range(B):
+        for h in range(H):
+            M = _avg_mask(oracle_mod, inp["mask"], ll, orders, b, h, H, L)
+            fq, fk = oracle_mod.phi(kind, q[b, h]), oracle_mod.phi(kind, k[b, h])
+            den = (M * (fq @ fk.T)).sum(1)
+            kap = (M * (np.abs(fq) @ np.abs(fk).T)).sum(1) / np.abs(den)
+            bad = err[b, h] > TOL_REORDER * np.maximum(1.0, kap)
+            assert not bad.any(), (b, h, np.argwhere(bad)[:3], err[b, h][bad][:3])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+@pytest.mark.parametrize("dtype", ("bf16", "fp32"))
+def test_reordered_matches_oracle(oracle_mod, mask, dtype):
+    rng = np.random.default_rng(1200)
+    inp = synth.make_inputs(2, 3, 197, 64, mask, dtype, seed=1201)
+    _reorder_check(oracle_mod, inp, _vit_grid_orders())
+    for n, (B, H, L, d) in enumerate(((1, 2, 300, 128), (2, 2, 7, 64), (1, 1, 1, 64), (1, 2, 515, 64))):
+        inp = synth.make_inputs(B, H, L, d, mask, dtype, seed=1210 + 10 * n)
+        _reorder_check(oracle_mod, inp, np.stack([rng.permutation(L), rng.permutation(L)]))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask,phi", (("s", 1), ("d", 2), ("lit", 3)))
+def test_reordered_feature_maps(oracle_mod, mask, phi):
+    rng = np.random.default_rng(1250)
+    inp = synth.make_inputs(2, 2, 150, 64, mask, "bf16", seed=1251)
+    if phi == 3:   # identity features need row sums away from zero
+        for key in ("q", "k"):
+            inp[key] = (inp[key].float().abs() + 0.25).to(inp[key].dtype)
+    _reorder_check(oracle_mod, inp, np.stack([rng.permutation(150), rng.permutation(150)]), phi=phi)
+
+
+@pytest.mark.gpu
+def test_reordered_invalid_orders_are_reported():
+    """A row that is not a permutation: the call returns OK, the kernels keep
+    every index in range, and the next status query says INVALID_ARG (then
+    the flag is clear)."""
+    inp = synth.make_inputs(1, 2, 40, 64, "s", "bf16", seed=1260)
+    g = _cuda(inp)
+    good = np.arange(40)
+    for bad in (np.r_[np.arange(39), 5], np.r_[np.arange(39), 45], np.r_[-1, np.arange(1, 40)]):
+        o = torch.from_numpy(np.stack([good, bad]).astype(np.int32)).cuda()
+        lion.attn_fwd_reordered(g["q"], g["k"], g["v"], g["log_lambda"], o, lion.MASK_S)
+        assert lion.sync_status() == lion.ERR_INVALID_ARG
+        assert lion.sync_status() == lion.OK
+    with pytest.raises(lion.LionError):
+        q32 = torch.zeros((1, 1, 8, 32), dtype=torch.bfloat16, device="cuda")
+        lion.attn_fwd_reordered(q32, q32, q32, None, torch.zeros((2, 8), dtype=torch.int32, device="cuda"),
+                                lion.MASK_LIT)
+
