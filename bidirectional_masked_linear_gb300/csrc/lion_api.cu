@@ -7,6 +7,10 @@
 #include "lion_common.cuh"
 #include "lion_internal.h"
 
+namespace lion {
+lion_status forward_checked(const lion_args* a);
+}
+
 namespace {
 
 using lion::Problem;
@@ -160,6 +164,15 @@ lion_status lion_attn_bwd(const lion_bwd_args* a) {
 lion_status lion_attn_fwd_ex(const lion_args* a) {
   lion_status st = validate(a);
   if (st != LION_OK) return st;
+  return lion::forward_checked(a);
+}
+
+}  // extern "C"
+
+// The forward on arguments that already passed validate(): the kernel choice,
+// the workspace and the launches (also the per-slice step of the host-buffer
+// entry point, whose buffers the library allocated itself).
+lion_status lion::forward_checked(const lion_args* a) {
   Problem p;
   p.q = a->q;
   p.k = a->k;
@@ -218,6 +231,8 @@ lion_status lion_attn_fwd_ex(const lion_args* a) {
   }
   return from_cuda(e);
 }
+
+extern "C" {
 
 lion_status lion_sync_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);

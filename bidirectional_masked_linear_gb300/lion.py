@@ -70,12 +70,24 @@ class _ReorderArgs(ctypes.Structure):
     ]
 
 
+class _HostArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_lambda", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int),
+        ("mask_kind", ctypes.c_int), ("form", ctypes.c_int), ("chunk", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("phi", ctypes.c_int), ("slices", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "lion_rnn_step",
            "lion_status_string", "lion_abi_version", "lion_sync_status",
            "lion_attn_fwd_rnn_noalloc", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
-           "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes")
+           "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes",
+           "lion_attn_fwd_host")
 NOALLOC_MAX_HEAD_TOKENS = 1 << 20
 
 
@@ -115,6 +127,8 @@ def load(path: str = LIB_PATH):
     lib.lion_attn_fwd_reordered.restype = i
     lib.lion_attn_reordered_workspace_bytes.argtypes = [i, i, i, i]
     lib.lion_attn_reordered_workspace_bytes.restype = ctypes.c_size_t
+    lib.lion_attn_fwd_host.argtypes = [ctypes.POINTER(_HostArgs)]
+    lib.lion_attn_fwd_host.restype = i
     _lib = lib
     return lib
 
@@ -323,3 +337,29 @@ def attn_fwd_reordered(q, k, v, log_lambda, orders, mask_kind, out=None, phi=PHI
                      _stream_handle(stream))
     _check(lib.lion_attn_fwd_reordered(ctypes.byref(a)))
     return out
+
+
+def attn_fwd_host(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None, phi=PHI_DEFAULT,
+                  slices=0, stream=None):
+    """The operator on CPU tensors (page-locked for overlap): the library
+    copies batch slices in, computes and copies them out on overlapping
+    streams.  Returns the CPU float32 output, complete once ``stream`` (the
+    current stream by default) is synchronised."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    if isinstance(form, str):
+        form = FORMS[form]
+    B, H, L, d = q.shape
+    if out is None:
+        out = torch.empty((B, H, L, d), dtype=torch.float32, pin_memory=True)
+    for t in (q, k, v, out) + ((log_lambda,) if log_lambda is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if t.is_cuda:
+            raise ValueError("attn_fwd_host takes host tensors; use attn_fwd for device tensors")
+    a = _HostArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(out), B, H, L, d, mask_kind, form, chunk,
+                  _dtype_code(q), phi, slices, _stream_handle(stream))
+    _check(lib.lion_attn_fwd_host(ctypes.byref(a)))
+    return out
+

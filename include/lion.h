@@ -237,6 +237,41 @@ lion_status lion_attn_bwd(const lion_bwd_args* a);
 size_t lion_attn_bwd_workspace_bytes(int B, int H, int L, int d);
 
 /*
+ * lion_attn_fwd_host -- lion_attn_fwd_ex on inputs and output in host memory.
+ * The library cuts the batch into `slices` slices (0: min(B, 4)) and, with two
+ * device buffer sets, copies slice s in on one internal stream, runs the
+ * operator on it on `stream` and copies its output out on another, so that
+ * copies in, compute and copies out of neighbouring slices overlap.  Every
+ * copy is a single cudaMemcpyAsync of a contiguous slice.
+ *   q, k, v, log_lambda, out: host memory with the layouts of lion_args.
+ *   Page-locked memory (cudaHostAlloc / cudaHostRegister) is needed for the
+ *   overlap; pageable memory is accepted and copied synchronously.  Device
+ *   memory is refused (LION_ERR_INVALID_ARG): use lion_attn_fwd_ex.
+ *   Other fields as lion_args.  Device memory for the slices is allocated
+ *   stream-ordered on `stream` and freed in its order.
+ * Asynchronous like the other entry points: work already queued on `stream`
+ * comes first, later work on `stream` comes after the last copy out, and out
+ * is complete once `stream` is synchronised.  The host buffers must stay
+ * valid until then.
+ */
+typedef struct {
+  const void* q;             /* host [B][H][L][d], dtype below             */
+  const void* k;
+  const void* v;
+  const float* log_lambda;   /* host, as lion_args                         */
+  float* out;                /* host [B][H][L][d] float32                  */
+  int B, H, L, d;
+  int mask_kind;             /* lion_mask_kind                             */
+  int form;                  /* lion_form                                  */
+  int chunk;                 /* LION_FORM_CHUNK only                       */
+  int dtype;                 /* lion_dtype of q, k, v                      */
+  int phi;                   /* lion_phi                                   */
+  int slices;                /* batch slices (0: the library picks)        */
+  cudaStream_t stream;
+} lion_host_args;
+lion_status lion_attn_fwd_host(const lion_host_args* a);
+
+/*
  * lion_attn_fwd_reordered -- the full form with the mask averaged over two
  * traversal orders of the tokens: LION-S (v2) and the reordered-patch LION-D
  * and LION-S (rebuttal page reply "P2: Comparison against vision SSMs",

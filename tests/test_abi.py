@@ -100,6 +100,28 @@ def test_reordered_invalid_arguments_rejected_before_launch(lib, kw):
     assert lib.lion_attn_fwd_reordered(None) == 1
 
 
+def _host(lib, **kw):
+    from bidirectional_masked_linear_gb300 import lion
+    buf = (ctypes.c_char * 65536)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    f = dict(q=base, k=base + 4096, v=base + 8192, log_lambda=base + 12288, out=base + 16384, B=1, H=1, L=8,
+             d=64, mask_kind=0, form=2, chunk=64, dtype=0, phi=0, slices=0, stream=0)
+    f.update(kw)
+    a = lion._HostArgs(**f)
+    lib.lion_attn_fwd_host.argtypes = [ctypes.POINTER(lion._HostArgs)]
+    return lib.lion_attn_fwd_host(ctypes.byref(a))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(k=0), dict(v=0), dict(out=0), dict(B=0), dict(H=0), dict(L=0), dict(d=48),
+    dict(mask_kind=3), dict(form=3), dict(chunk=0), dict(dtype=2), dict(phi=4), dict(slices=-1),
+    dict(mask_kind=2, log_lambda=0), dict(mask_kind=1, log_lambda=0),
+])
+def test_host_entry_invalid_arguments_rejected(lib, kw):
+    assert _host(lib, **kw) == 1
+    assert lib.lion_attn_fwd_host(None) == 1
+
+
 def _bwd(lib, **kw):
     from bidirectional_masked_linear_gb300 import lion
     f = dict(q=4096, k=8192, v=12288, log_lambda=0, dy=16384, dq=20480, dk=24576, dv=28672,

@@ -541,3 +541,33 @@ def test_reordered_invalid_orders_are_reported():
         lion.attn_fwd_reordered(q32, q32, q32, None, torch.zeros((2, 8), dtype=torch.int32, device="cuda"),
                                 lion.MASK_LIT)
 
+
+# ------------------------------------------------- host-buffer entry -----
+# lion_attn_fwd_host runs the same kernels on slices of the batch copied in
+# and out by the library: its output equals the device entry point's bit for
+# bit, whatever the slicing.
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_host_entry_matches_device_entry(mask):
+    for B, H, L, chunk, form, dtype in ((5, 3, 197, 128, "chunk", "bf16"), (3, 2, 300, 128, "chunk", "bf16"),
+                                        (4, 2, 64, 64, "full", "fp32"), (2, 2, 77, 16, "rnn", "fp32")):
+        inp = synth.make_inputs(B, H, L, 64, mask, dtype, seed=1300 + L)
+        g = _cuda(inp)
+        want = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], form, chunk).cpu()
+        host = {k: (None if inp[k] is None else inp[k].contiguous().pin_memory()) for k in ("q", "k", "v", "log_lambda")}
+        for slices in (0, 1, 2, 3, B):
+            got = lion.attn_fwd_host(host["q"], host["k"], host["v"], host["log_lambda"], inp["mask"], form, chunk,
+                                     slices=slices)
+            torch.cuda.synchronize()
+            assert torch.equal(got, want), (B, L, form, slices)
+    # pageable host memory is accepted (copied synchronously); device memory is refused
+    inp = synth.make_inputs(2, 2, 50, 64, mask, "bf16", seed=1390)
+    g = _cuda(inp)
+    want = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], "chunk", 64).cpu()
+    got = lion.attn_fwd_host(inp["q"], inp["k"], inp["v"], inp["log_lambda"], inp["mask"], "chunk", 64,
+                             out=torch.empty_like(want))
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    with pytest.raises(ValueError):
+        lion.attn_fwd_host(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], "chunk", 64)
+
