@@ -98,12 +98,13 @@ def _peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def algorithmic_bytes(w, mask: str) -> int:
-    """Bytes the operator must move per call: q, k, v read once, y (fp32)
-    written once, plus the decays (per token for LION-S, per head for D)."""
+def algorithmic_bytes(w, mask: str, out_bytes: int = 4) -> int:
+    """Bytes the operator must move per call: q, k, v read once, y (fp32, or
+    bf16 with out_bytes = 2) written once, plus the decays (per token for
+    LION-S, per head for D)."""
     el = 2 if w.dtype == "bf16" else 4
     n = w.B * w.H * w.L * w.d
-    b = 3 * n * el + 4 * n
+    b = 3 * n * el + out_bytes * n
     if mask == "s":
         b += 4 * w.B * w.H * w.L
     elif mask == "d":
@@ -226,11 +227,11 @@ def _workload(name, batch=0):
     return w
 
 
-def measure(name, mask, chunk, form, steps, warmup, flush, batch=0):
+def measure(name, mask, chunk, form, steps, warmup, flush, batch=0, out_dtype=torch.float32):
     w = _workload(name, batch)
     inp = synth.make_inputs(w.B, w.H, w.L, w.d, mask, w.dtype, w.seed, w.lam)
     dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
-    out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    out = torch.empty((w.B, w.H, w.L, w.d), dtype=out_dtype, device="cuda")
     fcode = lion.FORMS[form]
     wsb = lion.workspace_bytes(w.B, w.H, w.L, w.d, fcode, chunk)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
@@ -562,6 +563,19 @@ def main():
                             "frac": b3 / (ms3 * 1e-3) / 1e9 / hbm_peak}}
         del _k3
 
+    bf16_out = None
+    if not args.no_secondary and args.form == "chunk" and args.chunk == 128 and w.dtype == "bf16":
+        w4, _, t4, _k4 = measure(args.workload, args.mask, 128, "chunk", 50, 3, flush, args.batch,
+                                 out_dtype=torch.bfloat16)
+        ms4 = statistics.mean(t4)
+        b4 = algorithmic_bytes(w4, args.mask, out_bytes=2)
+        bf16_out = {"workload": _config(args, w)["workload"], "out_dtype": "bf16 (the fp32 result rounded to nearest even)",
+                    "value": w4.B * w4.L / (ms4 * 1e-3), "unit": "tokens/s", "ms_per_step": ms4,
+                    "roofline": {"bound": "hbm", "achieved": b4 / (ms4 * 1e-3) / 1e9, "peak": hbm_peak,
+                                 "unit": "GB/s", "frac": b4 / (ms4 * 1e-3) / 1e9 / hbm_peak,
+                                 "algorithmic_bytes": b4}}
+        del _k4
+
     backward = None
     if not args.no_backward and w.L <= lion.FULL_MAX_L:
         tb = measure_bwd(w, args.mask, 20, 3, flush)
@@ -623,6 +637,7 @@ def main():
             "wall_s_timed_region": t_wall,
             "secondary": secondary,
             "lra": lra,
+            "bf16_out": bf16_out,
             "backward": backward,
             "reordered": reordered,
             "streaming": streaming,

@@ -48,6 +48,7 @@ lion_status validate(const lion_args* a) {
   if (a->dtype != LION_DTYPE_BF16 && a->dtype != LION_DTYPE_FP32) return LION_ERR_INVALID_ARG;
   if (a->phi < LION_PHI_DEFAULT || a->phi > LION_PHI_IDENTITY) return LION_ERR_INVALID_ARG;
   if (a->form == LION_FORM_CHUNK && a->chunk < 1) return LION_ERR_INVALID_ARG;
+  if (a->out_bf16 != 0 && a->out_bf16 != 1) return LION_ERR_INVALID_ARG;
   if (a->mask_kind != LION_MASK_LIT && !a->log_lambda) return LION_ERR_INVALID_ARG;
   // 32-bit launch and index limits: B*H heads on one grid axis, L*d per head.
   if ((long long)a->B * a->H > 0x7fffffffLL || (long long)a->L * a->d > 0x7fffffffLL)
@@ -75,7 +76,7 @@ lion_status from_cuda(cudaError_t e) {
 
 extern "C" {
 
-int lion_abi_version(void) { return 1; }
+int lion_abi_version(void) { return 2; }
 
 const char* lion_status_string(lion_status s) {
   switch (s) {
@@ -214,6 +215,21 @@ lion_status lion::forward_checked(const lion_args* a) {
     }
     owned = true;
   }
+  // bfloat16 output: stored by the chunk-128 kernels themselves; the other
+  // paths write fp32 into a stream-ordered temporary that is then rounded
+  const size_t n_out = (size_t)a->B * a->H * a->L * a->d;
+  float* tmp = nullptr;
+  if (a->out_bf16 && (use_tc128 || use_tc128l)) {
+    p.out_bf16 = 1;
+  } else if (a->out_bf16) {
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&tmp), sizeof(float) * n_out, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      if (owned) cudaFreeAsync(ws, s);
+      return e == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
+    }
+    p.out = tmp;
+  }
   cudaError_t e = cudaSuccess;
   switch (a->form) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
@@ -224,6 +240,11 @@ lion_status lion::forward_checked(const lion_args* a) {
           : use_tc     ? lion::launch_chunk_tc(p, ws, dstatus, s)
                        : lion::launch_chunk_simt(p, (float*)ws, s);
       break;
+  }
+  if (tmp) {
+    if (e == cudaSuccess) e = lion::launch_f32_to_bf16(tmp, a->out, n_out, s);
+    cudaError_t f = cudaFreeAsync(tmp, s);
+    if (e == cudaSuccess) e = f;
   }
   if (owned) {
     cudaError_t f = cudaFreeAsync(ws, s);
@@ -281,11 +302,27 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
     }
     owned = true;
   }
+  const size_t n_out = (size_t)a->B * a->H * a->L * a->d;
+  float* tmp = nullptr;
+  if (a->out_bf16) {   // fp32 into a temporary, then rounded to bfloat16
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&tmp), sizeof(float) * n_out, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      if (owned) cudaFreeAsync(ws, s);
+      return e == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
+    }
+    p.out = tmp;
+  }
   cudaError_t e = cudaSuccess;
   switch (a->form) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
     case LION_FORM_CHUNK: e = lion::launch_chunk_simt(p, (float*)ws, s); break;
+  }
+  if (tmp) {
+    if (e == cudaSuccess) e = lion::launch_f32_to_bf16(tmp, a->out, n_out, s);
+    cudaError_t f = cudaFreeAsync(tmp, s);
+    if (e == cudaSuccess) e = f;
   }
   if (owned) {
     cudaError_t f = cudaFreeAsync(ws, s);

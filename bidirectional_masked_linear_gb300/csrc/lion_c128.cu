@@ -146,6 +146,7 @@ constexpr uint32_t T_S = 160;     // + 128 c: S_c, P_c in its first 64 columns
 struct C128Params {
   const float* log_lambda;
   int BH, H, L;
+  int out_bf16;   // 1: y stored as bfloat16 (one 64-column store per warp)
   int* status;
 };
 
@@ -623,8 +624,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = 1.f / ob1[0];
         const float2 inv2 = make_float2(inv, inv);
         uint8_t* row = stg + lane * 128;
+        if (prm.out_bf16) {
+          // the row's 64 columns as bfloat16 fill one 128-byte staging row:
+          // one store, the same values as the fp32 path, rounded
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
+          for (int blk = 0; blk < 4; ++blk) {
+            if (blk > 0) {
+              tmem_ld16(oa + 16 * blk, ob0);
+              tmem_wait_ld();
+              reg_fence16(ob0);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float y8[8];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const float2 y = mul2(make_float2(ob0[8 * e + 2 * t], ob0[8 * e + 2 * t + 1]), inv2);
+                y8[2 * t] = y.x;
+                y8[2 * t + 1] = y.y;
+              }
+              *reinterpret_cast<uint4*>(row + (((2 * blk + e) ^ (lane & 7)) << 4)) = pack8_bf(y8);
+            }
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&mapO, stg, 0, kC * g + 32 * q, bh);
+            bulk_commit();
+          }
+        }
+#pragma unroll 1
+        for (int half = 0; half < 2 && !prm.out_bf16; ++half) {
           if (half == 1) {
             // the first store has to be done reading the staging
             if (lane == 0) bulk_wait_read();
@@ -692,13 +722,14 @@ cudaError_t launch_chunk128_tc(const Problem& p, int* status, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mo;
   const int BH = p.B * p.H;
   if (!make_map128(&mq, p.q, p.L, BH) || !make_map128(&mk, p.k, p.L, BH) || !make_map128(&mv, p.v, p.L, BH) ||
-      !make_out_map(&mo, p.out, p.L, BH))
+      !(p.out_bf16 ? make_out_map_bf16(&mo, p.out, p.L, BH, 64) : make_out_map(&mo, p.out, p.L, BH)))
     return cudaErrorInvalidValue;
   C128Params prm;
   prm.log_lambda = p.log_lambda;
   prm.BH = BH;
   prm.H = p.H;
   prm.L = p.L;
+  prm.out_bf16 = p.out_bf16;
   prm.status = status;
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, C128Params) = nullptr;
 #define LION_C128_CASE(M, F) \

@@ -140,6 +140,7 @@ struct LongParams {
   const uint8_t* gst;       // [BH][chunks] pre-pass states (kGstBytes each)
   const float* segsum;
   const float* segin;
+  int out_bf16;   // 1: y stored as bfloat16 (64-byte staging rows)
   int* status;
 };
 
@@ -743,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_fence16(o);
           reg_fence16(tt);
           reg_fence16(rr);
+          float yv[16];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float2 x0 = make_float2(o[4 * e], o[4 * e + 1]), x1 = make_float2(o[4 * e + 2], o[4 * e + 3]);
@@ -752,7 +754,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             x1 = fma2(b2, make_float2(rr[4 * e + 2], rr[4 * e + 3]), x1);
             x0 = mul2(x0, inv2);
             x1 = mul2(x1, inv2);
-            *reinterpret_cast<float4*>(row + (((4 * h2 + e) ^ (lane & 7)) << 4)) = make_float4(x0.x, x0.y, x1.x, x1.y);
+            yv[4 * e] = x0.x;
+            yv[4 * e + 1] = x0.y;
+            yv[4 * e + 2] = x1.x;
+            yv[4 * e + 3] = x1.y;
+          }
+          if (prm.out_bf16) {
+            // bfloat16: 64-byte staging rows, no swizzle
+#pragma unroll
+            for (int c8 = 0; c8 < 2; ++c8)
+              *reinterpret_cast<uint4*>(stg + lane * 64 + ((2 * h2 + c8) << 4)) = pack8_bf(yv + 8 * c8);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<float4*>(row + (((4 * h2 + e) ^ (lane & 7)) << 4)) =
+                  make_float4(yv[4 * e], yv[4 * e + 1], yv[4 * e + 2], yv[4 * e + 3]);
           }
         }
         fence_async_smem();
@@ -817,9 +833,10 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   CUtensorMap mq, mk, mv, mo;
   const int BH = p.B * p.H;
   if (!make_map128(&mq, p.q, p.L, BH) || !make_map128(&mk, p.k, p.L, BH) || !make_map128(&mv, p.v, p.L, BH) ||
-      !make_out_map(&mo, p.out, p.L, BH))
+      !(p.out_bf16 ? make_out_map_bf16(&mo, p.out, p.L, BH, 32) : make_out_map(&mo, p.out, p.L, BH)))
     return cudaErrorInvalidValue;
   LongParams prm;
+  prm.out_bf16 = p.out_bf16;
   prm.log_lambda = p.log_lambda;
   prm.BH = BH;
   prm.H = p.H;

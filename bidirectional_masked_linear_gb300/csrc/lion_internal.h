@@ -12,13 +12,14 @@ struct Problem {
   const void* k;
   const void* v;
   const float* log_lambda;
-  float* out;
+  float* out;        // bfloat16 [B][H][L][d] when out_bf16 (chunk-128 kernels only)
   int B, H, L, d;
   int mask_kind;
   int phi;     // resolved (never PHI_DEFAULT)
   int dtype;   // DT_BF16 / DT_FP32
   int chunk;
   int causal = 0;   // 1: only j <= i (the forward half), SIMT kernels only
+  int out_bf16 = 0; // 1: the chunk-128 tensor-core kernels store y as bfloat16
 };
 
 // SIMT (CUDA-core) kernels: any d in {16,32,64,128}, both dtypes.
@@ -93,6 +94,9 @@ cudaError_t launch_bwd(const Problem& p, const float* dy, float* dq, float* dk, 
 size_t reorder_workspace_bytes(int B, int H, int L, int d);
 int reorder_launches(int mask_kind);
 cudaError_t launch_reordered(const Problem& p, const int* order, void* ws, int* status, cudaStream_t s);
+
+// y (fp32, n values) rounded to nearest even bfloat16.
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);
 
 // Device-side status word that kernels set when a bounded wait gives up
 // (kStatusTimeout) or a traversal order is not a permutation

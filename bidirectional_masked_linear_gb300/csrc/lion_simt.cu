@@ -548,6 +548,29 @@ cudaError_t step_launch(const void* q, const void* k, const void* v, const float
 
 }  // namespace
 
+namespace {
+// fp32 -> bfloat16, round to nearest even, four values a thread
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float* src, __nv_bfloat16* dst, size_t n) {
+  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i + 4 <= n) {
+    const float4 v = *reinterpret_cast<const float4*>(src + i);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst + i) = u;
+  } else {
+    for (size_t t = i; t < n; ++t) dst[t] = __float2bfloat16_rn(src[t]);
+  }
+}
+}  // namespace
+
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s) {
+  const size_t threads = (n + 3) / 4;
+  f32_to_bf16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(src, static_cast<__nv_bfloat16*>(dst), n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_full_simt(const Problem& p, cudaStream_t s) { return dispatch<FullF>(p, s); }
 cudaError_t launch_rnn_simt(const Problem& p, float* ws, cudaStream_t s) { return dispatch<RnnF>(p, ws, s); }
 cudaError_t launch_chunk_simt(const Problem& p, float* ws, cudaStream_t s) { return dispatch<ChunkF>(p, ws, s); }

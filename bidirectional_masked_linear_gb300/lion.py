@@ -42,7 +42,7 @@ class _Args(ctypes.Structure):
         ("mask_kind", ctypes.c_int), ("form", ctypes.c_int), ("chunk", ctypes.c_int),
         ("dtype", ctypes.c_int), ("phi", ctypes.c_int),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("stream", ctypes.c_void_p),
+        ("stream", ctypes.c_void_p), ("out_bf16", ctypes.c_int),
     ]
 
 
@@ -171,11 +171,12 @@ def workspace_bytes(B, H, L, d, form, chunk=64) -> int:
 
 
 def attn_fwd(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None,
-             phi=PHI_DEFAULT, workspace=None, stream=None):
+             phi=PHI_DEFAULT, workspace=None, stream=None, out_dtype=torch.float32):
     """Y = SCALE((phi(Q) phi(K)^T (.) M) V) for q, k, v of shape [B, H, L, d].
 
     ``log_lambda``: None (LIT), [H] (D) or [B, H, L] (S), float32, on the GPU.
-    Returns ``out`` ([B, H, L, d] float32)."""
+    Returns ``out`` ([B, H, L, d], float32, or bfloat16 with ``out_dtype``:
+    the fp32 result rounded to nearest even)."""
     lib = load()
     if isinstance(mask_kind, str):
         mask_kind = MASKS[mask_kind]
@@ -183,7 +184,10 @@ def attn_fwd(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None
         form = FORMS[form]
     B, H, L, d = q.shape
     if out is None:
-        out = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+        out = torch.empty((B, H, L, d), dtype=out_dtype, device=q.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
+    out_bf16 = int(out.dtype == torch.bfloat16)
     dt = _dtype_code(q)
     if log_lambda is not None and log_lambda.dtype != torch.float32:
         raise TypeError("log_lambda must be float32")
@@ -193,13 +197,14 @@ def attn_fwd(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None
     if q.dtype != k.dtype or q.dtype != v.dtype or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must share dtype and shape")
     stream_h = _stream_handle(stream)
-    if dt == DTYPE_BF16 and phi == PHI_DEFAULT and workspace is None:
+    if dt == DTYPE_BF16 and phi == PHI_DEFAULT and workspace is None and not out_bf16:
         st = lib.lion_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), B, H, L, d, mask_kind,
                                form, chunk, _ptr(out), stream_h)
     else:
         a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(out), B, H, L, d, mask_kind,
                   form, chunk, dt, phi, _ptr(workspace),
-                  0 if workspace is None else workspace.numel() * workspace.element_size(), stream_h)
+                  0 if workspace is None else workspace.numel() * workspace.element_size(), stream_h,
+                  out_bf16)
         st = lib.lion_attn_fwd_ex(ctypes.byref(a))
     _check(st)
     return out
@@ -289,7 +294,7 @@ class LionAttention(torch.autograd.Function):
 
 
 def attn_fwd_causal(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out=None,
-                    phi=PHI_DEFAULT, workspace=None, stream=None):
+                    phi=PHI_DEFAULT, workspace=None, stream=None, out_dtype=torch.float32):
     """The forward half alone (a unidirectional model): y_i = sum_{j<=i}
     M_ij s_ij v_j / sum_{j<=i} M_ij s_ij, in any form."""
     lib = load()
@@ -299,14 +304,16 @@ def attn_fwd_causal(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, o
         form = FORMS[form]
     B, H, L, d = q.shape
     if out is None:
-        out = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+        out = torch.empty((B, H, L, d), dtype=out_dtype, device=q.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
     for t in (q, k, v, out) + ((log_lambda,) if log_lambda is not None else ()):
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
     a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(out), B, H, L, d, mask_kind,
               form, chunk, _dtype_code(q), phi, _ptr(workspace),
               0 if workspace is None else workspace.numel() * workspace.element_size(),
-              _stream_handle(stream))
+              _stream_handle(stream), int(out.dtype == torch.bfloat16))
     _check(lib.lion_attn_fwd_causal(ctypes.byref(a)))
     return out
 

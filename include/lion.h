@@ -111,12 +111,21 @@ typedef struct {
   void* workspace;           /* device, 256-byte aligned, or NULL          */
   size_t workspace_bytes;    /* >= lion_attn_workspace_bytes(...) if given */
   cudaStream_t stream;
+  int out_bf16;              /* 0: out is float32; 1: out is bfloat16      */
 } lion_args;
 
 /*
  * lion_attn_fwd_ex -- as lion_attn_fwd with a dtype (BF16 or FP32 inputs), a
- * feature-map override and an optional caller workspace.  With
- * workspace == NULL the library allocates what it needs stream-ordered.
+ * feature-map override, an optional caller workspace and an optional
+ * bfloat16 output.  With workspace == NULL the library allocates what it
+ * needs stream-ordered.
+ *   out_bf16 = 1: out is [B][H][L][d] bfloat16 (16-byte aligned), each value
+ *   the fp32 result rounded to nearest even (the arithmetic is unchanged).
+ *   The chunk-128 tensor-core kernels (bf16 inputs, d = 64, chunk = 128)
+ *   store it themselves, which halves their output bytes; every other path
+ *   computes into a stream-ordered fp32 temporary of B*H*L*d floats
+ *   (allocated by the library, not part of the workspace) and rounds it.
+ *   lion_attn_fwd_causal takes the field the same way.
  */
 lion_status lion_attn_fwd_ex(const lion_args* a);
 

@@ -48,7 +48,7 @@ def test_status_strings_and_version(lib):
     assert lib.lion_status_string(0) == b"ok"
     assert b"invalid" in lib.lion_status_string(1)
     assert lib.lion_status_string(99) == b"unknown status"
-    assert lib.lion_abi_version() == 1
+    assert lib.lion_abi_version() == 2
 
 
 def test_workspace_query(lib):

@@ -20,6 +20,8 @@ def test_algorithmic_bytes_vit_b():
     # 3 bf16 inputs + fp32 output per (token, head, feature), plus the LION-S decays
     assert bench.algorithmic_bytes(w, "s") == w.B * w.H * w.L * (644)
     assert bench.algorithmic_bytes(w, "lit") == w.B * w.H * w.L * 640
+    # bf16 output: 2 bytes instead of 4 per output value
+    assert bench.algorithmic_bytes(w, "s", out_bytes=2) == w.B * w.H * w.L * 516
 
 
 def test_traffic_is_null_for_unknown_kernels():

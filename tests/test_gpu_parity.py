@@ -571,3 +571,30 @@ def test_host_entry_matches_device_entry(mask):
     with pytest.raises(ValueError):
         lion.attn_fwd_host(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], "chunk", 64)
 
+
+# --------------------------------------------------- bfloat16 output -----
+# out_bf16: the chunk-128 kernels store y as bfloat16 themselves; the other
+# paths round an fp32 temporary.  Either way each value must be the fp32
+# result rounded to nearest even, bit for bit.
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_bf16_output_is_the_rounded_fp32_output(mask):
+    for B, H, L, form, chunk, dtype in ((3, 4, 197, "chunk", 128, "bf16"),   # chunk-128, L <= 256
+                                        (2, 2, 700, "chunk", 128, "bf16"),   # chunk-128, long
+                                        (2, 2, 150, "chunk", 64, "bf16"),    # chunk-64, rounded after
+                                        (2, 2, 90, "full", 1, "fp32"), (2, 2, 90, "rnn", 1, "fp32")):
+        inp = synth.make_inputs(B, H, L, 64, mask, dtype, seed=1400 + L)
+        g = _cuda(inp)
+        y32 = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], form, chunk)
+        y16 = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], form, chunk,
+                            out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        assert y16.dtype == torch.bfloat16
+        assert torch.equal(y16, y32.to(torch.bfloat16)), (B, L, form, chunk)
+    inp = synth.make_inputs(2, 2, 100, 64, mask, "bf16", seed=1450)
+    g = _cuda(inp)
+    y32 = lion.attn_fwd_causal(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], "chunk", 32)
+    y16 = lion.attn_fwd_causal(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], "chunk", 32,
+                               out_dtype=torch.bfloat16)
+    assert torch.equal(y16, y32.to(torch.bfloat16))
+
