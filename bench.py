@@ -55,13 +55,13 @@ TRAFFIC_PER_HEAD = {
     # chunk-64 kernel, ViT-B shape at B=128, LION-S: 160.7 MB / 1536 heads
     ("fc4be66a869d6463b1ad06b8b0948a689343c3e6648cdb380430aac91fcace8c", "vit_b", "s", 64):
         (117664768 + 43027200) / 1536,
-    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 154.2 MB / 1536 heads
-    ("cd7374c887e34b93d59863825085e6318b533036691eec3187d21c51d5ee0c8b", "vit_b", "s", 128):
-        (117489408 + 36713728) / 1536,
+    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 153.4 MB / 1536 heads
+    ("1d94bfce7f698332337e9082c69accf2eb23926ea5fd5714a0ca66268b715025", "vit_b", "s", 128):
+        (117490176 + 35867392) / 1536,
     # chunk-128 main pass for long sequences, L=24337 (B=2, H=12), LION-S:
-    # 386.4 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
-    ("f5392832814fe3f453e48183bf94befb7eaf5f8eef334cc21c56b81c2d242666", "hires_2496", "s", 128):
-        (271398656 + 114964992) / 24,
+    # 386.3 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
+    ("9e4ae8f3d02e1d004ba40516a00124ecf0cf02e9d164a2890ac00e37e0f87b8f", "hires_2496", "s", 128):
+        (271414528 + 114904064) / 24,
 }
 
 
