@@ -164,6 +164,55 @@ def test_long_sequences_blocks_and_segments(oracle_mod, mask):
         check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 64), ref, inp, TOL_BF16)
 
 
+# ----------------------------------------------------- maximum lengths --
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("d", "s"))
+def test_full_form_at_its_maximum_length(oracle_mod, mask):
+    """L = LION_FULL_MAX_L through the full form, against the oracle's brute
+    force on sampled rows (first, last, tile edges and random ones)."""
+    L = lion.FULL_MAX_L
+    inp = synth.make_inputs(1, 2, L, 64, mask, "bf16", seed=1500)
+    y = run_gpu(inp, lion.FORM_FULL, 64)
+    q, k, v, ll = f64(inp)
+    rng = np.random.default_rng(1501)
+    rows = np.unique(np.r_[0, 1, 31, 32, 63, 64, L // 2, L - 33, L - 2, L - 1, rng.integers(0, L, 22)])
+    kind = 2 if inp["mask"] == lion.MASK_S else 1
+    for h in range(2):
+        ref = oracle_mod.rows(q, k, v, ll, inp["mask"], 0, h, rows)
+        err = row_errors(y[0, h, rows], ref)
+        for r, e in zip(rows, err):
+            kap = oracle_mod.row_kappa(q, k, ll, inp["mask"], 0, h, int(r), int(r) + 1, kind)[0]
+            assert e <= TOL_BF16 * max(1.0, kap), (h, int(r), e, kap)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("d", "s"))
+def test_backward_at_its_maximum_length(mask):
+    """Gradients at L = LION_FULL_MAX_L (the recompute build), checked by two
+    identities that hold at any size: y is homogeneous of degree 1 in v, so
+    sum_j dv_j . v_j = sum_i dy_i . y_i; and with identity features y_i does
+    not change when q_i is scaled, so dq_i . q_i = 0 for every row."""
+    L = lion.FULL_MAX_L
+    inp = synth.make_inputs(1, 1, L, 64, mask, "fp32", seed=1510)
+    for key in ("q", "k"):
+        inp[key] = inp[key].abs() + 0.25
+    g = _cuda(inp)
+    dy = torch.randn((1, 1, L, 64), device="cuda", generator=torch.Generator(device="cuda").manual_seed(1511))
+    dq, dk, dv, dll = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], dy, inp["mask"], 3)
+    y = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], lion.FORM_FULL, 64, phi=3)
+    torch.cuda.synchronize()
+    v = g["v"].double()
+    lhs = float((dv.double() * v).sum())
+    rhs = float((dy.double() * y.double()).sum())
+    scale = float((dv.double() * v).abs().sum() + (dy.double() * y.double()).abs().sum())
+    assert abs(lhs - rhs) <= 1e-5 * scale, (lhs, rhs, scale)
+    qd = g["q"].double()
+    dot = (dq.double() * qd).sum(-1).abs()
+    mag = (dq.double().abs() * qd.abs()).sum(-1)
+    assert bool((dot <= 1e-4 * mag + 1e-30).all()), float((dot / mag).max())
+    assert bool(torch.isfinite(dk).all()) and bool(torch.isfinite(dll).all())
+
+
 # ----------------------------------------------------------- edge cases --
 @pytest.mark.parametrize("mask", ("d", "s"))
 def test_vanishing_decay_is_identity(oracle_mod, mask):
