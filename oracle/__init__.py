@@ -74,6 +74,9 @@ def _load():
         lib.oracle_lion_full_bwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, dp, dp, dp, dp, i]
         lib.oracle_lion_full_reordered.argtypes = [dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int),
                                                    i, i, i, i, i, i, dp, i]
+        lib.oracle_lion_full_bwd_reordered.argtypes = [dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int), dp,
+                                                       i, i, i, i, i, i, dp, dp, dp, dp, i]
+        lib.oracle_lion_full_bwd_reordered.restype = ctypes.c_int
         for f in (lib.oracle_phi, lib.oracle_mask, lib.oracle_lion_full, lib.oracle_lion_rnn,
                   lib.oracle_lion_chunk, lib.oracle_lion_rows, lib.oracle_row_kappa,
                   lib.oracle_threads, lib.oracle_rnn_forward_half, lib.oracle_lion_full_bwd,
@@ -194,6 +197,30 @@ def full_bwd(q, k, v, log_lambda, dy, mask_kind, phi_kind=PHI_DEFAULT, threads=1
                                       threads)
     if rc:
         raise ValueError(f"oracle_lion_full_bwd failed ({rc})")
+    return dq, dk, dv, dll
+
+
+def full_bwd_reordered(q, k, v, log_lambda, orders, dy, mask_kind, phi_kind=PHI_DEFAULT, threads=1):
+    """Gradients of sum(dy * y) for the reordered full form (``orders`` as in
+    :func:`full_reordered`): ``(dq, dk, dv, dlog_lambda)`` shaped as
+    :func:`full_bwd`'s."""
+    q, k, v, ll = _prep(q, k, v, log_lambda)
+    B, H, L, d = q.shape
+    _check_ll(mask_kind, ll, B, H, L)
+    dy = _f64(dy)
+    if dy.shape != q.shape:
+        raise ValueError("dy must have the shape of q")
+    o = np.ascontiguousarray(np.asarray(orders, dtype=np.int32))
+    if o.shape != (2, L):
+        raise ValueError("orders must be [2][L]")
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    dll = None if mask_kind == MASK_LIT else np.empty((H,) if mask_kind == MASK_D else (B, H, L))
+    rc = _load().oracle_lion_full_bwd_reordered(_ptr(q), _ptr(k), _ptr(v), _ptr(ll),
+                                                o.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), _ptr(dy),
+                                                B, H, L, d, mask_kind, phi_kind, _ptr(dq), _ptr(dk),
+                                                _ptr(dv), _ptr(dll), threads)
+    if rc:
+        raise ValueError(f"oracle_lion_full_bwd_reordered failed ({rc})")
     return dq, dk, dv, dll
 
 

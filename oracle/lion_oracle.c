@@ -463,6 +463,131 @@ int oracle_lion_full_bwd(const double* q, const double* k, const double* v,
   return err;
 }
 
+/* Gradients of the reordered full form (one head).  With M = (M1 + M2) / 2
+ * the products are those of the full-form backward; the decay gradient
+ * follows from dM_ij / dl_u = (1/2) sum_p M^p_ij [the position of u in order
+ * p lies in (min, max] of the positions of i and j in order p], summed over
+ * every pair: dl_u = (1/2) sum_p sum_{i,j} A^p_ij dA_ij over the pairs whose
+ * interval along order p holds u, with A^p_ij = M^p_ij s_ij. */
+static void full_head_bwd_reordered(const double* q, const double* k, const double* v,
+                                    const double* l, const int* orders, const double* dy, int L,
+                                    int d, int phi, double* dq, double* dk, double* dv, double* dl,
+                                    double* fq, double* fk, double* M, double* Mp, double* Mo,
+                                    double* lo, int* pos, double* y, double* g, double* hh,
+                                    double* dfq, double* dfk) {
+  phi_rows(phi, q, k, L, d, fq, fk);
+  for (long t = 0; t < 2L * L * L; ++t) Mp[t] = 0.0;
+  for (int p = 0; p < 2; ++p) {
+    add_mask_along_order(l, orders + (long)p * L, L, 1.0, Mp + (long)p * L * L, lo, Mo);
+    for (int t = 0; t < L; ++t) pos[p * L + orders[(long)p * L + t]] = t;
+  }
+  for (long t = 0; t < (long)L * L; ++t) M[t] = 0.5 * (Mp[t] + Mp[(long)L * L + t]);
+  for (int i = 0; i < L; ++i) {
+    double den = 0.0;
+    for (int n = 0; n < d; ++n) y[(long)i * d + n] = 0.0;
+    for (int j = 0; j < L; ++j) {
+      double s = 0.0;
+      for (int m = 0; m < d; ++m) s += fq[(long)i * d + m] * fk[(long)j * d + m];
+      double a = M[(long)i * L + j] * s;
+      den += a;
+      for (int n = 0; n < d; ++n) y[(long)i * d + n] += a * v[(long)j * d + n];
+    }
+    double dyy = 0.0;
+    for (int n = 0; n < d; ++n) {
+      y[(long)i * d + n] /= den;
+      dyy += dy[(long)i * d + n] * y[(long)i * d + n];
+    }
+    for (int n = 0; n < d; ++n) g[(long)i * d + n] = dy[(long)i * d + n] / den;
+    hh[i] = -dyy / den;
+  }
+  for (long t = 0; t < (long)L * d; ++t) dv[t] = dfq[t] = dfk[t] = 0.0;
+  for (int u = 0; u < L; ++u) dl[u] = 0.0;
+  for (int i = 0; i < L; ++i) {
+    for (int j = 0; j < L; ++j) {
+      double s = 0.0, gv = 0.0;
+      for (int m = 0; m < d; ++m) s += fq[(long)i * d + m] * fk[(long)j * d + m];
+      for (int n = 0; n < d; ++n) gv += g[(long)i * d + n] * v[(long)j * d + n];
+      double mij = M[(long)i * L + j];
+      double a = mij * s;
+      double da = gv + hh[i];
+      for (int n = 0; n < d; ++n) dv[(long)j * d + n] += a * g[(long)i * d + n];
+      double ds = mij * da;
+      for (int m = 0; m < d; ++m) {
+        dfq[(long)i * d + m] += ds * fk[(long)j * d + m];
+        dfk[(long)j * d + m] += ds * fq[(long)i * d + m];
+      }
+      for (int p = 0; p < 2; ++p) {
+        const int* ord = orders + (long)p * L;
+        int pi = pos[p * L + i], pj = pos[p * L + j];
+        int lo_p = pi < pj ? pi : pj, hi_p = pi < pj ? pj : pi;
+        double ap = 0.5 * Mp[(long)p * L * L + (long)i * L + j] * s;
+        for (int w = lo_p + 1; w <= hi_p; ++w) dl[ord[w]] += ap * da;
+      }
+    }
+  }
+  for (int t = 0; t < L; ++t) {
+    phi_row_bwd(phi, q + (long)t * d, dfq + (long)t * d, d, dq + (long)t * d);
+    phi_row_bwd(phi, k + (long)t * d, dfk + (long)t * d, d, dk + (long)t * d);
+  }
+}
+
+/* Reordered full-form backward over all heads: arguments as
+ * oracle_lion_full_bwd plus the two orders ([2][L], permutations). */
+int oracle_lion_full_bwd_reordered(const double* q, const double* k, const double* v,
+                                   const double* log_lambda, const int* orders, const double* dy,
+                                   int B, int H, int L, int d, int mask_kind, int phi_kind,
+                                   double* dq, double* dk, double* dv, double* dlog_lambda,
+                                   int nthreads) {
+  if (check_args(q, k, v, log_lambda, B, H, L, d, mask_kind, phi_kind, dq)) return 1;
+  if (!dy || !dk || !dv || !orders) return 1;
+  if (not_a_permutation(orders, L) || not_a_permutation(orders + L, L)) return 1;
+  if (mask_kind != ORC_MASK_LIT && !dlog_lambda) return 1;
+  int phi = resolve_phi(mask_kind, phi_kind);
+  int nt = set_threads(nthreads);
+  int err = 0;
+  long heads = (long)B * H;
+  double* dl_all = (double*)malloc(sizeof(double) * (size_t)heads * L);
+  if (!dl_all) return 2;
+#pragma omp parallel for schedule(dynamic) num_threads(nt) reduction(| : err)
+  for (long bh = 0; bh < heads; ++bh) {
+    int b = (int)(bh / H), h = (int)(bh % H);
+    size_t Ld = (size_t)L * d, LL = (size_t)L * L;
+    double* l = (double*)malloc(sizeof(double) * L);
+    double* lo = (double*)malloc(sizeof(double) * L);
+    int* pos = (int*)malloc(sizeof(int) * 2 * (size_t)L);
+    double* fq = (double*)malloc(sizeof(double) * Ld);
+    double* fk = (double*)malloc(sizeof(double) * Ld);
+    double* M = (double*)malloc(sizeof(double) * LL);
+    double* Mp = (double*)malloc(sizeof(double) * 2 * LL);
+    double* Mo = (double*)malloc(sizeof(double) * LL);
+    double* y = (double*)malloc(sizeof(double) * Ld);
+    double* g = (double*)malloc(sizeof(double) * Ld);
+    double* hh = (double*)malloc(sizeof(double) * L);
+    double* dfq = (double*)malloc(sizeof(double) * Ld);
+    double* dfk = (double*)malloc(sizeof(double) * Ld);
+    if (!l || !lo || !pos || !fq || !fk || !M || !Mp || !Mo || !y || !g || !hh || !dfq || !dfk) {
+      err |= 2;
+    } else {
+      long off = bh * (long)Ld;
+      head_log_lambda(mask_kind, log_lambda, b, h, H, L, l);
+      full_head_bwd_reordered(q + off, k + off, v + off, l, orders, dy + off, L, d, phi, dq + off,
+                              dk + off, dv + off, dl_all + bh * L, fq, fk, M, Mp, Mo, lo, pos, y, g,
+                              hh, dfq, dfk);
+    }
+    free(l); free(lo); free(pos); free(fq); free(fk); free(M); free(Mp); free(Mo);
+    free(y); free(g); free(hh); free(dfq); free(dfk);
+  }
+  if (!err && mask_kind == ORC_MASK_S) {
+    memcpy(dlog_lambda, dl_all, sizeof(double) * (size_t)heads * L);
+  } else if (!err && mask_kind == ORC_MASK_D) {
+    for (int h = 0; h < H; ++h) dlog_lambda[h] = 0.0;
+    for (long bh = 0; bh < heads; ++bh)
+      for (int u = 0; u < L; ++u) dlog_lambda[bh % H] += dl_all[bh * L + u];
+  }
+  free(dl_all);
+  return err;
+}
+
 /* -------------------------------------------------------- RNN form ----- */
 
 /* Forward recurrence S^F_i = lambda_i S^F_{i-1} + phi(k_i) v_i^T,

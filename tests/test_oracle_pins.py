@@ -531,3 +531,66 @@ def test_reordered_rejects_non_permutations(oracle_mod):
     for bad in (np.array([0, 1, 2, 3, 3]), np.array([0, 1, 2, 3, 5]), np.array([-1, 1, 2, 3, 4])):
         with pytest.raises(ValueError):
             oracle_mod.full_reordered(q, k, v, ll, np.stack([good, bad]), 2)
+
+
+# ----------------------------------------- reordered full-form gradients --
+def _fd_loss_reordered(o, q, k, v, ll, orders, dy, mask_kind, phi_kind):
+    return float(np.sum(dy * o.full_reordered(q, k, v, ll, orders, mask_kind, phi_kind)))
+
+
+@pytest.mark.parametrize("mask_kind", MASKS)
+@pytest.mark.parametrize("phi_kind", (0, 3))
+def test_full_bwd_reordered_matches_finite_differences(oracle_mod, mask_kind, phi_kind):
+    """Every element of dq, dk, dv and dlog_lambda of the reordered full form
+    against central differences of its forward oracle (float64)."""
+    rng = np.random.default_rng(970 + 3 * mask_kind + phi_kind)
+    L = 6
+    q, k, v, ll = _inputs(rng, 1, 2, L, 4, mask_kind, lam_lo=0.5)
+    if phi_kind == 3:
+        q, k = np.abs(q) + 0.3, np.abs(k) + 0.3
+    orders = np.stack([_non_involution(rng, L), _non_involution(rng, L)])
+    dy = rng.standard_normal(q.shape)
+    dq, dk, dv, dll = oracle_mod.full_bwd_reordered(q, k, v, ll, orders, dy, mask_kind, phi_kind)
+    eps = 1e-6
+    named = {"q": (q, dq), "k": (k, dk), "v": (v, dv)}
+    if ll is not None:
+        named["ll"] = (ll, dll)
+    for name, (arr, grad) in named.items():
+        for idx in np.ndindex(arr.shape):
+            args = {"q": q, "k": k, "v": v, "ll": ll}
+            a = arr.copy()
+            a[idx] += eps
+            args[name] = a
+            fp = _fd_loss_reordered(oracle_mod, args["q"], args["k"], args["v"], args["ll"], orders, dy,
+                                    mask_kind, phi_kind)
+            a[idx] -= 2 * eps
+            fm = _fd_loss_reordered(oracle_mod, args["q"], args["k"], args["v"], args["ll"], orders, dy,
+                                    mask_kind, phi_kind)
+            fd = (fp - fm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 2e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+@pytest.mark.parametrize("mask_kind", MASKS)
+def test_full_bwd_reordered_one_order_twice(oracle_mod, mask_kind):
+    """Both orders equal to pi: the gradients of the plain operator on the
+    reordered sequence, put back in place (LIT: the plain gradients)."""
+    rng = np.random.default_rng(980 + mask_kind)
+    B, H, L, d = 2, 2, 9, 4
+    q, k, v, ll = _inputs(rng, B, H, L, d, mask_kind)
+    pi = _non_involution(rng, L)
+    dy = rng.standard_normal(q.shape)
+    got = oracle_mod.full_bwd_reordered(q, k, v, ll, np.stack([pi, pi]), dy, mask_kind)
+    llp = ll[..., pi] if mask_kind == 2 else ll
+    ref = oracle_mod.full_bwd(q[:, :, pi], k[:, :, pi], v[:, :, pi], llp, dy[:, :, pi], mask_kind)
+    for n, (g, r) in enumerate(zip(got[:3], ref[:3])):
+        back = np.empty_like(r)
+        back[:, :, pi] = r
+        assert _rel(g, back) < 1e-12, n
+    if mask_kind == 2:
+        back = np.empty_like(ref[3])
+        back[..., pi] = ref[3]
+        assert _rel(got[3], back) < 1e-12
+    elif mask_kind == 1:
+        assert _rel(got[3], ref[3]) < 1e-12
+    else:
+        assert got[3] is None
