@@ -373,6 +373,26 @@ def measure_reordered(w, mask, steps, warmup, flush):
     return t
 
 
+def measure_reordered_bwd(w, mask, steps, warmup, flush):
+    """CUDA-event time of one lion_attn_bwd_reordered call (the same orders as
+    measure_reordered) with preallocated gradients and workspace."""
+    inp = synth.make_inputs(w.B, w.H, w.L, w.d, mask, w.dtype, w.seed, w.lam)
+    dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
+    orders = vit_grid_orders(w.L).cuda()
+    dy = torch.randn((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(lion.reordered_bwd_workspace_bytes(w.B, w.H, w.L, w.d), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        lion.attn_bwd_reordered(dev["q"], dev["k"], dev["v"], dev["log_lambda"], orders, dy, inp["mask"],
+                                workspace=ws)
+
+    t = time_device(call, steps, warmup, flush, stream)
+    if lion.sync_status() != lion.OK:
+        raise RuntimeError("traversal order rejected on the device")
+    return t
+
+
 def stream_bytes(B, H, d, in_bytes=2) -> int:
     """Bytes one decode step must move: the fp32 state S (d x d) and z read
     and written, the token's q, k, v and log-lambda read, y_part and c_part
@@ -603,6 +623,14 @@ def main():
                                   "frac": flr / (msr * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
                                   "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
                                   "algorithmic_flops": flr}}
+        trb = measure_reordered_bwd(w, args.mask, 10, 3, flush)
+        msrb = statistics.mean(trb)
+        flb = bwd_flops(w)
+        reordered["backward"] = {"ms_per_call": msrb, "value": w.B * w.L / (msrb * 1e-3), "unit": "tokens/s",
+                                 "roofline": {"bound": "alu", "achieved": flb / (msrb * 1e-3) / 1e12,
+                                              "peak": FP32_ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
+                                              "frac": flb / (msrb * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
+                                              "algorithmic_flops": flb}}
 
     streaming = None
     if not args.no_streaming:

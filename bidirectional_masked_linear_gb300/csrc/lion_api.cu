@@ -331,6 +331,67 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
   return from_cuda(e);
 }
 
+size_t lion_attn_reordered_bwd_workspace_bytes(int B, int H, int L, int d) {
+  if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128)) return 0;
+  return lion::reorder_bwd_workspace_bytes(B, H, L, d);
+}
+
+lion_status lion_attn_bwd_reordered(const lion_reorder_bwd_args* a) {
+  if (!a) return LION_ERR_INVALID_ARG;
+  if (!a->q || !a->k || !a->v || !a->dy || !a->dq || !a->dk || !a->dv || !a->order) return LION_ERR_INVALID_ARG;
+  if (a->B < 1 || a->H < 1 || a->L < 1 || !valid_d(a->d)) return LION_ERR_INVALID_ARG;
+  if (a->mask_kind < LION_MASK_LIT || a->mask_kind > LION_MASK_S) return LION_ERR_INVALID_ARG;
+  if (a->dtype != LION_DTYPE_BF16 && a->dtype != LION_DTYPE_FP32) return LION_ERR_INVALID_ARG;
+  if (a->phi < LION_PHI_DEFAULT || a->phi > LION_PHI_IDENTITY) return LION_ERR_INVALID_ARG;
+  if (a->mask_kind != LION_MASK_LIT && (!a->log_lambda || !a->dlog_lambda)) return LION_ERR_INVALID_ARG;
+  if ((long long)a->B * a->H > 0x7fffffffLL || (long long)a->L * a->d > 0x7fffffffLL) return LION_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->q, a->k, a->v, a->dy, a->dq, a->dk, a->dv};
+  for (const void* q : ptrs)
+    if (!aligned(q, 16) || !device_accessible(q)) return LION_ERR_INVALID_ARG;
+  if (!aligned(a->order, 4) || !device_accessible(a->order)) return LION_ERR_INVALID_ARG;
+  if (a->mask_kind != LION_MASK_LIT &&
+      (!aligned(a->log_lambda, 4) || !aligned(a->dlog_lambda, 4) || !device_accessible(a->log_lambda) ||
+       !device_accessible(a->dlog_lambda)))
+    return LION_ERR_INVALID_ARG;
+  if (a->workspace && (!aligned(a->workspace, 256) || !device_accessible(a->workspace))) return LION_ERR_INVALID_ARG;
+  if (a->L > LION_FULL_MAX_L || (a->d != 64 && a->d != 128)) return LION_ERR_UNSUPPORTED;
+  const size_t need = lion::reorder_bwd_workspace_bytes(a->B, a->H, a->L, a->d);
+  if (a->workspace && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
+  int* dstatus = lion::device_status_ptr();
+  if (!dstatus) return LION_ERR_CUDA;
+  Problem p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.log_lambda = a->log_lambda;
+  p.out = nullptr;
+  p.B = a->B;
+  p.H = a->H;
+  p.L = a->L;
+  p.d = a->d;
+  p.mask_kind = a->mask_kind;
+  p.phi = lion::resolve_phi(a->mask_kind, a->phi);
+  p.dtype = a->dtype;
+  p.chunk = 0;
+  cudaStream_t s = a->stream;
+  void* ws = a->workspace;
+  bool owned = false;
+  if (!ws) {
+    cudaError_t e = cudaMallocAsync(&ws, need, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
+    }
+    owned = true;
+  }
+  cudaError_t e = lion::launch_reordered_bwd(p, a->order, a->dy, a->dq, a->dk, a->dv, a->dlog_lambda, ws, dstatus, s);
+  if (owned) {
+    cudaError_t f = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = f;
+  }
+  return from_cuda(e);
+}
+
 size_t lion_attn_reordered_workspace_bytes(int B, int H, int L, int d) {
   if (B < 1 || H < 1 || L < 1 || (d != 64 && d != 128)) return 0;
   return lion::reorder_workspace_bytes(B, H, L, d);

@@ -76,44 +76,6 @@ __device__ __forceinline__ float log_mask(int mask_kind, int i, int j, float lh,
   return 0.f;
 }
 
-// dphi -> dx for this thread's NC features of one row, the row's W threads
-// (adjacent lanes) together holding all of its features and cooperating on
-// the SiLU + L2 norm.
-template <int NC, int W = 8>
-__device__ __forceinline__ void phi_backward(int phi, const float* x, const float* dphi, float* dx) {
-  if (phi == PHI_ELU1) {
-#pragma unroll
-    for (int c = 0; c < NC; ++c) dx[c] = x[c] > 0.f ? dphi[c] : expf(x[c]) * dphi[c];
-  } else if (phi == PHI_SILU_L2) {
-    float u[NC], sg[NC], ss = 0.f;
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      sg[c] = 1.f / (1.f + expf(-x[c]));
-      u[c] = x[c] * sg[c];
-      ss += u[c] * u[c];
-    }
-    const float nrm = sqrtf(group_sum<W>(ss));
-    float dx_scale, dot = 0.f;
-    if (nrm >= 1e-12f) {
-#pragma unroll
-      for (int c = 0; c < NC; ++c) dot += u[c] / nrm * dphi[c];
-      dot = group_sum<W>(dot);
-      dx_scale = 1.f / nrm;
-    } else {
-      dx_scale = 1e12f;
-    }
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const float f = nrm >= 1e-12f ? u[c] / nrm : 0.f;
-      const float du = (dphi[c] - f * dot) * dx_scale;
-      dx[c] = du * sg[c] * (1.f + x[c] * (1.f - sg[c]));
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < NC; ++c) dx[c] = dphi[c];
-  }
-}
-
 struct BwdParams {
   const void* q;
   const void* k;

@@ -94,6 +94,11 @@ cudaError_t launch_bwd(const Problem& p, const float* dy, float* dq, float* dk, 
 size_t reorder_workspace_bytes(int B, int H, int L, int d);
 int reorder_launches(int mask_kind);
 cudaError_t launch_reordered(const Problem& p, const int* order, void* ws, int* status, cudaStream_t s);
+// Its gradients: dq, dk, dv [B][H][L][d], dll (LION-D [H], LION-S [B][H][L]).
+size_t reorder_bwd_workspace_bytes(int B, int H, int L, int d);
+int reorder_bwd_launches(int mask_kind);
+cudaError_t launch_reordered_bwd(const Problem& p, const int* order, const float* dy, float* dq, float* dk, float* dv,
+                                 float* dll, void* ws, int* status, cudaStream_t s);
 
 // y (fp32, n values) rounded to nearest even bfloat16.
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);

@@ -70,6 +70,19 @@ class _ReorderArgs(ctypes.Structure):
     ]
 
 
+class _ReorderBwdArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_lambda", ctypes.c_void_p), ("order", ctypes.c_void_p), ("dy", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dlog_lambda", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int),
+        ("mask_kind", ctypes.c_int), ("dtype", ctypes.c_int), ("phi", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
 class _HostArgs(ctypes.Structure):
     _fields_ = [
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
@@ -87,7 +100,7 @@ EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "li
            "lion_status_string", "lion_abi_version", "lion_sync_status",
            "lion_attn_fwd_rnn_noalloc", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
            "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes",
-           "lion_attn_fwd_host")
+           "lion_attn_fwd_host", "lion_attn_bwd_reordered", "lion_attn_reordered_bwd_workspace_bytes")
 NOALLOC_MAX_HEAD_TOKENS = 1 << 20
 
 
@@ -129,6 +142,10 @@ def load(path: str = LIB_PATH):
     lib.lion_attn_reordered_workspace_bytes.restype = ctypes.c_size_t
     lib.lion_attn_fwd_host.argtypes = [ctypes.POINTER(_HostArgs)]
     lib.lion_attn_fwd_host.restype = i
+    lib.lion_attn_bwd_reordered.argtypes = [ctypes.POINTER(_ReorderBwdArgs)]
+    lib.lion_attn_bwd_reordered.restype = i
+    lib.lion_attn_reordered_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.lion_attn_reordered_bwd_workspace_bytes.restype = ctypes.c_size_t
     _lib = lib
     return lib
 
@@ -369,4 +386,38 @@ def attn_fwd_host(q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=64, out
                   _dtype_code(q), phi, slices, _stream_handle(stream))
     _check(lib.lion_attn_fwd_host(ctypes.byref(a)))
     return out
+
+
+def reordered_bwd_workspace_bytes(B, H, L, d) -> int:
+    return int(load().lion_attn_reordered_bwd_workspace_bytes(B, H, L, d))
+
+
+def attn_bwd_reordered(q, k, v, log_lambda, orders, dy, mask_kind, phi=PHI_DEFAULT, workspace=None, stream=None):
+    """Gradients through attn_fwd_reordered given ``dy`` ([B, H, L, d]
+    float32): ``(dq, dk, dv, dlog_lambda)`` shaped as attn_bwd's."""
+    lib = load()
+    if isinstance(mask_kind, str):
+        mask_kind = MASKS[mask_kind]
+    B, H, L, d = q.shape
+    if orders.dtype != torch.int32 or tuple(orders.shape) != (2, L):
+        raise ValueError("orders must be int32 of shape [2, L]")
+    if dy.dtype != torch.float32 or dy.shape != q.shape:
+        raise ValueError("dy must be float32 with the shape of q")
+    for t in (q, k, v, dy, orders) + ((log_lambda,) if log_lambda is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    dq = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    dll = None
+    if mask_kind == MASK_D:
+        dll = torch.empty((H,), dtype=torch.float32, device=q.device)
+    elif mask_kind == MASK_S:
+        dll = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    a = _ReorderBwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(orders), _ptr(dy), _ptr(dq), _ptr(dk),
+                        _ptr(dv), _ptr(dll), B, H, L, d, mask_kind, _dtype_code(q), phi, _ptr(workspace),
+                        0 if workspace is None else workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream))
+    _check(lib.lion_attn_bwd_reordered(ctypes.byref(a)))
+    return dq, dk, dv, dll
 

@@ -324,6 +324,44 @@ lion_status lion_attn_fwd_reordered(const lion_reorder_args* a);
 /* Workspace bytes lion_attn_fwd_reordered needs (0 if d is not 64 or 128). */
 size_t lion_attn_reordered_workspace_bytes(int B, int H, int L, int d);
 
+/*
+ * lion_attn_bwd_reordered -- gradients of a scalar loss through
+ * lion_attn_fwd_reordered, given dy = dLoss/dy: the same products as
+ * lion_attn_bwd with the averaged mask, and for the decays the derivative
+ * of each order's mask (the product of the decays that order passes)
+ * taken along that order.
+ *   q, k, v, log_lambda, order, B, H, L, d, mask_kind, dtype, phi: as
+ *   lion_reorder_args; dy, dq, dk, dv, dlog_lambda: as lion_bwd_args.
+ *   A row of order that is not a permutation is reported as for the forward
+ *   (every access stays in bounds, the next lion_sync_status returns
+ *   LION_ERR_INVALID_ARG).  fp32 on the CUDA cores; d in {64, 128} (else
+ *   LION_ERR_UNSUPPORTED), L <= LION_FULL_MAX_L.  Workspace as returned by
+ *   lion_attn_reordered_bwd_workspace_bytes (NULL: stream-ordered allocation).
+ */
+typedef struct {
+  const void* q;             /* [B][H][L][d], dtype below                  */
+  const void* k;
+  const void* v;
+  const float* log_lambda;   /* as lion_args                               */
+  const int* order;          /* [2][L] device int32                        */
+  const float* dy;           /* [B][H][L][d] float32                       */
+  float* dq;                 /* [B][H][L][d] float32                       */
+  float* dk;
+  float* dv;
+  float* dlog_lambda;        /* as lion_bwd_args                           */
+  int B, H, L, d;
+  int mask_kind;             /* lion_mask_kind                             */
+  int dtype;                 /* lion_dtype of q, k, v                      */
+  int phi;                   /* lion_phi                                   */
+  void* workspace;           /* device, 256-byte aligned, or NULL          */
+  size_t workspace_bytes;
+  cudaStream_t stream;
+} lion_reorder_bwd_args;
+lion_status lion_attn_bwd_reordered(const lion_reorder_bwd_args* a);
+
+/* Workspace bytes lion_attn_bwd_reordered needs (0 if d is not 64 or 128). */
+size_t lion_attn_reordered_bwd_workspace_bytes(int B, int H, int L, int d);
+
 /* Static, human-readable text for a status. */
 const char* lion_status_string(lion_status s);
 

@@ -29,7 +29,8 @@ def test_header_declares_the_abi():
     names = _declared()
     for want in ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_rnn_step", "lion_status_string",
                  "lion_attn_workspace_bytes", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
-                 "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes"):
+                 "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes",
+                 "lion_attn_bwd_reordered", "lion_attn_reordered_bwd_workspace_bytes", "lion_attn_fwd_host"):
         assert want in names
 
 
@@ -76,6 +77,39 @@ def test_reordered_workspace_query(lib):
     assert need >= 2 * 3 * 10 * (2 * 64 + 2) * 4 + 2 * 10 * 4
     assert lion.reordered_workspace_bytes(0, 3, 10, 64) == 0
     assert lion.reordered_workspace_bytes(1, 1, 10, 32) == 0    # d = 64 and 128 only
+
+
+def test_reordered_bwd_workspace_query(lib):
+    from bidirectional_masked_linear_gb300 import lion
+    # phi(q), phi(k), dnum (L*d floats each); dden, the row shares (one float
+    # per head-token each), coordinates and the row and column terms (two
+    # each), two positions per token, a double per head
+    need = lion.reordered_bwd_workspace_bytes(2, 3, 10, 64)
+    assert need >= 2 * 3 * 10 * (3 * 64 + 8) * 4 + 2 * 10 * 4 + 2 * 3 * 8
+    assert lion.reordered_bwd_workspace_bytes(0, 3, 10, 64) == 0
+    assert lion.reordered_bwd_workspace_bytes(1, 1, 10, 16) == 0
+
+
+def _reorder_bwd(lib, **kw):
+    from bidirectional_masked_linear_gb300 import lion
+    f = dict(q=4096, k=8192, v=12288, log_lambda=0, order=16384, dy=20480, dq=24576, dk=28672, dv=32768,
+             dlog_lambda=0, B=1, H=1, L=8, d=64, mask_kind=0, dtype=0, phi=0, workspace=0, workspace_bytes=0,
+             stream=0)
+    f.update(kw)
+    a = lion._ReorderBwdArgs(**f)
+    lib.lion_attn_bwd_reordered.argtypes = [ctypes.POINTER(lion._ReorderBwdArgs)]
+    return lib.lion_attn_bwd_reordered(ctypes.byref(a))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(k=0), dict(v=0), dict(order=0), dict(dy=0), dict(dq=0), dict(dk=0), dict(dv=0),
+    dict(B=0), dict(H=0), dict(L=0), dict(d=48), dict(mask_kind=3), dict(dtype=2), dict(phi=4),
+    dict(mask_kind=1, log_lambda=36864, dlog_lambda=0), dict(mask_kind=2, log_lambda=0, dlog_lambda=36864),
+    dict(),   # pointers that are not device memory
+])
+def test_reordered_bwd_invalid_arguments_rejected_before_launch(lib, kw):
+    assert _reorder_bwd(lib, **kw) == 1
+    assert lib.lion_attn_bwd_reordered(None) == 1
 
 
 def _reorder(lib, **kw):

@@ -591,6 +591,64 @@ def test_reordered_invalid_orders_are_reported():
                                 lion.MASK_LIT)
 
 
+def _reorder_bwd_check(oracle_mod, inp, orders, seed, phi=0):
+    q64, k64, v64, ll64 = f64(inp)
+    dy = np.random.default_rng(seed).standard_normal(q64.shape).astype(np.float32)
+    ref = oracle_mod.full_bwd_reordered(q64, k64, v64, ll64, orders, dy.astype(np.float64), inp["mask"], phi)
+    g = _cuda(inp)
+    o = torch.from_numpy(np.ascontiguousarray(orders, dtype=np.int32)).cuda()
+    got = lion.attn_bwd_reordered(g["q"], g["k"], g["v"], g["log_lambda"], o, torch.from_numpy(dy).cuda(),
+                                  inp["mask"], phi)
+    assert lion.sync_status() == lion.OK
+    floor = 1e-2 * max(float(np.abs(r).max()) for r in ref if r is not None)
+    for name, r, x in zip(("dq", "dk", "dv", "dlog_lambda"), ref, got):
+        if r is None:
+            assert x is None
+            continue
+        x = x.cpu().numpy().astype(np.float64)
+        assert x.shape == r.shape, name
+        err = float(np.abs(x - r).max() / max(np.abs(r).max(), floor))
+        assert err <= TOL_BWD, (name, q64.shape, err)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+@pytest.mark.parametrize("dtype", ("bf16", "fp32"))
+def test_reordered_backward_matches_oracle(oracle_mod, mask, dtype):
+    """Gradients through the reordered full form against the oracle's (pinned
+    by finite differences), for ViT-grid and random orders."""
+    rng = np.random.default_rng(1600)
+    inp = synth.make_inputs(2, 3, 197, 64, mask, dtype, seed=1601)
+    _reorder_bwd_check(oracle_mod, inp, _vit_grid_orders(), 1602)
+    for n, (B, H, L, d) in enumerate(((1, 2, 150, 64), (1, 1, 130, 128), (2, 1, 7, 64))):
+        inp = synth.make_inputs(B, H, L, d, mask, dtype, seed=1610 + 10 * n)
+        _reorder_bwd_check(oracle_mod, inp, np.stack([rng.permutation(L), rng.permutation(L)]), 1611 + 10 * n)
+    # L = 1: y = v, so dv = dy and dq = dk = 0 up to the fp32 rounding of v - y
+    inp = synth.make_inputs(3, 2, 1, 64, mask, dtype, seed=1640)
+    g = _cuda(inp)
+    dy = torch.randn(3, 2, 1, 64, device="cuda")
+    o = torch.zeros((2, 1), dtype=torch.int32, device="cuda")
+    dq, dk, dv, dll = lion.attn_bwd_reordered(g["q"], g["k"], g["v"], g["log_lambda"], o, dy, inp["mask"])
+    scale = float(dy.abs().max())
+    assert float((dv - dy).abs().max()) <= 1e-5 * scale
+    assert float(dq.abs().max()) <= 1e-3 * scale and float(dk.abs().max()) <= 1e-3 * scale
+    if dll is not None:
+        assert float(dll.abs().max()) == 0.0
+
+
+@pytest.mark.gpu
+def test_reordered_backward_feature_map_and_invalid_orders(oracle_mod):
+    rng = np.random.default_rng(1650)
+    inp = synth.make_inputs(2, 2, 120, 64, "s", "bf16", seed=1651)
+    _reorder_bwd_check(oracle_mod, inp, np.stack([rng.permutation(120), rng.permutation(120)]), 1652, phi=1)
+    g = _cuda(inp)
+    bad = torch.from_numpy(np.stack([np.arange(120), np.r_[np.arange(119), 7]]).astype(np.int32)).cuda()
+    lion.attn_bwd_reordered(g["q"], g["k"], g["v"], g["log_lambda"], bad, torch.zeros((2, 2, 120, 64), device="cuda"),
+                            lion.MASK_S)
+    assert lion.sync_status() == lion.ERR_INVALID_ARG
+    assert lion.sync_status() == lion.OK
+
+
 # ------------------------------------------------- host-buffer entry -----
 # lion_attn_fwd_host runs the same kernels on slices of the batch copied in
 # and out by the library: its output equals the device entry point's bit for
