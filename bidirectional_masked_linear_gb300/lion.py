@@ -421,3 +421,24 @@ def attn_bwd_reordered(q, k, v, log_lambda, orders, dy, mask_kind, phi=PHI_DEFAU
     _check(lib.lion_attn_bwd_reordered(ctypes.byref(a)))
     return dq, dk, dv, dll
 
+
+class LionReorderedAttention(torch.autograd.Function):
+    """The full form with the mask averaged over two traversal orders as a
+    differentiable op: forward by attn_fwd_reordered, backward by
+    attn_bwd_reordered.  ``orders`` ([2, L] int32, on the GPU) gets no
+    gradient."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, log_lambda, orders, mask_kind, phi=PHI_DEFAULT):
+        ctx.save_for_backward(q, k, v, log_lambda, orders)
+        ctx.mask_kind, ctx.phi = mask_kind, phi
+        return attn_fwd_reordered(q, k, v, log_lambda, orders, mask_kind, phi=phi)
+
+    @staticmethod
+    def backward(ctx, dy):
+        q, k, v, log_lambda, orders = ctx.saved_tensors
+        dq, dk, dv, dll = attn_bwd_reordered(q, k, v, log_lambda, orders, dy.contiguous().float(), ctx.mask_kind,
+                                             ctx.phi)
+        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), None if log_lambda is None else dll, None, None,
+                None)
+

@@ -649,6 +649,23 @@ def test_reordered_backward_feature_map_and_invalid_orders(oracle_mod):
     assert lion.sync_status() == lion.OK
 
 
+@pytest.mark.gpu
+def test_reordered_autograd_function_uses_the_reordered_backward():
+    inp = synth.make_inputs(2, 3, 197, 64, "s", "bf16", seed=1660)
+    g = _cuda(inp)
+    o = torch.from_numpy(_vit_grid_orders()).cuda()
+    q = g["q"].clone().requires_grad_(True)
+    k = g["k"].clone().requires_grad_(True)
+    v = g["v"].clone().requires_grad_(True)
+    ll = g["log_lambda"].clone().requires_grad_(True)
+    y = lion.LionReorderedAttention.apply(q, k, v, ll, o, lion.MASK_S)
+    dy = torch.randn_like(y)
+    y.backward(dy)
+    dq, dk, dv, dll = lion.attn_bwd_reordered(g["q"], g["k"], g["v"], g["log_lambda"], o, dy, lion.MASK_S)
+    assert torch.equal(q.grad, dq.to(q.dtype)) and torch.equal(k.grad, dk.to(k.dtype))
+    assert torch.equal(v.grad, dv.to(v.dtype)) and torch.equal(ll.grad, dll)
+
+
 # ------------------------------------------------- host-buffer entry -----
 # lion_attn_fwd_host runs the same kernels on slices of the batch copied in
 # and out by the library: its output equals the device entry point's bit for
