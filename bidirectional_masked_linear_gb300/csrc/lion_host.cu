@@ -101,50 +101,50 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
   float* ll_fixed = reinterpret_cast<float*>(base + 2 * set_bytes);
   void* ws = base + 2 * set_bytes + align256(fixed ? sizeof(float) * H : 0);
 
-  cudaStream_t cin = nullptr, cout = nullptr;
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
   cudaEvent_t start = nullptr, in[2] = {nullptr, nullptr}, comp[2] = {nullptr, nullptr},
               freed[2] = {nullptr, nullptr};
   lion_status result = LION_OK;
   auto fail = [&](cudaError_t err) {
     if (result == LION_OK) result = err == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
   };
-  if ((e = cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking)) != cudaSuccess ||
-      (e = cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking)) != cudaSuccess)
+  if ((e = cudaStreamCreateWithFlags(&copy_in, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&copy_out, cudaStreamNonBlocking)) != cudaSuccess)
     fail(e);
   cudaEvent_t* evs[] = {&start, &in[0], &in[1], &comp[0], &comp[1], &freed[0], &freed[1]};
   for (cudaEvent_t* ev : evs)
     if (result == LION_OK && (e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) fail(e);
   if (result == LION_OK) {
     // the copies start after the caller's earlier work on its stream
-    if ((e = cudaEventRecord(start, s)) != cudaSuccess || (e = cudaStreamWaitEvent(cin, start, 0)) != cudaSuccess)
+    if ((e = cudaEventRecord(start, s)) != cudaSuccess || (e = cudaStreamWaitEvent(copy_in, start, 0)) != cudaSuccess)
       fail(e);
     if (result == LION_OK && fixed)
-      if ((e = cudaMemcpyAsync(ll_fixed, a->log_lambda, sizeof(float) * H, cudaMemcpyHostToDevice, cin)) !=
+      if ((e = cudaMemcpyAsync(ll_fixed, a->log_lambda, sizeof(float) * H, cudaMemcpyHostToDevice, copy_in)) !=
           cudaSuccess)
         fail(e);
   }
   for (int sl = 0; sl < nslices && result == LION_OK; ++sl) {
     const int b0 = sl * Bs, nb = B - b0 < Bs ? B - b0 : Bs, i = sl & 1;
     // copy in, once the slice two back has left this buffer set
-    if (sl >= 2 && (e = cudaStreamWaitEvent(cin, freed[i], 0)) != cudaSuccess) {
+    if (sl >= 2 && (e = cudaStreamWaitEvent(copy_in, freed[i], 0)) != cudaSuccess) {
       fail(e);
       break;
     }
     const uint8_t* hq = static_cast<const uint8_t*>(a->q) + (size_t)b0 * in_bytes;
     const uint8_t* hk = static_cast<const uint8_t*>(a->k) + (size_t)b0 * in_bytes;
     const uint8_t* hv = static_cast<const uint8_t*>(a->v) + (size_t)b0 * in_bytes;
-    if ((e = cudaMemcpyAsync(set[i].q, hq, in_bytes * nb, cudaMemcpyHostToDevice, cin)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(set[i].k, hk, in_bytes * nb, cudaMemcpyHostToDevice, cin)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(set[i].v, hv, in_bytes * nb, cudaMemcpyHostToDevice, cin)) != cudaSuccess) {
+    if ((e = cudaMemcpyAsync(set[i].q, hq, in_bytes * nb, cudaMemcpyHostToDevice, copy_in)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(set[i].k, hk, in_bytes * nb, cudaMemcpyHostToDevice, copy_in)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(set[i].v, hv, in_bytes * nb, cudaMemcpyHostToDevice, copy_in)) != cudaSuccess) {
       fail(e);
       break;
     }
     if (sel && (e = cudaMemcpyAsync(set[i].ll, a->log_lambda + (size_t)b0 * head_tokens, ll_bytes * nb,
-                                    cudaMemcpyHostToDevice, cin)) != cudaSuccess) {
+                                    cudaMemcpyHostToDevice, copy_in)) != cudaSuccess) {
       fail(e);
       break;
     }
-    if ((e = cudaEventRecord(in[i], cin)) != cudaSuccess || (e = cudaStreamWaitEvent(s, in[i], 0)) != cudaSuccess) {
+    if ((e = cudaEventRecord(in[i], copy_in)) != cudaSuccess || (e = cudaStreamWaitEvent(s, in[i], 0)) != cudaSuccess) {
       fail(e);
       break;
     }
@@ -174,28 +174,28 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
       break;
     }
     // copy out
-    if ((e = cudaEventRecord(comp[i], s)) != cudaSuccess || (e = cudaStreamWaitEvent(cout, comp[i], 0)) != cudaSuccess ||
+    if ((e = cudaEventRecord(comp[i], s)) != cudaSuccess || (e = cudaStreamWaitEvent(copy_out, comp[i], 0)) != cudaSuccess ||
         (e = cudaMemcpyAsync(a->out + (size_t)b0 * head_tokens * d, set[i].out, out_bytes * nb,
-                             cudaMemcpyDeviceToHost, cout)) != cudaSuccess ||
-        (e = cudaEventRecord(freed[i], cout)) != cudaSuccess) {
+                             cudaMemcpyDeviceToHost, copy_out)) != cudaSuccess ||
+        (e = cudaEventRecord(freed[i], copy_out)) != cudaSuccess) {
       fail(e);
       break;
     }
   }
   // the caller's stream resumes after the last copies; the buffers are freed
   // in its order after them
-  if (cin && cout && start) {
+  if (copy_in && copy_out && start) {
     cudaEvent_t done_in = nullptr, done_out = nullptr;
     if (cudaEventCreateWithFlags(&done_in, cudaEventDisableTiming) == cudaSuccess &&
         cudaEventCreateWithFlags(&done_out, cudaEventDisableTiming) == cudaSuccess) {
-      cudaEventRecord(done_in, cin);
-      cudaEventRecord(done_out, cout);
+      cudaEventRecord(done_in, copy_in);
+      cudaEventRecord(done_out, copy_out);
       cudaStreamWaitEvent(s, done_in, 0);
       cudaStreamWaitEvent(s, done_out, 0);
     } else {
       cudaGetLastError();
-      cudaStreamSynchronize(cin);
-      cudaStreamSynchronize(cout);
+      cudaStreamSynchronize(copy_in);
+      cudaStreamSynchronize(copy_out);
       fail(cudaErrorUnknown);
     }
     if (done_in) cudaEventDestroy(done_in);
@@ -204,8 +204,8 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
   cudaFreeAsync(base, s);
   for (cudaEvent_t* ev : evs)
     if (*ev) cudaEventDestroy(*ev);
-  if (cin) cudaStreamDestroy(cin);
-  if (cout) cudaStreamDestroy(cout);
+  if (copy_in) cudaStreamDestroy(copy_in);
+  if (copy_out) cudaStreamDestroy(copy_out);
   if (result == LION_OK && cudaGetLastError() != cudaSuccess) result = LION_ERR_CUDA;
   return result;
 }
