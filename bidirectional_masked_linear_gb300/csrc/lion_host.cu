@@ -5,10 +5,11 @@
 // overlap the compute and each other (the link carries the inputs in and the
 // output out at the same time).  Every copy is one cudaMemcpyAsync of a
 // contiguous slice.  Four slices is the default: at ViT-B (64 x 12 x 197,
-// d = 64) on one GB300 a call took 0.556 / 0.473 / 0.471 / 0.497 / 0.619 ms
-// with 1 / 2 / 4 / 8 / 16 slices, against 0.322 ms for the copies in and out
-// alone when run at the same time.  Finer slices lose because the kernel's
-// time per slice hardly shrinks with the heads in it.
+// d = 64) on one GB300 a call took 0.470 / 0.455 / 0.445 / 0.455 / 0.483 ms
+// with 2 / 3 / 4 / 5 / 8 slices (the first and last at half size), against
+// 0.322 ms for the copies in and out alone when run at the same time.  Equal
+// slices gave 0.473 ms at 4.  Finer slices lose because the kernel's time per
+// slice hardly shrinks with the heads in it.
 #include <stdint.h>
 #include <string.h>
 
@@ -32,6 +33,28 @@ bool host_memory(const void* p) {
     return false;
   }
   return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
+// Batch rows [bounds[s], bounds[s + 1]) of slice s: with S >= 3 (and enough
+// rows) the first and last slices weigh 1/2 and the others 1; returns the
+// number of slices.
+constexpr int kMaxSlices = 64;
+int slice_bounds(int B, int S, int* bounds) {
+  if (S < 1) S = 1;
+  if (S > B) S = B;
+  const bool taper = S >= 3 && B >= 2 * S;
+  const double total = taper ? S - 1.0 : (double)S;
+  double acc = 0.0;
+  bounds[0] = 0;
+  for (int s = 0; s < S; ++s) {
+    acc += taper && (s == 0 || s == S - 1) ? 0.5 : 1.0;
+    int b = (int)(acc / total * B + 0.5);
+    if (b <= bounds[s]) b = bounds[s] + 1;          // every slice holds a row
+    if (b > B - (S - 1 - s)) b = B - (S - 1 - s);   // and leaves one for each slice after it
+    bounds[s + 1] = b;
+  }
+  bounds[S] = B;
+  return S;
 }
 
 lion_status validate_host(const lion_host_args* a) {
@@ -61,9 +84,14 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
   lion_status st = validate_host(a);
   if (st != LION_OK) return st;
   const int B = a->B, H = a->H, L = a->L, d = a->d;
+  // Slice sizes: the first slice's copy in and the last slice's copy out
+  // overlap nothing, so with three or more slices those two get half the
+  // batch rows of the others.
   const int S = a->slices > 0 ? (a->slices < B ? a->slices : B) : (B < 4 ? B : 4);
-  const int Bs = (B + S - 1) / S;
-  const int nslices = (B + Bs - 1) / Bs;
+  int bounds[kMaxSlices + 1];
+  const int nslices = slice_bounds(B, S < kMaxSlices ? S : kMaxSlices, bounds);
+  int Bs = 0;
+  for (int sl = 0; sl < nslices; ++sl) Bs = bounds[sl + 1] - bounds[sl] > Bs ? bounds[sl + 1] - bounds[sl] : Bs;
   const size_t esz = a->dtype == LION_DTYPE_BF16 ? 2 : 4;
   const size_t head_tokens = (size_t)H * L;                 // per batch row
   const size_t in_bytes = head_tokens * d * esz;            // q, k or v of one batch row
@@ -124,7 +152,7 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
         fail(e);
   }
   for (int sl = 0; sl < nslices && result == LION_OK; ++sl) {
-    const int b0 = sl * Bs, nb = B - b0 < Bs ? B - b0 : Bs, i = sl & 1;
+    const int b0 = bounds[sl], nb = bounds[sl + 1] - bounds[sl], i = sl & 1;
     // copy in, once the slice two back has left this buffer set
     if (sl >= 2 && (e = cudaStreamWaitEvent(copy_in, freed[i], 0)) != cudaSuccess) {
       fail(e);
