@@ -68,6 +68,10 @@ struct ReorderParams {
   float* K;           // [2][BH][L] column terms per order (LION-S)
   float* dterm;       // [BH][L]    LION-D: each row's share of dLoss/dlog(lambda)
   double* dsum;       // [BH]       LION-D: per head
+  // stored-tile build (L <= kRbwdStoreMaxL): s_ij and dA_ij, [BH][L (i)][LP (j)]
+  float* St;
+  float* Dt;
+  int LP;
 };
 
 __device__ __forceinline__ int clamp_token(int a, int L) { return a < 0 ? 0 : a >= L ? L - 1 : a; }
@@ -225,7 +229,7 @@ constexpr size_t rbwd_cols_smem() {
 
 // Rows: 32 queries per CTA.  Pass A: den, num; then y, dnum, dden; pass B:
 // dphi(q) and the decay terms of each row.
-template <typename T, int D>
+template <typename T, int D, bool STORE>
 __global__ void __launch_bounds__(kTThreads) rbwd_rows_kernel(ReorderParams p) {
   constexpr int LD = D + 4, MF = D / 16, U = D / 64;
   extern __shared__ __align__(16) float smem[];
@@ -247,6 +251,8 @@ __global__ void __launch_bounds__(kTThreads) rbwd_rows_kernel(ReorderParams p) {
   const int* P1 = p.pos + L;
   const float* fkh = p.fk + (size_t)bh * L * D;
   const T* vh = head_of<T>(p.v, bh, L, D);
+  float* St = STORE ? p.St + (size_t)bh * L * p.LP : nullptr;
+  float* Dt = STORE ? p.Dt + (size_t)bh * L * p.LP : nullptr;
   stage_rows<D>(sQ, p.fq + (size_t)bh * L * D, i0, kTR, L);
   int ia[4];
   bool live[4];
@@ -296,6 +302,7 @@ __global__ void __launch_bounds__(kTThreads) rbwd_rows_kernel(ReorderParams p) {
         const float x = m * s[a][b];
         den[a] += x;
         sA[(ty + 8 * a) * kTAL + jl] = x;
+        if (STORE && live[a] && j < L) St[(size_t)ia[a] * p.LP + j] = s[a][b];
       }
     __syncthreads();
     tile_apply<D>(sA, sV, (nc + 3) & ~3, ty, tx, nr, num);
@@ -339,11 +346,20 @@ __global__ void __launch_bounds__(kTThreads) rbwd_rows_kernel(ReorderParams p) {
     for (int f = 0; f < MF; ++f) dfq[a][f] = 0.f;
   }
   for (int j0 = 0; j0 < L; j0 += kTC) {
+    float s[4][4], gv[4][4];
+    if (STORE) {   // s_ij as this thread wrote it in pass A
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int j = j0 + tx + 16 * b;
+          s[a][b] = live[a] && j < L ? St[(size_t)ia[a] * p.LP + j] : 0.f;
+        }
+    }
     stage_tile(j0);
     __syncthreads();
     const int nc = min(kTC, L - j0);
-    float s[4][4], gv[4][4];
-    tile_scores<D>(sQ, sK, ty, tx, nr, nc, s);
+    if (!STORE) tile_scores<D>(sQ, sK, ty, tx, nr, nc, s);
     tile_scores<D>(sG, sV, ty, tx, nr, nc, gv);
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -359,6 +375,7 @@ __global__ void __launch_bounds__(kTThreads) rbwd_rows_kernel(ReorderParams p) {
         const float m = !ok ? 0.f : lit ? 1.f : 0.5f * (m0 + m1);
         const float da = gv[a][b] + hi[a], e = s[a][b] * da;
         sA[(ty + 8 * a) * kTAL + jl] = m * da;
+        if (STORE && ok) Dt[(size_t)ia[a] * p.LP + j] = da;
         if (ms) {
           r0[a] += sgnf(sPs[jl] - q0[a]) * m0 * e;
           r1[a] += sgnf(sPs[kTC + jl] - q1[a]) * m1 * e;
@@ -517,6 +534,135 @@ __global__ void __launch_bounds__(kTThreads) rbwd_cols_kernel(ReorderParams p) {
   }
 }
 
+template <int D>
+constexpr size_t rbwd_cols_stored_smem() {
+  return sizeof(float) * ((size_t)2 * kTC * (D + 4) + 2 * kTC * kTSL + 4 * kTC + 2 * 4 * kTR);
+}
+
+// Columns from the stored s_ij and dA_ij: 32 keys per CTA.  Each tile is
+// first turned into A = M (.) s and M (.) dA in place (thread: one key, 16 of
+// the tile's queries, which also sums the key's column terms), then the two
+// products run with each thread holding keys 4ty + a (tile_apply_t).
+template <typename T, int D>
+__global__ void __launch_bounds__(kTThreads) rbwd_cols_stored_kernel(ReorderParams p) {
+  constexpr int LD = D + 4, MF = D / 16, U = D / 64, J4 = kTR / 4;
+  extern __shared__ __align__(16) float smem[];
+  float* sQ = smem;                  // [kTC][LD]   phi(q) of the tile
+  float* sG = sQ + kTC * LD;         // [kTC][LD]   dnum of the tile
+  float* sS = sG + kTC * LD;         // [kTC][kTSL] s, then A, over the tile's queries x the block's keys
+  float* sE = sS + kTC * kTSL;       // [kTC][kTSL] dA, then M (.) dA
+  float* sC = sE + kTC * kTSL;       // [2][kTC]    coordinates of the tile's queries
+  float* sPs = sC + 2 * kTC;         // [2][kTC]    their positions
+  float* sKp = sPs + 2 * kTC;        // [2][4][kTR] column terms per query group
+  const int L = p.L, LP = p.LP, BH = gridDim.x, bh = blockIdx.x, h = bh % p.H, j0b = blockIdx.y * kTR;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int kj = threadIdx.x & 31, grp = threadIdx.x >> 5;   // conversion role: key, query group
+  const bool lit = p.mask_kind == MASK_LIT, ms = p.mask_kind == MASK_S;
+  const float w = p.mask_kind == MASK_D ? -p.log_lambda[h] : 1.f;
+  const float* C0 = ms ? p.coord + (size_t)bh * L : p.coord;
+  const float* C1 = ms ? p.coord + ((size_t)BH + bh) * L : p.coord + L;
+  const int* P0 = p.pos;
+  const int* P1 = p.pos + L;
+  const float* fqh = p.fq + (size_t)bh * L * D;
+  const float* gh = p.g + (size_t)bh * L * D;
+  const float* St = p.St + (size_t)bh * L * LP;
+  const float* Dt = p.Dt + (size_t)bh * L * LP;
+  const int jk = j0b + kj;
+  const bool klive = jk < L;
+  const float kc0 = !lit && klive ? C0[jk] : 0.f, kc1 = !lit && klive ? C1[jk] : 0.f;
+  const float kp0 = !lit && klive ? (float)P0[jk] : 0.f, kp1 = !lit && klive ? (float)P1[jk] : 0.f;
+  float k0 = 0.f, k1 = 0.f;
+  float dfk[4][MF], dvj[4][MF];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int f = 0; f < MF; ++f) dfk[a][f] = dvj[a][f] = 0.f;
+  for (int i0 = 0; i0 < L; i0 += kTC) {
+    stage_rows<D>(sQ, fqh, i0, kTC, L);
+    stage_rows<D>(sG, gh, i0, kTC, L);
+    if (!lit) {
+      stage_vec(sC, C0, i0, kTC, L);
+      stage_vec(sC + kTC, C1, i0, kTC, L);
+      stage_pos(sPs, P0, i0, kTC, L);
+      stage_pos(sPs + kTC, P1, i0, kTC, L);
+    }
+    for (int idx = threadIdx.x; idx < kTC * J4; idx += kTThreads) {
+      const int r = idx / J4, c = (idx - r * J4) * 4, i = i0 + r, j = j0b + c;
+      float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = a4;
+      if (i < L && j < L) {
+        a4 = load4(St + (size_t)i * LP + j);
+        d4 = load4(Dt + (size_t)i * LP + j);
+        if (j + 1 >= L) a4.y = d4.y = 0.f;
+        if (j + 2 >= L) a4.z = d4.z = 0.f;
+        if (j + 3 >= L) a4.w = d4.w = 0.f;
+      }
+      *reinterpret_cast<float4*>(sS + r * kTSL + c) = a4;
+      *reinterpret_cast<float4*>(sE + r * kTSL + c) = d4;
+    }
+    __syncthreads();
+    const int nc = min(kTC, L - i0);
+#pragma unroll 4
+    for (int t = 0; t < 16; ++t) {
+      const int tq = 16 * grp + t;
+      const bool ok = klive && tq < nc;
+      const float sv = sS[tq * kTSL + kj], dav = sE[tq * kTSL + kj];
+      float m0 = 0.f, m1 = 0.f;
+      if (ok && !lit) {
+        m0 = expf(-fabsf(sC[tq] - kc0) * w);
+        m1 = expf(-fabsf(sC[kTC + tq] - kc1) * w);
+      }
+      const float m = !ok ? 0.f : lit ? 1.f : 0.5f * (m0 + m1);
+      sS[tq * kTSL + kj] = m * sv;
+      sE[tq * kTSL + kj] = m * dav;
+      if (ms && ok) {
+        const float e = sv * dav;
+        k0 += sgnf(sPs[tq] - kp0) * m0 * e;
+        k1 += sgnf(sPs[kTC + tq] - kp1) * m1 * e;
+      }
+    }
+    __syncthreads();
+    const int n4 = (nc + 3) & ~3;
+    tile_apply_t<D>(sE, kTSL, sQ, n4, ty, tx, dfk);
+    tile_apply_t<D>(sS, kTSL, sG, n4, ty, tx, dvj);
+    __syncthreads();
+  }
+  if (ms) {   // the key's column terms over the four query groups, in a fixed order
+    sKp[grp * kTR + kj] = k0;
+    sKp[(4 + grp) * kTR + kj] = k1;
+    __syncthreads();
+    if (grp == 0 && klive) {
+      p.K[(size_t)bh * L + jk] = sKp[kj] + sKp[kTR + kj] + sKp[2 * kTR + kj] + sKp[3 * kTR + kj];
+      p.K[((size_t)BH + bh) * L + jk] =
+          sKp[4 * kTR + kj] + sKp[5 * kTR + kj] + sKp[6 * kTR + kj] + sKp[7 * kTR + kj];
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int ja = j0b + 4 * ty + a;
+    const bool live = ja < L;
+    const T* kr = head_of<T>(p.k, bh, L, D) + (size_t)(live ? ja : L - 1) * D;
+    float x[MF], dx[MF];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float4 x4 = load4(kr + 4 * tx + 64 * u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[4 * u + e] = elem(x4, e);
+    }
+    phi_backward<MF, 16>(p.phi, x, dfk[a], dx);
+    if (live) {
+      float* dk = p.dk + ((size_t)bh * L + ja) * D;
+      float* dv = p.dv + ((size_t)bh * L + ja) * D;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        *reinterpret_cast<float4*>(dk + 4 * tx + 64 * u) =
+            make_float4(dx[4 * u], dx[4 * u + 1], dx[4 * u + 2], dx[4 * u + 3]);
+        *reinterpret_cast<float4*>(dv + 4 * tx + 64 * u) =
+            make_float4(dvj[a][4 * u], dvj[a][4 * u + 1], dvj[a][4 * u + 2], dvj[a][4 * u + 3]);
+      }
+    }
+  }
+}
+
 // LION-S, one CTA per head: dlog(lambda_u) = sum over the orders of the
 // suffix sum, from u's position, of -(1/2)(R + K) taken in that order.
 __global__ void __launch_bounds__(kScanThreads) rbwd_dl_kernel(ReorderParams p, int BH) {
@@ -595,13 +741,23 @@ cudaError_t rbwd_launch(const ReorderParams& p, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if ((e = launch_phi_rows<T, D>(p.q, p.k, p.fq, p.fk, BH * p.L, p.phi, s)) != cudaSuccess) return e;
-  constexpr size_t smem_r = rbwd_rows_smem<D>(), smem_c = rbwd_cols_smem<D>();
-  if ((e = allow_smem(rbwd_rows_kernel<T, D>, smem_r)) != cudaSuccess) return e;
-  if ((e = allow_smem(rbwd_cols_kernel<T, D>, smem_c)) != cudaSuccess) return e;
   const dim3 grid((unsigned)BH, (p.L + kTR - 1) / kTR);
-  rbwd_rows_kernel<T, D><<<grid, kTThreads, smem_r, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  rbwd_cols_kernel<T, D><<<grid, kTThreads, smem_c, s>>>(p);
+  constexpr size_t smem_r = rbwd_rows_smem<D>();
+  if (p.St) {
+    constexpr size_t smem_c = rbwd_cols_stored_smem<D>();
+    if ((e = allow_smem(rbwd_rows_kernel<T, D, true>, smem_r)) != cudaSuccess) return e;
+    if ((e = allow_smem(rbwd_cols_stored_kernel<T, D>, smem_c)) != cudaSuccess) return e;
+    rbwd_rows_kernel<T, D, true><<<grid, kTThreads, smem_r, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    rbwd_cols_stored_kernel<T, D><<<grid, kTThreads, smem_c, s>>>(p);
+  } else {
+    constexpr size_t smem_c = rbwd_cols_smem<D>();
+    if ((e = allow_smem(rbwd_rows_kernel<T, D, false>, smem_r)) != cudaSuccess) return e;
+    if ((e = allow_smem(rbwd_cols_kernel<T, D>, smem_c)) != cudaSuccess) return e;
+    rbwd_rows_kernel<T, D, false><<<grid, kTThreads, smem_r, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    rbwd_cols_kernel<T, D><<<grid, kTThreads, smem_c, s>>>(p);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.mask_kind == MASK_S) {
     rbwd_dl_kernel<<<(unsigned)BH, kScanThreads, 0, s>>>(p, (int)BH);
@@ -658,10 +814,15 @@ cudaError_t launch_reordered(const Problem& pr, const int* order, void* ws, int*
   return cudaErrorInvalidValue;
 }
 
+// Sequences up to this length keep s and dA in the workspace (8 L^2 bytes a
+// head) instead of recomputing the scores in the columns pass.
+constexpr int kRbwdStoreMaxL = 1024;
+
 size_t reorder_bwd_workspace_bytes(int B, int H, int L, int d) {
-  const size_t BH = (size_t)B * H, n = BH * L;
+  const size_t BH = (size_t)B * H, n = BH * L, LP = ((size_t)L + 3) & ~(size_t)3;
   return 3 * align256(sizeof(float) * n * d) + align256(sizeof(float) * n) + align256(sizeof(int) * 2 * (size_t)L) +
-         3 * align256(sizeof(float) * 2 * n) + align256(sizeof(float) * n) + align256(sizeof(double) * BH);
+         3 * align256(sizeof(float) * 2 * n) + align256(sizeof(float) * n) + align256(sizeof(double) * BH) +
+         (L <= kRbwdStoreMaxL ? 2 * align256(sizeof(float) * BH * L * LP) : 0);
 }
 
 int reorder_bwd_launches(int mask_kind) { return mask_kind == MASK_S ? 6 : mask_kind == MASK_D ? 6 : 4; }
@@ -707,6 +868,14 @@ cudaError_t launch_reordered_bwd(const Problem& pr, const int* order, const floa
   p.dterm = reinterpret_cast<float*>(w);
   w += align256(sizeof(float) * n);
   p.dsum = reinterpret_cast<double*>(w);
+  w += align256(sizeof(double) * BH);
+  p.LP = (pr.L + 3) & ~3;
+  p.St = p.Dt = nullptr;
+  if (pr.L <= kRbwdStoreMaxL) {
+    p.St = reinterpret_cast<float*>(w);
+    w += align256(sizeof(float) * BH * pr.L * p.LP);
+    p.Dt = reinterpret_cast<float*>(w);
+  }
   const bool bf = pr.dtype == DT_BF16;
   switch (pr.d) {
     case 64: return bf ? rbwd_launch<__nv_bfloat16, 64>(p, s) : rbwd_launch<float, 64>(p, s);

@@ -637,6 +637,15 @@ def test_reordered_backward_matches_oracle(oracle_mod, mask, dtype):
 
 
 @pytest.mark.gpu
+def test_reordered_backward_long_sequence(oracle_mod):
+    """L = 1100: above the stored-tile limit, the columns pass recomputes the
+    scores."""
+    rng = np.random.default_rng(1670)
+    inp = synth.make_inputs(1, 1, 1100, 64, "s", "bf16", seed=1671)
+    _reorder_bwd_check(oracle_mod, inp, np.stack([rng.permutation(1100), rng.permutation(1100)]), 1672)
+
+
+@pytest.mark.gpu
 def test_reordered_backward_feature_map_and_invalid_orders(oracle_mod):
     rng = np.random.default_rng(1650)
     inp = synth.make_inputs(2, 2, 120, 64, "s", "bf16", seed=1651)
