@@ -34,6 +34,8 @@
 // dlog(lambda_u) is the suffix sum of these along each order from u's
 // position, over both orders.  LION-D: dLoss/dlog(lambda_h) =
 // sum_ij e_ij (1/2) sum_p |pos_p(i) - pos_p(j)| M^p_ij, over the batch too.
+// Up to kRbwdStoreMaxL tokens the rows pass keeps s_ij and dA_ij and the
+// columns pass reads them; longer sequences recompute the scores there.
 #include <string.h>
 
 #include "lion_common.cuh"
@@ -785,6 +787,7 @@ int reorder_launches(int mask_kind) { return mask_kind == MASK_S ? 4 : 3; }
 
 cudaError_t launch_reordered(const Problem& pr, const int* order, void* ws, int* status, cudaStream_t s) {
   ReorderParams p;
+  memset(&p, 0, sizeof(p));
   p.q = pr.q;
   p.k = pr.k;
   p.v = pr.v;
