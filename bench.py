@@ -528,7 +528,10 @@ def main():
 
     torch.cuda.set_device(local)
     from bidirectional_masked_linear_gb300 import build
-    lion.load(build.build())
+    if rank == 0:   # one process compiles (if anything is stale); the others wait, then load it
+        build.build()
+    _barrier(dist)
+    lion.load(build.LIB)
     hbm_peak, bf16_peak, peak_src = _peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
