@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include "../../include/lion.h"
+#include "host_plan.h"
 #include "lion_common.cuh"
 #include "lion_internal.h"
 
@@ -33,28 +34,6 @@ bool host_memory(const void* p) {
     return false;
   }
   return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
-}
-
-// Batch rows [bounds[s], bounds[s + 1]) of slice s: with S >= 3 (and enough
-// rows) the first and last slices weigh 1/2 and the others 1; returns the
-// number of slices.
-constexpr int kMaxSlices = 64;
-int slice_bounds(int B, int S, int* bounds) {
-  if (S < 1) S = 1;
-  if (S > B) S = B;
-  const bool taper = S >= 3 && B >= 2 * S;
-  const double total = taper ? S - 1.0 : (double)S;
-  double acc = 0.0;
-  bounds[0] = 0;
-  for (int s = 0; s < S; ++s) {
-    acc += taper && (s == 0 || s == S - 1) ? 0.5 : 1.0;
-    int b = (int)(acc / total * B + 0.5);
-    if (b <= bounds[s]) b = bounds[s] + 1;          // every slice holds a row
-    if (b > B - (S - 1 - s)) b = B - (S - 1 - s);   // and leaves one for each slice after it
-    bounds[s + 1] = b;
-  }
-  bounds[S] = B;
-  return S;
 }
 
 lion_status validate_host(const lion_host_args* a) {
@@ -88,8 +67,8 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
   // overlap nothing, so with three or more slices those two get half the
   // batch rows of the others.
   const int S = a->slices > 0 ? (a->slices < B ? a->slices : B) : (B < 4 ? B : 4);
-  int bounds[kMaxSlices + 1];
-  const int nslices = slice_bounds(B, S < kMaxSlices ? S : kMaxSlices, bounds);
+  int bounds[lion::kMaxSlices + 1];
+  const int nslices = lion::slice_bounds(B, S < lion::kMaxSlices ? S : lion::kMaxSlices, bounds);
   int Bs = 0;
   for (int sl = 0; sl < nslices; ++sl) Bs = bounds[sl + 1] - bounds[sl] > Bs ? bounds[sl + 1] - bounds[sl] : Bs;
   const size_t esz = a->dtype == LION_DTYPE_BF16 ? 2 : 4;

@@ -239,3 +239,31 @@ def test_product_path_has_no_cpu_fallback():
             lion.load("/nonexistent/liblion.so")
     finally:
         lion._lib = saved
+
+
+def test_host_entry_slice_plan(tmp_path):
+    """lion_attn_fwd_host's batch slicing (host_plan.h, compiled here with the
+    host compiler): slices cover the batch in order, none is empty, there
+    are min(S, B) of them, and with three or more slices the first and last
+    are about half the others."""
+    src = tmp_path / "plan.cpp"
+    src.write_text(
+        '#include <cstdio>\n#include "host_plan.h"\n'
+        "int main() { int b[lion::kMaxSlices + 1];\n"
+        "  for (int B = 1; B <= 300; ++B) for (int S = 1; S <= lion::kMaxSlices; ++S) {\n"
+        "    int n = lion::slice_bounds(B, S, b); printf(\"%d %d %d\", B, S, n);\n"
+        "    for (int s = 0; s <= n; ++s) printf(\" %d\", b[s]); printf(\"\\n\"); } }\n")
+    exe = tmp_path / "plan"
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I", os.path.join(ROOT, "bidirectional_masked_linear_gb300", "csrc"),
+                    str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    for line in filter(None, out):
+        B, S, n, *bounds = map(int, line.split())
+        assert n == min(S, B) and len(bounds) == n + 1
+        assert bounds[0] == 0 and bounds[-1] == B
+        sizes = [b - a for a, b in zip(bounds, bounds[1:])]
+        assert min(sizes) >= 1
+        if n >= 3 and B >= 2 * n:
+            middle = sizes[1:-1]
+            for edge in (sizes[0], sizes[-1]):
+                assert edge <= min(middle) + 1 and edge >= max(middle) / 2 - 1, (B, S, sizes)
