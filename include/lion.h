@@ -34,14 +34,18 @@
  *   - Tensors are row-major and contiguous.  q, k, v, out: [B][H][L][d].
  *   - log_lambda holds log(lambda) (finite, <= 0): LIT ignores it (NULL
  *     allowed); D: [H]; S: [B][H][L].  All float32.
- *   - out is float32.  Every pointer is device memory owned by the caller.
+ *   - out is float32 (bfloat16 when lion_args.out_bf16 asks for it).  Every
+ *     pointer is memory owned by the caller: device memory, except the
+ *     host buffers that lion_attn_fwd_host takes.
  *   - Calls are asynchronous on `stream`.  Argument errors are detected on
  *     the host before anything is launched and return a status; nothing is
  *     written then.  A launch or runtime failure returns LION_ERR_CUDA.
  *   - d must be 16, 32, 64 or 128.  q, k, v, out and workspace must be
  *     16-byte aligned.
  *   - The library keeps no state between calls except a per-device cache of
- *     device properties and of resolved driver entry points.
+ *     device properties and of resolved driver entry points, the device
+ *     status word that lion_sync_status reads and clears, and the fixed
+ *     scratch array of lion_attn_fwd_rnn_noalloc.
  */
 #ifndef LION_H_
 #define LION_H_

@@ -267,3 +267,26 @@ def test_host_entry_slice_plan(tmp_path):
             middle = sizes[1:-1]
             for edge in (sizes[0], sizes[-1]):
                 assert edge <= min(middle) + 1 and edge >= max(middle) / 2 - 1, (B, S, sizes)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/lion.h compiles as C11 (no C++ in the ABI) and its structs
+    have the field layout the Python binding declares."""
+    from bidirectional_masked_linear_gb300 import lion
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "lion.h"\n'
+        "int main(void) {\n"
+        '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(lion_args), sizeof(lion_bwd_args),\n'
+        "         sizeof(lion_reorder_args), sizeof(lion_reorder_bwd_args), sizeof(lion_host_args),\n"
+        "         offsetof(lion_args, out_bf16));\n"
+        "  return 0; }\n")
+    exe = tmp_path / "abi"
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(cuda, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    sizes = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()))
+    want = [ctypes.sizeof(lion._Args), ctypes.sizeof(lion._BwdArgs), ctypes.sizeof(lion._ReorderArgs),
+            ctypes.sizeof(lion._ReorderBwdArgs), ctypes.sizeof(lion._HostArgs), lion._Args.out_bf16.offset]
+    assert sizes == want
