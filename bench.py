@@ -52,9 +52,6 @@ _TC_SOURCES = {
     (128, True): (_CSRC + "lion_c128L.cu", _CSRC + "c128_common.cuh", _CSRC + "tc_ptx.cuh"),
 }
 TRAFFIC_PER_HEAD = {
-    # chunk-64 kernel, ViT-B shape at B=128, LION-S: 160.7 MB / 1536 heads
-    ("fc4be66a869d6463b1ad06b8b0948a689343c3e6648cdb380430aac91fcace8c", "vit_b", "s", 64):
-        (117664768 + 43027200) / 1536,
     # chunk-128 kernel, ViT-B shape at B=128, LION-S: 153.4 MB / 1536 heads
     ("1d94bfce7f698332337e9082c69accf2eb23926ea5fd5714a0ca66268b715025", "vit_b", "s", 128):
         (117490176 + 35867392) / 1536,
