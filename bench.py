@@ -5,9 +5,10 @@ One step = one call of the operator (feature map, log-decay prefix,
 intra-chunk attention, chunk states, scans, combine/normalise) over one batch
 of synthetic inputs already resident in HBM.  Default workload: ViT-B
 (B=64, H=12, L=197, d=64), LION-S, chunk 128 (two chunks per head).  The
-L=24,337 high-resolution workload is measured in the same run (chunk 64: the
-tensor-core path for sequences longer than 256 tokens) and reported under
-``secondary``.
+L=24,337 high-resolution workload is measured in the same run at chunk 128
+(the pre-pass, segment scan and main pass of the long-sequence tensor-core
+path) and reported under ``secondary``; every other workload, mask, form and
+chunk length of the scope's configurations gets a line under ``configs``.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
 oracle instead, on a bounded sample of the same workload.
@@ -45,38 +46,42 @@ FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # (chunk, sequence longer than 256 tokens): the long chunk-128 path has its
 # own main pass.
 _CSRC = "bidirectional_masked_linear_gb300/csrc/"
-_TC_SOURCES = {
-    (64, False): (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
-    (64, True): (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
-    (128, False): (_CSRC + "lion_c128.cu", _CSRC + "c128_common.cuh", _CSRC + "tc_ptx.cuh"),
-    (128, True): (_CSRC + "lion_c128L.cu", _CSRC + "c128_common.cuh", _CSRC + "tc_ptx.cuh"),
+_COMMON = (_CSRC + "c128_common.cuh", _CSRC + "tc_ptx.cuh")
+# the kernels one call launches, per (chunk, sequence longer than 256 tokens),
+# with the sources each kernel is built from
+_CALL_KERNELS = {
+    (128, False): {"lion_chunk128_tc_kernel": (_CSRC + "lion_c128.cu",) + _COMMON},
+    (128, True): {"lion_chunk128_pre_kernel": (_CSRC + "lion_c128P.cu",) + _COMMON,
+                  "lion_segment_scan_kernel": (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
+                  "lion_chunk128_long_kernel": (_CSRC + "lion_c128L.cu",) + _COMMON},
 }
-TRAFFIC_PER_HEAD = {
-    # chunk-128 kernel, ViT-B shape at B=128, LION-S: 153.4 MB / 1536 heads
-    ("1d94bfce7f698332337e9082c69accf2eb23926ea5fd5714a0ca66268b715025", "vit_b", "s", 128):
-        (117490176 + 35867392) / 1536,
-    # chunk-128 main pass for long sequences, L=24337 (B=2, H=12), LION-S:
-    # 386.3 MB / 24 heads (q, k, v, log-lambda, the pre-pass states, y)
-    ("9e4ae8f3d02e1d004ba40516a00124ecf0cf02e9d164a2890ac00e37e0f87b8f", "hires_2496", "s", 128):
-        (271414528 + 114904064) / 24,
-}
+# (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
+# write) of one launch, from one ncu capture of that kernel
+TRAFFIC_PER_HEAD = {}
 
 
-def _sources_sha(key):
+def _sources_sha(files):
     import hashlib
     h = hashlib.sha256()
-    for rel in _TC_SOURCES.get(key, ()):
+    for rel in files:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
 def traffic_bytes(w, mask, chunk):
-    key = (chunk, w.L > 256)
-    if key not in _TC_SOURCES:
-        return None
-    per_head = TRAFFIC_PER_HEAD.get((_sources_sha(key), w.name, mask, chunk))
-    return None if per_head is None else per_head * w.B * w.H
+    """DRAM traffic of one whole call (every kernel it launches), with each
+    kernel's bytes; None when a kernel has no capture at its current sources."""
+    kernels = _CALL_KERNELS.get((chunk, w.L > 256))
+    if not kernels:
+        return None, None
+    per = {}
+    for name, files in kernels.items():
+        b = TRAFFIC_PER_HEAD.get((name, _sources_sha(files), w.name, mask, chunk))
+        if b is None:
+            return None, None
+        per[name] = b * w.B * w.H
+    return sum(per.values()), per
 
 
 def _peaks():
@@ -196,6 +201,30 @@ def _max_over_ranks(dist, x: float) -> float:
     t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _build_once(dist, rank):
+    """Rank 0 compiles the library (if anything is stale) while the others
+    wait for its outcome in the process group's key-value store; a failed
+    build ends every rank with the same error instead of leaving the others
+    in a collective."""
+    from bidirectional_masked_linear_gb300 import build
+    if dist is None:
+        build.build()
+        return
+    store = dist.distributed_c10d._get_default_store()
+    if rank == 0:
+        try:
+            build.build()
+            store.set("lion_build", "ok")
+        except Exception as e:  # noqa: BLE001 -- reported to every rank
+            store.set("lion_build", "failed: " + str(e).splitlines()[0][:200])
+            raise
+    else:
+        store.wait(["lion_build"])
+        outcome = store.get("lion_build").decode()
+        if outcome != "ok":
+            raise SystemExit(f"rank {rank}: library build on rank 0 {outcome}")
 
 
 def time_device(call, steps, warmup, flush, stream):
@@ -441,27 +470,39 @@ def measure_stream(B, H, d, mask, steps, warmup):
     return a.elapsed_time(b) / steps
 
 
-def cpu_baseline(name, mask, chunk, budget_s=10.0):
-    """The float64 oracle (chunk form, all host cores) on a bounded sample of
-    the same workload: batch rows (all H heads each) in order, wrapping round
-    to the first row, until `budget_s` of CPU time is spent.  tokens/s counts
-    L tokens per batch row."""
+def _oracle_sample(name, mask, budget_s, threads):
+    """tokens/s of the float64 oracle on a bounded sample of a workload: batch
+    rows (all H heads each) in order, wrapping round to the first row, until
+    `budget_s` of wall time is spent.  The form is the one the scope's
+    measurement plan names: the brute force up to 1024 tokens, the
+    recurrent form beyond (the brute force is O(L^2) in memory and time)."""
     import oracle
     w = synth.WORKLOADS[name]
     inp = synth.workload_inputs(name, mask)
     q, k, v, ll = (synth.as_f64(inp[x]) for x in ("q", "k", "v", "log_lambda"))
-    cores = oracle.threads(0)
+    fn, form = (oracle.full, "brute-force full form") if w.L <= 1024 else (oracle.rnn, "recurrent form")
+    oracle.threads(threads)
+    cores = oracle.threads(threads)
     rows, t0 = 0, time.perf_counter()
     while (time.perf_counter() - t0) < budget_s:
         b = rows % w.B
         sl = slice(b, b + 1)
         lls = None if ll is None else (ll if mask == "d" else ll[sl])
-        oracle.chunk(q[sl], k[sl], v[sl], lls, inp["mask"], chunk, threads=0)
+        fn(q[sl], k[sl], v[sl], lls, inp["mask"], threads=threads)
         rows += 1
     dt = time.perf_counter() - t0
+    par = "OpenMP over heads" if cores > 1 else "one thread"
     return {"value": rows * w.L / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{rows} batch rows of {w.B} (wrapping; {rows * w.H} heads x L={w.L}), "
-                      f"float64 chunk form (chunk {chunk}), OpenMP over heads, {dt:.1f} s"}
+                      f"float64 {form}, {par}, {dt:.1f} s"}
+
+
+def cpu_baseline(name, mask, budget_s=10.0):
+    """The float64 oracle as it stands, on all host cores and on one, each on
+    a bounded sample of the workload (see _oracle_sample)."""
+    res = _oracle_sample(name, mask, budget_s, 0)
+    res["single_thread"] = _oracle_sample(name, mask, budget_s / 2, 1)
+    return res
 
 
 def run_reference(args, dist, ws, rank):
@@ -471,7 +512,7 @@ def run_reference(args, dist, ws, rank):
     budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     res = []
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(args.workload, args.mask, args.chunk, budget_s=budget)
+        r = _oracle_sample(args.workload, args.mask, budget, 0)
         if i >= args.warmup:
             res.append(r)
     val = statistics.median(r["value"] for r in res)
@@ -486,6 +527,60 @@ def run_reference(args, dist, ws, rank):
 
 
 METRIC = "LION attn fwd tokens/s (chunkwise form)"
+
+# Every workload / mask / form / chunk of the scope's configurations that is
+# not the headline, each timed for its own line: (workload, mask, form, chunk)
+CONFIG_LINES = [
+    ("tiny_d_fp32", "d", "chunk", 16), ("tiny_d_fp32", "d", "full", 16), ("tiny_d_fp32", "d", "rnn", 16),
+    ("vit_t_s", "s", "chunk", 64),
+] + [("vit_b", m, "chunk", c) for m in ("lit", "d", "s") for c in (32, 64, 128)] + [
+    ("vit_b", m, "full", 0) for m in ("lit", "d", "s")] + [
+    ("bert_large", m, "chunk", c) for m in ("d", "s") for c in (64, 128)] + [
+    ("hires_2496", m, "chunk", c) for m in ("d", "s") for c in (64, 128)] + [
+    ("hires_2496", m, "rnn", 0) for m in ("d", "s")] + [
+    ("lra_4096", "s", "chunk", 64), ("lra_4096", "d", "chunk", 128), ("lra_4096", "s", "rnn", 0),
+]
+
+
+def full_flops(w) -> int:
+    """Algorithmic flops of the full form per call: phi(Q) phi(K)^T and the
+    masked product with [V | 1], 2 L^2 d flops each, per head."""
+    return 4 * w.B * w.H * w.L * w.L * w.d
+
+
+def measure_config(c, flush, hbm_peak, steps=20, warmup=3):
+    """One line of ``configs``: CUDA-event time of one call, tokens/s, and the
+    fraction of the roofline that bounds the path: HBM bytes for the chunk and
+    recurrent forms, the fp32 CUDA-core peak for the full form (O(L^2 d)
+    arithmetic on 16 + 4 bytes a token)."""
+    name, mask, form, chunk = c
+    w, _, t, _k = measure(name, mask, chunk or 64, form, steps, warmup, flush)
+    ms = statistics.mean(t)
+    line = {"workload": f"{w.name} B={w.B} H={w.H} L={w.L} d={w.d}", "mask": mask, "form": form,
+            "chunk": chunk if form == "chunk" else None, "input_dtype": w.dtype,
+            "value": w.B * w.L / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "launches_per_call": kernels_per_call(form, chunk, w),
+            "path": path_name(form, chunk, w)}
+    if form == "full":
+        fl = full_flops(w)
+        line["roofline"] = {"bound": "alu", "achieved": fl / (ms * 1e-3) / 1e12, "peak": FP32_ALU_PEAK_TFLOPS,
+                            "unit": "TFLOP/s", "frac": fl / (ms * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
+                            "algorithmic_flops": fl}
+    else:
+        b = algorithmic_bytes(w, mask)
+        line["roofline"] = {"bound": "hbm", "achieved": b / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                            "frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": b}
+    return line
+
+
+def path_name(form, chunk, w) -> str:
+    tc = form == "chunk" and w.d == 64 and w.dtype == "bf16"
+    if tc and chunk == 128:
+        return "tcgen05 chunk-128" + (" (pre-pass, segment scan, main pass)" if w.L > 256 else "")
+    if tc and chunk == 64:
+        return "tcgen05 chunk-64" + (" (pre-pass, segment scan, main pass)" if w.L > 256 else "")
+    return {"full": "full form, fp32 CUDA cores", "rnn": "recurrent form, fp32 CUDA cores",
+            "chunk": "chunk form, fp32 CUDA cores"}[form]
 
 
 def _config(args, w):
@@ -511,6 +606,7 @@ def main():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-streaming", action="store_true")
     ap.add_argument("--no-reordered", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling captures)")
     args = ap.parse_args()
@@ -525,9 +621,7 @@ def main():
 
     torch.cuda.set_device(local)
     from bidirectional_masked_linear_gb300 import build
-    if rank == 0:   # one process compiles (if anything is stale); the others wait, then load it
-        build.build()
-    _barrier(dist)
+    _build_once(dist, rank)
     lion.load(build.LIB)
     hbm_peak, bf16_peak, peak_src = _peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -563,13 +657,17 @@ def main():
                                  "chunk", 50, 3, flush)
         ms2 = statistics.mean(t2)
         b2 = algorithmic_bytes(w2, args.mask if args.mask != "lit" else "s")
+        tr2, tr2k = traffic_bytes(w2, args.mask if args.mask != "lit" else "s", HIRES_CHUNK)
         secondary = {"workload": f"{w2.name} B={w2.B} H={w2.H} L={w2.L} d={w2.d}", "chunk": HIRES_CHUNK,
                      "value": w2.B * w2.L / (ms2 * 1e-3), "unit": "tokens/s", "ms_per_step": ms2,
+                     "launches_per_call": kernels_per_call("chunk", HIRES_CHUNK, w2),
                      "roofline": {"bound": "hbm", "achieved": b2 / (ms2 * 1e-3) / 1e9,
                                   "peak": hbm_peak, "unit": "GB/s",
                                   "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak,
-                                  "traffic": traffic_bytes(w2, args.mask if args.mask != "lit" else "s",
-                                                           HIRES_CHUNK)}}
+                                  "algorithmic_bytes": b2,
+                                  "traffic": tr2, "traffic_per_kernel": tr2k,
+                                  "note": "achieved and traffic cover the whole call: pre-pass, segment scan "
+                                          "and main pass"}}
         del _k2
 
     lra = None
@@ -644,9 +742,14 @@ def main():
                                   "bytes_per_step": sb,
                                   "note": "the fp32 states (B*H*d*d*4 bytes) stay in the 129 MB L2 between steps"}}
 
+    configs = None
+    if not args.no_configs:
+        configs = [measure_config(c, flush, hbm_peak) for c in CONFIG_LINES
+                   if (c[0], c[1], c[2], c[3]) != (args.workload, args.mask, args.form, args.chunk)]
+
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:
-        cpu = cpu_baseline(args.workload, args.mask, args.chunk)
+        cpu = cpu_baseline(args.workload, args.mask)
 
     if rank == 0:
         line = {
@@ -656,7 +759,7 @@ def main():
             "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": _config(args, w),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic_bytes(w, args.mask, args.chunk),
+                         "frac": achieved / hbm_peak, "traffic": traffic_bytes(w, args.mask, args.chunk)[0],
                          "peak_source": peak_src, "algorithmic_bytes": abytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -669,6 +772,7 @@ def main():
             "backward": backward,
             "reordered": reordered,
             "streaming": streaming,
+            "configs": configs,
         }
         print(json.dumps(line))
     if dist is not None:

@@ -7,9 +7,6 @@
 #include "lion_common.cuh"
 #include "lion_internal.h"
 
-namespace lion {
-lion_status forward_checked(const lion_args* a);
-}
 
 namespace {
 
@@ -65,6 +62,14 @@ lion_status validate(const lion_args* a) {
   if (a->form == LION_FORM_FULL && a->L > LION_FULL_MAX_L) return LION_ERR_UNSUPPORTED;
   return LION_OK;
 }
+
+}  // namespace
+
+// Shared by every entry point that takes a lion_args (also the
+// allocation-free recurrent form in lion_noalloc.cu).
+lion_status lion::validate_args(const lion_args* a) { return validate(a); }
+
+namespace {
 
 lion_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return LION_OK;

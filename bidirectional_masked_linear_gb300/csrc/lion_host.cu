@@ -18,10 +18,6 @@
 #include "lion_common.cuh"
 #include "lion_internal.h"
 
-namespace lion {
-lion_status forward_checked(const lion_args* a);   // lion_api.cu
-}
-
 namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

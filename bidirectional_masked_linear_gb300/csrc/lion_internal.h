@@ -5,7 +5,16 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/lion.h"
+
 namespace lion {
+
+// Argument checks of lion_attn_fwd_ex (null pointers, sizes, enums,
+// alignment, device-accessible memory, the full form's length limit), done
+// on the host before anything is launched.
+lion_status validate_args(const lion_args* a);
+// The forward on arguments that already passed validate_args.
+lion_status forward_checked(const lion_args* a);
 
 struct Problem {
   const void* q;

@@ -15,13 +15,15 @@
 // Host code may not use the array's name as a device address (on the host it
 // is only a stand-in).  The device address is looked up once per device with
 // cudaGetSymbolAddress, with that device current, by the first call made on
-// that device; make that first call before any stream capture.
+// that device; make that first call before any stream capture.  The address
+// is kept for the life of the process: a cudaDeviceReset after the first
+// call is not supported.
 //
 // All calls share the one array and it keeps the previous call's contents.
 // The recurrent kernel writes every c^F_i before it reads it, so nothing
 // needs clearing.  Calls whose executions overlap on the GPU (different
 // streams, no ordering between them) race on the array: order them.
-#include <stdint.h>
+#include <atomic>
 
 #include "../../include/lion.h"
 #include "lion_common.cuh"
@@ -33,36 +35,27 @@ constexpr size_t kMaxHeadTokens = LION_NOALLOC_MAX_HEAD_TOKENS;
 
 static __device__ __align__(256) float g_noalloc_cF[kMaxHeadTokens];
 
+// Device address of the array, per device, resolved once.  Concurrent first
+// calls from several host threads may both resolve it; they store the same
+// value, and the atomic makes that well defined.
 constexpr int kMaxDevices = 64;
-float* g_noalloc_ptr[kMaxDevices] = {};
+std::atomic<float*> g_noalloc_ptr[kMaxDevices];
 
 // Device address of the scratch array on the current device (set-up on the
 // first call per device).
 float* noalloc_scratch() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_noalloc_ptr[dev]) {
-    float* ptr = nullptr;
+  float* ptr = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
     if (cudaGetSymbolAddress((void**)&ptr, g_noalloc_cF) != cudaSuccess || !ptr) {
       cudaGetLastError();
       return nullptr;
     }
-    g_noalloc_ptr[dev] = ptr;
+    g_noalloc_ptr[dev].store(ptr, std::memory_order_release);
   }
-  return g_noalloc_ptr[dev];
+  return ptr;
 }
-
-bool gpu_pointer(const void* p) {
-  cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
-  return at.type == cudaMemoryTypeHost && at.devicePointer != nullptr;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -70,19 +63,33 @@ extern "C" lion_status lion_attn_fwd_rnn_noalloc(const void* q, const void* k, c
                                                  const float* log_lambda, int B, int H, int L, int d,
                                                  int mask_kind, int dtype, float* out,
                                                  cudaStream_t stream) {
-  if (!q || !k || !v || !out) return LION_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || L < 1) return LION_ERR_INVALID_ARG;
-  if (d != 16 && d != 32 && d != 64 && d != 128) return LION_ERR_INVALID_ARG;
-  if (mask_kind < LION_MASK_LIT || mask_kind > LION_MASK_S) return LION_ERR_INVALID_ARG;
-  if (dtype != LION_DTYPE_BF16 && dtype != LION_DTYPE_FP32) return LION_ERR_INVALID_ARG;
-  if (mask_kind != LION_MASK_LIT && !log_lambda) return LION_ERR_INVALID_ARG;
+  // the checks of every other forward entry point (no workspace: the form's
+  // scratch is the fixed array)
+  lion_args a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.log_lambda = log_lambda;
+  a.out = out;
+  a.B = B;
+  a.H = H;
+  a.L = L;
+  a.d = d;
+  a.mask_kind = mask_kind;
+  a.form = LION_FORM_RNN;
+  a.chunk = 1;
+  a.dtype = dtype;
+  a.phi = LION_PHI_DEFAULT;
+  a.workspace = nullptr;
+  a.workspace_bytes = 0;
+  a.stream = stream;
+  a.out_bf16 = 0;
   // the scratch holds one float per head-token
-  if ((unsigned long long)B * (unsigned long long)H * (unsigned long long)L > kMaxHeadTokens)
+  if (B >= 1 && H >= 1 && L >= 1 &&
+      (unsigned long long)B * (unsigned long long)H * (unsigned long long)L > kMaxHeadTokens)
     return LION_ERR_UNSUPPORTED;
-  if ((long long)L * d > 0x7fffffffLL) return LION_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LION_ERR_INVALID_ARG;
-  if (!gpu_pointer(q) || !gpu_pointer(k) || !gpu_pointer(v) || !gpu_pointer(out)) return LION_ERR_INVALID_ARG;
-  if (mask_kind != LION_MASK_LIT && !gpu_pointer(log_lambda)) return LION_ERR_INVALID_ARG;
+  const lion_status st = lion::validate_args(&a);
+  if (st != LION_OK) return st;
   float* scratch = noalloc_scratch();
   if (!scratch) return LION_ERR_CUDA;
   lion::Problem p;

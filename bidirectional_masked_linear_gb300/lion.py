@@ -236,6 +236,15 @@ def attn_fwd_rnn_noalloc(q, k, v, log_lambda, mask_kind, out=None, stream=None):
     B, H, L, d = q.shape
     if out is None:
         out = torch.empty((B, H, L, d), dtype=torch.float32, device=q.device)
+    if out.dtype != torch.float32 or out.shape != q.shape:
+        raise TypeError("out must be float32 with the shape of q")
+    if log_lambda is not None and log_lambda.dtype != torch.float32:
+        raise TypeError("log_lambda must be float32")
+    for t in (q, k, v, out) + ((log_lambda,) if log_lambda is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if q.dtype != k.dtype or q.dtype != v.dtype or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share dtype and shape")
     st = lib.lion_attn_fwd_rnn_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), B, H, L, d,
                                        mask_kind, _dtype_code(q), _ptr(out), _stream_handle(stream))
     _check(st)

@@ -87,8 +87,10 @@ typedef enum {
  *   mask_kind   lion_mask_kind.   form: lion_form.
  *   chunk       chunk length for LION_FORM_CHUNK, 1 <= chunk <= 1024 (larger:
  *               LION_ERR_UNSUPPORTED).  The result does not depend on it up
- *               to rounding; bf16 with d = 64, chunk = 64 and L <= 256 runs
- *               on the tensor cores.  Ignored by the other forms.
+ *               to rounding.  With d = 64, chunk 64 and chunk 128 run on the
+ *               tensor cores at any L (chunk 128: one launch for L <= 256,
+ *               three above); every other chunk, and d != 64, runs on the
+ *               CUDA cores in fp32.  Ignored by the other forms.
  *   out         [B][H][L][d] float32, device, written entirely.
  * Workspace, when the form needs one, is taken from the stream-ordered
  * allocator (cudaMallocAsync/cudaFreeAsync on `stream`); use
@@ -195,8 +197,11 @@ lion_status lion_sync_status(cudaStream_t stream);
  *   larger problems return LION_ERR_UNSUPPORTED before anything launches.
  *   Nothing is allocated, ever.  The first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress) for that device: make it
- *   before any stream capture.  Every call shares the array; calls that
- *   overlap on the GPU (unordered streams) race on it -- order them.
+ *   before any stream capture.  The address is kept for the life of the
+ *   process, so a cudaDeviceReset after the first call is not supported.
+ *   Every call shares the array; calls that overlap on the GPU (unordered
+ *   streams) race on it -- order them.  Argument checks and errors are those
+ *   of lion_attn_fwd_ex.
  */
 #define LION_NOALLOC_MAX_HEAD_TOKENS (1u << 20)
 lion_status lion_attn_fwd_rnn_noalloc(const void* q, const void* k, const void* v,

@@ -17,3 +17,15 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print how much of the per-row error bound each labelled parity case
+    used (rows that needed the conditioning factor, the largest factor, the
+    worst error as a fraction of its bound)."""
+    from parity import STATS, format_stats
+    if not STATS:
+        return
+    terminalreporter.write_sep("-", "parity statistics")
+    for label, st in STATS:
+        terminalreporter.write_line(format_stats(label, st))

@@ -25,6 +25,11 @@ import numpy as np
 TOL_BF16 = 2e-3
 TOL_FP32 = 1e-5
 
+# One line per labelled check, printed at the end of the pytest run (see
+# conftest.pytest_terminal_summary): how much of the per-row bound each case
+# used and how many rows needed the conditioning factor.
+STATS = []
+
 
 def row_errors(y, ref):
     y = np.asarray(y, dtype=np.float64)
@@ -38,9 +43,13 @@ def row_errors(y, ref):
     return e
 
 
-def check_rows(oracle, y, ref, tol, q64, k64, ll64, mask_kind, phi_kind=0, max_kappa_rows=4096):
+def check_rows(oracle, y, ref, tol, q64, k64, ll64, mask_kind, phi_kind=0, max_kappa_rows=4096,
+               label=None):
     """Assert the per-row bound over y, ref of shape [B, H, L, d].  Returns a
-    summary dict (worst plain error, rows that needed kappa, worst scaled)."""
+    summary dict: rows, the worst plain error, the rows that needed kappa
+    (plain error above tol), the largest kappa among them, and the worst
+    error as a fraction of its row's bound.  With a label the summary is
+    also recorded in STATS."""
     e = row_errors(y, ref)
     bad = np.argwhere(e > tol)
     worst_scaled = float(np.max(np.minimum(e, 1e300))) / tol if e.size else 0.0
@@ -48,13 +57,28 @@ def check_rows(oracle, y, ref, tol, q64, k64, ll64, mask_kind, phi_kind=0, max_k
         raise AssertionError(f"{len(bad)} rows exceed tol {tol} before conditioning "
                              f"(worst {float(np.max(e)):.3e})")
     scaled = []
+    max_kappa = 0.0
     for b, h, i in bad:
         kap = oracle.row_kappa(q64, k64, ll64, mask_kind, int(b), int(h), int(i), int(i) + 1,
                                phi_kind)[0]
+        max_kappa = max(max_kappa, float(kap))
         s = e[b, h, i] / (tol * max(1.0, kap))
         scaled.append(s)
         assert s <= 1.0, (f"row (b={b}, h={h}, i={i}): err {e[b, h, i]:.3e} > "
                           f"{tol:.1e} * max(1, kappa={kap:.3e})")
     if scaled:
         worst_scaled = max(float(np.max(np.where(e <= tol, e, 0))) / tol, max(scaled))
-    return {"max_err": float(np.max(e)), "kappa_rows": len(bad), "worst_scaled": worst_scaled}
+    summary = {"rows": int(e.size), "max_err": float(np.max(e)), "kappa_rows": len(bad),
+               "max_kappa": max_kappa, "worst_scaled": worst_scaled}
+    if label is not None:
+        STATS.append((label, summary))
+    return summary
+
+
+def format_stats(label, st):
+    if "worst_scaled" not in st:
+        return f"{label}: " + ", ".join(f"{k} {v:.3g}" if isinstance(v, float) else f"{k} {v}"
+                                        for k, v in st.items())
+    return (f"{label}: rows {st['rows']}, max plain err {st['max_err']:.2e}, "
+            f"rows needing kappa {st['kappa_rows']} (largest kappa {st['max_kappa']:.1f}), "
+            f"worst err / bound {st['worst_scaled']:.3f}")

@@ -26,9 +26,25 @@ def test_algorithmic_bytes_vit_b():
 
 def test_traffic_is_null_for_unknown_kernels():
     w = synth.WORKLOADS["vit_b"]
-    assert bench.traffic_bytes(w, "s", 32) is None
-    t = bench.traffic_bytes(w, "s", 128)
-    assert t is None or t > 0
+    assert bench.traffic_bytes(w, "s", 32) == (None, None)
+    t, per = bench.traffic_bytes(w, "s", 128)
+    assert t is None or (t > 0 and abs(sum(per.values()) - t) < 1)
+
+
+def test_traffic_covers_every_kernel_of_the_call(monkeypatch):
+    """The long path's figure is the sum over its three kernels, and one
+    kernel without a capture at its current sources makes the whole figure
+    null."""
+    w = synth.WORKLOADS["hires_2496"]
+    kernels = bench._CALL_KERNELS[(128, True)]
+    assert len(kernels) == 3
+    table = {(name, bench._sources_sha(files), w.name, "s", 128): 1000.0 * (n + 1)
+             for n, (name, files) in enumerate(kernels.items())}
+    monkeypatch.setattr(bench, "TRAFFIC_PER_HEAD", table)
+    t, per = bench.traffic_bytes(w, "s", 128)
+    assert t == 6000.0 * w.B * w.H and len(per) == 3
+    table.pop(next(iter(table)))
+    assert bench.traffic_bytes(w, "s", 128) == (None, None)
 
 
 def test_launch_counts():
@@ -43,10 +59,31 @@ def test_launch_counts():
 
 def test_traffic_keys_follow_the_kernel_that_runs():
     # every sources list names files that exist, so a hash can be taken
-    for key, files in bench._TC_SOURCES.items():
-        for rel in files:
-            assert os.path.exists(os.path.join(ROOT, rel)), (key, rel)
-    assert bench._sources_sha((128, False)) != bench._sources_sha((128, True))
+    shas = set()
+    for key, kernels in bench._CALL_KERNELS.items():
+        for name, files in kernels.items():
+            for rel in files:
+                assert os.path.exists(os.path.join(ROOT, rel)), (key, name, rel)
+            shas.add(bench._sources_sha(files))
+    assert len(shas) == 4
+
+
+def test_config_lines_cover_the_scope_configurations():
+    """Every configuration's workload, mask, form and chunk length has a line
+    (the headline ViT-B LION-S chunk 128 is measured separately)."""
+    lines = set(bench.CONFIG_LINES)
+    assert ("tiny_d_fp32", "d", "chunk", 16) in lines
+    assert ("vit_t_s", "s", "chunk", 64) in lines
+    for m in ("lit", "d", "s"):
+        assert ("vit_b", m, "full", 0) in lines
+        for c in (32, 64, 128):
+            assert ("vit_b", m, "chunk", c) in lines
+    for m in ("d", "s"):
+        for c in (64, 128):
+            assert ("bert_large", m, "chunk", c) in lines
+        assert ("hires_2496", m, "rnn", 0) in lines and ("hires_2496", m, "chunk", 128) in lines
+    for name, *_ in lines:
+        assert name in synth.WORKLOADS
 
 
 def test_backward_flops_and_peak():

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from bidirectional_masked_linear_gb300 import lion, synth
-from parity import TOL_BF16, TOL_FP32, check_rows, row_errors
+from parity import STATS, TOL_BF16, TOL_FP32, check_rows, row_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -44,9 +44,9 @@ def f64(inp):
             synth.as_f64(inp["log_lambda"]))
 
 
-def check(oracle_mod, y, ref, inp, tol, phi=0):
+def check(oracle_mod, y, ref, inp, tol, phi=0, label=None):
     q, k, _, ll = f64(inp)
-    return check_rows(oracle_mod, y, ref, tol, q, k, ll, inp["mask"], phi)
+    return check_rows(oracle_mod, y, ref, tol, q, k, ll, inp["mask"], phi, label=label)
 
 
 # --------------------------------------------------------------- tiny ---
@@ -236,17 +236,24 @@ def test_unit_decay_equals_lit():
         assert np.max(row_errors(a, b)) < TOL_BF16
 
 
-def test_gpu_forms_agree():
-    """The three GPU forms agree with each other within the bf16 bound."""
-    for mask in ("lit", "d", "s"):
-        inp = synth.make_inputs(4, 3, 197, 64, mask, "bf16", seed=11)
-        ys = [run_gpu(inp, lion.FORM_FULL), run_gpu(inp, lion.FORM_RNN)] + \
-             [run_gpu(inp, lion.FORM_CHUNK, c) for c in (32, 64, 128)]
-        for y in ys[1:]:
-            e = row_errors(y, ys[0])
-            assert np.max(e) < TOL_BF16 or mask == "s"
-            if mask == "s":       # SiLU rows may be ill-conditioned: compare the bulk
-                assert np.quantile(e, 0.999) < TOL_BF16
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_gpu_forms_agree(oracle_mod, mask):
+    """The GPU forms (full, RNN, chunk 32 / 64 / 128) agree with each other
+    under the same per-row bound as against the oracle (Theorem 3.3: the
+    forms are equal): every row of every pair within tol * max(1, kappa_i),
+    and every form within that bound of the float64 oracle."""
+    inp = synth.make_inputs(4, 3, 197, 64, mask, "bf16", seed=11)
+    ys = {"full": run_gpu(inp, lion.FORM_FULL), "rnn": run_gpu(inp, lion.FORM_RNN)}
+    for c in (32, 64, 128):
+        ys[f"chunk{c}"] = run_gpu(inp, lion.FORM_CHUNK, c)
+    q, k, v, ll = f64(inp)
+    ref = oracle_mod.full(q, k, v, ll, inp["mask"])
+    names = list(ys)
+    for a in names:
+        check(oracle_mod, ys[a], ref, inp, TOL_BF16, label=f"forms {mask}: {a} vs oracle")
+    for n, a in enumerate(names):
+        for b in names[n + 1:]:
+            check(oracle_mod, ys[a], ys[b], inp, TOL_BF16, label=f"forms {mask}: {a} vs {b}")
 
 
 def test_device_status_clean_after_calls():
@@ -344,10 +351,21 @@ FULL_CASES = [
 
 @pytest.mark.parametrize("name,mask,form,chunk", FULL_CASES)
 def test_full_workload(oracle_mod, name, mask, form, chunk):
+    """Every output row of the workload against the float64 oracle.  Rows
+    whose plain error exceeds tol need the conditioning factor kappa_i; with
+    elu+1 features kappa = 1, so LIT and LION-D must have none, and with SiLU
+    features at most 1% of the rows may lean on it.  The counts, the largest
+    kappa used and the worst error as a fraction of its bound are printed at
+    the end of the run."""
     inp = _workload(name, mask)
     ref = _reference(name, mask)
     y = run_gpu(inp, form, chunk)
-    check(oracle_mod, y, ref, inp, TOL_BF16)
+    form_name = {lion.FORM_FULL: "full", lion.FORM_RNN: "rnn", lion.FORM_CHUNK: f"chunk{chunk}"}[form]
+    st = check(oracle_mod, y, ref, inp, TOL_BF16, label=f"workload {name} {mask} {form_name}")
+    if mask in ("lit", "d"):
+        assert st["kappa_rows"] == 0, st
+    else:
+        assert st["kappa_rows"] <= 0.01 * st["rows"], st
 
 
 # ------------------------------------------------------------- backward ---
@@ -370,18 +388,41 @@ def _bwd_check(oracle_mod, B, H, L, d, mask, dtype, phi=0, seed=0, positive=Fals
     got = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], torch.from_numpy(dy).cuda(),
                         inp["mask"], phi)
     torch.cuda.synchronize()
-    # a tensor whose exact value is 0 (dq and dk at L = 1) is measured against
-    # the scale of the case's other gradients
-    floor = 1e-2 * max(float(np.abs(r).max()) for r in ref if r is not None)
+    _grad_rows(ref, got, f"bwd {MASK_NAME[inp['mask']]} {dtype} ({B},{H},{L},{d}) phi {phi}")
+    return got
+
+
+def _grad_rows(ref, got, label):
+    """Per row (one token's d gradient entries of dq, dk, dv; one entry of
+    dlog_lambda) the error relative to that row's own scale, with a floor of
+    1e-3 of the tensor's largest entry for rows whose gradient cancels to
+    near zero.  The scale of a dq, dk or dv row is its largest entry.  LION-S's
+    dlog_lambda_u is the suffix sum over m >= u of dLoss/dP_m (the derivative
+    by the prefix of the decays), so its scale is the sum of the magnitudes
+    of those terms, sum_{m>=u} |dlog_lambda_m - dlog_lambda_{m+1}| (which is
+    at least |dlog_lambda_u|): the componentwise bound of a sum.  LION-D's
+    [H] vector is compared entry by entry.  A tensor whose exact value is 0
+    (dq and dk at L = 1) is measured against the case's other gradients."""
+    scale = max(float(np.abs(r).max()) for r in ref if r is not None)
+    worst = {}
     for name, r, x in zip(("dq", "dk", "dv", "dlog_lambda"), ref, got):
         if r is None:
             assert x is None
             continue
         x = x.cpu().numpy().astype(np.float64)
         assert x.shape == r.shape, name
-        err = float(np.abs(x - r).max() / max(np.abs(r).max(), floor))
-        assert err <= TOL_BWD, (name, B, H, L, d, dtype, err)
-    return got
+        rr = r.reshape(-1, r.shape[-1]) if name != "dlog_lambda" else r.reshape(-1, 1)
+        xx = x.reshape(rr.shape)
+        floor = 1e-3 * max(float(np.abs(rr).max()), 1e-2 * scale)
+        den = np.maximum(np.abs(rr).max(axis=1), floor)
+        if name == "dlog_lambda" and r.ndim == 3:
+            terms = np.abs(r - np.concatenate([r[..., 1:], np.zeros_like(r[..., :1])], axis=-1))
+            suffix = np.flip(np.cumsum(np.flip(terms, -1), -1), -1)
+            den = np.maximum(suffix.reshape(-1), floor)
+        err = np.abs(xx - rr).max(axis=1) / den
+        worst[name] = float(err.max())
+        assert worst[name] <= TOL_BWD, (label, name, worst[name], int(np.argmax(err)))
+    STATS.append((label, {f"worst {k} row err": v for k, v in worst.items()}))
 
 
 @pytest.mark.gpu
@@ -428,9 +469,7 @@ def test_backward_steep_decay(oracle_mod):
     ref = oracle_mod.full_bwd(q64, k64, v64, ll64, dy.astype(np.float64), inp["mask"], 1)
     g = _cuda(inp)
     got = lion.attn_bwd(g["q"], g["k"], g["v"], g["log_lambda"], torch.from_numpy(dy).cuda(), inp["mask"], 1)
-    for r, x in zip(ref, got):
-        x = x.cpu().numpy().astype(np.float64)
-        assert np.abs(x - r).max() <= TOL_BWD * max(np.abs(r).max(), 1e-30)
+    _grad_rows(ref, got, "bwd steep-decay s")
 
 
 @pytest.mark.gpu
@@ -600,15 +639,7 @@ def _reorder_bwd_check(oracle_mod, inp, orders, seed, phi=0):
     got = lion.attn_bwd_reordered(g["q"], g["k"], g["v"], g["log_lambda"], o, torch.from_numpy(dy).cuda(),
                                   inp["mask"], phi)
     assert lion.sync_status() == lion.OK
-    floor = 1e-2 * max(float(np.abs(r).max()) for r in ref if r is not None)
-    for name, r, x in zip(("dq", "dk", "dv", "dlog_lambda"), ref, got):
-        if r is None:
-            assert x is None
-            continue
-        x = x.cpu().numpy().astype(np.float64)
-        assert x.shape == r.shape, name
-        err = float(np.abs(x - r).max() / max(np.abs(r).max(), floor))
-        assert err <= TOL_BWD, (name, q64.shape, err)
+    _grad_rows(ref, got, f"reordered bwd {MASK_NAME[inp['mask']]} {tuple(q64.shape)} phi {phi}")
 
 
 @pytest.mark.gpu

@@ -36,6 +36,49 @@ def _worker(rank, port, out):
         dist.destroy_process_group()
 
 
+def _build_worker(rank, port, out, fail):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE="2", RANK=str(rank),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    from bidirectional_masked_linear_gb300 import build
+
+    def fake_build():
+        if fail:
+            raise RuntimeError("nvcc failed: planted error")
+        return build.LIB
+
+    build.build = fake_build
+    dist, ws, r, local = bench._dist()
+    try:
+        bench._build_once(dist, r)
+        out.put((r, "ok"))
+    except (RuntimeError, SystemExit) as e:
+        out.put((r, str(e)))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("fail", (False, True))
+def test_build_outcome_reaches_every_rank(fail):
+    """Rank 0 builds; a failed build ends the other rank with the same error
+    (through the process group's store) instead of leaving it in a barrier."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_build_worker, args=(r, port, q, fail)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    if fail:
+        assert "planted error" in res[0] and "planted error" in res[1] and "rank 1" in res[1]
+    else:
+        assert res == {0: "ok", 1: "ok"}
+
+
 def test_two_rank_helpers_over_gloo():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()

@@ -3,10 +3,11 @@
 It exists for callers that cannot allocate device memory -- code inside a
 framework that owns every byte through its own allocator, or a hot loop that
 must not call cudaMalloc/cudaFree.  Its scratch is a fixed array of the
-library; this checks, through the C ABI, that two calls in a row give the
-same answer as the regular recurrent form (which takes its workspace from the
-stream-ordered allocator), and that oversized problems are refused before
-anything launches.  This file is collected last on purpose."""
+library.  Through the C ABI, two calls in a row must give exactly what the
+regular recurrent form gives (the same kernel, whose scratch comes from the
+stream-ordered allocator instead), and the result must match the float64
+oracle; oversized problems are refused before anything launches.  This file
+is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -14,14 +15,9 @@ import pytest
 import torch
 
 from bidirectional_masked_linear_gb300 import lion, synth
+from parity import TOL_BF16, check_rows
 
 pytestmark = pytest.mark.gpu
-
-TOL_BF16 = 2e-3
-
-
-def _rows(y, ref):
-    return np.max(np.abs(y - ref), axis=-1) / np.max(np.abs(ref), axis=-1)
 
 
 @pytest.fixture(scope="module")
@@ -32,11 +28,18 @@ def lib():
     return lion.load(build.build())
 
 
-@pytest.mark.parametrize("mask", ("lit", "d", "s"))
-def test_noalloc_matches_rnn_form_twice(lib, mask):
-    inp = synth.make_inputs(3, 4, 150, 64, mask, "bf16", seed=77)
+def _dev(inp):
     q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
     ll = None if inp["log_lambda"] is None else inp["log_lambda"].cuda()
+    return q, k, v, ll
+
+
+@pytest.mark.parametrize("mask", ("lit", "d", "s"))
+def test_noalloc_matches_rnn_form_twice(lib, mask):
+    """Bit for bit the regular recurrent form, on two calls in a row (the
+    second finds the first call's values in the shared scratch)."""
+    inp = synth.make_inputs(3, 4, 150, 64, mask, "bf16", seed=77)
+    q, k, v, ll = _dev(inp)
     ref = lion.attn_fwd(q, k, v, ll, inp["mask"], lion.FORM_RNN).cpu().numpy()
     vp = ctypes.c_void_p
     p = lambda t: vp(0) if t is None else vp(t.data_ptr())  # noqa: E731
@@ -48,8 +51,27 @@ def test_noalloc_matches_rnn_form_twice(lib, mask):
         assert st == lion.OK
         torch.cuda.synchronize()
         y = out.cpu().numpy()
-        assert np.isfinite(y).all()
-        assert np.max(_rows(y, ref)) < TOL_BF16
+        assert np.array_equal(y, ref)
+
+
+def test_noalloc_matches_oracle_through_the_binding(lib, oracle_mod):
+    """LION-S at the ViT-T shape through lion.attn_fwd_rnn_noalloc, against
+    the float64 oracle under the per-row bound of every parity test."""
+    inp = synth.make_inputs(4, 3, 197, 64, "s", "bf16", seed=78)
+    q, k, v, ll = _dev(inp)
+    y = lion.attn_fwd_rnn_noalloc(q, k, v, ll, lion.MASK_S)
+    torch.cuda.synchronize()
+    q64, k64, v64, ll64 = (synth.as_f64(inp[x]) for x in ("q", "k", "v", "log_lambda"))
+    ref = oracle_mod.full(q64, k64, v64, ll64, lion.MASK_S)
+    check_rows(oracle_mod, y.cpu().numpy(), ref, TOL_BF16, q64, k64, ll64, lion.MASK_S)
+
+
+def test_noalloc_binding_refuses_strided_tensors(lib):
+    x = torch.zeros((1, 2, 16, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        lion.attn_fwd_rnn_noalloc(x.transpose(1, 2), x.transpose(1, 2), x.transpose(1, 2), None, lion.MASK_LIT)
+    with pytest.raises(TypeError):
+        lion.attn_fwd_rnn_noalloc(x, x, x, None, lion.MASK_LIT, out=torch.zeros_like(x))
 
 
 def test_noalloc_refuses_oversized_problem(lib):
