@@ -156,14 +156,16 @@ constexpr uint64_t kMnmajOnesStep = (2048 >> 4) - ((uint64_t)(2048 >> 4) << 16);
 // One 16-column block of the decay mask on a row of S (row i of its chunk,
 // columns j0..j0+15), in place.  Blocks entirely left (right) of every row
 // of the warp (rows row_lo..row_lo+31) take the lower (upper) factor pair
-// without a select.
+// without a select.  A row scale 2^lrow, already folded into the row
+// factors ai and ri, enters the per-element exponential of the exact branch.
 template <int MASK>
 __device__ __forceinline__ void mask_block(float* sv, int j0, int i, int row_lo, bool exact, float ai, float ri,
-                                           float pi, const float* alpha, const float* rho, const float* pp) {
+                                           float pi, const float* alpha, const float* rho, const float* pp,
+                                           float lrow = 0.f) {
   if (MASK == MASK_LIT) return;
   if (exact) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) sv[e] *= ex2(-fabsf(pi - pp[j0 + e]) * kLog2e);
+    for (int e = 0; e < 16; ++e) sv[e] *= ex2(fmaf(-fabsf(pi - pp[j0 + e]), kLog2e, lrow));
     return;
   }
   if (j0 + 15 < row_lo) {

@@ -60,10 +60,20 @@
 // middle of the chunk's prefix range; chunks whose decay range exceeds
 // 2 * 80 nats take exp(-|p_i - p_j|) per element instead.
 //
+// State decay folded into the row (SiLU + L2 features, LION-S and LION-D):
+// y_i is num_i / den_i, so scaling all of row i's O by 1/sigma_i changes
+// nothing.  The epi warps multiply row i's mask factors by 1/sigma_i, and the
+// state product takes phi(q_i) as prep wrote it, with no pass over the Q
+// tile.  Normalised features give |s_ij| <= 1, so P_ij / sigma_i stays below
+// 2^15 (fp16 holds it) for sigma_i >= 2^-15; rows with a smaller sigma_i
+// keep the in-place decay-scaled phi(q_i) and unscaled factors.  LIT needs
+// neither (sigma = 1); elu+1 and identity features, whose scores have no
+// fixed bound, keep the scaled phi(q) on every row.
+//
 // Precision: MMA operands are fp16 (11-bit significand) with fp32
 // accumulation; phi(K), phi(Q), the weighted phi(K), V, P and the two
 // states (with their z) are each rounded once to fp16, and the decay-scaled
-// phi(q) twice.
+// phi(q) (rows that do not fold) twice.
 // Precondition: |phi(q)|, |phi(k)|, |v| and the states below 65504.
 //
 // Every mbarrier wait is bounded; on timeout the kernel records an error in
@@ -91,6 +101,7 @@ constexpr int kPrepWarps = 16, kEpiWarps = 8;
 constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
 constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
 constexpr long long kWaitCycles = 2000000000LL;       // ~1 s at 2 GHz
+constexpr float kFoldMinSigma = 1.f / 32768.f;        // rows that fold 1/sigma into P
 constexpr uint32_t kSleepNs = 2000u;
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -511,9 +522,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!waitb(B_S0 + g, n & 1)) good = false;
       good = __all_sync(0xffffffffu, good);   // TMEM loads below are warp-collective
       tc_fence_after();
+      // this row's state decay sigma_i folded into its mask factors (header);
+      // factors large enough to overflow once scaled do not fold
+      const bool exact = info(s)[I_EX0 + g] != 0.f;
+      float ai = alpha[i], ri = rho[i], lrow = 0.f;
+      const float pi = pp[i];
+      const float sg = states && row_ok ? f[2 * kRows + tok] : 1.f;
+      const bool fold = states && MASK != MASK_LIT && PHI == PHI_SILU_L2 && sg >= kFoldMinSigma &&
+                        (exact || fmaxf(ai, ri) <= 1e33f);
       if (good && warp_ok) {
-        const bool exact = info(s)[I_EX0 + g] != 0.f;
-        const float ai = alpha[i], ri = rho[i], pi = pp[i];
+        if (fold) {
+          const float is = rcp(sg);
+          ai *= is;
+          ri *= is;
+          lrow = -__log2f(sg);
+        }
         const uint32_t sa = tbase + lane_off + T_S + 128 * g;
         float sb0[16], sb1[16];
         tmem_ld16(sa, sb0);
@@ -524,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[8];
           const bool has1 = jj + 1 < nk, has2 = jj + 2 < nk;
           if (has1) tmem_ld16(sa + 16 * (jj + 1), sb1);
-          mask_block<MASK>(sb0, 16 * jj, i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
+          mask_block<MASK>(sb0, 16 * jj, i, 32 * q, exact, ai, ri, pi, alpha, rho, pp, lrow);
 #pragma unroll
           for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb0[2 * e], sb0[2 * e + 1]);
           tmem_st8(sa + 8 * jj, pk);
@@ -532,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             reg_fence16(sb1);
             if (has2) tmem_ld16(sa + 16 * (jj + 2), sb0);
-            mask_block<MASK>(sb1, 16 * (jj + 1), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp);
+            mask_block<MASK>(sb1, 16 * (jj + 1), i, 32 * q, exact, ai, ri, pi, alpha, rho, pp, lrow);
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = pack_h2(sb1[2 * e], sb1[2 * e + 1]);
             tmem_st8(sa + 8 * (jj + 1), pk);
@@ -580,9 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (good && row_ok) {
-          // sigma_i phi(q_i), in place: the A operand of the state product
-          const float sg = f[2 * kRows + tok];
+        // sigma_i phi(q_i), in place: the A operand of the state product, for
+        // the rows that do not fold (LIT: sigma = 1, nothing to do)
+        const bool scale_row = MASK != MASK_LIT && row_ok && !fold;
+        if (good && __any_sync(0xffffffffu, scale_row) && scale_row) {
           const float2 sg2 = make_float2(sg, sg);
           uint8_t* qt = Qt(s, g);
 #pragma unroll
