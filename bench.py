@@ -306,6 +306,17 @@ def bwd_flops(w) -> int:
     return 12 * w.B * w.H * w.L * w.L * w.d
 
 
+def bwd_chunk_flops(w) -> int:
+    """Algorithmic flops of the chunkwise gradients per call, chunks of C
+    tokens: per chunk six C x C x d products (scores, A [V|1], dA, (M.dA)
+    phi(K), (M.dA)^T phi(Q), A^T G) and twelve C x d x d state products (two
+    summaries and two applications each of the phi(k) [v;1]^T and phi(q) G^T
+    states, forward and backward), 2 flops a multiply-add: 12 L C d + 24 L d^2
+    per head."""
+    C = 32 if w.d >= 128 else 64
+    return w.B * w.H * w.L * (12 * C * w.d + 24 * w.d * w.d)
+
+
 def bwd_launches(mask, d) -> int:
     """Kernels one lion_attn_bwd call launches: phi, rows and columns passes;
     the dl pass for LION-D and LION-S; the batch sum for LION-D; the prefix of
@@ -313,9 +324,10 @@ def bwd_launches(mask, d) -> int:
     return 3 + (mask != "lit") + (mask == "d") + (mask == "s" and d >= 64)
 
 
-def measure_bwd(w, mask, steps, warmup, flush):
-    """CUDA-event time of one gradient call (lion_attn_bwd, all its kernels)
-    through the C entry point with preallocated outputs and workspace."""
+def measure_bwd(w, mask, steps, warmup, flush, chunkwise=False):
+    """CUDA-event time of one gradient call (lion_attn_bwd, or
+    lion_attn_bwd_chunk with `chunkwise`, all its kernels) through the C entry
+    point with preallocated outputs and workspace."""
     import ctypes
     inp = synth.make_inputs(w.B, w.H, w.L, w.d, mask, w.dtype, w.seed, w.lam)
     dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
@@ -326,7 +338,7 @@ def measure_bwd(w, mask, steps, warmup, flush):
         dll = torch.empty((w.H,), dtype=torch.float32, device="cuda")
     elif inp["mask"] == lion.MASK_S:
         dll = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device="cuda")
-    wsb = lion.bwd_workspace_bytes(w.B, w.H, w.L, w.d)
+    wsb = lion.bwd_workspace_bytes(w.B, w.H, w.L, w.d, lion.FORM_CHUNK if chunkwise else lion.FORM_FULL)
     wsp = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     p = lambda t: None if t is None else t.data_ptr()
@@ -336,10 +348,12 @@ def measure_bwd(w, mask, steps, warmup, flush):
                       lion.PHI_DEFAULT, wsp.data_ptr(), wsb, stream.cuda_stream)
     lib = lion.load()
 
+    entry = lib.lion_attn_bwd_chunk if chunkwise else lib.lion_attn_bwd
+
     def call():
-        st = lib.lion_attn_bwd(ctypes.byref(a))
+        st = entry(ctypes.byref(a))
         if st:
-            raise RuntimeError(f"lion_attn_bwd failed ({st})")
+            raise RuntimeError(f"gradient call failed ({st})")
 
     return time_device(call, steps, warmup, flush, stream)
 
@@ -534,7 +548,7 @@ CONFIG_LINES = [
     ("tiny_d_fp32", "d", "chunk", 16), ("tiny_d_fp32", "d", "full", 16), ("tiny_d_fp32", "d", "rnn", 16),
     ("vit_t_s", "s", "chunk", 64),
 ] + [("vit_b", m, "chunk", c) for m in ("lit", "d", "s") for c in (32, 64, 128)] + [
-    ("vit_b", m, "full", 0) for m in ("lit", "d", "s")] + [
+    ("vit_b", m, f, 0) for m in ("lit", "d", "s") for f in ("full", "rnn")] + [
     ("bert_large", m, "chunk", c) for m in ("d", "s") for c in (64, 128)] + [
     ("hires_2496", m, "chunk", c) for m in ("d", "s") for c in (64, 128)] + [
     ("hires_2496", m, "rnn", 0) for m in ("d", "s")] + [
@@ -548,11 +562,19 @@ def full_flops(w) -> int:
     return 4 * w.B * w.H * w.L * w.L * w.d
 
 
+def rnn_flops(w) -> int:
+    """Algorithmic flops of the recurrent form per call: both sweeps update the
+    d x (d + 1) state (S and z) and apply it to phi(q), a multiply-add per
+    element each: 2 * 2 * 2 d (d + 1) per token and head."""
+    return 8 * w.B * w.H * w.L * w.d * (w.d + 1)
+
+
 def measure_config(c, flush, hbm_peak, steps=20, warmup=3):
     """One line of ``configs``: CUDA-event time of one call, tokens/s, and the
-    fraction of the roofline that bounds the path: HBM bytes for the chunk and
-    recurrent forms, the fp32 CUDA-core peak for the full form (O(L^2 d)
-    arithmetic on 16 + 4 bytes a token)."""
+    fraction of the roofline that bounds the path: HBM bytes for the chunk
+    form, the fp32 CUDA-core peak for the full form (O(L^2 d) arithmetic on
+    16 + 4 bytes a token) and for the recurrent form (O(d^2) arithmetic a
+    token, sequential along the tokens)."""
     name, mask, form, chunk = c
     w, _, t, _k = measure(name, mask, chunk or 64, form, steps, warmup, flush)
     ms = statistics.mean(t)
@@ -561,8 +583,8 @@ def measure_config(c, flush, hbm_peak, steps=20, warmup=3):
             "value": w.B * w.L / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "launches_per_call": kernels_per_call(form, chunk, w),
             "path": path_name(form, chunk, w)}
-    if form == "full":
-        fl = full_flops(w)
+    if form in ("full", "rnn"):
+        fl = full_flops(w) if form == "full" else rnn_flops(w)
         line["roofline"] = {"bound": "alu", "achieved": fl / (ms * 1e-3) / 1e12, "peak": FP32_ALU_PEAK_TFLOPS,
                             "unit": "TFLOP/s", "frac": fl / (ms * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
                             "algorithmic_flops": fl}
@@ -706,6 +728,22 @@ def main():
                                  "frac": fl / (msb * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
                                  "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz",
                                  "algorithmic_flops": fl}}
+
+    if not args.no_backward:
+        chunk_lines = []
+        for wb in (w, synth.WORKLOADS["hires_2496"]):
+            mb = args.mask if args.mask != "lit" or wb is w else "s"
+            tc = measure_bwd(wb, mb, 10 if wb.L > 4096 else 20, 3, flush, chunkwise=True)
+            msc = statistics.mean(tc)
+            flc = bwd_chunk_flops(wb)
+            chunk_lines.append({
+                "form": "chunk", "workload": f"{wb.name} B={wb.B} H={wb.H} L={wb.L} d={wb.d}", "mask": mb,
+                "value": wb.B * wb.L / (msc * 1e-3), "unit": "tokens/s", "ms_per_call": msc,
+                "launches_per_call": 5 + (mb != "lit") + (mb == "d"),
+                "roofline": {"bound": "alu", "achieved": flc / (msc * 1e-3) / 1e12, "peak": FP32_ALU_PEAK_TFLOPS,
+                             "unit": "TFLOP/s", "frac": flc / (msc * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
+                             "algorithmic_flops": flc}})
+        backward = dict(backward or {}, chunkwise=chunk_lines)
 
     reordered = None
     if not args.no_reordered and w.L <= lion.FULL_MAX_L and w.d in (64, 128):

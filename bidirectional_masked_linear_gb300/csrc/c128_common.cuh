@@ -59,6 +59,18 @@ __device__ __forceinline__ uint4 bf8_to_h8(uint4 v) {
   unpack8_bf(v, x);
   return pack8_h(x);
 }
+constexpr float kF16Max = 65504.f;   // the largest fp16
+// The same, raising `flag` (the CTA's range flag in shared memory) when a
+// value lies past the fp16 range: it would become an infinity in the tile.
+__device__ __forceinline__ uint4 bf8_to_h8_chk(uint4 v, volatile int* flag) {
+  float x[8];
+  unpack8_bf(v, x);
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e]));
+  if (!(m <= kF16Max)) *flag = 1;
+  return pack8_h(x);
+}
 
 // packed two-lane fp32 arithmetic (one instruction for both lanes)
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {

@@ -91,6 +91,7 @@ const char* lion_status_string(lion_status s) {
     case LION_ERR_CUDA: return "CUDA error";
     case LION_ERR_NO_MEMORY: return "out of device memory";
     case LION_ERR_TIMEOUT: return "device-side wait timed out";
+    case LION_ERR_RANGE: return "a value exceeded the fp16 range of the tensor-core path";
   }
   return "unknown status";
 }
@@ -114,7 +115,13 @@ size_t lion_attn_bwd_workspace_bytes(int B, int H, int L, int d) {
   return lion::bwd_workspace_bytes(B, H, L, d);
 }
 
-lion_status lion_attn_bwd(const lion_bwd_args* a) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks shared by the two gradient entry points (everything but
+// the length limit and the workspace size).
+lion_status validate_bwd(const lion_bwd_args* a) {
   if (!a) return LION_ERR_INVALID_ARG;
   if (!a->q || !a->k || !a->v || !a->dy || !a->dq || !a->dk || !a->dv) return LION_ERR_INVALID_ARG;
   if (a->B < 1 || a->H < 1 || a->L < 1 || !valid_d(a->d)) return LION_ERR_INVALID_ARG;
@@ -131,8 +138,13 @@ lion_status lion_attn_bwd(const lion_bwd_args* a) {
        !device_accessible(a->dlog_lambda)))
     return LION_ERR_INVALID_ARG;
   if (a->workspace && (!aligned(a->workspace, 256) || !device_accessible(a->workspace))) return LION_ERR_INVALID_ARG;
-  if (a->L > LION_FULL_MAX_L) return LION_ERR_UNSUPPORTED;
-  const size_t need = lion::bwd_workspace_bytes(a->B, a->H, a->L, a->d);
+  return LION_OK;
+}
+
+// The gradients through the form `chunkwise` selects, on checked arguments.
+lion_status run_bwd(const lion_bwd_args* a, bool chunkwise) {
+  const size_t need = chunkwise ? lion::bwd_chunk_workspace_bytes(a->B, a->H, a->L, a->d)
+                                : lion::bwd_workspace_bytes(a->B, a->H, a->L, a->d);
   if (a->workspace && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
   Problem p;
   p.q = a->q;
@@ -159,12 +171,39 @@ lion_status lion_attn_bwd(const lion_bwd_args* a) {
     }
     owned = true;
   }
-  cudaError_t e = lion::launch_bwd(p, a->dy, a->dq, a->dk, a->dv, a->dlog_lambda, ws, s);
+  cudaError_t e = chunkwise ? lion::launch_bwd_chunk(p, a->dy, a->dq, a->dk, a->dv, a->dlog_lambda, ws, s)
+                            : lion::launch_bwd(p, a->dy, a->dq, a->dk, a->dv, a->dlog_lambda, ws, s);
   if (owned) {
     cudaError_t f = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = f;
   }
   return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+lion_status lion_attn_bwd(const lion_bwd_args* a) {
+  const lion_status st = validate_bwd(a);
+  if (st != LION_OK) return st;
+  if (a->L > LION_FULL_MAX_L) return LION_ERR_UNSUPPORTED;
+  return run_bwd(a, false);
+}
+
+lion_status lion_attn_bwd_chunk(const lion_bwd_args* a) {
+  const lion_status st = validate_bwd(a);
+  if (st != LION_OK) return st;
+  // one CTA per (head, chunk) on one grid axis
+  const long long chunks = ((long long)a->L + lion::bwd_chunk_length(a->d) - 1) / lion::bwd_chunk_length(a->d);
+  if ((long long)a->B * a->H * chunks > 0x7fffffffLL || (long long)a->B * a->H * 1024 > 0x7fffffffLL)
+    return LION_ERR_UNSUPPORTED;
+  return run_bwd(a, true);
+}
+
+size_t lion_attn_bwd_chunk_workspace_bytes(int B, int H, int L, int d) {
+  if (B < 1 || H < 1 || L < 1 || !valid_d(d)) return 0;
+  return lion::bwd_chunk_workspace_bytes(B, H, L, d);
 }
 
 lion_status lion_attn_fwd_ex(const lion_args* a) {
@@ -270,7 +309,9 @@ lion_status lion_sync_status(cudaStream_t stream) {
   if (v != 0) {
     const int zero = 0;
     if (cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return LION_ERR_CUDA;
-    return v == lion::kStatusBadOrder ? LION_ERR_INVALID_ARG : LION_ERR_TIMEOUT;
+    return v == lion::kStatusBadOrder ? LION_ERR_INVALID_ARG
+           : v == lion::kStatusRange  ? LION_ERR_RANGE
+                                      : LION_ERR_TIMEOUT;
   }
   return LION_OK;
 }

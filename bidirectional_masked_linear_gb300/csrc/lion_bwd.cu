@@ -798,6 +798,25 @@ size_t stored_bytes(size_t BH, int L) {
 
 }  // namespace
 
+cudaError_t launch_dlog_lambda(int B, int H, int L, int mask_kind, const float* rowd, const float* cold, double* dsum,
+                               float* dll, cudaStream_t s) {
+  if (mask_kind == MASK_LIT) return cudaSuccess;
+  BwdParams p = {};
+  p.B = B;
+  p.H = H;
+  p.L = L;
+  p.mask_kind = mask_kind;
+  p.rowd = const_cast<float*>(rowd);
+  p.cold = const_cast<float*>(cold);
+  p.dsum = dsum;
+  p.dll = dll;
+  bwd_dl_kernel<<<B * H, kDlThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || mask_kind != MASK_D) return e;
+  bwd_dl_heads_kernel<<<(H + 127) / 128, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 size_t bwd_workspace_bytes(int B, int H, int L, int d) {
   const size_t BH = (size_t)B * H, n = BH * L;
   return 3 * align256(sizeof(float) * n * d) + 4 * align256(sizeof(float) * n) + align256(sizeof(double) * BH) +

@@ -74,7 +74,10 @@
 // accumulation; phi(K), phi(Q), the weighted phi(K), V, P and the two
 // states (with their z) are each rounded once to fp16, and the decay-scaled
 // phi(q) (rows that do not fold) twice.
-// Precondition: |phi(q)|, |phi(k)|, |v| and the states below 65504.
+// Precondition: |phi(q)|, |phi(k)|, |v| and the states below 65504.  A v past
+// that range (checked as prep converts it), or a non-finite row sum (an
+// infinite feature or score reached the row), sets the CTA's range flag,
+// which the kernel reports in `status` as kStatusRange at exit.
 //
 // Every mbarrier wait is bounded; on timeout the kernel records an error in
 // `status`, waits (bounded) for its own copies and MMAs in flight, releases
@@ -100,7 +103,6 @@ constexpr int kStTile = kStRows * 128;  // K-major 16-bit state tile
 constexpr int kPrepWarps = 16, kEpiWarps = 8;
 constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
 constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
-constexpr long long kWaitCycles = 2000000000LL;       // ~1 s at 2 GHz
 constexpr float kFoldMinSigma = 1.f / 32768.f;        // rows that fold 1/sigma into P
 constexpr uint32_t kSleepNs = 2000u;
 
@@ -159,6 +161,7 @@ struct C128Params {
   int BH, H, L;
   int out_bf16;   // 1: y stored as bfloat16 (one 64-column store per warp)
   int* status;
+  long long wait_cycles;   // bound of every mbarrier wait, in clock cycles
 };
 
 template <int MASK>
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 8);
+  volatile int* s_range = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 12);
   auto Qt = [&](int s, int c) { return smem + OFF_Q + (2 * s + c) * kTile; };
   auto Vt = [&](int s, int c) { return smem + OFF_V + (2 * s + c) * kTile; };
   auto Kt = [&](int c) { return smem + OFF_K + c * kTile; };
@@ -202,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mapO);
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b, nch));
     *s_abort = 0;
+    *s_range = 0;
     fence_mbar_init();
   }
   // the ones tile: 16 rows of the normaliser atom, 1 at column 0
@@ -218,17 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // bounded wait; after any timeout every later wait returns false at once
   auto waitb = [&](int b, uint32_t parity) -> bool {
-    if (*s_abort) return false;
-    if (mbar_try_wait(&bars[b], parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait_sleep(&bars[b], parity, kSleepNs)) {
-      if (*s_abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        *s_abort = 1;
-        return false;
-      }
-    }
-    return true;
+    return mbar_wait_or_abort(&bars[b], parity, prm.wait_cycles, kSleepNs, s_abort);
   };
   const int nheads = prm.BH > (int)blockIdx.x ? (prm.BH - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   auto head_of = [&](int n) { return (int)blockIdx.x + n * (int)gridDim.x; };
@@ -273,12 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           idle0 = clock64();
         } else {
           __nanosleep(64);
-          if (clock64() - idle0 > kWaitCycles) *s_abort = 1;
+          if (clock64() - idle0 > prm.wait_cycles) *s_abort = 1;
         }
       }
       if (*s_abort) {
         // let the copies already issued land before the CTA lets go of its memory
-        const long long lim = kWaitCycles / 4;
+        const long long lim = prm.wait_cycles / 4;
         for (int s = 0; s < 2; ++s) {
           const int v_is = (nv - s + 1) / 2, q_is = (nq - s + 1) / 2;   // loads issued into slot s
           if (v_is) mbar_wait(&bars[B_V0 + s], (v_is - 1) & 1, lim);
@@ -358,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*s_abort && issued) {
         mma_commit(&bars[B_DRAIN]);
-        mbar_wait(&bars[B_DRAIN], 0, kWaitCycles / 4);
+        mbar_wait(&bars[B_DRAIN], 0, prm.wait_cycles / 4);
       }
     }
   } else if (warp < W_EPI) {
@@ -417,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint4* a = reinterpret_cast<uint4*>(vt + sw128_offset(r, j0 + j));
-          *a = bf8_to_h8(*a);
+          *a = bf8_to_h8_chk(*a, s_range);
         }
       }
       // ---- K: phi(k) in place; the decay-weighted copy for the state MMA
@@ -646,6 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence16(ob0);
         reg_fence16(ob1);
         const float inv = 1.f / ob1[0];
+        // a score past the fp16 range (unbounded features) leaves the row sum
+        // non-finite: fp16 operands cannot make an fp32 sum overflow otherwise
+        if (row_ok && !(fabsf(ob1[0]) <= 3.0e38f)) *s_range = 1;
         const float2 inv2 = make_float2(inv, inv);
         uint8_t* row = stg + lane * 128;
         if (prm.out_bf16) {
@@ -728,7 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (tid == 0 && *s_abort) atomicExch(prm.status, 1);
+  if (tid == 0 && *s_abort) atomicExch(prm.status, kStatusTimeout);
+  if (tid == 0 && !*s_abort && *s_range) atomicExch(prm.status, kStatusRange);
   if (warp == W_TMA) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -755,6 +754,7 @@ cudaError_t launch_chunk128_tc(const Problem& p, int* status, cudaStream_t s) {
   prm.L = p.L;
   prm.out_bf16 = p.out_bf16;
   prm.status = status;
+  prm.wait_cycles = wait_limit_cycles();
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, C128Params) = nullptr;
 #define LION_C128_CASE(M, F) \
   if (p.mask_kind == M && p.phi == F) kern = lion_chunk128_tc_kernel<M, F>;

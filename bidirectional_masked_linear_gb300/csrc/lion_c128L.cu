@@ -68,7 +68,6 @@ constexpr int kStTile = kStRows * 128;
 constexpr int kPrepWarps = 16, kEpiWarps = 8;
 constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
 constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
-constexpr long long kWaitCycles = 2000000000LL;       // ~1 s at 2 GHz
 constexpr uint32_t kSleepNs = 2000u;
 constexpr int kGsegBytes = 64 * kLongStateCols * 4;  // one fp32 [64][80] state
 
@@ -142,6 +141,7 @@ struct LongParams {
   const float* segin;
   int out_bf16;   // 1: y stored as bfloat16 (64-byte staging rows)
   int* status;
+  long long wait_cycles;   // bound of every mbarrier wait, in clock cycles
 };
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 8);
+  volatile int* s_range = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 12);
   auto Qt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes; };
   auto Kt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes + kTile; };
   auto Vt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes + 2 * kTile; };
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mapO);
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b));
     *s_abort = 0;
+    *s_range = 0;
     fence_mbar_init();
   }
   for (int x = tid; x < 16 * 8; x += kThreads) {
@@ -233,17 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tslot;
 
   auto waitb = [&](int b, uint32_t parity) -> bool {
-    if (*s_abort) return false;
-    if (mbar_try_wait(&bars[b], parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait_sleep(&bars[b], parity, kSleepNs)) {
-      if (*s_abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        *s_abort = 1;
-        return false;
-      }
-    }
-    return true;
+    return mbar_wait_or_abort(&bars[b], parity, prm.wait_cycles, kSleepNs, s_abort);
   };
   auto nk_of = [&](int c) { return (min(kC, L - kC * c) + 15) >> 4; };
   // pre-pass state at the right edge of chunk c
@@ -307,11 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           idle0 = clock64();
         } else {
           __nanosleep(64);
-          if (clock64() - idle0 > kWaitCycles) *s_abort = 1;
+          if (clock64() - idle0 > prm.wait_cycles) *s_abort = 1;
         }
       }
       if (*s_abort) {
-        const long long lim = kWaitCycles / 4;
+        const long long lim = prm.wait_cycles / 4;
         for (int s = 0; s < 2; ++s)
           if (issued_ld[s]) mbar_wait(&bars[B_LD0 + s], (issued_ld[s] - 1) & 1, lim);
         if (ng) mbar_wait(&bars[B_GS], (ng - 1) & 1, lim);
@@ -388,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*s_abort && issued) {
         mma_commit(&bars[B_DRAIN]);
-        mbar_wait(&bars[B_DRAIN], 0, kWaitCycles / 4);
+        mbar_wait(&bars[B_DRAIN], 0, prm.wait_cycles / 4);
       }
     }
   } else if (warp < W_EPI) {
@@ -469,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint4* a = reinterpret_cast<uint4*>(vt + sw128_offset(t, j0 + j));
-          *a = bf8_to_h8(*a);
+          *a = bf8_to_h8_chk(*a, s_range);
         }
       }
       // ---- phi(k) in place and its weighted copy w_j phi(k_j), w_j = exp(p_e - p_j)
@@ -736,7 +728,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             z[2] = tmem_ld1(base + T_R + 64);
             tmem_wait_ld();
             asm volatile("" : "+f"(z[0]), "+f"(z[1]), "+f"(z[2]));
-            const float inv = 1.f / (z[0] + a_out * z[1] + b_out * z[2]);
+            const float den = z[0] + a_out * z[1] + b_out * z[2];
+            const float inv = 1.f / den;
+            // a score past the fp16 range (unbounded features) leaves the row sum
+            // non-finite: fp16 operands cannot make an fp32 sum overflow otherwise
+            if (!(fabsf(den) <= 3.0e38f)) *s_range = 1;
             inv2 = make_float2(inv, inv);
           } else {
             tmem_wait_ld();
@@ -787,7 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (tid == 0 && *s_abort) atomicExch(prm.status, 1);
+  if (tid == 0 && *s_abort) atomicExch(prm.status, kStatusTimeout);
+  if (tid == 0 && !*s_abort && *s_range) atomicExch(prm.status, kStatusRange);
   if (warp == W_TMA) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -848,6 +845,7 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   prm.segsum = segsum;
   prm.segin = segin;
   prm.status = status;
+  prm.wait_cycles = wait_limit_cycles();
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, LongParams) = nullptr;
 #define LION_C128L_CASE(M, F) \
   if (p.mask_kind == M && p.phi == F) kern = lion_chunk128_long_kernel<M, F>;

@@ -57,7 +57,6 @@ using namespace c128;
 constexpr int kPrepWarps = 16, kEpiWarps = 8;
 constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
 constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
-constexpr long long kWaitCycles = 2000000000LL;       // ~1 s at 2 GHz
 constexpr uint32_t kSleepNs = 2000u;
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -107,6 +106,7 @@ struct PreParams {
   uint8_t* gst;     // [BH][chunks] kGstBytes each
   float* segsum;    // [BH][nseg] kSegSumFloats each
   int* status;
+  long long wait_cycles;   // bound of every mbarrier wait, in clock cycles
 };
 
 template <int MASK>
@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 8);
+  volatile int* s_range = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 12);
   auto Kt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes; };
   auto Vt = [&](int s) { return smem + OFF_SLOT + s * kSlotBytes + kTile; };
   uint8_t* KBt = smem + OFF_KB;
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mapV);
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b));
     *s_abort = 0;
+    *s_range = 0;
     fence_mbar_init();
   }
   for (int x = tid; x < 16 * 8; x += kThreads) {
@@ -176,17 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tslot;
 
   auto waitb = [&](int b, uint32_t parity) -> bool {
-    if (*s_abort) return false;
-    if (mbar_try_wait(&bars[b], parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait_sleep(&bars[b], parity, kSleepNs)) {
-      if (*s_abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        *s_abort = 1;
-        return false;
-      }
-    }
-    return true;
+    return mbar_wait_or_abort(&bars[b], parity, prm.wait_cycles, kSleepNs, s_abort);
   };
   auto nk_of = [&](int c) { return (min(kC, L - kC * c) + 15) >> 4; };
 
@@ -223,11 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           idle0 = clock64();
         } else {
           __nanosleep(64);
-          if (clock64() - idle0 > kWaitCycles) *s_abort = 1;
+          if (clock64() - idle0 > prm.wait_cycles) *s_abort = 1;
         }
       }
       if (*s_abort) {
-        const long long lim = kWaitCycles / 4;
+        const long long lim = prm.wait_cycles / 4;
         for (int s = 0; s < 2; ++s)
           if (issued[s]) mbar_wait(&bars[B_LD0 + s], (issued[s] - 1) & 1, lim);
       }
@@ -265,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*s_abort && issued) {
         mma_commit(&bars[B_DRAIN]);
-        mbar_wait(&bars[B_DRAIN], 0, kWaitCycles / 4);
+        mbar_wait(&bars[B_DRAIN], 0, prm.wait_cycles / 4);
       }
     }
   } else if (warp < W_EPI) {
@@ -334,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint4* a = reinterpret_cast<uint4*>(vt + sw128_offset(t, j0 + j));
-          *a = bf8_to_h8(*a);
+          *a = bf8_to_h8_chk(*a, s_range);
         }
       }
       // ---- phi(k); the weighted copies once the previous chunk's MMAs read them
@@ -484,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (tid == 0 && *s_abort) atomicExch(prm.status, 1);
+  if (tid == 0 && *s_abort) atomicExch(prm.status, kStatusTimeout);
+  if (tid == 0 && !*s_abort && *s_range) atomicExch(prm.status, kStatusRange);
   if (warp == W_TMA) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -510,6 +503,7 @@ cudaError_t launch_chunk128_pre(const Problem& p, const LongPlan& plan, uint8_t*
   prm.gst = gst;
   prm.segsum = segsum;
   prm.status = status;
+  prm.wait_cycles = wait_limit_cycles();
   void (*kern)(const CUtensorMap, const CUtensorMap, PreParams) = nullptr;
 #define LION_C128P_CASE(M, F) \
   if (p.mask_kind == M && p.phi == F) kern = lion_chunk128_pre_kernel<M, F>;

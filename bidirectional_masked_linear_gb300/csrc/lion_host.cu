@@ -13,6 +13,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/lion.h"
 #include "host_plan.h"
 #include "lion_common.cuh"
@@ -49,6 +51,37 @@ lion_status validate_host(const lion_host_args* a) {
   if (a->mask_kind != LION_MASK_LIT && !host_memory(a->log_lambda)) return LION_ERR_INVALID_ARG;
   if (a->form == LION_FORM_FULL && a->L > LION_FULL_MAX_L) return LION_ERR_UNSUPPORTED;
   return LION_OK;
+}
+
+// The two copy streams and the call's events, created once per device and
+// reused by every call on it.  A call holds the device's lock while it
+// enqueues its work, so calls from several host threads take turns; a reused
+// event is recorded again only after the earlier call's waits on it were
+// enqueued, which is all that stream ordering needs.
+struct CopyEngine {
+  std::mutex m;
+  bool ready = false;
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t ev[9] = {};   // start, in[2], comp[2], freed[2], done_in, done_out
+};
+constexpr int kMaxDevices = 64;
+CopyEngine g_engines[kMaxDevices];
+
+// Creates the device's streams and events on first use (lock held).
+cudaError_t engine_ready(CopyEngine& ce) {
+  if (ce.ready) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(&ce.copy_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ce.copy_out, cudaStreamNonBlocking);
+  for (int i = 0; i < 9 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ce.ev[i], cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    for (cudaEvent_t& ev : ce.ev)
+      if (ev) cudaEventDestroy(ev), ev = nullptr;
+    if (ce.copy_in) cudaStreamDestroy(ce.copy_in), ce.copy_in = nullptr;
+    if (ce.copy_out) cudaStreamDestroy(ce.copy_out), ce.copy_out = nullptr;
+    return e;
+  }
+  ce.ready = true;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -104,20 +137,25 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
   float* ll_fixed = reinterpret_cast<float*>(base + 2 * set_bytes);
   void* ws = base + 2 * set_bytes + align256(fixed ? sizeof(float) * H : 0);
 
-  cudaStream_t copy_in = nullptr, copy_out = nullptr;
-  cudaEvent_t start = nullptr, in[2] = {nullptr, nullptr}, comp[2] = {nullptr, nullptr},
-              freed[2] = {nullptr, nullptr};
   lion_status result = LION_OK;
   auto fail = [&](cudaError_t err) {
     if (result == LION_OK) result = err == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
   };
-  if ((e = cudaStreamCreateWithFlags(&copy_in, cudaStreamNonBlocking)) != cudaSuccess ||
-      (e = cudaStreamCreateWithFlags(&copy_out, cudaStreamNonBlocking)) != cudaSuccess)
-    fail(e);
-  cudaEvent_t* evs[] = {&start, &in[0], &in[1], &comp[0], &comp[1], &freed[0], &freed[1]};
-  for (cudaEvent_t* ev : evs)
-    if (result == LION_OK && (e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) fail(e);
-  if (result == LION_OK) {
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaFreeAsync(base, s);
+    return LION_ERR_CUDA;
+  }
+  CopyEngine& ce = g_engines[dev];
+  std::lock_guard<std::mutex> lock(ce.m);
+  if ((e = engine_ready(ce)) != cudaSuccess) {
+    cudaFreeAsync(base, s);
+    return e == cudaErrorMemoryAllocation ? LION_ERR_NO_MEMORY : LION_ERR_CUDA;
+  }
+  cudaStream_t copy_in = ce.copy_in, copy_out = ce.copy_out;
+  cudaEvent_t start = ce.ev[0], in[2] = {ce.ev[1], ce.ev[2]}, comp[2] = {ce.ev[3], ce.ev[4]},
+              freed[2] = {ce.ev[5], ce.ev[6]};
+  {
     // the copies start after the caller's earlier work on its stream
     if ((e = cudaEventRecord(start, s)) != cudaSuccess || (e = cudaStreamWaitEvent(copy_in, start, 0)) != cudaSuccess)
       fail(e);
@@ -187,28 +225,17 @@ lion_status lion_attn_fwd_host(const lion_host_args* a) {
   }
   // the caller's stream resumes after the last copies; the buffers are freed
   // in its order after them
-  if (copy_in && copy_out && start) {
-    cudaEvent_t done_in = nullptr, done_out = nullptr;
-    if (cudaEventCreateWithFlags(&done_in, cudaEventDisableTiming) == cudaSuccess &&
-        cudaEventCreateWithFlags(&done_out, cudaEventDisableTiming) == cudaSuccess) {
-      cudaEventRecord(done_in, copy_in);
-      cudaEventRecord(done_out, copy_out);
-      cudaStreamWaitEvent(s, done_in, 0);
-      cudaStreamWaitEvent(s, done_out, 0);
-    } else {
+  {
+    cudaEvent_t done_in = ce.ev[7], done_out = ce.ev[8];
+    if (cudaEventRecord(done_in, copy_in) != cudaSuccess || cudaEventRecord(done_out, copy_out) != cudaSuccess ||
+        cudaStreamWaitEvent(s, done_in, 0) != cudaSuccess || cudaStreamWaitEvent(s, done_out, 0) != cudaSuccess) {
       cudaGetLastError();
       cudaStreamSynchronize(copy_in);
       cudaStreamSynchronize(copy_out);
       fail(cudaErrorUnknown);
     }
-    if (done_in) cudaEventDestroy(done_in);
-    if (done_out) cudaEventDestroy(done_out);
   }
   cudaFreeAsync(base, s);
-  for (cudaEvent_t* ev : evs)
-    if (*ev) cudaEventDestroy(*ev);
-  if (copy_in) cudaStreamDestroy(copy_in);
-  if (copy_out) cudaStreamDestroy(copy_out);
   if (result == LION_OK && cudaGetLastError() != cudaSuccess) result = LION_ERR_CUDA;
   return result;
 }

@@ -97,6 +97,22 @@ size_t bwd_workspace_bytes(int B, int H, int L, int d);
 cudaError_t launch_bwd(const Problem& p, const float* dy, float* dq, float* dk, float* dv, float* dll, void* ws,
                        cudaStream_t s);
 
+// dlog_lambda from the row and column terms of dLoss/dP ([B*H][L] each):
+// LION-S the suffix sums (position 0: 0), LION-D the position-weighted sum
+// per head (dsum, [B*H] doubles) and then over the batch; LIT nothing.
+cudaError_t launch_dlog_lambda(int B, int H, int L, int mask_kind, const float* rowd, const float* cold, double* dsum,
+                               float* dll, cudaStream_t s);
+
+// Gradients through the chunkwise form (fp32, CUDA cores), any L: chunks of
+// bwd_chunk_length(d) tokens, states scanned across chunks; outputs as
+// launch_bwd; workspace of bwd_chunk_workspace_bytes; bwd_chunk_launches
+// kernels a call.
+int bwd_chunk_length(int d);
+size_t bwd_chunk_workspace_bytes(int B, int H, int L, int d);
+int bwd_chunk_launches(int mask_kind);
+cudaError_t launch_bwd_chunk(const Problem& p, const float* dy, float* dq, float* dk, float* dv, float* dll, void* ws,
+                             cudaStream_t s);
+
 // Full form with the mask averaged over two traversal orders (order: device
 // int32 [2][L]); fp32 on the CUDA cores, d in {64, 128}; workspace of
 // reorder_workspace_bytes; reorder_launches kernels a call.
@@ -113,12 +129,18 @@ cudaError_t launch_reordered_bwd(const Problem& p, const int* order, const float
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream_t s);
 
 // Device-side status word that kernels set when a bounded wait gives up
-// (kStatusTimeout) or a traversal order is not a permutation
-// (kStatusBadOrder); address on the current device, nullptr if it cannot be
-// resolved.
+// (kStatusTimeout), a traversal order is not a permutation
+// (kStatusBadOrder), or a tensor-core kernel met a value that its fp16
+// operands cannot hold (kStatusRange); address on the current device,
+// nullptr if it cannot be resolved.
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusBadOrder = 2;
+constexpr int kStatusRange = 3;   // a value past the fp16 range of a tensor-core operand
 int* device_status_ptr();
+
+// Bound, in SM clock cycles, on every mbarrier wait of the tensor-core
+// kernels (a launch parameter; lion_debug_set_wait_cycles changes it).
+long long wait_limit_cycles();
 
 // Largest chunk the SIMT chunk kernel takes (its chunk-local prefix lives in
 // shared memory).

@@ -9,11 +9,7 @@
 // Transformer and infers like an RNN"):
 //   full_simt_kernel   Theorem 3.3 Eq 25, Y = SCALE(QK^T (.) M) V, with the
 //                      mask value generated per (i, j) -- never stored.
-//   rnn_simt_kernel    Theorem 3.3 Eq 20-24: forward recurrence storing only
-//                      y^F_i (in the output buffer) and c^F_i (workspace),
-//                      then the backward recurrence combining both and
-//                      removing the diagonal once (reply "1: Recurrence
-//                      Form", O(Ld + L) side storage).
+//   (the recurrent form, Theorem 3.3 Eq 20-24, is in lion_rnn.cu)
 //   chunk_simt_kernel  chunkwise form ("LION Part IV - Results", "LION
 //                      Chunk"): a right-to-left sweep applies the backward
 //                      chunk state, then a left-to-right sweep adds the
@@ -145,124 +141,7 @@ __global__ void __launch_bounds__(256) full_simt_kernel(Problem p) {
   }
 }
 
-// ------------------------------------------------------------------- RNN --
-constexpr int kRnnSplit = 4;   // threads sharing one column of the state
-constexpr int kRnnTile = 32;   // tokens staged per shared-memory tile
-
-template <typename T, int D>
-__global__ void __launch_bounds__(D * kRnnSplit) rnn_simt_kernel(Problem p, float* cF_all) {
-  constexpr int MS = D / kRnnSplit;
-  extern __shared__ float smem[];
-  float* sQ = smem;                      // [kRnnTile][D]
-  float* sK = sQ + kRnnTile * D;
-  float* sV = sK + kRnnTile * D;
-  float* sLam = sV + kRnnTile * D;       // [kRnnTile]
-  const int L = p.L, H = p.H, bh = blockIdx.x, h = bh % H;
-  const int n = threadIdx.x / kRnnSplit, r = threadIdx.x % kRnnSplit;
-  const T* q = head_ptr<T>(p.q, bh, L, D);
-  const T* k = head_ptr<T>(p.k, bh, L, D);
-  const T* v = head_ptr<T>(p.v, bh, L, D);
-  float* out = p.out + (size_t)bh * L * D;
-  float* cF = cF_all + (size_t)bh * L;
-  const float* ll = p.mask_kind == MASK_S ? p.log_lambda + (size_t)bh * L : nullptr;
-  const float lh = p.mask_kind == MASK_D ? p.log_lambda[h] : 0.f;
-
-  float S[MS], z[MS];
-#pragma unroll
-  for (int a = 0; a < MS; ++a) { S[a] = 0.f; z[a] = 0.f; }
-
-  // forward: S^F_i = lambda_i S^F_{i-1} + phi(k_i) v_i^T
-  for (int t0 = 0; t0 < L; t0 += kRnnTile) {
-    const int nt = min(kRnnTile, L - t0);
-    load_rows<T>(sQ, D, q, t0, kRnnTile, L, D);
-    load_rows<T>(sK, D, k, t0, kRnnTile, L, D);
-    load_rows<T>(sV, D, v, t0, kRnnTile, L, D);
-    for (int tt = threadIdx.x; tt < kRnnTile; tt += blockDim.x) {
-      const int i = t0 + tt;
-      float l = 0.f;
-      if (i < L) l = p.mask_kind == MASK_S ? ll[i] : lh;
-      sLam[tt] = expf(l);
-    }
-    __syncthreads();
-    phi_rows_inplace(sQ, kRnnTile, nt, D, D, p.phi);
-    phi_rows_inplace(sK, kRnnTile, nt, D, D, p.phi);
-    __syncthreads();
-    for (int tt = 0; tt < nt; ++tt) {
-      const float lam = sLam[tt], vn = sV[tt * D + n];
-      float y = 0.f, c = 0.f;
-#pragma unroll
-      for (int a = 0; a < MS; ++a) {
-        const int m = r * MS + a;
-        const float fk = sK[tt * D + m], fq = sQ[tt * D + m];
-        S[a] = lam * S[a] + fk * vn;
-        z[a] = lam * z[a] + fk;
-        y += fq * S[a];
-        c += fq * z[a];
-      }
-      y += __shfl_xor_sync(0xffffffffu, y, 1);
-      y += __shfl_xor_sync(0xffffffffu, y, 2);
-      c += __shfl_xor_sync(0xffffffffu, c, 1);
-      c += __shfl_xor_sync(0xffffffffu, c, 2);
-      if (r == 0) {
-        if (p.causal) {
-          out[(size_t)(t0 + tt) * D + n] = y / c;   // the forward half is the whole result
-        } else {
-          out[(size_t)(t0 + tt) * D + n] = y;
-          if (n == 0) cF[t0 + tt] = c;
-        }
-      }
-    }
-    __syncthreads();
-  }
-  if (p.causal) return;
-#pragma unroll
-  for (int a = 0; a < MS; ++a) { S[a] = 0.f; z[a] = 0.f; }
-
-  // backward: S^B_i = lambda_{i+1} S^B_{i+1} + phi(k_i) v_i^T, combined with
-  // the stored forward half, diagonal term removed once.
-  for (int t0 = ((L - 1) / kRnnTile) * kRnnTile; t0 >= 0; t0 -= kRnnTile) {
-    const int nt = min(kRnnTile, L - t0);
-    load_rows<T>(sQ, D, q, t0, kRnnTile, L, D);
-    load_rows<T>(sK, D, k, t0, kRnnTile, L, D);
-    load_rows<T>(sV, D, v, t0, kRnnTile, L, D);
-    for (int tt = threadIdx.x; tt < kRnnTile; tt += blockDim.x) {
-      const int i1 = t0 + tt + 1;
-      float lam = 0.f;
-      if (i1 < L) lam = expf(p.mask_kind == MASK_S ? ll[i1] : lh);
-      sLam[tt] = lam;
-    }
-    __syncthreads();
-    phi_rows_inplace(sQ, kRnnTile, nt, D, D, p.phi);
-    phi_rows_inplace(sK, kRnnTile, nt, D, D, p.phi);
-    __syncthreads();
-    for (int tt = nt - 1; tt >= 0; --tt) {
-      const float lam = sLam[tt], vn = sV[tt * D + n];
-      float y = 0.f, c = 0.f, sii = 0.f;
-#pragma unroll
-      for (int a = 0; a < MS; ++a) {
-        const int m = r * MS + a;
-        const float fk = sK[tt * D + m], fq = sQ[tt * D + m];
-        S[a] = lam * S[a] + fk * vn;
-        z[a] = lam * z[a] + fk;
-        y += fq * S[a];
-        c += fq * z[a];
-        sii += fq * fk;
-      }
-      y += __shfl_xor_sync(0xffffffffu, y, 1);
-      y += __shfl_xor_sync(0xffffffffu, y, 2);
-      c += __shfl_xor_sync(0xffffffffu, c, 1);
-      c += __shfl_xor_sync(0xffffffffu, c, 2);
-      sii += __shfl_xor_sync(0xffffffffu, sii, 1);
-      sii += __shfl_xor_sync(0xffffffffu, sii, 2);
-      if (r == 0) {
-        const int i = t0 + tt;
-        const float yF = out[(size_t)i * D + n];
-        out[(size_t)i * D + n] = (yF + y - sii * vn) / (cF[i] + c - sii);
-      }
-    }
-    __syncthreads();
-  }
-}
+constexpr int kRnnSplit = 4;   // threads sharing one column of the state (rnn_step_kernel)
 
 // ----------------------------------------------------------------- CHUNK --
 constexpr int kPanel = 32;      // tokens per shared-memory panel
@@ -494,16 +373,6 @@ cudaError_t full_launch(const Problem& p, cudaStream_t s) {
 }
 
 template <typename T, int D>
-cudaError_t rnn_launch(const Problem& p, float* ws, cudaStream_t s) {
-  size_t smem = sizeof(float) * (3 * kRnnTile * D + kRnnTile);
-  auto kern = rnn_simt_kernel<T, D>;
-  cudaError_t e = allow_smem(kern, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<p.B * p.H, D * kRnnSplit, smem, s>>>(p, ws);
-  return cudaGetLastError();
-}
-
-template <typename T, int D>
 cudaError_t chunk_launch(const Problem& p, float* ws, cudaStream_t s) {
   constexpr int W = D + 1;
   size_t smem = sizeof(float) * ((size_t)kPanel * (D + 8) + 2 * kPanel * D + kPanel * (kPanel + 1) +
@@ -529,9 +398,6 @@ cudaError_t dispatch(const Problem& p, A... args) {
 
 template <typename T, int D> struct FullF {
   static cudaError_t run(const Problem& p, cudaStream_t s) { return full_launch<T, D>(p, s); }
-};
-template <typename T, int D> struct RnnF {
-  static cudaError_t run(const Problem& p, float* ws, cudaStream_t s) { return rnn_launch<T, D>(p, ws, s); }
 };
 template <typename T, int D> struct ChunkF {
   static cudaError_t run(const Problem& p, float* ws, cudaStream_t s) { return chunk_launch<T, D>(p, ws, s); }
@@ -572,7 +438,6 @@ cudaError_t launch_f32_to_bf16(const float* src, void* dst, size_t n, cudaStream
 }
 
 cudaError_t launch_full_simt(const Problem& p, cudaStream_t s) { return dispatch<FullF>(p, s); }
-cudaError_t launch_rnn_simt(const Problem& p, float* ws, cudaStream_t s) { return dispatch<RnnF>(p, ws, s); }
 cudaError_t launch_chunk_simt(const Problem& p, float* ws, cudaStream_t s) { return dispatch<ChunkF>(p, ws, s); }
 
 cudaError_t launch_rnn_step(const void* q, const void* k, const void* v, const float* ll,

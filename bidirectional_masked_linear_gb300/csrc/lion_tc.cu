@@ -29,7 +29,9 @@
 // block boundary states exchanged through global memory for long sequences.
 // (One bf16 rounding of the unit-norm SiLU features costs ~5e-3 relative
 // error; fp16 stays within about half of the 2e-3 budget.)  Precondition:
-// |phi(q)|, |phi(k)|, |v| and the chunk states below the fp16 range (65504).
+// |phi(q)|, |phi(k)|, |v| and the chunk states below the fp16 range (65504);
+// a v past it, or a non-finite row sum, is reported in `status` as
+// kStatusRange.
 //
 // Work split.  Persistent CTAs (one per SM) walk work items.  An item is a
 // segment of one head: up to SEGB consecutive 256-token blocks.  Warp 16
@@ -82,7 +84,6 @@ constexpr int kWorkerWarps = 16;  // CUDA-core stages
 constexpr int kThreads = (kWorkerWarps + 1) * 32;  // + one TMA/MMA issuer warp
 constexpr int kTile = kC * 128;   // bytes of one 64-row x 64-element 16-bit swizzled tile
 constexpr int kQSlots = 4;
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 constexpr uint32_t kSleepNs = 20000u;            // longest sleep inside one try_wait
 constexpr float kMaxFactorRange = 80.f;          // exp(80) stays finite in fp32
 constexpr int kStateCols = 80;                   // global state rows: 64 values, z, padding
@@ -158,6 +159,7 @@ struct TcParams {
   float* segsum;       // [BH][nseg] segment summaries (pre-pass output)
   const float* segin;  // [BH][nseg] states entering each segment (scan output)
   int* status;
+  long long wait_cycles;   // bound of every mbarrier wait, in clock cycles
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -186,6 +188,16 @@ __device__ __forceinline__ uint4* chunk16(uint8_t* tile, int r, int c8) {
 }
 __device__ __forceinline__ __half* elem16(uint8_t* tile, int r, int col) {
   return reinterpret_cast<__half*>(tile + sw128_offset(r, col >> 3) + ((col & 7) << 1));
+}
+
+// Raises `flag` (the CTA's range flag in shared memory) when one of n fp32
+// values about to become an fp16 operand lies past the fp16 range (65504).
+template <int N>
+__device__ __forceinline__ void check_f16(const float* x, volatile int* flag) {
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < N; ++e) m = fmaxf(m, fabsf(x[e]));
+  if (!(m <= 65504.f)) *flag = 1;
 }
 
 // phi on 8 features of one row; the row's 8 owners are lanes l..l+7 (xor 1,2,4).
@@ -272,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 8);
+  volatile int* s_range = reinterpret_cast<volatile int*>(smem + OFF_TSLOT + 12);
   auto Kt = [&](int c) { return smem + OFF_K + c * kTile; };
   auto Vt = [&](int c) { return smem + OFF_V + c * kTile; };
   auto Wt = [&](int i) { return sWork + i * kTile; };
@@ -288,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (MODE == MODE_MAIN) prefetch_tmap(&mapQ);
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], bar_count(b));
     *s_abort = 0;
+    *s_range = 0;
     fence_mbar_init();
   }
   for (int x = tid; x < kC * 8; x += kThreads) {
@@ -302,17 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // bounded wait on a barrier phase; any timeout makes every later wait return at once
   auto waitb = [&](int b, uint32_t parity) -> bool {
-    if (*s_abort) return false;
-    if (mbar_try_wait(&bars[b], parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait_sleep(&bars[b], parity, kSleepNs)) {
-      if (*s_abort) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        *s_abort = 1;
-        return false;
-      }
-    }
-    return true;
+    return mbar_wait_or_abort(&bars[b], parity, prm.wait_cycles, kSleepNs, s_abort);
   };
 
   if (warp == kWorkerWarps) {
@@ -604,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float v8[8];
           unpack8_bf(*reinterpret_cast<const uint4*>(vp), v8);
+          check_f16<8>(v8, s_range);
           *reinterpret_cast<uint4*>(vp) = pack8_h(v8);
         } else if (MASK != MASK_LIT) {
           // K and V rows past the sequence arrived as zeros (bf16 0 == fp16 0);
@@ -869,6 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               float den = half ? dI1 : dI0;
               if (hasF) den += a * (half ? dF1 : dF0);
               if (hasG) den += bb * (half ? dG1 : dG0);
+              // a score past the fp16 range (unbounded features) leaves the row
+              // sum non-finite: fp16 operands cannot make an fp32 sum overflow
+              if (!(fabsf(den) <= 3.0e38f)) *s_range = 1;
               const float inv = 1.f / den;
               float y[4];
 #pragma unroll
@@ -910,7 +918,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
-  if (tid == 0 && *s_abort) atomicExch(prm.status, 1);
+  if (tid == 0 && *s_abort) atomicExch(prm.status, kStatusTimeout);
+  if (tid == 0 && !*s_abort && *s_range) atomicExch(prm.status, kStatusRange);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -1120,6 +1129,7 @@ cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_
   prm.segsum = nullptr;
   prm.segin = nullptr;
   prm.status = status;
+  prm.wait_cycles = wait_limit_cycles();
   const int items = BH * t.nseg;
   const int grid = items < num_sms() ? items : num_sms();
   if (t.NBL > 1) {

@@ -63,6 +63,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return true;
 }
 
+// The bounded wait of every warp-specialised kernel: wait for phase `parity`
+// of `bar`, sleeping up to `sleep_ns` inside each try; give up (false) at once
+// if the CTA's shared abort flag is set, or after `limit` SM clock cycles,
+// setting the flag so that every other wait of the CTA gives up too.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
+                                                   uint32_t sleep_ns, volatile int* abort) {
+  if (*abort) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity, sleep_ns)) {
+    if (*abort) return false;
+    if (clock64() - t0 > limit) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------- TMA --
 // 3-D tiled load global -> shared, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liblion.so")
 
 # enums of include/lion.h
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT, ERR_RANGE = range(7)
 MASK_LIT, MASK_D, MASK_S = 0, 1, 2
 FORM_FULL, FORM_RNN, FORM_CHUNK = 0, 1, 2
 DTYPE_BF16, DTYPE_FP32 = 0, 1
@@ -100,7 +100,9 @@ EXPORTS = ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_attn_workspace_bytes", "li
            "lion_status_string", "lion_abi_version", "lion_sync_status",
            "lion_attn_fwd_rnn_noalloc", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
            "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes",
-           "lion_attn_fwd_host", "lion_attn_bwd_reordered", "lion_attn_reordered_bwd_workspace_bytes")
+           "lion_attn_fwd_host", "lion_attn_bwd_reordered", "lion_attn_reordered_bwd_workspace_bytes",
+           "lion_attn_bwd_chunk", "lion_attn_bwd_chunk_workspace_bytes", "lion_debug_set_wait_cycles",
+           "lion_debug_wait_timeout")
 NOALLOC_MAX_HEAD_TOKENS = 1 << 20
 
 
@@ -136,6 +138,14 @@ def load(path: str = LIB_PATH):
     lib.lion_attn_bwd.restype = i
     lib.lion_attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.lion_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.lion_debug_set_wait_cycles.argtypes = [ctypes.c_longlong]
+    lib.lion_debug_set_wait_cycles.restype = i
+    lib.lion_debug_wait_timeout.argtypes = [vp]
+    lib.lion_debug_wait_timeout.restype = i
+    lib.lion_attn_bwd_chunk.argtypes = [ctypes.POINTER(_BwdArgs)]
+    lib.lion_attn_bwd_chunk.restype = i
+    lib.lion_attn_bwd_chunk_workspace_bytes.argtypes = [i, i, i, i]
+    lib.lion_attn_bwd_chunk_workspace_bytes.restype = ctypes.c_size_t
     lib.lion_attn_fwd_reordered.argtypes = [ctypes.POINTER(_ReorderArgs)]
     lib.lion_attn_fwd_reordered.restype = i
     lib.lion_attn_reordered_workspace_bytes.argtypes = [i, i, i, i]
@@ -179,7 +189,8 @@ def _dtype_code(t: torch.Tensor) -> int:
 def sync_status(stream=None) -> int:
     """Synchronise the stream and return the library's device status (OK;
     ERR_TIMEOUT if a kernel gave up on a bounded wait; ERR_INVALID_ARG if a
-    traversal order given to attn_fwd_reordered was not a permutation)."""
+    traversal order given to attn_fwd_reordered was not a permutation;
+    ERR_RANGE if a tensor-core kernel met a value past the fp16 range)."""
     return int(load().lion_sync_status(_stream_handle(stream)))
 
 
@@ -265,15 +276,18 @@ def rnn_step(q, k, v, log_lambda, S, z, y_part, c_part, mask_kind, stream=None):
     return y_part, c_part
 
 
-def bwd_workspace_bytes(B, H, L, d) -> int:
+def bwd_workspace_bytes(B, H, L, d, form=FORM_FULL) -> int:
+    if form == FORM_CHUNK:
+        return int(load().lion_attn_bwd_chunk_workspace_bytes(B, H, L, d))
     return int(load().lion_attn_bwd_workspace_bytes(B, H, L, d))
 
 
-def attn_bwd(q, k, v, log_lambda, dy, mask_kind, phi=PHI_DEFAULT, workspace=None, stream=None):
+def attn_bwd(q, k, v, log_lambda, dy, mask_kind, phi=PHI_DEFAULT, workspace=None, stream=None, form=FORM_FULL):
     """Gradients of a loss through Y = SCALE((phi(Q) phi(K)^T (.) M) V), given
     ``dy`` = dLoss/dY ([B, H, L, d] float32).  Returns ``(dq, dk, dv,
     dlog_lambda)`` as float32 tensors; ``dlog_lambda`` is None for LIT, [H]
-    for D and [B, H, L] for S."""
+    for D and [B, H, L] for S.  ``form``: FORM_FULL (lion_attn_bwd, L <=
+    FULL_MAX_L) or FORM_CHUNK (lion_attn_bwd_chunk, any L)."""
     lib = load()
     if isinstance(mask_kind, str):
         mask_kind = MASKS[mask_kind]
@@ -296,14 +310,20 @@ def attn_bwd(q, k, v, log_lambda, dy, mask_kind, phi=PHI_DEFAULT, workspace=None
                  _ptr(dll), B, H, L, d, mask_kind, dt, phi, _ptr(workspace),
                  0 if workspace is None else workspace.numel() * workspace.element_size(),
                  _stream_handle(stream))
-    _check(lib.lion_attn_bwd(ctypes.byref(a)))
+    if isinstance(form, str):
+        form = FORMS[form]
+    if form not in (FORM_FULL, FORM_CHUNK):
+        raise ValueError("the gradients run through the full or the chunkwise form")
+    entry = lib.lion_attn_bwd_chunk if form == FORM_CHUNK else lib.lion_attn_bwd
+    _check(entry(ctypes.byref(a)))
     return dq, dk, dv, dll
 
 
 class LionAttention(torch.autograd.Function):
     """Y = SCALE((phi(Q) phi(K)^T (.) M) V) as a differentiable op: the
     forward runs the library's forward in the given form, the backward its
-    gradient kernels (the forms agree, so the gradient is the same)."""
+    gradient kernels (the forms agree, so the gradient is the same): the
+    full form up to FULL_MAX_L tokens, the chunkwise form beyond."""
 
     @staticmethod
     def forward(ctx, q, k, v, log_lambda, mask_kind, form=FORM_CHUNK, chunk=128, phi=PHI_DEFAULT):
@@ -314,7 +334,9 @@ class LionAttention(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy):
         q, k, v, log_lambda = ctx.saved_tensors
-        dq, dk, dv, dll = attn_bwd(q, k, v, log_lambda, dy.contiguous().float(), ctx.mask_kind, ctx.phi)
+        form = FORM_FULL if q.shape[2] <= FULL_MAX_L else FORM_CHUNK
+        dq, dk, dv, dll = attn_bwd(q, k, v, log_lambda, dy.contiguous().float(), ctx.mask_kind, ctx.phi,
+                                   form=form)
         return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype),
                 None if log_lambda is None else dll, None, None, None, None)
 

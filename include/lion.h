@@ -63,7 +63,12 @@ typedef enum {
   LION_ERR_UNSUPPORTED = 2,  /* valid request this build does not handle   */
   LION_ERR_CUDA = 3,         /* a CUDA call or kernel launch failed        */
   LION_ERR_NO_MEMORY = 4,    /* workspace allocation failed                */
-  LION_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up         */
+  LION_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up         */
+  LION_ERR_RANGE = 6         /* a value exceeded the fp16 range (65504) of a
+                                tensor-core operand: v, or (seen through a
+                                non-finite row sum) unbounded features or a
+                                masked score; the output of that call is not
+                                valid                                        */
 } lion_status;
 
 typedef enum { LION_MASK_LIT = 0, LION_MASK_D = 1, LION_MASK_S = 2 } lion_mask_kind;
@@ -174,8 +179,11 @@ lion_status lion_rnn_step(const void* q, const void* k, const void* v,
 /*
  * lion_sync_status -- synchronise `stream`, then report whether any kernel
  * of this library on the current device gave up on a bounded device-side
- * wait since the last call (LION_ERR_TIMEOUT), or was given a traversal order
- * that is not a permutation (LION_ERR_INVALID_ARG); the flag is then cleared.
+ * wait since the last call (LION_ERR_TIMEOUT), was given a traversal order
+ * that is not a permutation (LION_ERR_INVALID_ARG), or, on the tensor-core
+ * chunk path, met a value its fp16 operands cannot hold (LION_ERR_RANGE: use
+ * LION_DTYPE_FP32, or a chunk length the CUDA cores take); the flag is then
+ * cleared.
  * Kernels never spin unboundedly: a wait that runs out records the error,
  * releases its tensor memory and returns.  LION_ERR_CUDA if the
  * synchronisation itself fails.
@@ -253,6 +261,26 @@ lion_status lion_attn_bwd(const lion_bwd_args* a);
 
 /* Workspace bytes lion_attn_bwd needs for this problem. */
 size_t lion_attn_bwd_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * lion_attn_bwd_chunk -- the same gradients as lion_attn_bwd through the
+ * chunkwise form, for any L (the forms agree, Theorem 3.3; "LION Part IV -
+ * Results", "LION Chunk").  Each gradient is a product of the masked
+ * structure the forward scans: inside chunks of 64 tokens (32 at d = 128) the
+ * masked score and dA tiles, across chunks the forward and backward states of
+ * phi(k) [v; 1]^T and of phi(q) G^T (G_i = [dy_i / den_i ; -(dy_i . y_i) /
+ * den_i]), each a d x (d + 1) fp32 matrix per chunk, carried by scans as in
+ * Theorem 3.3 Eq 20-24.  dlog_lambda from the row and column terms as in
+ * lion_attn_bwd.
+ *   Arguments, layouts and errors as lion_attn_bwd, without its length limit.
+ *   Computed in fp32 on the CUDA cores, O(L d^2 + L C d) per head.  Workspace
+ *   as returned by lion_attn_bwd_chunk_workspace_bytes (about 2 (d + 4)^2 / C
+ *   + d + 7 floats per head-token; NULL: stream-ordered allocation).
+ */
+lion_status lion_attn_bwd_chunk(const lion_bwd_args* a);
+
+/* Workspace bytes lion_attn_bwd_chunk needs for this problem (0 if invalid). */
+size_t lion_attn_bwd_chunk_workspace_bytes(int B, int H, int L, int d);
 
 /*
  * lion_attn_fwd_host -- lion_attn_fwd_ex on inputs and output in host memory.
@@ -370,6 +398,24 @@ lion_status lion_attn_bwd_reordered(const lion_reorder_bwd_args* a);
 
 /* Workspace bytes lion_attn_bwd_reordered needs (0 if d is not 64 or 128). */
 size_t lion_attn_reordered_bwd_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * Testing aids for the bound on device-side waits (no counterpart in the
+ * pages; not needed in normal use).
+ * lion_debug_set_wait_cycles -- the bound, in SM clock cycles, on every
+ *   mbarrier wait of the tensor-core kernels launched after the call
+ *   (process-wide).  0 restores the default of 2e9 cycles (about 1 s);
+ *   negative values return LION_ERR_INVALID_ARG.  A bound far below a
+ *   kernel's normal waits makes it give up and report LION_ERR_TIMEOUT.
+ * lion_debug_wait_timeout -- launches one warp on `stream` that waits, with
+ *   that bound, on an mbarrier that nothing arrives at, through the same
+ *   wait the kernels use.  No copy and no matrix product is in flight in it:
+ *   the wait gives up, the kernel records the timeout and returns, and the
+ *   next lion_sync_status returns LION_ERR_TIMEOUT (clearing the flag).
+ *   With the default bound the call lasts about a second.
+ */
+lion_status lion_debug_set_wait_cycles(long long cycles);
+lion_status lion_debug_wait_timeout(cudaStream_t stream);
 
 /* Static, human-readable text for a status. */
 const char* lion_status_string(lion_status s);

@@ -30,7 +30,8 @@ def test_header_declares_the_abi():
     for want in ("lion_attn_fwd", "lion_attn_fwd_ex", "lion_rnn_step", "lion_status_string",
                  "lion_attn_workspace_bytes", "lion_attn_bwd", "lion_attn_bwd_workspace_bytes",
                  "lion_attn_fwd_causal", "lion_attn_fwd_reordered", "lion_attn_reordered_workspace_bytes",
-                 "lion_attn_bwd_reordered", "lion_attn_reordered_bwd_workspace_bytes", "lion_attn_fwd_host"):
+                 "lion_attn_bwd_reordered", "lion_attn_reordered_bwd_workspace_bytes", "lion_attn_fwd_host",
+                 "lion_attn_bwd_chunk", "lion_attn_bwd_chunk_workspace_bytes"):
         assert want in names
 
 
@@ -177,6 +178,28 @@ def test_bwd_invalid_arguments_rejected_before_launch(lib, kw):
     lib.lion_attn_bwd.argtypes = [ctypes.POINTER(lion._BwdArgs)]
     assert _bwd(lib, **kw) == 1
     assert lib.lion_attn_bwd(None) == 1
+    # the chunkwise gradients share the checks
+    f = dict(q=4096, k=8192, v=12288, log_lambda=0, dy=16384, dq=20480, dk=24576, dv=28672,
+             dlog_lambda=0, B=1, H=1, L=8, d=64, mask_kind=0, dtype=0, phi=0, workspace=0,
+             workspace_bytes=0, stream=0)
+    f.update(kw)
+    assert lib.lion_attn_bwd_chunk(ctypes.byref(lion._BwdArgs(**f))) == 1
+    assert lib.lion_attn_bwd_chunk(None) == 1
+
+
+def test_bwd_chunk_workspace_query(lib):
+    from bidirectional_masked_linear_gb300 import lion
+    # per chunk of 64 tokens two (d+4)^2 states and its total; per token G
+    # (d + 4 floats) and two terms; a double per head
+    B, H, L, d = 2, 3, 200, 64
+    need = lion.bwd_workspace_bytes(B, H, L, d, lion.FORM_CHUNK)
+    N = (L + 63) // 64
+    assert need >= B * H * (N * (2 * 68 * 68 + 1) * 4 + L * (68 + 2) * 4 + 8)
+    assert lion.bwd_workspace_bytes(B, H, 100000, d, lion.FORM_CHUNK) > need
+    assert lion.bwd_workspace_bytes(0, 3, 10, 64, lion.FORM_CHUNK) == 0
+    assert lion.bwd_workspace_bytes(1, 1, 10, 48, lion.FORM_CHUNK) == 0
+    # chunks of 32 at d = 128
+    assert lion.bwd_workspace_bytes(1, 1, 64, 128, lion.FORM_CHUNK) >= 2 * (2 * 132 * 132) * 4
 
 
 def _fwd(lib, q=1, k=1, v=1, ll=None, B=1, H=1, L=8, d=64, mask=0, form=2, chunk=64, out=1):
@@ -290,3 +313,11 @@ def test_header_is_plain_c(tmp_path):
     want = [ctypes.sizeof(lion._Args), ctypes.sizeof(lion._BwdArgs), ctypes.sizeof(lion._ReorderArgs),
             ctypes.sizeof(lion._ReorderBwdArgs), ctypes.sizeof(lion._HostArgs), lion._Args.out_bf16.offset]
     assert sizes == want
+
+
+def test_wait_bound_setter(lib):
+    """The bound on device-side waits: negative values are refused, 0 restores
+    the default; no launch is involved."""
+    assert lib.lion_debug_set_wait_cycles(-1) == 1
+    assert lib.lion_debug_set_wait_cycles(100000) == 0
+    assert lib.lion_debug_set_wait_cycles(0) == 0

@@ -392,7 +392,7 @@ def _bwd_check(oracle_mod, B, H, L, d, mask, dtype, phi=0, seed=0, positive=Fals
     return got
 
 
-def _grad_rows(ref, got, label):
+def _grad_rows(ref, got, label, tol=TOL_BWD, tol_dll=None):
     """Per row (one token's d gradient entries of dq, dk, dv; one entry of
     dlog_lambda) the error relative to that row's own scale, with a floor of
     1e-3 of the tensor's largest entry for rows whose gradient cancels to
@@ -421,7 +421,8 @@ def _grad_rows(ref, got, label):
             den = np.maximum(suffix.reshape(-1), floor)
         err = np.abs(xx - rr).max(axis=1) / den
         worst[name] = float(err.max())
-        assert worst[name] <= TOL_BWD, (label, name, worst[name], int(np.argmax(err)))
+        lim = tol_dll if (name == "dlog_lambda" and tol_dll is not None) else tol
+        assert worst[name] <= lim, (label, name, worst[name], int(np.argmax(err)))
     STATS.append((label, {f"worst {k} row err": v for k, v in worst.items()}))
 
 
