@@ -57,7 +57,18 @@ _CALL_KERNELS = {
 }
 # (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
 # write) of one launch, from one ncu capture of that kernel
-TRAFFIC_PER_HEAD = {}
+TRAFFIC_PER_HEAD = {
+    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.5 MB written
+    ("lion_chunk128_tc_kernel", "4714b04341152b44a6e77620be92b69188a89821e7ff31dcf31c3da088bf9d3e",
+     "vit_b", "s", 128): (117487104 + 36458240) / 1536,
+    # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the three launches of a call
+    ("lion_chunk128_pre_kernel", "9dc968e12456057e91acf188c514a6c666ec3436efb9613eafbe26e4f4f51fe9",
+     "hires_2496", "s", 128): (152065536 + 22592256) / 24,
+    ("lion_segment_scan_kernel", "854d0aae925c16c75ee9ec0c10566dbdf687c95c0d95be815082bc6c8564e31f",
+     "hires_2496", "s", 128): (5927936 + 0) / 24,
+    ("lion_chunk128_long_kernel", "21c67ce1f16cafde5a26baf936897e415f3ba832994a70b5f681f719df45893d",
+     "hires_2496", "s", 128): (271416064 + 111205632) / 24,
+}
 
 
 def _sources_sha(files):

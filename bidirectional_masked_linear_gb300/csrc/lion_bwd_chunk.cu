@@ -24,7 +24,7 @@
 // column terms phi(k_m) against the strict phi(q)G-states applied to
 // [v_m; 1].
 //
-// Chunks of CB tokens (64; 32 at d = 128).  For chunk c starting at s with
+// Chunks of CB tokens (64; 32 at d = 128).  512 threads a CTA.  For chunk c starting at s with
 // local inclusive prefix p_t = sum_{u=s}^{t} l_u and total T = p_e:
 //   forward summary  U^F_c = sum_{j in c} exp(T - p_j) x_j w_j^T
 //   backward summary U^B_c = sum_{j in c} exp(p_j) x_j w_j^T
@@ -49,7 +49,7 @@
 namespace lion {
 namespace {
 
-constexpr int kThreads = 256;   // 16 x 16 thread grid for the block products
+constexpr int kThreads = 512;   // 32 x 16 thread grid for the block products
 
 template <int D>
 struct Cfg {
@@ -81,9 +81,10 @@ struct BcParams {
 // ---------------------------------------------------------------- products
 // Out[a][b] = sum_{k<K} X[a*ldx + k] Y[b*ldy + k] for a < MA, b < NB (the
 // "dot" form: the contraction index is contiguous in both operands).  Thread
-// (ti, tj) = (t / 16, t % 16) holds a = a0 + ti + 16 alpha, b = b0 + tj + 16 beta
-// of each 64 x 64 block and reads float4 along k; K % 4 == 0, ld % 4 == 0.
-// epi(a, b, value) receives every valid output exactly once.
+// (ti, tj) = (t / 16, t % 16) holds a = a0 + ti + 32 alpha (alpha < 2),
+// b = b0 + tj + 16 beta (beta < 4) of each 64 x 64 block and reads float4
+// along k; K % 4 == 0, ld % 4 == 0.  epi(a, b, value) receives every valid
+// output exactly once.
 template <typename Epi>
 __device__ __forceinline__ void mm_dot(const float* X, int ldx, const float* Y, int ldy, int MA, int NB, int K,
                                        Epi epi) {
@@ -91,27 +92,25 @@ __device__ __forceinline__ void mm_dot(const float* X, int ldx, const float* Y, 
   for (int a0 = 0; a0 < MA; a0 += 64) {
     for (int b0 = 0; b0 < NB; b0 += 64) {
       if (a0 + ti >= MA || b0 + tj >= NB) continue;
-      float acc[4][4];
+      float acc[2][4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
-      const float* xr[4];
+      const float* xr[2];
       const float* yr[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        xr[u] = X + (size_t)min(a0 + ti + 16 * u, MA - 1) * ldx;
-        yr[u] = Y + (size_t)min(b0 + tj + 16 * u, NB - 1) * ldy;
-      }
+      for (int u = 0; u < 2; ++u) xr[u] = X + (size_t)min(a0 + ti + 32 * u, MA - 1) * ldx;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) yr[u] = Y + (size_t)min(b0 + tj + 16 * u, NB - 1) * ldy;
       for (int k = 0; k < K; k += 4) {
-        float4 xv[4], yv[4];
+        float4 xv[2], yv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          xv[u] = *reinterpret_cast<const float4*>(xr[u] + k);
-          yv[u] = *reinterpret_cast<const float4*>(yr[u] + k);
-        }
+        for (int u = 0; u < 2; ++u) xv[u] = *reinterpret_cast<const float4*>(xr[u] + k);
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
+        for (int u = 0; u < 4; ++u) yv[u] = *reinterpret_cast<const float4*>(yr[u] + k);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
             acc[x][y] = fmaf(xv[x].x, yv[y].x, acc[x][y]);
@@ -121,10 +120,10 @@ __device__ __forceinline__ void mm_dot(const float* X, int ldx, const float* Y, 
           }
       }
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
-          const int a = a0 + ti + 16 * x, b = b0 + tj + 16 * y;
+          const int a = a0 + ti + 32 * x, b = b0 + tj + 16 * y;
           if (a < MA && b < NB) epi(a, b, acc[x][y]);
         }
     }
@@ -133,37 +132,37 @@ __device__ __forceinline__ void mm_dot(const float* X, int ldx, const float* Y, 
 
 // Out[a][b] = sum_{k<K} w_k X[k*ldx + a] Y[k*ldy + b] (the "outer" form: the
 // contraction index is the row of both operands; w == nullptr means 1).
-// Thread (ta, tb) holds the contiguous a = a0 + 4 ta + alpha, b = b0 + 4 tb +
-// beta; MA and NB are multiples of 4.
+// Thread (ta, tb) holds the contiguous a = a0 + 2 ta + alpha (alpha < 2),
+// b = b0 + 4 tb + beta (beta < 4); MA is even and NB a multiple of 4.
 template <typename Epi>
 __device__ __forceinline__ void mm_outer(const float* X, int ldx, const float* Y, int ldy, const float* w, int MA,
                                          int NB, int K, Epi epi) {
   const int ta = threadIdx.x >> 4, tb = threadIdx.x & 15;
   for (int a0 = 0; a0 < MA; a0 += 64) {
     for (int b0 = 0; b0 < NB; b0 += 64) {
-      const int a = a0 + 4 * ta, b = b0 + 4 * tb;
+      const int a = a0 + 2 * ta, b = b0 + 4 * tb;
       if (a >= MA || b >= NB) continue;
-      float acc[4][4];
+      float acc[2][4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
 #pragma unroll 4
       for (int k = 0; k < K; ++k) {
-        float4 xv = *reinterpret_cast<const float4*>(X + (size_t)k * ldx + a);
+        float2 xv = *reinterpret_cast<const float2*>(X + (size_t)k * ldx + a);
         const float4 yv = *reinterpret_cast<const float4*>(Y + (size_t)k * ldy + b);
         if (w) {
           const float wk = w[k];
-          xv = make_float4(xv.x * wk, xv.y * wk, xv.z * wk, xv.w * wk);
+          xv = make_float2(xv.x * wk, xv.y * wk);
         }
-        const float xs[4] = {xv.x, xv.y, xv.z, xv.w}, ys[4] = {yv.x, yv.y, yv.z, yv.w};
+        const float xs[2] = {xv.x, xv.y}, ys[4] = {yv.x, yv.y, yv.z, yv.w};
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
+        for (int x = 0; x < 2; ++x)
 #pragma unroll
           for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(xs[x], ys[y], acc[x][y]);
       }
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int y = 0; y < 4; ++y) epi(a + x, b + y, acc[x][y]);
     }
@@ -434,21 +433,21 @@ __global__ void __launch_bounds__(kThreads) bwc_rows_kernel(BcParams p) {
   // dA_ij = G_i . [v_j; 1]: the masked copy for dphi(q), and the row terms
   // sum_{j<i} c_ij - sum_{j>i} c_ij, c_ij = A_ij dA_ij
   {
-    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    float part[2] = {0.f, 0.f};
     const int ti = threadIdx.x >> 4;
     mm_dot(Gb, LDT, Vb, LDT, CB, CB, LDT, [&](int i, int j, float da) {
       const float a = At[j * LDC + i];
       Dt[j * LDC + i] = (i < len && j < len) ? da * expf(-fabsf(sp[i] - sp[j])) : 0.f;
       const float cij = a * da;
-      part[(i - ti) >> 4] += j < i ? cij : j > i ? -cij : 0.f;
+      part[(i - ti) >> 5] += j < i ? cij : j > i ? -cij : 0.f;
     });
-    // the 16 lanes with the same ti hold rows ti + 16 alpha
+    // the 16 lanes with the same ti hold rows ti + 32 alpha
 #pragma unroll
-    for (int x = 0; x < 4; ++x) part[x] = group_sum<16>(part[x]);
+    for (int x = 0; x < 2; ++x) part[x] = group_sum<16>(part[x]);
     if ((threadIdx.x & 15) == 0)
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
-        if (ti + 16 * x < CB) rowt[ti + 16 * x] += part[x];
+      for (int x = 0; x < 2; ++x)
+        if (ti + 32 * x < CB) rowt[ti + 32 * x] += part[x];
   }
   __syncthreads();
   // dphi(q_i) = sum_j M_ij dA_ij phi(k_j), then the states' parts; the row
@@ -460,21 +459,21 @@ __global__ void __launch_bounds__(kThreads) bwc_rows_kernel(BcParams p) {
     __syncthreads();
     const float* w = dir == 0 ? wl : wr;
     const float sgn = dir == 0 ? 1.f : -1.f;
-    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    float part[2] = {0.f, 0.f};
     const int ta = threadIdx.x >> 4;
     mm_outer(Gt, LDC, St, LDT, nullptr, CB, D, C::SR, [&](int i, int m, float val) {
       const float x = w[i] * val;
       Dq[i * LDT + m] += x;
-      part[i & 3] += Qf[i * LDT + m] * x;
+      part[i & 1] += Qf[i * LDT + m] * x;
     });
-    // lanes with the same ta share rows 4 ta .. 4 ta + 3 (per 64-column block
-    // a lane adds once per block, so the sums below cover every column)
+    // lanes with the same ta share rows 2 ta, 2 ta + 1 (per 64-column block a
+    // lane adds once per block, so the sums below cover every column)
 #pragma unroll
-    for (int x = 0; x < 4; ++x) part[x] = group_sum<16>(part[x]);
+    for (int x = 0; x < 2; ++x) part[x] = group_sum<16>(part[x]);
     if ((threadIdx.x & 15) == 0)
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
-        if (4 * ta + x < CB) rowt[4 * ta + x] += sgn * part[x];
+      for (int x = 0; x < 2; ++x)
+        if (2 * ta + x < CB) rowt[2 * ta + x] += sgn * part[x];
   }
   __syncthreads();
   // the phi(q) G^T summaries over this chunk's (consumed) states
@@ -529,7 +528,7 @@ __global__ void __launch_bounds__(kThreads) bwc_cols_kernel(BcParams p) {
   float* wl = sp + 64;             // [CB]
   float* wr = wl + CB;             // [CB]
   float* colt = wr + CB;           // [CB]
-  float* cpart = colt + CB;        // [8][CB] per-warp column sums
+  float* cpart = colt + CB;        // [warps][CB] per-warp column sums
   const int c = (int)(blockIdx.x % (unsigned)p.N), bh = (int)(blockIdx.x / (unsigned)p.N), L = p.L;
   const int s = c * CB, len = min(CB, L - s);
   const size_t tok0 = (size_t)bh * L + s;
@@ -573,7 +572,7 @@ __global__ void __launch_bounds__(kThreads) bwc_cols_kernel(BcParams p) {
       const float cij = Am[i * LDC + j] * da;
       part[(j - tj) >> 4] += i < j ? cij : i > j ? -cij : 0.f;
     });
-    // lanes tj and tj + 16 of a warp share columns; the 8 warps' sums are
+    // lanes tj and tj + 16 of a warp share columns; the warps' sums are
     // added in warp order (deterministic)
 #pragma unroll
     for (int x = 0; x < 4; ++x) part[x] += __shfl_xor_sync(0xffffffffu, part[x], 16);
@@ -598,19 +597,19 @@ __global__ void __launch_bounds__(kThreads) bwc_cols_kernel(BcParams p) {
     __syncthreads();
     const float* w = dir == 0 ? wl : wr;
     const float sgn = dir == 0 ? 1.f : -1.f;
-    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    float part[2] = {0.f, 0.f};
     const int ta = threadIdx.x >> 4;
     mm_outer(Vt, LDC, St, LDT, nullptr, CB, D, C::SR, [&](int j, int m, float val) {
       const float x = w[j] * val;
       Dk[j * LDT + m] += x;
-      part[j & 3] += Kf[j * LDT + m] * x;
+      part[j & 1] += Kf[j * LDT + m] * x;
     });
 #pragma unroll
-    for (int x = 0; x < 4; ++x) part[x] = group_sum<16>(part[x]);
+    for (int x = 0; x < 2; ++x) part[x] = group_sum<16>(part[x]);
     if ((threadIdx.x & 15) == 0)
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
-        if (4 * ta + x < CB) colt[4 * ta + x] += sgn * part[x];
+      for (int x = 0; x < 2; ++x)
+        if (2 * ta + x < CB) colt[2 * ta + x] += sgn * part[x];
     __syncthreads();
     mm_dot(Kf, LDT, St, LDT, CB, D, D, [&](int j, int n, float val) { Dv[j * LDT + n] += w[j] * val; });
   }

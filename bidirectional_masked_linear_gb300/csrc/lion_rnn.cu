@@ -14,10 +14,12 @@
 // Columns of the state are independent recurrences: column n of S follows
 // v_n, and z is the column of a constant 1.  So each CTA runs the whole
 // sequence for 8 columns of one head plus z, and a head's d columns spread
-// over d / 8 CTAs (24 heads at L = 24,337 fill 192 CTAs at d = 64).  Every
-// CTA of a head computes z, so each has the normaliser it divides by without
-// waiting for another; they all store the same c^F_i (the same arithmetic on
-// the same inputs).
+// over d / 8 CTAs.  Every CTA of a head computes z, so each has the
+// normaliser it divides by without waiting for another; they all store the
+// same c^F_i (the same arithmetic on the same inputs).  Every CTA of a head
+// also computes phi of the whole tile, so splitting a head finer (4 columns
+// a CTA when the heads are few) made the feature map, not the recurrence,
+// the larger share of each CTA's work and the form slower.
 //
 // Inside a CTA a warp holds four state columns, eight lanes a column and
 // d / 8 rows of it per lane, in registers.  A token costs each lane its rows'
@@ -33,16 +35,23 @@
 namespace lion {
 namespace {
 
-constexpr int kCols = 8;                                    // columns of v per CTA
 constexpr int kSlots = 4;                                   // state columns per warp
 constexpr int kG = 32 / kSlots;                             // lanes per column
-constexpr int kWarps = (kCols + 1 + kSlots - 1) / kSlots;   // the columns and z
-constexpr int kThr = 32 * kWarps;
 constexpr int kTile = 32;                                   // tokens per staged tile
+// NC columns of v per CTA: NC + 1 state columns with z, four a warp
+template <int NC>
+struct Cols {
+  static constexpr int kWarps = (NC + 1 + kSlots - 1) / kSlots;
+  static constexpr int kThr = 32 * kWarps;
+};
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(dst);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -50,23 +59,26 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <typename T, int D>
+template <typename T, int D, int NC>
 struct Lay {
   static constexpr int kRawQ = kTile * D * (int)sizeof(T);      // bytes of a raw q (or k) tile
-  static constexpr int kRawV = kTile * kCols * (int)sizeof(T);  // the CTA's columns of v
-  static constexpr int kRaw = 2 * kRawQ + kRawV;                // one raw slot
-  static constexpr int kF32 = (2 * kTile * D + kTile * kCols + 3 * kTile) * 4;
+  static constexpr int kRawV = kTile * NC * (int)sizeof(T);     // the CTA's columns of v
+  static constexpr int kRaw = 2 * kRawQ + ((kRawV + 15) & ~15); // one raw slot
+  static constexpr int kF32 = (2 * kTile * D + kTile * NC + 3 * kTile) * 4;
   static constexpr int kBytes = 2 * kRaw + kF32;
 };
 
 // Issue the copies of tile [t0, t0 + nt) of q, k and the CTA's v columns into
 // raw slot `dst` (one commit group).
-template <typename T, int D>
+template <typename T, int D, int NC>
 __device__ __forceinline__ void issue_tile(uint8_t* dst, const T* q, const T* k, const T* v, int n0, int t0,
                                            int nt) {
-  using Y = Lay<T, D>;
+  using Y = Lay<T, D, NC>;
+  constexpr int kThr = Cols<NC>::kThr;
   constexpr int kRowChunks = D * (int)sizeof(T) / 16;       // 16-byte pieces of a q row
-  constexpr int kVChunks = kCols * (int)sizeof(T) / 16;     // of the CTA's v columns in a row
+  constexpr int kVBytes = NC * (int)sizeof(T);              // the CTA's v columns in a row
+  constexpr int kVPiece = kVBytes < 16 ? kVBytes : 16;      // 8 (four bf16 columns) or 16
+  constexpr int kVChunks = kVBytes / kVPiece;
   for (int x = threadIdx.x; x < 2 * nt * kRowChunks; x += kThr) {
     const int which = x / (nt * kRowChunks), r = (x / kRowChunks) % nt, c = x % kRowChunks;
     const T* src = (which == 0 ? q : k) + (size_t)(t0 + r) * D + c * (16 / (int)sizeof(T));
@@ -74,24 +86,28 @@ __device__ __forceinline__ void issue_tile(uint8_t* dst, const T* q, const T* k,
   }
   for (int x = threadIdx.x; x < nt * kVChunks; x += kThr) {
     const int r = x / kVChunks, c = x % kVChunks;
-    cp_async16(dst + 2 * Y::kRawQ + r * kCols * (int)sizeof(T) + 16 * c,
-               v + (size_t)(t0 + r) * D + n0 + c * (16 / (int)sizeof(T)));
+    uint8_t* to = dst + 2 * Y::kRawQ + r * kVBytes + kVPiece * c;
+    const T* from = v + (size_t)(t0 + r) * D + n0 + c * (kVPiece / (int)sizeof(T));
+    if constexpr (kVPiece == 16) cp_async16(to, from);
+    else cp_async8(to, from);
   }
   cp_commit();
 }
 
 // phi of one raw row's PER features held by this lane; the row's other
 // features sit in the 7 lanes next to it (xor 1, 2, 4).
+// (The fast exponential and division err by a few ulp, far below what the
+// fp32 recurrence itself accumulates.)
 template <int PER>
 __device__ __forceinline__ void phi_lane(float* x, int phi) {
   if (phi == PHI_ELU1) {
 #pragma unroll
-    for (int e = 0; e < PER; ++e) x[e] = elu1(x[e]);
+    for (int e = 0; e < PER; ++e) x[e] = x[e] > 0.f ? x[e] + 1.f : __expf(x[e]);
   } else if (phi == PHI_SILU_L2) {
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-      x[e] = silu(x[e]);
+      x[e] = __fdividef(x[e], 1.f + __expf(-x[e]));
       ss = fmaf(x[e], x[e], ss);
     }
 #pragma unroll
@@ -105,12 +121,12 @@ __device__ __forceinline__ void phi_lane(float* x, int phi) {
 // phi(q) and phi(k) of the tile's rows, from the raw copies into fp32 rows,
 // and s_ii = phi(q_i) . phi(k_i): eight lanes a row (D/8 features each), four
 // rows a warp at a time.  Rows at or past nt come out zero.
-template <typename T, int D>
+template <typename T, int D, int NC>
 __device__ __forceinline__ void phi_tile(float* sQ, float* sK, float* sSii, const T* rq, const T* rk, int nt,
                                          int phi) {
   constexpr int PER = D / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 3, sub = lane & 7;
-  for (int r0 = 4 * warp; r0 < kTile; r0 += 4 * kWarps) {
+  for (int r0 = 4 * warp; r0 < kTile; r0 += 4 * Cols<NC>::kWarps) {
     const int r = r0 + g, c0 = r * D + sub * PER;
     const bool ok = r < nt;
     float xq[PER], xk[PER];
@@ -135,9 +151,10 @@ __device__ __forceinline__ void phi_tile(float* sQ, float* sK, float* sSii, cons
   }
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThr) rnn_cols_kernel(Problem p, float* cF_all) {
-  using Y = Lay<T, D>;
+template <typename T, int D, int NC>
+__global__ void __launch_bounds__(Cols<NC>::kThr) rnn_cols_kernel(Problem p, float* cF_all) {
+  using Y = Lay<T, D, NC>;
+  constexpr int kCols = NC, kThr = Cols<NC>::kThr;
   constexpr int RPL = D / kG;                  // state rows per lane
   constexpr int VW = RPL < 4 ? RPL : 4;        // rows read per vector load
   constexpr int NB = D / kCols;                // CTAs per head
@@ -170,13 +187,13 @@ __global__ void __launch_bounds__(kThr) rnn_cols_kernel(Problem p, float* cF_all
 #pragma unroll
     for (int r = 0; r < RPL; ++r) S[r] = 0.f;
     auto tile_t0 = [&](int i) { return (fwd ? i : ntiles - 1 - i) * kTile; };
-    issue_tile<T, D>(raw, q, k, v, n0, tile_t0(0), min(kTile, L - tile_t0(0)));
+    issue_tile<T, D, NC>(raw, q, k, v, n0, tile_t0(0), min(kTile, L - tile_t0(0)));
     for (int i = 0; i < ntiles; ++i) {
       const int t0 = tile_t0(i), nt = min(kTile, L - t0);
       uint8_t* slot = raw + (i & 1) * Y::kRaw;
       if (i + 1 < ntiles) {
         const int t1 = tile_t0(i + 1);
-        issue_tile<T, D>(raw + ((i + 1) & 1) * Y::kRaw, q, k, v, n0, t1, min(kTile, L - t1));
+        issue_tile<T, D, NC>(raw + ((i + 1) & 1) * Y::kRaw, q, k, v, n0, t1, min(kTile, L - t1));
         cp_wait<1>();
       } else {
         cp_wait<0>();
@@ -186,7 +203,7 @@ __global__ void __launch_bounds__(kThr) rnn_cols_kernel(Problem p, float* cF_all
       const T* rq = reinterpret_cast<const T*>(slot);
       const T* rk = reinterpret_cast<const T*>(slot + Y::kRawQ);
       const T* rv = reinterpret_cast<const T*>(slot + 2 * Y::kRawQ);
-      phi_tile<T, D>(sQ, sK, sSii, rq, rk, nt, p.phi);
+      phi_tile<T, D, NC>(sQ, sK, sSii, rq, rk, nt, p.phi);
       for (int x = threadIdx.x; x < kTile * kCols; x += kThr) sV[x] = x / kCols < nt ? to_f32(rv[x]) : 0.f;
       if (threadIdx.x < kTile) {
         // forward: lambda_t; backward: lambda_{t+1} (none after the last token)
@@ -280,17 +297,22 @@ __global__ void __launch_bounds__(kThr) rnn_cols_kernel(Problem p, float* cF_all
   }
 }
 
-template <typename T, int D>
-cudaError_t rnn_launch(const Problem& p, float* ws, cudaStream_t s) {
-  using Y = Lay<T, D>;
-  auto kern = rnn_cols_kernel<T, D>;
+template <typename T, int D, int NC>
+cudaError_t rnn_launch_nc(const Problem& p, float* ws, cudaStream_t s) {
+  using Y = Lay<T, D, NC>;
+  auto kern = rnn_cols_kernel<T, D, NC>;
   if (Y::kBytes > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Y::kBytes);
     if (e != cudaSuccess) return e;
   }
-  const size_t grid = (size_t)p.B * p.H * (D / kCols);
-  kern<<<(unsigned)grid, kThr, Y::kBytes, s>>>(p, ws);
+  const size_t grid = (size_t)p.B * p.H * (D / NC);
+  kern<<<(unsigned)grid, Cols<NC>::kThr, Y::kBytes, s>>>(p, ws);
   return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t rnn_launch(const Problem& p, float* ws, cudaStream_t s) {
+  return rnn_launch_nc<T, D, 8>(p, ws, s);
 }
 
 }  // namespace
