@@ -128,8 +128,12 @@ def algorithmic_bytes(w, mask: str, out_bytes: int = 4) -> int:
 def kernels_per_call(form: str, chunk: int, w) -> int:
     """Kernel launches one operator call makes: the tensor-core chunk paths
     (bf16, d=64, chunk 64 or 128) take one launch up to 256 tokens and three
-    (pre-pass, segment scan, main pass) beyond; every other path one."""
+    (pre-pass, segment scan, main pass) beyond; the recurrent form two with
+    its workspace (the features of every token, then the column CTAs);
+    every other path one."""
     tc = form == "chunk" and chunk in (64, 128) and w.d == 64 and w.dtype == "bf16"
+    if form == "rnn":
+        return 2
     return 3 if tc and w.L > 256 else 1
 
 
@@ -594,15 +598,18 @@ def measure_config(c, flush, hbm_peak, steps=20, warmup=3):
             "value": w.B * w.L / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "launches_per_call": kernels_per_call(form, chunk, w),
             "path": path_name(form, chunk, w)}
+    b = algorithmic_bytes(w, mask)
+    hbm = {"bound": "hbm", "achieved": b / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+           "frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": b}
     if form in ("full", "rnn"):
         fl = full_flops(w) if form == "full" else rnn_flops(w)
         line["roofline"] = {"bound": "alu", "achieved": fl / (ms * 1e-3) / 1e12, "peak": FP32_ALU_PEAK_TFLOPS,
                             "unit": "TFLOP/s", "frac": fl / (ms * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
                             "algorithmic_flops": fl}
+        # the same bytes the chunk form's roofline counts, for comparison
+        line["hbm"] = hbm
     else:
-        b = algorithmic_bytes(w, mask)
-        line["roofline"] = {"bound": "hbm", "achieved": b / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                            "frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": b}
+        line["roofline"] = hbm
     return line
 
 

@@ -31,8 +31,9 @@ bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 
 // Workspace bytes for (form, path).
-size_t simt_workspace_bytes(int B, int H, int L, int form) {
-  if (form == LION_FORM_RNN || form == LION_FORM_CHUNK) return sizeof(float) * (size_t)B * H * L;
+size_t simt_workspace_bytes(int B, int H, int L, int d, int form) {
+  if (form == LION_FORM_RNN) return lion::rnn_workspace_bytes(B, H, L, d);
+  if (form == LION_FORM_CHUNK) return sizeof(float) * (size_t)B * H * L;
   return 0;
 }
 
@@ -98,7 +99,7 @@ const char* lion_status_string(lion_status s) {
 
 size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk) {
   if (B < 1 || H < 1 || L < 1 || !valid_d(d)) return 0;
-  size_t need = simt_workspace_bytes(B, H, L, form);
+  size_t need = simt_workspace_bytes(B, H, L, d, form);
   if (form == LION_FORM_CHUNK && d == 64 && chunk == 64) {
     const size_t tc = lion::chunk_tc_workspace_bytes(B, H, L);
     if (tc > need) need = tc;
@@ -247,7 +248,7 @@ lion_status lion::forward_checked(const lion_args* a) {
   const size_t need = use_tc128   ? 0
                       : use_tc128l ? lion::chunk128_long_workspace_bytes(a->B, a->H, a->L)
                       : use_tc     ? lion::chunk_tc_workspace_bytes(a->B, a->H, a->L)
-                                   : simt_workspace_bytes(a->B, a->H, a->L, a->form);
+                                   : simt_workspace_bytes(a->B, a->H, a->L, a->d, a->form);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
@@ -277,7 +278,7 @@ lion_status lion::forward_checked(const lion_args* a) {
   cudaError_t e = cudaSuccess;
   switch (a->form) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
-    case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
+    case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, need, s); break;
     case LION_FORM_CHUNK:
       e = use_tc128    ? lion::launch_chunk128_tc(p, dstatus, s)
           : use_tc128l ? lion::launch_chunk128_long(p, ws, dstatus, s)
@@ -336,7 +337,7 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
   p.chunk = a->chunk;
   p.causal = 1;
   cudaStream_t s = a->stream;
-  const size_t need = simt_workspace_bytes(a->B, a->H, a->L, a->form);
+  const size_t need = simt_workspace_bytes(a->B, a->H, a->L, a->d, a->form);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
@@ -362,7 +363,7 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
   cudaError_t e = cudaSuccess;
   switch (a->form) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
-    case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, s); break;
+    case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, need, s); break;
     case LION_FORM_CHUNK: e = lion::launch_chunk_simt(p, (float*)ws, s); break;
   }
   if (tmp) {

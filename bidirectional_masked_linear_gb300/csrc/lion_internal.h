@@ -33,7 +33,11 @@ struct Problem {
 
 // SIMT (CUDA-core) kernels: any d in {16,32,64,128}, both dtypes.
 cudaError_t launch_full_simt(const Problem& p, cudaStream_t s);
-cudaError_t launch_rnn_simt(const Problem& p, float* ws_c /*[B*H*L]*/, cudaStream_t s);
+// The recurrent form.  The workspace holds c^F (B*H*L floats) and, when it
+// is rnn_workspace_bytes long, the features of every token, computed once
+// by a first launch; with the c^F part alone each column CTA computes them.
+size_t rnn_workspace_bytes(int B, int H, int L, int d);
+cudaError_t launch_rnn_simt(const Problem& p, float* ws, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_chunk_simt(const Problem& p, float* ws_den /*[B*H*L]*/, cudaStream_t s);
 cudaError_t launch_rnn_step(const void* q, const void* k, const void* v, const float* log_lambda,
                             float* S, float* z, float* y_part, float* c_part, int B, int H,

@@ -106,5 +106,7 @@ extern "C" lion_status lion_attn_fwd_rnn_noalloc(const void* q, const void* k, c
   p.phi = lion::resolve_phi(mask_kind, LION_PHI_DEFAULT);
   p.dtype = dtype;
   p.chunk = 1;
-  return lion::launch_rnn_simt(p, scratch, stream) == cudaSuccess ? LION_OK : LION_ERR_CUDA;
+  // c^F alone in the fixed array: every column CTA computes its features
+  const size_t cf_bytes = sizeof(float) * (size_t)B * H * L;
+  return lion::launch_rnn_simt(p, scratch, cf_bytes, stream) == cudaSuccess ? LION_OK : LION_ERR_CUDA;
 }

@@ -55,6 +55,8 @@ def test_launch_counts():
     assert bench.kernels_per_call("chunk", 64, hires) == 3
     assert bench.kernels_per_call("chunk", 128, hires) == 3
     assert bench.kernels_per_call("chunk", 32, hires) == 1
+    assert bench.kernels_per_call("rnn", 0, hires) == 2     # features, then the column CTAs
+    assert bench.kernels_per_call("full", 0, vit) == 1
 
 
 def test_traffic_keys_follow_the_kernel_that_runs():

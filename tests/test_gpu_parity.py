@@ -277,6 +277,32 @@ def test_errors_on_gpu():
                       out=torch.empty((1, 1, 16, 64), device="cuda"))
 
 
+@pytest.mark.parametrize("dtype", ("bf16", "fp32"))
+def test_rnn_caller_workspace(oracle_mod, dtype):
+    """The recurrent form with a caller workspace of lion_attn_workspace_bytes
+    (the features of every token computed once by a first launch) gives the
+    bits of the call whose workspace the library allocates, and matches the
+    oracle; a workspace holding only c^F (B*H*L floats) is refused."""
+    B, H, L, d = 2, 3, 301, 64
+    inp = synth.make_inputs(B, H, L, d, "s", dtype, seed=41)
+    g = _cuda(inp)
+    need = lion.workspace_bytes(B, H, L, d, lion.FORM_RNN)
+    assert need > 4 * B * H * L
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")    # NaN-patterned scratch
+    y0 = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], 2, lion.FORM_RNN)
+    y1 = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], 2, lion.FORM_RNN, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    tol = TOL_FP32 if dtype == "fp32" else TOL_BF16
+    q, k, v, ll = f64(inp)
+    check(oracle_mod, y1.cpu().numpy(), oracle_mod.full(q, k, v, ll, 2, threads=0), inp, tol,
+          label=f"rnn caller workspace {dtype}")
+    small = torch.empty((4 * B * H * L,), dtype=torch.uint8, device="cuda")
+    with pytest.raises(lion.LionError) as ei:
+        lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], 2, lion.FORM_RNN, workspace=small)
+    assert ei.value.status == lion.ERR_INVALID_ARG
+
+
 def test_rnn_step_matches_rnn_form(oracle_mod):
     """Feeding tokens one at a time through lion_rnn_step, forward and then
     backward (with lambda of the next token), and combining with the diagonal
