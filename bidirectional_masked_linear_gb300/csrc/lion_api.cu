@@ -283,7 +283,8 @@ lion_status lion::forward_checked(const lion_args* a) {
       e = use_tc128    ? lion::launch_chunk128_tc(p, dstatus, s)
           : use_tc128l ? lion::launch_chunk128_long(p, ws, dstatus, s)
           : use_tc     ? lion::launch_chunk_tc(p, ws, dstatus, s)
-                       : lion::launch_chunk_simt(p, (float*)ws, s);
+          : lion::chunk_tile_supported(p) ? lion::launch_chunk_tile(p, (float*)ws, s)
+                                          : lion::launch_chunk_simt(p, (float*)ws, s);
       break;
   }
   if (tmp) {
@@ -364,7 +365,10 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
   switch (a->form) {
     case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, need, s); break;
-    case LION_FORM_CHUNK: e = lion::launch_chunk_simt(p, (float*)ws, s); break;
+    case LION_FORM_CHUNK:
+      e = lion::chunk_tile_supported(p) ? lion::launch_chunk_tile(p, (float*)ws, s)
+                                        : lion::launch_chunk_simt(p, (float*)ws, s);
+      break;
   }
   if (tmp) {
     if (e == cudaSuccess) e = lion::launch_f32_to_bf16(tmp, a->out, n_out, s);
