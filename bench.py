@@ -125,15 +125,18 @@ def algorithmic_bytes(w, mask: str, out_bytes: int = 4) -> int:
     return b
 
 
-def kernels_per_call(form: str, chunk: int, w) -> int:
+def kernels_per_call(form: str, chunk: int, w, mask: str = "s") -> int:
     """Kernel launches one operator call makes: the tensor-core chunk paths
     (bf16, d=64, chunk 64 or 128) take one launch up to 256 tokens and three
     (pre-pass, segment scan, main pass) beyond; the recurrent form two with
-    its workspace (the features of every token, then the column CTAs);
-    every other path one."""
+    its workspace (the features of every token, then the column CTAs); the
+    full form at d = 64 and 128 two (the features, the tiled pass), three
+    for LION-S (its prefix first); every other path one."""
     tc = form == "chunk" and chunk in (64, 128) and w.d == 64 and w.dtype == "bf16"
     if form == "rnn":
         return 2
+    if form == "full" and w.d in (64, 128):
+        return 3 if mask == "s" else 2
     return 3 if tc and w.L > 256 else 1
 
 
@@ -596,7 +599,7 @@ def measure_config(c, flush, hbm_peak, steps=20, warmup=3):
     line = {"workload": f"{w.name} B={w.B} H={w.H} L={w.L} d={w.d}", "mask": mask, "form": form,
             "chunk": chunk if form == "chunk" else None, "input_dtype": w.dtype,
             "value": w.B * w.L / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "launches_per_call": kernels_per_call(form, chunk, w),
+            "launches_per_call": kernels_per_call(form, chunk, w, mask),
             "path": path_name(form, chunk, w)}
     b = algorithmic_bytes(w, mask)
     hbm = {"bound": "hbm", "achieved": b / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -619,6 +622,10 @@ def path_name(form, chunk, w) -> str:
         return "tcgen05 chunk-128" + (" (pre-pass, segment scan, main pass)" if w.L > 256 else "")
     if tc and chunk == 64:
         return "tcgen05 chunk-64" + (" (pre-pass, segment scan, main pass)" if w.L > 256 else "")
+    if form == "full" and w.d in (64, 128):
+        return "full form, fp32 CUDA cores, register-tiled"
+    if form == "chunk" and chunk <= 64:
+        return "chunk form, fp32 CUDA cores, register-tiled"
     return {"full": "full form, fp32 CUDA cores", "rnn": "recurrent form, fp32 CUDA cores",
             "chunk": "chunk form, fp32 CUDA cores"}[form]
 
@@ -819,7 +826,7 @@ def main():
                          "peak_source": peak_src, "algorithmic_bytes": abytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * kernels_per_call(args.form, args.chunk, w),
+            "gpu_launches": args.steps * kernels_per_call(args.form, args.chunk, w, args.mask),
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
             "secondary": secondary,

@@ -32,6 +32,7 @@ bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 // Workspace bytes for (form, path).
 size_t simt_workspace_bytes(int B, int H, int L, int d, int form) {
+  if (form == LION_FORM_FULL && (d == 64 || d == 128)) return lion::full_tiled_workspace_bytes(B, H, L, d);
   if (form == LION_FORM_RNN) return lion::rnn_workspace_bytes(B, H, L, d);
   if (form == LION_FORM_CHUNK) return sizeof(float) * (size_t)B * H * L;
   return 0;
@@ -277,7 +278,9 @@ lion_status lion::forward_checked(const lion_args* a) {
   }
   cudaError_t e = cudaSuccess;
   switch (a->form) {
-    case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
+    case LION_FORM_FULL:
+      e = lion::full_tiled_supported(p) ? lion::launch_full_tiled(p, ws, s) : lion::launch_full_simt(p, s);
+      break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, need, s); break;
     case LION_FORM_CHUNK:
       e = use_tc128    ? lion::launch_chunk128_tc(p, dstatus, s)
@@ -363,7 +366,9 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
   }
   cudaError_t e = cudaSuccess;
   switch (a->form) {
-    case LION_FORM_FULL: e = lion::launch_full_simt(p, s); break;
+    case LION_FORM_FULL:
+      e = lion::full_tiled_supported(p) ? lion::launch_full_tiled(p, ws, s) : lion::launch_full_simt(p, s);
+      break;
     case LION_FORM_RNN: e = lion::launch_rnn_simt(p, (float*)ws, need, s); break;
     case LION_FORM_CHUNK:
       e = lion::chunk_tile_supported(p) ? lion::launch_chunk_tile(p, (float*)ws, s)

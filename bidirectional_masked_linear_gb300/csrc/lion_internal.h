@@ -126,6 +126,13 @@ cudaError_t launch_bwd_chunk(const Problem& p, const float* dy, float* dq, float
 // int32 [2][L]); fp32 on the CUDA cores, d in {64, 128}; workspace of
 // reorder_workspace_bytes; reorder_launches kernels a call.
 size_t reorder_workspace_bytes(int B, int H, int L, int d);
+// The plain full form (d = 64 or 128) on the reordered form's register-tiled
+// kernel with the tokens' own order: phi(q), phi(k) and LION-S's prefix in a
+// workspace of full_tiled_workspace_bytes, full_tiled_launches kernels.
+bool full_tiled_supported(const Problem& p);
+size_t full_tiled_workspace_bytes(int B, int H, int L, int d);
+int full_tiled_launches(int mask_kind);
+cudaError_t launch_full_tiled(const Problem& p, void* ws, cudaStream_t s);
 int reorder_launches(int mask_kind);
 cudaError_t launch_reordered(const Problem& p, const int* order, void* ws, int* status, cudaStream_t s);
 // Its gradients: dq, dk, dv [B][H][L][d], dll (LION-D [H], LION-S [B][H][L]).

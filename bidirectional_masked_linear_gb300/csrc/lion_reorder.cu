@@ -53,6 +53,7 @@ struct ReorderParams {
   const int* order;   // [2][L]
   float* out;
   int B, H, L, mask_kind, phi;
+  int causal;         // 1: keys j <= i only (the natural order's forward half)
   float* fq;          // [BH][L][D] phi(q)
   float* fk;          // [BH][L][D] phi(k)
   int* pos;           // [2][L]     position of each token in each order
@@ -107,19 +108,20 @@ __global__ void __launch_bounds__(kOrderThreads) order_positions_kernel(ReorderP
     for (int t = threadIdx.x; t < L; t += blockDim.x) p.coord[(size_t)o * L + t] = (float)pos[t];
 }
 
-// (2) LION-S: grid (B*H, 2), kScanThreads threads.
+// (2) LION-S: grid (B*H, orders), kScanThreads threads.  Without an order
+// array (the plain full form) the order is the tokens' own.
 __global__ void __launch_bounds__(kScanThreads) order_prefix_kernel(ReorderParams p) {
   const int L = p.L, bh = blockIdx.x, o = blockIdx.y, t0 = threadIdx.x;
-  const int* ord = p.order + (size_t)o * L;
+  const int* ord = p.order ? p.order + (size_t)o * L : nullptr;
   const float* ll = p.log_lambda + (size_t)bh * L;
   float* C = p.coord + ((size_t)o * gridDim.x + bh) * L;
   const int per = (L + kScanThreads - 1) / kScanThreads;
   const int lo = min(L, t0 * per), hi = min(L, lo + per);
   double run = 0.0, all;
-  for (int t = lo; t < hi; ++t) run += (double)ll[clamp_token(ord[t], L)];
+  for (int t = lo; t < hi; ++t) run += (double)ll[ord ? clamp_token(ord[t], L) : t];
   double off = block_scan(run, &all) - run;
   for (int t = lo; t < hi; ++t) {
-    const int a = clamp_token(ord[t], L);
+    const int a = ord ? clamp_token(ord[t], L) : t;
     off += (double)ll[a];
     C[a] = (float)off;
   }
@@ -130,8 +132,10 @@ constexpr size_t reorder_smem() {
   return sizeof(float) * ((size_t)(kTR + 2 * kTC) * (D + 4) + kTR * kTAL + 2 * kTC);
 }
 
-// (4) 32 queries per CTA.
-template <typename T, int D>
+// (4) 32 queries per CTA.  NORD = 2: the mask averaged over the two orders;
+// NORD = 1: the plain full form, the tokens' own order (LION-D's coordinate
+// is then the token index itself), with p.causal keeping the keys j <= i.
+template <typename T, int D, int NORD>
 __global__ void __launch_bounds__(kTThreads) reorder_full_kernel(ReorderParams p) {
   constexpr int LD = D + 4, MF = D / 16, U = D / 64;
   extern __shared__ __align__(16) float smem[];
@@ -150,10 +154,11 @@ __global__ void __launch_bounds__(kTThreads) reorder_full_kernel(ReorderParams p
   if (p.mask_kind == MASK_S) {
     C0 = p.coord + (size_t)bh * L;
     C1 = p.coord + ((size_t)BH + bh) * L;
-  } else if (p.mask_kind == MASK_D) {
+  } else if (p.mask_kind == MASK_D && NORD == 2) {
     C0 = p.coord;
     C1 = p.coord + L;
   }
+  const bool index_coord = NORD == 1 && p.mask_kind == MASK_D;
   const float* fkh = p.fk + (size_t)bh * L * D;
   const T* vh = head_of<T>(p.v, bh, L, D);
   stage_rows<D>(sQ, p.fq + (size_t)bh * L * D, i0, kTR, L);
@@ -164,8 +169,8 @@ __global__ void __launch_bounds__(kTThreads) reorder_full_kernel(ReorderParams p
   for (int a = 0; a < 4; ++a) {
     ia[a] = i0 + ty + 8 * a;
     live[a] = ia[a] < L;
-    c0[a] = !lit && live[a] ? C0[ia[a]] : 0.f;
-    c1[a] = !lit && live[a] ? C1[ia[a]] : 0.f;
+    c0[a] = index_coord ? (float)ia[a] : !lit && live[a] ? C0[ia[a]] : 0.f;
+    c1[a] = NORD == 2 && !lit && live[a] ? C1[ia[a]] : 0.f;
   }
   float den[4], num[4][MF];
 #pragma unroll
@@ -174,12 +179,13 @@ __global__ void __launch_bounds__(kTThreads) reorder_full_kernel(ReorderParams p
 #pragma unroll
     for (int f = 0; f < MF; ++f) num[a][f] = 0.f;
   }
-  for (int j0 = 0; j0 < L; j0 += kTC) {
+  const int jend = p.causal ? min(L, i0 + kTR) : L;   // causal: keys up to the block's last row
+  for (int j0 = 0; j0 < jend; j0 += kTC) {
     stage_rows<D>(sK, fkh, j0, kTC, L);
     stage_rows<D>(sV, vh, j0, kTC, L);
-    if (!lit) {
+    if (!lit && !index_coord) {
       stage_vec(sC, C0, j0, kTC, L);
-      stage_vec(sC + kTC, C1, j0, kTC, L);
+      if (NORD == 2) stage_vec(sC + kTC, C1, j0, kTC, L);
     }
     __syncthreads();
     const int nc = min(kTC, L - j0);
@@ -191,9 +197,11 @@ __global__ void __launch_bounds__(kTThreads) reorder_full_kernel(ReorderParams p
       for (int b = 0; b < 4; ++b) {
         const int jl = tx + 16 * b, j = j0 + jl;
         float m = 0.f;
-        if (live[a] && j < L)
-          m = lit ? 1.f
-                  : 0.5f * (expf(-fabsf(c0[a] - sC[jl]) * w) + expf(-fabsf(c1[a] - sC[kTC + jl]) * w));
+        if (live[a] && j < L && (!p.causal || j <= ia[a])) {
+          if (lit) m = 1.f;
+          else if (NORD == 1) m = expf(-fabsf(c0[a] - (index_coord ? (float)j : sC[jl])) * w);
+          else m = 0.5f * (expf(-fabsf(c0[a] - sC[jl]) * w) + expf(-fabsf(c1[a] - sC[kTC + jl]) * w));
+        }
         const float x = m * s[a][b];
         den[a] += x;
         sA[(ty + 8 * a) * kTAL + jl] = x;
@@ -727,8 +735,24 @@ cudaError_t reorder_launch(const ReorderParams& p, int phi, cudaStream_t s) {
   }
   if ((e = launch_phi_rows<T, D>(p.q, p.k, p.fq, p.fk, BH * p.L, phi, s)) != cudaSuccess) return e;
   constexpr size_t smem = reorder_smem<D>();
-  if ((e = allow_smem(reorder_full_kernel<T, D>, smem)) != cudaSuccess) return e;
-  reorder_full_kernel<T, D><<<dim3((unsigned)BH, (p.L + kTR - 1) / kTR), kTThreads, smem, s>>>(p);
+  if ((e = allow_smem(reorder_full_kernel<T, D, 2>, smem)) != cudaSuccess) return e;
+  reorder_full_kernel<T, D, 2><<<dim3((unsigned)BH, (p.L + kTR - 1) / kTR), kTThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// The plain full form: features, LION-S's prefix, the tiled pass.
+template <typename T, int D>
+cudaError_t full_tiled_launch(const ReorderParams& p, cudaStream_t s) {
+  const long BH = (long)p.B * p.H;
+  cudaError_t e;
+  if (p.mask_kind == MASK_S) {
+    order_prefix_kernel<<<dim3((unsigned)BH, 1), kScanThreads, 0, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if ((e = launch_phi_rows<T, D>(p.q, p.k, p.fq, p.fk, BH * p.L, p.phi, s)) != cudaSuccess) return e;
+  constexpr size_t smem = reorder_smem<D>();
+  if ((e = allow_smem(reorder_full_kernel<T, D, 1>, smem)) != cudaSuccess) return e;
+  reorder_full_kernel<T, D, 1><<<dim3((unsigned)BH, (p.L + kTR - 1) / kTR), kTThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -784,6 +808,44 @@ size_t reorder_workspace_bytes(int B, int H, int L, int d) {
 }
 
 int reorder_launches(int mask_kind) { return mask_kind == MASK_S ? 4 : 3; }
+
+bool full_tiled_supported(const Problem& p) { return p.d == 64 || p.d == 128; }
+
+size_t full_tiled_workspace_bytes(int B, int H, int L, int d) {
+  const size_t n = (size_t)B * H * L;
+  return 2 * align256(sizeof(float) * n * d) + align256(sizeof(float) * n);
+}
+
+int full_tiled_launches(int mask_kind) { return mask_kind == MASK_S ? 3 : 2; }
+
+cudaError_t launch_full_tiled(const Problem& pr, void* ws, cudaStream_t s) {
+  ReorderParams p;
+  memset(&p, 0, sizeof(p));
+  p.q = pr.q;
+  p.k = pr.k;
+  p.v = pr.v;
+  p.log_lambda = pr.log_lambda;
+  p.out = pr.out;
+  p.B = pr.B;
+  p.H = pr.H;
+  p.L = pr.L;
+  p.mask_kind = pr.mask_kind;
+  p.phi = pr.phi;
+  p.causal = pr.causal;
+  const size_t n = (size_t)pr.B * pr.H * pr.L;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.fq = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n * pr.d);
+  p.fk = reinterpret_cast<float*>(w);
+  w += align256(sizeof(float) * n * pr.d);
+  p.coord = reinterpret_cast<float*>(w);
+  const bool bf = pr.dtype == DT_BF16;
+  switch (pr.d) {
+    case 64: return bf ? full_tiled_launch<__nv_bfloat16, 64>(p, s) : full_tiled_launch<float, 64>(p, s);
+    case 128: return bf ? full_tiled_launch<__nv_bfloat16, 128>(p, s) : full_tiled_launch<float, 128>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_reordered(const Problem& pr, const int* order, void* ws, int* status, cudaStream_t s) {
   ReorderParams p;

@@ -55,7 +55,9 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_query(lib):
     from bidirectional_masked_linear_gb300 import lion
-    assert lion.workspace_bytes(2, 3, 10, 64, lion.FORM_FULL) == 0
+    # the full form: the tiled kernel's features (and LION-S prefix) at d = 64, 128; none below
+    assert lion.workspace_bytes(2, 3, 10, 64, lion.FORM_FULL) >= 2 * (2 * 3 * 10 * 64) * 4
+    assert lion.workspace_bytes(2, 3, 10, 16, lion.FORM_FULL) == 0
     assert lion.workspace_bytes(2, 3, 10, 64, lion.FORM_RNN) >= 2 * 3 * 10 * 4
     assert lion.workspace_bytes(0, 3, 10, 64, lion.FORM_RNN) == 0
     assert lion.workspace_bytes(1, 1, 10, 48, lion.FORM_RNN) == 0      # d unsupported

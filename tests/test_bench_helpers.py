@@ -56,7 +56,9 @@ def test_launch_counts():
     assert bench.kernels_per_call("chunk", 128, hires) == 3
     assert bench.kernels_per_call("chunk", 32, hires) == 1
     assert bench.kernels_per_call("rnn", 0, hires) == 2     # features, then the column CTAs
-    assert bench.kernels_per_call("full", 0, vit) == 1
+    assert bench.kernels_per_call("full", 0, vit, "s") == 3   # prefix, features, the tiled pass
+    assert bench.kernels_per_call("full", 0, vit, "d") == 2
+    assert bench.kernels_per_call("full", 0, synth.WORKLOADS["tiny_d_fp32"], "d") == 1
 
 
 def test_traffic_keys_follow_the_kernel_that_runs():
