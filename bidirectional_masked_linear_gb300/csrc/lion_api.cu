@@ -31,9 +31,11 @@ bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 
 // Workspace bytes for (form, path).
-size_t simt_workspace_bytes(int B, int H, int L, int d, int form) {
+size_t simt_workspace_bytes(int B, int H, int L, int d, int form, int chunk) {
   if (form == LION_FORM_FULL && (d == 64 || d == 128)) return lion::full_tiled_workspace_bytes(B, H, L, d);
   if (form == LION_FORM_RNN) return lion::rnn_workspace_bytes(B, H, L, d);
+  if (form == LION_FORM_CHUNK && chunk >= 1 && chunk <= lion::kChunkTileMax)
+    return lion::chunk_tile_workspace_bytes(B, H, L, d);
   if (form == LION_FORM_CHUNK) return sizeof(float) * (size_t)B * H * L;
   return 0;
 }
@@ -100,7 +102,7 @@ const char* lion_status_string(lion_status s) {
 
 size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk) {
   if (B < 1 || H < 1 || L < 1 || !valid_d(d)) return 0;
-  size_t need = simt_workspace_bytes(B, H, L, d, form);
+  size_t need = simt_workspace_bytes(B, H, L, d, form, chunk);
   if (form == LION_FORM_CHUNK && d == 64 && chunk == 64) {
     const size_t tc = lion::chunk_tc_workspace_bytes(B, H, L);
     if (tc > need) need = tc;
@@ -249,7 +251,7 @@ lion_status lion::forward_checked(const lion_args* a) {
   const size_t need = use_tc128   ? 0
                       : use_tc128l ? lion::chunk128_long_workspace_bytes(a->B, a->H, a->L)
                       : use_tc     ? lion::chunk_tc_workspace_bytes(a->B, a->H, a->L)
-                                   : simt_workspace_bytes(a->B, a->H, a->L, a->d, a->form);
+                                   : simt_workspace_bytes(a->B, a->H, a->L, a->d, a->form, a->chunk);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;
@@ -341,7 +343,7 @@ lion_status lion_attn_fwd_causal(const lion_args* a) {
   p.chunk = a->chunk;
   p.causal = 1;
   cudaStream_t s = a->stream;
-  const size_t need = simt_workspace_bytes(a->B, a->H, a->L, a->d, a->form);
+  const size_t need = simt_workspace_bytes(a->B, a->H, a->L, a->d, a->form, a->chunk);
   void* ws = a->workspace;
   bool owned = false;
   if (need > 0 && ws && a->workspace_bytes < need) return LION_ERR_INVALID_ARG;

@@ -24,6 +24,10 @@
 // left-to-right sweep adds its own and divides.  With Problem::causal only
 // the left-to-right sweep runs, with j <= i inside the chunk.
 //
+// phi(q) and phi(k) of every token go to the workspace first (one launch,
+// the same kernel as the full form's), so that the two sweeps read fp32
+// features as float4 rows and compute no feature map.
+//
 // Products (256 threads as a 16 x 16 grid, 4 x 4 outputs a thread, float4
 // operand reads from shared memory): "dot" when the contraction index is
 // contiguous in both operands (scores, the state applied to the queries),
@@ -32,6 +36,7 @@
 // is summed apart, so that each product covers exactly d columns.
 #include "lion_common.cuh"
 #include "lion_internal.h"
+#include "tile_simt.cuh"
 
 namespace lion {
 namespace {
@@ -43,42 +48,42 @@ struct TileCfg {
   static constexpr int LD = D + 4;       // row stride of d-wide rows (column d: the 1 of [v; 1])
   static constexpr int LDS = CT + 4;     // row stride of the transposed scores
   static constexpr int SR = D + 4;       // state rows: d value columns, z, padding
-  static constexpr size_t floats = 4 * (size_t)CT * LD + (size_t)SR * LD + (size_t)CT * LDS + 3 * CT;
+  static constexpr size_t floats = 4 * (size_t)CT * LD + (size_t)SR * LD + (size_t)CT * LDS + 3 * CT + 4;
 };
 
 // out[a][b] = sum_{k<K} X[a*ldx + k] Y[b*ldy + k] for a < MA, b < NB.  Thread
-// (ti, tj) holds a = a0 + ti + 16 alpha, b = b0 + tj + 16 beta of each 64 x 64
-// block; K % 4 == 0.  epi(a, b, value) sees every output once.
-template <typename Epi>
+// (ti, tj) holds a = a0 + ti + 16 alpha (alpha < RA), b = b0 + tj + 16 beta
+// (beta < RB) of each (16 RA) x (16 RB) block, so that a chunk of 16 or 32
+// rows takes one or two rows a thread; K % 4 == 0.  epi(a, b, value) sees
+// every output once.
+template <int RA, int RB, typename Epi>
 __device__ __forceinline__ void dot_tiles(const float* X, int ldx, const float* Y, int ldy, int MA, int NB, int K,
                                           Epi epi) {
   const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
-  for (int a0 = 0; a0 < MA; a0 += 64) {
-    for (int b0 = 0; b0 < NB; b0 += 64) {
+  for (int a0 = 0; a0 < MA; a0 += 16 * RA) {
+    for (int b0 = 0; b0 < NB; b0 += 16 * RB) {
       if (a0 + ti >= MA || b0 + tj >= NB) continue;
-      float acc[4][4];
+      float acc[RA][RB];
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < RA; ++x)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
-      const float* xr[4];
-      const float* yr[4];
+        for (int y = 0; y < RB; ++y) acc[x][y] = 0.f;
+      const float* xr[RA];
+      const float* yr[RB];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        xr[u] = X + (size_t)min(a0 + ti + 16 * u, MA - 1) * ldx;
-        yr[u] = Y + (size_t)min(b0 + tj + 16 * u, NB - 1) * ldy;
-      }
+      for (int u = 0; u < RA; ++u) xr[u] = X + (size_t)min(a0 + ti + 16 * u, MA - 1) * ldx;
+#pragma unroll
+      for (int u = 0; u < RB; ++u) yr[u] = Y + (size_t)min(b0 + tj + 16 * u, NB - 1) * ldy;
       for (int k = 0; k < K; k += 4) {
-        float4 xv[4], yv[4];
+        float4 xv[RA], yv[RB];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          xv[u] = *reinterpret_cast<const float4*>(xr[u] + k);
-          yv[u] = *reinterpret_cast<const float4*>(yr[u] + k);
-        }
+        for (int u = 0; u < RA; ++u) xv[u] = *reinterpret_cast<const float4*>(xr[u] + k);
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
+        for (int u = 0; u < RB; ++u) yv[u] = *reinterpret_cast<const float4*>(yr[u] + k);
 #pragma unroll
-          for (int y = 0; y < 4; ++y) {
+        for (int x = 0; x < RA; ++x)
+#pragma unroll
+          for (int y = 0; y < RB; ++y) {
             acc[x][y] = fmaf(xv[x].x, yv[y].x, acc[x][y]);
             acc[x][y] = fmaf(xv[x].y, yv[y].y, acc[x][y]);
             acc[x][y] = fmaf(xv[x].z, yv[y].z, acc[x][y]);
@@ -86,9 +91,9 @@ __device__ __forceinline__ void dot_tiles(const float* X, int ldx, const float* 
           }
       }
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+      for (int x = 0; x < RA; ++x)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) {
+        for (int y = 0; y < RB; ++y) {
           const int a = a0 + ti + 16 * x, b = b0 + tj + 16 * y;
           if (a < MA && b < NB) epi(a, b, acc[x][y]);
         }
@@ -135,20 +140,36 @@ __device__ __forceinline__ void outer_tiles(const float* X, int ldx, const float
 }
 
 // Rows [s, s + len) of a token-major [L][D] tensor into a [CT][LD] fp32 tile,
-// zero beyond len.
+// four features a thread, zero beyond len.
 template <typename T, int D, int CT>
 __device__ __forceinline__ void load_tile(float* dst, const T* src, int s, int len) {
-  constexpr int LD = TileCfg<D, CT>::LD;
-  for (int idx = threadIdx.x; idx < CT * D; idx += kThr) {
-    const int r = idx / D, m = idx - r * D;
-    dst[r * LD + m] = r < len ? to_f32(src[(size_t)(s + r) * D + m]) : 0.f;
+  constexpr int LD = TileCfg<D, CT>::LD, V = D / 4;
+  for (int idx = threadIdx.x; idx < CT * V; idx += kThr) {
+    const int r = idx / V, m = (idx - r * V) * 4;
+    *reinterpret_cast<float4*>(dst + r * LD + m) =
+        r < len ? load4(src + (size_t)(s + r) * D + m) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
+// Workspace (floats, each section padded to 64): the right-to-left sweep's
+// normalisers [BH L], phi(q) [BH L d], phi(k) [BH L d].
+__host__ __device__ constexpr size_t pad64(size_t n) { return (n + 63) & ~size_t(63); }
+struct TileWs {
+  size_t den, fq, fk, total;
+  __host__ __device__ TileWs(size_t BHL, int d) {
+    den = 0;
+    fq = pad64(BHL);
+    fk = fq + pad64(BHL * (size_t)d);
+    total = fk + pad64(BHL * (size_t)d);
+  }
+};
+
 template <typename T, int D, int CT>
-__global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_all) {
+__global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* ws) {
   using C = TileCfg<D, CT>;
   constexpr int LD = C::LD, LDS = C::LDS;
+  constexpr int RC = CT / 16;                 // chunk rows (or columns) a thread in a dot product
+  constexpr int RD = D >= 64 ? 4 : D / 16;    // feature columns a thread
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   float* sQ = sm;                     // [CT][LD] phi(q)
@@ -160,14 +181,16 @@ __global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_
   float* sP = sS + CT * LDS;          // [CT] chunk-local inclusive prefix
   float* sW = sP + CT;                // [CT] state weights of the chunk's keys
   float* sR = sW + CT;                // [CT] state factors of the chunk's queries
+  float* sLn = sR + CT;               // [1] l at the token after the chunk
 
   const int L = p.L, H = p.H, Cr = p.chunk, bh = blockIdx.x;
   const int N = (L + Cr - 1) / Cr;
-  const T* q = reinterpret_cast<const T*>(p.q) + (size_t)bh * L * D;
-  const T* k = reinterpret_cast<const T*>(p.k) + (size_t)bh * L * D;
+  const TileWs w((size_t)p.B * H * L, D);
+  const float* fq = ws + w.fq + (size_t)bh * L * D;
+  const float* fk = ws + w.fk + (size_t)bh * L * D;
   const T* v = reinterpret_cast<const T*>(p.v) + (size_t)bh * L * D;
   float* out = p.out + (size_t)bh * L * D;
-  float* den = den_all + (size_t)bh * L;
+  float* den = ws + w.den + (size_t)bh * L;
   const float* ll = p.mask_kind == MASK_S ? p.log_lambda + (size_t)bh * L : nullptr;
   const float lh = p.mask_kind == MASK_D ? __ldg(p.log_lambda + bh % H) : 0.f;
   auto ell = [&](int t) -> float { return ll ? __ldg(ll + t) : lh; };
@@ -180,16 +203,24 @@ __global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_
       const int s = c * Cr, len = min(Cr, L - s);
       const bool has_state = fwd ? c > 0 : c < N - 1;
       const bool carry = fwd ? c < N - 1 : c > 0;
-      // ---- tiles, prefix, feature maps
-      load_tile<T, D, CT>(sQ, q, s, len);
-      load_tile<T, D, CT>(sK, k, s, len);
+      // ---- tiles and prefix (the decays are requested first, so that their
+      //      loads overlap the tiles')
+      float la = 0.f, lb = 0.f, ln = 0.f;
+      if (threadIdx.x < 32 && p.mask_kind != MASK_LIT) {
+        // two tokens a lane (CT <= 64), and l after the chunk
+        const int lane = threadIdx.x;
+        if (2 * lane < len) la = ell(s + 2 * lane);
+        if (2 * lane + 1 < len) lb = ell(s + 2 * lane + 1);
+        if (lane == 0 && s + len < L) ln = ell(s + len);
+      }
+      load_tile<float, D, CT>(sQ, fq, s, len);
+      load_tile<float, D, CT>(sK, fk, s, len);
       load_tile<T, D, CT>(sV, v, s, len);
       for (int r = threadIdx.x; r < CT; r += kThr) sV[r * LD + D] = r < len ? 1.f : 0.f;
       if (threadIdx.x < 32) {
-        // two tokens a lane (CT <= 64)
         const int lane = threadIdx.x;
-        const float a = (p.mask_kind != MASK_LIT && 2 * lane < len) ? ell(s + 2 * lane) : 0.f;
-        const float b = (p.mask_kind != MASK_LIT && 2 * lane + 1 < len) ? ell(s + 2 * lane + 1) : 0.f;
+        const float a = la, b = lb;
+        if (lane == 0) *sLn = ln;
         float x = a + b;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -200,11 +231,8 @@ __global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_
         if (2 * lane + 1 < CT) sP[2 * lane + 1] = x;
       }
       __syncthreads();
-      phi_rows_inplace(sQ, CT, len, D, LD, p.phi);
-      phi_rows_inplace(sK, CT, len, D, LD, p.phi);
       {
-        const float T_c = sP[len - 1], l0 = sP[0];
-        const float lnext = (s + len < L && p.mask_kind != MASK_LIT) ? ell(s + len) : 0.f;
+        const float T_c = sP[len - 1], l0 = sP[0], lnext = *sLn;
         for (int t = threadIdx.x; t < CT; t += kThr) {
           const bool ok = t < len;
           // query factor of the state applied to this chunk, key weight in
@@ -216,7 +244,7 @@ __global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_
       __syncthreads();
       // ---- num: the chunk's own keys (left-to-right sweep), then the state
       if (fwd) {
-        dot_tiles(sQ, LD, sK, LD, CT, CT, D, [&](int i, int j, float sv) {
+        dot_tiles<RC, RC>(sQ, LD, sK, LD, CT, CT, D, [&](int i, int j, float sv) {
           const bool in = i < len && j < len && (!p.causal || j <= i);
           sS[j * LDS + i] = in ? sv * expf(-fabsf(sP[i] - sP[j])) : 0.f;
         });
@@ -230,7 +258,7 @@ __global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_
       }
       if (has_state) {
         if (fwd) __syncthreads();
-        dot_tiles(sQ, LD, sSt, LD, CT, D, D, [&](int i, int n, float val) {
+        dot_tiles<RC, RD>(sQ, LD, sSt, LD, CT, D, D, [&](int i, int n, float val) {
           sAcc[i * LD + n] = (fwd ? sAcc[i * LD + n] : 0.f) + sR[i] * val;
         });
         for (int i = threadIdx.x; i < CT; i += kThr) {
@@ -261,9 +289,7 @@ __global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_
         for (int i = threadIdx.x; i < len; i += kThr) den[s + i] = sAcc[i * LD + D];
       // ---- the state carried to the next chunk of the sweep
       if (carry) {
-        const float decay = fwd ? expf(sP[len - 1])
-                                : expf(sP[len - 1] - sP[0] +
-                                       ((s + len < L && p.mask_kind != MASK_LIT) ? ell(s + len) : 0.f));
+        const float decay = fwd ? expf(sP[len - 1]) : expf(sP[len - 1] - sP[0] + *sLn);
         outer_tiles(sV, LD, sK, LD, sW, D, D, CT,
                     [&](int n, int m, float val) { sSt[n * LD + m] = decay * sSt[n * LD + m] + val; });
         for (int m = threadIdx.x; m < D; m += kThr) {
@@ -279,10 +305,13 @@ __global__ void __launch_bounds__(kThr) chunk_tile_kernel(Problem p, float* den_
 
 template <typename T, int D, int CT>
 cudaError_t tile_launch(const Problem& p, float* ws, cudaStream_t s) {
+  const TileWs w((size_t)p.B * p.H * p.L, D);
+  cudaError_t e = launch_phi_rows<T, D>(p.q, p.k, ws + w.fq, ws + w.fk, (long)p.B * p.H * p.L, p.phi, s);
+  if (e != cudaSuccess) return e;
   const size_t bytes = sizeof(float) * TileCfg<D, CT>::floats;
   auto kern = chunk_tile_kernel<T, D, CT>;
   if (bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
   }
   kern<<<p.B * p.H, kThr, bytes, s>>>(p, ws);
@@ -299,6 +328,10 @@ cudaError_t tile_launch_ct(const Problem& p, float* ws, cudaStream_t s) {
 }  // namespace
 
 bool chunk_tile_supported(const Problem& p) { return p.chunk >= 1 && p.chunk <= kChunkTileMax; }
+
+size_t chunk_tile_workspace_bytes(int B, int H, int L, int d) {
+  return sizeof(float) * TileWs((size_t)B * H * L, d).total;
+}
 
 cudaError_t launch_chunk_tile(const Problem& p, float* ws, cudaStream_t s) {
   const bool bf = p.dtype == DT_BF16;

@@ -40,10 +40,13 @@ size_t rnn_workspace_bytes(int B, int H, int L, int d);
 cudaError_t launch_rnn_simt(const Problem& p, float* ws, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_chunk_simt(const Problem& p, float* ws_den /*[B*H*L]*/, cudaStream_t s);
 // The chunk form on the CUDA cores with register-tiled block products, for
-// chunks of at most kChunkTileMax tokens (same workspace as launch_chunk_simt).
+// chunks of at most kChunkTileMax tokens: a workspace of
+// chunk_tile_workspace_bytes (the normalisers and the features of every
+// token), two launches.
 constexpr int kChunkTileMax = 64;
 bool chunk_tile_supported(const Problem& p);
-cudaError_t launch_chunk_tile(const Problem& p, float* ws_den /*[B*H*L]*/, cudaStream_t s);
+size_t chunk_tile_workspace_bytes(int B, int H, int L, int d);
+cudaError_t launch_chunk_tile(const Problem& p, float* ws, cudaStream_t s);
 cudaError_t launch_rnn_step(const void* q, const void* k, const void* v, const float* log_lambda,
                             float* S, float* z, float* y_part, float* c_part, int B, int H,
                             int d, int mask_kind, int phi, int dtype, cudaStream_t s);
