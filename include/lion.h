@@ -151,10 +151,10 @@ size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk
  * "Q5").  Arguments as lion_attn_fwd_ex, in every form (FULL: keys up to the
  * row; RNN: the forward recurrence alone; CHUNK: the forward chunk scan and
  * the lower triangle of each chunk).  Computed on the CUDA cores in fp32,
- * chunk <= 1024.  Workspace: lion_attn_workspace_bytes of the form (the RNN
- * form's holds the features of every token besides B*H*L floats; CHUNK
- * needs B*H*L floats; FULL the features of every token at d = 64 and 128,
- * none at d = 16 and 32; NULL: stream-ordered allocation).
+ * chunk <= 1024.  Workspace: lion_attn_workspace_bytes of the form (B*H*L
+ * floats for RNN and CHUNK, plus the features of every token for RNN, for
+ * CHUNK with chunk <= 64, and for FULL at d = 64 and 128, which needs
+ * nothing else; NULL: stream-ordered allocation).
  */
 lion_status lion_attn_fwd_causal(const lion_args* a);
 
