@@ -551,6 +551,7 @@ lion_status lion_rnn_step(const void* q, const void* k, const void* v, const flo
   const void* ptrs[] = {q, k, v, S, z, y_part, c_part};
   for (const void* ptr : ptrs)
     if (!aligned(ptr, 4) || !device_accessible(ptr)) return LION_ERR_INVALID_ARG;
+  if (!aligned(S, 16)) return LION_ERR_INVALID_ARG;   // the state moves as float4 rows
   if (mask_kind != LION_MASK_LIT && !device_accessible(log_lambda)) return LION_ERR_INVALID_ARG;
   const int phi = lion::resolve_phi(mask_kind, LION_PHI_DEFAULT);
   return from_cuda(lion::launch_rnn_step(q, k, v, log_lambda, S, z, y_part, c_part, B, H, d,

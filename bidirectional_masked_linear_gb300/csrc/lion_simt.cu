@@ -141,8 +141,6 @@ __global__ void __launch_bounds__(256) full_simt_kernel(Problem p) {
   }
 }
 
-constexpr int kRnnSplit = 4;   // threads sharing one column of the state (rnn_step_kernel)
-
 // ----------------------------------------------------------------- CHUNK --
 constexpr int kPanel = 32;      // tokens per shared-memory panel
 
@@ -298,22 +296,36 @@ __global__ void __launch_bounds__(256) chunk_simt_kernel(Problem p, float* den_a
 }
 
 // ------------------------------------------------------------ RNN step --
+// One token of one direction for every head: a CTA per head, the state read
+// and written as float4 rows (four value columns a thread, the head's rows
+// split over the rest of the CTA), so that each row of S moves as whole
+// coalesced segments; the column sums of phi(q) . S are reduced through
+// shared memory.
+constexpr int kStepThreads = 256;
+
+template <int D>
+struct StepCfg {
+  static constexpr int CG = D / 4;                                   // float4 column groups
+  static constexpr int RG = kStepThreads / CG < D ? kStepThreads / CG : D;   // row groups
+  static constexpr int RPT = D / RG;                                 // rows per thread
+};
+
 template <typename T, int D>
-__global__ void __launch_bounds__(D * kRnnSplit) rnn_step_kernel(
+__global__ void __launch_bounds__(kStepThreads) rnn_step_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
     const float* __restrict__ log_lambda, float* __restrict__ S, float* __restrict__ z,
     float* __restrict__ y_part, float* __restrict__ c_part, int H, int mask_kind, int phi) {
-  constexpr int MS = D / kRnnSplit;
+  using C = StepCfg<D>;
   __shared__ float sQ[D], sK[D], sV[D];
-  const int bh = blockIdx.x, h = bh % H;
-  const int n = threadIdx.x / kRnnSplit, r = threadIdx.x % kRnnSplit;
-  for (int m = threadIdx.x; m < D; m += blockDim.x) {
+  __shared__ __align__(16) float red[C::RG][D];
+  const int bh = blockIdx.x, h = bh % H, t = threadIdx.x;
+  for (int m = t; m < D; m += blockDim.x) {
     sQ[m] = to_f32(q[(size_t)bh * D + m]);
     sK[m] = to_f32(k[(size_t)bh * D + m]);
     sV[m] = to_f32(v[(size_t)bh * D + m]);
   }
   __syncthreads();
-  if (threadIdx.x < 32) {
+  if (t < 32) {
     phi_rows_inplace(sQ, 1, 1, D, D, phi);   // warp 0 only: one row each
     phi_rows_inplace(sK, 1, 1, D, D, phi);
   }
@@ -323,33 +335,56 @@ __global__ void __launch_bounds__(D * kRnnSplit) rnn_step_kernel(
   else if (mask_kind == MASK_S) l = log_lambda[bh];
   const float lam = expf(l);
   float* Sh = S + (size_t)bh * D * D;
-  float* zh = z + (size_t)bh * D;
-  float y = 0.f, c = 0.f;
-  const float vn = sV[n];
+  const int cg = t % C::CG, rg = t / C::CG, n0 = 4 * cg;
+  if (rg < C::RG) {
+    const float4 v4 = *reinterpret_cast<const float4*>(sV + n0);
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int a = 0; a < MS; ++a) {
-    const int m = r * MS + a;
-    const float s_new = lam * Sh[(size_t)m * D + n] + sK[m] * vn;
-    Sh[(size_t)m * D + n] = s_new;
-    y += sQ[m] * s_new;
-  }
-  // z: the threads of column 0 own it
-  if (n == 0) {
-#pragma unroll
-    for (int a = 0; a < MS; ++a) {
-      const int m = r * MS + a;
-      const float z_new = lam * zh[m] + sK[m];
-      zh[m] = z_new;
-      c += sQ[m] * z_new;
+    for (int a = 0; a < C::RPT; ++a) {
+      const int m = rg + C::RG * a;
+      float4* row = reinterpret_cast<float4*>(Sh + (size_t)m * D + n0);
+      float4 s4 = *row;
+      const float km = sK[m], qm = sQ[m];
+      s4.x = fmaf(lam, s4.x, km * v4.x);
+      s4.y = fmaf(lam, s4.y, km * v4.y);
+      s4.z = fmaf(lam, s4.z, km * v4.z);
+      s4.w = fmaf(lam, s4.w, km * v4.w);
+      *row = s4;
+      y.x = fmaf(qm, s4.x, y.x);
+      y.y = fmaf(qm, s4.y, y.y);
+      y.z = fmaf(qm, s4.z, y.z);
+      y.w = fmaf(qm, s4.w, y.w);
     }
+    *reinterpret_cast<float4*>(&red[rg][n0]) = y;
   }
-  y += __shfl_xor_sync(0xffffffffu, y, 1);
-  y += __shfl_xor_sync(0xffffffffu, y, 2);
-  c += __shfl_xor_sync(0xffffffffu, c, 1);
-  c += __shfl_xor_sync(0xffffffffu, c, 2);
-  if (r == 0) {
-    y_part[(size_t)bh * D + n] = y;
-    if (n == 0) c_part[bh] = c;
+  // z and its dot product: one thread a row
+  float c = 0.f;
+  if (t < D) {
+    float* zh = z + (size_t)bh * D;
+    const float z_new = lam * zh[t] + sK[t];
+    zh[t] = z_new;
+    c = sQ[t] * z_new;
+  }
+  __syncthreads();
+  if (t < D) {
+    float y = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < C::RG; ++r) y += red[r][t];
+    y_part[(size_t)bh * D + t] = y;
+  }
+  // c = phi(q) . z: the first D threads hold the terms (whole warps, at most four)
+  __shared__ float cw[4];
+  if (t < 32 * ((D + 31) / 32)) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if ((t & 31) == 0) cw[t >> 5] = c;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float cs = 0.f;
+#pragma unroll
+    for (int w = 0; w < (D + 31) / 32; ++w) cs += cw[w];
+    c_part[bh] = cs;
   }
 }
 
@@ -407,7 +442,7 @@ template <typename T, int D>
 cudaError_t step_launch(const void* q, const void* k, const void* v, const float* ll, float* S,
                         float* z, float* y, float* c, int B, int H, int mask_kind, int phi,
                         cudaStream_t s) {
-  rnn_step_kernel<T, D><<<B * H, D * kRnnSplit, 0, s>>>(
+  rnn_step_kernel<T, D><<<B * H, kStepThreads, 0, s>>>(
       (const T*)q, (const T*)k, (const T*)v, ll, S, z, y, c, H, mask_kind, phi);
   return cudaGetLastError();
 }

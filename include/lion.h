@@ -167,7 +167,8 @@ lion_status lion_attn_fwd_causal(const lion_args* a);
  *   q, k, v     [B][H][d] in `dtype` (lion_dtype), device.
  *   log_lambda  LIT: ignored; D: [H]; S: [B][H] (this token's lambda; for
  *               the backward direction pass lambda of the token after it).
- *   S           [B][H][d][d] float32, row m = feature of phi(k), updated in place.
+ *   S           [B][H][d][d] float32, row m = feature of phi(k), updated in place;
+ *               16-byte aligned (LION_ERR_INVALID_ARG otherwise).
  *   z           [B][H][d] float32, updated in place.
  *   y_part      [B][H][d] float32 out;  c_part [B][H] float32 out.
  * The caller owns the state.  Combining the two directions into y_i uses

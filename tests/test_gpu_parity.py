@@ -275,6 +275,13 @@ def test_errors_on_gpu():
     with pytest.raises(lion.LionError):
         lion.attn_fwd(host, host, host, None, 0, lion.FORM_CHUNK,
                       out=torch.empty((1, 1, 16, 64), device="cuda"))
+    # the decode step's state moves as 16-byte rows: a state 4 bytes off is refused
+    x = torch.zeros((1, 1, 64), dtype=torch.bfloat16, device="cuda")
+    S = torch.zeros(64 * 64 + 1, device="cuda")[1:].view(1, 1, 64, 64)
+    z, yp, cp = (torch.zeros(s_, device="cuda") for s_ in ((1, 1, 64), (1, 1, 64), (1, 1)))
+    with pytest.raises(lion.LionError) as ei:
+        lion.rnn_step(x, x, x, None, S, z, yp, cp, lion.MASK_LIT)
+    assert ei.value.status == lion.ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("dtype", ("bf16", "fp32"))
@@ -303,12 +310,13 @@ def test_rnn_caller_workspace(oracle_mod, dtype):
     assert ei.value.status == lion.ERR_INVALID_ARG
 
 
-def test_rnn_step_matches_rnn_form(oracle_mod):
+@pytest.mark.parametrize("d", (16, 32, 64, 128))
+def test_rnn_step_matches_rnn_form(oracle_mod, d):
     """Feeding tokens one at a time through lion_rnn_step, forward and then
     backward (with lambda of the next token), and combining with the diagonal
-    removed once reproduces the operator."""
-    B, H, L, d = 2, 3, 24, 32
-    inp = synth.make_inputs(B, H, L, d, "s", "bf16", seed=12)
+    removed once reproduces the operator, at every head dim."""
+    B, H, L = 2, 3, 24
+    inp = synth.make_inputs(B, H, L, d, "s", "bf16", seed=12 + d)
     q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
     ll = inp["log_lambda"].cuda()
     yF = torch.empty((B, H, L, d), device="cuda")
@@ -337,7 +345,36 @@ def test_rnn_step_matches_rnn_form(oracle_mod):
     y = (yF.double() + yB.double() - sii[..., None] * v.double()) / (cF.double() + cB.double() - sii)[..., None]
     qq, kk, vv, lll = f64(inp)
     ref = oracle_mod.full(qq, kk, vv, lll, 2)
-    check(oracle_mod, y.cpu().numpy(), ref, inp, TOL_BF16)
+    check(oracle_mod, y.cpu().numpy(), ref, inp, TOL_BF16, label=f"rnn_step d={d}")
+
+
+def test_rnn_step_in_a_cuda_graph():
+    """A decode loop of lion_rnn_step calls captured into a CUDA graph and
+    replayed gives the bits of the same calls launched one by one."""
+    B, H, d, T = 4, 3, 64, 6
+    g = torch.Generator(device="cuda").manual_seed(77)
+    q, k, v = (torch.randn((T, B, H, d), device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
+    ll = torch.nn.functional.logsigmoid(torch.randn((T, B, H), device="cuda", generator=g) + 3.0)
+
+    def run(S, z, ys, cs):
+        for t in range(T):
+            lion.rnn_step(q[t], k[t], v[t], ll[t], S, z, ys[t], cs[t], lion.MASK_S,
+                          stream=torch.cuda.current_stream())
+
+    fresh = lambda: (torch.zeros((B, H, d, d), device="cuda"), torch.zeros((B, H, d), device="cuda"),
+                     torch.zeros((T, B, H, d), device="cuda"), torch.zeros((T, B, H), device="cuda"))
+    S0, z0, y0, c0 = fresh()
+    run(S0, z0, y0, c0)
+    S1, z1, y1, c1 = fresh()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        run(S1, z1, y1, c1)
+    S1.zero_()
+    z1.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in ((S0, S1), (z0, z1), (y0, y1), (c0, c1)):
+        assert torch.equal(a, b)
 
 
 # ----------------------------------------------------- full workloads ----
