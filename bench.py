@@ -458,6 +458,24 @@ def stream_bytes(B, H, d, in_bytes=2) -> int:
     return B * H * (2 * (d * d + d) * 4 + 3 * d * in_bytes + 4 + d * 4 + 4)
 
 
+def measure_causal(w, mask, form, chunk, steps, warmup, flush):
+    """The forward half alone (lion_attn_fwd_causal) on the workload's
+    inputs, with its workspace passed in; CUDA events, L2 flushed."""
+    inp = synth.make_inputs(w.B, w.H, w.L, w.d, mask, w.dtype, w.seed, w.lam)
+    dev = {k: (None if inp[k] is None else inp[k].cuda()) for k in ("q", "k", "v", "log_lambda")}
+    out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device="cuda")
+    fcode = lion.FORMS[form]
+    wsb = lion.workspace_bytes(w.B, w.H, w.L, w.d, fcode, max(chunk, 1))
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        lion.attn_fwd_causal(dev["q"], dev["k"], dev["v"], dev["log_lambda"], inp["mask"], fcode, max(chunk, 1),
+                             out=out, workspace=ws)
+
+    return time_device(call, steps, warmup, flush, stream)
+
+
 def measure_stream(B, H, d, mask, steps, warmup):
     """Decode: `steps` consecutive lion_rnn_step calls (one direction, one
     token each for B*H heads), every step's inputs resident in HBM before
@@ -808,6 +826,17 @@ def main():
                                               "frac": flb / (msrb * 1e-3) / 1e12 / FP32_ALU_PEAK_TFLOPS,
                                               "algorithmic_flops": flb}}
 
+    causal = None
+    if not args.no_streaming:
+        causal = []
+        for cform, cchunk in (("full", 0), ("chunk", 64), ("rnn", 0)):
+            tc = measure_causal(w, args.mask, cform, cchunk, 20, 3, flush)
+            msc = statistics.mean(tc)
+            causal.append({"workload": f"{w.name} B={w.B} H={w.H} L={w.L} d={w.d}", "mask": args.mask,
+                           "form": cform, "chunk": cchunk or None, "value": w.B * w.L / (msc * 1e-3),
+                           "unit": "tokens/s", "ms_per_call": msc,
+                           "path": "lion_attn_fwd_causal (the forward half), fp32 CUDA cores"})
+
     streaming = None
     if not args.no_streaming:
         ms_s, ms_eager = measure_stream(w.B, w.H, w.d, args.mask, 200, 10)
@@ -850,6 +879,7 @@ def main():
             "bf16_out": bf16_out,
             "backward": backward,
             "reordered": reordered,
+            "causal": causal,
             "streaming": streaming,
             "configs": configs,
         }
