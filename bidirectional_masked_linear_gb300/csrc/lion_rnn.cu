@@ -265,15 +265,15 @@ __global__ void __launch_bounds__(Split<D, G>::kThr) rnn_cols_kernel(Problem p, 
     for (int i = 0; i < ntiles; ++i) {
       const int t0 = tile_t0(i), nt = min(kTile, L - t0);
       uint8_t* slot = raw + (i & 1) * Y::kRaw;
+      // this tile landed and every thread is done with the previous one, so
+      // the next tile may go into the slot the one before it used
+      cp_wait<0>();
+      __syncthreads();
       if (i + 1 < ntiles) {
         const int t1 = tile_t0(i + 1);
         issue_tile<T, D, G, kTile, PRE>(raw + ((i + 1) & 1) * Y::kRaw, qsrc, ksrc, siisrc, v, n0, t1,
                                         min(kTile, L - t1));
-        cp_wait<1>();
-      } else {
-        cp_wait<0>();
       }
-      __syncthreads();
       // ---- the tile's features and s_ii, the v column table, the decays
       const float* tQ;
       const float* tK;
@@ -396,8 +396,8 @@ __global__ void __launch_bounds__(Split<D, G>::kThr) rnn_cols_kernel(Problem p, 
           }
         }
       }
-      __syncthreads();
     }
+    __syncthreads();   // the next sweep's first tile reuses slot 0
   };
   sweep(std::integral_constant<bool, true>{});
   if (!p.causal) sweep(std::integral_constant<bool, false>{});
