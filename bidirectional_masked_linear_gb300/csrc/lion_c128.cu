@@ -51,9 +51,13 @@
 // the state part of the row sum.  The ones of [V | 1] come from a 2 KB
 // constant tile addressed through the descriptor's leading byte offset.
 //
-// TMEM (512 columns): X_0^T then O_0 at [0, 80), X_1^T then O_1 at [80, 160),
-// S_0 at [160, 288), S_1 at [288, 416); P_c overwrites the first 64 columns
-// of S_c.
+// TMEM (512 columns): X_0^T at [0, 64), X_1^T then O_1 at [80, 160), S_0 at
+// [160, 288), S_1 at [288, 416), O_0 at [416, 496); P_c overwrites the first
+// 64 columns of S_c.  O_0 has columns of its own so that P_0 [V_0 | 1] can
+// start before X_0 has been read into its tile: group 0 hands P_0 to the MMA
+// thread two 16-column blocks at a time, and each pair's K steps run while
+// the group masks the next pair.  The state product follows the last pair, in
+// the same accumulation order as a single hand-off.
 //
 // Mask factors: within a chunk M_ij = alpha_i rho_j (j <= i) or rho_i alpha_j
 // (j > i) with alpha_t = exp(p_t - p_ref), rho_t = 1 / alpha_t and p_ref the
@@ -105,6 +109,7 @@ constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
 constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
 constexpr float kFoldMinSigma = 1.f / 32768.f;        // rows that fold 1/sigma into P
 constexpr uint32_t kSleepNs = 2000u;
+constexpr int KPB = 2;   // P blocks per hand-off
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr int OFF_Q = 0;                          // [slot][chunk] phi(Q) tiles; output staging
@@ -117,7 +122,7 @@ constexpr int OFF_FAC = OFF_ONES + 2048;          // [slot] float alpha[256], rh
 constexpr int OFF_INFO = OFF_FAC + 2 * 4 * kRows * 4;  // [slot] float[8] per-head scalars
 constexpr int OFF_RED = OFF_INFO + 2 * 8 * 4;     // [parity] float[32] prep scan scratch
 constexpr int OFF_BAR = OFF_RED + 2 * 32 * 4;
-constexpr int kNumBars = 24;
+constexpr int kNumBars = 28;
 constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -143,18 +148,22 @@ enum {
   B_QE0 = 19,     // + slot: Q tiles free: every epi warp's output store has read its staging
   B_ED0 = 21,     // + c: epi group c: O_c read (4 arrivals)
   B_DRAIN = 23,   // MMA commit used when unwinding
+  B_PP0 = 24,     // + pair: epi group 0: P_0 for keys [32 pair, 32 pair + 32) written (4 arrivals)
 };
 __device__ __forceinline__ uint32_t bar_count(int b, int nch) {
   if (b == B_KVR || b == B_QR) return kPrepWarps;
   if (b == B_PR0 || b == B_PR0 + 1 || b == B_ED0 || b == B_ED0 + 1) return 4;
+  if (b >= B_PP0 && b < B_PP0 + 4) return 4;
   if (b == B_QE0 || b == B_QE0 + 1) return 4 * nch;   // the warps of the groups with a chunk
   return 1;
 }
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t T_O = 0;       // + 80 c: the transposed state chunk c applies, then O_c
+constexpr uint32_t T_O = 0;       // + 80 c: the transposed state chunk c applies (chunk 1: then O_1)
 constexpr uint32_t T_S = 160;     // + 128 c: S_c, P_c in its first 64 columns
+constexpr uint32_t T_O0 = 416;    // O_0, apart from its state so that P_0 [V_0 | 1] can start early
+__device__ __forceinline__ uint32_t o_col(int c) { return c == 0 ? T_O0 : T_O + 80; }
 
 struct C128Params {
   const float* log_lambda;
@@ -315,7 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (states) {
           // the state group g applies comes from chunk 1 - g
           for (int g = 0; g < 2 && ok; ++g) {
-            if (n >= 1 && !waitb(B_ED0 + g, (n - 1) & 1)) ok = false;   // O_g of the previous head read
+            // X_1 shares its columns with O_1: wait until the previous head's O_1
+            // is read.  X_0 has columns of its own, read (into the state tile)
+            // before the previous head's O_0 was committed.
+            if (g == 1 && n >= 1 && !waitb(B_ED0 + g, (n - 1) & 1)) ok = false;
             if (!ok) break;
             tc_fence_after();
             const int c = 1 - g, nk = c == 0 ? nk0 : nk1;
@@ -330,23 +342,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars[B_KWE]);
           if (k_after_u) mma_commit(&bars[B_KE]);
         }
-        for (int c = 0; c < nch && ok; ++c) {
-          if (!states && n >= 1 && !waitb(B_ED0 + c, (n - 1) & 1)) ok = false;
-          if (ok && !waitb(B_PR0 + c, n & 1)) ok = false;
-          if (!ok) break;
-          tc_fence_after();
-          const int nk = c == 0 ? nk0 : nk1;
-          const uint32_t v = smem_u32(Vt(s, c));
-          uint64_t dv = mnmaj(v, 0, ones - v);
-          for (int k = 0; k < nk; ++k, dv += kMnmajOnesStep)
-            mma_tmem_a(tbase + T_O + 80 * c, tbase + T_S + 128 * c + 8 * k, dv, idPV, k > 0 ? 1u : 0u);
-          if (states) {
-            uint64_t dq = kmaj(Qt(s, c), 0), dx = kmaj(STt(c), 0);
+        // O_0 = P_0 [V_0 | 1] goes out a pair of 16-column blocks at a time, as
+        // group 0 writes P_0, then its state product once the state tile is
+        // written; then O_1, once group 1 has handed over P_1 and its state
+        // tile.  (A pair arrival of head n also means that group 0 has read
+        // O_0 of head n - 1: its warps arrive in that order.)
+        {
+          const int np0 = (nk0 + KPB - 1) / KPB;
+          auto o_state = [&](int c) {
+            if (states) {
+              uint64_t dq = kmaj(Qt(s, c), 0), dx = kmaj(STt(c), 0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k, dq += kKmajStep, dx += kKmajStep)
-              mma_bf16(tbase + T_O + 80 * c, dq, dx, idQX, 1u);
+              for (int k = 0; k < 4; ++k, dq += kKmajStep, dx += kKmajStep)
+                mma_bf16(tbase + o_col(c), dq, dx, idQX, 1u);
+            }
+            mma_commit(&bars[B_O0 + c]);
+          };
+          const uint32_t v0 = smem_u32(Vt(s, 0));
+          const uint64_t dv0 = mnmaj(v0, 0, ones - v0);
+          for (int kp = 0; kp < np0 && ok; ++kp) {
+            if (!waitb(B_PP0 + kp, n & 1)) { ok = false; break; }
+            tc_fence_after();
+            for (int k = KPB * kp; k < KPB * kp + KPB && k < nk0; ++k)
+              mma_tmem_a(tbase + T_O0, tbase + T_S + 8 * k, dv0 + (uint64_t)k * kMnmajOnesStep, idPV,
+                         k > 0 ? 1u : 0u);
           }
-          mma_commit(&bars[B_O0 + c]);
+          if (ok && waitb(B_PR0, n & 1)) {
+            tc_fence_after();
+            o_state(0);
+          } else {
+            ok = false;
+          }
+          if (ok && nch == 2) {
+            if (waitb(B_PR0 + 1, n & 1)) {
+              tc_fence_after();
+              const uint32_t v = smem_u32(Vt(s, 1));
+              uint64_t dv = mnmaj(v, 0, ones - v);
+              for (int k = 0; k < nk1; ++k, dv += kMnmajOnesStep)
+                mma_tmem_a(tbase + o_col(1), tbase + T_S + 128 + 8 * k, dv, idPV, k > 0 ? 1u : 0u);
+              o_state(1);
+            } else {
+              ok = false;
+            }
+          }
         }
         if (!ok) break;
         mma_commit(&bars[B_VE0 + s]);
@@ -525,6 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sg = states && row_ok ? f[2 * kRows + tok] : 1.f;
       const bool fold = states && MASK != MASK_LIT && PHI == PHI_SILU_L2 && sg >= kFoldMinSigma &&
                         (exact || fmaxf(ai, ri) <= 1e33f);
+      // group 0 hands P_0 over a pair of blocks at a time (warps without rows,
+      // and all warps after an abort, arrive for every pair)
+      const int npair = g == 0 ? (nk + KPB - 1) / KPB : 0;
+      int handed = 0;
       if (good && warp_ok) {
         if (fold) {
           const float is = rcp(sg);
@@ -559,8 +601,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               reg_fence16(sb0);
             }
           }
+          if (g == 0 && ((jj + 2) % KPB == 0 || jj + 2 >= nk)) {
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_PP0 + handed]);
+            ++handed;
+          }
         }
       }
+      for (; handed < npair; ++handed)
+        if (lane == 0) mbar_arrive(&bars[B_PP0 + handed]);
       // ---- the state tile this chunk applies (K-major, rows = output
       //      columns, row 64 = z) and the decay-scaled phi(q)
       if (states) {
@@ -632,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
       if (good && warp_ok) {
-        const uint32_t oa = tbase + lane_off + T_O + 80 * g;
+        const uint32_t oa = tbase + lane_off + o_col(g);
         uint8_t* stg = Qt(s, g) + 32 * q * 128;
         float ob0[16], ob1[16];
         tmem_ld16(oa + 64, ob1);            // column 64: the row sum
