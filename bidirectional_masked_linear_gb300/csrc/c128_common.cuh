@@ -148,6 +148,11 @@ __device__ __forceinline__ void reg_fence16(float* v) {
                "+f"(v[14]), "+f"(v[15]));
 }
 
+__device__ __forceinline__ void reg_fence8(float* v) {
+  asm volatile("" : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+               "+f"(v[7]));
+}
+
 __device__ __forceinline__ uint64_t kmaj(const uint8_t* tile, int k) {
   return desc_sw128(smem_u32(tile) + 32 * k, 16, 1024);
 }

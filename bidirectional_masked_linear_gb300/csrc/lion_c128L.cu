@@ -631,10 +631,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!waitb(B_S, n & 1)) good = false;
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
-      // this step's scalars, read now: once its output product is done the
-      // slot (and with it these factors) may be refilled for step n + 2
-      const float dec = MASK == MASK_LIT ? 1.f : __expf(info(s)[I_T]);
-      const float a_out = f[2 * kC + i], b_out = f[3 * kC + i];
       if (good && warp_ok && hc < nk) {
         const bool exact = info(s)[I_EXACT] != 0.f;
         const float ai = alpha[i], ri = rho[i], pi = pp[i];
@@ -661,6 +657,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // this step's scalars, read before P is handed over (the output product
+      // needs P): once that product is done the slot, and with it these
+      // factors, may be refilled for step n + 2.  Read here rather than before
+      // the mask, they hold no registers through it.
+      const float dec = MASK == MASK_LIT ? 1.f : __expf(info(s)[I_T]);
+      const float a_out = f[2 * kC + i], b_out = f[3 * kC + i];
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -712,59 +714,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t base = tbase + lane_off;
         uint8_t* stg = smem + OFF_STG + ew * 4096;
         uint8_t* row = stg + lane * 128;
-        float o[16], tt[16], rr[16];
         float2 inv2 = make_float2(0.f, 0.f);
+        {
+          // column 64, the row sums
+          float z[3];
+          z[0] = tmem_ld1(base + T_O + 64);
+          z[1] = tmem_ld1(base + T_T + 64);
+          z[2] = tmem_ld1(base + T_R + 64);
+          tmem_wait_ld();
+          asm volatile("" : "+f"(z[0]), "+f"(z[1]), "+f"(z[2]));
+          const float den = z[0] + a_out * z[1] + b_out * z[2];
+          const float inv = 1.f / den;
+          // a score past the fp16 range (unbounded features) leaves the row sum
+          // non-finite: fp16 operands cannot make an fp32 sum overflow otherwise
+          if (!(fabsf(den) <= 3.0e38f)) *s_range = 1;
+          inv2 = make_float2(inv, inv);
+        }
 #pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int col = 32 * hc + 16 * h2;
-          tmem_ld16(base + T_O + col, o);
-          tmem_ld16(base + T_T + col, tt);
-          tmem_ld16(base + T_R + col, rr);
-          if (h2 == 0) {
-            // column 64, the row sums, with the first block
-            float z[3];
-            z[0] = tmem_ld1(base + T_O + 64);
-            z[1] = tmem_ld1(base + T_T + 64);
-            z[2] = tmem_ld1(base + T_R + 64);
-            tmem_wait_ld();
-            asm volatile("" : "+f"(z[0]), "+f"(z[1]), "+f"(z[2]));
-            const float den = z[0] + a_out * z[1] + b_out * z[2];
-            const float inv = 1.f / den;
-            // a score past the fp16 range (unbounded features) leaves the row sum
-            // non-finite: fp16 operands cannot make an fp32 sum overflow otherwise
-            if (!(fabsf(den) <= 3.0e38f)) *s_range = 1;
-            inv2 = make_float2(inv, inv);
-          } else {
-            tmem_wait_ld();
-          }
-          reg_fence16(o);
-          reg_fence16(tt);
-          reg_fence16(rr);
-          float yv[16];
+        for (int h4 = 0; h4 < 4; ++h4) {
+          const int col = 32 * hc + 8 * h4;
+          float o[8], tt[8], rr[8];
+          tmem_ld8(base + T_O + col, o);
+          tmem_ld8(base + T_T + col, tt);
+          tmem_ld8(base + T_R + col, rr);
+          tmem_wait_ld();
+          reg_fence8(o);
+          reg_fence8(tt);
+          reg_fence8(rr);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float2 x0 = make_float2(o[4 * e], o[4 * e + 1]), x1 = make_float2(o[4 * e + 2], o[4 * e + 3]);
-            x0 = fma2(a2, make_float2(tt[4 * e], tt[4 * e + 1]), x0);
-            x1 = fma2(a2, make_float2(tt[4 * e + 2], tt[4 * e + 3]), x1);
-            x0 = fma2(b2, make_float2(rr[4 * e], rr[4 * e + 1]), x0);
-            x1 = fma2(b2, make_float2(rr[4 * e + 2], rr[4 * e + 3]), x1);
-            x0 = mul2(x0, inv2);
-            x1 = mul2(x1, inv2);
-            yv[4 * e] = x0.x;
-            yv[4 * e + 1] = x0.y;
-            yv[4 * e + 2] = x1.x;
-            yv[4 * e + 3] = x1.y;
+            float2 x = make_float2(o[2 * e], o[2 * e + 1]);
+            x = fma2(a2, make_float2(tt[2 * e], tt[2 * e + 1]), x);
+            x = fma2(b2, make_float2(rr[2 * e], rr[2 * e + 1]), x);
+            x = mul2(x, inv2);
+            o[2 * e] = x.x;
+            o[2 * e + 1] = x.y;
           }
           if (prm.out_bf16) {
             // bfloat16: 64-byte staging rows, no swizzle
-#pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8)
-              *reinterpret_cast<uint4*>(stg + lane * 64 + ((2 * h2 + c8) << 4)) = pack8_bf(yv + 8 * c8);
+            *reinterpret_cast<uint4*>(stg + lane * 64 + (h4 << 4)) = pack8_bf(o);
           } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<float4*>(row + (((4 * h2 + e) ^ (lane & 7)) << 4)) =
-                  make_float4(yv[4 * e], yv[4 * e + 1], yv[4 * e + 2], yv[4 * e + 3]);
+            for (int e = 0; e < 2; ++e)
+              *reinterpret_cast<float4*>(row + (((2 * h4 + e) ^ (lane & 7)) << 4)) =
+                  make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
           }
         }
         fence_async_smem();
