@@ -140,6 +140,31 @@ __device__ __forceinline__ void phi_part(float* x, uint32_t peers) {
   }
 }
 
+// The inclusive prefix of l over a 128-token chunk, taken by one warp on its
+// own: lane w holds l of tokens 4w .. 4w + 3 in e[0..3].  Returns in *p the
+// prefix at token t (any token of the chunk), in *T the chunk's sum and in
+// *first l at its first token.
+__device__ __forceinline__ void chunk_prefix_warp(const float* e, int t, float* p, float* T, float* first) {
+  const int lane = threadIdx.x & 31;
+  const float a0 = e[0], a1 = a0 + e[1], a2 = a1 + e[2], a3 = a2 + e[3];
+  float x = a3;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  float ex = __shfl_up_sync(0xffffffffu, x, 1);
+  if (lane == 0) ex = 0.f;
+  const int sl = t >> 2, r = t & 3;
+  const float v0 = __shfl_sync(0xffffffffu, ex + a0, sl);
+  const float v1 = __shfl_sync(0xffffffffu, ex + a1, sl);
+  const float v2 = __shfl_sync(0xffffffffu, ex + a2, sl);
+  const float v3 = __shfl_sync(0xffffffffu, ex + a3, sl);
+  *p = r == 0 ? v0 : r == 1 ? v1 : r == 2 ? v2 : v3;
+  *T = __shfl_sync(0xffffffffu, x, 31);
+  *first = __shfl_sync(0xffffffffu, e[0], 0);
+}
+
 // Orders every later use of v[0..15] after the preceding tcgen05.wait::ld
 // (the TMEM load writes its registers asynchronously).
 __device__ __forceinline__ void reg_fence16(float* v) {

@@ -82,8 +82,7 @@ constexpr int OFF_STG = OFF_ONES + 2048;              // [8 epi warps] 4 KB outp
 constexpr int OFF_GSEG = OFF_STG + kEpiWarps * 4096;  // the segment's entering backward state (fp32 [64][80])
 constexpr int OFF_FAC = OFF_GSEG + kGsegBytes;        // [slot] alpha, rho, a, b, p [128] each
 constexpr int OFF_INFO = OFF_FAC + 2 * 5 * kC * 4;    // [slot] float[8] per-chunk scalars
-constexpr int OFF_RED = OFF_INFO + 2 * 8 * 4;         // [parity] float[32] prep scan scratch
-constexpr int OFF_BAR = OFF_RED + 2 * 32 * 4;
+constexpr int OFF_BAR = OFF_INFO + 2 * 8 * 4;
 constexpr int kNumBars = 24;
 constexpr int OFF_TSLOT = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_TSLOT + 16 + 1024;     // + alignment slack
@@ -390,24 +389,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = pt >> 2, qq = pt & 3;      // token within the chunk, quarter row
     const int j0 = 2 * qq;                   // first 16-byte chunk of this quarter row
     const uint32_t peers = 0xfu << (lane & 28);
-    float* red = reinterpret_cast<float*>(smem + OFF_RED);
     bool good = true;
     Step st;
     st.item = blockIdx.x;
     if (st.valid(prm)) st.set_item(prm, st.item);
-    float ell_next = 0.f, lnext_next = 0.f;
+    // l of the chunk's tokens 4 lane .. 4 lane + 3 (every warp takes the whole
+    // chunk's prefix by itself)
+    float ell_next[4] = {0.f, 0.f, 0.f, 0.f}, lnext_next = 0.f;
     auto load_ell = [&](const Step& x, float* e, float* en) {
       const int bh = x.item / prm.nseg;
       const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
-      *e = ell_at<MASK>(prm, bh, kC * x.c + t, lh);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) e[r] = ell_at<MASK>(prm, bh, kC * x.c + 4 * lane + r, lh);
       *en = ell_at<MASK>(prm, bh, kC * x.c + kC, lh);   // first token after the chunk
     };
-    if (st.valid(prm)) load_ell(st, &ell_next, &lnext_next);
+    if (st.valid(prm)) load_ell(st, ell_next, &lnext_next);
     int ng = 0;                               // items started
     float cum = 0.f, tseg = 0.f, lafter = 0.f;
     for (int n = 0; st.valid(prm); ++n) {
       const int s = n & 1, tok = kC * st.c + t;
-      const float ell = ell_next, lnext = lnext_next;
+      float ell[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) ell[r] = ell_next[r];
+      const float lnext = lnext_next;
       const bool first = st.c == st.c_lo, last = st.c + 1 == st.c_hi;
       if (first) {
         // a new segment: bookkeeping for its backward entering state
@@ -418,37 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         cum = 0.f;
         ++ng;
       }
-      // ---- chunk-local inclusive prefix (each token's value sits in its four lanes)
-      float x = ell;
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      float* rd = red + 32 * (n & 1);
-      if (lane == 31) rd[pw] = x;
-      if (pt == 0) rd[16] = ell;
-      good = bar_and(1, kPrepWarps * 32, good);
-      if (!good) break;
+      // ---- chunk-local inclusive prefix
+      float p, T, pfirst;
+      chunk_prefix_warp(ell, t, &p, &T, &pfirst);
       {
         // the next step's decays, loaded a whole step ahead of their use
         Step nx = st;
         nx.next(prm);
-        if (nx.valid(prm)) load_ell(nx, &ell_next, &lnext_next);
+        if (nx.valid(prm)) load_ell(nx, ell_next, &lnext_next);
       }
-      // the warps' totals, one per lane, scanned: the chunk total and this
-      // warp's offset
-      float sc = lane < 16 ? rd[lane] : 0.f;
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, sc, o);
-        if (lane >= o) sc += y;
-      }
-      const float T = __shfl_sync(0xffffffffu, sc, 15);
-      const float pre_l = __shfl_sync(0xffffffffu, sc, (pw + 15) & 15);   // lane pw - 1 (warp-uniform)
-      const float pre = pw == 0 ? 0.f : pre_l;
-      const float p = x + pre;
-      const float pfirst = rd[16];
       const float pref = 0.5f * (pfirst + T);
       const bool exact = (pfirst - T) > 2.f * kMaxFactorRange;
       const bool live = tok < L;
