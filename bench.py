@@ -58,16 +58,16 @@ _CALL_KERNELS = {
 # (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
 # write) of one launch, from one ncu capture of that kernel
 TRAFFIC_PER_HEAD = {
-    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.5 MB written
-    ("lion_chunk128_tc_kernel", "4714b04341152b44a6e77620be92b69188a89821e7ff31dcf31c3da088bf9d3e",
-     "vit_b", "s", 128): (117487104 + 36458240) / 1536,
+    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 35.9 MB written
+    ("lion_chunk128_tc_kernel", "2a12a37b06baf9029ef769fc21c14bdcdf3dc972d8be05d46a5d9ea949712465",
+     "vit_b", "s", 128): (117497344 + 35942912) / 1536,
     # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the three launches of a call
-    ("lion_chunk128_pre_kernel", "9dc968e12456057e91acf188c514a6c666ec3436efb9613eafbe26e4f4f51fe9",
-     "hires_2496", "s", 128): (152065536 + 22592256) / 24,
-    ("lion_segment_scan_kernel", "854d0aae925c16c75ee9ec0c10566dbdf687c95c0d95be815082bc6c8564e31f",
-     "hires_2496", "s", 128): (5927936 + 0) / 24,
-    ("lion_chunk128_long_kernel", "21c67ce1f16cafde5a26baf936897e415f3ba832994a70b5f681f719df45893d",
-     "hires_2496", "s", 128): (271416064 + 111205632) / 24,
+    ("lion_chunk128_pre_kernel", "5614e7c9a10ee897e9b9fcded6621ed3d749c75625ebbf62434836e7b7127b02",
+     "hires_2496", "s", 128): (152017408 + 22167552) / 24,
+    ("lion_segment_scan_kernel", "ac12f62bec1d86b3ae2411f85f0b944900d000aba9eac5e8437a272651a52708",
+     "hires_2496", "s", 128): (5928192 + 0) / 24,
+    ("lion_chunk128_long_kernel", "1d02e7b98770e1ec9b943d6ae5568e5f5fe5d8121807750f0766cd2669bca465",
+     "hires_2496", "s", 128): (271000832 + 110137856) / 24,
 }
 
 

@@ -52,12 +52,13 @@
 // constant tile addressed through the descriptor's leading byte offset.
 //
 // TMEM (512 columns): X_0^T at [0, 64), X_1^T then O_1 at [80, 160), S_0 at
-// [160, 288), S_1 at [288, 416), O_0 at [416, 496); P_c overwrites the first
-// 64 columns of S_c.  O_0 has columns of its own so that P_0 [V_0 | 1] can
-// start before X_0 has been read into its tile: group 0 hands P_0 to the MMA
-// thread two 16-column blocks at a time, and each pair's K steps run while
-// the group masks the next pair.  The state product follows the last pair, in
-// the same accumulation order as a single hand-off.
+// [160, 288), S_1 at [288, 416), O_0 at [416, 496) (LION-S; see below); P_c overwrites the first
+// 64 columns of S_c.  For LION-S, O_0 has columns of its own so that
+// P_0 [V_0 | 1] can start before X_0 has been read into its tile: group 0
+// hands P_0 to the MMA thread two 16-column blocks at a time, and each pair's
+// K steps run while the group masks the next pair.  The state product follows
+// the last pair, in the same accumulation order as a single hand-off.  D and
+// LIT hand each chunk over once, with O_0 over X_0 at [0, 80).
 //
 // Mask factors: within a chunk M_ij = alpha_i rho_j (j <= i) or rho_i alpha_j
 // (j > i) with alpha_t = exp(p_t - p_ref), rho_t = 1 / alpha_t and p_ref the
@@ -109,7 +110,13 @@ constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = W_PREP + kPrepWarps;
 constexpr int kThreads = (W_EPI + kEpiWarps) * 32;   // 832
 constexpr float kFoldMinSigma = 1.f / 32768.f;        // rows that fold 1/sigma into P
 constexpr uint32_t kSleepNs = 2000u;
-constexpr int KPB = 2;   // P blocks per hand-off
+constexpr int KPB = 2;   // P blocks per hand-off (LION-S)
+// LION-S hands P_0 over in pairs of blocks, with O_0 in columns of its own
+// (its mask takes long enough for the earlier pairs' products to run under
+// it); D and LIT, whose cheaper masks gained nothing from it (and whose
+// builds then spilled), hand each chunk over once, with O_0 over X_0.
+template <int MASK>
+__host__ __device__ constexpr bool split_o() { return MASK == MASK_S; }
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr int OFF_Q = 0;                          // [slot][chunk] phi(Q) tiles; output staging
@@ -163,7 +170,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t T_O = 0;       // + 80 c: the transposed state chunk c applies (chunk 1: then O_1)
 constexpr uint32_t T_S = 160;     // + 128 c: S_c, P_c in its first 64 columns
 constexpr uint32_t T_O0 = 416;    // O_0, apart from its state so that P_0 [V_0 | 1] can start early
-__device__ __forceinline__ uint32_t o_col(int c) { return c == 0 ? T_O0 : T_O + 80; }
+template <int MASK>
+__device__ __forceinline__ uint32_t o_col(int c) { return c == 0 && split_o<MASK>() ? T_O0 : T_O + 80 * c; }
 
 struct C128Params {
   const float* log_lambda;
@@ -327,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // X_1 shares its columns with O_1: wait until the previous head's O_1
             // is read.  X_0 has columns of its own, read (into the state tile)
             // before the previous head's O_0 was committed.
-            if (g == 1 && n >= 1 && !waitb(B_ED0 + g, (n - 1) & 1)) ok = false;
+            if ((g == 1 || !split_o<MASK>()) && n >= 1 && !waitb(B_ED0 + g, (n - 1) & 1)) ok = false;
             if (!ok) break;
             tc_fence_after();
             const int c = 1 - g, nk = c == 0 ? nk0 : nk1;
@@ -347,43 +355,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         // written; then O_1, once group 1 has handed over P_1 and its state
         // tile.  (A pair arrival of head n also means that group 0 has read
         // O_0 of head n - 1: its warps arrive in that order.)
-        {
-          const int np0 = (nk0 + KPB - 1) / KPB;
-          auto o_state = [&](int c) {
+        if constexpr (split_o<MASK>()) {
+          {
+            const int np0 = (nk0 + KPB - 1) / KPB;
+            auto o_state = [&](int c) {
+              if (states) {
+                uint64_t dq = kmaj(Qt(s, c), 0), dx = kmaj(STt(c), 0);
+  #pragma unroll
+                for (int k = 0; k < 4; ++k, dq += kKmajStep, dx += kKmajStep)
+                  mma_bf16(tbase + o_col<MASK>(c), dq, dx, idQX, 1u);
+              }
+              mma_commit(&bars[B_O0 + c]);
+            };
+            const uint32_t v0 = smem_u32(Vt(s, 0));
+            const uint64_t dv0 = mnmaj(v0, 0, ones - v0);
+            for (int kp = 0; kp < np0 && ok; ++kp) {
+              if (!waitb(B_PP0 + kp, n & 1)) { ok = false; break; }
+              tc_fence_after();
+              for (int k = KPB * kp; k < KPB * kp + KPB && k < nk0; ++k)
+                mma_tmem_a(tbase + T_O0, tbase + T_S + 8 * k, dv0 + (uint64_t)k * kMnmajOnesStep, idPV,
+                           k > 0 ? 1u : 0u);
+            }
+            if (ok && waitb(B_PR0, n & 1)) {
+              tc_fence_after();
+              o_state(0);
+            } else {
+              ok = false;
+            }
+            if (ok && nch == 2) {
+              if (waitb(B_PR0 + 1, n & 1)) {
+                tc_fence_after();
+                const uint32_t v = smem_u32(Vt(s, 1));
+                uint64_t dv = mnmaj(v, 0, ones - v);
+                for (int k = 0; k < nk1; ++k, dv += kMnmajOnesStep)
+                  mma_tmem_a(tbase + o_col<MASK>(1), tbase + T_S + 128 + 8 * k, dv, idPV, k > 0 ? 1u : 0u);
+                o_state(1);
+              } else {
+                ok = false;
+              }
+            }
+          }
+        } else {
+          for (int c = 0; c < nch && ok; ++c) {
+            if (!states && n >= 1 && !waitb(B_ED0 + c, (n - 1) & 1)) ok = false;
+            if (ok && !waitb(B_PR0 + c, n & 1)) ok = false;
+            if (!ok) break;
+            tc_fence_after();
+            const int nk = c == 0 ? nk0 : nk1;
+            const uint32_t v = smem_u32(Vt(s, c));
+            uint64_t dv = mnmaj(v, 0, ones - v);
+            for (int k = 0; k < nk; ++k, dv += kMnmajOnesStep)
+              mma_tmem_a(tbase + T_O + 80 * c, tbase + T_S + 128 * c + 8 * k, dv, idPV, k > 0 ? 1u : 0u);
             if (states) {
               uint64_t dq = kmaj(Qt(s, c), 0), dx = kmaj(STt(c), 0);
 #pragma unroll
               for (int k = 0; k < 4; ++k, dq += kKmajStep, dx += kKmajStep)
-                mma_bf16(tbase + o_col(c), dq, dx, idQX, 1u);
+                mma_bf16(tbase + T_O + 80 * c, dq, dx, idQX, 1u);
             }
             mma_commit(&bars[B_O0 + c]);
-          };
-          const uint32_t v0 = smem_u32(Vt(s, 0));
-          const uint64_t dv0 = mnmaj(v0, 0, ones - v0);
-          for (int kp = 0; kp < np0 && ok; ++kp) {
-            if (!waitb(B_PP0 + kp, n & 1)) { ok = false; break; }
-            tc_fence_after();
-            for (int k = KPB * kp; k < KPB * kp + KPB && k < nk0; ++k)
-              mma_tmem_a(tbase + T_O0, tbase + T_S + 8 * k, dv0 + (uint64_t)k * kMnmajOnesStep, idPV,
-                         k > 0 ? 1u : 0u);
-          }
-          if (ok && waitb(B_PR0, n & 1)) {
-            tc_fence_after();
-            o_state(0);
-          } else {
-            ok = false;
-          }
-          if (ok && nch == 2) {
-            if (waitb(B_PR0 + 1, n & 1)) {
-              tc_fence_after();
-              const uint32_t v = smem_u32(Vt(s, 1));
-              uint64_t dv = mnmaj(v, 0, ones - v);
-              for (int k = 0; k < nk1; ++k, dv += kMnmajOnesStep)
-                mma_tmem_a(tbase + o_col(1), tbase + T_S + 128 + 8 * k, dv, idPV, k > 0 ? 1u : 0u);
-              o_state(1);
-            } else {
-              ok = false;
-            }
           }
         }
         if (!ok) break;
@@ -565,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (exact || fmaxf(ai, ri) <= 1e33f);
       // group 0 hands P_0 over a pair of blocks at a time (warps without rows,
       // and all warps after an abort, arrive for every pair)
-      const int npair = g == 0 ? (nk + KPB - 1) / KPB : 0;
+      const int npair = g == 0 && split_o<MASK>() ? (nk + KPB - 1) / KPB : 0;
       int handed = 0;
       if (good && warp_ok) {
         if (fold) {
@@ -601,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               reg_fence16(sb0);
             }
           }
-          if (g == 0 && ((jj + 2) % KPB == 0 || jj + 2 >= nk)) {
+          if (split_o<MASK>() && g == 0 && ((jj + 2) % KPB == 0 || jj + 2 >= nk)) {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -683,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       good = __all_sync(0xffffffffu, good);
       tc_fence_after();
       if (good && warp_ok) {
-        const uint32_t oa = tbase + lane_off + o_col(g);
+        const uint32_t oa = tbase + lane_off + o_col<MASK>(g);
         uint8_t* stg = Qt(s, g) + 32 * q * 128;
         float ob0[16], ob1[16];
         tmem_ld16(oa + 64, ob1);            // column 64: the row sum
