@@ -52,8 +52,9 @@
 // constant tile addressed through the descriptor's leading byte offset.
 //
 // TMEM (512 columns): X_0^T at [0, 64), X_1^T then O_1 at [80, 160), S_0 at
-// [160, 288), S_1 at [288, 416), O_0 at [416, 496) (LION-S; see below); P_c overwrites the first
-// 64 columns of S_c.  For LION-S, O_0 has columns of its own so that
+// [160, 288), S_1 at [288, 416), O_0 at [416, 496) (LION-S; see below); P_c
+// overwrites the first 64 columns of S_c.  For LION-S, O_0 has columns of its
+// own so that
 // P_0 [V_0 | 1] can start before X_0 has been read into its tile: group 0
 // hands P_0 to the MMA thread two 16-column blocks at a time, and each pair's
 // K steps run while the group masks the next pair.  The state product follows
