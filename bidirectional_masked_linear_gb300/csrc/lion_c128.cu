@@ -54,12 +54,11 @@
 // TMEM (512 columns): X_0^T at [0, 64), X_1^T then O_1 at [80, 160), S_0 at
 // [160, 288), S_1 at [288, 416), O_0 at [416, 496) (LION-S; see below); P_c
 // overwrites the first 64 columns of S_c.  For LION-S, O_0 has columns of its
-// own so that
-// P_0 [V_0 | 1] can start before X_0 has been read into its tile: group 0
-// hands P_0 to the MMA thread two 16-column blocks at a time, and each pair's
-// K steps run while the group masks the next pair.  The state product follows
-// the last pair, in the same accumulation order as a single hand-off.  D and
-// LIT hand each chunk over once, with O_0 over X_0 at [0, 80).
+// own so that P_0 [V_0 | 1] can start before X_0 has been read into its tile:
+// group 0 hands P_0 to the MMA thread two 16-column blocks at a time, and each
+// pair's K steps run while the group masks the next pair.  The state product
+// follows the last pair, in the same accumulation order as a single hand-off.
+// D and LIT hand each chunk over once, with O_0 over X_0 at [0, 80).
 //
 // Mask factors: within a chunk M_ij = alpha_i rho_j (j <= i) or rho_i alpha_j
 // (j > i) with alpha_t = exp(p_t - p_ref), rho_t = 1 / alpha_t and p_ref the
