@@ -163,10 +163,12 @@ __device__ __forceinline__ float ell_at(const LongParams& p, int bh, int t, floa
 // + gridDim.x, ...; the 128-token chunks of each item left to right.
 struct Step {
   int item, c, c_lo, c_hi;   // chunk c of [c_lo, c_hi)
+  int bh, seg;               // the item's head and segment
   __device__ void set_item(const LongParams& p, int it) {
     item = it;
+    bh = it / p.nseg;
+    seg = it - bh * p.nseg;
     const int nch = (p.L + kC - 1) / kC;
-    const int seg = it % p.nseg;
     c_lo = 2 * seg * p.SEGB;
     c_hi = min(nch, 2 * (seg + 1) * p.SEGB);
     c = c_lo;
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int s = n & 1;
         if (ld.valid(prm) && (n < 2 || mbar_try_wait(&bars[B_KE0 + s], ((n >> 1) - 1) & 1))) {
-          const int bh = ld.item / prm.nseg;
+          const int bh = ld.bh;
           mbar_arrive_expect_tx(&bars[B_LD0 + s], (uint32_t)(3 * kTile + kGstBytes));
           tma_load_3d(Vt(s), &mapV, &bars[B_LD0 + s], 0, kC * ld.c, bh);
           tma_load_3d(Kt(s), &mapK, &bars[B_LD0 + s], 0, kC * ld.c, bh);
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             Step pf = ld;
             pf.next(prm);
             if (pf.valid(prm)) {
-              const int bhp = pf.item / prm.nseg;
+              const int bhp = pf.bh;
               tma_prefetch_3d(&mapV, 0, kC * pf.c, bhp);
               tma_prefetch_3d(&mapK, 0, kC * pf.c, bhp);
               tma_prefetch_3d(&mapQ, 0, kC * pf.c, bhp);
@@ -397,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's prefix by itself)
     float ell_next[4] = {0.f, 0.f, 0.f, 0.f}, lnext_next = 0.f;
     auto load_ell = [&](const Step& x, float* e, float* en) {
-      const int bh = x.item / prm.nseg;
+      const int bh = x.bh;
       const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) e[r] = ell_at<MASK>(prm, bh, kC * x.c + 4 * lane + r, lh);
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool first = st.c == st.c_lo, last = st.c + 1 == st.c_hi;
       if (first) {
         // a new segment: bookkeeping for its backward entering state
-        const int bh = st.item / prm.nseg, seg = st.item % prm.nseg;
+        const int bh = st.bh, seg = st.seg;
         tseg = __ldg(prm.segsum + (size_t)st.item * kSegSumFloats + 2 * 64 * kLongStateCols);
         const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
         lafter = ell_at<MASK>(prm, bh, 256 * min(prm.NBL, (seg + 1) * prm.SEGB), lh);
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     st.item = blockIdx.x;
     if (st.valid(prm)) st.set_item(prm, st.item);
     for (int n = 0; st.valid(prm) && good; ++n) {
-      const int s = n & 1, c = st.c, nk = nk_of(c), bh = st.item / prm.nseg;
+      const int s = n & 1, c = st.c, nk = nk_of(c), bh = st.bh;
       const bool first = c == st.c_lo, last = c + 1 == st.c_hi, warp_ok = kC * c + 32 * q < L;
       const float* f = fac(s);
       const float* alpha = f;

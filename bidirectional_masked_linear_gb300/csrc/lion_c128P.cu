@@ -120,10 +120,12 @@ __device__ __forceinline__ float ell_at(const PreParams& p, int bh, int t, float
 // + gridDim.x, ...; the 128-token chunks of each item right to left.
 struct Step {
   int item, c, c_lo, c_hi;   // chunk c of [c_lo, c_hi)
+  int bh, seg;               // the item's head and segment
   __device__ void set_item(const PreParams& p, int it) {
     item = it;
+    bh = it / p.nseg;
+    seg = it - bh * p.nseg;
     const int nch = (p.L + kC - 1) / kC;
-    const int seg = it % p.nseg;
     c_lo = 2 * seg * p.SEGB;
     c_hi = min(nch, 2 * (seg + 1) * p.SEGB);
     c = c_hi - 1;
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ld.valid(prm) && !*s_abort) {
         const int s = n & 1;
         if (n < 2 || mbar_try_wait(&bars[B_KVE0 + s], ((n >> 1) - 1) & 1)) {
-          const int bh = ld.item / prm.nseg;
+          const int bh = ld.bh;
           mbar_arrive_expect_tx(&bars[B_LD0 + s], (uint32_t)(2 * kTile));
           tma_load_3d(Kt(s), &mapK, &bars[B_LD0 + s], 0, kC * ld.c, bh);
           tma_load_3d(Vt(s), &mapV, &bars[B_LD0 + s], 0, kC * ld.c, bh);
@@ -207,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             Step pf = ld;
             pf.next(prm);
             if (pf.valid(prm)) {
-              tma_prefetch_3d(&mapK, 0, kC * pf.c, pf.item / prm.nseg);
-              tma_prefetch_3d(&mapV, 0, kC * pf.c, pf.item / prm.nseg);
+              tma_prefetch_3d(&mapK, 0, kC * pf.c, pf.bh);
+              tma_prefetch_3d(&mapV, 0, kC * pf.c, pf.bh);
             }
           }
           idle0 = clock64();
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk's prefix by itself)
     float ell_next[4] = {0.f, 0.f, 0.f, 0.f}, lnext_next = 0.f;
     auto load_ell = [&](const Step& x, float* e, float* en) {
-      const int bh = x.item / prm.nseg;
+      const int bh = x.bh;
       const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) e[r] = ell_at<MASK>(prm, bh, kC * x.c + 4 * lane + r, lh);
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (st.valid(prm)) st.set_item(prm, st.item);
     float tsum = 0.f;
     for (int n = 0; st.valid(prm); ++n) {
-      const int s = n & 1, c = st.c, bh = st.item / prm.nseg;
+      const int s = n & 1, c = st.c, bh = st.bh;
       const bool first = c == st.c_hi - 1, last = c == st.c_lo;
       if (first) tsum = 0.f;
       // ---- the state entering this chunk from the right, out as its fp16 tile
