@@ -800,6 +800,33 @@ def test_host_entry_matches_device_entry(mask):
         lion.attn_fwd_host(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], "chunk", 64)
 
 
+# Consecutive calls on two caller streams in turn (how a serving loop issues
+# batches, and how bench.py times the end-to-end path): the calls share the
+# library's copy streams, and one call's copies in overlap the previous call's
+# compute and copies out.  Each batch's output must still be its own, bit for
+# bit the device entry point's.
+@pytest.mark.gpu
+def test_host_entry_on_two_streams_in_turn():
+    B, H, L = 6, 3, 197
+    batches = [synth.make_inputs(B, H, L, 64, "s", "bf16", seed=1400 + i) for i in range(4)]
+    wants = []
+    for inp in batches:
+        g = _cuda(inp)
+        wants.append(lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], inp["mask"], "chunk", 128).cpu())
+    hosts = [{k: inp[k].contiguous().pin_memory() for k in ("q", "k", "v", "log_lambda")} for inp in batches]
+    outs = [torch.empty((B, H, L, 64), dtype=torch.float32).pin_memory() for _ in batches]
+    streams = [torch.cuda.current_stream(), torch.cuda.Stream()]
+    for rep in range(3):
+        for o in outs:
+            o.fill_(float("nan"))
+        for i, (h, o) in enumerate(zip(hosts, outs)):
+            lion.attn_fwd_host(h["q"], h["k"], h["v"], h["log_lambda"], "s", "chunk", 128, out=o,
+                               slices=1 if rep == 0 else rep + 1, stream=streams[i % 2])
+        torch.cuda.synchronize()
+        for i, (o, want) in enumerate(zip(outs, wants)):
+            assert torch.equal(o, want), (rep, i)
+
+
 # --------------------------------------------------- bfloat16 output -----
 # out_bf16: the chunk-128 kernels store y as bfloat16 themselves; the other
 # paths round an fp32 temporary.  Either way each value must be the fp32
