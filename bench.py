@@ -58,16 +58,16 @@ _CALL_KERNELS = {
 # (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
 # write) of one launch, from one ncu capture of that kernel
 TRAFFIC_PER_HEAD = {
-    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 35.9 MB written
-    ("lion_chunk128_tc_kernel", "2a12a37b06baf9029ef769fc21c14bdcdf3dc972d8be05d46a5d9ea949712465",
-     "vit_b", "s", 128): (117497344 + 35942912) / 1536,
+    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.3 MB written
+    ("lion_chunk128_tc_kernel", "dae441bb30eaca7d5dc775985d93741c8efca2d56458614e586ed0f43f2c4691",
+     "vit_b", "s", 128): (117506304 + 36263936) / 1536,
     # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the three launches of a call
-    ("lion_chunk128_pre_kernel", "5614e7c9a10ee897e9b9fcded6621ed3d749c75625ebbf62434836e7b7127b02",
-     "hires_2496", "s", 128): (152017408 + 22167552) / 24,
+    ("lion_chunk128_pre_kernel", "aa1280094c62fe3ed580ba4a396ed0e1f3975eb3b8a8f370a5390b2debda4cf0",
+     "hires_2496", "s", 128): (152019712 + 22125824) / 24,
     ("lion_segment_scan_kernel", "ac12f62bec1d86b3ae2411f85f0b944900d000aba9eac5e8437a272651a52708",
-     "hires_2496", "s", 128): (5928192 + 0) / 24,
-    ("lion_chunk128_long_kernel", "1d02e7b98770e1ec9b943d6ae5568e5f5fe5d8121807750f0766cd2669bca465",
-     "hires_2496", "s", 128): (271000832 + 110137856) / 24,
+     "hires_2496", "s", 128): (5928960 + 0) / 24,
+    ("lion_chunk128_long_kernel", "cd9945a38a4e5f5729ecda5815a0f8857f6308324ce504c3b00c8b866cec7641",
+     "hires_2496", "s", 128): (271020544 + 110052864) / 24,
 }
 
 
