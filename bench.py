@@ -125,19 +125,37 @@ def algorithmic_bytes(w, mask: str, out_bytes: int = 4) -> int:
     return b
 
 
-def kernels_per_call(form: str, chunk: int, w, mask: str = "s") -> int:
+def _sm_count() -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+
+
+def long_segments(w, sms: int) -> int:
+    """Segments a head's 256-token blocks are cut into on the long chunk
+    paths: enough that B*H*segments fills the SMs, one when the heads alone
+    do."""
+    nbl = (w.L + 255) // 256
+    bh = w.B * w.H
+    nseg = min(nbl, max(1, sms // bh)) if nbl > 1 and bh < sms else 1
+    segb = (nbl + nseg - 1) // nseg
+    return (nbl + segb - 1) // segb
+
+
+def kernels_per_call(form: str, chunk: int, w, mask: str = "s", sms: int = 152) -> int:
     """Kernel launches one operator call makes: the tensor-core chunk paths
     (bf16, d=64, chunk 64 or 128) take one launch up to 256 tokens and three
-    (pre-pass, segment scan, main pass) beyond; the recurrent form two with
-    its workspace (the features of every token, then the column CTAs); the
-    full form at d = 64 and 128 two (the features, the tiled pass), three
-    for LION-S (its prefix first); every other path one."""
+    (pre-pass, segment scan, main pass) beyond, chunk 128 two when every
+    head is one segment (no scan); the recurrent form two with its workspace
+    (the features of every token, then the column CTAs); the full form at
+    d = 64 and 128 two (the features, the tiled pass), three for LION-S (its
+    prefix first); every other path one."""
     tc = form == "chunk" and chunk in (64, 128) and w.d == 64 and w.dtype == "bf16"
     if form == "rnn":
         return 2
     if form == "full" and w.d in (64, 128):
         return 3 if mask == "s" else 2
-    return 3 if tc and w.L > 256 else 1
+    if tc and w.L > 256:
+        return 2 if chunk == 128 and long_segments(w, sms) == 1 else 3
+    return 1
 
 
 class Clocks:
@@ -639,7 +657,7 @@ def measure_config(c, flush, hbm_peak, steps=20, warmup=3):
     line = {"workload": f"{w.name} B={w.B} H={w.H} L={w.L} d={w.d}", "mask": mask, "form": form,
             "chunk": chunk if form == "chunk" else None, "input_dtype": w.dtype,
             "value": w.B * w.L / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "launches_per_call": kernels_per_call(form, chunk, w, mask),
+            "launches_per_call": kernels_per_call(form, chunk, w, mask, _sm_count()),
             "path": path_name(form, chunk, w)}
     b = algorithmic_bytes(w, mask)
     hbm = {"bound": "hbm", "achieved": b / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -748,7 +766,7 @@ def main():
         tr2, tr2k = traffic_bytes(w2, args.mask if args.mask != "lit" else "s", HIRES_CHUNK)
         secondary = {"workload": f"{w2.name} B={w2.B} H={w2.H} L={w2.L} d={w2.d}", "chunk": HIRES_CHUNK,
                      "value": w2.B * w2.L / (ms2 * 1e-3), "unit": "tokens/s", "ms_per_step": ms2,
-                     "launches_per_call": kernels_per_call("chunk", HIRES_CHUNK, w2),
+                     "launches_per_call": kernels_per_call("chunk", HIRES_CHUNK, w2, "s", _sm_count()),
                      "roofline": {"bound": "hbm", "achieved": b2 / (ms2 * 1e-3) / 1e9,
                                   "peak": hbm_peak, "unit": "GB/s",
                                   "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak,
@@ -879,7 +897,7 @@ def main():
                          "peak_source": peak_src, "algorithmic_bytes": abytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * kernels_per_call(args.form, args.chunk, w, args.mask),
+            "gpu_launches": args.steps * kernels_per_call(args.form, args.chunk, w, args.mask, _sm_count()),
             "clocks": clocks,
             "wall_s_timed_region": t_wall,
             "secondary": secondary,

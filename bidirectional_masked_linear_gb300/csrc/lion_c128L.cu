@@ -257,6 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ld.set_item(prm, ld.item);
         gs.set_item(prm, gs.item);
       }
+      // one segment a head: the entering states are zero, nothing to load
+      if (prm.nseg == 1) gs.item = prm.BH;
       int n = 0, ng = 0;   // steps issued; segment states issued
       int issued_ld[2] = {0, 0};
       long long idle0 = clock64();
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (first) {
         // a new segment: bookkeeping for its backward entering state
         const int bh = st.bh, seg = st.seg;
-        tseg = __ldg(prm.segsum + (size_t)st.item * kSegSumFloats + 2 * 64 * kLongStateCols);
+        tseg = prm.nseg > 1 ? __ldg(prm.segsum + (size_t)st.item * kSegSumFloats + 2 * 64 * kLongStateCols) : 0.f;
         const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
         lafter = ell_at<MASK>(prm, bh, 256 * min(prm.NBL, (seg + 1) * prm.SEGB), lh);
         cum = 0.f;
@@ -524,9 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- X_G = pre-pass state + decay * the segment's backward entering
       //      state, in place in the slot's pre-pass tile (row i = state column
       //      i, 64 = z; this thread: row t, state rows m = 16 qq .. 16 qq + 15)
-      if (first && !waitb(B_GS, (ng - 1) & 1)) good = false;
+      // (one segment a head: no entering state, X_G is the tile as loaded)
+      if (prm.nseg > 1 && first && !waitb(B_GS, (ng - 1) & 1)) good = false;
       good = __all_sync(0xffffffffu, good);
-      if (good && t < 65) {
+      if (prm.nseg > 1 && good && t < 65) {
         // exp(P at the first token after the segment - P at the first token after the chunk)
         const float fdec = __expf(tseg - (cum + T) - lnext + lafter);
         uint8_t* grow = Gt(s) + t * 128;
@@ -601,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = st_row ? __ldg(fin + (32 * hc + 16 * h2 + e) * kLongStateCols + i) : 0.f;
+            for (int e = 0; e < 16; ++e)
+              v[e] = st_row && prm.nseg > 1 ? __ldg(fin + (32 * hc + 16 * h2 + e) * kLongStateCols + i) : 0.f;
             tmem_st16(tbase + lane_off + T_F + 32 * hc + 16 * h2, v);
           }
           tmem_wait_st();
@@ -802,8 +806,12 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   float* segin = reinterpret_cast<float*>(gst + w.gst + w.segsum);
   cudaError_t e = launch_chunk128_pre(p, plan, gst, segsum, status, s);
   if (e != cudaSuccess) return e;
-  e = launch_segment_scan(p, plan, segsum, segin, s);
-  if (e != cudaSuccess) return e;
+  // with one segment a head there is nothing to chain: the main pass takes
+  // zero entering states and reads neither summaries nor scan output
+  if (plan.nseg > 1) {
+    e = launch_segment_scan(p, plan, segsum, segin, s);
+    if (e != cudaSuccess) return e;
+  }
   CUtensorMap mq, mk, mv, mo;
   const int BH = p.B * p.H;
   if (!make_map128(&mq, p.q, p.L, BH) || !make_map128(&mk, p.k, p.L, BH) || !make_map128(&mv, p.v, p.L, BH) ||

@@ -430,14 +430,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 16; ++e) g[e] = fmaf(dec, g[e], u[e]);
           }
           tmem_st16(tbase + lane_off + T_G + m0, g);
-          if (last && i < kLongStateCols) {
+          if (last && prm.nseg > 1 && i < kLongStateCols) {
             // column i of the backward summary is this lane's G (anchored at the
             // segment's first token), of the forward one its forward sum
             // (anchored at the segment's last token)
 #pragma unroll
             for (int e = 0; e < 16; ++e) ss[64 * kLongStateCols + (m0 + e) * kLongStateCols + i] = g[e];
           }
-          if (last) {
+          if (last && prm.nseg > 1) {
             tmem_ld16(tbase + lane_off + T_FA + m0, u);
             tmem_wait_ld();
             reg_fence16(u);
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (last && i == 0 && hc == 0) ss[2 * 64 * kLongStateCols] = tsum;
+        if (last && prm.nseg > 1 && i == 0 && hc == 0) ss[2 * 64 * kLongStateCols] = tsum;
         tmem_wait_st();
       }
       tc_fence_before();

@@ -54,6 +54,14 @@ def test_launch_counts():
     assert bench.kernels_per_call("chunk", 64, vit) == 1
     assert bench.kernels_per_call("chunk", 64, hires) == 3
     assert bench.kernels_per_call("chunk", 128, hires) == 3
+    # every head one segment (B*H at least the SMs, or fewer heads than half
+    # the SMs can split): pre-pass and main pass, no segment scan
+    assert bench.long_segments(hires, 152) == 6
+    assert bench.long_segments(synth.WORKLOADS["bert_large"], 152) == 1
+    assert bench.long_segments(synth.WORKLOADS["lra_4096"], 152) == 1
+    assert bench.kernels_per_call("chunk", 128, synth.WORKLOADS["bert_large"]) == 2
+    assert bench.kernels_per_call("chunk", 128, synth.WORKLOADS["lra_4096"]) == 2
+    assert bench.kernels_per_call("chunk", 64, synth.WORKLOADS["lra_4096"]) == 3
     assert bench.kernels_per_call("chunk", 32, hires) == 1
     assert bench.kernels_per_call("rnn", 0, hires) == 2     # features, then the column CTAs
     assert bench.kernels_per_call("full", 0, vit, "s") == 3   # prefix, features, the tiled pass

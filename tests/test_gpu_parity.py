@@ -143,9 +143,11 @@ def test_chunk128_long_sequences(oracle_mod, mask):
     """Sequences longer than 256 tokens at chunk 128: the pre-pass and segment
     scan, then the chunk-sequential main pass carrying the forward state,
     with ragged last chunks, blocks with one or two chunks, one or several
-    segments per head and several heads per CTA."""
+    segments per head and several heads per CTA.  With at least as many
+    heads as SMs every head is one segment (40 x 9 and 2 x 80 here): no
+    segment scan, zero entering states."""
     for B, H, L in ((1, 2, 257), (1, 2, 384), (1, 3, 700), (2, 1, 2000), (8, 5, 1000), (1, 6, 3000),
-                    (40, 9, 300)):
+                    (40, 9, 300), (2, 80, 700)):
         inp = synth.make_inputs(B, H, L, 64, mask, "bf16", seed=900 + L + B)
         q, k, v, ll = f64(inp)
         ref = oracle_mod.rnn(q, k, v, ll, inp["mask"], threads=0)
