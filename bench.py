@@ -143,8 +143,8 @@ def long_segments(w, sms: int) -> int:
 def kernels_per_call(form: str, chunk: int, w, mask: str = "s", sms: int = 152) -> int:
     """Kernel launches one operator call makes: the tensor-core chunk paths
     (bf16, d=64, chunk 64 or 128) take one launch up to 256 tokens and three
-    (pre-pass, segment scan, main pass) beyond, chunk 128 two when every
-    head is one segment (no scan); the recurrent form two with its workspace
+    (pre-pass, segment scan, main pass) beyond, two when every head is one
+    segment (no scan); the recurrent form two with its workspace
     (the features of every token, then the column CTAs); the full form at
     d = 64 and 128 two (the features, the tiled pass), three for LION-S (its
     prefix first); every other path one."""
@@ -154,7 +154,7 @@ def kernels_per_call(form: str, chunk: int, w, mask: str = "s", sms: int = 152) 
     if form == "full" and w.d in (64, 128):
         return 3 if mask == "s" else 2
     if tc and w.L > 256:
-        return 2 if chunk == 128 and long_segments(w, sms) == 1 else 3
+        return 2 if long_segments(w, sms) == 1 else 3
     return 1
 
 

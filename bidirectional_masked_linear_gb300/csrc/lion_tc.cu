@@ -533,7 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) kv[e] = 0.f;
         float tseg = 0.f, lseg_after = 0.f;
-        if (MODE == MODE_MAIN && prm.NBL > 1) {
+        // (one segment a head: zero entering states, no scan output to read)
+        if (MODE == MODE_MAIN && prm.NBL > 1 && prm.nseg > 1) {
           const float* sin = prm.segin + so * kSegInFloats;
           const float* src = sin + (fwd ? 0 : kD * kStateCols) + m * kStateCols;
 #pragma unroll
@@ -650,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* gl = prm.gloc + ((size_t)bh * prm.NBL + b) * kGlocBytes;
                 const __half* gv = reinterpret_cast<const __half*>(gl) + m * kD + 16 * wg;
                 const float rb = uni_f[5] - uni_f[7] - tblk;   // sum of l over this segment's blocks after b
-                const float f = __expf(rb - sMisc[NC] + uni_f[6]);
+                // (one segment a head: no entering state, and rb is not a
+                // segment's sum then, so the factor is not evaluated)
+                const float f = prm.nseg > 1 ? __expf(rb - sMisc[NC] + uni_f[6]) : 0.f;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) st[e] = __half2float(gv[e]) + f * kv[e];
                 if (wg == 3) stz = reinterpret_cast<const float*>(gl + kD * kD * 2)[m] + f * kz;
@@ -715,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == MODE_PRE) {
         // segment summaries once the leftmost block is done
         const int seg_lo = seg * prm.SEGB;
-        if (b == seg_lo) {
+        if (b == seg_lo && prm.nseg > 1) {
           float* ss = prm.segsum + (size_t)cur.item * kSegSumFloats;
           float* dst = ss + (fwd ? 0 : kD * kStateCols) + m * kStateCols;
           float sv[16], sz;
@@ -1142,9 +1145,12 @@ cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_
     cudaError_t e = launch_mode<MODE_PRE>(p, mq, mk, mv, prm, grid, s);
     if (e != cudaSuccess) return e;
     const dim3 sgrid((2 * kD * kStateCols + kScanThreads - 1) / kScanThreads, BH);
-    if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-    else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-    else lion_segment_scan_kernel<MASK_S><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
+    // with one segment a head there is nothing to chain
+    if (t.nseg > 1) {
+      if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
+      else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
+      else lion_segment_scan_kernel<MASK_S><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

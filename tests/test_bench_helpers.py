@@ -61,7 +61,8 @@ def test_launch_counts():
     assert bench.long_segments(synth.WORKLOADS["lra_4096"], 152) == 1
     assert bench.kernels_per_call("chunk", 128, synth.WORKLOADS["bert_large"]) == 2
     assert bench.kernels_per_call("chunk", 128, synth.WORKLOADS["lra_4096"]) == 2
-    assert bench.kernels_per_call("chunk", 64, synth.WORKLOADS["lra_4096"]) == 3
+    assert bench.kernels_per_call("chunk", 64, synth.WORKLOADS["lra_4096"]) == 2
+    assert bench.kernels_per_call("chunk", 64, hires) == 3
     assert bench.kernels_per_call("chunk", 32, hires) == 1
     assert bench.kernels_per_call("rnn", 0, hires) == 2     # features, then the column CTAs
     assert bench.kernels_per_call("full", 0, vit, "s") == 3   # prefix, features, the tiled pass
