@@ -676,10 +676,12 @@ def measure_config(c, flush, hbm_peak, steps=20, warmup=3):
 
 def path_name(form, chunk, w) -> str:
     tc = form == "chunk" and w.d == 64 and w.dtype == "bf16"
-    if tc and chunk == 128:
-        return "tcgen05 chunk-128" + (" (pre-pass, segment scan, main pass)" if w.L > 256 else "")
-    if tc and chunk == 64:
-        return "tcgen05 chunk-64" + (" (pre-pass, segment scan, main pass)" if w.L > 256 else "")
+    if tc and chunk in (64, 128):
+        passes = ""
+        if w.L > 256:
+            passes = (" (pre-pass, main pass; one segment a head)" if long_segments(w, _sm_count()) == 1
+                      else " (pre-pass, segment scan, main pass)")
+        return f"tcgen05 chunk-{chunk}" + passes
     if form == "full" and w.d in (64, 128):
         return "full form, fp32 CUDA cores, register-tiled"
     if form == "chunk" and chunk <= 64:
