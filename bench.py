@@ -58,16 +58,16 @@ _CALL_KERNELS = {
 # (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
 # write) of one launch, from one ncu capture of that kernel
 TRAFFIC_PER_HEAD = {
-    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.3 MB written
+    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.1 MB written
     ("lion_chunk128_tc_kernel", "dae441bb30eaca7d5dc775985d93741c8efca2d56458614e586ed0f43f2c4691",
-     "vit_b", "s", 128): (117506304 + 36263936) / 1536,
+     "vit_b", "s", 128): (117484032 + 36051712) / 1536,
     # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the three launches of a call
-    ("lion_chunk128_pre_kernel", "aa1280094c62fe3ed580ba4a396ed0e1f3975eb3b8a8f370a5390b2debda4cf0",
-     "hires_2496", "s", 128): (152019712 + 22125824) / 24,
-    ("lion_segment_scan_kernel", "ac12f62bec1d86b3ae2411f85f0b944900d000aba9eac5e8437a272651a52708",
-     "hires_2496", "s", 128): (5928960 + 0) / 24,
-    ("lion_chunk128_long_kernel", "cd9945a38a4e5f5729ecda5815a0f8857f6308324ce504c3b00c8b866cec7641",
-     "hires_2496", "s", 128): (271020544 + 110052864) / 24,
+    ("lion_chunk128_pre_kernel", "bb77d9caab3ecc3b715546f116a88c3c01332b0d8e989088a8ba396c4409f96f",
+     "hires_2496", "s", 128): (152026112 + 22388992) / 24,
+    ("lion_segment_scan_kernel", "1451e8bf52f51aebe756182b22f66ce3bf0fa66fac4d00ed04bd42a80888aef1",
+     "hires_2496", "s", 128): (5929216 + 0) / 24,
+    ("lion_chunk128_long_kernel", "77fee63844d922ac8f69aad0907a97ee3b6d82abca3345705a55945d5f449f95",
+     "hires_2496", "s", 128): (270996224 + 110349824) / 24,
 }
 
 
