@@ -247,10 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t da = da0, db = mnmaj(bb, 0, 0);
         for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
           mma_bf16(tbase + T_U, da, db, idUT, k > 0 ? 1u : 0u);
-        da = da0;
-        db = mnmaj(bf, 0, 0);
-        for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
-          mma_bf16(tbase + T_FA, da, db, idUT, (k > 0 || !first) ? 1u : 0u);
+        if (prm.nseg > 1) {   // the forward summary only feeds the segment scan
+          da = da0;
+          db = mnmaj(bf, 0, 0);
+          for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
+            mma_bf16(tbase + T_FA, da, db, idUT, (k > 0 || !first) ? 1u : 0u);
+        }
         mma_commit(&bars[B_U]);
         mma_commit(&bars[B_KWE]);
         mma_commit(&bars[B_KVE0 + s]);
@@ -336,22 +338,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           const float wb = live ? ex2((p - pfirst) * kLog2e) : 0.f;
-          const float wf = live ? ex2((D + T - p) * kLog2e) : 0.f;
-          const float2 wb2 = make_float2(wb, wb), wf2 = make_float2(wf, wf);
+          const float2 wb2 = make_float2(wb, wb);
+          // the forward-summary copy only feeds the segment scan
+          const bool fsum = prm.nseg > 1;
+          const float wf = live && fsum ? ex2((D + T - p) * kLog2e) : 0.f;
+          const float2 wf2 = make_float2(wf, wf);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             float yb[8], yf[8];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
               const float2 k2 = live ? make_float2(kv[8 * j + e], kv[8 * j + e + 1]) : make_float2(0.f, 0.f);
-              const float2 ub = mul2(k2, wb2), uf = mul2(k2, wf2);
+              const float2 ub = mul2(k2, wb2);
               yb[e] = ub.x;
               yb[e + 1] = ub.y;
-              yf[e] = uf.x;
-              yf[e + 1] = uf.y;
+              if (fsum) {
+                const float2 uf = mul2(k2, wf2);
+                yf[e] = uf.x;
+                yf[e + 1] = uf.y;
+              }
             }
             *reinterpret_cast<uint4*>(KBt + sw128_offset(t, j0 + j)) = pack8_h(yb);
-            *reinterpret_cast<uint4*>(KFt + sw128_offset(t, j0 + j)) = pack8_h(yf);
+            if (fsum) *reinterpret_cast<uint4*>(KFt + sw128_offset(t, j0 + j)) = pack8_h(yf);
           }
         }
         if (pt == 0) {
