@@ -58,16 +58,16 @@ _CALL_KERNELS = {
 # (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
 # write) of one launch, from one ncu capture of that kernel
 TRAFFIC_PER_HEAD = {
-    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.1 MB written
+    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.0 MB written
     ("lion_chunk128_tc_kernel", "dae441bb30eaca7d5dc775985d93741c8efca2d56458614e586ed0f43f2c4691",
-     "vit_b", "s", 128): (117484032 + 36051712) / 1536,
+     "vit_b", "s", 128): (117484032 + 36044032) / 1536,
     # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the three launches of a call
-    ("lion_chunk128_pre_kernel", "bb77d9caab3ecc3b715546f116a88c3c01332b0d8e989088a8ba396c4409f96f",
-     "hires_2496", "s", 128): (152026112 + 22388992) / 24,
+    ("lion_chunk128_pre_kernel", "a9883d6625d5647420e9052aa1e612479f4d2bdd46384f108380d956584f62f5",
+     "hires_2496", "s", 128): (152017408 + 22212096) / 24,
     ("lion_segment_scan_kernel", "1451e8bf52f51aebe756182b22f66ce3bf0fa66fac4d00ed04bd42a80888aef1",
-     "hires_2496", "s", 128): (5929216 + 0) / 24,
+     "hires_2496", "s", 128): (5927936 + 0) / 24,
     ("lion_chunk128_long_kernel", "77fee63844d922ac8f69aad0907a97ee3b6d82abca3345705a55945d5f449f95",
-     "hires_2496", "s", 128): (270996224 + 110349824) / 24,
+     "hires_2496", "s", 128): (270981376 + 110274304) / 24,
 }
 
 
