@@ -52,7 +52,6 @@ _COMMON = (_CSRC + "c128_common.cuh", _CSRC + "tc_ptx.cuh")
 _CALL_KERNELS = {
     (128, False): {"lion_chunk128_tc_kernel": (_CSRC + "lion_c128.cu",) + _COMMON},
     (128, True): {"lion_chunk128_pre_kernel": (_CSRC + "lion_c128P.cu",) + _COMMON,
-                  "lion_segment_scan_kernel": (_CSRC + "lion_tc.cu", _CSRC + "tc_ptx.cuh"),
                   "lion_chunk128_long_kernel": (_CSRC + "lion_c128L.cu",) + _COMMON},
 }
 # (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
@@ -61,11 +60,9 @@ TRAFFIC_PER_HEAD = {
     # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.0 MB written
     ("lion_chunk128_tc_kernel", "dae441bb30eaca7d5dc775985d93741c8efca2d56458614e586ed0f43f2c4691",
      "vit_b", "s", 128): (117484032 + 36044032) / 1536,
-    # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the three launches of a call
+    # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the two launches of a call
     ("lion_chunk128_pre_kernel", "a9883d6625d5647420e9052aa1e612479f4d2bdd46384f108380d956584f62f5",
      "hires_2496", "s", 128): (152017408 + 22212096) / 24,
-    ("lion_segment_scan_kernel", "1451e8bf52f51aebe756182b22f66ce3bf0fa66fac4d00ed04bd42a80888aef1",
-     "hires_2496", "s", 128): (5927936 + 0) / 24,
     ("lion_chunk128_long_kernel", "77fee63844d922ac8f69aad0907a97ee3b6d82abca3345705a55945d5f449f95",
      "hires_2496", "s", 128): (270981376 + 110274304) / 24,
 }
@@ -142,9 +139,10 @@ def long_segments(w, sms: int) -> int:
 
 def kernels_per_call(form: str, chunk: int, w, mask: str = "s", sms: int = 152) -> int:
     """Kernel launches one operator call makes: the tensor-core chunk paths
-    (bf16, d=64, chunk 64 or 128) take one launch up to 256 tokens and three
-    (pre-pass, segment scan, main pass) beyond, two when every head is one
-    segment (no scan); the recurrent form two with its workspace
+    (bf16, d=64, chunk 64 or 128) take one launch up to 256 tokens; beyond,
+    chunk 128 two (pre-pass, main pass, which chains the segments itself)
+    and chunk 64 three (pre-pass, segment scan, main pass), two when every
+    head is one segment; the recurrent form two with its workspace
     (the features of every token, then the column CTAs); the full form at
     d = 64 and 128 two (the features, the tiled pass), three for LION-S (its
     prefix first); every other path one."""
@@ -154,7 +152,7 @@ def kernels_per_call(form: str, chunk: int, w, mask: str = "s", sms: int = 152) 
     if form == "full" and w.d in (64, 128):
         return 3 if mask == "s" else 2
     if tc and w.L > 256:
-        return 2 if long_segments(w, sms) == 1 else 3
+        return 2 if chunk == 128 or long_segments(w, sms) == 1 else 3
     return 1
 
 
@@ -679,7 +677,8 @@ def path_name(form, chunk, w) -> str:
     if tc and chunk in (64, 128):
         passes = ""
         if w.L > 256:
-            passes = (" (pre-pass, main pass; one segment a head)" if long_segments(w, _sm_count()) == 1
+            passes = (" (pre-pass, main pass)" if chunk == 128 else
+                      " (pre-pass, main pass; one segment a head)" if long_segments(w, _sm_count()) == 1
                       else " (pre-pass, segment scan, main pass)")
         return f"tcgen05 chunk-{chunk}" + passes
     if form == "full" and w.d in (64, 128):

@@ -17,10 +17,14 @@
 // at s_{c+1}), both [phi(k) (x) [v; 1]] sums weighted by the decay.
 //
 // The sequence is cut into segments of 256-token blocks.  A pre-pass (run
-// right to left over each segment, lion_c128P.cu) and a segment scan provide,
-// per chunk, the backward state entering it from the right within its
-// segment, and per segment the states entering it from both sides.  This pass
-// walks one segment left to right, one chunk at a time:
+// right to left over each segment, lion_c128P.cu) provides, per chunk, the
+// backward state entering it from the right within its segment, and per
+// segment its forward and backward summaries.  This pass chains the
+// summaries of the other segments of its head into the states entering its
+// segment from both sides (with several segments a head each CTA has one
+// segment, so the chaining runs once, before the first chunk; with one
+// segment a head both are zero), then walks the segment left to right, one
+// chunk at a time:
 //   F_c     carried in TMEM (fp32, transposed: lane = output column, lane 64
 //           = z), starting from the segment's entering state, and advanced
 //           after every chunk: F_{c+1} = exp(T_c) F_c + U_c with
@@ -38,8 +42,8 @@
 // with the decay mask applied to S on the CUDA cores as in lion_c128.cu.
 //
 // Warps: 0 TMA (Q, K, V and the pre-pass state of a chunk into one of two
-// slots; the segment's entering backward state), 1 MMA issue, 2-17 "prep"
-// (four threads per token: prefix, V -> fp16, phi(k) and its weighted copy,
+// slots), 1 MMA issue, 2-17 "prep" (the segment's entering states; then four
+// threads per token: prefix, V -> fp16, phi(k) and its weighted copy,
 // phi(q), factors, the X_G tile), 18-25 "epi" (two warps per TMEM lane
 // quarter, each one column half: mask, carried state and the next chunk's
 // X_F while the chunk's output product runs, then the output through TMA).
@@ -99,7 +103,6 @@ enum { I_EXACT = 0, I_T = 1, I_LNEXT = 2 };
 // mbarriers
 enum {
   B_LD0 = 0,     // + slot: Q, K, V, pre-pass state landed (TMA, tx bytes)
-  B_GS = 2,      // segment's entering backward state landed (tx bytes)
   B_KVR = 3,     // prep: V, phi(K), weighted phi(K) written (16 arrivals)
   B_QR = 4,      // prep: phi(Q), factors written (16 arrivals)
   B_S = 5,       // MMA commit: S done
@@ -114,11 +117,10 @@ enum {
   B_PM = 15,     // epi: P written (8 arrivals)
   B_ED = 16,     // epi: O, T, R read (8 arrivals)
   B_DRAIN = 19,  // MMA commit used when unwinding
-  B_GF = 20,     // prep: the item's last X_G written, the segment state may be replaced (16 arrivals)
   B_TD = 21,     // MMA commit: T done (X_F read)
 };
 __device__ __forceinline__ uint32_t bar_count(int b) {
-  if (b == B_KVR || b == B_QR || b == B_XG || b == B_GF) return kPrepWarps;
+  if (b == B_KVR || b == B_QR || b == B_XG) return kPrepWarps;
   if (b == B_XF || b == B_CU || b == B_PM || b == B_ED) return kEpiWarps;
   return 1;
 }
@@ -137,7 +139,6 @@ struct LongParams {
   int NBL, SEGB, nseg;
   const uint8_t* gst;       // [BH][chunks] pre-pass states (kGstBytes each)
   const float* segsum;
-  const float* segin;
   int out_bf16;   // 1: y stored as bfloat16 (64-byte staging rows)
   int* status;
   long long wait_cycles;   // bound of every mbarrier wait, in clock cycles
@@ -246,35 +247,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == W_TMA) {
     // =========================== TMA producer ===================================
     // Step n's Q, K, V and pre-pass state go into slot n & 1 once step n-2's
-    // MMAs have read K and its output stores Q and V; the segment's entering
-    // backward state once the previous item's last state tile is written
-    // (a barrier that completes once per item, so that its phases cannot be
-    // confused while polling).
+    // MMAs have read K and its output stores Q and V.
     if (lane == 0) {
-      Step ld, gs;
-      ld.item = gs.item = blockIdx.x;
-      if (ld.valid(prm)) {
-        ld.set_item(prm, ld.item);
-        gs.set_item(prm, gs.item);
-      }
-      // one segment a head: the entering states are zero, nothing to load
-      if (prm.nseg == 1) gs.item = prm.BH;
-      int n = 0, ng = 0;   // steps issued; segment states issued
+      Step ld;
+      ld.item = blockIdx.x;
+      if (ld.valid(prm)) ld.set_item(prm, ld.item);
+      int n = 0;   // steps issued
       int issued_ld[2] = {0, 0};
       long long idle0 = clock64();
-      while ((ld.valid(prm) || gs.valid(prm)) && !*s_abort) {
+      while (ld.valid(prm) && !*s_abort) {
         bool progress = false;
-        if (gs.valid(prm) && (ng == 0 || mbar_try_wait(&bars[B_GF], (ng - 1) & 1))) {
-          mbar_arrive_expect_tx(&bars[B_GS], (uint32_t)kGsegBytes);
-          bulk_load(smem + OFF_GSEG, prm.segin + (size_t)gs.item * kSegInFloats + 64 * kLongStateCols,
-                    (uint32_t)kGsegBytes, &bars[B_GS]);
-          ++ng;
-          gs.item += gridDim.x;
-          if (gs.valid(prm)) gs.set_item(prm, gs.item);
-          progress = true;
-        }
         const int s = n & 1;
-        if (ld.valid(prm) && (n < 2 || mbar_try_wait(&bars[B_KE0 + s], ((n >> 1) - 1) & 1))) {
+        if (n < 2 || mbar_try_wait(&bars[B_KE0 + s], ((n >> 1) - 1) & 1)) {
           const int bh = ld.bh;
           mbar_arrive_expect_tx(&bars[B_LD0 + s], (uint32_t)(3 * kTile + kGstBytes));
           tma_load_3d(Vt(s), &mapV, &bars[B_LD0 + s], 0, kC * ld.c, bh);
@@ -309,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long lim = prm.wait_cycles / 4;
         for (int s = 0; s < 2; ++s)
           if (issued_ld[s]) mbar_wait(&bars[B_LD0 + s], (issued_ld[s] - 1) & 1, lim);
-        if (ng) mbar_wait(&bars[B_GS], (ng - 1) & 1, lim);
       }
     }
   } else if (warp == W_MMA) {
@@ -408,7 +391,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       *en = ell_at<MASK>(prm, bh, kC * x.c + kC, lh);   // first token after the chunk
     };
     if (st.valid(prm)) load_ell(st, ell_next, &lnext_next);
-    int ng = 0;                               // items started
     float cum = 0.f, tseg = 0.f, lafter = 0.f;
     for (int n = 0; st.valid(prm); ++n) {
       const int s = n & 1, tok = kC * st.c + t;
@@ -416,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int r = 0; r < 4; ++r) ell[r] = ell_next[r];
       const float lnext = lnext_next;
-      const bool first = st.c == st.c_lo, last = st.c + 1 == st.c_hi;
+      const bool first = st.c == st.c_lo;
       if (first) {
         // a new segment: bookkeeping for its backward entering state
         const int bh = st.bh, seg = st.seg;
@@ -424,7 +406,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lh = MASK == MASK_D ? __ldg(prm.log_lambda + bh % prm.H) : 0.f;
         lafter = ell_at<MASK>(prm, bh, 256 * min(prm.NBL, (seg + 1) * prm.SEGB), lh);
         cum = 0.f;
-        ++ng;
+        if (prm.nseg > 1) {
+          // The segment's entering states, chained from the summaries the
+          // pre-pass wrote (with several segments a head each CTA has one
+          // item, so this runs once, before any chunk):
+          // * forward, into the carried TMEM state: F = exp(T_s) F + U_s for
+          //   s = 0 .. seg - 1 (this warp: TMEM lanes of its quarter, 16 of
+          //   the 64 columns m);
+          // * backward, into shared memory: G = d_s G + U_s from the last
+          //   segment down to seg + 1, d_s the decay across segment s shifted
+          //   by one token.
+          {
+            const int lq = warp & 3, ln = 32 * lq + lane;   // TMEM lane = state column n
+            const int m0 = 16 * ((warp - W_PREP) >> 2);
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.f;
+            if (ln < kLongStateCols) {
+#pragma unroll 1
+              for (int sg = 0; sg < seg; ++sg) {
+                const float* ss = prm.segsum + ((size_t)bh * prm.nseg + sg) * kSegSumFloats;
+                const float dsg = __expf(__ldg(ss + 2 * 64 * kLongStateCols));
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = dsg * v[e] + __ldg(ss + (m0 + e) * kLongStateCols + ln);
+              }
+            }
+            tmem_st16(tbase + ((uint32_t)(32 * lq) << 16) + T_F + m0, v);
+            tmem_wait_st();
+          }
+          const int segtok = prm.SEGB * 256;
+          float* gw = reinterpret_cast<float*>(smem + OFF_GSEG);
+          float g[10];
+#pragma unroll
+          for (int r = 0; r < 10; ++r) g[r] = 0.f;
+#pragma unroll 1
+          for (int sg = prm.nseg - 1; sg > seg; --sg) {
+            // every load of a segment in flight at once
+            const float* ss = prm.segsum + ((size_t)bh * prm.nseg + sg) * kSegSumFloats;
+            float u[10];
+#pragma unroll
+            for (int r = 0; r < 10; ++r) u[r] = __ldg(ss + 64 * kLongStateCols + pt + 512 * r);
+            const float ts = __ldg(ss + 2 * 64 * kLongStateCols);
+            const float lfirst = ell_at<MASK>(prm, bh, sg * segtok, lh);
+            const float lnx = ell_at<MASK>(prm, bh, (sg + 1) * segtok, lh);
+            const float dsg = __expf(ts - lfirst + lnx);
+#pragma unroll
+            for (int r = 0; r < 10; ++r) g[r] = dsg * g[r] + u[r];
+          }
+#pragma unroll
+          for (int r = 0; r < 10; ++r) gw[pt + 512 * r] = g[r];
+          tc_fence_before();
+          // every prep thread's share written, and the epilogue may read the
+          // carried state
+          bar_and(3, (kPrepWarps + kEpiWarps) * 32, true);
+        }
       }
       // ---- chunk-local inclusive prefix
       float p, T, pfirst;
@@ -527,8 +562,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       //      state, in place in the slot's pre-pass tile (row i = state column
       //      i, 64 = z; this thread: row t, state rows m = 16 qq .. 16 qq + 15)
       // (one segment a head: no entering state, X_G is the tile as loaded)
-      if (prm.nseg > 1 && first && !waitb(B_GS, (ng - 1) & 1)) good = false;
-      good = __all_sync(0xffffffffu, good);
       if (prm.nseg > 1 && good && t < 65) {
         // exp(P at the first token after the segment - P at the first token after the chunk)
         const float fdec = __expf(tseg - (cum + T) - lnext + lafter);
@@ -547,10 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n >= 1 && !waitb(B_O, (n - 1) & 1)) good = false;
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[B_XG]);
-        if (last) mbar_arrive(&bars[B_GF]);   // done with this segment's state
-      }
+      if (lane == 0) mbar_arrive(&bars[B_XG]);
       st.next(prm);
     }
   } else {
@@ -588,6 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     Step st;
     st.item = blockIdx.x;
     if (st.valid(prm)) st.set_item(prm, st.item);
+    // with several segments a head the prep warps chain the entering forward
+    // state into the carried TMEM state before any chunk: wait for it
+    if (prm.nseg > 1 && st.valid(prm)) {
+      bar_and(3, (kPrepWarps + kEpiWarps) * 32, true);
+      tc_fence_after();
+    }
     for (int n = 0; st.valid(prm) && good; ++n) {
       const int s = n & 1, c = st.c, nk = nk_of(c), bh = st.bh;
       const bool first = c == st.c_lo, last = c + 1 == st.c_hi, warp_ok = kC * c + 32 * q < L;
@@ -598,16 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (first) {
         // a new segment: its forward entering state into the carried TMEM
         // state, then X_F once the previous chunk's T has read the tile
-        const float* fin = prm.segin + (size_t)st.item * kSegInFloats;   // [64 m][80]
-        if (q < 3) {
+        // (with several segments a head the state was chained before the loop)
+        if (prm.nseg == 1 && q < 3) {
           float v[16];
-#pragma unroll 1
-          for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              v[e] = st_row && prm.nseg > 1 ? __ldg(fin + (32 * hc + 16 * h2 + e) * kLongStateCols + i) : 0.f;
-            tmem_st16(tbase + lane_off + T_F + 32 * hc + 16 * h2, v);
-          }
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+          tmem_st16(tbase + lane_off + T_F + 32 * hc, v);
+          tmem_st16(tbase + lane_off + T_F + 32 * hc + 16, v);
           tmem_wait_st();
         }
         if (n >= 1 && !waitb(B_TD, (n - 1) & 1)) good = false;
@@ -782,19 +815,18 @@ bool chunk128_long_supported(const Problem& p) {
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct LongWs {
-  size_t gst, segsum, segin;
+  size_t gst, segsum;
 };
 LongWs long_ws(int B, int H, int L, const LongPlan& plan) {
   const size_t BH = (size_t)B * H, nch = (size_t)(L + kC - 1) / kC;
-  return {align256(BH * nch * kGstBytes), align256(BH * plan.nseg * kSegSumFloats * 4),
-          align256(BH * plan.nseg * kSegInFloats * 4)};
+  return {align256(BH * nch * kGstBytes), align256(BH * plan.nseg * kSegSumFloats * 4)};
 }
 }  // namespace
 
 size_t chunk128_long_workspace_bytes(int B, int H, int L) {
   if (L <= 2 * kC) return 0;
   const LongWs w = long_ws(B, H, L, long_plan(B, H, L));
-  return w.gst + w.segsum + w.segin;
+  return w.gst + w.segsum;
 }
 
 cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaStream_t s) {
@@ -803,17 +835,14 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   const LongWs w = long_ws(p.B, p.H, p.L, plan);
   uint8_t* gst = static_cast<uint8_t*>(ws);
   float* segsum = reinterpret_cast<float*>(gst + w.gst);
-  float* segin = reinterpret_cast<float*>(gst + w.gst + w.segsum);
+  const int BH = p.B * p.H;
+  // The main pass chains the segments' entering states itself from the
+  // pre-pass summaries, which needs one item a CTA when heads are cut into
+  // segments (B * H * segments never exceeds the SMs then)
+  if (plan.nseg > 1 && BH * plan.nseg > sm_count()) return cudaErrorInvalidValue;
   cudaError_t e = launch_chunk128_pre(p, plan, gst, segsum, status, s);
   if (e != cudaSuccess) return e;
-  // with one segment a head there is nothing to chain: the main pass takes
-  // zero entering states and reads neither summaries nor scan output
-  if (plan.nseg > 1) {
-    e = launch_segment_scan(p, plan, segsum, segin, s);
-    if (e != cudaSuccess) return e;
-  }
   CUtensorMap mq, mk, mv, mo;
-  const int BH = p.B * p.H;
   if (!make_map128(&mq, p.q, p.L, BH) || !make_map128(&mk, p.k, p.L, BH) || !make_map128(&mv, p.v, p.L, BH) ||
       !(p.out_bf16 ? make_out_map_bf16(&mo, p.out, p.L, BH, 32) : make_out_map(&mo, p.out, p.L, BH)))
     return cudaErrorInvalidValue;
@@ -828,7 +857,6 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   prm.nseg = plan.nseg;
   prm.gst = gst;
   prm.segsum = segsum;
-  prm.segin = segin;
   prm.status = status;
   prm.wait_cycles = wait_limit_cycles();
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, LongParams) = nullptr;

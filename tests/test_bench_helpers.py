@@ -32,17 +32,17 @@ def test_traffic_is_null_for_unknown_kernels():
 
 
 def test_traffic_covers_every_kernel_of_the_call(monkeypatch):
-    """The long path's figure is the sum over its three kernels, and one
-    kernel without a capture at its current sources makes the whole figure
-    null."""
+    """The long path's figure is the sum over its two kernels (pre-pass and
+    main pass), and one kernel without a capture at its current sources makes
+    the whole figure null."""
     w = synth.WORKLOADS["hires_2496"]
     kernels = bench._CALL_KERNELS[(128, True)]
-    assert len(kernels) == 3
+    assert len(kernels) == 2
     table = {(name, bench._sources_sha(files), w.name, "s", 128): 1000.0 * (n + 1)
              for n, (name, files) in enumerate(kernels.items())}
     monkeypatch.setattr(bench, "TRAFFIC_PER_HEAD", table)
     t, per = bench.traffic_bytes(w, "s", 128)
-    assert t == 6000.0 * w.B * w.H and len(per) == 3
+    assert t == 3000.0 * w.B * w.H and len(per) == 2
     table.pop(next(iter(table)))
     assert bench.traffic_bytes(w, "s", 128) == (None, None)
 
@@ -53,7 +53,7 @@ def test_launch_counts():
     assert bench.kernels_per_call("chunk", 128, vit) == 1
     assert bench.kernels_per_call("chunk", 64, vit) == 1
     assert bench.kernels_per_call("chunk", 64, hires) == 3
-    assert bench.kernels_per_call("chunk", 128, hires) == 3
+    assert bench.kernels_per_call("chunk", 128, hires) == 2   # the main pass chains the segments
     # every head one segment (B*H at least the SMs, or fewer heads than half
     # the SMs can split): pre-pass and main pass, no segment scan
     assert bench.long_segments(hires, 152) == 6
@@ -78,7 +78,7 @@ def test_traffic_keys_follow_the_kernel_that_runs():
             for rel in files:
                 assert os.path.exists(os.path.join(ROOT, rel)), (key, name, rel)
             shas.add(bench._sources_sha(files))
-    assert len(shas) == 4
+    assert len(shas) == 3
 
 
 def test_config_lines_cover_the_scope_configurations():
