@@ -59,12 +59,12 @@ _CALL_KERNELS = {
 TRAFFIC_PER_HEAD = {
     # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.0 MB written
     ("lion_chunk128_tc_kernel", "dae441bb30eaca7d5dc775985d93741c8efca2d56458614e586ed0f43f2c4691",
-     "vit_b", "s", 128): (117484032 + 36044032) / 1536,
+     "vit_b", "s", 128): (117484288 + 36038912) / 1536,
     # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the two launches of a call
     ("lion_chunk128_pre_kernel", "a9883d6625d5647420e9052aa1e612479f4d2bdd46384f108380d956584f62f5",
-     "hires_2496", "s", 128): (152017408 + 22212096) / 24,
-    ("lion_chunk128_long_kernel", "77fee63844d922ac8f69aad0907a97ee3b6d82abca3345705a55945d5f449f95",
-     "hires_2496", "s", 128): (270981376 + 110274304) / 24,
+     "hires_2496", "s", 128): (152015616 + 22336256) / 24,
+    ("lion_chunk128_long_kernel", "70e11493ee6757a792d579ca4782f3b5c63542d2e4e13f89ed287871c7312f78",
+     "hires_2496", "s", 128): (270043648 + 110133760) / 24,
 }
 
 
