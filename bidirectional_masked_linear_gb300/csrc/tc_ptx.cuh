@@ -254,6 +254,12 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // All `nthreads` threads of barrier `id` arrive; returns true only if every
 // one of them passed true.  Lets a group leave a loop together after one of
 // its members gave up on a bounded wait.
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start before the grid ahead of it on the stream has
+// ended; pdl_wait() returns once that grid has completed and its memory
+// operations are visible (at once when the grid was launched plainly).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ bool bar_and(int id, int nthreads, bool pred) {
   uint32_t r;
   asm volatile(
