@@ -58,13 +58,13 @@ _CALL_KERNELS = {
 # write) of one launch, from one ncu capture of that kernel
 TRAFFIC_PER_HEAD = {
     # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.0 MB written
-    ("lion_chunk128_tc_kernel", "dae441bb30eaca7d5dc775985d93741c8efca2d56458614e586ed0f43f2c4691",
-     "vit_b", "s", 128): (117484288 + 36038912) / 1536,
+    ("lion_chunk128_tc_kernel", "5dd15b36b1d88a0130d751da3af2ef9cc4b7e06423483cb1ffe51fca1118ae0c",
+     "vit_b", "s", 128): (117535488 + 36010240) / 1536,
     # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the two launches of a call
-    ("lion_chunk128_pre_kernel", "a9883d6625d5647420e9052aa1e612479f4d2bdd46384f108380d956584f62f5",
-     "hires_2496", "s", 128): (152015616 + 22336256) / 24,
-    ("lion_chunk128_long_kernel", "70e11493ee6757a792d579ca4782f3b5c63542d2e4e13f89ed287871c7312f78",
-     "hires_2496", "s", 128): (270043648 + 110133760) / 24,
+    ("lion_chunk128_pre_kernel", "09cfde51aef5e530a1da30d6e2bb971931abe0f7683503465039ff16deb97a1c",
+     "hires_2496", "s", 128): (152016896 + 22448384) / 24,
+    ("lion_chunk128_long_kernel", "a3a914f41092aef8898f07df693b654839b67bc513c8134bfca0220eadc387b6",
+     "hires_2496", "s", 128): (270041600 + 110072576) / 24,
 }
 
 
