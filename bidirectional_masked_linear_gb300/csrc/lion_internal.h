@@ -79,8 +79,6 @@ struct LongPlan {
   int NBL, SEGB, nseg;
 };
 LongPlan long_plan(int B, int H, int L);
-cudaError_t launch_segment_scan(const Problem& p, const LongPlan& plan, const float* segsum, float* segin,
-                                cudaStream_t s);
 
 // Per-chunk backward states of the 128-token-chunk path: for chunk c of a
 // head, the backward state entering it from the right, from the tokens after

@@ -1087,24 +1087,6 @@ LongPlan long_plan(int B, int H, int L) {
   return lp;
 }
 
-cudaError_t launch_segment_scan(const Problem& p, const LongPlan& plan, const float* segsum, float* segin,
-                                cudaStream_t s) {
-  TcParams prm = {};
-  prm.log_lambda = p.log_lambda;
-  prm.BH = p.B * p.H;
-  prm.H = p.H;
-  prm.L = p.L;
-  prm.NBL = plan.NBL;
-  prm.SEGB = plan.SEGB;
-  prm.nseg = plan.nseg;
-  prm.segsum = const_cast<float*>(segsum);
-  const dim3 sgrid((2 * kD * kStateCols + kScanThreads - 1) / kScanThreads, prm.BH);
-  if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-  else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-  else lion_segment_scan_kernel<MASK_S><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-  return cudaGetLastError();
-}
-
 size_t chunk_tc_workspace_bytes(int B, int H, int L) {
   const TcPlan t = plan_tc(B, H, L);
   if (t.NBL == 1) return 0;
