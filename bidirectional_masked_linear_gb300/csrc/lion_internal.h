@@ -68,10 +68,11 @@ cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_
 //                 token), backward summary [64][80] (exp(P_j - P_first) ...,
 //                 anchored at its first token), then the sum of log(lambda)
 //                 over the segment;
-// and the scan chains them into
+// and the chunk-64 path's scan chains them into
 //   segin[bh][s]  (fp32): forward state entering segment s from the left
 //                 [64][80], backward state entering it from the right [64][80]
-// (column 64 of a [64][80] state is z; 65..79 are zero).
+// (column 64 of a [64][80] state is z; 65..79 are zero).  The chunk-128
+// path's main pass chains them itself, with the same recurrences.
 constexpr int kLongStateCols = 80;
 constexpr int kSegSumFloats = 2 * 64 * kLongStateCols + 4;
 constexpr int kSegInFloats = 2 * 64 * kLongStateCols;
