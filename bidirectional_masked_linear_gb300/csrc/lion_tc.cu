@@ -474,6 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // =================== worker warps: CUDA-core stages =======================
+    // (the main pass of a long sequence reads the pre-pass's and the scan's
+    // output: it may have been launched before they ended)
+    if (MODE == MODE_MAIN) pdl_wait();
     auto arrive = [&](int b) {   // every worker warp arrives once
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[b]);
@@ -938,6 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kScanThreads = 128;
 template <int MASK>
 __global__ void __launch_bounds__(kScanThreads) lion_segment_scan_kernel(TcParams prm, float* segin) {
+  pdl_wait();   // the summaries come from the pre-pass, the grid before this one
   const int bh = blockIdx.y, h = bh % prm.H;
   const int x = blockIdx.x * kScanThreads + threadIdx.x;     // [0, 2 * kD * kStateCols)
   if (x >= 2 * kD * kStateCols) return;
@@ -1053,6 +1057,23 @@ TcPlan plan_tc(int B, int H, int L) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Launches kern as a programmatic dependent of the work before it on s.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int MODE>
 cudaError_t launch_mode(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const TcParams& prm, int grid, cudaStream_t s) {
@@ -1072,8 +1093,15 @@ cudaError_t launch_mode(const Problem& p, const CUtensorMap& mq, const CUtensorM
   if (!kern) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);
-  return cudaGetLastError();
+  if (MODE == MODE_PRE || prm.NBL == 1) {
+    kern<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);
+    return cudaGetLastError();
+  }
+  // the main pass after a pre-pass (and scan): launched as a programmatic
+  // dependent, so that its launch and set-up overlap the end of the grid
+  // before; its worker warps wait for that grid (pdl_wait) before they read
+  // its output
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, mq, mk, mv, prm);
 }
 
 }  // namespace
@@ -1129,9 +1157,11 @@ cudaError_t launch_chunk_tc(const Problem& p, void* ws, int* status, cudaStream_
     const dim3 sgrid((2 * kD * kStateCols + kScanThreads - 1) / kScanThreads, BH);
     // with one segment a head there is nothing to chain
     if (t.nseg > 1) {
-      if (p.mask_kind == MASK_LIT) lion_segment_scan_kernel<MASK_LIT><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-      else if (p.mask_kind == MASK_D) lion_segment_scan_kernel<MASK_D><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
-      else lion_segment_scan_kernel<MASK_S><<<sgrid, kScanThreads, 0, s>>>(prm, segin);
+      void (*scan)(TcParams, float*) = p.mask_kind == MASK_LIT ? lion_segment_scan_kernel<MASK_LIT>
+                                       : p.mask_kind == MASK_D ? lion_segment_scan_kernel<MASK_D>
+                                                               : lion_segment_scan_kernel<MASK_S>;
+      cudaError_t es = launch_dependent(scan, sgrid, dim3(kScanThreads), 0, s, prm, segin);
+      if (es != cudaSuccess) return es;
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
