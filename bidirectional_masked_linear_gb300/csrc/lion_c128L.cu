@@ -884,17 +884,7 @@ cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaSt
   // output wait for it (pdl_wait).  (The pre-pass signals nothing early: main
   // pass CTAs idling on the SMs the pre-pass leaves free cost more than they
   // saved at the LRA shape, 186.5 against 184.8 us.)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, prm);
+  e = launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, mq, mk, mv, mo, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

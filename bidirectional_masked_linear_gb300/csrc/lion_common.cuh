@@ -68,4 +68,24 @@ __device__ __forceinline__ float mask_exponent(int i, int j, float Pi, float Pj)
   return i >= j ? Pi - Pj : Pj - Pi;
 }
 
+
+// Launches kern as a programmatic dependent of the work before it on s: it
+// may start before that work ends, and waits for it (griddepcontrol.wait)
+// before it reads what that work wrote.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace lion

@@ -1057,23 +1057,6 @@ TcPlan plan_tc(int B, int H, int L) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Launches kern as a programmatic dependent of the work before it on s.
-template <typename... Args>
-cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                             Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 template <int MODE>
 cudaError_t launch_mode(const Problem& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const TcParams& prm, int grid, cudaStream_t s) {
