@@ -154,6 +154,27 @@ def test_chunk128_long_sequences(oracle_mod, mask):
         check(oracle_mod, run_gpu(inp, lion.FORM_CHUNK, 128), ref, inp, TOL_BF16)
 
 
+# The long paths' later launches start before the earlier ones end
+# (programmatic dependent launch) and wait for them only where they read their
+# output.  Calls made back to back on one stream, with the workspace memory of
+# one call reused by the next, must still give each call's own result: bit
+# for bit the result of the same call made on its own.
+@pytest.mark.gpu
+@pytest.mark.parametrize("chunk", (64, 128))
+def test_long_calls_back_to_back(chunk):
+    shapes = ((1, 3, 3000), (2, 80, 700), (1, 2, 1500), (1, 6, 2000))   # several and one segment a head
+    inps = [synth.make_inputs(B, H, L, 64, "s", "bf16", seed=1500 + i) for i, (B, H, L) in enumerate(shapes)]
+    alone = [run_gpu(inp, lion.FORM_CHUNK, chunk) for inp in inps]
+    devs = [_cuda(inp) for inp in inps]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        outs = [lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], "s", "chunk", chunk) for g in devs]
+        torch.cuda.synchronize()
+        assert lion.sync_status() == 0
+        for i, (y, want) in enumerate(zip(outs, alone)):
+            assert np.array_equal(y.cpu().numpy(), want), (chunk, rep, i)
+
+
 @pytest.mark.parametrize("mask", ("lit", "d", "s"))
 def test_long_sequences_blocks_and_segments(oracle_mod, mask):
     """Sequences longer than one 256-token block: the tensor-core path chains
