@@ -35,7 +35,9 @@ struct Problem {
 cudaError_t launch_full_simt(const Problem& p, cudaStream_t s);
 // The recurrent form.  The workspace holds c^F (B*H*L floats) and, when it
 // is rnn_workspace_bytes long, the features of every token, computed once
-// by a first launch; with the c^F part alone each column CTA computes them.
+// by a first launch, and room for the backward sweep's sums when the two
+// sweeps run apart; with the c^F part alone each column CTA computes the
+// features and runs both sweeps.
 size_t rnn_workspace_bytes(int B, int H, int L, int d);
 cudaError_t launch_rnn_simt(const Problem& p, float* ws, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_chunk_simt(const Problem& p, float* ws_den /*[B*H*L]*/, cudaStream_t s);
@@ -94,8 +96,8 @@ constexpr int kGstBytes = 65 * 128;
 bool chunk128_tc_supported(const Problem& p);
 cudaError_t launch_chunk128_tc(const Problem& p, int* status, cudaStream_t s);
 // The same for L > 256: a backward pre-pass over 128-token chunks (per-chunk
-// states and segment summaries), the segment scan, and the main pass (three
-// launches; workspace as returned).
+// states and segment summaries) and the main pass, which chains the
+// segment summaries at its start (two launches; workspace as returned).
 bool chunk128_long_supported(const Problem& p);
 size_t chunk128_long_workspace_bytes(int B, int H, int L);
 cudaError_t launch_chunk128_long(const Problem& p, void* ws, int* status, cudaStream_t s);

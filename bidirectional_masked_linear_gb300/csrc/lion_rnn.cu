@@ -18,6 +18,15 @@
 // normaliser it divides by without waiting for another; they all store the
 // same c^F_i (the same arithmetic on the same inputs).
 //
+// Sweeps.  When the heads are few (under two column CTAs an SM) and the
+// workspace is whole, the two sweeps run at the same time in separate CTAs
+// (gridDim.y = 2): the backward CTAs store their sums y^B_i and c^B_i
+// beside y^F_i and c^F_i (the O(Ld + L) side storage of both directions),
+// and a last launch combines them.  Otherwise each CTA runs the forward
+// sweep, then the backward one, which combines as it goes.  Both ways the
+// combination is one helper with every rounding explicit, so they give the
+// same bits.
+//
 // Feature maps.  With a workspace of rnn_workspace_bytes, a first launch
 // writes phi(q), phi(k) (fp32) and s_ii of every token once, and the column
 // CTAs of a head copy them in; with only the c^F scratch (the allocation-
@@ -78,18 +87,28 @@ __device__ __forceinline__ void cp_wait() {
 }
 
 // Workspace sections (floats, each padded to 64): c^F [BH L], s_ii [BH L],
-// phi(q) [BH L d], phi(k) [BH L d].
+// phi(q) [BH L d], phi(k) [BH L d] (up to `features`), then for the split
+// sweeps y^B [BH L d] and c^B [BH L].
 __host__ __device__ constexpr size_t pad64(size_t n) { return (n + 63) & ~size_t(63); }
 struct RnnWs {
-  size_t cF, sii, fq, fk, total;   // float offsets and size
+  size_t cF, sii, fq, fk, yB, cB, features, total;   // float offsets and sizes
   __host__ __device__ RnnWs(size_t BHL, int d) {
     cF = 0;
     sii = pad64(BHL);
     fq = sii + pad64(BHL);
     fk = fq + pad64(BHL * (size_t)d);
-    total = fk + pad64(BHL * (size_t)d);
+    features = fk + pad64(BHL * (size_t)d);
+    yB = features;
+    cB = yB + pad64(BHL * (size_t)d);
+    total = cB + pad64(BHL);
   }
 };
+
+// y_i from the two sweeps' sums, each of which counts the diagonal term:
+// (y^F + y^B - s_ii v) / (c^F + c^B - s_ii), every rounding explicit.
+__device__ __forceinline__ float combine_y(float yf, float yb, float sii, float vn, float cf, float cb) {
+  return __fdiv_rn(__fmaf_rn(-sii, vn, __fadd_rn(yf, yb)), __fsub_rn(__fadd_rn(cf, cb), sii));
+}
 
 // phi of one row's PER features held by this lane; the row's other
 // features sit in the 7 lanes next to it (xor 1, 2, 4).
@@ -247,6 +266,10 @@ __global__ void __launch_bounds__(Split<D, G>::kThr) rnn_cols_kernel(Problem p, 
   const T* v = reinterpret_cast<const T*>(p.v) + (size_t)bh * L * D;
   float* out = p.out + (size_t)bh * L * D;
   float* cF = ws + w.cF + (size_t)bh * L;
+  // split sweeps: this CTA's direction is blockIdx.y (0 forward, 1 backward)
+  const bool split = gridDim.y == 2;
+  float* yB = split ? ws + w.yB + (size_t)bh * L * D : nullptr;
+  float* cB = split ? ws + w.cB + (size_t)bh * L : nullptr;
   const float* ll = p.mask_kind == MASK_S ? p.log_lambda + (size_t)bh * L : nullptr;
   const float lh = p.mask_kind == MASK_D ? __ldg(p.log_lambda + bh % H) : 0.f;
   const int ntiles = (L + kTile - 1) / kTile;
@@ -375,6 +398,7 @@ __global__ void __launch_bounds__(Split<D, G>::kThr) rnn_cols_kernel(Problem p, 
           if (tt < nt) {
             sC[tt] = part[e];
             if (fwd && !p.causal) cF[t0 + tt] = part[e];
+            if (!fwd && split) cB[t0 + tt] = part[e];
           }
         }
       }
@@ -390,21 +414,42 @@ __global__ void __launch_bounds__(Split<D, G>::kThr) rnn_cols_kernel(Problem p, 
             out[o] = part[e] / sC[tt];
           } else if (fwd) {
             out[o] = part[e];
+          } else if (split) {
+            yB[o] = part[e];
           } else {
-            const float sii = tSii[tt], vn = sV[tt * kSlotCols + col];
-            out[o] = (out[o] + part[e] - sii * vn) / (cF[t0 + tt] + sC[tt] - sii);
+            out[o] = combine_y(out[o], part[e], tSii[tt], sV[tt * kSlotCols + col], cF[t0 + tt], sC[tt]);
           }
         }
       }
     }
     __syncthreads();   // the next sweep's first tile reuses slot 0
   };
-  sweep(std::integral_constant<bool, true>{});
-  if (!p.causal) sweep(std::integral_constant<bool, false>{});
+  if (!split || blockIdx.y == 0) sweep(std::integral_constant<bool, true>{});
+  if (!p.causal && (!split || blockIdx.y == 1)) sweep(std::integral_constant<bool, false>{});
+}
+
+// The split sweeps' combination, four features of one token a thread.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) rnn_combine_kernel(Problem p, const float* ws) {
+  constexpr int Q = D / 4;
+  const size_t rows = (size_t)p.B * p.H * p.L, n = rows * Q;
+  const RnnWs w(rows, D);
+  const T* v = reinterpret_cast<const T*>(p.v);
+  for (size_t x = (size_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = x / Q, o = r * D + 4 * (x - r * Q);
+    const float4 yb = *reinterpret_cast<const float4*>(ws + w.yB + o);
+    float4 y = *reinterpret_cast<const float4*>(p.out + o);
+    const float sii = ws[w.sii + r], cf = ws[w.cF + r], cb = ws[w.cB + r];
+    y.x = combine_y(y.x, yb.x, sii, to_f32(v[o]), cf, cb);
+    y.y = combine_y(y.y, yb.y, sii, to_f32(v[o + 1]), cf, cb);
+    y.z = combine_y(y.z, yb.z, sii, to_f32(v[o + 2]), cf, cb);
+    y.w = combine_y(y.w, yb.w, sii, to_f32(v[o + 3]), cf, cb);
+    *reinterpret_cast<float4*>(p.out + o) = y;
+  }
 }
 
 template <typename T, int D, int G, int TT>
-cudaError_t rnn_launch_g(const Problem& p, float* ws, bool pre, cudaStream_t s) {
+cudaError_t rnn_launch_g(const Problem& p, float* ws, bool pre, bool split, cudaStream_t s) {
   auto kern = pre ? rnn_cols_kernel<T, D, G, TT, true> : rnn_cols_kernel<T, D, G, TT, false>;
   const int bytes = pre ? Lay<T, D, G, TT, true>::kBytes : Lay<T, D, G, TT, false>::kBytes;
   if (bytes > 48 * 1024) {
@@ -412,14 +457,23 @@ cudaError_t rnn_launch_g(const Problem& p, float* ws, bool pre, cudaStream_t s) 
     if (e != cudaSuccess) return e;
   }
   const size_t grid = (size_t)p.B * p.H * (D / kNC);
-  kern<<<(unsigned)grid, Split<D, G>::kThr, bytes, s>>>(p, ws);
+  kern<<<dim3((unsigned)grid, split ? 2u : 1u), Split<D, G>::kThr, bytes, s>>>(p, ws);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !split) return e;
+  const size_t n = (size_t)p.B * p.H * p.L * (D / 4);
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)c128::sm_count() * 8);
+  rnn_combine_kernel<T, D><<<blocks, 256, 0, s>>>(p, ws);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t rnn_launch(const Problem& p, float* ws, size_t ws_floats, cudaStream_t s) {
   const size_t BHL = (size_t)p.B * p.H * p.L;
-  const bool pre = ws_floats >= RnnWs(BHL, D).total;
+  const RnnWs w(BHL, D);
+  const bool pre = ws_floats >= w.features;
+  // the two sweeps at once when the column CTAs leave the SMs under two each
+  const long long ctas = (long long)p.B * p.H * (D / kNC);
+  const bool split = pre && ws_floats >= w.total && !p.causal && ctas < 2LL * c128::sm_count();
   if (pre) {
     const size_t warps = (BHL + 3) / 4;
     const unsigned blocks = (unsigned)std::min<size_t>((warps + 7) / 8, (size_t)c128::sm_count() * 16);
@@ -429,11 +483,10 @@ cudaError_t rnn_launch(const Problem& p, float* ws, size_t ws_floats, cudaStream
   }
   if constexpr (D >= 64) {
     // one column a warp when two a warp would leave fewer than two CTAs an SM
-    const long long ctas = (long long)p.B * p.H * (D / kNC);
-    if (ctas < 2LL * c128::sm_count()) return rnn_launch_g<T, D, 32, 32>(p, ws, pre, s);
-    return rnn_launch_g<T, D, 16, kTileMany>(p, ws, pre, s);
+    if (ctas < 2LL * c128::sm_count()) return rnn_launch_g<T, D, 32, 32>(p, ws, pre, split, s);
+    return rnn_launch_g<T, D, 16, kTileMany>(p, ws, pre, split, s);
   } else {
-    return rnn_launch_g<T, D, 8, 32>(p, ws, pre, s);
+    return rnn_launch_g<T, D, 8, 32>(p, ws, pre, split, s);
   }
 }
 

@@ -64,7 +64,11 @@ def test_launch_counts():
     assert bench.kernels_per_call("chunk", 64, synth.WORKLOADS["lra_4096"]) == 2
     assert bench.kernels_per_call("chunk", 64, hires) == 3
     assert bench.kernels_per_call("chunk", 32, hires) == 1
-    assert bench.kernels_per_call("rnn", 0, hires) == 2     # features, then the column CTAs
+    # features, the column CTAs, and with few heads the combination of the
+    # two sweeps run apart
+    assert bench.kernels_per_call("rnn", 0, hires) == 3
+    assert bench.kernels_per_call("rnn", 0, vit) == 2
+    assert bench.kernels_per_call("rnn", 0, synth.WORKLOADS["lra_4096"]) == 2
     assert bench.kernels_per_call("full", 0, vit, "s") == 3   # prefix, features, the tiled pass
     assert bench.kernels_per_call("full", 0, vit, "d") == 2
     assert bench.kernels_per_call("full", 0, synth.WORKLOADS["tiny_d_fp32"], "d") == 1

@@ -333,6 +333,28 @@ def test_rnn_caller_workspace(oracle_mod, dtype):
     assert ei.value.status == lion.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("d,B,H", ((16, 8, 20), (32, 8, 10)))
+def test_rnn_split_sweeps_equal_fused_sweeps(d, B, H):
+    """With few heads (under two column CTAs an SM) the recurrent form runs
+    its two sweeps at once in separate CTAs and combines them in a last
+    launch; with many, each CTA runs them one after the other.  A batch row
+    computed alone (split sweeps) gives the bits it gets inside the whole
+    batch (fused sweeps).  At d >= 64 the same head count also sets how many
+    lanes share a state column, and with it the order of the column sums, so
+    there the allocation-free entry point (fused sweeps, same lanes) is the
+    comparison."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * H * (d // 8) >= 2 * sms > H * (d // 8)
+    inp = synth.make_inputs(B, H, 300, d, "s", "bf16", seed=91)
+    g = _cuda(inp)
+    y_all = lion.attn_fwd(g["q"], g["k"], g["v"], g["log_lambda"], 2, lion.FORM_RNN)
+    for b in (0, B - 1):
+        one = {x: g[x][b:b + 1].contiguous() for x in ("q", "k", "v", "log_lambda")}
+        y_one = lion.attn_fwd(one["q"], one["k"], one["v"], one["log_lambda"], 2, lion.FORM_RNN)
+        torch.cuda.synchronize()
+        assert torch.equal(y_one, y_all[b:b + 1])
+
+
 @pytest.mark.parametrize("d", (16, 32, 64, 128))
 def test_rnn_step_matches_rnn_form(oracle_mod, d):
     """Feeding tokens one at a time through lion_rnn_step, forward and then

@@ -37,7 +37,10 @@ def _dev(inp):
 @pytest.mark.parametrize("mask", ("lit", "d", "s"))
 def test_noalloc_matches_rnn_form_twice(lib, mask):
     """Bit for bit the regular recurrent form, on two calls in a row (the
-    second finds the first call's values in the shared scratch)."""
+    second finds the first call's values in the shared scratch).  With 12
+    heads the regular form runs its two sweeps apart and combines them in a
+    last launch, while this entry point runs them one after the other in
+    each CTA: the two must still agree exactly."""
     inp = synth.make_inputs(3, 4, 150, 64, mask, "bf16", seed=77)
     q, k, v, ll = _dev(inp)
     ref = lion.attn_fwd(q, k, v, ll, inp["mask"], lion.FORM_RNN).cpu().numpy()
