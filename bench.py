@@ -6,8 +6,8 @@ intra-chunk attention, chunk states, scans, combine/normalise) over one batch
 of synthetic inputs already resident in HBM.  Default workload: ViT-B
 (B=64, H=12, L=197, d=64), LION-S, chunk 128 (two chunks per head).  The
 L=24,337 high-resolution workload is measured in the same run at chunk 128
-(the pre-pass, segment scan and main pass of the long-sequence tensor-core
-path) and reported under ``secondary``; every other workload, mask, form and
+(the pre-pass and the main pass of the long-sequence tensor-core path; the
+main pass chains the segments itself) and reported under ``secondary``; every other workload, mask, form and
 chunk length of the scope's configurations gets a line under ``configs``.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
@@ -775,8 +775,8 @@ def main():
                                   "frac": b2 / (ms2 * 1e-3) / 1e9 / hbm_peak,
                                   "algorithmic_bytes": b2,
                                   "traffic": tr2, "traffic_per_kernel": tr2k,
-                                  "note": "achieved and traffic cover the whole call: pre-pass, segment scan "
-                                          "and main pass"}}
+                                  "note": "achieved and traffic cover the whole call: pre-pass and main "
+                                          "pass (which chains the segments itself)"}}
         del _k2
 
     lra = None

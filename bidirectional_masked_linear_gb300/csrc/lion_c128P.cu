@@ -17,14 +17,15 @@
 //
 // where P_{s_{c+1}} - P_{s_c} = T_c - l_{s_c} + l_{s_{c+1}} (T_c the sum of l
 // over the chunk: the backward decay is shifted by one token).  Each CTA walks
-// one segment of a head (the 256-token-block segments of the segment scan)
+// one segment of a head (the 256-token-block segments of the segment plan)
 // from right to left, one chunk at a time, and writes
 //   * G_c restricted to the segment (zero for the segment's last chunk) for
 //     every chunk, as an fp16 tile transposed to rows n of [state column n
 //     over m; z], the layout of the main pass's operand tile;
 //   * the segment's backward summary (G after its first chunk) and forward
 //     summary sum_j exp(P_last - P_j) phi(k_j) [v_j; 1]^T, with the sum of l
-//     over the segment, for the segment scan.
+//     over the segment, which the main pass chains into each segment's
+//     entering states.
 // The carried G lives in TMEM (fp32, transposed: lane n = state column, lane
 // 64 = z) and is advanced by the epilogue warps; U^B_c and the forward
 // summary come from MMAs
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t da = da0, db = mnmaj(bb, 0, 0);
         for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
           mma_bf16(tbase + T_U, da, db, idUT, k > 0 ? 1u : 0u);
-        if (prm.nseg > 1) {   // the forward summary only feeds the segment scan
+        if (prm.nseg > 1) {   // the forward summary only feeds the segment chaining
           da = da0;
           db = mnmaj(bf, 0, 0);
           for (int k = 0; k < nk; ++k, da += kMnmajOnesStep, db += kMnmajStep)
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const float wb = live ? ex2((p - pfirst) * kLog2e) : 0.f;
           const float2 wb2 = make_float2(wb, wb);
-          // the forward-summary copy only feeds the segment scan
+          // the forward-summary copy only feeds the segment chaining
           const bool fsum = prm.nseg > 1;
           const float wf = live && fsum ? ex2((D + T - p) * kLog2e) : 0.f;
           const float2 wf2 = make_float2(wf, wf);
