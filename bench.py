@@ -57,14 +57,14 @@ _CALL_KERNELS = {
 # (kernel, sources sha, workload, mask, chunk) -> DRAM bytes per head (read +
 # write) of one launch, from one ncu capture of that kernel
 TRAFFIC_PER_HEAD = {
-    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 36.3 MB written
+    # ViT-B shape at B = 128 (1536 heads), LION-S: 117.5 MB read + 35.9 MB written
     ("lion_chunk128_tc_kernel", "5dd15b36b1d88a0130d751da3af2ef9cc4b7e06423483cb1ffe51fca1118ae0c",
-     "vit_b", "s", 128): (117485568 + 36278784) / 1536,
+     "vit_b", "s", 128): (117484288 + 35912448) / 1536,
     # L = 24,337 (B = 2, H = 12, 24 heads), LION-S, the two launches of a call
-    ("lion_chunk128_pre_kernel", "09cfde51aef5e530a1da30d6e2bb971931abe0f7683503465039ff16deb97a1c",
-     "hires_2496", "s", 128): (152016384 + 22604544) / 24,
+    ("lion_chunk128_pre_kernel", "d8fc821aac36c539e362804654aebf24bd9d6d12636b2681774f8785d1d68d67",
+     "hires_2496", "s", 128): (152046592 + 22330624) / 24,
     ("lion_chunk128_long_kernel", "90361246639db1e489f6cb005845a359cd6356e849622cdadd27fb782e4cfa79",
-     "hires_2496", "s", 128): (270041600 + 110265600) / 24,
+     "hires_2496", "s", 128): (270046208 + 110145536) / 24,
 }
 
 
