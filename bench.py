@@ -563,18 +563,20 @@ def measure_stream(B, H, d, mask, steps, warmup):
 def _oracle_sample(name, mask, budget_s, threads):
     """tokens/s of the float64 oracle on a bounded sample of a workload: batch
     rows (all H heads each) in order, wrapping round to the first row, until
-    `budget_s` of wall time is spent.  The form is the one the scope's
-    measurement plan names: the brute force up to 1024 tokens, the
-    recurrent form beyond (the brute force is O(L^2) in memory and time)."""
+    `budget_s` of wall time is spent (at least one row).  The form is the one
+    the scope's measurement plan names: the brute force for the ViT-length
+    workloads (up to 256 tokens), the recurrent form for the longer ones
+    (BERT-large, L = 24,337, LRA: the brute force is O(L^2) in memory and
+    time)."""
     import oracle
     w = synth.WORKLOADS[name]
     inp = synth.workload_inputs(name, mask)
     q, k, v, ll = (synth.as_f64(inp[x]) for x in ("q", "k", "v", "log_lambda"))
-    fn, form = (oracle.full, "brute-force full form") if w.L <= 1024 else (oracle.rnn, "recurrent form")
+    fn, form = (oracle.full, "brute-force full form") if w.L <= 256 else (oracle.rnn, "recurrent form")
     oracle.threads(threads)
     cores = oracle.threads(threads)
     rows, t0 = 0, time.perf_counter()
-    while (time.perf_counter() - t0) < budget_s:
+    while rows == 0 or (time.perf_counter() - t0) < budget_s:
         b = rows % w.B
         sl = slice(b, b + 1)
         lls = None if ll is None else (ll if mask == "d" else ll[sl])
@@ -887,6 +889,10 @@ def main():
     cpu = None
     if rank == 0 and ws >= 1 and not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(args.workload, args.mask)
+        if secondary is not None:
+            # the long workload's baseline: the recurrent-form oracle
+            secondary["cpu_baseline"] = cpu_baseline("hires_2496", args.mask if args.mask != "lit" else "s",
+                                                     budget_s=5.0)
 
     if rank == 0:
         line = {

@@ -290,8 +290,10 @@ __global__ void __launch_bounds__(kThreads) bwc_summary_kernel(BcParams p) {
 }
 
 // (2), (4) the scans: F_c (dir 0, from the left) and B_c (dir 1, from the
-// right) replace the summaries in place.  One thread per state element.
-template <int D>
+// right) replace the summaries in place.  One thread per state element,
+// with the loads of U chunks in flight at once (16 for long sequences, 4 for
+// short ones, where more registers would only cost resident CTAs).
+template <int D, int U>
 __global__ void __launch_bounds__(kThreads) bwc_scan_kernel(BcParams p) {
   using C = Cfg<D>;
   constexpr int NB = (C::SZ + kThreads - 1) / kThreads;   // blocks per state
@@ -302,7 +304,6 @@ __global__ void __launch_bounds__(kThreads) bwc_scan_kernel(BcParams p) {
   float* base = p.st + (size_t)bh * N * 2 * C::SZ + (size_t)dir * C::SZ + x;
   const float* Tt = p.T + (size_t)bh * N;
   float run = 0.f;
-  constexpr int U = 4;
   for (int n0 = 0; n0 < N; n0 += U) {
     float u[U], e[U];
 #pragma unroll
@@ -657,13 +658,14 @@ cudaError_t bwc_launch(const BcParams& p, cudaStream_t s) {
   if ((e = allow_smem(bwc_summary_kernel<T, D>, sm1)) != cudaSuccess) return e;
   if ((e = allow_smem(bwc_rows_kernel<T, D>, sm3)) != cudaSuccess) return e;
   if ((e = allow_smem(bwc_cols_kernel<T, D>, sm5)) != cudaSuccess) return e;
+  auto scan = p.N >= 32 ? bwc_scan_kernel<D, 16> : bwc_scan_kernel<D, 4>;
   bwc_summary_kernel<T, D><<<gchunks, kThreads, sm1, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwc_scan_kernel<D><<<gscan, kThreads, 0, s>>>(p);
+  scan<<<gscan, kThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bwc_rows_kernel<T, D><<<gchunks, kThreads, sm3, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwc_scan_kernel<D><<<gscan, kThreads, 0, s>>>(p);
+  scan<<<gscan, kThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bwc_cols_kernel<T, D><<<gchunks, kThreads, sm5, s>>>(p);
   return cudaGetLastError();

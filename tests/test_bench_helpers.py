@@ -103,6 +103,13 @@ def test_config_lines_cover_the_scope_configurations():
         assert name in synth.WORKLOADS
 
 
+def test_oracle_baseline_forms():
+    """The CPU baseline times the brute force on the ViT-length workloads and
+    the recurrent form on the longer ones, as the measurement plan names."""
+    assert "brute-force" in bench._oracle_sample("tiny_d_fp32", "d", 0.0, 1)["sample"]
+    assert "recurrent" in bench._oracle_sample("bert_large", "s", 0.0, 1)["sample"]
+
+
 def test_backward_flops_and_peak():
     w = synth.WORKLOADS["vit_b"]
     # six L x L x d products of 2 L^2 d flops per head
