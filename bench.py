@@ -902,7 +902,8 @@ def main():
             "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": _config(args, w),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic_bytes(w, args.mask, args.chunk)[0],
+                         "frac": achieved / hbm_peak,
+                         "traffic": traffic_bytes(w, args.mask, args.chunk)[0] if args.form == "chunk" else None,
                          "peak_source": peak_src, "algorithmic_bytes": abytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
