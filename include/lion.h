@@ -152,7 +152,8 @@ size_t lion_attn_workspace_bytes(int B, int H, int L, int d, int form, int chunk
  * row; RNN: the forward recurrence alone; CHUNK: the forward chunk scan and
  * the lower triangle of each chunk).  Computed on the CUDA cores in fp32,
  * chunk <= 1024.  Workspace: lion_attn_workspace_bytes of the form (B*H*L
- * floats for RNN and CHUNK, plus the features of every token for RNN, for
+ * floats for RNN and CHUNK, plus the features of every token for RNN (whose
+ * size also holds the bidirectional form's backward sums, unused here), for
  * CHUNK with chunk <= 64, and for FULL at d = 64 and 128, which needs
  * nothing else; NULL: stream-ordered allocation).
  */
