@@ -893,6 +893,10 @@ def main():
             # the long workload's baseline: the recurrent-form oracle
             secondary["cpu_baseline"] = cpu_baseline("hires_2496", args.mask if args.mask != "lit" else "s",
                                                      budget_s=5.0)
+        for c in configs or []:
+            # BERT-large's baseline (the recurrent-form oracle), beside its LION-S chunk-128 line
+            if c["workload"].startswith("bert_large ") and c["mask"] == "s" and c.get("chunk") == 128:
+                c["cpu_baseline"] = cpu_baseline("bert_large", "s", budget_s=2.0)
 
     if rank == 0:
         line = {
