@@ -144,13 +144,14 @@ def kernels_per_call(form: str, chunk: int, w, mask: str = "s", sms: int = 152) 
     and chunk 64 three (pre-pass, segment scan, main pass), two when every
     head is one segment; the recurrent form two with its workspace
     (the features of every token, then the column CTAs), three when the
-    column CTAs (d / 8 a head) number under two an SM, so that the two sweeps
-    run in separate CTAs and a last launch combines them; the full form at
+    column CTAs (d / 8 a head) number under two an SM and L >= 256, so that
+    the two sweeps run in separate CTAs and a last launch combines them; the
+    full form at
     d = 64 and 128 two (the features, the tiled pass), three for LION-S (its
     prefix first); every other path one."""
     tc = form == "chunk" and chunk in (64, 128) and w.d == 64 and w.dtype == "bf16"
     if form == "rnn":
-        return 3 if w.B * w.H * (w.d // 8) < 2 * sms else 2
+        return 3 if w.B * w.H * (w.d // 8) < 2 * sms and w.L >= 256 else 2
     if form == "full" and w.d in (64, 128):
         return 3 if mask == "s" else 2
     if tc and w.L > 256:

@@ -18,8 +18,9 @@
 // normaliser it divides by without waiting for another; they all store the
 // same c^F_i (the same arithmetic on the same inputs).
 //
-// Sweeps.  When the heads are few (under two column CTAs an SM) and the
-// workspace is whole, the two sweeps run at the same time in separate CTAs
+// Sweeps.  When the heads are few (under two column CTAs an SM), the sequence
+// has 256 tokens or more and the workspace is whole, the two sweeps run at
+// the same time in separate CTAs
 // (gridDim.y = 2): the backward CTAs store their sums y^B_i and c^B_i
 // beside y^F_i and c^F_i (the O(Ld + L) side storage of both directions),
 // and a last launch combines them.  Otherwise each CTA runs the forward
@@ -472,8 +473,9 @@ cudaError_t rnn_launch(const Problem& p, float* ws, size_t ws_floats, cudaStream
   const RnnWs w(BHL, D);
   const bool pre = ws_floats >= w.features;
   // the two sweeps at once when the column CTAs leave the SMs under two each
+  // and the sequence is long enough for a sweep to outlast the extra launch
   const long long ctas = (long long)p.B * p.H * (D / kNC);
-  const bool split = pre && ws_floats >= w.total && !p.causal && ctas < 2LL * c128::sm_count();
+  const bool split = pre && ws_floats >= w.total && !p.causal && ctas < 2LL * c128::sm_count() && p.L >= 256;
   if (pre) {
     const size_t warps = (BHL + 3) / 4;
     const unsigned blocks = (unsigned)std::min<size_t>((warps + 7) / 8, (size_t)c128::sm_count() * 16);

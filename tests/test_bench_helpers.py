@@ -69,6 +69,7 @@ def test_launch_counts():
     assert bench.kernels_per_call("rnn", 0, hires) == 3
     assert bench.kernels_per_call("rnn", 0, vit) == 2
     assert bench.kernels_per_call("rnn", 0, synth.WORKLOADS["lra_4096"]) == 2
+    assert bench.kernels_per_call("rnn", 0, synth.WORKLOADS["tiny_d_fp32"]) == 2   # 64 tokens
     assert bench.kernels_per_call("full", 0, vit, "s") == 3   # prefix, features, the tiled pass
     assert bench.kernels_per_call("full", 0, vit, "d") == 2
     assert bench.kernels_per_call("full", 0, synth.WORKLOADS["tiny_d_fp32"], "d") == 1

@@ -38,10 +38,10 @@ def _dev(inp):
 def test_noalloc_matches_rnn_form_twice(lib, mask):
     """Bit for bit the regular recurrent form, on two calls in a row (the
     second finds the first call's values in the shared scratch).  With 12
-    heads the regular form runs its two sweeps apart and combines them in a
+    heads of 300 tokens the regular form runs its two sweeps apart and combines them in a
     last launch, while this entry point runs them one after the other in
     each CTA: the two must still agree exactly."""
-    inp = synth.make_inputs(3, 4, 150, 64, mask, "bf16", seed=77)
+    inp = synth.make_inputs(3, 4, 300, 64, mask, "bf16", seed=77)
     q, k, v, ll = _dev(inp)
     ref = lion.attn_fwd(q, k, v, ll, inp["mask"], lion.FORM_RNN).cpu().numpy()
     vp = ctypes.c_void_p
@@ -49,7 +49,7 @@ def test_noalloc_matches_rnn_form_twice(lib, mask):
     stream = vp(torch.cuda.current_stream().cuda_stream)
     for _ in range(2):
         out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
-        st = lib.lion_attn_fwd_rnn_noalloc(p(q), p(k), p(v), p(ll), 3, 4, 150, 64, inp["mask"],
+        st = lib.lion_attn_fwd_rnn_noalloc(p(q), p(k), p(v), p(ll), 3, 4, 300, 64, inp["mask"],
                                            lion.DTYPE_BF16, p(out), stream)
         assert st == lion.OK
         torch.cuda.synchronize()
